@@ -1,0 +1,485 @@
+#!/usr/bin/env python
+"""Benchmark of the simulated-rank ring allreduce on one GB300.
+
+Workload: ring allreduce (sum) over 8 simulated ranks, 134,217,728 bf16
+elements (256 MiB) per rank drawn N(0, 1e-3), fp32 accumulation, every rank
+buffer resident in one GPU's HBM.  One step = one allreduce through the C ABI
+(plan lookup, stream fork/join, k-way reduce, all-gather moves).
+
+Prints one JSON line: bus bandwidth (nccl-tests convention, 2(k-1)/k * S / t)
+as `value`, plus the HBM-roofline fraction of the executed schedule, SMs
+used, the probe-kernel slowdown per path, the end-to-end figure through host
+buffers, the clocks seen during the timed region, and the CPU oracle timed on
+a sample of the same workload.
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the path does not shard): `value` = all ranks' bus bytes / max time.
+
+`--impl reference` times the CPU oracle (the slow reference implementation)
+on a bounded sample instead; only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "simulated-rank allreduce bus GB/s & % HBM roofline; SMs used; probe slowdown"
+K_RANKS = 8
+N_ELEMS = 134_217_728
+SIGMA = 1e-3
+WORKLOAD = ("ring allreduce (sum), 8 simulated ranks, 134,217,728 bf16 elements (256 MiB) per rank, "
+            "N(0, 1e-3), fp32 accumulation")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--path", default="auto", choices=["auto", "ce", "tma", "fused"])
+    ap.add_argument("--chunk-bytes", type=int, default=4 << 20)
+    ap.add_argument("--copy-streams", type=int, default=4)
+    ap.add_argument("--no-extras", action="store_true", help="skip the per-path, probe and e2e legs")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------- inputs
+def _gen_rank(r: int):
+    from collective_communication_schedules_gb300 import inputs
+    return inputs.normal_bf16(N_ELEMS, inputs.seed_for(2, 0, r), SIGMA)
+
+
+def generate_inputs(k: int):
+    """Seeded inputs, one process per rank (spawned before any CUDA call)."""
+    import multiprocessing as mp
+    from concurrent.futures import ProcessPoolExecutor
+
+    workers = max(1, min(k, os.cpu_count() or 1))
+    with ProcessPoolExecutor(max_workers=workers, mp_context=mp.get_context("spawn")) as ex:
+        return list(ex.map(_gen_rank, range(k)))
+
+
+# --------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_id_for(dev: int) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [v for v in vis.split(",") if v.strip()]
+        return ids[dev] if dev < len(ids) else str(dev)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if it matches today's kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(kernel)
+    if not e:
+        return None
+    src = os.path.join(ROOT, "collective_communication_schedules_gb300", "csrc", e.get("source", "reduce.cu"))
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return e.get("bytes_per_launch") if digest == e.get("source_sha256_16") else None
+
+
+# ---------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value: float, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def bus_bytes(k: int, per_rank_bytes: int) -> float:
+    return 2.0 * (k - 1) / k * per_rank_bytes
+
+
+# ------------------------------------------------------------- CPU baseline
+def cpu_baseline(xs_host, seconds: float, device_out=None):
+    """The oracle, as it stands, on the first quarter of every rank's buffer."""
+    import numpy as np
+
+    from oracle import ring
+
+    n = N_ELEMS // 4
+    xs = [x[:n] for x in xs_host]
+    t0 = time.perf_counter()
+    reps = 0
+    y = None
+    while True:
+        y = ring.allreduce(xs, "bfloat16")
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    out = {"value": round(bus_bytes(K_RANKS, n * 2) / dt / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "sample": f"numpy ring-order fold of the first {n:,} of {N_ELEMS:,} bf16 elements per rank "
+                     f"(8 ranks), {reps} repetitions, {dt:.2f} s each; host has {os.cpu_count()} cores, "
+                     "numpy elementwise runs on 1",
+           "seconds_per_step": round(dt, 4)}
+    if device_out is not None:
+        # The GPU result on the same sample must equal the oracle bit for bit.
+        import torch
+        rng = np.random.default_rng(123)
+        idx = np.sort(rng.choice(n, size=min(n, 1 << 20), replace=False))
+        ti = torch.from_numpy(idx).to(device_out[0].device)
+        ok = True
+        for r in range(K_RANKS):
+            got = device_out[r].view(torch.int16).index_select(0, ti).cpu().numpy().view(np.uint16)
+            ok = ok and bool(np.array_equal(got, y[r][idx]))
+        out["parity_sample_ok"] = ok
+    return out
+
+
+def run_reference(args, world, rank):
+    """--impl reference: the oracle as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return
+    from collective_communication_schedules_gb300 import inputs
+    from oracle import ring
+
+    n = 8 << 20
+    xs = [inputs.normal_bf16(n, inputs.seed_for(2, 0, r), SIGMA) for r in range(K_RANKS)]
+    for _ in range(args.warmup):
+        ring.allreduce(xs, "bfloat16")
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        ring.allreduce(xs, "bfloat16")
+    dt = (time.perf_counter() - t0) / args.steps
+    v = bus_bytes(K_RANKS, n * 2) / dt / 1e9
+    sample = (f"numpy ring-order fold of 8,388,608 of the 134,217,728 bf16 elements per rank (8 ranks) per step; "
+              f"host has {os.cpu_count()} cores, numpy elementwise runs on 1")
+    line = {"metric": METRIC, "value": round(v, 3), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "k": K_RANKS, "count": N_ELEMS, "sample_count": n},
+            "impl": "reference",
+            "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(v, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- GPU legs
+def time_allreduce(comm, send, recv, stream, steps, profile_kind=None):
+    import torch
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        comm.allreduce(send, recv, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int):
+    """Slowdown of the FMA probe while the collective runs back to back beside it."""
+    import torch
+
+    from collective_communication_schedules_gb300 import hoc
+
+    ctas, threads = 64 * sms, 256
+    sp = torch.cuda.Stream()
+    gate = torch.cuda.Stream()
+
+    def run_probe(iters, with_coll=False, n_coll=0):
+        ev_gate = torch.cuda.Event()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        hoc.probe_launch(sms, 256, 60000, stream=gate)      # ~1 ms gate: both streams start together
+        ev_gate.record(gate)
+        sp.wait_event(ev_gate)
+        stream_c.wait_event(ev_gate)
+        if with_coll:
+            for _ in range(n_coll):
+                run_coll(stream_c)
+        a.record(sp)
+        hoc.probe_launch(ctas, threads, iters, stream=sp)
+        b.record(sp)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    base = run_probe(200)
+    iters = max(200, int(200 * 10.0 / max(base, 1e-3)))      # ~10 ms probe alone
+    alone = statistics.median(run_probe(iters) for _ in range(3))
+    n_coll = int(math.ceil(1.5 * alone / max(coll_ms, 1e-3))) + 2
+    with_c = statistics.median(run_probe(iters, True, n_coll) for _ in range(3))
+    return {"probe_alone_ms": round(alone, 3), "probe_with_ms": round(with_c, 3),
+            "slowdown": round(with_c / alone - 1.0, 4), "collectives_beside": n_coll}
+
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    xs_host = generate_inputs(K_RANKS)          # before the first CUDA call (spawned workers)
+    from collective_communication_schedules_gb300 import hoc
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sms = hoc.sm_count(local)
+    peak, peak_kind = measured_peaks()
+    per_rank = N_ELEMS * 2
+    k = K_RANKS
+    h_send = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in xs_host]
+    send = [t.to(dev) for t in h_send]
+    recv = [torch.empty_like(t) for t in send]
+    stream = torch.cuda.Stream(device=dev)
+    cfg = hoc.Config(path=args.path, chunk_bytes=args.chunk_bytes, n_copy_streams=args.copy_streams)
+    comm = hoc.Comm(k, local, cfg)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            comm.allreduce(send, recv, stream=stream)
+    torch.cuda.synchronize()
+    st = comm.last_stats()
+    fused = st["path"] == hoc.PATH_FUSED
+    kernel_kind = hoc.KERNEL_FUSED if fused else hoc.KERNEL_REDUCE
+
+    # ---- timed region (device events on the launching stream; inputs 2 GiB > L2)
+    sampler = ClockSampler(gpu_id_for(local))
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    if fused:
+        comm.profile_enable(True)      # one launch per step, no graph: events bracket the kernel itself
+    ms = time_allreduce(comm, send, recv, stream, args.steps)
+    clocks = sampler.stop()
+    torch.cuda.synchronize()
+    barrier(world)
+    if not fused:
+        comm.profile_enable(True)      # graphs are off while profiling: a separate pass of the same steps
+        time_allreduce(comm, send, recv, stream, args.steps)
+    launches, kern_ms = comm.profile_read(kernel_kind)
+    comm.profile_enable(False)
+    ms_max = max_over_ranks(world, ms, dev)
+    busbw = bus_bytes(k, per_rank) / (ms_max * 1e-3) / 1e9
+    value = world * busbw
+    st = comm.last_stats()
+    hbm_frac = st["bytes_exec"] / (ms_max * 1e-3) / (peak * 1e9)
+    lb_frac = st["bytes_min"] / (ms_max * 1e-3) / (peak * 1e9)
+    # algorithmic bytes of the dominant kernel per launch
+    if fused:
+        kern_bytes = 2 * k * per_rank
+        kname = "fused_reduce_broadcast"
+    else:
+        launches_per_step = max(1, launches // max(1, args.steps))
+        kern_bytes = (k + 1) * per_rank // launches_per_step
+        kname = "reduce"
+    avg_launch_ms = kern_ms / max(1, launches)
+    achieved = kern_bytes / (avg_launch_ms * 1e-3) / 1e9 if launches else None
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1) if achieved else None,
+                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4) if achieved else None,
+                "traffic": recorded_traffic(kname), "bytes_per_launch": kern_bytes,
+                "avg_launch_ms": round(avg_launch_ms, 4), "launches": launches,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s"}
+
+    extras = {}
+    if not args.no_extras:
+        # per-path figures
+        paths = {}
+        for p in ("fused", "ce", "tma"):
+            c2 = hoc.Comm(k, local, hoc.Config(path=p, chunk_bytes=args.chunk_bytes, n_copy_streams=args.copy_streams))
+            for _ in range(3):
+                c2.allreduce(send, recv, stream=stream)
+            pm = time_allreduce(c2, send, recv, stream, max(5, args.steps // 2))
+            s2 = c2.last_stats()
+            paths[p] = {"ms": round(pm, 4), "bus_gbs": round(bus_bytes(k, per_rank) / (pm * 1e-3) / 1e9, 1),
+                        "hbm_frac": round(s2["bytes_exec"] / (pm * 1e-3) / (peak * 1e9), 4),
+                        "lower_bound_frac": round(s2["bytes_min"] / (pm * 1e-3) / (peak * 1e9), 4),
+                        "sms_used": s2["sms_used"], "kernels_per_step": s2["kernels"],
+                        "copies_per_step": s2["copies"]}
+            paths[p]["probe"] = probe_slowdown(lambda s, c2=c2: c2.allreduce(send, recv, stream=s), pm, stream, sms)
+            c2.close()
+        # the move half alone: all-gather of the 32 MiB blocks, copy engines vs TMA
+        ag = {}
+        blk = N_ELEMS // k
+        ag_send = [t[:blk] for t in send]
+        for p in ("ce", "tma"):
+            c3 = hoc.Comm(k, local, hoc.Config(path=p, chunk_bytes=args.chunk_bytes, n_copy_streams=args.copy_streams))
+            run = lambda s, c3=c3: c3.allgather(ag_send, recv, stream=s)
+            for _ in range(3):
+                run(stream)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(10):
+                run(stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            am = e0.elapsed_time(e1) / 10
+            s3 = c3.last_stats()
+            ag[p] = {"ms": round(am, 4), "bytes_gbs": round(s3["bytes_exec"] / (am * 1e-3) / 1e9, 1),
+                     "sms_used": s3["sms_used"], "kernels_per_step": s3["kernels"],
+                     "probe": probe_slowdown(run, am, stream, sms)}
+            c3.close()
+        extras["paths"] = paths
+        extras["allgather_moves"] = ag
+
+    # ---- end to end: pinned host inputs -> device, allreduce, results -> host
+    h_recv = [torch.empty_like(t).pin_memory() for t in h_send]
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            for r in range(k):
+                send[r].copy_(h_send[r], non_blocking=True)
+            comm.allreduce(send, recv, stream=stream)
+            for r in range(k):
+                h_recv[r].copy_(recv[r], non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1) / args.e2e_steps, dev)
+    e2e = {"value": round(world * bus_bytes(k, per_rank) / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": k * per_rank, "d2h_bytes_per_step": k * per_rank, "ms_per_step": round(e2e_ms, 3)}
+
+    cpu = None
+    if rank == 0:
+        cpu = cpu_baseline(xs_host, args.cpu_seconds, device_out=recv)
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": WORKLOAD, "k": k, "count": N_ELEMS, "path": args.path,
+                           "resolved_path": {0: "auto", 1: "ce", 2: "tma", 3: "fused"}[st["path"]],
+                           "chunk_bytes": args.chunk_bytes, "copy_streams": args.copy_streams,
+                           "l2": "no flush: each step reads 2 GiB of inputs and writes 2 GiB, > 129 MB L2",
+                           "parallelism": f"{world} independent replica(s), one per GPU"},
+                "algbw_gbs": round(per_rank / (ms_max * 1e-3) / 1e9, 2),
+                "hbm_frac": round(hbm_frac, 4), "lower_bound_frac": round(lb_frac, 4),
+                "sms_used": st["sms_used"], "gpu_launches": st["kernels"] * args.steps,
+                "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks}
+        line.update(extras)
+        print(json.dumps(line), flush=True)
+    comm.close()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
+        return
+    world, rank, local = dist_setup()
+    run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

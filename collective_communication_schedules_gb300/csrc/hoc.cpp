@@ -1,0 +1,964 @@
+// C ABI of the collective library: communicator, stream manager and
+// point-to-point executor.
+//
+// Stream manager (HOCCL section 3.2, Fig. 4): the paper keeps communication
+// ordered against the kernels before and after it on a GPU stream through a
+// CPU-GPU flag handshake.  On one GPU the same ordering comes from CUDA
+// events: the caller's stream records a fork event that the internal copy
+// streams wait on, cross-stream plan edges are event waits, and the caller's
+// stream waits on a join event of every internal stream.  No host thread ever
+// blocks, and no device-side wait is unbounded.
+//
+// P2P executor (section 3.3): a move is one cudaMemcpyAsync on an internal
+// copy stream (copy engines, zero SMs) or a job of the TMA bulk-copy kernel.
+// Chunks striped over several copy streams play the role of the paper's
+// multi-QP striping (section 3.3.1): several chunks in flight hide per-copy
+// startup latency.  Each call's issue sequence can be captured once as a CUDA
+// graph and replayed, which removes the per-chunk host launch cost the paper
+// measures in Fig. 9.
+#include <algorithm>
+#include <chrono>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <list>
+#include <mutex>
+#include <string>
+#include <thread>
+#include <unordered_map>
+#include <vector>
+
+#include "hoc.h"
+#include "hoc_internal.h"
+#include "plan.h"
+
+namespace hoc {
+namespace {
+
+thread_local std::string g_detail;
+
+void set_detail(const char* what, cudaError_t e) {
+  char buf[256];
+  snprintf(buf, sizeof buf, "%s: %s (%d)", what, cudaGetErrorString(e), int(e));
+  g_detail = buf;
+}
+void set_detail(const char* what) { g_detail = what; }
+
+#define HOC_CK(call)                  \
+  do {                                \
+    cudaError_t e_ = (call);          \
+    if (e_ != cudaSuccess) {          \
+      set_detail(#call, e_);          \
+      return HOC_ERR_CUDA;            \
+    }                                 \
+  } while (0)
+
+#define HOC_TRY(expr)                 \
+  do {                                \
+    hocResult_t r_ = (expr);          \
+    if (r_ != HOC_SUCCESS) return r_; \
+  } while (0)
+
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+int env_int(const char* name, int dflt) {
+  const char* v = getenv(name);
+  return v && *v ? atoi(v) : dflt;
+}
+
+}  // namespace
+
+struct ProfPair {
+  cudaEvent_t start, stop;
+  int kind;
+};
+
+struct Bind {
+  const void* send[kMaxRanks] = {};
+  void* recv[kMaxRanks] = {};
+};
+
+}  // namespace hoc
+
+struct hocComm {
+  int k = 0;
+  int device = 0;
+  int sms = 0;
+  hoc::Cfg cfg;
+  std::mutex mu;
+  std::vector<cudaStream_t> copy;  // internal copy streams
+  cudaStream_t capture = nullptr;  // origin stream for graph capture
+  std::vector<cudaEvent_t> ev;     // plan edges (timing disabled)
+  std::vector<cudaEvent_t> join;   // one per internal stream
+  cudaEvent_t fork = nullptr;
+  int* status = nullptr;           // device status word(s) of the TMA kernel
+  std::unordered_map<std::string, hoc::Plan> plans;
+  struct GraphEntry {
+    cudaGraphExec_t exec;
+    std::list<std::string>::iterator lru;
+    int max_ctas;
+  };
+  std::unordered_map<std::string, GraphEntry> graphs;
+  std::list<std::string> lru;
+  hocOpStats_t last{};
+  bool profiling = false;
+  std::vector<hoc::ProfPair> prof_pending;
+  std::vector<cudaEvent_t> prof_free;
+  int prof_launches[3] = {0, 0, 0};
+  double prof_ms[3] = {0, 0, 0};
+  int reduce_ctas_per_sm[3][hoc::kMaxRanks + 1][2] = {};
+};
+
+namespace hoc {
+namespace {
+
+constexpr size_t kMaxGraphs = 64;
+
+hocResult_t get_event(hocComm* c, std::vector<cudaEvent_t>& pool, size_t i) {
+  while (pool.size() <= i) {
+    cudaEvent_t e;
+    HOC_CK(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    pool.push_back(e);
+  }
+  (void)c;
+  return HOC_SUCCESS;
+}
+
+hocResult_t prof_event(hocComm* c, cudaEvent_t* e) {
+  if (!c->prof_free.empty()) {
+    *e = c->prof_free.back();
+    c->prof_free.pop_back();
+    return HOC_SUCCESS;
+  }
+  HOC_CK(cudaEventCreate(e));
+  return HOC_SUCCESS;
+}
+
+int ctas_per_sm(hocComm* c, int dtype, int k, int broadcast) {
+  int& v = c->reduce_ctas_per_sm[dtype == HOC_BFLOAT16 ? 2 : dtype == HOC_FLOAT32 ? 1 : 0][k][broadcast];
+  if (v == 0) v = reduce_ctas_per_sm(dtype, k, broadcast);
+  return v;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Kernel launch with optional timing events and debug checks.
+template <class F>
+hocResult_t timed_launch(hocComm* c, int kind, cudaStream_t s, F&& launch) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (c->profiling) {
+    HOC_TRY(prof_event(c, &a));
+    HOC_TRY(prof_event(c, &b));
+    HOC_CK(cudaEventRecord(a, s));
+  }
+  cudaError_t e = launch();
+  if (e != cudaSuccess) {
+    set_detail("kernel launch", e);
+    return HOC_ERR_CUDA;
+  }
+  if (c->profiling) {
+    HOC_CK(cudaEventRecord(b, s));
+    c->prof_pending.push_back(ProfPair{a, b, kind});
+  }
+  if (c->cfg.debug) {
+    HOC_CK(cudaStreamSynchronize(s));
+    HOC_CK(cudaGetLastError());
+  }
+  return HOC_SUCCESS;
+}
+
+const void* buf_ptr(const Bind& b, int rank, int which) {
+  return which == HOC_BUF_SEND ? b.send[rank] : b.recv[rank];
+}
+
+hocResult_t run_reduce(hocComm* c, const Plan& p, const Step& st, const Bind& bd, cudaStream_t s, int* max_ctas) {
+  ReduceParams rp;
+  memset(&rp, 0, sizeof rp);
+  const int k = p.k;
+  rp.k = k;
+  rp.dtype = p.dtype;
+  rp.broadcast = st.kind == kStepFused ? 1 : 0;
+  const int lanes = dtype_lanes(p.dtype);
+  const size_t b = dtype_bytes(p.dtype);
+  bool bases_aligned = true;
+  for (int r = 0; r < k; ++r) {
+    rp.in[r] = bd.send[r];
+    rp.out[r] = bd.recv[r];
+    bases_aligned = bases_aligned && aligned16(bd.send[r]) && aligned16(bd.recv[r]);
+  }
+  // operand order of block `owner`: succ(owner), succ^2(owner), ..., owner
+  std::vector<int> pos(k);
+  for (int i = 0; i < k; ++i) pos[c->cfg.order[i]] = i;
+  for (int o = 0; o < k; ++o)
+    for (int j = 0; j < k; ++j) rp.seq[o][j] = uint8_t(c->cfg.order[(pos[o] + 1 + j) % k]);
+  rp.nseg = int(st.segs.size());
+  rp.tile_start[0] = 0;
+  for (int i = 0; i < rp.nseg; ++i) {
+    ReduceSeg g = st.segs[i];
+    g.vec = (bases_aligned && (g.out_off % lanes) == (g.elem_off % lanes)) ? 1u : 0u;
+    rp.seg[i] = g;
+    rp.tile_start[i + 1] = rp.tile_start[i] + reduce_seg_tiles(p.dtype, g);
+  }
+  (void)b;
+  const uint64_t tiles = rp.tile_start[rp.nseg];
+  if (tiles == 0) return HOC_SUCCESS;
+  uint64_t cap;
+  if (c->cfg.reduce_max_sms > 0) cap = uint64_t(std::min(c->cfg.reduce_max_sms, c->sms));
+  else cap = uint64_t(c->sms) * ctas_per_sm(c, p.dtype, k, rp.broadcast);
+  const int grid = int(std::min<uint64_t>(tiles, cap));
+  *max_ctas = std::max(*max_ctas, grid);
+  return timed_launch(c, rp.broadcast ? HOC_KERNEL_FUSED : HOC_KERNEL_REDUCE, s,
+                      [&] { return launch_reduce(rp, grid, s); });
+}
+
+hocResult_t run_tma(hocComm* c, const Step& st, const Bind& bd, cudaStream_t s, int* max_ctas) {
+  const uint32_t pb = tma_piece_bytes();
+  size_t i = 0;
+  while (i < st.moves.size()) {
+    CopyParams cp;
+    memset(&cp, 0, sizeof cp);
+    cp.piece_bytes = pb;
+    cp.status = c->status;
+    int nj = 0;
+    for (; i < st.moves.size() && nj < kMaxCopyJobs; ++i) {
+      const Move& m = st.moves[i];
+      CopyJob j;
+      j.src = static_cast<const char*>(buf_ptr(bd, m.src_rank, m.src_buf)) + m.src_off;
+      j.dst = static_cast<char*>(const_cast<void*>(buf_ptr(bd, m.dst_rank, m.dst_buf))) + m.dst_off;
+      j.bytes = m.bytes;
+      if (!j.bytes || j.src == j.dst) continue;  // nothing to move (in-place self block)
+      cp.job[nj] = j;
+      cp.piece_start[nj + 1] = cp.piece_start[nj] + tma_job_pieces(j, pb);
+      ++nj;
+    }
+    cp.njobs = nj;
+    if (!nj) continue;
+    const uint64_t pieces = cp.piece_start[nj];
+    const int cap = c->cfg.copy_max_sms > 0 ? std::min(c->cfg.copy_max_sms, c->sms) : c->sms * tma_ctas_per_sm();
+    const int grid = int(std::min<uint64_t>(pieces, uint64_t(cap)));
+    *max_ctas = std::max(*max_ctas, grid);
+    HOC_TRY(timed_launch(c, HOC_KERNEL_TMA, s, [&] { return launch_tma_copy(cp, grid, s); }));
+  }
+  return HOC_SUCCESS;
+}
+
+// Issue the plan: stream 0 is `s0`; 1..n are the internal copy streams.
+hocResult_t issue(hocComm* c, const Plan& p, const Bind& bd, cudaStream_t s0, int* max_ctas) {
+  std::vector<cudaStream_t> st(p.n_streams);
+  st[0] = s0;
+  for (int i = 1; i < p.n_streams; ++i) st[i] = c->copy[i - 1];
+  if (p.n_streams > 1) {
+    HOC_CK(cudaEventRecord(c->fork, s0));
+    for (int i = 1; i < p.n_streams; ++i) HOC_CK(cudaStreamWaitEvent(st[i], c->fork, 0));
+  }
+  HOC_TRY(get_event(c, c->ev, p.steps.size()));
+  for (size_t i = 0; i < p.steps.size(); ++i) {
+    const Step& step = p.steps[i];
+    cudaStream_t s = st[step.stream];
+    for (int w : step.waits)
+      if (p.steps[w].stream != step.stream) HOC_CK(cudaStreamWaitEvent(s, c->ev[w], 0));
+    switch (step.kind) {
+      case kStepReduce:
+      case kStepFused: HOC_TRY(run_reduce(c, p, step, bd, s, max_ctas)); break;
+      case kStepTma: HOC_TRY(run_tma(c, step, bd, s, max_ctas)); break;
+      case kStepCopy:
+        for (const Move& m : step.moves) {
+          const char* src = static_cast<const char*>(buf_ptr(bd, m.src_rank, m.src_buf)) + m.src_off;
+          char* dst = static_cast<char*>(const_cast<void*>(buf_ptr(bd, m.dst_rank, m.dst_buf))) + m.dst_off;
+          if (!m.bytes || src == dst) continue;  // nothing to move (in-place self block)
+          HOC_CK(cudaMemcpyAsync(dst, src, m.bytes, cudaMemcpyDeviceToDevice, s));
+        }
+        if (c->cfg.debug) {
+          HOC_CK(cudaStreamSynchronize(s));
+          HOC_CK(cudaGetLastError());
+        }
+        break;
+      default: return HOC_ERR_INVALID_ARG;
+    }
+    if (step.record) HOC_CK(cudaEventRecord(c->ev[i], s));
+  }
+  if (p.n_streams > 1) {
+    HOC_TRY(get_event(c, c->join, size_t(p.n_streams)));
+    for (int i = 1; i < p.n_streams; ++i) {
+      HOC_CK(cudaEventRecord(c->join[i], st[i]));
+      HOC_CK(cudaStreamWaitEvent(s0, c->join[i], 0));
+    }
+  }
+  return HOC_SUCCESS;
+}
+
+std::string graph_key(const std::string& pkey, const Bind& bd, int k) {
+  std::string key = pkey;
+  key.append(reinterpret_cast<const char*>(bd.send), sizeof(void*) * k);
+  key.append(reinterpret_cast<const char*>(bd.recv), sizeof(void*) * k);
+  return key;
+}
+
+hocResult_t execute(hocComm* c, const CallShape& shape, const Bind& bd, cudaStream_t stream) {
+  const std::string pkey = plan_key(shape);
+  auto it = c->plans.find(pkey);
+  if (it == c->plans.end()) {
+    Plan p;
+    HOC_TRY(build_plan(c->cfg, shape, &p));
+    if (c->plans.size() > 256) c->plans.clear();
+    it = c->plans.emplace(pkey, std::move(p)).first;
+  }
+  const Plan& p = it->second;
+  hocOpStats_t stats{};
+  stats.path = p.path;
+  stats.kernels = p.kernels;
+  stats.copies = p.copies;
+  stats.bytes_exec = p.bytes_exec;
+  stats.bytes_min = p.bytes_min;
+  int max_ctas = 0;
+  if (p.steps.empty()) {
+    c->last = stats;
+    return HOC_SUCCESS;
+  }
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  HOC_CK(cudaStreamIsCapturing(stream, &cs));
+  const bool worth = p.steps.size() > 1 || p.n_streams > 1 || p.copies > 1;
+  const bool use_graph = c->cfg.use_graphs && !c->profiling && !c->cfg.debug && cs == cudaStreamCaptureStatusNone && worth;
+  if (!use_graph) {
+    HOC_TRY(issue(c, p, bd, stream, &max_ctas));
+  } else {
+    const std::string gkey = graph_key(pkey, bd, p.k);
+    auto g = c->graphs.find(gkey);
+    if (g == c->graphs.end()) {
+      HOC_CK(cudaStreamBeginCapture(c->capture, cudaStreamCaptureModeThreadLocal));
+      hocResult_t r = issue(c, p, bd, c->capture, &max_ctas);
+      cudaGraph_t graph = nullptr;
+      cudaError_t e = cudaStreamEndCapture(c->capture, &graph);
+      if (r != HOC_SUCCESS) {
+        if (graph) cudaGraphDestroy(graph);
+        return r;
+      }
+      if (e != cudaSuccess) {
+        set_detail("cudaStreamEndCapture", e);
+        return HOC_ERR_CUDA;
+      }
+      cudaGraphExec_t exec = nullptr;
+      e = cudaGraphInstantiate(&exec, graph, 0);
+      cudaGraphDestroy(graph);
+      if (e != cudaSuccess) {
+        set_detail("cudaGraphInstantiate", e);
+        return HOC_ERR_CUDA;
+      }
+      if (c->graphs.size() >= kMaxGraphs) {
+        const std::string victim = c->lru.back();
+        c->lru.pop_back();
+        auto v = c->graphs.find(victim);
+        if (v != c->graphs.end()) {
+          cudaGraphExecDestroy(v->second.exec);
+          c->graphs.erase(v);
+        }
+      }
+      c->lru.push_front(gkey);
+      g = c->graphs.emplace(gkey, hocComm::GraphEntry{exec, c->lru.begin(), max_ctas}).first;
+    } else {
+      c->lru.splice(c->lru.begin(), c->lru, g->second.lru);
+      stats.graph_replayed = 1;
+      max_ctas = g->second.max_ctas;
+    }
+    HOC_CK(cudaGraphLaunch(g->second.exec, stream));
+  }
+  stats.max_ctas = max_ctas;
+  stats.sms_used = std::min(max_ctas, c->sms);
+  c->last = stats;
+  return HOC_SUCCESS;
+}
+
+}  // namespace
+}  // namespace hoc
+
+// ============================================================== C ABI
+namespace hoc {
+namespace {
+
+hocResult_t read_cfg(const hocConfig_t* in, int k, Cfg* out) {
+  Cfg c;
+  if (in) {
+    c.path = in->path;
+    if (in->chunk_bytes) c.chunk_bytes = in->chunk_bytes;
+    if (in->n_copy_streams) c.n_copy = in->n_copy_streams;
+    c.depth = in->pipeline_depth;
+    c.reduce_max_sms = in->reduce_max_sms;
+    c.copy_max_sms = in->copy_max_sms;
+    c.use_graphs = in->use_graphs;
+    c.a2a_interleave = in->a2a_interleave;
+    c.a2a_stage_sync = in->a2a_stage_sync;
+    if (in->ring_order) c.order.assign(in->ring_order, in->ring_order + k);
+  }
+  if (const char* v = getenv("HOC_PATH")) {
+    if (!strcmp(v, "ce")) c.path = HOC_PATH_CE;
+    else if (!strcmp(v, "tma")) c.path = HOC_PATH_TMA;
+    else if (!strcmp(v, "fused")) c.path = HOC_PATH_FUSED;
+    else if (!strcmp(v, "auto")) c.path = HOC_PATH_AUTO;
+  }
+  if (const char* v = getenv("HOC_CHUNK_BYTES")) c.chunk_bytes = size_t(strtoull(v, nullptr, 10));
+  c.n_copy = env_int("HOC_COPY_STREAMS", c.n_copy);
+  c.use_graphs = env_int("HOC_USE_GRAPHS", c.use_graphs);
+  c.reduce_max_sms = env_int("HOC_REDUCE_MAX_SMS", c.reduce_max_sms);
+  c.copy_max_sms = env_int("HOC_COPY_MAX_SMS", c.copy_max_sms);
+  c.depth = env_int("HOC_PIPELINE_DEPTH", c.depth);
+  c.debug = env_int("HOC_DEBUG", 0);
+  if (const char* v = getenv("HOC_FAULT")) {
+    if (!strcmp(v, "drop_chunk")) c.fault = kFaultDropChunk;
+    else if (!strcmp(v, "dup_chunk")) c.fault = kFaultDupChunk;
+    else if (!strcmp(v, "wrong_order")) c.fault = kFaultWrongOrder;
+    else if (!strcmp(v, "proxy_stall")) c.fault = kFaultProxyStall;
+  }
+  if (c.order.empty())
+    for (int i = 0; i < k; ++i) c.order.push_back(i);
+  std::vector<int> seen(k, 0);
+  for (int v : c.order) {
+    if (v < 0 || v >= k || seen[v]) {
+      set_detail("ring_order is not a permutation of 0..k-1");
+      return HOC_ERR_INVALID_ARG;
+    }
+    seen[v] = 1;
+  }
+  if (c.path < HOC_PATH_AUTO || c.path > HOC_PATH_FUSED || c.n_copy < 1 || c.n_copy > 16 || c.chunk_bytes < 256 ||
+      c.depth < 0 || c.reduce_max_sms < 0 || c.copy_max_sms < 0) {
+    set_detail("configuration value out of range");
+    return HOC_ERR_INVALID_ARG;
+  }
+  c.use_graphs = c.use_graphs ? 1 : 0;
+  *out = c;
+  return HOC_SUCCESS;
+}
+
+void free_comm(hocComm* c) {
+  if (!c) return;
+  for (auto& g : c->graphs) cudaGraphExecDestroy(g.second.exec);
+  for (cudaEvent_t e : c->ev) cudaEventDestroy(e);
+  for (cudaEvent_t e : c->join) cudaEventDestroy(e);
+  for (cudaEvent_t e : c->prof_free) cudaEventDestroy(e);
+  for (auto& pp : c->prof_pending) {
+    cudaEventDestroy(pp.start);
+    cudaEventDestroy(pp.stop);
+  }
+  if (c->fork) cudaEventDestroy(c->fork);
+  for (cudaStream_t s : c->copy) cudaStreamDestroy(s);
+  if (c->capture) cudaStreamDestroy(c->capture);
+  if (c->status) cudaFree(c->status);
+  delete c;
+}
+
+bool dtype_ok(int dtype, bool reduction) {
+  if (reduction) return dtype == HOC_INT32 || dtype == HOC_FLOAT32 || dtype == HOC_BFLOAT16;
+  return dtype_bytes(dtype) != 0;
+}
+
+bool elem_aligned(const void* p, size_t b) { return (reinterpret_cast<uintptr_t>(p) % b) == 0; }
+
+struct Range {
+  uintptr_t lo, hi;
+  bool writable;
+  int rank;
+};
+
+// Writable ranges may not overlap any other range; read-only ranges may
+// overlap each other.  `same_ok(a, b)` names the allowed in-place pairs.
+template <class F>
+hocResult_t check_overlaps(const std::vector<Range>& rs, F&& same_ok) {
+  for (size_t i = 0; i < rs.size(); ++i)
+    for (size_t j = i + 1; j < rs.size(); ++j) {
+      const Range &a = rs[i], &b = rs[j];
+      if (!(a.writable || b.writable)) continue;
+      if (a.lo >= b.hi || b.lo >= a.hi) continue;
+      if (same_ok(a, b)) continue;
+      set_detail("rank buffers overlap");
+      return HOC_ERR_INVALID_ARG;
+    }
+  return HOC_SUCCESS;
+}
+
+hocResult_t check_array(const void* const* a, int k, size_t b) {
+  if (!a) {
+    set_detail("NULL buffer array");
+    return HOC_ERR_INVALID_ARG;
+  }
+  for (int r = 0; r < k; ++r) {
+    if (!a[r]) {
+      set_detail("NULL rank buffer");
+      return HOC_ERR_INVALID_ARG;
+    }
+    if (!elem_aligned(a[r], b)) {
+      set_detail("rank buffer not aligned to its element size");
+      return HOC_ERR_INVALID_ARG;
+    }
+  }
+  return HOC_SUCCESS;
+}
+
+hocResult_t check_reduce_args(hocComm* c, int dtype, int op) {
+  if (!c) return HOC_ERR_NOT_INITIALIZED;
+  if (!dtype_ok(dtype, true)) {
+    set_detail(dtype == HOC_UINT8 ? "reductions take int32, float32 or bfloat16" : "unknown dtype");
+    return dtype == HOC_UINT8 ? HOC_ERR_UNSUPPORTED : HOC_ERR_INVALID_ARG;
+  }
+  if (op != HOC_SUM) {
+    set_detail("only HOC_SUM is implemented");
+    return HOC_ERR_UNSUPPORTED;
+  }
+  return HOC_SUCCESS;
+}
+
+uintptr_t U(const void* p) { return reinterpret_cast<uintptr_t>(p); }
+
+hocResult_t run(hocComm* c, const CallShape& shape, const Bind& bd, void* stream) {
+  std::lock_guard<std::mutex> lock(c->mu);
+  DeviceGuard g(c->device);
+  if (!g.ok) {
+    set_detail("cudaSetDevice failed");
+    return HOC_ERR_CUDA;
+  }
+  return execute(c, shape, bd, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+}  // namespace hoc
+
+using namespace hoc;
+
+extern "C" {
+
+hocResult_t hoc_config_default(hocConfig_t* cfg) {
+  if (!cfg) return HOC_ERR_INVALID_ARG;
+  memset(cfg, 0, sizeof *cfg);
+  cfg->path = HOC_PATH_AUTO;
+  cfg->chunk_bytes = size_t(4) << 20;
+  cfg->n_copy_streams = 4;
+  cfg->pipeline_depth = 0;
+  cfg->reduce_max_sms = 0;
+  cfg->copy_max_sms = 0;
+  cfg->use_graphs = 1;
+  cfg->a2a_interleave = 1;
+  cfg->a2a_stage_sync = 0;
+  cfg->ring_order = nullptr;
+  return HOC_SUCCESS;
+}
+
+hocResult_t hoc_init(hocComm_t* comm, int nranks, int device, const hocConfig_t* cfg) {
+  if (!comm) return HOC_ERR_INVALID_ARG;
+  *comm = nullptr;
+  if (nranks < 1 || nranks > kMaxRanks) {
+    set_detail("nranks must be 1..HOC_MAX_RANKS");
+    return HOC_ERR_INVALID_ARG;
+  }
+  Cfg c;
+  HOC_TRY(read_cfg(cfg, nranks, &c));
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0) {
+    cudaGetLastError();
+    set_detail("no CUDA device");
+    return HOC_ERR_NO_DEVICE;
+  }
+  if (device < 0 || device >= ndev) {
+    set_detail("device index out of range");
+    return HOC_ERR_INVALID_ARG;
+  }
+  DeviceGuard g(device);
+  if (!g.ok) {
+    set_detail("cudaSetDevice failed");
+    return HOC_ERR_CUDA;
+  }
+  hocComm* h = new (std::nothrow) hocComm();
+  if (!h) return HOC_ERR_OOM;
+  h->k = nranks;
+  h->device = device;
+  h->cfg = c;
+  auto fail = [&](const char* what, cudaError_t e) {
+    set_detail(what, e);
+    free_comm(h);
+    return e == cudaErrorMemoryAllocation ? HOC_ERR_OOM : HOC_ERR_CUDA;
+  };
+  cudaError_t e = cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, device);
+  if (e != cudaSuccess) return fail("cudaDeviceGetAttribute", e);
+  for (int i = 0; i < c.n_copy; ++i) {
+    cudaStream_t s;
+    e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return fail("cudaStreamCreateWithFlags", e);
+    h->copy.push_back(s);
+  }
+  e = cudaStreamCreateWithFlags(&h->capture, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return fail("cudaStreamCreateWithFlags", e);
+  e = cudaEventCreateWithFlags(&h->fork, cudaEventDisableTiming);
+  if (e != cudaSuccess) return fail("cudaEventCreateWithFlags", e);
+  e = cudaMalloc(&h->status, 256);
+  if (e != cudaSuccess) return fail("cudaMalloc(status)", e);
+  e = cudaMemset(h->status, 0, 256);
+  if (e != cudaSuccess) return fail("cudaMemset(status)", e);
+  e = tma_prepare();
+  if (e != cudaSuccess) return fail("tma_prepare", e);
+  // occupancy of every reduce kernel this communicator can launch, queried
+  // now so that nothing but stream work happens while a graph is captured
+  for (int dt : {int(HOC_INT32), int(HOC_FLOAT32), int(HOC_BFLOAT16)})
+    for (int bc = 0; bc < 2; ++bc) ctas_per_sm(h, dt, nranks, bc);
+  *comm = h;
+  return HOC_SUCCESS;
+}
+
+hocResult_t hoc_destroy(hocComm_t comm) {
+  if (!comm) return HOC_ERR_NOT_INITIALIZED;
+  {
+    DeviceGuard g(comm->device);
+    for (cudaStream_t s : comm->copy) cudaStreamSynchronize(s);
+    free_comm(comm);
+  }
+  return HOC_SUCCESS;
+}
+
+hocResult_t hoc_allreduce(hocComm_t comm, const void* const* send, void* const* recv, size_t count,
+                          hocDataType_t dtype, hocRedOp_t op, void* stream) {
+  HOC_TRY(check_reduce_args(comm, dtype, op));
+  if (count == 0) return HOC_SUCCESS;
+  const int k = comm->k;
+  const size_t b = dtype_bytes(dtype);
+  HOC_TRY(check_array(send, k, b));
+  HOC_TRY(check_array(const_cast<const void* const*>(reinterpret_cast<void* const*>(recv)), k, b));
+  std::vector<Range> rs;
+  for (int r = 0; r < k; ++r) {
+    rs.push_back(Range{U(send[r]), U(send[r]) + count * b, false, r});
+    rs.push_back(Range{U(recv[r]), U(recv[r]) + count * b, true, r});
+  }
+  HOC_TRY(check_overlaps(rs, [](const Range& a, const Range& b2) {
+    return a.rank == b2.rank && a.writable != b2.writable && a.lo == b2.lo;  // in place: send[r] == recv[r]
+  }));
+  CallShape s;
+  s.op = HOC_OP_ALLREDUCE;
+  s.k = k;
+  s.dtype = dtype;
+  s.count = count;
+  Bind bd;
+  for (int r = 0; r < k; ++r) {
+    bd.send[r] = send[r];
+    bd.recv[r] = recv[r];
+  }
+  return run(comm, s, bd, stream);
+}
+
+hocResult_t hoc_reduce_scatter(hocComm_t comm, const void* const* send, void* const* recv, size_t recvcount,
+                               hocDataType_t dtype, hocRedOp_t op, void* stream) {
+  HOC_TRY(check_reduce_args(comm, dtype, op));
+  if (recvcount == 0) return HOC_SUCCESS;
+  const int k = comm->k;
+  const size_t b = dtype_bytes(dtype);
+  HOC_TRY(check_array(send, k, b));
+  HOC_TRY(check_array(const_cast<const void* const*>(reinterpret_cast<void* const*>(recv)), k, b));
+  std::vector<Range> rs;
+  for (int r = 0; r < k; ++r) {
+    rs.push_back(Range{U(send[r]), U(send[r]) + size_t(k) * recvcount * b, false, r});
+    rs.push_back(Range{U(recv[r]), U(recv[r]) + recvcount * b, true, r});
+  }
+  HOC_TRY(check_overlaps(rs, [&](const Range& a, const Range& b2) {
+    if (a.rank != b2.rank || a.writable == b2.writable) return false;
+    const Range& w = a.writable ? a : b2;
+    const Range& ro = a.writable ? b2 : a;
+    return w.lo == ro.lo + size_t(a.rank) * recvcount * b;  // in place: recv[r] = send[r] + r*recvcount
+  }));
+  CallShape s;
+  s.op = HOC_OP_REDUCE_SCATTER;
+  s.k = k;
+  s.dtype = dtype;
+  s.count = recvcount;
+  Bind bd;
+  for (int r = 0; r < k; ++r) {
+    bd.send[r] = send[r];
+    bd.recv[r] = recv[r];
+  }
+  return run(comm, s, bd, stream);
+}
+
+hocResult_t hoc_allgather(hocComm_t comm, const void* const* send, void* const* recv, size_t sendcount,
+                          hocDataType_t dtype, void* stream) {
+  if (!comm) return HOC_ERR_NOT_INITIALIZED;
+  if (!dtype_ok(dtype, false)) {
+    set_detail("unknown dtype");
+    return HOC_ERR_INVALID_ARG;
+  }
+  if (sendcount == 0) return HOC_SUCCESS;
+  const int k = comm->k;
+  const size_t b = dtype_bytes(dtype);
+  HOC_TRY(check_array(send, k, b));
+  HOC_TRY(check_array(const_cast<const void* const*>(reinterpret_cast<void* const*>(recv)), k, b));
+  std::vector<Range> rs;
+  for (int r = 0; r < k; ++r) {
+    rs.push_back(Range{U(send[r]), U(send[r]) + sendcount * b, false, r});
+    rs.push_back(Range{U(recv[r]), U(recv[r]) + size_t(k) * sendcount * b, true, r});
+  }
+  HOC_TRY(check_overlaps(rs, [&](const Range& a, const Range& b2) {
+    if (a.rank != b2.rank || a.writable == b2.writable) return false;
+    const Range& w = a.writable ? a : b2;
+    const Range& ro = a.writable ? b2 : a;
+    return ro.lo == w.lo + size_t(a.rank) * sendcount * b;  // in place: send[r] = recv[r] + r*sendcount
+  }));
+  CallShape s;
+  s.op = HOC_OP_ALLGATHER;
+  s.k = k;
+  s.dtype = dtype;
+  s.count = sendcount;
+  Bind bd;
+  for (int r = 0; r < k; ++r) {
+    bd.send[r] = send[r];
+    bd.recv[r] = recv[r];
+  }
+  return run(comm, s, bd, stream);
+}
+
+hocResult_t hoc_alltoall(hocComm_t comm, const void* const* send, const size_t* sendcounts, const size_t* sdispls,
+                         void* const* recv, const size_t* rdispls, size_t count_if_uniform, hocDataType_t dtype,
+                         void* stream) {
+  if (!comm) return HOC_ERR_NOT_INITIALIZED;
+  if (!dtype_ok(dtype, false)) {
+    set_detail("unknown dtype");
+    return HOC_ERR_INVALID_ARG;
+  }
+  const int k = comm->k;
+  const size_t b = dtype_bytes(dtype);
+  const size_t kk = size_t(k) * k;
+  std::vector<size_t> cnt(kk), sd(kk), rd(kk);
+  size_t total = 0;
+  for (size_t i = 0; i < kk; ++i) {
+    cnt[i] = sendcounts ? sendcounts[i] : count_if_uniform;
+    total += cnt[i];
+  }
+  if (total == 0) return HOC_SUCCESS;
+  for (int a = 0; a < k; ++a)
+    for (int d = 0; d < k; ++d)
+      sd[size_t(a) * k + d] = sdispls ? sdispls[size_t(a) * k + d] : (d ? sd[size_t(a) * k + d - 1] + cnt[size_t(a) * k + d - 1] : 0);
+  for (int d = 0; d < k; ++d)
+    for (int a = 0; a < k; ++a)
+      rd[size_t(d) * k + a] = rdispls ? rdispls[size_t(d) * k + a] : (a ? rd[size_t(d) * k + a - 1] + cnt[size_t(a - 1) * k + d] : 0);
+  HOC_TRY(check_array(send, k, b));
+  HOC_TRY(check_array(const_cast<const void* const*>(reinterpret_cast<void* const*>(recv)), k, b));
+  std::vector<Range> rs;
+  for (int a = 0; a < k; ++a)
+    for (int d = 0; d < k; ++d) {
+      const size_t n = cnt[size_t(a) * k + d] * b;
+      if (!n) continue;
+      rs.push_back(Range{U(send[a]) + sd[size_t(a) * k + d] * b, U(send[a]) + sd[size_t(a) * k + d] * b + n, false, a});
+      rs.push_back(Range{U(recv[d]) + rd[size_t(d) * k + a] * b, U(recv[d]) + rd[size_t(d) * k + a] * b + n, true, d});
+    }
+  HOC_TRY(check_overlaps(rs, [](const Range&, const Range&) { return false; }));
+  CallShape s;
+  s.op = HOC_OP_ALLTOALL;
+  s.k = k;
+  s.dtype = dtype;
+  if (sendcounts) s.counts = cnt;
+  else s.count = count_if_uniform;
+  if (sdispls) s.sdispls = sd;
+  if (rdispls) s.rdispls = rd;
+  Bind bd;
+  for (int r = 0; r < k; ++r) {
+    bd.send[r] = send[r];
+    bd.recv[r] = recv[r];
+  }
+  return run(comm, s, bd, stream);
+}
+
+hocResult_t hoc_sendrecv(hocComm_t comm, int src_rank, const void* send, int dst_rank, void* recv, size_t count,
+                         hocDataType_t dtype, void* stream) {
+  if (!comm) return HOC_ERR_NOT_INITIALIZED;
+  if (!dtype_ok(dtype, false)) {
+    set_detail("unknown dtype");
+    return HOC_ERR_INVALID_ARG;
+  }
+  if (src_rank < 0 || src_rank >= comm->k || dst_rank < 0 || dst_rank >= comm->k) {
+    set_detail("rank out of range");
+    return HOC_ERR_INVALID_ARG;
+  }
+  if (count == 0) return HOC_SUCCESS;
+  const size_t b = dtype_bytes(dtype);
+  if (!send || !recv || !elem_aligned(send, b) || !elem_aligned(recv, b)) {
+    set_detail("NULL or misaligned buffer");
+    return HOC_ERR_INVALID_ARG;
+  }
+  if (send == recv) return HOC_SUCCESS;
+  const uintptr_t a = U(send), d = U(recv);
+  if (a < d + count * b && d < a + count * b) {
+    set_detail("send and recv overlap");
+    return HOC_ERR_INVALID_ARG;
+  }
+  CallShape s;
+  s.op = HOC_OP_SENDRECV;
+  s.k = comm->k;
+  s.dtype = dtype;
+  s.count = count;
+  s.src_rank = src_rank;
+  s.dst_rank = dst_rank;
+  Bind bd;
+  bd.send[src_rank] = send;
+  bd.recv[dst_rank] = recv;
+  return run(comm, s, bd, stream);
+}
+
+hocResult_t hoc_wait(hocComm_t comm, void* stream, int timeout_ms) {
+  if (!comm) return HOC_ERR_NOT_INITIALIZED;
+  DeviceGuard g(comm->device);
+  const auto deadline = std::chrono::steady_clock::now() + std::chrono::milliseconds(timeout_ms < 0 ? 0 : timeout_ms);
+  std::vector<cudaStream_t> all(comm->copy);
+  all.push_back(static_cast<cudaStream_t>(stream));
+  for (cudaStream_t s : all) {
+    for (;;) {
+      cudaError_t e = cudaStreamQuery(s);
+      if (e == cudaSuccess) break;
+      if (e != cudaErrorNotReady) {
+        set_detail("cudaStreamQuery", e);
+        return HOC_ERR_CUDA;
+      }
+      if (std::chrono::steady_clock::now() >= deadline) {
+        set_detail("hoc_wait: work still running at the deadline");
+        return HOC_ERR_TIMEOUT;
+      }
+      std::this_thread::sleep_for(std::chrono::microseconds(50));
+    }
+  }
+  if (comm->cfg.fault == kFaultProxyStall) {
+    // Injected on the host: a completion that never arrives.
+    std::this_thread::sleep_until(deadline);
+    set_detail("hoc_wait: injected proxy stall");
+    return HOC_ERR_TIMEOUT;
+  }
+  int st = 0;
+  HOC_CK(cudaMemcpy(&st, comm->status, sizeof st, cudaMemcpyDeviceToHost));
+  if (st != 0) {
+    HOC_CK(cudaMemset(comm->status, 0, sizeof st));
+    char buf[96];
+    snprintf(buf, sizeof buf, "TMA copy kernel gave up on a bounded wait (status 0x%x)", st);
+    set_detail(buf);
+    return HOC_ERR_TIMEOUT;
+  }
+  return HOC_SUCCESS;
+}
+
+hocResult_t hoc_last_stats(hocComm_t comm, hocOpStats_t* stats) {
+  if (!comm) return HOC_ERR_NOT_INITIALIZED;
+  if (!stats) return HOC_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(comm->mu);
+  *stats = comm->last;
+  return HOC_SUCCESS;
+}
+
+hocResult_t hoc_profile_enable(hocComm_t comm, int enable) {
+  if (!comm) return HOC_ERR_NOT_INITIALIZED;
+  std::lock_guard<std::mutex> lock(comm->mu);
+  comm->profiling = enable != 0;
+  return HOC_SUCCESS;
+}
+
+hocResult_t hoc_profile_read(hocComm_t comm, hocKernel_t kernel, int* launches, double* total_ms) {
+  if (!comm) return HOC_ERR_NOT_INITIALIZED;
+  if (kernel < HOC_KERNEL_REDUCE || kernel > HOC_KERNEL_TMA || !launches || !total_ms) return HOC_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(comm->mu);
+  DeviceGuard g(comm->device);
+  for (const ProfPair& pp : comm->prof_pending) {
+    HOC_CK(cudaEventSynchronize(pp.stop));
+    float ms = 0.f;
+    HOC_CK(cudaEventElapsedTime(&ms, pp.start, pp.stop));
+    comm->prof_launches[pp.kind] += 1;
+    comm->prof_ms[pp.kind] += ms;
+    comm->prof_free.push_back(pp.start);
+    comm->prof_free.push_back(pp.stop);
+  }
+  comm->prof_pending.clear();
+  *launches = comm->prof_launches[kernel];
+  *total_ms = comm->prof_ms[kernel];
+  comm->prof_launches[kernel] = 0;
+  comm->prof_ms[kernel] = 0;
+  return HOC_SUCCESS;
+}
+
+const char* hoc_error_string(hocResult_t r) {
+  switch (r) {
+    case HOC_SUCCESS: return "success";
+    case HOC_ERR_INVALID_ARG: return "invalid argument";
+    case HOC_ERR_CUDA: return "CUDA error";
+    case HOC_ERR_OOM: return "out of memory";
+    case HOC_ERR_NOT_INITIALIZED: return "communicator not initialized";
+    case HOC_ERR_UNSUPPORTED: return "unsupported";
+    case HOC_ERR_TIMEOUT: return "timeout";
+    case HOC_ERR_NO_DEVICE: return "no CUDA device";
+    default: return "unknown result code";
+  }
+}
+
+const char* hoc_last_error_detail(void) { return g_detail.c_str(); }
+
+hocResult_t hoc_plan_query(int nranks, const hocConfig_t* cfg, int op, size_t count, hocDataType_t dtype,
+                           const size_t* counts, hocPlanItem_t* items, size_t cap, size_t* n_items) {
+  if (!n_items) return HOC_ERR_INVALID_ARG;
+  *n_items = 0;
+  if (nranks < 1 || nranks > kMaxRanks) return HOC_ERR_INVALID_ARG;
+  Cfg c;
+  HOC_TRY(read_cfg(cfg, nranks, &c));
+  CallShape s;
+  s.op = op;
+  s.k = nranks;
+  s.dtype = dtype;
+  s.count = count;
+  if (op == HOC_OP_ALLTOALL && counts) s.counts.assign(counts, counts + size_t(nranks) * nranks);
+  if (op == HOC_OP_SENDRECV) {
+    s.src_rank = 0;
+    s.dst_rank = 1 % nranks;
+  }
+  Plan p;
+  HOC_TRY(build_plan(c, s, &p));
+  const size_t b = dtype_bytes(dtype);
+  size_t n = 0;
+  auto put = [&](const hocPlanItem_t& it) {
+    if (items && n < cap) items[n] = it;
+    ++n;
+  };
+  for (size_t i = 0; i < p.steps.size(); ++i) {
+    const Step& st = p.steps[i];
+    hocPlanItem_t base{};
+    base.step = int(i);
+    base.stream = st.stream;
+    base.stage = st.stage;
+    base.n_waits = int(st.waits.size());
+    base.wait0 = st.waits.empty() ? -1 : st.waits[0];
+    if (st.kind == kStepReduce || st.kind == kStepFused) {
+      for (const ReduceSeg& g : st.segs) {
+        hocPlanItem_t it = base;
+        it.kind = st.kind == kStepFused ? HOC_ITEM_FUSED : HOC_ITEM_REDUCE;
+        it.src_rank = -1;
+        it.dst_rank = int(g.owner);
+        it.src_buf = HOC_BUF_SEND;
+        it.dst_buf = HOC_BUF_RECV;
+        it.src_off = g.elem_off * b;
+        it.dst_off = g.out_off * b;
+        it.bytes = g.elems * b;
+        put(it);
+      }
+    } else {
+      for (const Move& m : st.moves) {
+        hocPlanItem_t it = base;
+        it.kind = st.kind == kStepTma ? HOC_ITEM_TMA : HOC_ITEM_COPY;
+        it.src_rank = m.src_rank;
+        it.dst_rank = m.dst_rank;
+        it.src_buf = m.src_buf;
+        it.dst_buf = m.dst_buf;
+        it.src_off = m.src_off;
+        it.dst_off = m.dst_off;
+        it.bytes = m.bytes;
+        put(it);
+      }
+    }
+  }
+  *n_items = n;
+  return HOC_SUCCESS;
+}
+
+}  // extern "C"

@@ -1,0 +1,73 @@
+// Internal declarations shared by the host runtime and the CUDA kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "hoc.h"
+
+namespace hoc {
+
+constexpr int kMaxRanks = HOC_MAX_RANKS;
+constexpr int kMaxCopyJobs = 192;  // jobs per TMA copy launch (kernel parameter space)
+
+// ----------------------------------------------------------------- reduce
+// One segment = one block's element range of one launch.  Every rank's input
+// is read at [elem_off, elem_off + elems); the folded result goes to the
+// output buffer(s) at [out_off, out_off + elems).
+struct ReduceSeg {
+  uint64_t elem_off;
+  uint64_t elems;
+  uint64_t out_off;
+  uint32_t owner;  // block owner: selects the operand order and, without broadcast, the output rank
+  uint32_t vec;    // 1 when every input and output pointer of the segment is co-aligned to 16 bytes
+};
+
+struct ReduceParams {
+  const void* in[kMaxRanks];
+  void* out[kMaxRanks];
+  ReduceSeg seg[kMaxRanks];
+  uint64_t tile_start[kMaxRanks + 1];  // prefix sums of the tiles of each segment
+  uint8_t seq[kMaxRanks][kMaxRanks];   // seq[owner][j] = rank of the j-th operand (ring order)
+  int32_t k;
+  int32_t nseg;
+  int32_t broadcast;  // 1: write the result to out[0..k-1]; 0: to out[owner]
+  int32_t dtype;      // hocDataType_t (INT32, FLOAT32, BFLOAT16)
+};
+
+// Elements covered by one reduce tile for `dtype` (threads x vectors x lanes).
+uint64_t reduce_tile_elems(int dtype);
+// Tiles of a segment (0 for an empty segment).
+uint64_t reduce_seg_tiles(int dtype, const ReduceSeg& s);
+// Resident CTAs per SM of the reduce kernel for (dtype, k, broadcast).
+int reduce_ctas_per_sm(int dtype, int k, int broadcast);
+cudaError_t launch_reduce(const ReduceParams& p, int grid, cudaStream_t stream);
+
+// -------------------------------------------------------------- TMA copy
+struct CopyJob {
+  const char* src;
+  char* dst;
+  uint64_t bytes;
+};
+
+struct CopyParams {
+  CopyJob job[kMaxCopyJobs];
+  uint64_t piece_start[kMaxCopyJobs + 1];  // prefix sums of the pieces of each job
+  int32_t njobs;
+  uint32_t piece_bytes;  // bytes per piece: one shared-memory stage
+  int* status;           // device word; the kernel writes a non-zero code on a wait timeout
+};
+
+uint32_t tma_piece_bytes();
+uint64_t tma_job_pieces(const CopyJob& j, uint32_t piece_bytes);
+int tma_ctas_per_sm();
+cudaError_t tma_prepare();  // one-time per device: shared-memory opt-in
+cudaError_t launch_tma_copy(const CopyParams& p, int grid, cudaStream_t stream);
+
+// Device status codes written by kernels.
+constexpr int kStatusTimeoutLoad = 0x1001;
+constexpr int kStatusTimeoutDrain = 0x1002;
+
+}  // namespace hoc

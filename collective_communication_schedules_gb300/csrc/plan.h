@@ -1,0 +1,95 @@
+// Collective scheduler: turns one collective call into a plan of steps.
+//
+// HOCCL section 3.4 (Fig. 6): a collective becomes a traffic matrix of flows,
+// the flows are grouped into contention-free stages, and each flow is cut into
+// fixed-size chunks that share the DMA-engine work queues.  Here a plan is an
+// ordered list of steps; each step runs on one stream (0 = the caller's
+// stream, 1..n = internal copy streams) and may wait on earlier steps of
+// other streams.  Plans depend only on the shape of the call (op, k, counts,
+// dtype, configuration), never on buffer addresses, so they are cached.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "hoc.h"
+#include "hoc_internal.h"
+
+namespace hoc {
+
+struct Cfg {
+  int path = HOC_PATH_AUTO;
+  size_t chunk_bytes = size_t(4) << 20;
+  int n_copy = 4;
+  int depth = 0;
+  int reduce_max_sms = 0;
+  int copy_max_sms = 0;
+  int use_graphs = 1;
+  int a2a_interleave = 1;
+  int a2a_stage_sync = 0;
+  std::vector<int> order;  // ring order, size k
+  int debug = 0;
+  int fault = 0;           // host-side fault injection (Fault)
+};
+
+enum Fault { kFaultNone = 0, kFaultDropChunk = 1, kFaultDupChunk = 2, kFaultWrongOrder = 3, kFaultProxyStall = 4 };
+
+enum StepKind { kStepReduce = 0, kStepFused = 1, kStepCopy = 2, kStepTma = 3 };
+
+struct Move {
+  int src_rank, dst_rank;
+  int src_buf, dst_buf;  // hocBuf_t
+  size_t src_off, dst_off, bytes;
+};
+
+struct Step {
+  int kind = kStepCopy;
+  int stream = 0;
+  int stage = 0;
+  std::vector<ReduceSeg> segs;  // reduce / fused (vec is filled in at bind time)
+  std::vector<Move> moves;      // copy / tma
+  std::vector<int> waits;       // earlier steps on other streams
+  bool record = false;          // some later step waits on this one
+};
+
+struct Plan {
+  int op = 0, k = 0, dtype = 0, path = 0;
+  size_t count = 0;
+  int n_streams = 1;  // streams used including stream 0
+  std::vector<Step> steps;
+  size_t bytes_exec = 0, bytes_min = 0;
+  int kernels = 0, copies = 0;
+};
+
+struct CallShape {
+  int op = 0;
+  int k = 0;
+  int dtype = 0;
+  size_t count = 0;
+  std::vector<size_t> counts;  // alltoall: k*k sendcounts (elements); empty = uniform
+  std::vector<size_t> sdispls, rdispls;
+  int src_rank = 0, dst_rank = 0;  // sendrecv
+};
+
+size_t dtype_bytes(int dtype);
+int dtype_lanes(int dtype);  // elements per 16-byte vector
+
+// Builds the plan; returns HOC_ERR_INVALID_ARG / UNSUPPORTED for bad shapes.
+hocResult_t build_plan(const Cfg& cfg, const CallShape& shape, Plan* plan);
+
+// Block partition of n elements over k owners (sizes differ by at most one).
+void block_partition(size_t n, int k, std::vector<size_t>* sizes, std::vector<size_t>* offs);
+
+// Order in which a copy queue serves the chunks of several flows.  Input: the
+// chunk count of each flow.  Output: (flow, chunk) pairs.  Flow-size-aware:
+// chunk j of flow f is due at virtual time (j + 1) / n_f and chunks are served
+// in due order (ties by flow index), so every flow advances in proportion to
+// its size.  FIFO: all chunks of flow 0, then flow 1, ...
+std::vector<std::pair<int, size_t>> interleave_chunks(const std::vector<size_t>& chunks_per_flow, bool size_aware);
+
+// Key that identifies a plan (shape + configuration).
+std::string plan_key(const CallShape& s);
+
+}  // namespace hoc

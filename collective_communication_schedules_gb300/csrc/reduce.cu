@@ -1,0 +1,274 @@
+// k-way chunk-reduce kernel: the reduction of ring reduce-scatter with the
+// ring's k-1 hops collapsed into one pass over the k rank buffers.
+//
+// HOCCL (section 5, Limitations) leaves reductions to SM-side execution; the
+// fold order here is the textbook ring reduce-scatter hop order: block r
+// starts from rank succ(r)'s input and every later hop adds the receiving
+// rank's input, ending with r itself.  Because every hop of the ring is
+// folded in the same order, the bits equal those of the hop-by-hop ring with
+// binary32 partials.
+//
+// Layout: rank buffers are 1-D arrays in HBM.  A launch covers one element
+// range (a chunk) of every block: one segment per block.  Segments are cut into
+// tiles of kThreads x kVecPerThread 16-byte vectors; CTAs stride over tiles.
+// Each thread issues all k x kVecPerThread 16-byte loads before folding, so a
+// 256-thread CTA keeps k * 8 KiB of loads in flight.
+//
+// Arithmetic: fp32 adds with __fadd_rn (round to nearest even, no contraction,
+// no flush to zero); bf16 widens exactly to fp32, adds in fp32 and rounds once
+// with __float2bfloat16_rn; int32 adds modulo 2^32 in uint32.
+#include <cuda_bf16.h>
+
+#include "hoc_internal.h"
+
+namespace hoc {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kVecPerThread = 2;
+constexpr uint64_t kTileVecs = uint64_t(kThreads) * kVecPerThread;
+
+__host__ __device__ inline int lanes_of(int dtype) { return dtype == HOC_BFLOAT16 ? 8 : 4; }
+
+// Elements before the first 16-byte-aligned element of a vector segment.
+__host__ __device__ inline uint64_t seg_head(const ReduceSeg& s, int lanes) {
+  const uint64_t mis = s.elem_off % lanes;
+  uint64_t h = mis ? uint64_t(lanes) - mis : 0;
+  return h > s.elems ? s.elems : h;
+}
+
+__host__ __device__ inline uint64_t seg_tiles(const ReduceSeg& s, int lanes) {
+  if (s.elems == 0) return 0;
+  if (s.vec) {
+    const uint64_t nvec = (s.elems - seg_head(s, lanes)) / lanes;
+    const uint64_t t = (nvec + kTileVecs - 1) / kTileVecs;
+    return t ? t : 1;
+  }
+  const uint64_t per = kTileVecs * lanes;
+  return (s.elems + per - 1) / per;
+}
+
+// ---------------------------------------------------------------- dtype traits
+struct TrF32 {
+  static constexpr int kLanes = 4;
+  static constexpr int kBytes = 4;
+  using Elem = uint32_t;
+  struct Acc { float v[4]; };
+  struct Acc1 { float v; };
+  __device__ static Acc widen(uint4 x) {
+    return {{__uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z), __uint_as_float(x.w)}};
+  }
+  __device__ static void add(Acc& a, uint4 x) {
+    a.v[0] = __fadd_rn(a.v[0], __uint_as_float(x.x));
+    a.v[1] = __fadd_rn(a.v[1], __uint_as_float(x.y));
+    a.v[2] = __fadd_rn(a.v[2], __uint_as_float(x.z));
+    a.v[3] = __fadd_rn(a.v[3], __uint_as_float(x.w));
+  }
+  __device__ static uint4 narrow(const Acc& a) {
+    return make_uint4(__float_as_uint(a.v[0]), __float_as_uint(a.v[1]), __float_as_uint(a.v[2]),
+                      __float_as_uint(a.v[3]));
+  }
+  __device__ static Acc1 widen1(Elem e) { return {__uint_as_float(e)}; }
+  __device__ static void add1(Acc1& a, Elem e) { a.v = __fadd_rn(a.v, __uint_as_float(e)); }
+  __device__ static Elem narrow1(const Acc1& a) { return __float_as_uint(a.v); }
+};
+
+struct TrI32 {
+  static constexpr int kLanes = 4;
+  static constexpr int kBytes = 4;
+  using Elem = uint32_t;
+  struct Acc { uint32_t v[4]; };
+  struct Acc1 { uint32_t v; };
+  __device__ static Acc widen(uint4 x) { return {{x.x, x.y, x.z, x.w}}; }
+  __device__ static void add(Acc& a, uint4 x) {
+    a.v[0] += x.x;
+    a.v[1] += x.y;
+    a.v[2] += x.z;
+    a.v[3] += x.w;
+  }
+  __device__ static uint4 narrow(const Acc& a) { return make_uint4(a.v[0], a.v[1], a.v[2], a.v[3]); }
+  __device__ static Acc1 widen1(Elem e) { return {e}; }
+  __device__ static void add1(Acc1& a, Elem e) { a.v += e; }
+  __device__ static Elem narrow1(const Acc1& a) { return a.v; }
+};
+
+struct TrBF16 {
+  static constexpr int kLanes = 8;
+  static constexpr int kBytes = 2;
+  using Elem = uint16_t;
+  struct Acc { float v[8]; };
+  struct Acc1 { float v; };
+  // Element 2w is the low half of 32-bit word w (little endian).
+  __device__ static float lo(uint32_t w) { return __uint_as_float(w << 16); }
+  __device__ static float hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+  __device__ static Acc widen(uint4 x) {
+    return {{lo(x.x), hi(x.x), lo(x.y), hi(x.y), lo(x.z), hi(x.z), lo(x.w), hi(x.w)}};
+  }
+  __device__ static void add(Acc& a, uint4 x) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      a.v[2 * i] = __fadd_rn(a.v[2 * i], lo(w[i]));
+      a.v[2 * i + 1] = __fadd_rn(a.v[2 * i + 1], hi(w[i]));
+    }
+  }
+  __device__ static uint32_t pack(float a, float b) {
+    const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(a));
+    const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(b));
+    return l | (h << 16);
+  }
+  __device__ static uint4 narrow(const Acc& a) {
+    return make_uint4(pack(a.v[0], a.v[1]), pack(a.v[2], a.v[3]), pack(a.v[4], a.v[5]), pack(a.v[6], a.v[7]));
+  }
+  __device__ static Acc1 widen1(Elem e) { return {__uint_as_float(uint32_t(e) << 16)}; }
+  __device__ static void add1(Acc1& a, Elem e) { a.v = __fadd_rn(a.v, __uint_as_float(uint32_t(e) << 16)); }
+  __device__ static Elem narrow1(const Acc1& a) { return __bfloat16_as_ushort(__float2bfloat16_rn(a.v)); }
+};
+
+__device__ __forceinline__ const void* at(const void* base, uint64_t elem, int bytes) {
+  return static_cast<const char*>(base) + elem * uint64_t(bytes);
+}
+__device__ __forceinline__ void* at(void* base, uint64_t elem, int bytes) {
+  return static_cast<char*>(base) + elem * uint64_t(bytes);
+}
+
+template <class Tr>
+__device__ __forceinline__ void store_vec(const ReduceParams& p, uint32_t owner, int k, uint64_t o, uint4 y) {
+  if (p.broadcast) {
+    for (int r = 0; r < k; ++r) *static_cast<uint4*>(at(p.out[r], o, Tr::kBytes)) = y;
+  } else {
+    *static_cast<uint4*>(at(p.out[owner], o, Tr::kBytes)) = y;
+  }
+}
+
+// One element through the scalar path (heads, tails, misaligned segments).
+template <class Tr>
+__device__ __forceinline__ void scalar_elem(const ReduceParams& p, const uint8_t* seq, uint32_t owner, int k,
+                                            uint64_t e, uint64_t o) {
+  using E = typename Tr::Elem;
+  typename Tr::Acc1 acc = Tr::widen1(*static_cast<const E*>(at(p.in[seq[0]], e, Tr::kBytes)));
+  for (int j = 1; j < k; ++j) Tr::add1(acc, *static_cast<const E*>(at(p.in[seq[j]], e, Tr::kBytes)));
+  const E y = Tr::narrow1(acc);
+  if (p.broadcast) {
+    for (int r = 0; r < k; ++r) *static_cast<E*>(at(p.out[r], o, Tr::kBytes)) = y;
+  } else {
+    *static_cast<E*>(at(p.out[owner], o, Tr::kBytes)) = y;
+  }
+}
+
+// K > 0: compile-time rank count (all loads hoisted); K == 0: runtime p.k.
+template <class Tr, int K>
+__global__ void __launch_bounds__(kThreads) reduce_kernel(const __grid_constant__ ReduceParams p) {
+  constexpr int L = Tr::kLanes;
+  const int k = K > 0 ? K : p.k;
+  const uint64_t total = p.tile_start[p.nseg];
+  for (uint64_t t = blockIdx.x; t < total; t += gridDim.x) {
+    int s = 0;
+    while (t >= p.tile_start[s + 1]) ++s;
+    const ReduceSeg& sg = p.seg[s];
+    const uint64_t lt = t - p.tile_start[s];
+    const uint8_t* seq = p.seq[sg.owner];
+    if (sg.vec) {
+      const uint64_t head = seg_head(sg, L);
+      const uint64_t body = sg.elems - head;
+      const uint64_t nvec = body / L;
+      const uint64_t e0 = sg.elem_off + head;
+      const uint64_t o0 = sg.out_off + head;
+      const uint64_t vbase = lt * kTileVecs + threadIdx.x;
+      if constexpr (K > 0) {
+        uint4 x[K][kVecPerThread];
+#pragma unroll
+        for (int i = 0; i < kVecPerThread; ++i) {
+          const uint64_t v = vbase + uint64_t(i) * kThreads;
+          if (v < nvec) {
+#pragma unroll
+            for (int j = 0; j < K; ++j) x[j][i] = __ldcs(static_cast<const uint4*>(at(p.in[seq[j]], e0 + v * L, Tr::kBytes)));
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < kVecPerThread; ++i) {
+          const uint64_t v = vbase + uint64_t(i) * kThreads;
+          if (v < nvec) {
+            typename Tr::Acc acc = Tr::widen(x[0][i]);
+#pragma unroll
+            for (int j = 1; j < K; ++j) Tr::add(acc, x[j][i]);
+            store_vec<Tr>(p, sg.owner, K, o0 + v * L, Tr::narrow(acc));
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < kVecPerThread; ++i) {
+          const uint64_t v = vbase + uint64_t(i) * kThreads;
+          if (v < nvec) {
+            typename Tr::Acc acc = Tr::widen(__ldcs(static_cast<const uint4*>(at(p.in[seq[0]], e0 + v * L, Tr::kBytes))));
+            for (int j = 1; j < k; ++j)
+              Tr::add(acc, __ldcs(static_cast<const uint4*>(at(p.in[seq[j]], e0 + v * L, Tr::kBytes))));
+            store_vec<Tr>(p, sg.owner, k, o0 + v * L, Tr::narrow(acc));
+          }
+        }
+      }
+      if (lt == 0 && threadIdx.x < head) scalar_elem<Tr>(p, seq, sg.owner, k, sg.elem_off + threadIdx.x, sg.out_off + threadIdx.x);
+      const uint64_t tail = body - nvec * L;
+      const uint64_t last = p.tile_start[s + 1] - p.tile_start[s] - 1;
+      if (lt == last && threadIdx.x < tail)
+        scalar_elem<Tr>(p, seq, sg.owner, k, e0 + nvec * L + threadIdx.x, o0 + nvec * L + threadIdx.x);
+    } else {
+      const uint64_t base = lt * kTileVecs * L;
+#pragma unroll 4
+      for (int i = 0; i < kVecPerThread * L; ++i) {
+        const uint64_t e = base + uint64_t(i) * kThreads + threadIdx.x;
+        if (e < sg.elems) scalar_elem<Tr>(p, seq, sg.owner, k, sg.elem_off + e, sg.out_off + e);
+      }
+    }
+  }
+}
+
+template <class Tr>
+const void* pick_kernel(int k) {
+  switch (k) {
+    case 2: return reinterpret_cast<const void*>(&reduce_kernel<Tr, 2>);
+    case 3: return reinterpret_cast<const void*>(&reduce_kernel<Tr, 3>);
+    case 4: return reinterpret_cast<const void*>(&reduce_kernel<Tr, 4>);
+    case 5: return reinterpret_cast<const void*>(&reduce_kernel<Tr, 5>);
+    case 6: return reinterpret_cast<const void*>(&reduce_kernel<Tr, 6>);
+    case 7: return reinterpret_cast<const void*>(&reduce_kernel<Tr, 7>);
+    case 8: return reinterpret_cast<const void*>(&reduce_kernel<Tr, 8>);
+    default: return reinterpret_cast<const void*>(&reduce_kernel<Tr, 0>);
+  }
+}
+
+const void* kernel_for(int dtype, int k) {
+  switch (dtype) {
+    case HOC_FLOAT32: return pick_kernel<TrF32>(k);
+    case HOC_INT32: return pick_kernel<TrI32>(k);
+    case HOC_BFLOAT16: return pick_kernel<TrBF16>(k);
+    default: return nullptr;
+  }
+}
+
+}  // namespace
+
+uint64_t reduce_tile_elems(int dtype) { return kTileVecs * uint64_t(lanes_of(dtype)); }
+
+uint64_t reduce_seg_tiles(int dtype, const ReduceSeg& s) { return seg_tiles(s, lanes_of(dtype)); }
+
+int reduce_ctas_per_sm(int dtype, int k, int /*broadcast*/) {
+  const void* fn = kernel_for(dtype, k);
+  if (!fn) return 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, 0) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    return 1;
+  }
+  return n;
+}
+
+cudaError_t launch_reduce(const ReduceParams& p, int grid, cudaStream_t stream) {
+  const void* fn = kernel_for(p.dtype, p.k);
+  if (!fn) return cudaErrorInvalidValue;
+  if (grid < 1) return cudaSuccess;
+  void* args[] = {const_cast<ReduceParams*>(&p)};
+  return cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, 0, stream);
+}
+
+}  // namespace hoc

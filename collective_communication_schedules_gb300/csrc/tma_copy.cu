@@ -1,0 +1,235 @@
+// SM-driven chunk mover: bulk asynchronous copies (cp.async.bulk) through
+// shared memory, the comparison path to the copy-engine executor.
+//
+// HOCCL's point-to-point executor (section 3.3) moves every chunk with a DMA
+// engine so that no SM takes part.  This kernel does the same moves from SMs,
+// the way SM-based communication libraries do (section 2.2.1, Fig. 1a), but
+// with the Blackwell tensor-memory accelerator: one thread per CTA issues
+// global->shared bulk loads that complete on an mbarrier, then shared->global
+// bulk stores, keeping kStages pieces in flight.  A CTA has two warps: lane 0
+// of warp 0 drives the bulk pipeline; warp 1 copies the bytes a bulk copy
+// cannot take (heads and tails that are not 16-byte aligned, and jobs whose
+// source and destination are aligned differently).
+//
+// Every wait is bounded by the global timer.  On a timeout the kernel writes a
+// status code to p.status, waits (again bounded) for its own copies in flight
+// and returns; the host reports HOC_ERR_TIMEOUT.
+#include "hoc_internal.h"
+
+namespace hoc {
+namespace {
+
+constexpr int kStages = 4;
+constexpr uint32_t kPieceBytes = 32768;
+constexpr int kCopyThreads = 64;
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t tx) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(tx) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t deadline) {
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() > deadline) return false;
+  }
+  return true;
+}
+__device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst_smem)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_addr(src_smem)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__host__ __device__ inline bool co_aligned(const CopyJob& j) {
+  return ((reinterpret_cast<uintptr_t>(j.src) ^ reinterpret_cast<uintptr_t>(j.dst)) & 15u) == 0;
+}
+__host__ __device__ inline uint64_t job_head(const CopyJob& j) {
+  const uint64_t mis = reinterpret_cast<uintptr_t>(j.src) & 15u;
+  const uint64_t h = mis ? 16 - mis : 0;
+  return h > j.bytes ? j.bytes : h;
+}
+__host__ __device__ inline uint64_t job_body(const CopyJob& j) { return (j.bytes - job_head(j)) & ~uint64_t(15); }
+__host__ __device__ inline uint64_t job_pieces(const CopyJob& j, uint32_t pb) {
+  if (j.bytes == 0) return 0;
+  const uint64_t span = co_aligned(j) ? job_body(j) : j.bytes;
+  const uint64_t n = (span + pb - 1) / pb;
+  return n ? n : 1;
+}
+
+// Which job owns global piece `pc`, and the piece's index inside it.
+__device__ __forceinline__ int find_job(const CopyParams& p, uint64_t pc) {
+  int lo = 0, hi = p.njobs - 1;
+  while (lo < hi) {  // last job with piece_start <= pc
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.piece_start[mid] <= pc) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Bulk part of a piece: [off, off + n) bytes of its job (n == 0: none).
+__device__ __forceinline__ void piece_bulk(const CopyParams& p, uint64_t pc, const char*& src, char*& dst,
+                                           uint32_t& n) {
+  const int j = find_job(p, pc);
+  const CopyJob& jb = p.job[j];
+  n = 0;
+  if (!co_aligned(jb)) return;
+  const uint64_t i = pc - p.piece_start[j];
+  const uint64_t body = job_body(jb);
+  const uint64_t off = i * p.piece_bytes;
+  if (off >= body) return;
+  const uint64_t len = body - off < p.piece_bytes ? body - off : p.piece_bytes;
+  const uint64_t h = job_head(jb);
+  src = jb.src + h + off;
+  dst = jb.dst + h + off;
+  n = static_cast<uint32_t>(len);
+}
+
+__device__ __forceinline__ void copy_bytes(const char* src, char* dst, uint64_t n, int lane) {
+  for (uint64_t i = lane; i < n; i += 32) dst[i] = src[i];
+}
+
+__global__ void __launch_bounds__(kCopyThreads, 1) tma_copy_kernel(const __grid_constant__ CopyParams p) {
+  extern __shared__ __align__(128) unsigned char stage_mem[];
+  __shared__ __align__(8) uint64_t bar[kStages];
+  const uint64_t total = p.piece_start[p.njobs];
+  const uint64_t mine = total > blockIdx.x ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&bar[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+
+  if (warp == 1) {
+    // Bytes outside the bulk bodies.
+    for (uint64_t i = 0; i < mine; ++i) {
+      const uint64_t pc = blockIdx.x + i * gridDim.x;
+      const int j = find_job(p, pc);
+      const CopyJob& jb = p.job[j];
+      const uint64_t local = pc - p.piece_start[j];
+      if (!co_aligned(jb)) {
+        const uint64_t off = local * p.piece_bytes;
+        const uint64_t len = jb.bytes - off < p.piece_bytes ? jb.bytes - off : p.piece_bytes;
+        copy_bytes(jb.src + off, jb.dst + off, len, lane);
+      } else if (local == 0) {
+        const uint64_t h = job_head(jb);
+        const uint64_t end = h + job_body(jb);
+        copy_bytes(jb.src, jb.dst, h, lane);
+        copy_bytes(jb.src + end, jb.dst + end, jb.bytes - end, lane);
+      }
+    }
+    return;
+  }
+  if (lane != 0) return;
+
+  // Bulk pipeline: loads run kStages ahead of stores.
+  uint32_t stage_bytes[kStages];
+  char* stage_dst[kStages];
+  uint64_t next = 0;  // next of my pieces to look at for a load
+  uint32_t nload = 0, nstore = 0;
+  auto issue_next_load = [&]() -> bool {
+    while (next < mine) {
+      const uint64_t pc = blockIdx.x + next * gridDim.x;
+      ++next;
+      const char* src;
+      char* dst;
+      uint32_t n;
+      piece_bulk(p, pc, src, dst, n);
+      if (n == 0) continue;
+      const int s = nload % kStages;
+      stage_bytes[s] = n;
+      stage_dst[s] = dst;
+      mbar_arrive_expect_tx(&bar[s], n);
+      bulk_load(stage_mem + size_t(s) * p.piece_bytes, src, n, &bar[s]);
+      ++nload;
+      return true;
+    }
+    return false;
+  };
+  for (int s = 0; s < kStages; ++s)
+    if (!issue_next_load()) break;
+  bool failed = false;
+  while (nstore < nload) {
+    const int s = nstore % kStages;
+    if (!mbar_wait_bounded(&bar[s], (nstore / kStages) & 1u, global_ns() + kWaitNs)) {
+      failed = true;
+      break;
+    }
+    bulk_store(stage_dst[s], stage_mem + size_t(s) * p.piece_bytes, stage_bytes[s]);
+    bulk_commit();
+    ++nstore;
+    if (nstore >= 2) {
+      // once the store before this one has read its stage, refill that stage
+      bulk_wait_read_1();
+      issue_next_load();
+    }
+  }
+  if (failed) {
+    atomicExch(p.status, kStatusTimeoutLoad);
+    // Drain: every load still in flight, bounded again.
+    const uint64_t deadline = global_ns() + kWaitNs;
+    for (uint32_t b = nstore; b < nload; ++b) {
+      if (!mbar_wait_bounded(&bar[b % kStages], (b / kStages) & 1u, deadline)) {
+        atomicExch(p.status, kStatusTimeoutDrain);
+        break;
+      }
+    }
+  }
+  bulk_wait_all();
+}
+
+}  // namespace
+
+uint32_t tma_piece_bytes() { return kPieceBytes; }
+
+uint64_t tma_job_pieces(const CopyJob& j, uint32_t piece_bytes) { return job_pieces(j, piece_bytes); }
+
+int tma_ctas_per_sm() { return 1; }
+
+cudaError_t tma_prepare() {
+  return cudaFuncSetAttribute(reinterpret_cast<const void*>(&tma_copy_kernel),
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, int(kStages * kPieceBytes));
+}
+
+cudaError_t launch_tma_copy(const CopyParams& p, int grid, cudaStream_t stream) {
+  if (grid < 1 || p.njobs < 1) return cudaSuccess;
+  if (p.piece_bytes != kPieceBytes) return cudaErrorInvalidValue;
+  void* args[] = {const_cast<CopyParams*>(&p)};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(&tma_copy_kernel), dim3(grid), dim3(kCopyThreads), args,
+                          size_t(kStages) * kPieceBytes, stream);
+}
+
+}  // namespace hoc

@@ -1,0 +1,95 @@
+// Kernels that run beside the collectives: the compute-bound FMA probe whose
+// slowdown measures SM contention (HOCCL section 2.1, Eq. 1 and Fig. 2b) and
+// the XOR transform that stands in for a pipeline stage's compute.
+#include "hoc_internal.h"
+#include "hoc_workload.h"
+
+namespace hoc {
+namespace {
+
+// Eight independent FMA chains per thread; no memory traffic.  The only store
+// happens if the result equals a sentinel the chains cannot reach (their
+// values stay in (0, 1]), which keeps the compiler from removing the work.
+__global__ void probe_kernel(int iters, float* sink) {
+  float a[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) a[j] = 0.5f + 0.0625f * j + 1e-7f * threadIdx.x;
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) a[j] = fmaf(a[j], 0.999f, 0.0005f);
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) s += a[j];
+  if (s == -1.0f && sink != nullptr) sink[0] = s;
+}
+
+// 16-byte vectors of eight 16-bit words; a scalar loop covers the unaligned
+// head and the tail.
+__global__ void xor16_kernel(const uint16_t* __restrict__ in, uint16_t* __restrict__ out, size_t n, uint32_t key2,
+                             size_t head, size_t nvec) {
+  const size_t tid = blockIdx.x * size_t(blockDim.x) + threadIdx.x;
+  const size_t stride = size_t(gridDim.x) * blockDim.x;
+  const uint4* vin = reinterpret_cast<const uint4*>(in + head);
+  uint4* vout = reinterpret_cast<uint4*>(out + head);
+  for (size_t v = tid; v < nvec; v += stride) {
+    uint4 x = __ldcs(vin + v);
+    x.x ^= key2;
+    x.y ^= key2;
+    x.z ^= key2;
+    x.w ^= key2;
+    __stcs(vout + v, x);
+  }
+  const uint16_t key = static_cast<uint16_t>(key2 & 0xFFFFu);
+  const size_t tail0 = head + nvec * 8;
+  for (size_t i = tid; i < head; i += stride) out[i] = in[i] ^ key;
+  for (size_t i = tid; i < n - tail0; i += stride) out[tail0 + i] = in[tail0 + i] ^ key;
+}
+
+}  // namespace
+}  // namespace hoc
+
+extern "C" hocResult_t hoc_probe_launch(void* stream, int ctas, int threads, int iters, float* sink) {
+  if (ctas < 1 || threads < 32 || threads > 1024 || (threads % 32) != 0 || iters < 0) return HOC_ERR_INVALID_ARG;
+  hoc::probe_kernel<<<ctas, threads, 0, static_cast<cudaStream_t>(stream)>>>(iters, sink);
+  return cudaGetLastError() == cudaSuccess ? HOC_SUCCESS : HOC_ERR_CUDA;
+}
+
+extern "C" hocResult_t hoc_xor16_launch(void* stream, const uint16_t* in, uint16_t* out, size_t n, uint16_t key) {
+  if (n == 0) return HOC_SUCCESS;
+  if (in == nullptr || out == nullptr) return HOC_ERR_INVALID_ARG;
+  const uintptr_t ai = reinterpret_cast<uintptr_t>(in), ao = reinterpret_cast<uintptr_t>(out);
+  if ((ai & 1u) || (ao & 1u)) return HOC_ERR_INVALID_ARG;
+  if (ai != ao && ai < ao + 2 * n && ao < ai + 2 * n) return HOC_ERR_INVALID_ARG;
+  size_t head = 0, nvec = 0;
+  if (((ai ^ ao) & 15u) == 0) {
+    head = ((16 - (ai & 15u)) & 15u) / 2;
+    if (head > n) head = n;
+    nvec = (n - head) / 8;
+  } else {
+    head = n;  // no common alignment: every word through the scalar path
+  }
+  int dev = 0, sms = 1;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const size_t scalar = head > 8 ? head : 8;
+  size_t want = (nvec > scalar ? nvec : scalar) + 255;
+  want /= 256;
+  const size_t cap = size_t(sms) * 8;
+  const int grid = static_cast<int>(want < cap ? want : cap);
+  const uint32_t key2 = uint32_t(key) | (uint32_t(key) << 16);
+  hoc::xor16_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(in, out, n, key2, head, nvec);
+  return cudaGetLastError() == cudaSuccess ? HOC_SUCCESS : HOC_ERR_CUDA;
+}
+
+extern "C" hocResult_t hoc_device_sm_count(int device, int* sms) {
+  if (sms == nullptr) return HOC_ERR_INVALID_ARG;
+  int n = 0;
+  if (cudaGetDeviceCount(&n) != cudaSuccess || n == 0) {
+    cudaGetLastError();
+    return HOC_ERR_NO_DEVICE;
+  }
+  if (device < 0 || device >= n) return HOC_ERR_INVALID_ARG;
+  return cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, device) == cudaSuccess ? HOC_SUCCESS
+                                                                                             : HOC_ERR_CUDA;
+}

@@ -1,0 +1,298 @@
+"""Python binding of libhoc.so (ctypes).  Argument marshalling only.
+
+Every collective runs in the library's CUDA kernels and copy-engine copies;
+this module converts tensors (or raw device pointers) and streams into the
+C ABI declared in include/hoc.h and turns result codes into exceptions.  If
+the library is missing it raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass, field
+from typing import Optional, Sequence
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libhoc.so")
+
+SUCCESS, ERR_INVALID_ARG, ERR_CUDA, ERR_OOM, ERR_NOT_INITIALIZED, ERR_UNSUPPORTED, ERR_TIMEOUT, ERR_NO_DEVICE = range(8)
+INT32, FLOAT32, BFLOAT16, UINT8 = 0, 1, 2, 3
+SUM = 0
+PATH_AUTO, PATH_CE, PATH_TMA, PATH_FUSED = 0, 1, 2, 3
+KERNEL_REDUCE, KERNEL_FUSED, KERNEL_TMA = 0, 1, 2
+OP_ALLREDUCE, OP_REDUCE_SCATTER, OP_ALLGATHER, OP_ALLTOALL, OP_SENDRECV = range(5)
+ITEM_REDUCE, ITEM_FUSED, ITEM_COPY, ITEM_TMA, ITEM_JOIN = range(5)
+BUF_SEND, BUF_RECV = 0, 1
+MAX_RANKS = 16
+PATHS = {"auto": PATH_AUTO, "ce": PATH_CE, "tma": PATH_TMA, "fused": PATH_FUSED}
+
+
+class HocError(RuntimeError):
+    def __init__(self, code: int, where: str, detail: str):
+        self.code = code
+        super().__init__(f"{where}: {error_string(code)} ({code}): {detail}")
+
+
+class _Config(C.Structure):
+    _fields_ = [("path", C.c_int), ("chunk_bytes", C.c_size_t), ("n_copy_streams", C.c_int),
+                ("pipeline_depth", C.c_int), ("reduce_max_sms", C.c_int), ("copy_max_sms", C.c_int),
+                ("use_graphs", C.c_int), ("a2a_interleave", C.c_int), ("a2a_stage_sync", C.c_int),
+                ("ring_order", C.POINTER(C.c_int))]
+
+
+class _Stats(C.Structure):
+    _fields_ = [("path", C.c_int), ("kernels", C.c_int), ("copies", C.c_int), ("max_ctas", C.c_int),
+                ("sms_used", C.c_int), ("graph_replayed", C.c_int), ("bytes_exec", C.c_size_t),
+                ("bytes_min", C.c_size_t)]
+
+
+class _PlanItem(C.Structure):
+    _fields_ = [("kind", C.c_int), ("step", C.c_int), ("stream", C.c_int), ("stage", C.c_int),
+                ("src_rank", C.c_int), ("dst_rank", C.c_int), ("src_buf", C.c_int), ("dst_buf", C.c_int),
+                ("src_off", C.c_size_t), ("dst_off", C.c_size_t), ("bytes", C.c_size_t),
+                ("n_waits", C.c_int), ("wait0", C.c_int)]
+
+
+_lib = None
+
+# Exported symbol -> (restype, argtypes)
+_SIGS = {
+    "hoc_config_default": (C.c_int, [C.POINTER(_Config)]),
+    "hoc_init": (C.c_int, [C.POINTER(C.c_void_p), C.c_int, C.c_int, C.POINTER(_Config)]),
+    "hoc_destroy": (C.c_int, [C.c_void_p]),
+    "hoc_allreduce": (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_size_t, C.c_int,
+                                C.c_int, C.c_void_p]),
+    "hoc_reduce_scatter": (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_size_t,
+                                     C.c_int, C.c_int, C.c_void_p]),
+    "hoc_allgather": (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_size_t, C.c_int,
+                                C.c_void_p]),
+    "hoc_alltoall": (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.POINTER(C.c_size_t), C.POINTER(C.c_size_t),
+                               C.POINTER(C.c_void_p), C.POINTER(C.c_size_t), C.c_size_t, C.c_int, C.c_void_p]),
+    "hoc_sendrecv": (C.c_int, [C.c_void_p, C.c_int, C.c_void_p, C.c_int, C.c_void_p, C.c_size_t, C.c_int,
+                               C.c_void_p]),
+    "hoc_wait": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int]),
+    "hoc_last_stats": (C.c_int, [C.c_void_p, C.POINTER(_Stats)]),
+    "hoc_profile_enable": (C.c_int, [C.c_void_p, C.c_int]),
+    "hoc_profile_read": (C.c_int, [C.c_void_p, C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_double)]),
+    "hoc_error_string": (C.c_char_p, [C.c_int]),
+    "hoc_last_error_detail": (C.c_char_p, []),
+    "hoc_plan_query": (C.c_int, [C.c_int, C.POINTER(_Config), C.c_int, C.c_size_t, C.c_int, C.POINTER(C.c_size_t),
+                                 C.POINTER(_PlanItem), C.c_size_t, C.POINTER(C.c_size_t)]),
+    "hoc_probe_launch": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p]),
+    "hoc_xor16_launch": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_uint16]),
+    "hoc_device_sm_count": (C.c_int, [C.c_int, C.POINTER(C.c_int)]),
+}
+
+
+def lib():
+    """Load libhoc.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m collective_communication_schedules_gb300.build`")
+        h = C.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(h, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = h
+    return _lib
+
+
+def error_string(code: int) -> str:
+    return lib().hoc_error_string(code).decode()
+
+
+def last_error_detail() -> str:
+    return lib().hoc_last_error_detail().decode()
+
+
+def _check(code: int, where: str):
+    if code != SUCCESS:
+        raise HocError(code, where, last_error_detail())
+
+
+# ----------------------------------------------------------------- marshalling
+def _dtype_code(x) -> int:
+    import torch
+    m = {torch.int32: INT32, torch.float32: FLOAT32, torch.bfloat16: BFLOAT16, torch.uint8: UINT8}
+    if x.dtype not in m:
+        raise TypeError(f"unsupported tensor dtype {x.dtype}")
+    return m[x.dtype]
+
+
+def _ptr(x) -> int:
+    if isinstance(x, int):
+        return x
+    if not x.is_cuda:
+        raise ValueError("rank buffers must be CUDA tensors")
+    return x.data_ptr()
+
+
+def _ptr_array(xs: Sequence) -> C.Array:
+    return (C.c_void_p * len(xs))(*[_ptr(x) for x in xs])
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _sizes(vals, n) -> Optional[C.Array]:
+    if vals is None:
+        return None
+    flat = [int(v) for row in vals for v in (row if hasattr(row, "__len__") else [row])]
+    if len(flat) != n:
+        raise ValueError(f"expected {n} values, got {len(flat)}")
+    return (C.c_size_t * n)(*flat)
+
+
+@dataclass
+class Config:
+    path: str = "auto"
+    chunk_bytes: int = 4 << 20
+    n_copy_streams: int = 4
+    pipeline_depth: int = 0
+    reduce_max_sms: int = 0
+    copy_max_sms: int = 0
+    use_graphs: bool = True
+    a2a_interleave: bool = True
+    a2a_stage_sync: bool = False
+    ring_order: Optional[Sequence[int]] = None
+    _keep: list = field(default_factory=list, repr=False)
+
+    def to_c(self) -> _Config:
+        c = _Config()
+        c.path = PATHS[self.path] if isinstance(self.path, str) else int(self.path)
+        c.chunk_bytes = int(self.chunk_bytes)
+        c.n_copy_streams = int(self.n_copy_streams)
+        c.pipeline_depth = int(self.pipeline_depth)
+        c.reduce_max_sms = int(self.reduce_max_sms)
+        c.copy_max_sms = int(self.copy_max_sms)
+        c.use_graphs = int(bool(self.use_graphs))
+        c.a2a_interleave = int(bool(self.a2a_interleave))
+        c.a2a_stage_sync = int(bool(self.a2a_stage_sync))
+        if self.ring_order is not None:
+            arr = (C.c_int * len(self.ring_order))(*[int(v) for v in self.ring_order])
+            self._keep = [arr]
+            c.ring_order = C.cast(arr, C.POINTER(C.c_int))
+        else:
+            c.ring_order = None
+        return c
+
+
+class Comm:
+    """A communicator over `nranks` simulated ranks on one CUDA device."""
+
+    def __init__(self, nranks: int, device: int = 0, config: Optional[Config] = None):
+        self.k = nranks
+        self.device = device
+        self.config = config or Config()
+        h = C.c_void_p()
+        cfg = self.config.to_c()
+        _check(lib().hoc_init(C.byref(h), nranks, device, C.byref(cfg)), "hoc_init")
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None):
+            _check(lib().hoc_destroy(self._h), "hoc_destroy")
+            self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ------------------------------------------------------------ collectives
+    def allreduce(self, send, recv, count=None, dtype=None, stream=None):
+        count = send[0].numel() if count is None else count
+        dtype = _dtype_code(send[0]) if dtype is None else dtype
+        _check(lib().hoc_allreduce(self._h, _ptr_array(send), _ptr_array(recv), count, dtype, SUM,
+                                   _stream(stream)), "hoc_allreduce")
+
+    def reduce_scatter(self, send, recv, recvcount=None, dtype=None, stream=None):
+        recvcount = recv[0].numel() if recvcount is None else recvcount
+        dtype = _dtype_code(send[0]) if dtype is None else dtype
+        _check(lib().hoc_reduce_scatter(self._h, _ptr_array(send), _ptr_array(recv), recvcount, dtype, SUM,
+                                        _stream(stream)), "hoc_reduce_scatter")
+
+    def allgather(self, send, recv, sendcount=None, dtype=None, stream=None):
+        sendcount = send[0].numel() if sendcount is None else sendcount
+        dtype = _dtype_code(send[0]) if dtype is None else dtype
+        _check(lib().hoc_allgather(self._h, _ptr_array(send), _ptr_array(recv), sendcount, dtype,
+                                   _stream(stream)), "hoc_allgather")
+
+    def alltoall(self, send, recv, sendcounts=None, sdispls=None, rdispls=None, count=0, dtype=None,
+                 stream=None):
+        """sendcounts: k x k (row = source) in elements; None = uniform `count`."""
+        dtype = _dtype_code(send[0]) if dtype is None else dtype
+        kk = self.k * self.k
+        _check(lib().hoc_alltoall(self._h, _ptr_array(send), _sizes(sendcounts, kk), _sizes(sdispls, kk),
+                                  _ptr_array(recv), _sizes(rdispls, kk), int(count), dtype, _stream(stream)),
+               "hoc_alltoall")
+
+    def sendrecv(self, src_rank, send, dst_rank, recv, count=None, dtype=None, stream=None):
+        count = send.numel() if count is None else count
+        dtype = _dtype_code(send) if dtype is None else dtype
+        _check(lib().hoc_sendrecv(self._h, int(src_rank), _ptr(send), int(dst_rank), _ptr(recv), count, dtype,
+                                  _stream(stream)), "hoc_sendrecv")
+
+    # ------------------------------------------------------------- control
+    def wait(self, stream=None, timeout_ms: int = 60000):
+        _check(lib().hoc_wait(self._h, _stream(stream), int(timeout_ms)), "hoc_wait")
+
+    def last_stats(self) -> dict:
+        s = _Stats()
+        _check(lib().hoc_last_stats(self._h, C.byref(s)), "hoc_last_stats")
+        return {name: getattr(s, name) for name, _ in _Stats._fields_}
+
+    def profile_enable(self, on: bool = True):
+        _check(lib().hoc_profile_enable(self._h, int(bool(on))), "hoc_profile_enable")
+
+    def profile_read(self, kernel: int):
+        n = C.c_int()
+        ms = C.c_double()
+        _check(lib().hoc_profile_read(self._h, int(kernel), C.byref(n), C.byref(ms)), "hoc_profile_read")
+        return n.value, ms.value
+
+
+# ---------------------------------------------------------------- workload
+def probe_launch(ctas: int, threads: int, iters: int, sink=None, stream=None):
+    _check(lib().hoc_probe_launch(_stream(stream), int(ctas), int(threads), int(iters),
+                                  None if sink is None else _ptr(sink)), "hoc_probe_launch")
+
+
+def xor16(src, dst, n: int, key: int, stream=None):
+    _check(lib().hoc_xor16_launch(_stream(stream), _ptr(src), _ptr(dst), int(n), int(key) & 0xFFFF),
+           "hoc_xor16_launch")
+
+
+def sm_count(device: int = 0) -> int:
+    n = C.c_int()
+    _check(lib().hoc_device_sm_count(int(device), C.byref(n)), "hoc_device_sm_count")
+    return n.value
+
+
+def plan_query(nranks: int, op: int, count: int, dtype: int, counts=None, config: Optional[Config] = None):
+    """The plan the scheduler would run, as a list of dicts (host only, no GPU)."""
+    cfg = (config or Config()).to_c()
+    cnt = _sizes(counts, nranks * nranks) if counts is not None else None
+    n = C.c_size_t()
+    _check(lib().hoc_plan_query(nranks, C.byref(cfg), op, int(count), dtype, cnt, None, 0, C.byref(n)),
+           "hoc_plan_query")
+    items = (_PlanItem * max(1, n.value))()
+    _check(lib().hoc_plan_query(nranks, C.byref(cfg), op, int(count), dtype, cnt, items, n.value, C.byref(n)),
+           "hoc_plan_query")
+    return [{name: getattr(items[i], name) for name, _ in _PlanItem._fields_} for i in range(n.value)]

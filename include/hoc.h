@@ -1,0 +1,215 @@
+/*
+ * hoc.h -- zero-SM collective schedules over k simulated ranks on one GPU.
+ *
+ * Operations follow "HOCCL: Offloading Collective Communication from GPU Cores
+ * to Accelerate Distributed Training":
+ *   - the stream manager (section 3.2, Fig. 4) orders each collective against
+ *     the kernels before and after it on the caller's stream;
+ *   - the point-to-point executor (section 3.3) moves every chunk as one
+ *     direct copy into the receiver's buffer, on copy engines (zero SMs) or,
+ *     for comparison, on a TMA bulk-copy kernel (SM-driven);
+ *   - the collective scheduler (section 3.4, Fig. 6) splits flows into chunks,
+ *     orders all-to-all flows into contention-free shift stages (Eq. 6-8) and
+ *     interleaves chunks in proportion to flow size on each copy queue.
+ * Reductions (AllReduce, ReduceScatter) are outside the paper's zero-SM scope
+ * (section 5, Limitations); here their arithmetic runs in a k-way reduce
+ * kernel that folds each block in ring order (see hoc_allreduce).
+ *
+ * Conventions for every call:
+ *   - Rank buffers are device pointers on the communicator's device, one per
+ *     simulated rank, owned by the caller.  Pointer arrays are host arrays
+ *     read during the call and not retained.
+ *   - Counts are in elements of `dtype`; a count of 0 is a successful no-op.
+ *   - Work is ordered after all prior work on `stream` and later work on
+ *     `stream` sees the results.  Calls never block the host (except the
+ *     first call of a new shape in graph mode, which builds a CUDA graph).
+ *     `stream` is a cudaStream_t; NULL is the legacy default stream.
+ *   - Errors are return codes; nothing is thrown across the ABI.  Errors of
+ *     asynchronous work show up in a later call or in hoc_wait().
+ *   - Buffers of different ranks must not overlap, except the in-place forms
+ *     stated per call.  Any alignment is accepted; 16-byte-aligned buffers
+ *     take the vector / bulk-copy paths, others the scalar paths.
+ */
+#ifndef HOC_H
+#define HOC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define HOC_MAX_RANKS 16
+
+typedef enum {
+  HOC_SUCCESS = 0,
+  HOC_ERR_INVALID_ARG = 1,     /* bad rank count, pointer, size, dtype, op, alias */
+  HOC_ERR_CUDA = 2,            /* a CUDA call failed; hoc_last_error_detail() says which */
+  HOC_ERR_OOM = 3,             /* host or device allocation failed */
+  HOC_ERR_NOT_INITIALIZED = 4, /* NULL communicator */
+  HOC_ERR_UNSUPPORTED = 5,     /* valid request this build does not implement */
+  HOC_ERR_TIMEOUT = 6,         /* a bounded wait (host or device) gave up */
+  HOC_ERR_NO_DEVICE = 7        /* no usable CUDA device */
+} hocResult_t;
+
+typedef enum { HOC_INT32 = 0, HOC_FLOAT32 = 1, HOC_BFLOAT16 = 2, HOC_UINT8 = 3 } hocDataType_t;
+typedef enum { HOC_SUM = 0 } hocRedOp_t;
+
+/* How chunk moves are executed. */
+typedef enum {
+  HOC_PATH_AUTO = 0,  /* allreduce -> FUSED; moves -> CE */
+  HOC_PATH_CE = 1,    /* cudaMemcpyAsync on internal copy streams: zero SMs */
+  HOC_PATH_TMA = 2,   /* cp.async.bulk kernel: SM-driven comparison path */
+  HOC_PATH_FUSED = 3  /* allreduce only: one kernel reduces and writes all k outputs */
+} hocPath_t;
+
+/* Communicator configuration; hoc_config_default() fills the defaults.
+ * Environment variables HOC_PATH (ce|tma|fused|auto), HOC_CHUNK_BYTES,
+ * HOC_COPY_STREAMS, HOC_USE_GRAPHS, HOC_REDUCE_MAX_SMS, HOC_DEBUG override
+ * the values passed in. */
+typedef struct {
+  int path;              /* hocPath_t */
+  size_t chunk_bytes;    /* pipeline unit inside a block / flow; default 4 MiB */
+  int n_copy_streams;    /* internal copy streams (the multi-QP analogue); default 4, max 16 */
+  int pipeline_depth;    /* allreduce CE/TMA: reduce of chunk q waits for the moves of
+                            chunk q - depth; 0 = no limit */
+  int reduce_max_sms;    /* cap on CTAs of reduce kernels (one CTA per SM); 0 = whole GPU */
+  int copy_max_sms;      /* CTAs of the TMA copy kernel; 0 = whole GPU */
+  int use_graphs;        /* 1: cache each call's issue sequence as a CUDA graph and replay it */
+  int a2a_interleave;    /* 1: flow-size-aware chunk interleave per copy queue; 0: per-flow FIFO */
+  int a2a_stage_sync;    /* 1: all copy queues join between all-to-all shift stages */
+  const int* ring_order; /* k ranks in ring order (a permutation); NULL = identity; copied */
+} hocConfig_t;
+
+typedef struct hocComm* hocComm_t;
+
+/* Statistics of the last collective issued on a communicator. */
+typedef struct {
+  int path;             /* path actually taken (hocPath_t) */
+  int kernels;          /* kernels of this library launched by the call */
+  int copies;           /* copy-engine copies issued by the call */
+  int max_ctas;         /* largest grid among those kernels */
+  int sms_used;         /* SMs those kernels can occupy: min(max_ctas, SM count); 0 on pure CE */
+  int graph_replayed;   /* 1 if the call replayed a cached CUDA graph */
+  size_t bytes_exec;    /* algorithmic HBM bytes of the executed schedule */
+  size_t bytes_min;     /* lower bound: read every input and write every output once */
+} hocOpStats_t;
+
+/* Kernel classes for hoc_profile_read(). */
+typedef enum { HOC_KERNEL_REDUCE = 0, HOC_KERNEL_FUSED = 1, HOC_KERNEL_TMA = 2 } hocKernel_t;
+
+/* Fill `cfg` with the defaults listed in hocConfig_t. Never fails for non-NULL cfg. */
+hocResult_t hoc_config_default(hocConfig_t* cfg);
+
+/* Create a communicator for `nranks` (1..HOC_MAX_RANKS) simulated ranks on CUDA
+ * device `device`.  `cfg` may be NULL (defaults).  The communicator owns its
+ * internal streams, events, plan and graph caches and a small device status
+ * buffer.  Returns HOC_ERR_NO_DEVICE without a GPU. */
+hocResult_t hoc_init(hocComm_t* comm, int nranks, int device, const hocConfig_t* cfg);
+
+/* Wait for the communicator's internal work, then free everything it owns. */
+hocResult_t hoc_destroy(hocComm_t comm);
+
+/* AllReduce (sum).  send[r], recv[r]: `count` elements each.  Each rank buffer
+ * is split into k blocks, B_r = floor(count/k) + (r < count mod k) elements,
+ * owned by rank r.  Block r is folded in ring order: start from rank succ(r),
+ * add succ^2(r), ..., end with r's own input (textbook ring reduce-scatter
+ * hop order; succ follows cfg.ring_order).  fp32 adds in binary32 with round to
+ * nearest even; bf16 widens to binary32, adds in binary32 and rounds once to
+ * bf16; int32 wraps modulo 2^32.  Every rank then receives every block (ring
+ * all-gather, section 6.2 "AllGather").  In place: send[r] == recv[r]. */
+hocResult_t hoc_allreduce(hocComm_t comm, const void* const* send, void* const* recv, size_t count,
+                          hocDataType_t dtype, hocRedOp_t op, void* stream);
+
+/* ReduceScatter (sum).  send[r] holds k*recvcount elements, recv[r] recvcount.
+ * recv[r] = block r of the fold above (block size recvcount for every rank).
+ * In place: recv[r] == (elem*)send[r] + r*recvcount. */
+hocResult_t hoc_reduce_scatter(hocComm_t comm, const void* const* send, void* const* recv,
+                               size_t recvcount, hocDataType_t dtype, hocRedOp_t op, void* stream);
+
+/* AllGather (section 6.2, "AllGather").  recv[d][r*sendcount ...] = send[r][0 .. sendcount).
+ * In place: send[r] == (elem*)recv[r] + r*sendcount. */
+hocResult_t hoc_allgather(hocComm_t comm, const void* const* send, void* const* recv,
+                          size_t sendcount, hocDataType_t dtype, void* stream);
+
+/* All-to-all(v) (section 6.2 "All-to-All"; traffic matrix C of section 3.4).
+ * sendcounts: k*k host array, row = source: rank s sends sendcounts[s*k+d]
+ * elements from send[s] + sdispls[s*k+d] to recv[d] + rdispls[d*k+s].
+ * sendcounts == NULL means the uniform exchange of `count_if_uniform`
+ * elements per pair.  sdispls / rdispls == NULL mean prefix sums in rank
+ * order.  Receive regions must not overlap each other or any send region. */
+hocResult_t hoc_alltoall(hocComm_t comm, const void* const* send, const size_t* sendcounts,
+                         const size_t* sdispls, void* const* recv, const size_t* rdispls,
+                         size_t count_if_uniform, hocDataType_t dtype, void* stream);
+
+/* Send/recv (section 3.3.2): move `count` elements from rank src_rank's buffer
+ * `send` into rank dst_rank's buffer `recv` with one direct copy (split into
+ * chunks over the copy queues).  src_rank may equal dst_rank. */
+hocResult_t hoc_sendrecv(hocComm_t comm, int src_rank, const void* send, int dst_rank, void* recv,
+                         size_t count, hocDataType_t dtype, void* stream);
+
+/* Bounded host wait: polls until all work on `stream` (and the communicator's
+ * internal streams) has finished, or `timeout_ms` ms pass (HOC_ERR_TIMEOUT).
+ * Also reports device-side timeouts of the TMA copy kernel (HOC_ERR_TIMEOUT). */
+hocResult_t hoc_wait(hocComm_t comm, void* stream, int timeout_ms);
+
+/* Statistics of the last collective issued on `comm`. */
+hocResult_t hoc_last_stats(hocComm_t comm, hocOpStats_t* stats);
+
+/* Per-kernel timing.  While enabled, every kernel this communicator launches
+ * is bracketed by CUDA events on the stream it is launched on (graphs are not
+ * used while enabled).  hoc_profile_read() waits for those events and returns,
+ * for one kernel class, the number of launches and their summed duration in
+ * milliseconds since the last read, then clears that class. */
+hocResult_t hoc_profile_enable(hocComm_t comm, int enable);
+hocResult_t hoc_profile_read(hocComm_t comm, hocKernel_t kernel, int* launches, double* total_ms);
+
+/* Static description of a result code. */
+const char* hoc_error_string(hocResult_t result);
+
+/* Text of the last CUDA or argument error seen by this process (thread-local). */
+const char* hoc_last_error_detail(void);
+
+/* ---------------------------------------------------------------------------
+ * Plan introspection (host only, needs no GPU).  Builds the plan a
+ * communicator with `cfg` would execute and returns it as a flat item list:
+ * one item per reduce segment, per copy, or per join.  Used to test the
+ * scheduler on machines without a GPU.
+ * ------------------------------------------------------------------------- */
+typedef enum { HOC_OP_ALLREDUCE = 0, HOC_OP_REDUCE_SCATTER = 1, HOC_OP_ALLGATHER = 2,
+               HOC_OP_ALLTOALL = 3, HOC_OP_SENDRECV = 4 } hocOp_t;
+typedef enum { HOC_ITEM_REDUCE = 0, HOC_ITEM_FUSED = 1, HOC_ITEM_COPY = 2, HOC_ITEM_TMA = 3,
+               HOC_ITEM_JOIN = 4 } hocItemKind_t;
+typedef enum { HOC_BUF_SEND = 0, HOC_BUF_RECV = 1 } hocBuf_t;
+
+typedef struct {
+  int kind;       /* hocItemKind_t */
+  int step;       /* index of the launch / copy step the item belongs to */
+  int stream;     /* 0 = caller stream, 1..n = internal copy streams */
+  int stage;      /* chunk index (allreduce, allgather) or shift stage (alltoall) */
+  int src_rank;   /* REDUCE/FUSED: -1 (all ranks are read) */
+  int dst_rank;   /* REDUCE/FUSED: block owner; FUSED writes every rank */
+  int src_buf;    /* hocBuf_t */
+  int dst_buf;    /* hocBuf_t */
+  size_t src_off; /* bytes from the start of the source rank buffer */
+  size_t dst_off; /* bytes from the start of the destination rank buffer */
+  size_t bytes;
+  int n_waits;    /* number of earlier steps this step waits on (cross-stream) */
+  int wait0;      /* first of them, -1 if none */
+} hocPlanItem_t;
+
+/* `op` is hocOp_t; `count` as in the matching call (recvcount for reduce
+ * scatter, sendcount for allgather, count_if_uniform for alltoall, count for
+ * sendrecv); `counts` is the k*k sendcounts matrix for alltoall or NULL.
+ * For sendrecv, src/dst ranks are 0 and 1 % nranks.  Writes at most `cap`
+ * items to `items` (may be NULL) and the full count to `n_items`. */
+hocResult_t hoc_plan_query(int nranks, const hocConfig_t* cfg, int op, size_t count,
+                           hocDataType_t dtype, const size_t* counts, hocPlanItem_t* items,
+                           size_t cap, size_t* n_items);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HOC_H */

@@ -1,0 +1,43 @@
+/*
+ * hoc_workload.h -- measurement and workload kernels that run beside the
+ * collectives (they are not collectives themselves).
+ *
+ * HOCCL section 2.1 defines the contention rate I_x (Eq. 1): the share of SMs
+ * that communication of class x occupies while compute kernels are active,
+ * and Fig. 2b shows compute slowing down as it grows.  The probe below is the
+ * compute kernel whose slowdown measures that contention on one GPU.  The XOR
+ * transform stands in for a pipeline stage's compute on its activations
+ * (section 2.1, PP overlaps activation transfers with compute) with an exact,
+ * invertible result.
+ */
+#ifndef HOC_WORKLOAD_H
+#define HOC_WORKLOAD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "hoc.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Compute-bound probe: `ctas` CTAs of `threads` threads on `stream`; each
+ * thread runs 8 independent FMA chains for `iters` iterations and touches no
+ * memory except one store to `sink` (device, >= 4 bytes, may be NULL) in the
+ * unreachable case that its result equals a sentinel.  ctas >= 1,
+ * 32 <= threads <= 1024 (a multiple of 32), iters >= 0. */
+hocResult_t hoc_probe_launch(void* stream, int ctas, int threads, int iters, float* sink);
+
+/* out[i] = in[i] XOR key for `n` 16-bit words (device pointers; in == out is
+ * allowed, other overlaps are not). */
+hocResult_t hoc_xor16_launch(void* stream, const uint16_t* in, uint16_t* out, size_t n, uint16_t key);
+
+/* Number of SMs of `device` (a query, no kernel). */
+hocResult_t hoc_device_sm_count(int device, int* sms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HOC_WORKLOAD_H */

@@ -1,0 +1,282 @@
+"""GPU parity: every collective through the C ABI against the CPU oracle.
+
+Small and ragged sizes that span several reduce tiles, TMA pieces and copy
+chunks; every path (copy engines, TMA bulk copies, fused reduce); in-place
+forms; misaligned pointers; guard bands around every buffer.
+"""
+import numpy as np
+import pytest
+import torch
+
+from collective_communication_schedules_gb300 import hoc, inputs
+from oracle import alltoall as o_a2a
+from oracle import ring as o_ring
+from tests.gpu_util import Guarded, assert_bits_equal, to_device, to_host
+
+pytestmark = pytest.mark.gpu
+
+SIZES = [1, 7, 4099, 70001]
+PATHS = ["ce", "tma", "fused"]
+
+
+def _inputs(dtype, k, n, seed):
+    rng = np.random.default_rng(seed)
+    if dtype == "float32":
+        return [(rng.standard_normal(n) * (2.0 ** rng.integers(-20, 20, n))).astype(np.float32) for _ in range(k)]
+    return inputs.rank_inputs(dtype, k, n, workload=7, slot=seed % 50)
+
+
+def _comm(k, path="auto", **kw):
+    return hoc.Comm(k, 0, hoc.Config(path=path, **kw))
+
+
+@pytest.mark.parametrize("dtype", ["int32", "float32", "bfloat16"])
+@pytest.mark.parametrize("k", [1, 2, 3, 4, 8])
+@pytest.mark.parametrize("path", PATHS)
+def test_allreduce_parity(dtype, k, path):
+    rng = np.random.default_rng(k * 31 + len(path))
+    for n in SIZES:
+        xs = _inputs(dtype, k, n, seed=n + k)
+        order = list(rng.permutation(k))
+        want = o_ring.allreduce(xs, dtype, order)
+        with _comm(k, path, chunk_bytes=4096, ring_order=order) as c:
+            send = [Guarded(n, dtype) for _ in range(k)]
+            recv = [Guarded(n, dtype) for _ in range(k)]
+            for g, x in zip(send, xs):
+                g.load(x)
+            c.allreduce([g.ptr() for g in send], [g.ptr() for g in recv], n, hoc.__dict__[dtype.upper()])
+            torch.cuda.synchronize()
+            c.wait()
+            for r in range(k):
+                recv[r].check()
+                send[r].check()
+                assert_bits_equal(recv[r].host(), want[r], dtype, f"{path} k={k} n={n} rank {r}")
+                assert_bits_equal(send[r].host(), xs[r], dtype, "send buffer modified")
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
+def test_allreduce_in_place_and_misaligned(path, dtype):
+    k, n = 4, 12345
+    xs = _inputs(dtype, k, n, seed=5)
+    want = o_ring.allreduce(xs, dtype)
+    code = hoc.FLOAT32 if dtype == "float32" else hoc.BFLOAT16
+    with _comm(k, path, chunk_bytes=8192) as c:
+        bufs = [Guarded(n, dtype) for _ in range(k)]
+        for g, x in zip(bufs, xs):
+            g.load(x)
+        c.allreduce([g.ptr() for g in bufs], [g.ptr() for g in bufs], n, code)
+        c.wait()
+        for r in range(k):
+            bufs[r].check()
+            assert_bits_equal(bufs[r].host(), want[r], dtype, f"in place {path} rank {r}")
+        # pointers shifted by 1..k elements: scalar paths, same bits
+        send = [Guarded(n, dtype, offset_elems=r + 1) for r in range(k)]
+        recv = [Guarded(n, dtype, offset_elems=(3 * r) % 5) for r in range(k)]
+        for g, x in zip(send, xs):
+            g.load(x)
+        c.allreduce([g.ptr() for g in send], [g.ptr() for g in recv], n, code)
+        c.wait()
+        for r in range(k):
+            recv[r].check()
+            assert_bits_equal(recv[r].host(), want[r], dtype, f"misaligned {path} rank {r}")
+
+
+@pytest.mark.parametrize("dtype", ["int32", "float32", "bfloat16"])
+@pytest.mark.parametrize("k", [1, 3, 8])
+def test_reduce_scatter_parity(dtype, k):
+    code = hoc.__dict__[dtype.upper()]
+    for rc in (1, 5, 3001):
+        xs = _inputs(dtype, k, k * rc, seed=rc + 3 * k)
+        want = o_ring.reduce_scatter(xs, rc, dtype)
+        with _comm(k) as c:
+            send = [Guarded(k * rc, dtype) for _ in range(k)]
+            recv = [Guarded(rc, dtype) for _ in range(k)]
+            for g, x in zip(send, xs):
+                g.load(x)
+            c.reduce_scatter([g.ptr() for g in send], [g.ptr() for g in recv], rc, code)
+            c.wait()
+            for r in range(k):
+                recv[r].check()
+                assert_bits_equal(recv[r].host(), want[r], dtype, f"rs k={k} rc={rc} rank {r}")
+            # in place: recv[r] = send[r] + r * rc
+            c.reduce_scatter([g.ptr() for g in send],
+                             [g.ptr() + r * rc * np.dtype(np.float32 if dtype != "bfloat16" else np.uint16).itemsize
+                              for r, g in enumerate(send)], rc, code)
+            c.wait()
+            for r in range(k):
+                got = send[r].host()[r * rc:(r + 1) * rc]
+                assert_bits_equal(got, want[r], dtype, f"rs in place k={k} rank {r}")
+
+
+@pytest.mark.parametrize("path", ["ce", "tma"])
+@pytest.mark.parametrize("k", [1, 2, 5, 8])
+def test_allgather_parity(path, k):
+    for sc in (1, 13, 50003):
+        xs = inputs.rank_inputs("bfloat16", k, sc, workload=8, slot=k)
+        want = o_ring.allgather(xs)
+        with _comm(k, path, chunk_bytes=4096) as c:
+            send = [Guarded(sc, "bfloat16", offset_elems=r % 3) for r in range(k)]
+            recv = [Guarded(k * sc, "bfloat16") for _ in range(k)]
+            for g, x in zip(send, xs):
+                g.load(x)
+            c.allgather([g.ptr() for g in send], [g.ptr() for g in recv], sc, hoc.BFLOAT16)
+            c.wait()
+            for r in range(k):
+                recv[r].check()
+                assert_bits_equal(recv[r].host(), want[r], "bfloat16", f"ag {path} k={k} sc={sc} rank {r}")
+            st = c.last_stats()
+            if path == "ce":
+                assert st["kernels"] == 0 and st["sms_used"] == 0
+            # in place
+            full = [Guarded(k * sc, "bfloat16") for _ in range(k)]
+            for r in range(k):
+                full[r].tensor[r * sc:(r + 1) * sc].copy_(to_device(xs[r], "bfloat16"))
+            c.allgather([g.ptr() + r * sc * 2 for r, g in enumerate(full)], [g.ptr() for g in full], sc, hoc.BFLOAT16)
+            c.wait()
+            for r in range(k):
+                full[r].check()
+                assert_bits_equal(full[r].host(), want[r], "bfloat16", f"ag in place {path} rank {r}")
+
+
+@pytest.mark.parametrize("path", ["ce", "tma"])
+@pytest.mark.parametrize("interleave", [True, False])
+@pytest.mark.parametrize("stage_sync", [True, False])
+def test_alltoallv_parity(path, interleave, stage_sync):
+    rng = np.random.default_rng(11)
+    for k in (1, 2, 5, 8):
+        counts = rng.integers(0, 3000, size=(k, k))
+        counts[0, :] = 0 if k > 1 else counts[0, :]
+        sends = [rng.integers(0, 1 << 16, size=int(counts[s].sum())).astype(np.uint16) for s in range(k)]
+        want = o_a2a.alltoallv(sends, counts)
+        lens = o_a2a.recv_lengths(counts)
+        with _comm(k, path, chunk_bytes=1024, a2a_interleave=interleave, a2a_stage_sync=stage_sync) as c:
+            sb = [Guarded(max(1, len(x)), "bfloat16") for x in sends]
+            rb = [Guarded(max(1, n), "bfloat16") for n in lens]
+            for g, x in zip(sb, sends):
+                if len(x):
+                    g.tensor[: len(x)].copy_(to_device(x, "bfloat16"))
+            c.alltoall([g.ptr() for g in sb], [g.ptr() for g in rb], sendcounts=counts, dtype=hoc.BFLOAT16)
+            c.wait()
+            for d in range(k):
+                rb[d].check()
+                assert_bits_equal(rb[d].host()[: lens[d]], want[d], "bfloat16", f"a2a {path} k={k} dst {d}")
+
+
+@pytest.mark.parametrize("path", ["ce", "tma"])
+def test_alltoall_uniform_involution(path):
+    k, cnt = 8, 777
+    xs = inputs.rank_inputs("int32", k, k * cnt, workload=8, slot=40)
+    with _comm(k, path) as c:
+        a = [to_device(x, "int32") for x in xs]
+        b = [torch.empty_like(t) for t in a]
+        back = [torch.empty_like(t) for t in a]
+        c.alltoall(a, b, count=cnt)
+        c.alltoall(b, back, count=cnt)
+        c.wait()
+        want = o_a2a.alltoall_uniform(xs, cnt)
+        for r in range(k):
+            assert_bits_equal(to_host(b[r], "int32"), want[r], "int32", "uniform a2a")
+            assert_bits_equal(to_host(back[r], "int32"), xs[r], "int32", "involution")
+
+
+@pytest.mark.parametrize("path", ["ce", "tma"])
+def test_sendrecv_parity(path):
+    with _comm(4, path, chunk_bytes=65536) as c:
+        for n in (1, 3, 100003):
+            x = inputs.rank_inputs("uint8" if False else "int32", 1, n, workload=8, slot=41)[0].view(np.uint8)
+            src = Guarded(len(x), "uint8", offset_elems=3)
+            dst = Guarded(len(x), "uint8", offset_elems=5)
+            src.load(x)
+            c.sendrecv(1, src.ptr(), 2, dst.ptr(), len(x), hoc.UINT8)
+            c.wait()
+            dst.check()
+            assert np.array_equal(dst.host(), x)
+
+
+def test_graph_replay_and_profiling_agree():
+    k, n = 8, 1 << 20
+    xs = inputs.rank_inputs("bfloat16", k, n, workload=2, slot=60, sigma=1e-3)
+    want = o_ring.allreduce(xs, "bfloat16")
+    for path in ("ce", "tma", "fused"):
+        with _comm(k, path, chunk_bytes=1 << 18) as c:
+            send = [to_device(x, "bfloat16") for x in xs]
+            recv = [torch.empty_like(t) for t in send]
+            for it in range(3):
+                for t in recv:
+                    t.zero_()
+                c.allreduce(send, recv)
+                st = c.last_stats()
+                assert st["graph_replayed"] == (1 if it > 0 and path != "fused" else 0), (path, it, st)
+                c.wait()
+                for r in range(k):
+                    assert_bits_equal(to_host(recv[r], "bfloat16"), want[r], "bfloat16", f"{path} iter {it}")
+            c.profile_enable(True)
+            c.allreduce(send, recv)
+            c.wait()
+            kind = hoc.KERNEL_FUSED if path == "fused" else hoc.KERNEL_REDUCE
+            launches, ms = c.profile_read(kind)
+            assert launches >= 1 and ms > 0
+            for r in range(k):
+                assert_bits_equal(to_host(recv[r], "bfloat16"), want[r], "bfloat16", f"{path} profiled")
+
+
+def test_user_graph_capture():
+    k, n = 4, 50000
+    xs = inputs.rank_inputs("float32", k, n, workload=7, slot=61)
+    want = o_ring.allreduce(xs, "float32")
+    with _comm(k, "ce", chunk_bytes=16384) as c:
+        send = [to_device(x, "float32") for x in xs]
+        recv = [torch.empty_like(t) for t in send]
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            c.allreduce(send, recv)  # warm the plan cache outside capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            c.allreduce(send, recv, stream=s)
+        for t in recv:
+            t.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for r in range(k):
+            assert_bits_equal(to_host(recv[r], "float32"), want[r], "float32", "captured")
+
+
+def test_stream_ordering_against_producer_and_consumer():
+    """Work before the call on the caller's stream is seen; work after sees the result."""
+    k, n = 8, 1 << 22
+    with _comm(k, "ce", chunk_bytes=1 << 20) as c:
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            send = [torch.zeros(n, dtype=torch.int32, device="cuda") for _ in range(k)]
+            recv = [torch.zeros(n, dtype=torch.int32, device="cuda") for _ in range(k)]
+            for r in range(k):
+                hoc.probe_launch(hoc.sm_count() * 4, 256, 20000, stream=s)  # delay the producer
+                send[r].fill_(r + 1)
+            c.allreduce(send, recv, stream=s)
+            out = torch.stack([t.sum() for t in recv])
+        torch.cuda.synchronize()
+        assert out.tolist() == [n * k * (k + 1) // 2] * k
+
+
+def test_errors_are_codes():
+    with _comm(2) as c:
+        a = torch.zeros(16, dtype=torch.float32, device="cuda")
+        b = torch.zeros(16, dtype=torch.float32, device="cuda")
+        with pytest.raises(hoc.HocError) as e:
+            c.allreduce([a, a], [b, b])          # two ranks share a recv buffer
+        assert e.value.code == hoc.ERR_INVALID_ARG
+        with pytest.raises(hoc.HocError) as e:
+            c.allreduce([a, b], [a.data_ptr() + 2, b.data_ptr()], 4, hoc.FLOAT32)  # misaligned fp32
+        assert e.value.code == hoc.ERR_INVALID_ARG
+        with pytest.raises(hoc.HocError) as e:
+            c.allreduce([a, b], [a, b], 16, hoc.UINT8)
+        assert e.value.code == hoc.ERR_UNSUPPORTED
+        c.allreduce([a, b], [a, b], 0, hoc.FLOAT32)   # count 0 is a no-op
+    with pytest.raises(hoc.HocError) as e:
+        hoc.Comm(0)
+    assert e.value.code == hoc.ERR_INVALID_ARG
+    with pytest.raises(hoc.HocError) as e:
+        hoc.Comm(3, 0, hoc.Config(ring_order=[0, 0, 1]))
+    assert e.value.code == hoc.ERR_INVALID_ARG

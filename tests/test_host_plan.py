@@ -1,0 +1,249 @@
+"""Host logic on CPU: the scheduler's plans (via hoc_plan_query), the C ABI
+exports, and host-side fault injection.  No GPU needed."""
+import os
+import re
+from collections import defaultdict
+
+import numpy as np
+import pytest
+
+from collective_communication_schedules_gb300 import hoc
+from oracle import ring as o_ring
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    from collective_communication_schedules_gb300 import build
+    build.build()
+
+
+def _cover(intervals):
+    """Sorted, merged coverage of byte intervals and whether any overlapped."""
+    iv = sorted(intervals)
+    overlap = any(iv[i][1] > iv[i + 1][0] for i in range(len(iv) - 1))
+    return iv, overlap
+
+
+def _total(iv):
+    return sum(b - a for a, b in iv)
+
+
+# ------------------------------------------------------------------ exports
+def test_every_declared_symbol_is_exported():
+    lib = hoc.lib()
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            names |= set(re.findall(r"^\s*(?:hocResult_t|const char\*)\s+(hoc_\w+)\s*\(", text, re.M))
+    assert len(names) >= 18
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(hoc._SIGS) <= names
+
+
+def test_no_device_is_a_clean_error():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(hoc.HocError) as e:
+        hoc.Comm(4)
+    assert e.value.code == hoc.ERR_NO_DEVICE
+    with pytest.raises(hoc.HocError):
+        hoc.sm_count()
+
+
+# ---------------------------------------------------------------- allreduce
+@pytest.mark.parametrize("path", ["ce", "tma"])
+@pytest.mark.parametrize("k,n,chunk", [(4, 1 << 20, 1 << 18), (8, 1000003, 1 << 16), (3, 17, 256), (5, 4096 * 5 + 3, 4096)])
+def test_allreduce_plan_covers_every_block_once(path, k, n, chunk):
+    b = 4
+    items = hoc.plan_query(k, hoc.OP_ALLREDUCE, n, hoc.FLOAT32, config=hoc.Config(path=path, chunk_bytes=chunk))
+    sizes, offs = o_ring.block_partition(n, k)
+    red = defaultdict(list)
+    moves = defaultdict(list)
+    steps = {}
+    for it in items:
+        steps.setdefault(it["step"], it)
+        if it["kind"] == hoc.ITEM_REDUCE:
+            assert it["stream"] == 0
+            red[it["dst_rank"]].append((it["src_off"], it["src_off"] + it["bytes"]))
+            assert it["src_off"] == it["dst_off"]
+        else:
+            assert it["kind"] == (hoc.ITEM_TMA if path == "tma" else hoc.ITEM_COPY)
+            assert it["src_buf"] == hoc.BUF_RECV and it["dst_buf"] == hoc.BUF_RECV
+            assert it["src_off"] == it["dst_off"] and it["src_rank"] != it["dst_rank"]
+            moves[(it["src_rank"], it["dst_rank"])].append((it["src_off"], it["src_off"] + it["bytes"]))
+            # the move waits for the reduce step of its own chunk
+            w = steps[it["wait0"]]
+            assert it["n_waits"] >= 1 and w["kind"] == hoc.ITEM_REDUCE and w["stage"] == it["stage"]
+    for r in range(k):
+        iv, ov = _cover(red[r])
+        assert not ov and _total(iv) == sizes[r] * b
+        assert iv[0][0] == offs[r] * b and iv[-1][1] == (offs[r] + sizes[r]) * b
+        for d in range(k):
+            if d == r:
+                continue
+            iv, ov = _cover(moves[(r, d)])
+            assert not ov and _total(iv) == sizes[r] * b
+            assert iv[0][0] == offs[r] * b
+
+
+def test_allreduce_chunking_and_striping():
+    k, n = 8, 134_217_728
+    cfg = hoc.Config(path="ce", chunk_bytes=4 << 20, n_copy_streams=4)
+    items = hoc.plan_query(k, hoc.OP_ALLREDUCE, n, hoc.BFLOAT16, config=cfg)
+    reduce_steps = {it["step"] for it in items if it["kind"] == hoc.ITEM_REDUCE}
+    assert len(reduce_steps) == (n // k * 2) // (4 << 20)           # 32 MiB blocks / 4 MiB chunks
+    streams = {it["stream"] for it in items if it["kind"] == hoc.ITEM_COPY}
+    assert streams == {1, 2, 3, 4}
+    per_stream = defaultdict(int)
+    for it in items:
+        if it["kind"] == hoc.ITEM_COPY:
+            per_stream[it["stream"]] += it["bytes"]
+    assert max(per_stream.values()) == min(per_stream.values())      # even striping
+
+
+def test_fused_allreduce_is_one_launch():
+    items = hoc.plan_query(8, hoc.OP_ALLREDUCE, 1001, hoc.BFLOAT16, config=hoc.Config(path="fused"))
+    assert {it["kind"] for it in items} == {hoc.ITEM_FUSED}
+    assert len({it["step"] for it in items}) == 1 and len(items) == 8
+    auto = hoc.plan_query(8, hoc.OP_ALLREDUCE, 1001, hoc.BFLOAT16, config=hoc.Config(path="auto"))
+    assert auto == items
+
+
+def test_pipeline_depth_adds_backpressure_edges():
+    cfg = hoc.Config(path="ce", chunk_bytes=1 << 16, pipeline_depth=2)
+    items = hoc.plan_query(4, hoc.OP_ALLREDUCE, 1 << 20, hoc.FLOAT32, config=cfg)
+    by_step = {}
+    for it in items:
+        by_step.setdefault(it["step"], it)
+    reds = sorted((it for it in by_step.values() if it["kind"] == hoc.ITEM_REDUCE), key=lambda x: x["stage"])
+    assert reds[0]["n_waits"] == 0 and reds[1]["n_waits"] == 0
+    for r in reds[2:]:
+        w = by_step[r["wait0"]]
+        assert w["kind"] == hoc.ITEM_COPY and w["stage"] == r["stage"] - 2
+
+
+def test_reduce_scatter_plan():
+    k, rc = 8, 1_638_400
+    items = hoc.plan_query(k, hoc.OP_REDUCE_SCATTER, rc, hoc.BFLOAT16)
+    assert len(items) == k and all(it["kind"] == hoc.ITEM_REDUCE for it in items)
+    for it in items:
+        r = it["dst_rank"]
+        assert it["src_off"] == r * rc * 2 and it["dst_off"] == 0 and it["bytes"] == rc * 2
+
+
+# ---------------------------------------------------------------- allgather
+@pytest.mark.parametrize("path", ["ce", "tma"])
+def test_allgather_plan_covers_every_pair(path):
+    k, sc = 5, 300001
+    items = hoc.plan_query(k, hoc.OP_ALLGATHER, sc, hoc.BFLOAT16, config=hoc.Config(path=path, chunk_bytes=1 << 16))
+    got = defaultdict(list)
+    for it in items:
+        assert it["src_buf"] == hoc.BUF_SEND and it["dst_buf"] == hoc.BUF_RECV
+        assert it["dst_off"] - it["src_off"] == it["src_rank"] * sc * 2
+        got[(it["src_rank"], it["dst_rank"])].append((it["src_off"], it["src_off"] + it["bytes"]))
+    assert len(got) == k * k
+    for iv in got.values():
+        iv, ov = _cover(iv)
+        assert not ov and _total(iv) == sc * 2
+
+
+# ---------------------------------------------------------------- all-to-all
+def _zipf_counts(k, seed=0):
+    rng = np.random.default_rng(seed)
+    c = rng.integers(1, 50, size=(k, k)) * (np.arange(k)[None, :] == 0) * 20 + rng.integers(0, 40, size=(k, k))
+    return c
+
+
+@pytest.mark.parametrize("interleave", [True, False])
+@pytest.mark.parametrize("stage_sync", [True, False])
+def test_alltoall_plan_stages_and_coverage(interleave, stage_sync):
+    k = 8
+    counts = _zipf_counts(k)
+    cfg = hoc.Config(path="ce", chunk_bytes=1024, a2a_interleave=interleave, a2a_stage_sync=stage_sync)
+    items = hoc.plan_query(k, hoc.OP_ALLTOALL, 0, hoc.BFLOAT16, counts=counts, config=cfg)
+    flows = defaultdict(list)
+    per_stage = defaultdict(set)
+    for it in items:
+        s, d = it["src_rank"], it["dst_rank"]
+        assert it["stage"] == (d - s) % k                      # shift stage s holds u -> u+s
+        per_stage[it["stage"]].add((s, d))
+        flows[(s, d)].append((it["src_off"], it["src_off"] + it["bytes"]))
+    for st, pairs in per_stage.items():                         # Eq. 8: one out / one in per rank
+        assert len({s for s, _ in pairs}) == len(pairs) == len({d for _, d in pairs})
+    for s in range(k):                                          # Eq. 7: the stages cover C exactly
+        for d in range(k):
+            iv, ov = _cover(flows.get((s, d), []))
+            assert not ov and _total(iv) == counts[s][d] * 2
+    if stage_sync:
+        first = {}
+        for it in items:
+            first.setdefault(it["step"], it)
+        for it in first.values():
+            if it["stage"] > 0:
+                assert it["n_waits"] >= 1 and first[it["wait0"]]["stage"] < it["stage"]
+
+
+def test_flow_size_aware_interleave_spreads_small_flows():
+    k = 2
+    counts = np.array([[0, 8 * 512], [2 * 512, 0]])        # flows of 8 and 2 chunks of 1 KiB (bf16)
+    def order(interleave):
+        items = hoc.plan_query(k, hoc.OP_ALLTOALL, 0, hoc.BFLOAT16, counts=counts,
+                               config=hoc.Config(path="ce", chunk_bytes=1024, n_copy_streams=1,
+                                                 a2a_interleave=interleave))
+        return [it["src_rank"] for it in items]
+    fifo = order(False)
+    aware = order(True)
+    assert fifo == [0] * 8 + [1] * 2
+    # weighted interleave: chunk j of a flow of n chunks is due at (j+1)/n.
+    # Big flow: 1/8, 2/8, ..., 8/8; small flow: 1/2, 2/2; ties go to flow 0,
+    # so the small flow's chunks sit at positions 4 and 9, not 8 and 9.
+    pos = [i for i, s in enumerate(aware) if s == 1]
+    assert pos == [4, 9]
+    assert sorted(aware) == sorted(fifo)
+
+
+def test_tma_alltoall_is_one_launch_on_caller_stream():
+    counts = _zipf_counts(8, 3)
+    items = hoc.plan_query(8, hoc.OP_ALLTOALL, 0, hoc.BFLOAT16, counts=counts, config=hoc.Config(path="tma"))
+    assert {it["kind"] for it in items} == {hoc.ITEM_TMA}
+    assert {it["stream"] for it in items} == {0} and len({it["step"] for it in items}) == 1
+
+
+def test_sendrecv_plan_chunks():
+    items = hoc.plan_query(8, hoc.OP_SENDRECV, 16_777_216, hoc.BFLOAT16,
+                           config=hoc.Config(path="ce", chunk_bytes=4 << 20, n_copy_streams=4))
+    assert len(items) == 8 and {it["stream"] for it in items} == {1, 2, 3, 4}
+    iv, ov = _cover([(it["src_off"], it["src_off"] + it["bytes"]) for it in items])
+    assert not ov and _total(iv) == 32 << 20
+
+
+# ------------------------------------------------------------ fault injection
+@pytest.mark.parametrize("fault", ["drop_chunk", "dup_chunk", "wrong_order"])
+def test_host_fault_injection_breaks_the_plan_invariants(fault, monkeypatch):
+    k, n = 4, 1 << 16
+    cfg = hoc.Config(path="ce", chunk_bytes=1 << 14)
+    good = hoc.plan_query(k, hoc.OP_ALLREDUCE, n, hoc.FLOAT32, config=cfg)
+    monkeypatch.setenv("HOC_FAULT", fault)
+    bad = hoc.plan_query(k, hoc.OP_ALLREDUCE, n, hoc.FLOAT32, config=cfg)
+    if fault == "drop_chunk":
+        assert sum(i["bytes"] for i in bad) < sum(i["bytes"] for i in good)
+    elif fault == "dup_chunk":
+        assert len(bad) == len(good) + 1
+    else:
+        assert all(i["n_waits"] == 0 for i in bad) and any(i["n_waits"] for i in good)
+
+
+def test_bad_config_rejected():
+    with pytest.raises(hoc.HocError) as e:
+        hoc.plan_query(3, hoc.OP_ALLREDUCE, 10, hoc.FLOAT32, config=hoc.Config(ring_order=[0, 1, 1]))
+    assert e.value.code == hoc.ERR_INVALID_ARG
+    with pytest.raises(hoc.HocError):
+        hoc.plan_query(3, hoc.OP_ALLREDUCE, 10, hoc.FLOAT32, config=hoc.Config(n_copy_streams=17))
+    with pytest.raises(hoc.HocError) as e:
+        hoc.plan_query(3, hoc.OP_ALLREDUCE, 10, hoc.UINT8)
+    assert e.value.code == hoc.ERR_UNSUPPORTED
