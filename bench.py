@@ -56,23 +56,26 @@ def parse():
     ap.add_argument("--no-extras", action="store_true", help="skip the per-path, probe and e2e legs")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--count", type=int, default=N_ELEMS,
+                    help="elements per rank (default: the full 134,217,728; smaller only for profiling captures)")
     return ap.parse_args()
 
 
 # --------------------------------------------------------------------- inputs
-def _gen_rank(r: int):
+def _gen_rank(args):
     from collective_communication_schedules_gb300 import inputs
-    return inputs.normal_bf16(N_ELEMS, inputs.seed_for(2, 0, r), SIGMA)
+    r, n = args
+    return inputs.normal_bf16(n, inputs.seed_for(2, 0, r), SIGMA)
 
 
-def generate_inputs(k: int):
+def generate_inputs(k: int, n: int):
     """Seeded inputs, one process per rank (spawned before any CUDA call)."""
     import multiprocessing as mp
     from concurrent.futures import ProcessPoolExecutor
 
     workers = max(1, min(k, os.cpu_count() or 1))
     with ProcessPoolExecutor(max_workers=workers, mp_context=mp.get_context("spawn")) as ex:
-        return list(ex.map(_gen_rank, range(k)))
+        return list(ex.map(_gen_rank, [(r, n) for r in range(k)]))
 
 
 # --------------------------------------------------------------------- clocks
@@ -214,7 +217,8 @@ def cpu_baseline(xs_host, seconds: float, device_out=None):
 
     from oracle import ring
 
-    n = N_ELEMS // 4
+    total = len(xs_host[0])
+    n = total // 4
     xs = [x[:n] for x in xs_host]
     t0 = time.perf_counter()
     reps = 0
@@ -226,7 +230,7 @@ def cpu_baseline(xs_host, seconds: float, device_out=None):
             break
     dt = (time.perf_counter() - t0) / reps
     out = {"value": round(bus_bytes(K_RANKS, n * 2) / dt / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
-           "sample": f"numpy ring-order fold of the first {n:,} of {N_ELEMS:,} bf16 elements per rank "
+           "sample": f"numpy ring-order fold of the first {n:,} of {total:,} bf16 elements per rank "
                      f"(8 ranks), {reps} repetitions, {dt:.2f} s each; host has {os.cpu_count()} cores, "
                      "numpy elementwise runs on 1",
            "seconds_per_step": round(dt, 4)}
@@ -286,13 +290,22 @@ def time_allreduce(comm, send, recv, stream, steps, profile_kind=None):
     return e0.elapsed_time(e1) / steps
 
 
-def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int):
+PROBE_SHAPES = {
+    # many small CTAs that can share an SM with a collective kernel's CTAs
+    "coresident": dict(waves=64, threads=256, smem=0),
+    # CTAs that hold a whole SM (1024 threads, 200 KiB shared memory), as a GEMM tile does
+    "exclusive": dict(waves=16, threads=1024, smem=200 * 1024),
+}
+
+
+def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int, shape: str = "exclusive"):
     """Slowdown of the FMA probe while the collective runs back to back beside it."""
     import torch
 
     from collective_communication_schedules_gb300 import hoc
 
-    ctas, threads = 64 * sms, 256
+    cfg = PROBE_SHAPES[shape]
+    ctas, threads, smem = cfg["waves"] * sms, cfg["threads"], cfg["smem"]
     sp = torch.cuda.Stream()
     gate = torch.cuda.Stream()
 
@@ -308,7 +321,7 @@ def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int):
             for _ in range(n_coll):
                 run_coll(stream_c)
         a.record(sp)
-        hoc.probe_launch(ctas, threads, iters, stream=sp)
+        hoc.probe_launch(ctas, threads, iters, stream=sp, smem_bytes=smem)
         b.record(sp)
         torch.cuda.synchronize()
         return a.elapsed_time(b)
@@ -318,22 +331,28 @@ def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int):
     alone = statistics.median(run_probe(iters) for _ in range(3))
     n_coll = int(math.ceil(1.5 * alone / max(coll_ms, 1e-3))) + 2
     with_c = statistics.median(run_probe(iters, True, n_coll) for _ in range(3))
-    return {"probe_alone_ms": round(alone, 3), "probe_with_ms": round(with_c, 3),
+    return {"shape": f"{ctas} CTAs x {threads} threads, {smem // 1024} KiB smem",
+            "probe_alone_ms": round(alone, 3), "probe_with_ms": round(with_c, 3),
             "slowdown": round(with_c / alone - 1.0, 4), "collectives_beside": n_coll}
+
+
+def probes(run_coll, coll_ms, stream_c, sms):
+    return {shape: probe_slowdown(run_coll, coll_ms, stream_c, sms, shape) for shape in PROBE_SHAPES}
 
 
 def run_ours(args, world, rank, local):
     import numpy as np
     import torch
 
-    xs_host = generate_inputs(K_RANKS)          # before the first CUDA call (spawned workers)
+    n_el = args.count
+    xs_host = generate_inputs(K_RANKS, n_el)    # spawned workers, before the first CUDA call
     from collective_communication_schedules_gb300 import hoc
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     sms = hoc.sm_count(local)
     peak, peak_kind = measured_peaks()
-    per_rank = N_ELEMS * 2
+    per_rank = n_el * 2
     k = K_RANKS
     h_send = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in xs_host]
     send = [t.to(dev) for t in h_send]
@@ -403,11 +422,11 @@ def run_ours(args, world, rank, local):
                         "lower_bound_frac": round(s2["bytes_min"] / (pm * 1e-3) / (peak * 1e9), 4),
                         "sms_used": s2["sms_used"], "kernels_per_step": s2["kernels"],
                         "copies_per_step": s2["copies"]}
-            paths[p]["probe"] = probe_slowdown(lambda s, c2=c2: c2.allreduce(send, recv, stream=s), pm, stream, sms)
+            paths[p]["probe"] = probes(lambda s, c2=c2: c2.allreduce(send, recv, stream=s), pm, stream, sms)
             c2.close()
         # the move half alone: all-gather of the 32 MiB blocks, copy engines vs TMA
         ag = {}
-        blk = N_ELEMS // k
+        blk = n_el // k
         ag_send = [t[:blk] for t in send]
         for p in ("ce", "tma"):
             c3 = hoc.Comm(k, local, hoc.Config(path=p, chunk_bytes=args.chunk_bytes, n_copy_streams=args.copy_streams))
@@ -425,10 +444,24 @@ def run_ours(args, world, rank, local):
             s3 = c3.last_stats()
             ag[p] = {"ms": round(am, 4), "bytes_gbs": round(s3["bytes_exec"] / (am * 1e-3) / 1e9, 1),
                      "sms_used": s3["sms_used"], "kernels_per_step": s3["kernels"],
-                     "probe": probe_slowdown(run, am, stream, sms)}
+                     "probe": probes(run, am, stream, sms)}
             c3.close()
         extras["paths"] = paths
         extras["allgather_moves"] = ag
+        # copy-engine allreduce: chunk size and copy-queue sweeps
+        sweep = []
+        for chunk_mib, nq in ((1, 4), (4, 4), (16, 4), (32, 4), (32, 8), (8, 8), (8, 16)):
+            c4 = hoc.Comm(k, local, hoc.Config(path="ce", chunk_bytes=chunk_mib << 20, n_copy_streams=nq))
+            for _ in range(3):
+                c4.allreduce(send, recv, stream=stream)
+            cm = time_allreduce(c4, send, recv, stream, 10)
+            s4 = c4.last_stats()
+            sweep.append({"chunk_mib": chunk_mib, "copy_streams": nq, "ms": round(cm, 4),
+                          "bus_gbs": round(bus_bytes(k, per_rank) / (cm * 1e-3) / 1e9, 1),
+                          "lower_bound_frac": round(s4["bytes_min"] / (cm * 1e-3) / (peak * 1e9), 4),
+                          "copies_per_step": s4["copies"]})
+            c4.close()
+        extras["ce_sweep"] = sweep
 
     # ---- end to end: pinned host inputs -> device, allreduce, results -> host
     h_recv = [torch.empty_like(t).pin_memory() for t in h_send]
@@ -455,7 +488,8 @@ def run_ours(args, world, rank, local):
         line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": WORKLOAD, "k": k, "count": N_ELEMS, "path": args.path,
+                "config": {"workload": WORKLOAD if n_el == N_ELEMS else f"profiling case: 8 ranks x {n_el:,} bf16",
+                           "k": k, "count": n_el, "path": args.path,
                            "resolved_path": {0: "auto", 1: "ce", 2: "tma", 3: "fused"}[st["path"]],
                            "chunk_bytes": args.chunk_bytes, "copy_streams": args.copy_streams,
                            "l2": "no flush: each step reads 2 GiB of inputs and writes 2 GiB, > 129 MB L2",

@@ -229,6 +229,8 @@ hocResult_t run_tma(hocComm* c, const Step& st, const Bind& bd, cudaStream_t s, 
     memset(&cp, 0, sizeof cp);
     cp.piece_bytes = pb;
     cp.status = c->status;
+    cp.tx_pad = c->cfg.fault == kFaultTmaStall ? 16u : 0u;
+    cp.wait_ns = c->cfg.fault == kFaultTmaStall ? 100000000ull : 2000000000ull;  // 0.1 s under injection, else 2 s
     int nj = 0;
     for (; i < st.moves.size() && nj < kMaxCopyJobs; ++i) {
       const Move& m = st.moves[i];
@@ -417,6 +419,7 @@ hocResult_t read_cfg(const hocConfig_t* in, int k, Cfg* out) {
     else if (!strcmp(v, "dup_chunk")) c.fault = kFaultDupChunk;
     else if (!strcmp(v, "wrong_order")) c.fault = kFaultWrongOrder;
     else if (!strcmp(v, "proxy_stall")) c.fault = kFaultProxyStall;
+    else if (!strcmp(v, "tma_stall")) c.fault = kFaultTmaStall;
   }
   if (c.order.empty())
     for (int i = 0; i < k; ++i) c.order.push_back(i);

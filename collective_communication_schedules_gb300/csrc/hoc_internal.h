@@ -57,6 +57,8 @@ struct CopyParams {
   uint64_t piece_start[kMaxCopyJobs + 1];  // prefix sums of the pieces of each job
   int32_t njobs;
   uint32_t piece_bytes;  // bytes per piece: one shared-memory stage
+  uint32_t tx_pad;       // extra bytes each mbarrier expects (0; >0 only for host-injected stalls)
+  uint64_t wait_ns;      // bound of every mbarrier wait
   int* status;           // device word; the kernel writes a non-zero code on a wait timeout
 };
 

@@ -34,7 +34,14 @@ struct Cfg {
   int fault = 0;           // host-side fault injection (Fault)
 };
 
-enum Fault { kFaultNone = 0, kFaultDropChunk = 1, kFaultDupChunk = 2, kFaultWrongOrder = 3, kFaultProxyStall = 4 };
+enum Fault {
+  kFaultNone = 0,
+  kFaultDropChunk = 1,
+  kFaultDupChunk = 2,
+  kFaultWrongOrder = 3,
+  kFaultProxyStall = 4,
+  kFaultTmaStall = 5  // the TMA kernel's mbarriers expect bytes that never arrive
+};
 
 enum StepKind { kStepReduce = 0, kStepFused = 1, kStepCopy = 2, kStepTma = 3 };
 

@@ -11,9 +11,12 @@
 // cannot take (heads and tails that are not 16-byte aligned, and jobs whose
 // source and destination are aligned differently).
 //
-// Every wait is bounded by the global timer.  On a timeout the kernel writes a
-// status code to p.status, waits (again bounded) for its own copies in flight
-// and returns; the host reports HOC_ERR_TIMEOUT.
+// Every wait is bounded by the global timer (p.wait_ns).  On a timeout the
+// kernel writes a status code to p.status, waits (again bounded) for its own
+// copies in flight and returns; the host reports HOC_ERR_TIMEOUT.  A host-side
+// fault injection (p.tx_pad > 0) makes every mbarrier expect more bytes than
+// its load delivers, so the phase never completes and this path runs without
+// any fault on the GPU.
 #include "hoc_internal.h"
 
 namespace hoc {
@@ -22,7 +25,6 @@ namespace {
 constexpr int kStages = 4;
 constexpr uint32_t kPieceBytes = 32768;
 constexpr int kCopyThreads = 64;
-constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -172,7 +174,7 @@ __global__ void __launch_bounds__(kCopyThreads, 1) tma_copy_kernel(const __grid_
       const int s = nload % kStages;
       stage_bytes[s] = n;
       stage_dst[s] = dst;
-      mbar_arrive_expect_tx(&bar[s], n);
+      mbar_arrive_expect_tx(&bar[s], n + p.tx_pad);
       bulk_load(stage_mem + size_t(s) * p.piece_bytes, src, n, &bar[s]);
       ++nload;
       return true;
@@ -184,7 +186,7 @@ __global__ void __launch_bounds__(kCopyThreads, 1) tma_copy_kernel(const __grid_
   bool failed = false;
   while (nstore < nload) {
     const int s = nstore % kStages;
-    if (!mbar_wait_bounded(&bar[s], (nstore / kStages) & 1u, global_ns() + kWaitNs)) {
+    if (!mbar_wait_bounded(&bar[s], (nstore / kStages) & 1u, global_ns() + p.wait_ns)) {
       failed = true;
       break;
     }
@@ -200,7 +202,7 @@ __global__ void __launch_bounds__(kCopyThreads, 1) tma_copy_kernel(const __grid_
   if (failed) {
     atomicExch(p.status, kStatusTimeoutLoad);
     // Drain: every load still in flight, bounded again.
-    const uint64_t deadline = global_ns() + kWaitNs;
+    const uint64_t deadline = global_ns() + p.wait_ns;
     for (uint32_t b = nstore; b < nload; ++b) {
       if (!mbar_wait_bounded(&bar[b % kStages], (b / kStages) & 1u, deadline)) {
         atomicExch(p.status, kStatusTimeoutDrain);

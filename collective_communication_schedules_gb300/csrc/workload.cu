@@ -49,9 +49,21 @@ __global__ void xor16_kernel(const uint16_t* __restrict__ in, uint16_t* __restri
 }  // namespace
 }  // namespace hoc
 
-extern "C" hocResult_t hoc_probe_launch(void* stream, int ctas, int threads, int iters, float* sink) {
-  if (ctas < 1 || threads < 32 || threads > 1024 || (threads % 32) != 0 || iters < 0) return HOC_ERR_INVALID_ARG;
-  hoc::probe_kernel<<<ctas, threads, 0, static_cast<cudaStream_t>(stream)>>>(iters, sink);
+extern "C" hocResult_t hoc_probe_launch(void* stream, int ctas, int threads, int smem_bytes, int iters,
+                                        float* sink) {
+  if (ctas < 1 || threads < 32 || threads > 1024 || (threads % 32) != 0 || iters < 0 || smem_bytes < 0)
+    return HOC_ERR_INVALID_ARG;
+  if (smem_bytes > 48 * 1024) {
+    int dev = 0, limit = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&limit, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return HOC_ERR_CUDA;
+    if (smem_bytes > limit) return HOC_ERR_INVALID_ARG;
+    if (cudaFuncSetAttribute(reinterpret_cast<const void*>(&hoc::probe_kernel),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
+      return HOC_ERR_CUDA;
+  }
+  hoc::probe_kernel<<<ctas, threads, size_t(smem_bytes), static_cast<cudaStream_t>(stream)>>>(iters, sink);
   return cudaGetLastError() == cudaSuccess ? HOC_SUCCESS : HOC_ERR_CUDA;
 }
 

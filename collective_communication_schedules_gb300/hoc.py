@@ -78,7 +78,7 @@ _SIGS = {
     "hoc_last_error_detail": (C.c_char_p, []),
     "hoc_plan_query": (C.c_int, [C.c_int, C.POINTER(_Config), C.c_int, C.c_size_t, C.c_int, C.POINTER(C.c_size_t),
                                  C.POINTER(_PlanItem), C.c_size_t, C.POINTER(C.c_size_t)]),
-    "hoc_probe_launch": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p]),
+    "hoc_probe_launch": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p]),
     "hoc_xor16_launch": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_uint16]),
     "hoc_device_sm_count": (C.c_int, [C.c_int, C.POINTER(C.c_int)]),
 }
@@ -269,8 +269,8 @@ class Comm:
 
 
 # ---------------------------------------------------------------- workload
-def probe_launch(ctas: int, threads: int, iters: int, sink=None, stream=None):
-    _check(lib().hoc_probe_launch(_stream(stream), int(ctas), int(threads), int(iters),
+def probe_launch(ctas: int, threads: int, iters: int, sink=None, stream=None, smem_bytes: int = 0):
+    _check(lib().hoc_probe_launch(_stream(stream), int(ctas), int(threads), int(smem_bytes), int(iters),
                                   None if sink is None else _ptr(sink)), "hoc_probe_launch")
 
 
