@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--no-extras", action="store_true", help="skip the per-path, probe and e2e legs")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--workloads", action="store_true",
+                    help="also measure the DP bucket stream, the 1F1B pipeline and the EP dispatch/combine")
     ap.add_argument("--count", type=int, default=N_ELEMS,
                     help="elements per rank (default: the full 134,217,728; smaller only for profiling captures)")
     return ap.parse_args()
@@ -292,9 +294,9 @@ def time_allreduce(comm, send, recv, stream, steps, profile_kind=None):
 
 PROBE_SHAPES = {
     # many small CTAs that can share an SM with a collective kernel's CTAs
-    "coresident": dict(waves=64, threads=256, smem=0),
-    # CTAs that hold a whole SM (1024 threads, 200 KiB shared memory), as a GEMM tile does
-    "exclusive": dict(waves=16, threads=1024, smem=200 * 1024),
+    "coresident": dict(waves=64, threads=256, whole_sm=False),
+    # CTAs that hold a whole SM (all registers, nearly all shared memory), as a GEMM tile does
+    "whole_sm": dict(waves=16, threads=1024, whole_sm=True),
 }
 
 
@@ -305,7 +307,7 @@ def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int, shape: str = "e
     from collective_communication_schedules_gb300 import hoc
 
     cfg = PROBE_SHAPES[shape]
-    ctas, threads, smem = cfg["waves"] * sms, cfg["threads"], cfg["smem"]
+    ctas, threads, whole = cfg["waves"] * sms, cfg["threads"], cfg["whole_sm"]
     sp = torch.cuda.Stream()
     gate = torch.cuda.Stream()
 
@@ -321,7 +323,7 @@ def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int, shape: str = "e
             for _ in range(n_coll):
                 run_coll(stream_c)
         a.record(sp)
-        hoc.probe_launch(ctas, threads, iters, stream=sp, smem_bytes=smem)
+        hoc.probe_launch(ctas, threads, iters, stream=sp, whole_sm=whole)
         b.record(sp)
         torch.cuda.synchronize()
         return a.elapsed_time(b)
@@ -331,7 +333,7 @@ def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int, shape: str = "e
     alone = statistics.median(run_probe(iters) for _ in range(3))
     n_coll = int(math.ceil(1.5 * alone / max(coll_ms, 1e-3))) + 2
     with_c = statistics.median(run_probe(iters, True, n_coll) for _ in range(3))
-    return {"shape": f"{ctas} CTAs x {threads} threads, {smem // 1024} KiB smem",
+    return {"shape": f"{ctas} CTAs x {threads} threads" + (", whole SM each" if whole else ""),
             "probe_alone_ms": round(alone, 3), "probe_with_ms": round(with_c, 3),
             "slowdown": round(with_c / alone - 1.0, 4), "collectives_beside": n_coll}
 
@@ -340,12 +342,155 @@ def probes(run_coll, coll_ms, stream_c, sms):
     return {shape: probe_slowdown(run_coll, coll_ms, stream_c, sms, shape) for shape in PROBE_SHAPES}
 
 
+# ------------------------------------------------------ the other workloads
+def _gen_bucket(args):
+    from collective_communication_schedules_gb300 import inputs
+    slot, r = args
+    return inputs.normal_bf16(13_107_200, inputs.seed_for(3, slot, r), SIGMA)
+
+
+def leg_bucket_stream(host_pool, sms, peak):
+    """8 ranks, 268 reduce-scatters of 25 MiB buckets back to back, probe beside; SM budget sweep."""
+    import torch
+
+    from collective_communication_schedules_gb300 import hoc
+
+    k, nb, be, pool = 8, 268, 13_107_200, 16
+    rc = be // k
+    dev = torch.device("cuda")
+    pool_in = [[torch.from_numpy(host_pool[s * k + r].view("int16")).view(torch.bfloat16).to(dev)
+                for r in range(k)] for s in range(pool)]
+    outs = torch.empty((nb, k, rc), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream()
+    out = {"buckets": nb, "bucket_bytes_per_rank": be * 2, "budgets": []}
+    for m in (4, 8, 16, 32, 0):
+        with hoc.Comm(k, 0, hoc.Config(reduce_max_sms=m)) as c:
+            def run(s, c=c):
+                for b in range(nb):
+                    c.reduce_scatter(pool_in[b % pool], [outs[b, r] for r in range(k)], rc, stream=s)
+            run(stream)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run(stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            st = c.last_stats()
+            per = ms / nb
+            entry = {"reduce_max_sms": m or sms, "ms_total": round(ms, 3), "ms_per_bucket": round(per, 4),
+                     "rs_bus_gbs": round((k - 1) / k * be * 2 / (per * 1e-3) / 1e9, 1),
+                     "hbm_frac": round(st["bytes_exec"] / (per * 1e-3) / (peak * 1e9), 4),
+                     "sms_used": st["sms_used"]}
+            entry["probe"] = probes(run, ms, stream, sms)
+            out["budgets"].append(entry)
+    del pool_in, outs
+    torch.cuda.empty_cache()
+    return out
+
+
+def leg_pipeline(sms):
+    """8 stages x 16 micro-batches of 32 MiB bf16 activations in 1F1B order."""
+    import torch
+
+    from collective_communication_schedules_gb300 import hoc, inputs
+    from collective_communication_schedules_gb300.pipeline import Pipeline1F1B
+
+    p, m, elems = 8, 16, 4096 * 4096
+    keys = inputs.pp_keys(p, m)
+    g = torch.Generator(device="cuda").manual_seed(4100)
+    xs = [torch.randn(elems, generator=g, device="cuda").to(torch.bfloat16) for _ in range(m)]
+    out = {}
+    for path in ("ce", "tma"):
+        with hoc.Comm(p, 0, hoc.Config(path=path)) as c:
+            res = {}
+            for label, send in (("with_sends", True), ("compute_only", False)):
+                pipe = Pipeline1F1B(c, p, m, elems, keys, probe_ctas=2 * sms, probe_iters=2000)
+                if not send:
+                    pipe.comm = _NoSend()
+                pipe.load(xs)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                pipe.issue()
+                e1.record()
+                torch.cuda.synchronize()
+                res[label + "_ms"] = round(e0.elapsed_time(e1), 3)
+                del pipe
+                torch.cuda.empty_cache()
+            sends = 2 * (p - 1) * m
+            res["sends"] = sends
+            res["send_bytes"] = sends * elems * 2
+            res["comm_overhead_ms"] = round(res["with_sends_ms"] - res["compute_only_ms"], 3)
+            out[path] = res
+    return out
+
+
+class _NoSend:
+    """Stands in for the communicator to time the pipeline's compute alone."""
+
+    def sendrecv(self, *a, **kw):
+        return None
+
+
+def leg_expert_dispatch(peak):
+    """8 ranks x 4096 tokens x 2048 bf16, top-6 of 64 experts (Zipf 1.1): dispatch + combine."""
+    import numpy as np
+    import torch
+
+    from collective_communication_schedules_gb300 import hoc, inputs
+
+    w = inputs.EP_DISPATCH
+    k, h = w["k"], w["hidden"]
+    routing = inputs.ep_routing(k, w["tokens"], w["experts"], w["topk"], w["zipf"])
+    counts = np.zeros((k, k), dtype=np.int64)
+    for r in range(k):
+        counts[r] = np.bincount(routing[r].reshape(-1) // (w["experts"] // k), minlength=k)
+    ecounts = counts * h
+    rows = counts.sum(axis=1)
+    g = torch.Generator(device="cuda").manual_seed(5500)
+    send = [torch.randn(int(rows[r]) * h, generator=g, device="cuda").to(torch.bfloat16) for r in range(k)]
+    recv = [torch.empty(int(ecounts[:, d].sum()), dtype=torch.bfloat16, device="cuda") for d in range(k)]
+    back = [torch.empty_like(t) for t in send]
+    moved = int(ecounts.sum()) * 2
+    out = {"rows_per_dst": [int(v) for v in counts.sum(axis=0)], "bytes_per_direction": moved}
+    for path, inter in (("ce", True), ("ce", False), ("tma", True)):
+        with hoc.Comm(k, 0, hoc.Config(path=path, a2a_interleave=inter)) as c:
+            def run(c=c):
+                c.alltoall(send, recv, sendcounts=ecounts, dtype=hoc.BFLOAT16)
+                c.alltoall(recv, back, sendcounts=ecounts.T.copy(), dtype=hoc.BFLOAT16)
+            run()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(5):
+                run()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / 5
+            st = c.last_stats()
+            out[f"{path}{'' if inter else '_fifo'}"] = {
+                "dispatch_plus_combine_ms": round(ms, 4),
+                "algbw_gbs": round(2 * moved / (ms * 1e-3) / 1e9, 1),
+                "hbm_frac": round(2 * st["bytes_exec"] / (ms * 1e-3) / (peak * 1e9), 4),
+                "sms_used": st["sms_used"], "copies_per_call": st["copies"]}
+    ok = all(torch.equal(a.view(torch.int16), b.view(torch.int16)) for a, b in zip(send, back))
+    out["combine_restores_dispatch_input"] = bool(ok)
+    return out
+
+
 def run_ours(args, world, rank, local):
     import numpy as np
     import torch
 
     n_el = args.count
     xs_host = generate_inputs(K_RANKS, n_el)    # spawned workers, before the first CUDA call
+    bucket_pool = None
+    if args.workloads:
+        import multiprocessing as mp
+        from concurrent.futures import ProcessPoolExecutor
+        with ProcessPoolExecutor(max_workers=min(16, os.cpu_count() or 1), mp_context=mp.get_context("spawn")) as ex:
+            bucket_pool = list(ex.map(_gen_bucket, [(s_, r_) for s_ in range(16) for r_ in range(K_RANKS)]))
     from collective_communication_schedules_gb300 import hoc
 
     torch.cuda.set_device(local)
@@ -462,6 +607,11 @@ def run_ours(args, world, rank, local):
                           "copies_per_step": s4["copies"]})
             c4.close()
         extras["ce_sweep"] = sweep
+    if args.workloads:
+        extras["workloads"] = {"dp_bucket_stream": leg_bucket_stream(bucket_pool, sms, peak),
+                               "pp_1f1b": leg_pipeline(sms),
+                               "ep_dispatch_combine": leg_expert_dispatch(peak)}
+        bucket_pool = None
 
     # ---- end to end: pinned host inputs -> device, allreduce, results -> host
     h_recv = [torch.empty_like(t).pin_memory() for t in h_send]

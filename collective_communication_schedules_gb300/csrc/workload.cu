@@ -24,6 +24,26 @@ __global__ void probe_kernel(int iters, float* sink) {
   if (s == -1.0f && sink != nullptr) sink[0] = s;
 }
 
+// Whole-SM variant: 1024 threads, 48 independent chains per thread.  The
+// chains need about 64 registers per thread, i.e. the SM's whole register file
+// for one CTA, and the launch also reserves most of the shared memory, so no
+// other kernel's CTA can share the SM while one of these runs -- the
+// footprint of a GEMM tile.
+constexpr int kWideChains = 48;
+__global__ void __launch_bounds__(1024, 1) probe_wide_kernel(int iters, float* sink) {
+  float a[kWideChains];
+#pragma unroll
+  for (int j = 0; j < kWideChains; ++j) a[j] = 0.25f + 0.01f * j + 1e-7f * threadIdx.x;
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int j = 0; j < kWideChains; ++j) a[j] = fmaf(a[j], 0.999f, 0.0005f);
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < kWideChains; ++j) s += a[j];
+  if (s == -1.0f && sink != nullptr) sink[0] = s;
+}
+
 // 16-byte vectors of eight 16-bit words; a scalar loop covers the unaligned
 // head and the tail.
 __global__ void xor16_kernel(const uint16_t* __restrict__ in, uint16_t* __restrict__ out, size_t n, uint32_t key2,
@@ -49,21 +69,23 @@ __global__ void xor16_kernel(const uint16_t* __restrict__ in, uint16_t* __restri
 }  // namespace
 }  // namespace hoc
 
-extern "C" hocResult_t hoc_probe_launch(void* stream, int ctas, int threads, int smem_bytes, int iters,
-                                        float* sink) {
-  if (ctas < 1 || threads < 32 || threads > 1024 || (threads % 32) != 0 || iters < 0 || smem_bytes < 0)
-    return HOC_ERR_INVALID_ARG;
-  if (smem_bytes > 48 * 1024) {
-    int dev = 0, limit = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&limit, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-      return HOC_ERR_CUDA;
-    if (smem_bytes > limit) return HOC_ERR_INVALID_ARG;
-    if (cudaFuncSetAttribute(reinterpret_cast<const void*>(&hoc::probe_kernel),
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
-      return HOC_ERR_CUDA;
+extern "C" hocResult_t hoc_probe_launch(void* stream, int ctas, int threads, int iters, int whole_sm, float* sink) {
+  if (ctas < 1 || threads < 32 || threads > 1024 || (threads % 32) != 0 || iters < 0) return HOC_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!whole_sm) {
+    hoc::probe_kernel<<<ctas, threads, 0, s>>>(iters, sink);
+    return cudaGetLastError() == cudaSuccess ? HOC_SUCCESS : HOC_ERR_CUDA;
   }
-  hoc::probe_kernel<<<ctas, threads, size_t(smem_bytes), static_cast<cudaStream_t>(stream)>>>(iters, sink);
+  if (threads != 1024) return HOC_ERR_INVALID_ARG;
+  int dev = 0, smem = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return HOC_ERR_CUDA;
+  smem -= 1024;  // leave the per-CTA reservation headroom
+  if (cudaFuncSetAttribute(reinterpret_cast<const void*>(&hoc::probe_wide_kernel),
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return HOC_ERR_CUDA;
+  hoc::probe_wide_kernel<<<ctas, 1024, size_t(smem), s>>>(iters, sink);
   return cudaGetLastError() == cudaSuccess ? HOC_SUCCESS : HOC_ERR_CUDA;
 }
 

@@ -269,8 +269,8 @@ class Comm:
 
 
 # ---------------------------------------------------------------- workload
-def probe_launch(ctas: int, threads: int, iters: int, sink=None, stream=None, smem_bytes: int = 0):
-    _check(lib().hoc_probe_launch(_stream(stream), int(ctas), int(threads), int(smem_bytes), int(iters),
+def probe_launch(ctas: int, threads: int, iters: int, sink=None, stream=None, whole_sm: bool = False):
+    _check(lib().hoc_probe_launch(_stream(stream), int(ctas), int(threads), int(iters), int(bool(whole_sm)),
                                   None if sink is None else _ptr(sink)), "hoc_probe_launch")
 
 

@@ -23,15 +23,18 @@ extern "C" {
 #endif
 
 /* Compute-bound probe: `ctas` CTAs of `threads` threads on `stream`; each
- * thread runs 8 independent FMA chains for `iters` iterations and touches no
+ * thread runs independent FMA chains for `iters` iterations and touches no
  * memory except one store to `sink` (device, >= 4 bytes, may be NULL) in the
- * unreachable case that its result equals a sentinel.  `smem_bytes` of dynamic
- * shared memory are reserved per CTA and never touched: a large value (e.g.
- * 200 KiB with 1024 threads) makes each CTA hold a whole SM, the way a GEMM
- * tile does, so any SM a collective kernel occupies is lost to the probe.
- * ctas >= 1, 32 <= threads <= 1024 (a multiple of 32), iters >= 0,
- * 0 <= smem_bytes <= the device's opt-in limit per block. */
-hocResult_t hoc_probe_launch(void* stream, int ctas, int threads, int smem_bytes, int iters, float* sink);
+ * unreachable case that its result equals a sentinel.
+ *   whole_sm == 0: 8 chains per thread, small CTAs that can share an SM with
+ *                  other kernels' CTAs.
+ *   whole_sm != 0: threads must be 1024; 48 chains per thread (about 64
+ *                  registers, the SM's whole register file for one CTA) and
+ *                  nearly all shared memory reserved, so each CTA holds a whole
+ *                  SM the way a GEMM tile does and any SM a collective kernel
+ *                  occupies is lost to the probe.
+ * ctas >= 1, 32 <= threads <= 1024 (a multiple of 32), iters >= 0. */
+hocResult_t hoc_probe_launch(void* stream, int ctas, int threads, int iters, int whole_sm, float* sink);
 
 /* out[i] = in[i] XOR key for `n` 16-bit words (device pointers; in == out is
  * allowed, other overlaps are not). */
