@@ -11,7 +11,7 @@
 namespace hoc {
 
 constexpr int kMaxRanks = HOC_MAX_RANKS;
-constexpr int kMaxCopyJobs = 192;  // jobs per TMA copy launch (kernel parameter space)
+constexpr int kMaxCopyJobs = HOC_NOALLOC_MAX_MOVES;  // jobs per TMA copy launch (kernel parameter space)
 
 // ----------------------------------------------------------------- reduce
 // One segment = one block's element range of one launch.  Every rank's input

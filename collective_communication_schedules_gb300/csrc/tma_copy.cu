@@ -17,6 +17,9 @@
 // fault injection (p.tx_pad > 0) makes every mbarrier expect more bytes than
 // its load delivers, so the phase never completes and this path runs without
 // any fault on the GPU.
+#include <cstring>
+#include <mutex>
+
 #include "hoc_internal.h"
 
 namespace hoc {
@@ -235,3 +238,84 @@ cudaError_t launch_tma_copy(const CopyParams& p, int grid, cudaStream_t stream) 
 }
 
 }  // namespace hoc
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point.  The bulk-copy kernel needs one piece of device
+// scratch: the status word its bounded waits write on a timeout.  A
+// communicator allocates that word with cudaMalloc in hoc_init; callers that
+// cannot allocate device memory use this entry point instead, whose status
+// words live in the file-scope array below (loaded with the library and held
+// by every GPU that loads it until the process exits).
+// ---------------------------------------------------------------------------
+namespace hoc {
+namespace {
+
+constexpr int kNoAllocStatusWords = HOC_NOALLOC_SCRATCH_BYTES / int(sizeof(int));
+static __device__ __align__(256) int g_noalloc_status[kNoAllocStatusWords];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+int* g_noalloc_ptr[kMaxDevices] = {};  // device address of g_noalloc_status, per device
+
+// Once per device, with that device current: opt the kernel into its shared
+// memory size and resolve the scratch array's device address (in host code
+// the symbol itself is only a host-side stand-in).
+cudaError_t noalloc_setup(int dev, int** out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    cudaError_t e = tma_prepare();
+    if (e != cudaSuccess) return e;
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_status);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = static_cast<int*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace hoc
+
+extern "C" hocResult_t hoc_tma_moves_noalloc(const void* const* src, void* const* dst, const size_t* bytes, int n,
+                                             int max_ctas, void* stream, int wait) {
+  using namespace hoc;
+  if (n < 0 || n > HOC_NOALLOC_MAX_MOVES || max_ctas < 0) return HOC_ERR_INVALID_ARG;
+  if (n == 0) return HOC_SUCCESS;
+  if (!src || !dst || !bytes) return HOC_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return HOC_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return HOC_ERR_CUDA;
+  int* status = nullptr;
+  if (noalloc_setup(dev, &status) != cudaSuccess) return HOC_ERR_CUDA;
+  CopyParams cp;
+  memset(&cp, 0, sizeof cp);
+  cp.piece_bytes = kPieceBytes;
+  cp.wait_ns = 2000000000ull;
+  cp.status = status;
+  int nj = 0;
+  for (int i = 0; i < n; ++i) {
+    if (bytes[i] == 0) continue;
+    if (!src[i] || !dst[i]) return HOC_ERR_INVALID_ARG;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(src[i]), d = reinterpret_cast<uintptr_t>(dst[i]);
+    if (a < d + bytes[i] && d < a + bytes[i]) return HOC_ERR_INVALID_ARG;  // a move may not overlap itself
+    CopyJob j{static_cast<const char*>(src[i]), static_cast<char*>(dst[i]), uint64_t(bytes[i])};
+    cp.job[nj] = j;
+    cp.piece_start[nj + 1] = cp.piece_start[nj] + job_pieces(j, kPieceBytes);
+    ++nj;
+  }
+  cp.njobs = nj;
+  if (nj == 0) return HOC_SUCCESS;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The array keeps the previous call's contents: the status must start at zero.
+  if (cudaMemsetAsync(status, 0, sizeof(int) * kNoAllocStatusWords, s) != cudaSuccess) return HOC_ERR_CUDA;
+  const int cap = max_ctas > 0 ? (max_ctas < sms ? max_ctas : sms) : sms;
+  const uint64_t pieces = cp.piece_start[nj];
+  const int grid = int(pieces < uint64_t(cap) ? pieces : uint64_t(cap));
+  if (launch_tma_copy(cp, grid, s) != cudaSuccess) return HOC_ERR_CUDA;
+  if (!wait) return HOC_SUCCESS;
+  int st = 0;
+  if (cudaMemcpyAsync(&st, status, sizeof st, cudaMemcpyDeviceToHost, s) != cudaSuccess) return HOC_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return HOC_ERR_CUDA;
+  return st == 0 ? HOC_SUCCESS : HOC_ERR_TIMEOUT;
+}

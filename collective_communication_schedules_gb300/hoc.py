@@ -81,7 +81,10 @@ _SIGS = {
     "hoc_probe_launch": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p]),
     "hoc_xor16_launch": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_uint16]),
     "hoc_device_sm_count": (C.c_int, [C.c_int, C.POINTER(C.c_int)]),
+    "hoc_tma_moves_noalloc": (C.c_int, [C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.POINTER(C.c_size_t),
+                                        C.c_int, C.c_int, C.c_void_p, C.c_int]),
 }
+NOALLOC_MAX_MOVES = 192
 
 
 def lib():
@@ -277,6 +280,17 @@ def probe_launch(ctas: int, threads: int, iters: int, sink=None, stream=None, wh
 def xor16(src, dst, n: int, key: int, stream=None):
     _check(lib().hoc_xor16_launch(_stream(stream), _ptr(src), _ptr(dst), int(n), int(key) & 0xFFFF),
            "hoc_xor16_launch")
+
+
+def tma_moves_noalloc(src, dst, nbytes, max_ctas: int = 0, stream=None, wait: bool = True):
+    """Byte moves src[i] -> dst[i] on the TMA bulk-copy kernel with no device
+    allocation (for callers that cannot call cudaMalloc); see include/hoc.h."""
+    n = len(nbytes)
+    if len(src) != n or len(dst) != n:
+        raise ValueError("src, dst and nbytes must have the same length")
+    sizes = (C.c_size_t * max(1, n))(*[int(b) for b in nbytes])
+    _check(lib().hoc_tma_moves_noalloc(_ptr_array(src), _ptr_array(dst), sizes, n, int(max_ctas), _stream(stream),
+                                       int(bool(wait))), "hoc_tma_moves_noalloc")
 
 
 def sm_count(device: int = 0) -> int:

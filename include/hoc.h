@@ -172,6 +172,39 @@ const char* hoc_error_string(hocResult_t result);
 const char* hoc_last_error_detail(void);
 
 /* ---------------------------------------------------------------------------
+ * Allocation-free moves.  The paper has no counterpart to this call.
+ *
+ * Everything above needs a communicator, and hoc_init allocates device memory
+ * (a status word for the bulk-copy kernel's bounded waits).  Some callers
+ * cannot call cudaMalloc: a plug-in running inside a runtime that has already
+ * claimed the device's memory with its own allocator, code that must not own
+ * device memory, or a step that must not risk the device-wide
+ * synchronisation cudaMalloc / cudaFree can cause.  hoc_tma_moves_noalloc
+ * moves `n` byte ranges, src[i] -> dst[i] of bytes[i] bytes (device pointers
+ * on the current device, any alignment), with the TMA bulk-copy kernel and
+ * allocates nothing: its scratch is a file-scope device array of
+ * HOC_NOALLOC_SCRATCH_BYTES (256) bytes that every GPU loading the library
+ * holds until the process exits.
+ *   - At most HOC_NOALLOC_MAX_MOVES moves per call (what one launch's
+ *     parameters carry); more returns HOC_ERR_INVALID_ARG.  A move whose
+ *     source and destination overlap is rejected the same way.
+ *   - The first call on a device sets that device up (kernel attributes and
+ *     the scratch array's device address); make that first call before any
+ *     stream capture.
+ *   - All calls share the scratch array: calls that overlap on the GPU (on
+ *     different streams without ordering between them) race on it.  Each call
+ *     clears it on `stream` before its launch.
+ *   - max_ctas caps the kernel's CTAs (0 = one per SM).  With wait != 0 the
+ *     call waits for `stream` and returns HOC_ERR_TIMEOUT if a bounded wait in
+ *     the kernel gave up; with wait == 0 it returns once the work is queued.
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine.
+ * ------------------------------------------------------------------------- */
+#define HOC_NOALLOC_MAX_MOVES 192
+#define HOC_NOALLOC_SCRATCH_BYTES 256
+hocResult_t hoc_tma_moves_noalloc(const void* const* src, void* const* dst, const size_t* bytes, int n,
+                                  int max_ctas, void* stream, int wait);
+
+/* ---------------------------------------------------------------------------
  * Plan introspection (host only, needs no GPU).  Builds the plan a
  * communicator with `cfg` would execute and returns it as a flat item list:
  * one item per reduce segment, per copy, or per join.  Used to test the
