@@ -56,8 +56,8 @@ def parse():
     ap.add_argument("--no-extras", action="store_true", help="skip the per-path, probe and e2e legs")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--workloads", action="store_true",
-                    help="also measure the DP bucket stream, the 1F1B pipeline and the EP dispatch/combine")
+    ap.add_argument("--no-workloads", dest="workloads", action="store_false",
+                    help="skip the DP bucket stream, 1F1B pipeline and EP dispatch/combine legs")
     ap.add_argument("--count", type=int, default=N_ELEMS,
                     help="elements per rank (default: the full 134,217,728; smaller only for profiling captures)")
     return ap.parse_args()
@@ -293,21 +293,28 @@ def time_allreduce(comm, send, recv, stream, steps, profile_kind=None):
 
 
 PROBE_SHAPES = {
-    # many small CTAs that can share an SM with a collective kernel's CTAs
-    "coresident": dict(waves=64, threads=256, whole_sm=False),
+    # small CTAs (8 x 256 threads per SM per wave) that can share an SM with a collective's CTAs
+    "coresident": dict(ctas_per_sm=8, threads=256, whole_sm=False),
     # CTAs that hold a whole SM (all registers, nearly all shared memory), as a GEMM tile does
-    "whole_sm": dict(waves=16, threads=1024, whole_sm=True),
+    "whole_sm": dict(ctas_per_sm=1, threads=1024, whole_sm=True),
 }
+PROBE_KERNELS = 40          # the probe is a train of one-wave kernels, ~0.25 ms each
 
 
-def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int, shape: str = "exclusive"):
-    """Slowdown of the FMA probe while the collective runs back to back beside it."""
+def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int, shape: str = "whole_sm"):
+    """Slowdown of the FMA probe train while the collective runs back to back beside it.
+
+    The probe is a train of short one-wave kernels, like a sequence of layer
+    kernels: between two probe kernels the block scheduler hands SMs to
+    whichever kernel launched first, so a collective that needs SMs takes them
+    from the probe, and one that needs none (copy engines) leaves it alone.
+    """
     import torch
 
     from collective_communication_schedules_gb300 import hoc
 
     cfg = PROBE_SHAPES[shape]
-    ctas, threads, whole = cfg["waves"] * sms, cfg["threads"], cfg["whole_sm"]
+    ctas, threads, whole = cfg["ctas_per_sm"] * sms, cfg["threads"], cfg["whole_sm"]
     sp = torch.cuda.Stream()
     gate = torch.cuda.Stream()
 
@@ -323,17 +330,18 @@ def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int, shape: str = "e
             for _ in range(n_coll):
                 run_coll(stream_c)
         a.record(sp)
-        hoc.probe_launch(ctas, threads, iters, stream=sp, whole_sm=whole)
+        for _ in range(PROBE_KERNELS):
+            hoc.probe_launch(ctas, threads, iters, stream=sp, whole_sm=whole)
         b.record(sp)
         torch.cuda.synchronize()
         return a.elapsed_time(b)
 
-    base = run_probe(200)
-    iters = max(200, int(200 * 10.0 / max(base, 1e-3)))      # ~10 ms probe alone
+    base = run_probe(100)
+    iters = max(100, int(100 * 10.0 / max(base, 1e-3)))      # ~10 ms for the whole train alone
     alone = statistics.median(run_probe(iters) for _ in range(3))
     n_coll = int(math.ceil(1.5 * alone / max(coll_ms, 1e-3))) + 2
     with_c = statistics.median(run_probe(iters, True, n_coll) for _ in range(3))
-    return {"shape": f"{ctas} CTAs x {threads} threads" + (", whole SM each" if whole else ""),
+    return {"shape": f"{PROBE_KERNELS} kernels x {ctas} CTAs x {threads} threads" + (", whole SM each" if whole else ""),
             "probe_alone_ms": round(alone, 3), "probe_with_ms": round(with_c, 3),
             "slowdown": round(with_c / alone - 1.0, 4), "collectives_beside": n_coll}
 
@@ -363,8 +371,9 @@ def leg_bucket_stream(host_pool, sms, peak):
     outs = torch.empty((nb, k, rc), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.Stream()
     out = {"buckets": nb, "bucket_bytes_per_rank": be * 2, "budgets": []}
-    for m in (4, 8, 16, 32, 0):
-        with hoc.Comm(k, 0, hoc.Config(reduce_max_sms=m)) as c:
+    for m, eng in ((4, "lsu"), (4, "tma"), (8, "lsu"), (8, "tma"), (16, "lsu"), (16, "tma"), (32, "lsu"),
+                   (32, "tma"), (0, "lsu"), (0, "tma")):
+        with hoc.Comm(k, 0, hoc.Config(reduce_max_sms=m, reduce_engine=eng)) as c:
             def run(s, c=c):
                 for b in range(nb):
                     c.reduce_scatter(pool_in[b % pool], [outs[b, r] for r in range(k)], rc, stream=s)
@@ -378,7 +387,7 @@ def leg_bucket_stream(host_pool, sms, peak):
             ms = e0.elapsed_time(e1)
             st = c.last_stats()
             per = ms / nb
-            entry = {"reduce_max_sms": m or sms, "ms_total": round(ms, 3), "ms_per_bucket": round(per, 4),
+            entry = {"reduce_max_sms": m or sms, "engine": eng, "ms_total": round(ms, 3), "ms_per_bucket": round(per, 4),
                      "rs_bus_gbs": round((k - 1) / k * be * 2 / (per * 1e-3) / 1e9, 1),
                      "hbm_frac": round(st["bytes_exec"] / (per * 1e-3) / (peak * 1e9), 4),
                      "sms_used": st["sms_used"]}
@@ -486,7 +495,7 @@ def run_ours(args, world, rank, local):
     n_el = args.count
     xs_host = generate_inputs(K_RANKS, n_el)    # spawned workers, before the first CUDA call
     bucket_pool = None
-    if args.workloads:
+    if args.workloads and not args.no_extras:
         import multiprocessing as mp
         from concurrent.futures import ProcessPoolExecutor
         with ProcessPoolExecutor(max_workers=min(16, os.cpu_count() or 1), mp_context=mp.get_context("spawn")) as ex:
@@ -556,12 +565,14 @@ def run_ours(args, world, rank, local):
     if not args.no_extras:
         # per-path figures
         paths = {}
-        for p in ("fused", "ce", "tma"):
-            c2 = hoc.Comm(k, local, hoc.Config(path=p, chunk_bytes=args.chunk_bytes, n_copy_streams=args.copy_streams))
+        for p, eng in (("fused", "lsu"), ("fused", "tma"), ("ce", "lsu"), ("tma", "lsu")):
+            c2 = hoc.Comm(k, local, hoc.Config(path=p, chunk_bytes=args.chunk_bytes, n_copy_streams=args.copy_streams,
+                                               reduce_engine=eng))
             for _ in range(3):
                 c2.allreduce(send, recv, stream=stream)
             pm = time_allreduce(c2, send, recv, stream, max(5, args.steps // 2))
             s2 = c2.last_stats()
+            p = p if eng == "lsu" else f"{p}_{eng}"
             paths[p] = {"ms": round(pm, 4), "bus_gbs": round(bus_bytes(k, per_rank) / (pm * 1e-3) / 1e9, 1),
                         "hbm_frac": round(s2["bytes_exec"] / (pm * 1e-3) / (peak * 1e9), 4),
                         "lower_bound_frac": round(s2["bytes_min"] / (pm * 1e-3) / (peak * 1e9), 4),
@@ -607,7 +618,7 @@ def run_ours(args, world, rank, local):
                           "copies_per_step": s4["copies"]})
             c4.close()
         extras["ce_sweep"] = sweep
-    if args.workloads:
+    if args.workloads and not args.no_extras:
         extras["workloads"] = {"dp_bucket_stream": leg_bucket_stream(bucket_pool, sms, peak),
                                "pp_1f1b": leg_pipeline(sms),
                                "ep_dispatch_combine": leg_expert_dispatch(peak)}

@@ -96,7 +96,14 @@ struct hocComm {
   int sms = 0;
   hoc::Cfg cfg;
   std::mutex mu;
-  std::vector<cudaStream_t> copy;  // internal copy streams
+  // Internal copy streams, one set per caller stream (the paper's stream
+  // manager keeps its handshake state per GPU stream): calls issued on
+  // different caller streams never queue behind each other.
+  struct StreamSet {
+    cudaStream_t owner;
+    std::vector<cudaStream_t> copy;
+  };
+  std::vector<StreamSet> sets;
   cudaStream_t capture = nullptr;  // origin stream for graph capture
   std::vector<cudaEvent_t> ev;     // plan edges (timing disabled)
   std::vector<cudaEvent_t> join;   // one per internal stream
@@ -123,6 +130,31 @@ namespace hoc {
 namespace {
 
 constexpr size_t kMaxGraphs = 64;
+constexpr size_t kMaxStreamSets = 16;
+
+// The copy streams serving caller stream `s0` (created on first use).
+hocResult_t copy_streams_for(hocComm* c, cudaStream_t s0, std::vector<cudaStream_t>** out) {
+  for (auto& set : c->sets)
+    if (set.owner == s0) {
+      *out = &set.copy;
+      return HOC_SUCCESS;
+    }
+  if (c->sets.size() >= kMaxStreamSets) {
+    // more caller streams than sets: share one (still correct, may serialise)
+    *out = &c->sets[reinterpret_cast<uintptr_t>(s0) % c->sets.size()].copy;
+    return HOC_SUCCESS;
+  }
+  hocComm::StreamSet set;
+  set.owner = s0;
+  for (int i = 0; i < c->cfg.n_copy; ++i) {
+    cudaStream_t s;
+    HOC_CK(cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking));
+    set.copy.push_back(s);
+  }
+  c->sets.push_back(std::move(set));
+  *out = &c->sets.back().copy;
+  return HOC_SUCCESS;
+}
 
 hocResult_t get_event(hocComm* c, std::vector<cudaEvent_t>& pool, size_t i) {
   while (pool.size() <= i) {
@@ -202,23 +234,37 @@ hocResult_t run_reduce(hocComm* c, const Plan& p, const Step& st, const Bind& bd
   for (int o = 0; o < k; ++o)
     for (int j = 0; j < k; ++j) rp.seq[o][j] = uint8_t(c->cfg.order[(pos[o] + 1 + j) % k]);
   rp.nseg = int(st.segs.size());
-  rp.tile_start[0] = 0;
+  bool all_vec = true;
   for (int i = 0; i < rp.nseg; ++i) {
     ReduceSeg g = st.segs[i];
     g.vec = (bases_aligned && (g.out_off % lanes) == (g.elem_off % lanes)) ? 1u : 0u;
+    all_vec = all_vec && g.vec;
     rp.seg[i] = g;
-    rp.tile_start[i + 1] = rp.tile_start[i] + reduce_seg_tiles(p.dtype, g);
   }
   (void)b;
+  const int budget = c->cfg.reduce_max_sms;
+  int engine = c->cfg.reduce_engine;
+  if (engine == HOC_REDUCE_AUTO) engine = budget > 0 ? HOC_REDUCE_TMA : HOC_REDUCE_LSU;
+  if (!all_vec) engine = HOC_REDUCE_LSU;  // bulk copies need co-aligned 16-byte rows
+  rp.tile_start[0] = 0;
+  for (int i = 0; i < rp.nseg; ++i)
+    rp.tile_start[i + 1] = rp.tile_start[i] + (engine == HOC_REDUCE_TMA ? reduce_tma_seg_tiles(p.dtype, rp.seg[i], k)
+                                                                       : reduce_seg_tiles(p.dtype, rp.seg[i]));
   const uint64_t tiles = rp.tile_start[rp.nseg];
   if (tiles == 0) return HOC_SUCCESS;
+  const int kind = rp.broadcast ? HOC_KERNEL_FUSED : HOC_KERNEL_REDUCE;
+  if (engine == HOC_REDUCE_TMA) {
+    const uint64_t cap = uint64_t(budget > 0 ? std::min(budget, c->sms) : c->sms);
+    const int grid = int(std::min<uint64_t>(tiles, cap));
+    *max_ctas = std::max(*max_ctas, grid);
+    return timed_launch(c, kind, s, [&] { return launch_reduce_tma(rp, grid, c->status, s); });
+  }
   uint64_t cap;
-  if (c->cfg.reduce_max_sms > 0) cap = uint64_t(std::min(c->cfg.reduce_max_sms, c->sms));
+  if (budget > 0) cap = uint64_t(std::min(budget, c->sms));
   else cap = uint64_t(c->sms) * ctas_per_sm(c, p.dtype, k, rp.broadcast);
   const int grid = int(std::min<uint64_t>(tiles, cap));
   *max_ctas = std::max(*max_ctas, grid);
-  return timed_launch(c, rp.broadcast ? HOC_KERNEL_FUSED : HOC_KERNEL_REDUCE, s,
-                      [&] { return launch_reduce(rp, grid, s); });
+  return timed_launch(c, kind, s, [&] { return launch_reduce(rp, grid, s); });
 }
 
 hocResult_t run_tma(hocComm* c, const Step& st, const Bind& bd, cudaStream_t s, int* max_ctas) {
@@ -258,7 +304,11 @@ hocResult_t run_tma(hocComm* c, const Step& st, const Bind& bd, cudaStream_t s, 
 hocResult_t issue(hocComm* c, const Plan& p, const Bind& bd, cudaStream_t s0, int* max_ctas) {
   std::vector<cudaStream_t> st(p.n_streams);
   st[0] = s0;
-  for (int i = 1; i < p.n_streams; ++i) st[i] = c->copy[i - 1];
+  if (p.n_streams > 1) {
+    std::vector<cudaStream_t>* copy = nullptr;
+    HOC_TRY(copy_streams_for(c, s0, &copy));
+    for (int i = 1; i < p.n_streams; ++i) st[i] = (*copy)[i - 1];
+  }
   if (p.n_streams > 1) {
     HOC_CK(cudaEventRecord(c->fork, s0));
     for (int i = 1; i < p.n_streams; ++i) HOC_CK(cudaStreamWaitEvent(st[i], c->fork, 0));
@@ -329,7 +379,10 @@ hocResult_t execute(hocComm* c, const CallShape& shape, const Bind& bd, cudaStre
   }
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   HOC_CK(cudaStreamIsCapturing(stream, &cs));
-  const bool worth = p.steps.size() > 1 || p.n_streams > 1 || p.copies > 1;
+  // Graphs pay off when a call issues many operations over several streams;
+  // a single copy or kernel is cheaper to issue directly (and a graph per
+  // distinct buffer address would only churn the cache).
+  const bool worth = p.n_streams > 1 && p.copies + p.kernels >= 8;
   const bool use_graph = c->cfg.use_graphs && !c->profiling && !c->cfg.debug && cs == cudaStreamCaptureStatusNone && worth;
   if (!use_graph) {
     HOC_TRY(issue(c, p, bd, stream, &max_ctas));
@@ -400,6 +453,7 @@ hocResult_t read_cfg(const hocConfig_t* in, int k, Cfg* out) {
     c.a2a_interleave = in->a2a_interleave;
     c.a2a_stage_sync = in->a2a_stage_sync;
     if (in->ring_order) c.order.assign(in->ring_order, in->ring_order + k);
+    c.reduce_engine = in->reduce_engine;
   }
   if (const char* v = getenv("HOC_PATH")) {
     if (!strcmp(v, "ce")) c.path = HOC_PATH_CE;
@@ -413,6 +467,11 @@ hocResult_t read_cfg(const hocConfig_t* in, int k, Cfg* out) {
   c.reduce_max_sms = env_int("HOC_REDUCE_MAX_SMS", c.reduce_max_sms);
   c.copy_max_sms = env_int("HOC_COPY_MAX_SMS", c.copy_max_sms);
   c.depth = env_int("HOC_PIPELINE_DEPTH", c.depth);
+  if (const char* v = getenv("HOC_REDUCE_ENGINE")) {
+    if (!strcmp(v, "lsu")) c.reduce_engine = HOC_REDUCE_LSU;
+    else if (!strcmp(v, "tma")) c.reduce_engine = HOC_REDUCE_TMA;
+    else if (!strcmp(v, "auto")) c.reduce_engine = HOC_REDUCE_AUTO;
+  }
   c.debug = env_int("HOC_DEBUG", 0);
   if (const char* v = getenv("HOC_FAULT")) {
     if (!strcmp(v, "drop_chunk")) c.fault = kFaultDropChunk;
@@ -432,7 +491,8 @@ hocResult_t read_cfg(const hocConfig_t* in, int k, Cfg* out) {
     seen[v] = 1;
   }
   if (c.path < HOC_PATH_AUTO || c.path > HOC_PATH_FUSED || c.n_copy < 1 || c.n_copy > 16 || c.chunk_bytes < 256 ||
-      c.depth < 0 || c.reduce_max_sms < 0 || c.copy_max_sms < 0) {
+      c.depth < 0 || c.reduce_max_sms < 0 || c.copy_max_sms < 0 || c.reduce_engine < HOC_REDUCE_AUTO ||
+      c.reduce_engine > HOC_REDUCE_TMA) {
     set_detail("configuration value out of range");
     return HOC_ERR_INVALID_ARG;
   }
@@ -452,7 +512,8 @@ void free_comm(hocComm* c) {
     cudaEventDestroy(pp.stop);
   }
   if (c->fork) cudaEventDestroy(c->fork);
-  for (cudaStream_t s : c->copy) cudaStreamDestroy(s);
+  for (auto& set : c->sets)
+    for (cudaStream_t s : set.copy) cudaStreamDestroy(s);
   if (c->capture) cudaStreamDestroy(c->capture);
   if (c->status) cudaFree(c->status);
   delete c;
@@ -550,6 +611,7 @@ hocResult_t hoc_config_default(hocConfig_t* cfg) {
   cfg->a2a_interleave = 1;
   cfg->a2a_stage_sync = 0;
   cfg->ring_order = nullptr;
+  cfg->reduce_engine = HOC_REDUCE_AUTO;
   return HOC_SUCCESS;
 }
 
@@ -589,14 +651,15 @@ hocResult_t hoc_init(hocComm_t* comm, int nranks, int device, const hocConfig_t*
   };
   cudaError_t e = cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, device);
   if (e != cudaSuccess) return fail("cudaDeviceGetAttribute", e);
-  for (int i = 0; i < c.n_copy; ++i) {
-    cudaStream_t s;
-    e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
-    if (e != cudaSuccess) return fail("cudaStreamCreateWithFlags", e);
-    h->copy.push_back(s);
-  }
   e = cudaStreamCreateWithFlags(&h->capture, cudaStreamNonBlocking);
   if (e != cudaSuccess) return fail("cudaStreamCreateWithFlags", e);
+  {
+    std::vector<cudaStream_t>* unused = nullptr;  // the set graph captures fork into
+    if (copy_streams_for(h, h->capture, &unused) != HOC_SUCCESS) {
+      free_comm(h);
+      return HOC_ERR_CUDA;
+    }
+  }
   e = cudaEventCreateWithFlags(&h->fork, cudaEventDisableTiming);
   if (e != cudaSuccess) return fail("cudaEventCreateWithFlags", e);
   e = cudaMalloc(&h->status, 256);
@@ -605,6 +668,8 @@ hocResult_t hoc_init(hocComm_t* comm, int nranks, int device, const hocConfig_t*
   if (e != cudaSuccess) return fail("cudaMemset(status)", e);
   e = tma_prepare();
   if (e != cudaSuccess) return fail("tma_prepare", e);
+  e = reduce_tma_prepare();
+  if (e != cudaSuccess) return fail("reduce_tma_prepare", e);
   // occupancy of every reduce kernel this communicator can launch, queried
   // now so that nothing but stream work happens while a graph is captured
   for (int dt : {int(HOC_INT32), int(HOC_FLOAT32), int(HOC_BFLOAT16)})
@@ -617,7 +682,8 @@ hocResult_t hoc_destroy(hocComm_t comm) {
   if (!comm) return HOC_ERR_NOT_INITIALIZED;
   {
     DeviceGuard g(comm->device);
-    for (cudaStream_t s : comm->copy) cudaStreamSynchronize(s);
+    for (auto& set : comm->sets)
+      for (cudaStream_t s : set.copy) cudaStreamSynchronize(s);
     free_comm(comm);
   }
   return HOC_SUCCESS;
@@ -811,7 +877,8 @@ hocResult_t hoc_wait(hocComm_t comm, void* stream, int timeout_ms) {
   if (!comm) return HOC_ERR_NOT_INITIALIZED;
   DeviceGuard g(comm->device);
   const auto deadline = std::chrono::steady_clock::now() + std::chrono::milliseconds(timeout_ms < 0 ? 0 : timeout_ms);
-  std::vector<cudaStream_t> all(comm->copy);
+  std::vector<cudaStream_t> all;
+  for (auto& set : comm->sets) all.insert(all.end(), set.copy.begin(), set.copy.end());
   all.push_back(static_cast<cudaStream_t>(stream));
   for (cudaStream_t s : all) {
     for (;;) {

@@ -45,6 +45,11 @@ uint64_t reduce_seg_tiles(int dtype, const ReduceSeg& s);
 int reduce_ctas_per_sm(int dtype, int k, int broadcast);
 cudaError_t launch_reduce(const ReduceParams& p, int grid, cudaStream_t stream);
 
+// TMA-fed variant (reduce_tma.cu): same fold, bulk copies through shared memory.
+uint64_t reduce_tma_seg_tiles(int dtype, const ReduceSeg& s, int k);
+cudaError_t reduce_tma_prepare();  // one-time per device: shared-memory opt-in
+cudaError_t launch_reduce_tma(const ReduceParams& p, int grid, int* status, cudaStream_t stream);
+
 // -------------------------------------------------------------- TMA copy
 struct CopyJob {
   const char* src;

@@ -337,7 +337,7 @@ hocResult_t plan_sendrecv(const Cfg& cfg, const CallShape& s, Plan* p) {
   const size_t bytes = s.count * dtype_bytes(s.dtype);
   Move m{s.src_rank, s.dst_rank, HOC_BUF_SEND, HOC_BUF_RECV, 0, 0, bytes};
   std::vector<Move> chunks;
-  if (p->path == HOC_PATH_TMA) chunks.push_back(m);
+  if (p->path == HOC_PATH_TMA || bytes <= kSendrecvStripeBytes) chunks.push_back(m);
   else split_move(m, cfg.chunk_bytes, &chunks);
   std::vector<int> ids;
   emit_moves(cfg, p->path, chunks, 0, {}, false, p, &ids);

@@ -30,9 +30,14 @@ struct Cfg {
   int a2a_interleave = 1;
   int a2a_stage_sync = 0;
   std::vector<int> order;  // ring order, size k
+  int reduce_engine = HOC_REDUCE_AUTO;
   int debug = 0;
   int fault = 0;           // host-side fault injection (Fault)
 };
+
+// Send/recv messages up to this size go as one copy on the caller's stream;
+// larger ones are chunked and striped over the copy queues.
+constexpr size_t kSendrecvStripeBytes = size_t(64) << 20;
 
 enum Fault {
   kFaultNone = 0,

@@ -1,0 +1,387 @@
+// k-way chunk-reduce fed by the tensor-memory accelerator.
+//
+// Same fold as reduce.cu (ring order: succ(owner), ..., owner; binary32 adds
+// with round to nearest even, bf16 rounded once at the end; int32 modulo 2^32)
+// and the same segments, but the bytes move by bulk asynchronous copies
+// instead of per-thread loads and stores:
+//   * one producer thread per CTA streams the k operand tiles of a work tile
+//     (tile_bytes each, operand j = ring position j) into a shared-memory
+//     stage with cp.async.bulk, completing on that stage's "full" mbarrier;
+//   * four consumer warps fold the k tiles element by element from shared
+//     memory into an output tile, release the stage on its "empty" mbarrier,
+//     and one consumer thread bulk-stores the output tile to the owner's
+//     buffer (or to all k buffers: the fused allreduce);
+//   * stages cycle, so several tiles of loads are in flight per SM while the
+//     consumers work and earlier stores drain.
+// One CTA per SM (persistent over tiles).  Only the 16-byte-aligned body of
+// each segment moves by bulk copies; the few elements before the first
+// aligned element and after the last whole vector go through plain loads.
+//
+// Every mbarrier wait is bounded by the global timer; on a timeout the CTA
+// records a status code, stops issuing work, waits (bounded) for its own
+// loads in flight and returns.
+#include <cuda_bf16.h>
+
+#include "hoc_internal.h"
+
+namespace hoc {
+namespace {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kConsumers = 32 * kConsumerWarps;
+constexpr int kThreadsT = kConsumers + 32;  // + one producer warp
+constexpr int kOutBufs = 2;
+
+__device__ __forceinline__ uint32_t sa(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+__device__ __forceinline__ uint64_t now_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mb_init(uint64_t* b, uint32_t n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(b)), "r"(n) : "memory");
+}
+__device__ __forceinline__ void mb_expect(uint64_t* b, uint32_t tx) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sa(b)), "r"(tx) : "memory");
+}
+__device__ __forceinline__ void mb_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sa(b)) : "memory");
+}
+__device__ __forceinline__ bool mb_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(sa(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mb_wait(uint64_t* b, uint32_t parity, uint64_t deadline) {
+  while (!mb_try(b, parity))
+    if (now_ns() > deadline) return false;
+  return true;
+}
+__device__ __forceinline__ void bulk_g2s(void* s, const void* g, uint32_t n, uint64_t* b) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(sa(s)),
+               "l"(g), "r"(n), "r"(sa(b))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_s2g(void* g, const void* s, uint32_t n) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(g), "r"(sa(s)), "r"(n) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Barrier over the consumer warps that also ORs a predicate: every consumer
+// gets the same answer, so they leave the loop together.
+__device__ __forceinline__ bool consumers_sync_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(uint32_t(v)), "n"(kConsumers)
+      : "memory");
+  return r != 0;
+}
+
+__host__ __device__ inline int lanes_for(int dtype) { return dtype == HOC_BFLOAT16 ? 8 : 4; }
+__host__ __device__ inline int bytes_for(int dtype) { return dtype == HOC_BFLOAT16 ? 2 : 4; }
+
+// Work tiles of a segment: the aligned body cut into tile_bytes pieces (the
+// last may be shorter, always a multiple of 16 bytes); at least one tile when
+// the segment is not empty, so that its head and tail elements get an owner.
+__host__ __device__ inline uint64_t tma_seg_body_vecs(const ReduceSeg& s, int lanes) {
+  const uint64_t mis = s.elem_off % lanes;
+  uint64_t h = mis ? lanes - mis : 0;
+  if (h > s.elems) h = s.elems;
+  return (s.elems - h) / lanes;
+}
+__host__ __device__ inline uint64_t tma_seg_tiles(const ReduceSeg& s, int dtype, uint32_t tile_bytes) {
+  if (s.elems == 0) return 0;
+  const uint64_t vecs_per_tile = tile_bytes / 16;
+  const uint64_t v = tma_seg_body_vecs(s, lanes_for(dtype));
+  const uint64_t t = (v + vecs_per_tile - 1) / vecs_per_tile;
+  return t ? t : 1;
+}
+
+template <class E, class F, class N>
+__device__ __forceinline__ void scalar_fold(const ReduceParams& p, const uint8_t* seq, uint32_t owner, uint64_t e,
+                                            uint64_t o, F widen_add, N narrow) {
+  float acc = 0.f;
+  uint32_t iacc = 0;
+  for (int j = 0; j < p.k; ++j) {
+    const E x = static_cast<const E*>(p.in[seq[j]])[e];
+    widen_add(acc, iacc, x, j == 0);
+  }
+  const E y = narrow(acc, iacc);
+  if (p.broadcast) {
+    for (int r = 0; r < p.k; ++r) static_cast<E*>(p.out[r])[o] = y;
+  } else {
+    static_cast<E*>(p.out[owner])[o] = y;
+  }
+}
+
+__device__ __forceinline__ void scalar_elem(const ReduceParams& p, const uint8_t* seq, uint32_t owner, uint64_t e,
+                                            uint64_t o) {
+  if (p.dtype == HOC_BFLOAT16) {
+    scalar_fold<uint16_t>(
+        p, seq, owner, e, o,
+        [](float& a, uint32_t&, uint16_t x, bool first) {
+          const float v = __uint_as_float(uint32_t(x) << 16);
+          a = first ? v : __fadd_rn(a, v);
+        },
+        [](float a, uint32_t) { return static_cast<uint16_t>(__bfloat16_as_ushort(__float2bfloat16_rn(a))); });
+  } else if (p.dtype == HOC_FLOAT32) {
+    scalar_fold<uint32_t>(
+        p, seq, owner, e, o,
+        [](float& a, uint32_t&, uint32_t x, bool first) {
+          const float v = __uint_as_float(x);
+          a = first ? v : __fadd_rn(a, v);
+        },
+        [](float a, uint32_t) { return __float_as_uint(a); });
+  } else {
+    scalar_fold<uint32_t>(
+        p, seq, owner, e, o, [](float&, uint32_t& a, uint32_t x, bool first) { a = first ? x : a + x; },
+        [](float, uint32_t a) { return a; });
+  }
+}
+
+// Fold one 16-byte vector position of the k tiles in a stage.
+__device__ __forceinline__ uint4 fold_vec(const unsigned char* stage, uint32_t tile_bytes, int k, uint32_t off,
+                                          int dtype) {
+  const uint4* t0 = reinterpret_cast<const uint4*>(stage + off);
+  uint4 x = *t0;
+  if (dtype == HOC_BFLOAT16) {
+    float a[8];
+    const uint32_t w0[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      a[2 * i] = __uint_as_float(w0[i] << 16);
+      a[2 * i + 1] = __uint_as_float(w0[i] & 0xFFFF0000u);
+    }
+    for (int j = 1; j < k; ++j) {
+      const uint4 y = *reinterpret_cast<const uint4*>(stage + size_t(j) * tile_bytes + off);
+      const uint32_t w[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        a[2 * i] = __fadd_rn(a[2 * i], __uint_as_float(w[i] << 16));
+        a[2 * i + 1] = __fadd_rn(a[2 * i + 1], __uint_as_float(w[i] & 0xFFFF0000u));
+      }
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      o[i] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(a[2 * i]))) |
+             (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(a[2 * i + 1]))) << 16);
+    return make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (dtype == HOC_FLOAT32) {
+    float a0 = __uint_as_float(x.x), a1 = __uint_as_float(x.y), a2 = __uint_as_float(x.z), a3 = __uint_as_float(x.w);
+    for (int j = 1; j < k; ++j) {
+      const uint4 y = *reinterpret_cast<const uint4*>(stage + size_t(j) * tile_bytes + off);
+      a0 = __fadd_rn(a0, __uint_as_float(y.x));
+      a1 = __fadd_rn(a1, __uint_as_float(y.y));
+      a2 = __fadd_rn(a2, __uint_as_float(y.z));
+      a3 = __fadd_rn(a3, __uint_as_float(y.w));
+    }
+    return make_uint4(__float_as_uint(a0), __float_as_uint(a1), __float_as_uint(a2), __float_as_uint(a3));
+  }
+  for (int j = 1; j < k; ++j) {
+    const uint4 y = *reinterpret_cast<const uint4*>(stage + size_t(j) * tile_bytes + off);
+    x.x += y.x;
+    x.y += y.y;
+    x.z += y.z;
+    x.w += y.w;
+  }
+  return x;
+}
+
+struct TileRef {
+  int seg;
+  uint64_t local;
+};
+
+__device__ __forceinline__ TileRef tile_of(const ReduceParams& p, uint64_t t) {
+  int s = 0;
+  while (t >= p.tile_start[s + 1]) ++s;
+  return {s, t - p.tile_start[s]};
+}
+
+// Byte range [off, off + n) of the segment's aligned body covered by a tile.
+__device__ __forceinline__ void tile_body(const ReduceParams& p, const ReduceSeg& sg, uint64_t local,
+                                          uint32_t tile_bytes, uint64_t& body_elem0, uint64_t& off_b, uint32_t& n) {
+  const int lanes = lanes_for(p.dtype);
+  const uint64_t mis = sg.elem_off % lanes;
+  uint64_t h = mis ? lanes - mis : 0;
+  if (h > sg.elems) h = sg.elems;
+  body_elem0 = h;
+  const uint64_t body_bytes = tma_seg_body_vecs(sg, lanes) * 16;
+  off_b = local * tile_bytes;
+  n = off_b >= body_bytes ? 0u : uint32_t(body_bytes - off_b < tile_bytes ? body_bytes - off_b : tile_bytes);
+}
+
+__global__ void __launch_bounds__(kThreadsT, 1)
+    reduce_tma_kernel(const __grid_constant__ ReduceParams p, uint32_t tile_bytes, int stages, int* status,
+                      uint64_t wait_ns) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ __align__(8) uint64_t full[8];
+  __shared__ __align__(8) uint64_t empty[8];
+  __shared__ int abort_flag;
+  const int k = p.k;
+  const int eb = bytes_for(p.dtype);
+  const uint32_t stage_bytes = uint32_t(k) * tile_bytes;
+  unsigned char* out_tiles = smem + size_t(stages) * stage_bytes;
+  const uint64_t total = p.tile_start[p.nseg];
+  const uint64_t mine = total > blockIdx.x ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mb_init(&full[s], 1);
+      mb_init(&empty[s], kConsumerWarps);
+    }
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    if (lane != 0) return;
+    uint64_t issued = 0;
+    for (uint64_t it = 0; it < mine; ++it) {
+      const int s = int(it % stages);
+      if (it >= uint64_t(stages) &&
+          !mb_wait(&empty[s], uint32_t((it / stages - 1) & 1), now_ns() + wait_ns)) {
+        atomicExch(status, kStatusTimeoutLoad);
+        atomicExch(&abort_flag, 1);
+        break;
+      }
+      if (*(volatile int*)&abort_flag) break;
+      const TileRef tr = tile_of(p, blockIdx.x + it * gridDim.x);
+      const ReduceSeg& sg = p.seg[tr.seg];
+      uint64_t e0, off;
+      uint32_t n;
+      tile_body(p, sg, tr.local, tile_bytes, e0, off, n);
+      if (n == 0) {
+        mb_arrive(&full[s]);  // nothing to load (a segment shorter than one vector)
+      } else {
+        mb_expect(&full[s], n * uint32_t(k));
+        const uint8_t* seq = p.seq[sg.owner];
+        const uint64_t gb = (sg.elem_off + e0) * eb + off;
+        for (int j = 0; j < k; ++j)
+          bulk_g2s(smem + size_t(s) * stage_bytes + size_t(j) * tile_bytes,
+                   static_cast<const char*>(p.in[seq[j]]) + gb, n, &full[s]);
+      }
+      issued = it + 1;
+    }
+    // Do not leave while loads still target this CTA's shared memory.
+    const uint64_t first = issued > uint64_t(stages) ? issued - stages : 0;
+    const uint64_t deadline = now_ns() + wait_ns;
+    for (uint64_t it = first; it < issued; ++it)
+      if (!mb_wait(&full[it % stages], uint32_t((it / stages) & 1), deadline)) {
+        atomicExch(status, kStatusTimeoutDrain);
+        break;
+      }
+    return;
+  }
+
+  // ------------------------------------------------------------ consumers
+  const int ct = threadIdx.x - 32;
+  bool prev_stored = false;  // (thread ct == 0) whether the previous tile committed a store group
+  for (uint64_t it = 0; it < mine; ++it) {
+    const int s = int(it % stages);
+    const int ob = int(it % kOutBufs);
+    if (ct == 0 && it >= kOutBufs) {
+      // the stores of tile it-2 must have read out buffer ob before it is rewritten
+      if (prev_stored) bulk_wait_read1();
+      else bulk_wait_read0();
+    }
+    bool bad = !mb_wait(&full[s], uint32_t((it / stages) & 1), now_ns() + wait_ns);
+    if (bad) atomicExch(status, kStatusTimeoutLoad);
+    bad = bad || *(volatile int*)&abort_flag;
+    if (consumers_sync_or(bad)) {
+      if (lane == 0) atomicExch(&abort_flag, 1);
+      break;
+    }
+    const TileRef tr = tile_of(p, blockIdx.x + it * gridDim.x);
+    const ReduceSeg& sg = p.seg[tr.seg];
+    const uint8_t* seq = p.seq[sg.owner];
+    uint64_t e0, off;
+    uint32_t n;
+    tile_body(p, sg, tr.local, tile_bytes, e0, off, n);
+    unsigned char* stage = smem + size_t(s) * stage_bytes;
+    unsigned char* ot = out_tiles + size_t(ob) * tile_bytes;
+    for (uint32_t v = uint32_t(ct) * 16; v < n; v += kConsumers * 16)
+      *reinterpret_cast<uint4*>(ot + v) = fold_vec(stage, tile_bytes, k, v, p.dtype);
+    __syncwarp();
+    if (lane == 0) mb_arrive(&empty[s]);
+    // head and tail elements of the segment (plain loads)
+    const uint64_t tiles_here = p.tile_start[tr.seg + 1] - p.tile_start[tr.seg];
+    if (tr.local == 0 && uint64_t(ct) < e0) scalar_elem(p, seq, sg.owner, sg.elem_off + ct, sg.out_off + ct);
+    if (tr.local == tiles_here - 1) {
+      const uint64_t done = e0 + tma_seg_body_vecs(sg, lanes_for(p.dtype)) * lanes_for(p.dtype);
+      if (uint64_t(ct) < sg.elems - done) scalar_elem(p, seq, sg.owner, sg.elem_off + done + ct, sg.out_off + done + ct);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // st.shared visible to the bulk stores
+    consumers_sync();
+    if (ct == 0) {
+      prev_stored = n != 0;
+      if (n) {
+        const uint64_t gb = (sg.out_off + e0) * eb + off;
+        if (p.broadcast) {
+          for (int r = 0; r < k; ++r) bulk_s2g(static_cast<char*>(p.out[r]) + gb, ot, n);
+        } else {
+          bulk_s2g(static_cast<char*>(p.out[sg.owner]) + gb, ot, n);
+        }
+        bulk_commit();
+      }
+    }
+  }
+  if (ct == 0) bulk_wait_all();
+}
+
+}  // namespace
+
+uint32_t reduce_tma_tile_bytes(int k) { return k <= 8 ? 4096u : 2048u; }
+
+int reduce_tma_stages(int k) {
+  const uint32_t stage = uint32_t(k) * reduce_tma_tile_bytes(k);
+  const uint32_t budget = 200u * 1024u - kOutBufs * reduce_tma_tile_bytes(k);
+  int s = int(budget / stage);
+  return s < 2 ? 2 : (s > 8 ? 8 : s);
+}
+
+size_t reduce_tma_smem(int k) {
+  return size_t(reduce_tma_stages(k)) * k * reduce_tma_tile_bytes(k) + kOutBufs * reduce_tma_tile_bytes(k);
+}
+
+uint64_t reduce_tma_seg_tiles(int dtype, const ReduceSeg& s, int k) {
+  return tma_seg_tiles(s, dtype, reduce_tma_tile_bytes(k));
+}
+
+cudaError_t reduce_tma_prepare() {
+  size_t most = 0;
+  for (int k = 1; k <= kMaxRanks; ++k) most = reduce_tma_smem(k) > most ? reduce_tma_smem(k) : most;
+  return cudaFuncSetAttribute(reinterpret_cast<const void*>(&reduce_tma_kernel),
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, int(most));
+}
+
+cudaError_t launch_reduce_tma(const ReduceParams& p, int grid, int* status, cudaStream_t stream) {
+  if (grid < 1) return cudaSuccess;
+  uint32_t tb = reduce_tma_tile_bytes(p.k);
+  int stages = reduce_tma_stages(p.k);
+  uint64_t wait_ns = 2000000000ull;
+  void* args[] = {const_cast<ReduceParams*>(&p), &tb, &stages, &status, &wait_ns};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(&reduce_tma_kernel), dim3(grid), dim3(kThreadsT), args,
+                          reduce_tma_smem(p.k), stream);
+}
+
+}  // namespace hoc

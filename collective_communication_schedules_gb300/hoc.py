@@ -25,6 +25,8 @@ ITEM_REDUCE, ITEM_FUSED, ITEM_COPY, ITEM_TMA, ITEM_JOIN = range(5)
 BUF_SEND, BUF_RECV = 0, 1
 MAX_RANKS = 16
 PATHS = {"auto": PATH_AUTO, "ce": PATH_CE, "tma": PATH_TMA, "fused": PATH_FUSED}
+REDUCE_AUTO, REDUCE_LSU, REDUCE_TMA = 0, 1, 2
+ENGINES = {"auto": REDUCE_AUTO, "lsu": REDUCE_LSU, "tma": REDUCE_TMA}
 
 
 class HocError(RuntimeError):
@@ -37,7 +39,7 @@ class _Config(C.Structure):
     _fields_ = [("path", C.c_int), ("chunk_bytes", C.c_size_t), ("n_copy_streams", C.c_int),
                 ("pipeline_depth", C.c_int), ("reduce_max_sms", C.c_int), ("copy_max_sms", C.c_int),
                 ("use_graphs", C.c_int), ("a2a_interleave", C.c_int), ("a2a_stage_sync", C.c_int),
-                ("ring_order", C.POINTER(C.c_int))]
+                ("ring_order", C.POINTER(C.c_int)), ("reduce_engine", C.c_int)]
 
 
 class _Stats(C.Structure):
@@ -167,6 +169,7 @@ class Config:
     a2a_interleave: bool = True
     a2a_stage_sync: bool = False
     ring_order: Optional[Sequence[int]] = None
+    reduce_engine: str = "auto"
     _keep: list = field(default_factory=list, repr=False)
 
     def to_c(self) -> _Config:
@@ -180,6 +183,7 @@ class Config:
         c.use_graphs = int(bool(self.use_graphs))
         c.a2a_interleave = int(bool(self.a2a_interleave))
         c.a2a_stage_sync = int(bool(self.a2a_stage_sync))
+        c.reduce_engine = ENGINES[self.reduce_engine] if isinstance(self.reduce_engine, str) else int(self.reduce_engine)
         if self.ring_order is not None:
             arr = (C.c_int * len(self.ring_order))(*[int(v) for v in self.ring_order])
             self._keep = [arr]

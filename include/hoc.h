@@ -64,10 +64,17 @@ typedef enum {
   HOC_PATH_FUSED = 3  /* allreduce only: one kernel reduces and writes all k outputs */
 } hocPath_t;
 
+/* How the k-way reduce kernel moves its bytes. */
+typedef enum {
+  HOC_REDUCE_AUTO = 0, /* TMA under an SM budget (reduce_max_sms > 0), else LSU */
+  HOC_REDUCE_LSU = 1,  /* every thread issues 16-byte vector loads and stores */
+  HOC_REDUCE_TMA = 2   /* bulk async copies through shared memory; one CTA per SM */
+} hocReduceEngine_t;
+
 /* Communicator configuration; hoc_config_default() fills the defaults.
  * Environment variables HOC_PATH (ce|tma|fused|auto), HOC_CHUNK_BYTES,
- * HOC_COPY_STREAMS, HOC_USE_GRAPHS, HOC_REDUCE_MAX_SMS, HOC_DEBUG override
- * the values passed in. */
+ * HOC_COPY_STREAMS, HOC_USE_GRAPHS, HOC_REDUCE_MAX_SMS, HOC_REDUCE_ENGINE
+ * (lsu|tma|auto), HOC_DEBUG override the values passed in. */
 typedef struct {
   int path;              /* hocPath_t */
   size_t chunk_bytes;    /* pipeline unit inside a block / flow; default 4 MiB */
@@ -80,6 +87,7 @@ typedef struct {
   int a2a_interleave;    /* 1: flow-size-aware chunk interleave per copy queue; 0: per-flow FIFO */
   int a2a_stage_sync;    /* 1: all copy queues join between all-to-all shift stages */
   const int* ring_order; /* k ranks in ring order (a permutation); NULL = identity; copied */
+  int reduce_engine;     /* hocReduceEngine_t */
 } hocConfig_t;
 
 typedef struct hocComm* hocComm_t;
@@ -144,8 +152,9 @@ hocResult_t hoc_alltoall(hocComm_t comm, const void* const* send, const size_t* 
                          size_t count_if_uniform, hocDataType_t dtype, void* stream);
 
 /* Send/recv (section 3.3.2): move `count` elements from rank src_rank's buffer
- * `send` into rank dst_rank's buffer `recv` with one direct copy (split into
- * chunks over the copy queues).  src_rank may equal dst_rank. */
+ * `send` into rank dst_rank's buffer `recv` with one direct copy on `stream`
+ * (messages above 64 MiB are split into chunks striped over the copy queues).
+ * src_rank may equal dst_rank. */
 hocResult_t hoc_sendrecv(hocComm_t comm, int src_rank, const void* send, int dst_rank, void* recv,
                          size_t count, hocDataType_t dtype, void* stream);
 

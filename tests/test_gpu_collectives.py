@@ -32,14 +32,15 @@ def _comm(k, path="auto", **kw):
 
 @pytest.mark.parametrize("dtype", ["int32", "float32", "bfloat16"])
 @pytest.mark.parametrize("k", [1, 2, 3, 4, 8])
-@pytest.mark.parametrize("path", PATHS)
-def test_allreduce_parity(dtype, k, path):
+@pytest.mark.parametrize("path,engine", [("ce", "lsu"), ("tma", "lsu"), ("fused", "lsu"), ("fused", "tma"),
+                                         ("ce", "tma")])
+def test_allreduce_parity(dtype, k, path, engine):
     rng = np.random.default_rng(k * 31 + len(path))
     for n in SIZES:
         xs = _inputs(dtype, k, n, seed=n + k)
         order = list(rng.permutation(k))
         want = o_ring.allreduce(xs, dtype, order)
-        with _comm(k, path, chunk_bytes=4096, ring_order=order) as c:
+        with _comm(k, path, chunk_bytes=4096, ring_order=order, reduce_engine=engine) as c:
             send = [Guarded(n, dtype) for _ in range(k)]
             recv = [Guarded(n, dtype) for _ in range(k)]
             for g, x in zip(send, xs):
@@ -56,12 +57,13 @@ def test_allreduce_parity(dtype, k, path):
 
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
-def test_allreduce_in_place_and_misaligned(path, dtype):
+@pytest.mark.parametrize("engine", ["lsu", "tma"])
+def test_allreduce_in_place_and_misaligned(path, dtype, engine):
     k, n = 4, 12345
     xs = _inputs(dtype, k, n, seed=5)
     want = o_ring.allreduce(xs, dtype)
     code = hoc.FLOAT32 if dtype == "float32" else hoc.BFLOAT16
-    with _comm(k, path, chunk_bytes=8192) as c:
+    with _comm(k, path, chunk_bytes=8192, reduce_engine=engine) as c:
         bufs = [Guarded(n, dtype) for _ in range(k)]
         for g, x in zip(bufs, xs):
             g.load(x)
@@ -83,13 +85,14 @@ def test_allreduce_in_place_and_misaligned(path, dtype):
 
 
 @pytest.mark.parametrize("dtype", ["int32", "float32", "bfloat16"])
-@pytest.mark.parametrize("k", [1, 3, 8])
-def test_reduce_scatter_parity(dtype, k):
+@pytest.mark.parametrize("k", [1, 3, 8, 16])
+@pytest.mark.parametrize("engine,budget", [("lsu", 0), ("tma", 0), ("tma", 3), ("lsu", 5)])
+def test_reduce_scatter_parity(dtype, k, engine, budget):
     code = hoc.__dict__[dtype.upper()]
-    for rc in (1, 5, 3001):
+    for rc in (1, 5, 3001, 40000):
         xs = _inputs(dtype, k, k * rc, seed=rc + 3 * k)
         want = o_ring.reduce_scatter(xs, rc, dtype)
-        with _comm(k) as c:
+        with _comm(k, reduce_engine=engine, reduce_max_sms=budget) as c:
             send = [Guarded(k * rc, dtype) for _ in range(k)]
             recv = [Guarded(rc, dtype) for _ in range(k)]
             for g, x in zip(send, xs):

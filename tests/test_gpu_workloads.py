@@ -86,12 +86,13 @@ def large_inputs():
     return dev, idx, want
 
 
-@pytest.mark.parametrize("path,chunk_mib", [("fused", 4), ("ce", 1), ("ce", 4), ("ce", 16), ("ce", 64),
-                                             ("tma", 4), ("tma", 32)])
-def test_large_allreduce_workload(large_inputs, path, chunk_mib):
+@pytest.mark.parametrize("path,chunk_mib,engine", [("fused", 4, "lsu"), ("fused", 4, "tma"), ("ce", 1, "lsu"),
+                                                    ("ce", 4, "lsu"), ("ce", 16, "tma"), ("ce", 64, "lsu"),
+                                                    ("tma", 4, "lsu"), ("tma", 32, "lsu")])
+def test_large_allreduce_workload(large_inputs, path, chunk_mib, engine):
     send, idx, want = large_inputs
     recv = [torch.empty_like(t) for t in send]
-    with hoc.Comm(8, 0, hoc.Config(path=path, chunk_bytes=chunk_mib << 20)) as c:
+    with hoc.Comm(8, 0, hoc.Config(path=path, chunk_bytes=chunk_mib << 20, reduce_engine=engine)) as c:
         c.allreduce(send, recv)
         c.wait()
         st = c.last_stats()
@@ -106,7 +107,8 @@ def test_large_allreduce_workload(large_inputs, path, chunk_mib):
 
 
 # ------------------------------------------------------------------ workload 3
-def test_bucket_stream_reduce_scatter_workload():
+@pytest.mark.parametrize("budget,engine", [(0, "lsu"), (16, "tma")])
+def test_bucket_stream_reduce_scatter_workload(budget, engine):
     w = inputs.RS_BUCKETS
     k, nb, be, pool = w["k"], w["buckets"], w["bucket_elems"], w["pool"]
     rc = be // k
@@ -120,7 +122,7 @@ def test_bucket_stream_reduce_scatter_workload():
     sms = hoc.sm_count()
     probe_stream = torch.cuda.Stream()
     coll_stream = torch.cuda.Stream()
-    with hoc.Comm(k, 0) as c:
+    with hoc.Comm(k, 0, hoc.Config(reduce_max_sms=budget, reduce_engine=engine)) as c:
         hoc.probe_launch(64 * sms, 256, 4000, stream=probe_stream)
         for b in range(nb):
             c.reduce_scatter(pool_in[b % pool], [outs[b, r] for r in range(k)], rc, stream=coll_stream)

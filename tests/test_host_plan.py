@@ -215,11 +215,16 @@ def test_tma_alltoall_is_one_launch_on_caller_stream():
 
 
 def test_sendrecv_plan_chunks():
+    # a 32 MiB activation (the PP workload) is one direct copy on the caller's stream
     items = hoc.plan_query(8, hoc.OP_SENDRECV, 16_777_216, hoc.BFLOAT16,
                            config=hoc.Config(path="ce", chunk_bytes=4 << 20, n_copy_streams=4))
-    assert len(items) == 8 and {it["stream"] for it in items} == {1, 2, 3, 4}
+    assert len(items) == 1 and items[0]["stream"] == 0 and items[0]["bytes"] == 32 << 20
+    # above 64 MiB the message is chunked and striped over the copy queues
+    items = hoc.plan_query(8, hoc.OP_SENDRECV, 64 << 20, hoc.BFLOAT16,
+                           config=hoc.Config(path="ce", chunk_bytes=4 << 20, n_copy_streams=4))
+    assert len(items) == 32 and {it["stream"] for it in items} == {1, 2, 3, 4}
     iv, ov = _cover([(it["src_off"], it["src_off"] + it["bytes"]) for it in items])
-    assert not ov and _total(iv) == 32 << 20
+    assert not ov and _total(iv) == 128 << 20
 
 
 # ------------------------------------------------------------ fault injection
