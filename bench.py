@@ -317,6 +317,8 @@ def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int, shape: str = "w
     ctas, threads, whole = cfg["ctas_per_sm"] * sms, cfg["threads"], cfg["whole_sm"]
     sp = torch.cuda.Stream()
     gate = torch.cuda.Stream()
+    sink = torch.zeros(4, dtype=torch.float32, device="cuda")
+    mhz = []
 
     def run_probe(iters, with_coll=False, n_coll=0):
         ev_gate = torch.cuda.Event()
@@ -331,19 +333,27 @@ def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int, shape: str = "w
                 run_coll(stream_c)
         a.record(sp)
         for _ in range(PROBE_KERNELS):
-            hoc.probe_launch(ctas, threads, iters, stream=sp, whole_sm=whole)
+            hoc.probe_launch(ctas, threads, iters, stream=sp, whole_sm=whole, sink=sink)
         b.record(sp)
         torch.cuda.synchronize()
+        cyc, ns = sink[0].item(), sink[1].item()
+        mhz.append(1e3 * cyc / ns if ns > 0 else None)
         return a.elapsed_time(b)
 
     base = run_probe(100)
     iters = max(100, int(100 * 10.0 / max(base, 1e-3)))      # ~10 ms for the whole train alone
+    mhz.clear()
     alone = statistics.median(run_probe(iters) for _ in range(3))
+    mhz_alone = [m for m in mhz if m]
+    mhz.clear()
     n_coll = int(math.ceil(1.5 * alone / max(coll_ms, 1e-3))) + 2
     with_c = statistics.median(run_probe(iters, True, n_coll) for _ in range(3))
+    mhz_with = [m for m in mhz if m]
     return {"shape": f"{PROBE_KERNELS} kernels x {ctas} CTAs x {threads} threads" + (", whole SM each" if whole else ""),
             "probe_alone_ms": round(alone, 3), "probe_with_ms": round(with_c, 3),
-            "slowdown": round(with_c / alone - 1.0, 4), "collectives_beside": n_coll}
+            "slowdown": round(with_c / alone - 1.0, 4), "collectives_beside": n_coll,
+            "sm_mhz_alone": round(statistics.median(mhz_alone), 1) if mhz_alone else None,
+            "sm_mhz_with": round(statistics.median(mhz_with), 1) if mhz_with else None}
 
 
 def probes(run_coll, coll_ms, stream_c, sms):
@@ -488,6 +498,95 @@ def leg_expert_dispatch(peak):
     return out
 
 
+def leg_sweeps(sms):
+    """Bandwidth vs size, 2 MB - 1 GB: copy engines vs TMA (all SMs, or 1/2/4/8 SMs).
+
+    Sizes follow the nccl-tests convention of the paper's benchmarks: P2P = the
+    message, AllGather = each rank's receive buffer, All-to-All = each rank's
+    send buffer; algorithm bandwidth = size / time.  8 simulated ranks.
+    """
+    import torch
+
+    from collective_communication_schedules_gb300 import hoc
+
+    k = 8
+    sizes_mb = [2, 8, 32, 128, 512, 1024]
+    variants = [("ce", 0), ("tma", 0), ("tma", 1), ("tma", 2), ("tma", 4), ("tma", 8)]
+    big = max(sizes_mb) << 20
+    src = [torch.empty(big, dtype=torch.uint8, device="cuda") for _ in range(k)]
+    dst = [torch.empty(big, dtype=torch.uint8, device="cuda") for _ in range(k)]
+    for t in src:
+        t.fill_(7)
+    stream = torch.cuda.Stream()
+    out = {"sizes_mb": sizes_mb, "p2p": {}, "allgather": {}, "alltoall": {}}
+    for path, ctas in variants:
+        name = path if ctas == 0 else f"{path}_{ctas}sm"
+        c = hoc.Comm(k, 0, hoc.Config(path=path, copy_max_sms=ctas))
+        for op in ("p2p", "allgather", "alltoall"):
+            row = []
+            for mb in sizes_mb:
+                n = mb << 20
+                if op == "p2p":
+                    run = lambda n=n: c.sendrecv(0, src[0], 1, dst[1], n, hoc.UINT8, stream=stream)
+                elif op == "allgather":
+                    run = lambda n=n: c.allgather(src, dst, n // k, hoc.UINT8, stream=stream)
+                else:
+                    run = lambda n=n: c.alltoall(src, dst, count=n // k, dtype=hoc.UINT8, stream=stream)
+                run()
+                torch.cuda.synchronize()
+                reps = 3 if mb >= 512 else 10
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(reps):
+                    run()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1) / reps
+                row.append(round(n / (ms * 1e-3) / 1e9, 1))
+            out[op][name] = row
+        c.close()
+    del src, dst
+    torch.cuda.empty_cache()
+    return out
+
+
+def leg_host_overhead():
+    """Host time of one call (CPU launch overhead, cf. Fig. 9), median over 200 calls."""
+    import time as _t
+
+    import torch
+
+    from collective_communication_schedules_gb300 import hoc
+
+    k, n = 8, 1 << 20
+    a = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(k)]
+    b = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(k)]
+    g = [torch.empty(k * n, dtype=torch.bfloat16, device="cuda") for _ in range(k)]
+    stream = torch.cuda.Stream()
+    out = {}
+    cases = {
+        "allreduce_fused": ("fused", lambda c: c.allreduce(a, b, stream=stream)),
+        "allreduce_ce_graph": ("ce", lambda c: c.allreduce(a, b, stream=stream)),
+        "allgather_ce_graph": ("ce", lambda c: c.allgather(a, g, stream=stream)),
+        "sendrecv_ce": ("ce", lambda c: c.sendrecv(0, a[0], 1, b[1], stream=stream)),
+        "sendrecv_tma": ("tma", lambda c: c.sendrecv(0, a[0], 1, b[1], stream=stream)),
+    }
+    for name, (path, fn) in cases.items():
+        with hoc.Comm(k, 0, hoc.Config(path=path, chunk_bytes=1 << 18)) as c:
+            fn(c)
+            torch.cuda.synchronize()
+            ts = []
+            for i in range(200):
+                t0 = _t.perf_counter()
+                fn(c)
+                ts.append((_t.perf_counter() - t0) * 1e6)
+                if i % 20 == 19:
+                    torch.cuda.synchronize()
+            torch.cuda.synchronize()
+            out[name] = {"median_us": round(statistics.median(ts), 2), "p90_us": round(sorted(ts)[180], 2)}
+    return out
+
+
 def run_ours(args, world, rank, local):
     import numpy as np
     import torch
@@ -623,6 +722,8 @@ def run_ours(args, world, rank, local):
                                "pp_1f1b": leg_pipeline(sms),
                                "ep_dispatch_combine": leg_expert_dispatch(peak)}
         bucket_pool = None
+        extras["sweeps"] = leg_sweeps(sms)
+        extras["host_overhead_us"] = leg_host_overhead()
 
     # ---- end to end: pinned host inputs -> device, allreduce, results -> host
     h_recv = [torch.empty_like(t).pin_memory() for t in h_send]

@@ -244,12 +244,13 @@ hocResult_t run_reduce(hocComm* c, const Plan& p, const Step& st, const Bind& bd
   (void)b;
   const int budget = c->cfg.reduce_max_sms;
   int engine = c->cfg.reduce_engine;
-  if (engine == HOC_REDUCE_AUTO) engine = budget > 0 ? HOC_REDUCE_TMA : HOC_REDUCE_LSU;
+  if (engine == HOC_REDUCE_AUTO) engine = HOC_REDUCE_LSU;  // measured faster in both shapes
+  const bool wide = budget > 0;  // one CTA per SM: the 1024-thread shape
   if (!all_vec) engine = HOC_REDUCE_LSU;  // bulk copies need co-aligned 16-byte rows
   rp.tile_start[0] = 0;
   for (int i = 0; i < rp.nseg; ++i)
     rp.tile_start[i + 1] = rp.tile_start[i] + (engine == HOC_REDUCE_TMA ? reduce_tma_seg_tiles(p.dtype, rp.seg[i], k)
-                                                                       : reduce_seg_tiles(p.dtype, rp.seg[i]));
+                                                                       : reduce_seg_tiles(p.dtype, rp.seg[i], wide));
   const uint64_t tiles = rp.tile_start[rp.nseg];
   if (tiles == 0) return HOC_SUCCESS;
   const int kind = rp.broadcast ? HOC_KERNEL_FUSED : HOC_KERNEL_REDUCE;
@@ -264,7 +265,7 @@ hocResult_t run_reduce(hocComm* c, const Plan& p, const Step& st, const Bind& bd
   else cap = uint64_t(c->sms) * ctas_per_sm(c, p.dtype, k, rp.broadcast);
   const int grid = int(std::min<uint64_t>(tiles, cap));
   *max_ctas = std::max(*max_ctas, grid);
-  return timed_launch(c, kind, s, [&] { return launch_reduce(rp, grid, s); });
+  return timed_launch(c, kind, s, [&] { return launch_reduce(rp, grid, wide, s); });
 }
 
 hocResult_t run_tma(hocComm* c, const Step& st, const Bind& bd, cudaStream_t s, int* max_ctas) {

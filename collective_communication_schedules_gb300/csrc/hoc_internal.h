@@ -37,13 +37,12 @@ struct ReduceParams {
   int32_t dtype;      // hocDataType_t (INT32, FLOAT32, BFLOAT16)
 };
 
-// Elements covered by one reduce tile for `dtype` (threads x vectors x lanes).
-uint64_t reduce_tile_elems(int dtype);
-// Tiles of a segment (0 for an empty segment).
-uint64_t reduce_seg_tiles(int dtype, const ReduceSeg& s);
-// Resident CTAs per SM of the reduce kernel for (dtype, k, broadcast).
+// Tiles of a segment (0 for an empty segment) for the whole-GPU shape
+// (wide = false) or the one-CTA-per-SM shape used under an SM budget.
+uint64_t reduce_seg_tiles(int dtype, const ReduceSeg& s, bool wide);
+// Resident CTAs per SM of the whole-GPU reduce kernel for (dtype, k, broadcast).
 int reduce_ctas_per_sm(int dtype, int k, int broadcast);
-cudaError_t launch_reduce(const ReduceParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_reduce(const ReduceParams& p, int grid, bool wide, cudaStream_t stream);
 
 // TMA-fed variant (reduce_tma.cu): same fold, bulk copies through shared memory.
 uint64_t reduce_tma_seg_tiles(int dtype, const ReduceSeg& s, int k);

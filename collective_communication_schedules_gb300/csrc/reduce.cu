@@ -10,9 +10,12 @@
 //
 // Layout: rank buffers are 1-D arrays in HBM.  A launch covers one element
 // range (a chunk) of every block: one segment per block.  Segments are cut into
-// tiles of kThreads x kVecPerThread 16-byte vectors; CTAs stride over tiles.
-// Each thread issues all k x kVecPerThread 16-byte loads before folding, so a
-// 256-thread CTA keeps k * 8 KiB of loads in flight.
+// tiles of THREADS x VPT 16-byte vectors; CTAs stride over tiles.  Each thread
+// issues all k x VPT 16-byte loads before folding.  Two shapes:
+//   * whole GPU: 256-thread CTAs, 2 vectors per thread, several CTAs per SM
+//     (k * 8 KiB of loads in flight per CTA);
+//   * SM budget (one CTA per SM): 1024-thread CTAs, 1 vector per thread, so
+//     each of the few SMs keeps k * 16 KiB of loads in flight.
 //
 // Arithmetic: fp32 adds with __fadd_rn (round to nearest even, no contraction,
 // no flush to zero); bf16 widens exactly to fp32, adds in fp32 and rounds once
@@ -24,11 +27,13 @@
 namespace hoc {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kVecPerThread = 2;
-constexpr uint64_t kTileVecs = uint64_t(kThreads) * kVecPerThread;
+constexpr int kThreadsNarrow = 256, kVecNarrow = 2;  // whole GPU
+constexpr int kThreadsWide = 1024, kVecWide = 1;     // one CTA per SM under a budget
 
 __host__ __device__ inline int lanes_of(int dtype) { return dtype == HOC_BFLOAT16 ? 8 : 4; }
+__host__ __device__ inline uint64_t tile_vecs(bool wide) {
+  return wide ? uint64_t(kThreadsWide) * kVecWide : uint64_t(kThreadsNarrow) * kVecNarrow;
+}
 
 // Elements before the first 16-byte-aligned element of a vector segment.
 __host__ __device__ inline uint64_t seg_head(const ReduceSeg& s, int lanes) {
@@ -37,14 +42,14 @@ __host__ __device__ inline uint64_t seg_head(const ReduceSeg& s, int lanes) {
   return h > s.elems ? s.elems : h;
 }
 
-__host__ __device__ inline uint64_t seg_tiles(const ReduceSeg& s, int lanes) {
+__host__ __device__ inline uint64_t seg_tiles(const ReduceSeg& s, int lanes, uint64_t tvecs) {
   if (s.elems == 0) return 0;
   if (s.vec) {
     const uint64_t nvec = (s.elems - seg_head(s, lanes)) / lanes;
-    const uint64_t t = (nvec + kTileVecs - 1) / kTileVecs;
+    const uint64_t t = (nvec + tvecs - 1) / tvecs;
     return t ? t : 1;
   }
-  const uint64_t per = kTileVecs * lanes;
+  const uint64_t per = tvecs * lanes;
   return (s.elems + per - 1) / per;
 }
 
@@ -157,9 +162,10 @@ __device__ __forceinline__ void scalar_elem(const ReduceParams& p, const uint8_t
 }
 
 // K > 0: compile-time rank count (all loads hoisted); K == 0: runtime p.k.
-template <class Tr, int K>
+template <class Tr, int K, int kThreads, int kVecPerThread>
 __global__ void __launch_bounds__(kThreads) reduce_kernel(const __grid_constant__ ReduceParams p) {
   constexpr int L = Tr::kLanes;
+  constexpr uint64_t kTileVecs = uint64_t(kThreads) * kVecPerThread;
   const int k = K > 0 ? K : p.k;
   const uint64_t total = p.tile_start[p.nseg];
   for (uint64_t t = blockIdx.x; t < total; t += gridDim.x) {
@@ -223,52 +229,57 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const __grid_constant_
   }
 }
 
-template <class Tr>
+template <class Tr, int T, int V>
 const void* pick_kernel(int k) {
   switch (k) {
-    case 2: return reinterpret_cast<const void*>(&reduce_kernel<Tr, 2>);
-    case 3: return reinterpret_cast<const void*>(&reduce_kernel<Tr, 3>);
-    case 4: return reinterpret_cast<const void*>(&reduce_kernel<Tr, 4>);
-    case 5: return reinterpret_cast<const void*>(&reduce_kernel<Tr, 5>);
-    case 6: return reinterpret_cast<const void*>(&reduce_kernel<Tr, 6>);
-    case 7: return reinterpret_cast<const void*>(&reduce_kernel<Tr, 7>);
-    case 8: return reinterpret_cast<const void*>(&reduce_kernel<Tr, 8>);
-    default: return reinterpret_cast<const void*>(&reduce_kernel<Tr, 0>);
+    case 2: return reinterpret_cast<const void*>(&reduce_kernel<Tr, 2, T, V>);
+    case 3: return reinterpret_cast<const void*>(&reduce_kernel<Tr, 3, T, V>);
+    case 4: return reinterpret_cast<const void*>(&reduce_kernel<Tr, 4, T, V>);
+    case 5: return reinterpret_cast<const void*>(&reduce_kernel<Tr, 5, T, V>);
+    case 6: return reinterpret_cast<const void*>(&reduce_kernel<Tr, 6, T, V>);
+    case 7: return reinterpret_cast<const void*>(&reduce_kernel<Tr, 7, T, V>);
+    case 8: return reinterpret_cast<const void*>(&reduce_kernel<Tr, 8, T, V>);
+    default: return reinterpret_cast<const void*>(&reduce_kernel<Tr, 0, T, V>);
   }
 }
 
-const void* kernel_for(int dtype, int k) {
+template <class Tr>
+const void* pick_shape(int k, bool wide) {
+  return wide ? pick_kernel<Tr, kThreadsWide, kVecWide>(k) : pick_kernel<Tr, kThreadsNarrow, kVecNarrow>(k);
+}
+
+const void* kernel_for(int dtype, int k, bool wide) {
   switch (dtype) {
-    case HOC_FLOAT32: return pick_kernel<TrF32>(k);
-    case HOC_INT32: return pick_kernel<TrI32>(k);
-    case HOC_BFLOAT16: return pick_kernel<TrBF16>(k);
+    case HOC_FLOAT32: return pick_shape<TrF32>(k, wide);
+    case HOC_INT32: return pick_shape<TrI32>(k, wide);
+    case HOC_BFLOAT16: return pick_shape<TrBF16>(k, wide);
     default: return nullptr;
   }
 }
 
 }  // namespace
 
-uint64_t reduce_tile_elems(int dtype) { return kTileVecs * uint64_t(lanes_of(dtype)); }
-
-uint64_t reduce_seg_tiles(int dtype, const ReduceSeg& s) { return seg_tiles(s, lanes_of(dtype)); }
+uint64_t reduce_seg_tiles(int dtype, const ReduceSeg& s, bool wide) {
+  return seg_tiles(s, lanes_of(dtype), tile_vecs(wide));
+}
 
 int reduce_ctas_per_sm(int dtype, int k, int /*broadcast*/) {
-  const void* fn = kernel_for(dtype, k);
+  const void* fn = kernel_for(dtype, k, false);
   if (!fn) return 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, 0) != cudaSuccess || n < 1) {
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreadsNarrow, 0) != cudaSuccess || n < 1) {
     cudaGetLastError();
     return 1;
   }
   return n;
 }
 
-cudaError_t launch_reduce(const ReduceParams& p, int grid, cudaStream_t stream) {
-  const void* fn = kernel_for(p.dtype, p.k);
+cudaError_t launch_reduce(const ReduceParams& p, int grid, bool wide, cudaStream_t stream) {
+  const void* fn = kernel_for(p.dtype, p.k, wide);
   if (!fn) return cudaErrorInvalidValue;
   if (grid < 1) return cudaSuccess;
   void* args[] = {const_cast<ReduceParams*>(&p)};
-  return cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, 0, stream);
+  return cudaLaunchKernel(fn, dim3(grid), dim3(wide ? kThreadsWide : kThreadsNarrow), args, 0, stream);
 }
 
 }  // namespace hoc

@@ -7,10 +7,28 @@
 namespace hoc {
 namespace {
 
-// Eight independent FMA chains per thread; no memory traffic.  The only store
-// happens if the result equals a sentinel the chains cannot reach (their
-// values stay in (0, 1]), which keeps the compiler from removing the work.
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// CTA 0's thread 0 reports how many SM cycles and nanoseconds it ran, so the
+// host can see the SM clock the probe actually got.
+__device__ __forceinline__ void report_clock(float* sink, long long c0, uint64_t t0) {
+  if (sink != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {
+    sink[0] = float(clock64() - c0);
+    sink[1] = float(gtimer() - t0);
+  }
+}
+
+// Eight independent FMA chains per thread; no memory traffic besides the
+// clock report.  The chains' result is stored only if it equals a sentinel
+// the chains cannot reach (their values stay in (0, 1]), which keeps the
+// compiler from removing the work.
 __global__ void probe_kernel(int iters, float* sink) {
+  const long long c0 = clock64();
+  const uint64_t t0 = gtimer();
   float a[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) a[j] = 0.5f + 0.0625f * j + 1e-7f * threadIdx.x;
@@ -21,7 +39,8 @@ __global__ void probe_kernel(int iters, float* sink) {
   float s = 0.f;
 #pragma unroll
   for (int j = 0; j < 8; ++j) s += a[j];
-  if (s == -1.0f && sink != nullptr) sink[0] = s;
+  if (s == -1.0f && sink != nullptr) sink[2] = s;
+  report_clock(sink, c0, t0);
 }
 
 // Whole-SM variant: 1024 threads, 48 independent chains per thread.  The
@@ -31,6 +50,8 @@ __global__ void probe_kernel(int iters, float* sink) {
 // footprint of a GEMM tile.
 constexpr int kWideChains = 48;
 __global__ void __launch_bounds__(1024, 1) probe_wide_kernel(int iters, float* sink) {
+  const long long c0 = clock64();
+  const uint64_t t0 = gtimer();
   float a[kWideChains];
 #pragma unroll
   for (int j = 0; j < kWideChains; ++j) a[j] = 0.25f + 0.01f * j + 1e-7f * threadIdx.x;
@@ -41,7 +62,8 @@ __global__ void __launch_bounds__(1024, 1) probe_wide_kernel(int iters, float* s
   float s = 0.f;
 #pragma unroll
   for (int j = 0; j < kWideChains; ++j) s += a[j];
-  if (s == -1.0f && sink != nullptr) sink[0] = s;
+  if (s == -1.0f && sink != nullptr) sink[2] = s;
+  report_clock(sink, c0, t0);
 }
 
 // 16-byte vectors of eight 16-bit words; a scalar loop covers the unaligned

@@ -66,7 +66,7 @@ typedef enum {
 
 /* How the k-way reduce kernel moves its bytes. */
 typedef enum {
-  HOC_REDUCE_AUTO = 0, /* TMA under an SM budget (reduce_max_sms > 0), else LSU */
+  HOC_REDUCE_AUTO = 0, /* LSU (measured faster on GB300 with and without an SM budget) */
   HOC_REDUCE_LSU = 1,  /* every thread issues 16-byte vector loads and stores */
   HOC_REDUCE_TMA = 2   /* bulk async copies through shared memory; one CTA per SM */
 } hocReduceEngine_t;
@@ -81,7 +81,7 @@ typedef struct {
   int n_copy_streams;    /* internal copy streams (the multi-QP analogue); default 4, max 16 */
   int pipeline_depth;    /* allreduce CE/TMA: reduce of chunk q waits for the moves of
                             chunk q - depth; 0 = no limit */
-  int reduce_max_sms;    /* cap on CTAs of reduce kernels (one CTA per SM); 0 = whole GPU */
+  int reduce_max_sms;    /* cap on CTAs of reduce kernels (one 1024-thread CTA per SM); 0 = whole GPU */
   int copy_max_sms;      /* CTAs of the TMA copy kernel; 0 = whole GPU */
   int use_graphs;        /* 1: cache each call's issue sequence as a CUDA graph and replay it */
   int a2a_interleave;    /* 1: flow-size-aware chunk interleave per copy queue; 0: per-flow FIFO */

@@ -24,8 +24,10 @@ extern "C" {
 
 /* Compute-bound probe: `ctas` CTAs of `threads` threads on `stream`; each
  * thread runs independent FMA chains for `iters` iterations and touches no
- * memory except one store to `sink` (device, >= 4 bytes, may be NULL) in the
- * unreachable case that its result equals a sentinel.
+ * memory except `sink` (device, >= 12 bytes, may be NULL): the first CTA
+ * writes the SM cycles and nanoseconds it ran to sink[0] and sink[1] (floats),
+ * and sink[2] is written only in the unreachable case that a result equals a
+ * sentinel.
  *   whole_sm == 0: 8 chains per thread, small CTAs that can share an SM with
  *                  other kernels' CTAs.
  *   whole_sm != 0: threads must be 1024; 48 chains per thread (about 64

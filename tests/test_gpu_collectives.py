@@ -210,7 +210,9 @@ def test_graph_replay_and_profiling_agree():
                     t.zero_()
                 c.allreduce(send, recv)
                 st = c.last_stats()
-                assert st["graph_replayed"] == (1 if it > 0 and path != "fused" else 0), (path, it, st)
+                # a graph is kept for plans with several streams and >= 8 operations
+                graphed = path != "fused" and st["kernels"] + st["copies"] >= 8
+                assert st["graph_replayed"] == (1 if it > 0 and graphed else 0), (path, it, st)
                 c.wait()
                 for r in range(k):
                     assert_bits_equal(to_host(recv[r], "bfloat16"), want[r], "bfloat16", f"{path} iter {it}")
