@@ -87,6 +87,10 @@ _SIGS = {
                                         C.c_int, C.c_int, C.c_void_p, C.c_int]),
 }
 NOALLOC_MAX_MOVES = 192
+_SIGS["hoc_topo_schedule"] = (C.c_int, [C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_int), C.POINTER(C.c_uint64),
+                                        C.c_uint64, C.c_uint64, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64),
+                                        C.POINTER(C.c_double), C.c_int, C.POINTER(C.c_int),
+                                        C.POINTER(C.c_double)])
 
 
 def lib():
@@ -295,6 +299,29 @@ def tma_moves_noalloc(src, dst, nbytes, max_ctas: int = 0, stream=None, wait: bo
     sizes = (C.c_size_t * max(1, n))(*[int(b) for b in nbytes])
     _check(lib().hoc_tma_moves_noalloc(_ptr_array(src), _ptr_array(dst), sizes, n, int(max_ctas), _stream(stream),
                                        int(bool(wait))), "hoc_tma_moves_noalloc")
+
+
+def topo_schedule(C_matrix, node_of, sym, bw_nvlink: int, bw_rdma: int):
+    """Two-domain stage schedule (host only): returns (T, stages, taus, total)."""
+    G = len(node_of)
+    flat = [int(v) for row in C_matrix for v in row]
+    if len(flat) != G * G:
+        raise ValueError("C must be G x G")
+    cm = (C.c_uint64 * (G * G))(*flat)
+    no = (C.c_int * G)(*[int(v) for v in node_of])
+    sy = (C.c_int * G)(*[int(v) for v in sym])
+    n = C.c_int()
+    tot = C.c_double()
+    _check(lib().hoc_topo_schedule(G, no, sy, cm, int(bw_nvlink), int(bw_rdma), None, None, None, 0, C.byref(n),
+                                   C.byref(tot)), "hoc_topo_schedule")
+    T = (C.c_uint64 * (G * G))()
+    st = (C.c_uint64 * max(1, n.value * G * G))()
+    ta = (C.c_double * max(1, n.value))()
+    _check(lib().hoc_topo_schedule(G, no, sy, cm, int(bw_nvlink), int(bw_rdma), T, st, ta, n.value, C.byref(n),
+                                   C.byref(tot)), "hoc_topo_schedule")
+    Tm = [[T[u * G + v] for v in range(G)] for u in range(G)]
+    stages = [[[st[s * G * G + u * G + v] for v in range(G)] for u in range(G)] for s in range(n.value)]
+    return Tm, stages, [ta[s] for s in range(n.value)], tot.value
 
 
 def sm_count(device: int = 0) -> int:

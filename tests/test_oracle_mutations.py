@@ -119,3 +119,41 @@ def test_pipeline_missing_transform_caught():
         keys[p - 1, :, 1] = 0          # last stage forgets its backward transform
         return pipeline.simulate(x, keys, p, m)
     assert _fails(pins.check_pipeline_closed_form, bad, np.random.default_rng(6))
+
+
+# ------------------------------------------------------------ two-domain scheduler
+def test_topo_wrong_forwarding_cell_caught():
+    from oracle import topo
+    from tests import test_topo_sched as tt
+
+    def bad_traffic_matrix(C, node_of, sym):
+        G = len(C)
+        inter, _ = topo.domains(node_of)
+        A = [sum(C[u][v] for v in range(G) if (u, v) in inter) for u in range(G)]
+        B = [sum(C[u][v] for u in range(G) if (u, v) in inter) for v in range(G)]
+        T = [row[:] for row in C]
+        for u in range(G):
+            T[u][sym[u]] += A[u] + B[u]          # receiver side on the wrong GPU
+        return T
+
+    T = bad_traffic_matrix(tt.fig6_matrix(), tt.FIG6_NODES, tt.FIG6_SYM)
+    assert T[0][1] != tt.f(1, 2, 3, 8, 11)
+
+
+def test_topo_dropped_degree_constraint_caught():
+    import numpy as np
+    from oracle import topo
+    from tests import test_topo_sched as tt
+
+    real = topo.greedy_matching
+    try:
+        topo.greedy_matching = lambda entries: sorted(entries)          # takes every flow at once
+        rng = np.random.default_rng(0)
+        caught = False
+        for _ in range(20):
+            C, nodes, sym = tt._random_case(rng, 8, 2)
+            T, stages, _ = topo.schedule(C, nodes, sym, 5, 3)
+            caught = caught or _fails(tt._check_invariants, C, nodes, sym, T, stages)
+        assert caught
+    finally:
+        topo.greedy_matching = real
