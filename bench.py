@@ -608,6 +608,7 @@ def run_ours(args, world, rank, local):
     per_rank = n_el * 2
     k = K_RANKS
     h_send = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in xs_host]
+    h_recv = [torch.empty_like(t).pin_memory() for t in h_send]
     send = [t.to(dev) for t in h_send]
     recv = [torch.empty_like(t) for t in send]
     stream = torch.cuda.Stream(device=dev)
@@ -659,6 +660,29 @@ def run_ours(args, world, rank, local):
                 "avg_launch_ms": round(avg_launch_ms, 4), "launches": launches,
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s"}
+
+    # ---- end to end: pinned host inputs -> device, allreduce, results -> host
+    with torch.cuda.stream(stream):               # one untimed step: first touch of every buffer
+        for r in range(k):
+            send[r].copy_(h_send[r], non_blocking=True)
+        comm.allreduce(send, recv, stream=stream)
+        for r in range(k):
+            h_recv[r].copy_(recv[r], non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            for r in range(k):
+                send[r].copy_(h_send[r], non_blocking=True)
+            comm.allreduce(send, recv, stream=stream)
+            for r in range(k):
+                h_recv[r].copy_(recv[r], non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1) / args.e2e_steps, dev)
+    e2e = {"value": round(world * bus_bytes(k, per_rank) / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": k * per_rank, "d2h_bytes_per_step": k * per_rank, "ms_per_step": round(e2e_ms, 3)}
 
     extras = {}
     if not args.no_extras:
@@ -724,24 +748,6 @@ def run_ours(args, world, rank, local):
         bucket_pool = None
         extras["sweeps"] = leg_sweeps(sms)
         extras["host_overhead_us"] = leg_host_overhead()
-
-    # ---- end to end: pinned host inputs -> device, allreduce, results -> host
-    h_recv = [torch.empty_like(t).pin_memory() for t in h_send]
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(args.e2e_steps):
-            for r in range(k):
-                send[r].copy_(h_send[r], non_blocking=True)
-            comm.allreduce(send, recv, stream=stream)
-            for r in range(k):
-                h_recv[r].copy_(recv[r], non_blocking=True)
-        e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1) / args.e2e_steps, dev)
-    e2e = {"value": round(world * bus_bytes(k, per_rank) / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-           "h2d_bytes_per_step": k * per_rank, "d2h_bytes_per_step": k * per_rank, "ms_per_step": round(e2e_ms, 3)}
 
     cpu = None
     if rank == 0:
