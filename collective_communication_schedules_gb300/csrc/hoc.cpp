@@ -28,6 +28,7 @@
 #include <unordered_map>
 #include <vector>
 
+#include "comm.h"
 #include "hoc.h"
 #include "hoc_internal.h"
 #include "plan.h"
@@ -78,53 +79,7 @@ int env_int(const char* name, int dflt) {
 
 }  // namespace
 
-struct ProfPair {
-  cudaEvent_t start, stop;
-  int kind;
-};
-
-struct Bind {
-  const void* send[kMaxRanks] = {};
-  void* recv[kMaxRanks] = {};
-};
-
 }  // namespace hoc
-
-struct hocComm {
-  int k = 0;
-  int device = 0;
-  int sms = 0;
-  hoc::Cfg cfg;
-  std::mutex mu;
-  // Internal copy streams, one set per caller stream (the paper's stream
-  // manager keeps its handshake state per GPU stream): calls issued on
-  // different caller streams never queue behind each other.
-  struct StreamSet {
-    cudaStream_t owner;
-    std::vector<cudaStream_t> copy;
-  };
-  std::vector<StreamSet> sets;
-  cudaStream_t capture = nullptr;  // origin stream for graph capture
-  std::vector<cudaEvent_t> ev;     // plan edges (timing disabled)
-  std::vector<cudaEvent_t> join;   // one per internal stream
-  cudaEvent_t fork = nullptr;
-  int* status = nullptr;           // device status word(s) of the TMA kernel
-  std::unordered_map<std::string, hoc::Plan> plans;
-  struct GraphEntry {
-    cudaGraphExec_t exec;
-    std::list<std::string>::iterator lru;
-    int max_ctas;
-  };
-  std::unordered_map<std::string, GraphEntry> graphs;
-  std::list<std::string> lru;
-  hocOpStats_t last{};
-  bool profiling = false;
-  std::vector<hoc::ProfPair> prof_pending;
-  std::vector<cudaEvent_t> prof_free;
-  int prof_launches[3] = {0, 0, 0};
-  double prof_ms[3] = {0, 0, 0};
-  int reduce_ctas_per_sm[3][hoc::kMaxRanks + 1][2] = {};
-};
 
 namespace hoc {
 namespace {
@@ -350,6 +305,29 @@ hocResult_t issue(hocComm* c, const Plan& p, const Bind& bd, cudaStream_t s0, in
   return HOC_SUCCESS;
 }
 
+}  // namespace
+
+hocResult_t issue_plan(hocComm* c, const Plan& p, const Bind& bd, cudaStream_t s0, int* max_ctas) {
+  return issue(c, p, bd, s0, max_ctas);
+}
+
+hocResult_t get_plan(hocComm* c, const CallShape& shape, const Plan** plan) {
+  const std::string pkey = plan_key(shape);
+  auto it = c->plans.find(pkey);
+  if (it == c->plans.end()) {
+    Plan p;
+    HOC_TRY(build_plan(c->cfg, shape, &p));
+    if (c->plans.size() > 256) c->plans.clear();
+    it = c->plans.emplace(pkey, std::move(p)).first;
+  }
+  *plan = &it->second;
+  return HOC_SUCCESS;
+}
+
+void set_error_detail(const char* what) { set_detail(what); }
+
+namespace {
+
 std::string graph_key(const std::string& pkey, const Bind& bd, int k) {
   std::string key = pkey;
   key.append(reinterpret_cast<const char*>(bd.send), sizeof(void*) * k);
@@ -359,14 +337,9 @@ std::string graph_key(const std::string& pkey, const Bind& bd, int k) {
 
 hocResult_t execute(hocComm* c, const CallShape& shape, const Bind& bd, cudaStream_t stream) {
   const std::string pkey = plan_key(shape);
-  auto it = c->plans.find(pkey);
-  if (it == c->plans.end()) {
-    Plan p;
-    HOC_TRY(build_plan(c->cfg, shape, &p));
-    if (c->plans.size() > 256) c->plans.clear();
-    it = c->plans.emplace(pkey, std::move(p)).first;
-  }
-  const Plan& p = it->second;
+  const Plan* pp = nullptr;
+  HOC_TRY(get_plan(c, shape, &pp));
+  const Plan& p = *pp;
   hocOpStats_t stats{};
   stats.path = p.path;
   stats.kernels = p.kernels;
@@ -681,6 +654,7 @@ hocResult_t hoc_init(hocComm_t* comm, int nranks, int device, const hocConfig_t*
 
 hocResult_t hoc_destroy(hocComm_t comm) {
   if (!comm) return HOC_ERR_NOT_INITIALIZED;
+  proxy_shutdown(comm);
   {
     DeviceGuard g(comm->device);
     for (auto& set : comm->sets)
@@ -896,7 +870,11 @@ hocResult_t hoc_wait(hocComm_t comm, void* stream, int timeout_ms) {
       std::this_thread::sleep_for(std::chrono::microseconds(50));
     }
   }
-  if (comm->cfg.fault == kFaultProxyStall) {
+  if (const int perr = proxy_take_error(comm)) {
+    set_detail("a device-count all-to-all was released by the proxy on an error or its watchdog");
+    return hocResult_t(perr);
+  }
+  if (comm->cfg.fault == kFaultProxyStall && !comm->proxy) {
     // Injected on the host: a completion that never arrives.
     std::this_thread::sleep_until(deadline);
     set_detail("hoc_wait: injected proxy stall");

@@ -87,6 +87,10 @@ _SIGS = {
                                         C.c_int, C.c_int, C.c_void_p, C.c_int]),
 }
 NOALLOC_MAX_MOVES = 192
+_SIGS["hoc_alltoall_device_counts"] = (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p),
+                                                 C.c_void_p, C.POINTER(C.c_size_t), C.c_int, C.c_void_p])
+_SIGS["hoc_proxy_status"] = (C.c_int, [C.c_void_p, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64),
+                                       C.POINTER(C.c_int)])
 _SIGS["hoc_topo_schedule"] = (C.c_int, [C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_int), C.POINTER(C.c_uint64),
                                         C.c_uint64, C.c_uint64, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64),
                                         C.POINTER(C.c_double), C.c_int, C.POINTER(C.c_int),
@@ -259,6 +263,23 @@ class Comm:
         dtype = _dtype_code(send) if dtype is None else dtype
         _check(lib().hoc_sendrecv(self._h, int(src_rank), _ptr(send), int(dst_rank), _ptr(recv), count, dtype,
                                   _stream(stream)), "hoc_sendrecv")
+
+    def alltoall_device_counts(self, send, recv, d_counts, recv_capacity, dtype=None, stream=None):
+        """All-to-all(v) whose k x k counts (uint64/int64, elements, row = source) live on the device.
+
+        The counts reach a host proxy through the stream-memory-operation
+        handshake; the call returns without waiting (see include/hoc_proxy.h)."""
+        dtype = _dtype_code(send[0]) if dtype is None else dtype
+        cap = (C.c_size_t * self.k)(*[int(v) for v in recv_capacity])
+        _check(lib().hoc_alltoall_device_counts(self._h, _ptr_array(send), _ptr_array(recv), _ptr(d_counts), cap,
+                                                dtype, _stream(stream)), "hoc_alltoall_device_counts")
+
+    def proxy_status(self) -> dict:
+        done = C.c_uint64()
+        rel = C.c_uint64()
+        err = C.c_int()
+        _check(lib().hoc_proxy_status(self._h, C.byref(done), C.byref(rel), C.byref(err)), "hoc_proxy_status")
+        return {"completed": done.value, "released_on_error": rel.value, "first_error": err.value}
 
     # ------------------------------------------------------------- control
     def wait(self, stream=None, timeout_ms: int = 60000):

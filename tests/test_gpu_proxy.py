@@ -1,0 +1,106 @@
+"""Stream-memory-operation handshake with the host proxy, on the GPU.
+
+The counts of an all-to-all(v) are computed on the device (as an expert
+router would); the caller's stream hands them to the host proxy through the
+start / end flags and the proxy moves the data on copy engines.  Checked
+against the CPU oracle; the watchdog and error paths must release the stream
+(no stream is left waiting on a flag).
+"""
+import numpy as np
+import pytest
+import torch
+
+from collective_communication_schedules_gb300 import hoc, inputs
+from oracle import alltoall as o_a2a
+from tests.gpu_util import to_device, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+def _device_counts(routing_dev, k, experts, hidden):
+    """k x k element counts from device-resident routing (the producer kernel)."""
+    rows = []
+    for r in range(k):
+        dst = routing_dev[r].reshape(-1) // (experts // k)
+        rows.append(torch.bincount(dst, minlength=k) * hidden)
+    return torch.stack(rows).to(torch.int64).contiguous()
+
+
+def test_device_count_alltoall_matches_oracle():
+    k, tokens, hidden, experts, topk = 8, 512, 256, 64, 6
+    routing = inputs.ep_routing(k, tokens, experts, topk, 1.1, seed_base=5100)
+    counts = np.stack([np.bincount(r.reshape(-1) // (experts // k), minlength=k) for r in routing]) * hidden
+    rng = np.random.default_rng(3)
+    sends = [rng.integers(0, 1 << 16, size=int(counts[s].sum())).astype(np.uint16) for s in range(k)]
+    want = o_a2a.alltoallv(sends, counts)
+    lens = o_a2a.recv_lengths(counts)
+    with hoc.Comm(k, 0, hoc.Config(chunk_bytes=1 << 16)) as c:
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            rdev = [torch.from_numpy(r).cuda() for r in routing]
+            d_counts = _device_counts(rdev, k, experts, hidden)
+            sd = [to_device(x, "bfloat16") for x in sends]
+            rv = [torch.full((int(lens[d]) + 100,), -1, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+                  for d in range(k)]
+        c.alltoall_device_counts(sd, rv, d_counts, [t.numel() for t in rv], hoc.BFLOAT16, stream=s)
+        after = torch.zeros(1, device="cuda")
+        with torch.cuda.stream(s):
+            after += 1                                   # work after the call waits for the moves
+        c.wait(s, timeout_ms=30000)
+        torch.cuda.synchronize()
+        for d in range(k):
+            got = to_host(rv[d], "bfloat16")
+            assert np.array_equal(got[: lens[d]], want[d]), d
+            assert np.all(got[lens[d]:] == 0xFFFF)       # nothing written past the received rows
+        st = c.proxy_status()
+        assert st["completed"] == 1 and st["released_on_error"] == 0
+
+
+def test_many_tasks_reuse_slots_and_two_streams():
+    k, n = 4, 5000
+    rng = np.random.default_rng(9)
+    with hoc.Comm(k, 0) as c:
+        streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+        for it in range(40):                              # more tasks than proxy slots
+            st = streams[it % 2]
+            counts = rng.integers(0, n, size=(k, k))
+            sends = [rng.integers(0, 1 << 31, size=int(counts[s].sum())).astype(np.int32) for s in range(k)]
+            want = o_a2a.alltoallv(sends, counts)
+            with torch.cuda.stream(st):
+                d_counts = torch.from_numpy(counts.astype(np.int64)).cuda()
+                sd = [to_device(x, "int32") if len(x) else torch.zeros(1, dtype=torch.int32, device="cuda") for x in sends]
+                rv = [torch.zeros(max(1, int(counts[:, d].sum())), dtype=torch.int32, device="cuda") for d in range(k)]
+            c.alltoall_device_counts(sd, rv, d_counts, [t.numel() for t in rv], hoc.INT32, stream=st)
+            st.synchronize()
+            for d in range(k):
+                assert np.array_equal(to_host(rv[d], "int32")[: len(want[d])], want[d]), (it, d)
+        assert c.proxy_status()["completed"] == 40
+
+
+def test_capacity_overflow_releases_the_stream():
+    k = 2
+    with hoc.Comm(k, 0) as c:
+        d_counts = torch.tensor([[10, 10], [10, 10]], dtype=torch.int64, device="cuda")
+        sd = [torch.ones(20, dtype=torch.int32, device="cuda") for _ in range(k)]
+        rv = [torch.zeros(20, dtype=torch.int32, device="cuda") for _ in range(k)]
+        c.alltoall_device_counts(sd, rv, d_counts, [5, 20], hoc.INT32)
+        with pytest.raises(hoc.HocError) as e:
+            c.wait(timeout_ms=30000)
+        assert e.value.code == hoc.ERR_INVALID_ARG
+        torch.cuda.synchronize()                         # the stream was released
+        assert int(rv[0].sum()) == 0 and int(rv[1].sum()) == 0
+
+
+def test_watchdog_releases_a_stalled_task(monkeypatch):
+    monkeypatch.setenv("HOC_FAULT", "proxy_stall")
+    k = 2
+    with hoc.Comm(k, 0) as c:
+        d_counts = torch.tensor([[4, 4], [4, 4]], dtype=torch.int64, device="cuda")
+        sd = [torch.ones(8, dtype=torch.int32, device="cuda") for _ in range(k)]
+        rv = [torch.zeros(8, dtype=torch.int32, device="cuda") for _ in range(k)]
+        c.alltoall_device_counts(sd, rv, d_counts, [8, 8], hoc.INT32)
+        with pytest.raises(hoc.HocError) as e:
+            c.wait(timeout_ms=30000)
+        assert e.value.code == hoc.ERR_TIMEOUT
+        torch.cuda.synchronize()
+        assert c.proxy_status()["released_on_error"] == 1
