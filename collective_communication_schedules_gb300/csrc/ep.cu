@@ -1,0 +1,161 @@
+// Expert-parallel pack and combine around the dispatch / combine all-to-all
+// (HOCCL section 2.1 and Table 1: EP token dispatch and combine).
+//
+// pack   (dispatch side): a stable counting sort of the (token, slot) pairs of
+//        one source rank by expert -- experts of a rank are contiguous, so this
+//        is the (destination rank, expert, token, slot) order -- followed by a
+//        row gather into the send buffer and the per-destination element counts
+//        that the all-to-all needs (on the device, for hoc_alltoall_device_counts).
+// combine (unpack): every token's output row is the gate-weighted sum of its
+//        topk returned rows, folded in slot order in binary32 (products and sums
+//        each rounded to nearest even, no fused multiply-add) and rounded once to
+//        bf16.
+// Pairs whose expert id lies outside [0, experts) are dropped: they are sent
+// nowhere and add nothing to the combine.
+#include <cuda_bf16.h>
+
+#include "hoc_internal.h"
+#include "hoc_ep.h"
+
+namespace hoc {
+namespace {
+
+constexpr int kEpThreads = 256;
+
+// One CTA per expert: how many pairs chose it.
+__global__ void ep_count_kernel(const int32_t* __restrict__ ids, int n, int32_t* __restrict__ cnt) {
+  const int e = blockIdx.x;
+  int total = 0;
+  for (int base = 0; base < n; base += kEpThreads) {
+    const int i = base + threadIdx.x;
+    total += __syncthreads_count(i < n && ids[i] == e);
+  }
+  if (threadIdx.x == 0) cnt[e] = total;
+}
+
+// One CTA per expert: place its pairs, in (token, slot) order, after the pairs
+// of all smaller experts.
+__global__ void ep_place_kernel(const int32_t* __restrict__ ids, int n, const int32_t* __restrict__ cnt,
+                                int32_t* __restrict__ perm, int32_t* __restrict__ pos_of,
+                                unsigned long long* __restrict__ dst_counts, int hidden, int per_rank) {
+  __shared__ int warp_n[kEpThreads / 32];
+  const int e = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int offset = 0;
+  for (int j = 0; j < e; ++j) offset += cnt[j];
+  int running = 0;
+  for (int base = 0; base < n; base += kEpThreads) {
+    const int i = base + threadIdx.x;
+    const bool mine = i < n && ids[i] == e;
+    const unsigned ballot = __ballot_sync(0xFFFFFFFFu, mine);
+    if (lane == 0) warp_n[warp] = __popc(ballot);
+    __syncthreads();
+    int before = 0, chunk = 0;
+    for (int w = 0; w < kEpThreads / 32; ++w) {
+      if (w < warp) before += warp_n[w];
+      chunk += warp_n[w];
+    }
+    if (mine) {
+      const int pos = offset + running + before + __popc(ballot & ((1u << lane) - 1u));
+      perm[pos] = i;
+      pos_of[i] = pos;
+    }
+    running += chunk;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0 && cnt[e] > 0) atomicAdd(dst_counts + e / per_rank, (unsigned long long)cnt[e] * hidden);
+}
+
+// Warp per row: send[pos] = x[perm[pos] / topk]; rows of `hb` bytes.
+__global__ void ep_gather_kernel(const char* __restrict__ x, const int32_t* __restrict__ perm, int n, int topk,
+                                 int hb, char* __restrict__ send, int vec) {
+  const int warps = blockDim.x >> 5;
+  const int lane = threadIdx.x & 31;
+  for (int pos = blockIdx.x * warps + (threadIdx.x >> 5); pos < n; pos += gridDim.x * warps) {
+    const int src = perm[pos];
+    if (src < 0) continue;  // dropped pair: nothing to send
+    const char* s = x + size_t(src / topk) * hb;
+    char* d = send + size_t(pos) * hb;
+    if (vec) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(s);
+      uint4* d4 = reinterpret_cast<uint4*>(d);
+      for (int v = lane; v < hb / 16; v += 32) d4[v] = __ldg(s4 + v);
+    } else {
+      for (int b = lane; b < hb; b += 32) d[b] = s[b];
+    }
+  }
+}
+
+// Warp per token: y[t] = bf16(sum_j fp32(w[t,j] * row[pos_of[t*topk + j]])).
+__global__ void ep_combine_kernel(const uint16_t* __restrict__ rows, const int32_t* __restrict__ pos_of,
+                                  const float* __restrict__ w, int tokens, int topk, int hidden, int n_rows,
+                                  uint16_t* __restrict__ y) {
+  const int warps = blockDim.x >> 5;
+  const int lane = threadIdx.x & 31;
+  for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < tokens; t += gridDim.x * warps) {
+    for (int h = lane; h < hidden; h += 32) {
+      float acc = 0.f;
+      bool any = false;
+      for (int j = 0; j < topk; ++j) {
+        const int p = pos_of[size_t(t) * topk + j];
+        if (p < 0 || p >= n_rows) continue;
+        const float r = __uint_as_float(uint32_t(rows[size_t(p) * hidden + h]) << 16);
+        const float prod = __fmul_rn(w[size_t(t) * topk + j], r);
+        acc = any ? __fadd_rn(acc, prod) : prod;
+        any = true;
+      }
+      y[size_t(t) * hidden + h] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+    }
+  }
+}
+
+int grid_for(int items, int per_cta) {
+  int dev = 0, sms = 1;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int want = (items + per_cta - 1) / per_cta;
+  const int cap = sms * 8;
+  return want < 1 ? 1 : (want < cap ? want : cap);
+}
+
+}  // namespace
+}  // namespace hoc
+
+extern "C" hocResult_t hoc_ep_pack(const int32_t* expert_ids, const void* x, int tokens, int topk, int hidden,
+                                   int experts, int nranks, void* send, int32_t* perm, int32_t* pos_of,
+                                   uint64_t* dst_counts, int32_t* workspace, void* stream) {
+  using namespace hoc;
+  if (tokens < 0 || topk < 1 || hidden < 1 || experts < 1 || nranks < 1 || experts % nranks != 0)
+    return HOC_ERR_INVALID_ARG;
+  if (tokens == 0) return HOC_SUCCESS;
+  if (!expert_ids || !x || !send || !perm || !pos_of || !dst_counts || !workspace) return HOC_ERR_INVALID_ARG;
+  if (size_t(tokens) * topk > size_t(INT32_MAX)) return HOC_ERR_INVALID_ARG;
+  const int n = tokens * topk;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(perm, 0xFF, sizeof(int32_t) * size_t(n), s) != cudaSuccess ||
+      cudaMemsetAsync(pos_of, 0xFF, sizeof(int32_t) * size_t(n), s) != cudaSuccess ||
+      cudaMemsetAsync(dst_counts, 0, sizeof(uint64_t) * size_t(nranks), s) != cudaSuccess)
+    return HOC_ERR_CUDA;
+  ep_count_kernel<<<experts, kEpThreads, 0, s>>>(expert_ids, n, workspace);
+  ep_place_kernel<<<experts, kEpThreads, 0, s>>>(expert_ids, n, workspace, perm, pos_of,
+                                                 reinterpret_cast<unsigned long long*>(dst_counts), hidden,
+                                                 experts / nranks);
+  const int hb = hidden * 2;
+  const int vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(send)) & 15u) == 0 && hb % 16 == 0;
+  ep_gather_kernel<<<grid_for(n, 8), 256, 0, s>>>(static_cast<const char*>(x), perm, n, topk, hb,
+                                                  static_cast<char*>(send), vec);
+  return cudaGetLastError() == cudaSuccess ? HOC_SUCCESS : HOC_ERR_CUDA;
+}
+
+extern "C" hocResult_t hoc_ep_combine(const void* rows, const int32_t* pos_of, const float* weights, int tokens,
+                                      int topk, int hidden, void* y, void* stream) {
+  using namespace hoc;
+  if (tokens < 0 || topk < 1 || hidden < 1) return HOC_ERR_INVALID_ARG;
+  if (tokens == 0) return HOC_SUCCESS;
+  if (!rows || !pos_of || !weights || !y) return HOC_ERR_INVALID_ARG;
+  if (size_t(tokens) * topk > size_t(INT32_MAX)) return HOC_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ep_combine_kernel<<<grid_for(tokens, 8), 256, 0, s>>>(static_cast<const uint16_t*>(rows), pos_of, weights, tokens,
+                                                        topk, hidden, tokens * topk, static_cast<uint16_t*>(y));
+  return cudaGetLastError() == cudaSuccess ? HOC_SUCCESS : HOC_ERR_CUDA;
+}

@@ -48,6 +48,7 @@ struct Slot {
   Bind bind;
   int dtype = 0;
   std::vector<size_t> cap;
+  int transpose = 0;
   cudaEvent_t done = nullptr;
   bool stalled = false;  // host-injected: the moves are never reported complete
   std::chrono::steady_clock::time_point deadline;
@@ -98,7 +99,9 @@ void start_task(Proxy* P, Slot& s) {
   std::atomic_thread_fence(std::memory_order_acquire);
   const int k = P->k;
   std::vector<size_t> cnt(size_t(k) * k);
-  for (size_t i = 0; i < cnt.size(); ++i) cnt[i] = size_t(s.counts[i]);
+  for (int a = 0; a < k; ++a)
+    for (int b = 0; b < k; ++b)
+      cnt[size_t(a) * k + b] = size_t(s.transpose ? s.counts[size_t(b) * k + a] : s.counts[size_t(a) * k + b]);
   *s.start = 0;  // acknowledge: the stream moves on to wait for the end flag
   std::atomic_thread_fence(std::memory_order_seq_cst);
   {
@@ -309,8 +312,8 @@ int proxy_take_error(hocComm* c) { return c->proxy ? c->proxy->first_error.excha
 using namespace hoc;
 
 extern "C" hocResult_t hoc_alltoall_device_counts(hocComm_t comm, const void* const* send, void* const* recv,
-                                                  const uint64_t* d_sendcounts, const size_t* recv_capacity,
-                                                  hocDataType_t dtype, void* stream) {
+                                                  const uint64_t* d_sendcounts, int transpose,
+                                                  const size_t* recv_capacity, hocDataType_t dtype, void* stream) {
   if (!comm) return HOC_ERR_NOT_INITIALIZED;
   if (!send || !recv || !d_sendcounts || !recv_capacity || dtype_bytes(dtype) == 0) return HOC_ERR_INVALID_ARG;
   const int k = comm->k;
@@ -357,6 +360,7 @@ extern "C" hocResult_t hoc_alltoall_device_counts(hocComm_t comm, const void* co
       slot->bind.recv[r] = recv[r];
     }
     slot->dtype = dtype;
+    slot->transpose = transpose != 0;
     slot->cap.assign(recv_capacity, recv_capacity + k);
     slot->state = kQueued;
   }

@@ -88,7 +88,11 @@ _SIGS = {
 }
 NOALLOC_MAX_MOVES = 192
 _SIGS["hoc_alltoall_device_counts"] = (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p),
-                                                 C.c_void_p, C.POINTER(C.c_size_t), C.c_int, C.c_void_p])
+                                                 C.c_void_p, C.c_int, C.POINTER(C.c_size_t), C.c_int, C.c_void_p])
+_SIGS["hoc_ep_pack"] = (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p,
+                                  C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p])
+_SIGS["hoc_ep_combine"] = (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p,
+                                     C.c_void_p])
 _SIGS["hoc_proxy_status"] = (C.c_int, [C.c_void_p, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64),
                                        C.POINTER(C.c_int)])
 _SIGS["hoc_topo_schedule"] = (C.c_int, [C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_int), C.POINTER(C.c_uint64),
@@ -264,15 +268,17 @@ class Comm:
         _check(lib().hoc_sendrecv(self._h, int(src_rank), _ptr(send), int(dst_rank), _ptr(recv), count, dtype,
                                   _stream(stream)), "hoc_sendrecv")
 
-    def alltoall_device_counts(self, send, recv, d_counts, recv_capacity, dtype=None, stream=None):
+    def alltoall_device_counts(self, send, recv, d_counts, recv_capacity, dtype=None, stream=None,
+                               transpose: bool = False):
         """All-to-all(v) whose k x k counts (uint64/int64, elements, row = source) live on the device.
 
         The counts reach a host proxy through the stream-memory-operation
         handshake; the call returns without waiting (see include/hoc_proxy.h)."""
         dtype = _dtype_code(send[0]) if dtype is None else dtype
         cap = (C.c_size_t * self.k)(*[int(v) for v in recv_capacity])
-        _check(lib().hoc_alltoall_device_counts(self._h, _ptr_array(send), _ptr_array(recv), _ptr(d_counts), cap,
-                                                dtype, _stream(stream)), "hoc_alltoall_device_counts")
+        _check(lib().hoc_alltoall_device_counts(self._h, _ptr_array(send), _ptr_array(recv), _ptr(d_counts),
+                                                int(bool(transpose)), cap, dtype, _stream(stream)),
+               "hoc_alltoall_device_counts")
 
     def proxy_status(self) -> dict:
         done = C.c_uint64()
@@ -343,6 +349,21 @@ def topo_schedule(C_matrix, node_of, sym, bw_nvlink: int, bw_rdma: int):
     Tm = [[T[u * G + v] for v in range(G)] for u in range(G)]
     stages = [[[st[s * G * G + u * G + v] for v in range(G)] for u in range(G)] for s in range(n.value)]
     return Tm, stages, [ta[s] for s in range(n.value)], tot.value
+
+
+def ep_pack(expert_ids, x, experts: int, nranks: int, send, perm, pos_of, dst_counts, workspace, stream=None):
+    """Dispatch-side pack of one source rank (device tensors; see include/hoc_ep.h)."""
+    tokens, hidden = x.shape
+    topk = expert_ids.numel() // tokens
+    _check(lib().hoc_ep_pack(_ptr(expert_ids), _ptr(x), int(tokens), int(topk), int(hidden), int(experts),
+                             int(nranks), _ptr(send), _ptr(perm), _ptr(pos_of), _ptr(dst_counts), _ptr(workspace),
+                             _stream(stream)), "hoc_ep_pack")
+
+
+def ep_combine(rows, pos_of, weights, tokens: int, topk: int, hidden: int, y, stream=None):
+    """Gate-weighted top-k combine of one source rank (see include/hoc_ep.h)."""
+    _check(lib().hoc_ep_combine(_ptr(rows), _ptr(pos_of), _ptr(weights), int(tokens), int(topk), int(hidden),
+                                _ptr(y), _stream(stream)), "hoc_ep_combine")
 
 
 def sm_count(device: int = 0) -> int:

@@ -34,7 +34,9 @@ extern "C" {
 
 /* All-to-all(v) with device-resident counts.  d_sendcounts: device array of
  * k*k uint64 element counts (row = source), valid when the work before this
- * call on `stream` has finished.  recv_capacity: host array of k element
+ * call on `stream` has finished; with transpose != 0 the matrix is read
+ * transposed (row = destination), so the counts of a dispatch serve the
+ * inverse exchange (the combine) unchanged.  recv_capacity: host array of k element
  * capacities of the receive buffers (the counts are unknown at call time);
  * if a receiver's total exceeds its capacity nothing is moved and the error is
  * reported.  Displacements are prefix sums in rank order.  Returns as soon as
@@ -42,7 +44,7 @@ extern "C" {
  * data.  The first call starts the proxy thread and allocates its pinned host
  * flags.  Not allowed while `stream` is being captured into a graph. */
 hocResult_t hoc_alltoall_device_counts(hocComm_t comm, const void* const* send, void* const* recv,
-                                       const uint64_t* d_sendcounts, const size_t* recv_capacity,
+                                       const uint64_t* d_sendcounts, int transpose, const size_t* recv_capacity,
                                        hocDataType_t dtype, void* stream);
 
 /* Proxy bookkeeping: tasks completed, tasks released by the watchdog or an
