@@ -495,6 +495,51 @@ def leg_expert_dispatch(peak):
                 "sms_used": st["sms_used"], "copies_per_call": st["copies"]}
     ok = all(torch.equal(a.view(torch.int16), b.view(torch.int16)) for a, b in zip(send, back))
     out["combine_restores_dispatch_input"] = bool(ok)
+
+    # The whole round on the device, with no host synchronisation: pack kernels,
+    # dispatch with device-computed counts (stream-memop handshake with the host
+    # proxy), the inverse exchange, and the weighted top-k combine kernel.
+    tokens, topk, experts = w["tokens"], w["topk"], w["experts"]
+    s = torch.cuda.Stream()
+    xs = [torch.randn((tokens, h), generator=g, device="cuda").to(torch.bfloat16) for _ in range(k)]
+    ids = [torch.from_numpy(routing[r].astype(np.int32)).cuda() for r in range(k)]
+    gate = [torch.rand(tokens * topk, generator=g, device="cuda") for _ in range(k)]
+    n = tokens * topk
+    psend = [torch.empty((n, h), dtype=torch.bfloat16, device="cuda") for _ in range(k)]
+    perm = [torch.empty(n, dtype=torch.int32, device="cuda") for _ in range(k)]
+    pos = [torch.empty(n, dtype=torch.int32, device="cuda") for _ in range(k)]
+    wsp = [torch.empty(experts, dtype=torch.int32, device="cuda") for _ in range(k)]
+    d_counts = torch.empty((k, k), dtype=torch.int64, device="cuda")
+    cap = [int(ecounts[:, d].sum()) for d in range(k)]
+    precv = [torch.empty(cap[d], dtype=torch.bfloat16, device="cuda") for d in range(k)]
+    pback = [torch.empty(n * h, dtype=torch.bfloat16, device="cuda") for _ in range(k)]
+    ys = [torch.empty((tokens, h), dtype=torch.bfloat16, device="cuda") for _ in range(k)]
+
+    with hoc.Comm(k, 0) as c:
+        def round_trip():
+            for r in range(k):
+                hoc.ep_pack(ids[r], xs[r], experts, k, psend[r], perm[r], pos[r], d_counts[r], wsp[r], stream=s)
+            c.alltoall_device_counts([t.view(-1) for t in psend], precv, d_counts, cap, hoc.BFLOAT16, stream=s)
+            c.alltoall_device_counts(precv, pback, d_counts, [n * h] * k, hoc.BFLOAT16, stream=s, transpose=True)
+            for r in range(k):
+                hoc.ep_combine(pback[r], pos[r], gate[r], tokens, topk, h, ys[r], stream=s)
+        round_trip()
+        c.wait(s, timeout_ms=60000)
+        host_us = []
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(5):
+            t0 = time.perf_counter()
+            round_trip()
+            host_us.append((time.perf_counter() - t0) * 1e6)
+        e1.record(s)
+        c.wait(s, timeout_ms=60000)
+        ms = e0.elapsed_time(e1) / 5
+        st = c.proxy_status()
+    out["device_round_trip"] = {
+        "ms": round(ms, 4), "host_issue_us": round(statistics.median(host_us), 1),
+        "steps": "pack kernels -> dispatch (device counts, host proxy) -> combine exchange -> weighted combine kernel",
+        "proxy_tasks_completed": st["completed"], "proxy_tasks_released_on_error": st["released_on_error"]}
     return out
 
 
