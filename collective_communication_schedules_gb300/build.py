@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libhoc.so")
 
-SOURCES = ["reduce.cu", "reduce_tma.cu", "tma_copy.cu", "workload.cu", "plan.cpp", "hoc.cpp", "topo_sched.cpp", "proxy.cpp", "ep.cu"]
+SOURCES = ["reduce.cu", "reduce_tma.cu", "tma_copy.cu", "workload.cu", "plan.cpp", "hoc.cpp", "topo_sched.cpp", "proxy.cpp", "ep.cu", "host_ar.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 # IEEE arithmetic in the reduce kernels: no flush to zero, no fast math.

@@ -65,6 +65,7 @@ struct hocComm {
   double prof_ms[3] = {0, 0, 0};
   int reduce_ctas_per_sm[3][hoc::kMaxRanks + 1][2] = {};
   hoc::Proxy* proxy = nullptr;  // created by the first device-count all-to-all
+  void* host_ar = nullptr;      // staging and streams of hoc_allreduce_host (host_ar.cpp)
 };
 
 namespace hoc {
@@ -75,6 +76,8 @@ hocResult_t get_plan(hocComm* c, const CallShape& shape, const Plan** plan);
 hocResult_t issue_plan(hocComm* c, const Plan& p, const Bind& bd, cudaStream_t s0, int* max_ctas);
 // Release the proxy (waits, bounded, for its tasks; see proxy.cpp).
 void proxy_shutdown(hocComm* c);
+// Free what hoc_allreduce_host set up (staging slots, streams, graphs).
+void host_ar_free(hocComm* c);
 // First error of a proxy task since the last call (0 if none), then cleared.
 int proxy_take_error(hocComm* c);
 void set_error_detail(const char* what);

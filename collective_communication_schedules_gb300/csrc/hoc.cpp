@@ -477,6 +477,7 @@ hocResult_t read_cfg(const hocConfig_t* in, int k, Cfg* out) {
 
 void free_comm(hocComm* c) {
   if (!c) return;
+  host_ar_free(c);
   for (auto& g : c->graphs) cudaGraphExecDestroy(g.second.exec);
   for (cudaEvent_t e : c->ev) cudaEventDestroy(e);
   for (cudaEvent_t e : c->join) cudaEventDestroy(e);

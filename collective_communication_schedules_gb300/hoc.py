@@ -93,6 +93,8 @@ _SIGS["hoc_ep_pack"] = (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_
                                   C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p])
 _SIGS["hoc_ep_combine"] = (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p,
                                      C.c_void_p])
+_SIGS["hoc_allreduce_host"] = (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_size_t,
+                                         C.c_int, C.c_int, C.c_void_p])
 _SIGS["hoc_proxy_status"] = (C.c_int, [C.c_void_p, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64),
                                        C.POINTER(C.c_int)])
 _SIGS["hoc_topo_schedule"] = (C.c_int, [C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_int), C.POINTER(C.c_uint64),
@@ -240,6 +242,14 @@ class Comm:
         dtype = _dtype_code(send[0]) if dtype is None else dtype
         _check(lib().hoc_allreduce(self._h, _ptr_array(send), _ptr_array(recv), count, dtype, SUM,
                                    _stream(stream)), "hoc_allreduce")
+
+    def allreduce_host(self, h_send, h_recv, count=None, dtype=None, stream=None):
+        """AllReduce of host (CPU) tensors, pipelined with the host<->device copies."""
+        count = h_send[0].numel() if count is None else count
+        dtype = _dtype_code(h_send[0]) if dtype is None else dtype
+        ptrs = lambda xs: (C.c_void_p * len(xs))(*[x if isinstance(x, int) else x.data_ptr() for x in xs])
+        _check(lib().hoc_allreduce_host(self._h, ptrs(h_send), ptrs(h_recv), count, dtype, SUM, _stream(stream)),
+               "hoc_allreduce_host")
 
     def reduce_scatter(self, send, recv, recvcount=None, dtype=None, stream=None):
         recvcount = recv[0].numel() if recvcount is None else recvcount

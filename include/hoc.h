@@ -130,6 +130,19 @@ hocResult_t hoc_destroy(hocComm_t comm);
 hocResult_t hoc_allreduce(hocComm_t comm, const void* const* send, void* const* recv, size_t count,
                           hocDataType_t dtype, hocRedOp_t op, void* stream);
 
+/* AllReduce over HOST buffers: h_send[r], h_recv[r] are host pointers (pinned
+ * memory gives the copy engines full speed; pageable memory works, slower).
+ * Same fold and bits as hoc_allreduce.  The element range is cut into 8 MiB
+ * chunks per rank; the host->device copies of chunk q+1, the reduce of chunk
+ * q and the device->host copies of chunk q-1 overlap (both copy directions and
+ * the SMs at once), through two device staging slots the communicator
+ * allocates on first use.  Stream-ordered like every call; in place:
+ * h_send[r] == h_recv[r].  Calls that run at the same time on the GPU (on
+ * different streams without ordering between them) share those staging
+ * slots and race. */
+hocResult_t hoc_allreduce_host(hocComm_t comm, const void* const* h_send, void* const* h_recv, size_t count,
+                               hocDataType_t dtype, hocRedOp_t op, void* stream);
+
 /* ReduceScatter (sum).  send[r] holds k*recvcount elements, recv[r] recvcount.
  * recv[r] = block r of the fold above (block size recvcount for every rank).
  * In place: recv[r] == (elem*)send[r] + r*recvcount. */
