@@ -707,27 +707,34 @@ def run_ours(args, world, rank, local):
                 if peak_kind == "measured" else "fallback 6.8 TB/s"}
 
     # ---- end to end: pinned host inputs -> device, allreduce, results -> host
-    with torch.cuda.stream(stream):               # one untimed step: first touch of every buffer
-        for r in range(k):
-            send[r].copy_(h_send[r], non_blocking=True)
-        comm.allreduce(send, recv, stream=stream)
-        for r in range(k):
-            h_recv[r].copy_(recv[r], non_blocking=True)
+    # End to end through the host-buffer call: every step copies the 2 GiB of
+    # inputs in from pinned host memory and the 2 GiB of results out, with
+    # the copies pipelined against the reduce inside hoc_allreduce_host.
+    comm.allreduce_host(h_send, h_recv, stream=stream)          # untimed: first touch, graph capture
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        comm.allreduce_host(h_send, h_recv, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1) / args.e2e_steps, dev)
+    # the same step done the plain way: all inputs in, allreduce, all results out
+    e0.record(stream)
     with torch.cuda.stream(stream):
-        e0.record(stream)
         for _ in range(args.e2e_steps):
             for r in range(k):
                 send[r].copy_(h_send[r], non_blocking=True)
             comm.allreduce(send, recv, stream=stream)
             for r in range(k):
                 h_recv[r].copy_(recv[r], non_blocking=True)
-        e1.record(stream)
+    e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1) / args.e2e_steps, dev)
+    plain_ms = e0.elapsed_time(e1) / args.e2e_steps
     e2e = {"value": round(world * bus_bytes(k, per_rank) / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-           "h2d_bytes_per_step": k * per_rank, "d2h_bytes_per_step": k * per_rank, "ms_per_step": round(e2e_ms, 3)}
+           "h2d_bytes_per_step": k * per_rank, "d2h_bytes_per_step": k * per_rank, "ms_per_step": round(e2e_ms, 3),
+           "call": "hoc_allreduce_host (pinned host buffers, copies pipelined with the reduce)",
+           "unpipelined_ms_per_step": round(plain_ms, 3)}
 
     extras = {}
     if not args.no_extras:
