@@ -28,6 +28,8 @@
 #include <unordered_map>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "comm.h"
 #include "hoc.h"
 #include "hoc_internal.h"
@@ -556,7 +558,25 @@ hocResult_t check_reduce_args(hocComm* c, int dtype, int op) {
 
 uintptr_t U(const void* p) { return reinterpret_cast<uintptr_t>(p); }
 
+const char* op_name(int op) {
+  switch (op) {
+    case HOC_OP_ALLREDUCE: return "hoc_allreduce";
+    case HOC_OP_REDUCE_SCATTER: return "hoc_reduce_scatter";
+    case HOC_OP_ALLGATHER: return "hoc_allgather";
+    case HOC_OP_ALLTOALL: return "hoc_alltoall";
+    default: return "hoc_sendrecv";
+  }
+}
+
+// NVTX range around the host side of every call (visible in any profiler that
+// records NVTX; a no-op otherwise).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+
 hocResult_t run(hocComm* c, const CallShape& shape, const Bind& bd, void* stream) {
+  NvtxRange range(op_name(shape.op));
   std::lock_guard<std::mutex> lock(c->mu);
   DeviceGuard g(c->device);
   if (!g.ok) {
