@@ -285,3 +285,70 @@ def test_errors_are_codes():
     with pytest.raises(hoc.HocError) as e:
         hoc.Comm(3, 0, hoc.Config(ring_order=[0, 0, 1]))
     assert e.value.code == hoc.ERR_INVALID_ARG
+
+
+def test_graph_cache_eviction_keeps_results_right():
+    """More distinct buffer sets than the graph cache holds (64): evicted graphs are rebuilt."""
+    k, n = 4, 20000
+    xs = inputs.rank_inputs("float32", k, n, workload=7, slot=62)
+    want = o_ring.allreduce(xs, "float32")
+    with _comm(k, "ce", chunk_bytes=4096) as c:
+        sets = []
+        for i in range(70):
+            send = [to_device(x, "float32") for x in xs]
+            recv = [torch.empty_like(t) for t in send]
+            sets.append((send, recv))
+            c.allreduce(send, recv)
+        for send, recv in sets[:3] + sets[-3:]:     # the oldest were evicted, the newest replay
+            for t in recv:
+                t.zero_()
+            c.allreduce(send, recv)
+        c.wait()
+        for send, recv in sets:
+            for r in range(k):
+                assert_bits_equal(to_host(recv[r], "float32"), want[r], "float32", "after eviction")
+
+
+def test_debug_mode_syncs_and_checks(monkeypatch):
+    monkeypatch.setenv("HOC_DEBUG", "1")
+    k, n = 3, 9999
+    xs = inputs.rank_inputs("bfloat16", k, n, workload=7, slot=63)
+    want = o_ring.allreduce(xs, "bfloat16")
+    for path in ("ce", "tma", "fused"):
+        with _comm(k, path, chunk_bytes=2048) as c:
+            send = [to_device(x, "bfloat16") for x in xs]
+            recv = [torch.empty_like(t) for t in send]
+            c.allreduce(send, recv)
+            assert c.last_stats()["graph_replayed"] == 0          # debug mode issues directly
+            c.wait()
+            for r in range(k):
+                assert_bits_equal(to_host(recv[r], "bfloat16"), want[r], "bfloat16", f"debug {path}")
+
+
+def test_two_host_threads_share_a_communicator():
+    import threading
+
+    k, n = 4, 100000
+    xs = inputs.rank_inputs("int32", k, n, workload=7, slot=64)
+    want = o_ring.allreduce(xs, "int32")
+    errors = []
+    with _comm(k, "ce", chunk_bytes=65536) as c:
+        def worker(seed):
+            try:
+                s = torch.cuda.Stream()
+                with torch.cuda.stream(s):
+                    send = [to_device(x, "int32") for x in xs]
+                    recv = [torch.empty_like(t) for t in send]
+                for _ in range(10):
+                    c.allreduce(send, recv, stream=s)
+                s.synchronize()
+                for r in range(k):
+                    assert np.array_equal(to_host(recv[r], "int32"), want[r])
+            except Exception as e:  # pragma: no cover - reported below
+                errors.append(e)
+        th = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+        for t in th:
+            t.start()
+        for t in th:
+            t.join()
+    assert not errors, errors
