@@ -31,6 +31,10 @@ import sys
 import threading
 import time
 
+# More hardware work queues than the default 8, before any CUDA call: the
+# host-proxy handshake keeps a stream waiting on a flag while copies run.
+os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)

@@ -87,6 +87,7 @@ namespace hoc {
 namespace {
 
 constexpr size_t kMaxGraphs = 64;
+constexpr uint64_t kReduceWaves = 8;
 constexpr size_t kMaxStreamSets = 16;
 
 // The copy streams serving caller stream `s0` (created on first use).
@@ -217,9 +218,11 @@ hocResult_t run_reduce(hocComm* c, const Plan& p, const Step& st, const Bind& bd
     *max_ctas = std::max(*max_ctas, grid);
     return timed_launch(c, kind, s, [&] { return launch_reduce_tma(rp, grid, c->status, s); });
   }
+  // Whole GPU: several waves of CTAs rather than one persistent wave, so a CTA
+  // that finishes its tiles is replaced at once and loads keep streaming.
   uint64_t cap;
   if (budget > 0) cap = uint64_t(std::min(budget, c->sms));
-  else cap = uint64_t(c->sms) * ctas_per_sm(c, p.dtype, k, rp.broadcast);
+  else cap = uint64_t(c->sms) * ctas_per_sm(c, p.dtype, k, rp.broadcast) * kReduceWaves;
   const int grid = int(std::min<uint64_t>(tiles, cap));
   *max_ctas = std::max(*max_ctas, grid);
   return timed_launch(c, kind, s, [&] { return launch_reduce(rp, grid, wide, s); });

@@ -14,6 +14,7 @@
 #include <atomic>
 #include <chrono>
 #include <condition_variable>
+#include <cstdlib>
 #include <cstring>
 #include <thread>
 
@@ -223,7 +224,18 @@ void proxy_loop(Proxy* P) {
   }
 }
 
+// While the caller's stream waits on a flag, the copy-engine work the proxy
+// issues must not sit behind that wait in the same hardware queue.  CUDA maps
+// streams onto CUDA_DEVICE_MAX_CONNECTIONS queues (8 unless set before the
+// first CUDA call); with fewer than 16 the proxy refuses to run.
+constexpr int kMinConnections = 16;
+
 hocResult_t proxy_create(hocComm* c, Proxy** out) {
+  const char* conn = getenv("CUDA_DEVICE_MAX_CONNECTIONS");
+  if (!conn || atoi(conn) < kMinConnections) {
+    set_error_detail("the host-proxy handshake needs CUDA_DEVICE_MAX_CONNECTIONS >= 16 set before the first CUDA call");
+    return HOC_ERR_UNSUPPORTED;
+  }
   Proxy* P = new (std::nothrow) Proxy();
   if (!P) return HOC_ERR_OOM;
   P->c = c;

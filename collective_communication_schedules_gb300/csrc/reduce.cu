@@ -137,10 +137,14 @@ __device__ __forceinline__ void* at(void* base, uint64_t elem, int bytes) {
   return static_cast<char*>(base) + elem * uint64_t(bytes);
 }
 
+// Broadcast outputs (the fused allreduce) are not read again soon: streaming
+// stores keep them from displacing the inputs' lines in L2.  The owner-only
+// output of the copy-engine path is read right away by the all-gather copies,
+// so it is stored normally and stays in L2 for them.
 template <class Tr>
 __device__ __forceinline__ void store_vec(const ReduceParams& p, uint32_t owner, int k, uint64_t o, uint4 y) {
   if (p.broadcast) {
-    for (int r = 0; r < k; ++r) *static_cast<uint4*>(at(p.out[r], o, Tr::kBytes)) = y;
+    for (int r = 0; r < k; ++r) __stcs(static_cast<uint4*>(at(p.out[r], o, Tr::kBytes)), y);
   } else {
     *static_cast<uint4*>(at(p.out[owner], o, Tr::kBytes)) = y;
   }

@@ -19,6 +19,15 @@
  * the counts are invalid, the stream is released and hoc_proxy_status() /
  * hoc_wait() report the error.  The flags live in mapped pinned host memory
  * and the stream operations are cuStreamWriteValue32 / cuStreamWaitValue32.
+ *
+ * Requirement: while the caller's stream waits on the end flag, the copies the
+ * proxy issues must not queue behind that wait in the same hardware work
+ * queue.  CUDA spreads streams over CUDA_DEVICE_MAX_CONNECTIONS queues (8 by
+ * default); set it to 16 or more (32 is the maximum) in the environment before
+ * the process makes its first CUDA call.  Without it the call returns
+ * HOC_ERR_UNSUPPORTED.  Should a collision still happen (more streams than
+ * queues), the watchdog releases the stream after its deadline and the error
+ * is reported; no stream waits forever.
  */
 #ifndef HOC_PROXY_H
 #define HOC_PROXY_H
