@@ -60,6 +60,9 @@ def parse():
     ap.add_argument("--no-extras", action="store_true", help="skip the per-path, probe and e2e legs")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--mode", default="allreduce", choices=["allreduce", "allgather"],
+                    help="allgather: time only the all-gather moves of the workload's 32 MiB blocks "
+                         "(a profiling case: the copy-engine path launches no kernel)")
     ap.add_argument("--no-workloads", dest="workloads", action="store_false",
                     help="skip the DP bucket stream, 1F1B pipeline and EP dispatch/combine legs")
     ap.add_argument("--count", type=int, default=N_ELEMS,
@@ -827,13 +830,48 @@ def run_ours(args, world, rank, local):
     comm.close()
 
 
+def run_allgather_only(args, world, rank, local):
+    """The move half alone: 8 ranks x 32 MiB blocks gathered to every rank."""
+    import torch
+
+    from collective_communication_schedules_gb300 import hoc
+
+    torch.cuda.set_device(local)
+    k, blk = K_RANKS, args.count // K_RANKS
+    g = torch.Generator(device="cuda").manual_seed(2)
+    send = [torch.randn(blk, generator=g, device="cuda").to(torch.bfloat16) for _ in range(k)]
+    recv = [torch.empty(k * blk, dtype=torch.bfloat16, device="cuda") for _ in range(k)]
+    stream = torch.cuda.Stream()
+    with hoc.Comm(k, local, hoc.Config(path=args.path if args.path != "fused" else "ce",
+                                       chunk_bytes=args.chunk_bytes, n_copy_streams=args.copy_streams)) as c:
+        for _ in range(args.warmup):
+            c.allgather(send, recv, stream=stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            c.allgather(send, recv, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        st = c.last_stats()
+    if rank == 0:
+        print(json.dumps({"metric": "simulated-rank allgather moved GB/s (profiling case)", "unit": "GB/s",
+                          "value": round(st["bytes_exec"] / (ms * 1e-3) / 1e9, 1), "ms_per_step": round(ms, 4),
+                          "steps": args.steps, "path": args.path, "kernels_per_step": st["kernels"],
+                          "copies_per_step": st["copies"], "sms_used": st["sms_used"]}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
         return
     world, rank, local = dist_setup()
-    run_ours(args, world, rank, local)
+    if args.mode == "allgather":
+        run_allgather_only(args, world, rank, local)
+    else:
+        run_ours(args, world, rank, local)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
