@@ -72,6 +72,9 @@ int tma_ctas_per_sm();
 cudaError_t tma_prepare();  // one-time per device: shared-memory opt-in
 cudaError_t launch_tma_copy(const CopyParams& p, int grid, cudaStream_t stream);
 
+// Text for hoc_last_error_detail() (defined with the C ABI).
+void set_error_detail(const char* what);
+
 // Device status codes written by kernels.
 constexpr int kStatusTimeoutLoad = 0x1001;
 constexpr int kStatusTimeoutDrain = 0x1002;

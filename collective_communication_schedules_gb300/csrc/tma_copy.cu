@@ -280,9 +280,19 @@ cudaError_t noalloc_setup(int dev, int** out) {
 extern "C" hocResult_t hoc_tma_moves_noalloc(const void* const* src, void* const* dst, const size_t* bytes, int n,
                                              int max_ctas, void* stream, int wait) {
   using namespace hoc;
-  if (n < 0 || n > HOC_NOALLOC_MAX_MOVES || max_ctas < 0) return HOC_ERR_INVALID_ARG;
+  if (n > HOC_NOALLOC_MAX_MOVES) {
+    set_error_detail("hoc_tma_moves_noalloc: more than HOC_NOALLOC_MAX_MOVES (192) moves in one call");
+    return HOC_ERR_INVALID_ARG;
+  }
+  if (n < 0 || max_ctas < 0) {
+    set_error_detail("hoc_tma_moves_noalloc: negative move count or CTA cap");
+    return HOC_ERR_INVALID_ARG;
+  }
   if (n == 0) return HOC_SUCCESS;
-  if (!src || !dst || !bytes) return HOC_ERR_INVALID_ARG;
+  if (!src || !dst || !bytes) {
+    set_error_detail("hoc_tma_moves_noalloc: NULL array");
+    return HOC_ERR_INVALID_ARG;
+  }
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return HOC_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return HOC_ERR_CUDA;
@@ -298,7 +308,10 @@ extern "C" hocResult_t hoc_tma_moves_noalloc(const void* const* src, void* const
     if (bytes[i] == 0) continue;
     if (!src[i] || !dst[i]) return HOC_ERR_INVALID_ARG;
     const uintptr_t a = reinterpret_cast<uintptr_t>(src[i]), d = reinterpret_cast<uintptr_t>(dst[i]);
-    if (a < d + bytes[i] && d < a + bytes[i]) return HOC_ERR_INVALID_ARG;  // a move may not overlap itself
+    if (a < d + bytes[i] && d < a + bytes[i]) {  // a move may not overlap itself
+      set_error_detail("hoc_tma_moves_noalloc: a move's source and destination overlap");
+      return HOC_ERR_INVALID_ARG;
+    }
     CopyJob j{static_cast<const char*>(src[i]), static_cast<char*>(dst[i]), uint64_t(bytes[i])};
     cp.job[nj] = j;
     cp.piece_start[nj + 1] = cp.piece_start[nj] + job_pieces(j, kPieceBytes);

@@ -58,3 +58,4 @@ def test_noalloc_rejects_too_many_moves():
     with pytest.raises(hoc.HocError) as e:
         hoc.tma_moves_noalloc([a] * n, [b] * n, [16] * n)
     assert e.value.code == hoc.ERR_INVALID_ARG
+    assert "192" in str(e.value)
