@@ -72,8 +72,11 @@ namespace hoc {
 
 // Build (or fetch from the cache) the plan of a call shape.
 hocResult_t get_plan(hocComm* c, const CallShape& shape, const Plan** plan);
-// Issue a plan with stream 0 = s0 (forks to and joins from s0's copy streams).
-hocResult_t issue_plan(hocComm* c, const Plan& p, const Bind& bd, cudaStream_t s0, int* max_ctas);
+// Issue a plan with stream 0 = s0, forking to and joining from the copy
+// streams `copy_streams` (at least n_streams - 1 of them), or s0's own set
+// when that is null.
+hocResult_t issue_plan(hocComm* c, const Plan& p, const Bind& bd, cudaStream_t s0,
+                       const std::vector<cudaStream_t>* copy_streams, int* max_ctas);
 // Release the proxy (waits, bounded, for its tasks; see proxy.cpp).
 void proxy_shutdown(hocComm* c);
 // Free what hoc_allreduce_host set up (staging slots, streams, graphs).

@@ -261,14 +261,20 @@ hocResult_t run_tma(hocComm* c, const Step& st, const Bind& bd, cudaStream_t s, 
   return HOC_SUCCESS;
 }
 
-// Issue the plan: stream 0 is `s0`; 1..n are the internal copy streams.
-hocResult_t issue(hocComm* c, const Plan& p, const Bind& bd, cudaStream_t s0, int* max_ctas) {
+// Issue the plan: stream 0 is `s0`; 1..n are the internal copy streams
+// (those of `s0`'s set, or `given` when the caller picked them).
+hocResult_t issue(hocComm* c, const Plan& p, const Bind& bd, cudaStream_t s0, const std::vector<cudaStream_t>* given,
+                  int* max_ctas) {
   std::vector<cudaStream_t> st(p.n_streams);
   st[0] = s0;
   if (p.n_streams > 1) {
     std::vector<cudaStream_t>* copy = nullptr;
-    HOC_TRY(copy_streams_for(c, s0, &copy));
-    for (int i = 1; i < p.n_streams; ++i) st[i] = (*copy)[i - 1];
+    if (given) {
+      if (given->size() < size_t(p.n_streams - 1)) return HOC_ERR_INVALID_ARG;
+    } else {
+      HOC_TRY(copy_streams_for(c, s0, &copy));
+    }
+    for (int i = 1; i < p.n_streams; ++i) st[i] = given ? (*given)[i - 1] : (*copy)[i - 1];
   }
   if (p.n_streams > 1) {
     HOC_CK(cudaEventRecord(c->fork, s0));
@@ -312,8 +318,9 @@ hocResult_t issue(hocComm* c, const Plan& p, const Bind& bd, cudaStream_t s0, in
 
 }  // namespace
 
-hocResult_t issue_plan(hocComm* c, const Plan& p, const Bind& bd, cudaStream_t s0, int* max_ctas) {
-  return issue(c, p, bd, s0, max_ctas);
+hocResult_t issue_plan(hocComm* c, const Plan& p, const Bind& bd, cudaStream_t s0,
+                       const std::vector<cudaStream_t>* copy_streams, int* max_ctas) {
+  return issue(c, p, bd, s0, copy_streams, max_ctas);
 }
 
 hocResult_t get_plan(hocComm* c, const CallShape& shape, const Plan** plan) {
@@ -364,13 +371,13 @@ hocResult_t execute(hocComm* c, const CallShape& shape, const Bind& bd, cudaStre
   const bool worth = p.n_streams > 1 && p.copies + p.kernels >= 8;
   const bool use_graph = c->cfg.use_graphs && !c->profiling && !c->cfg.debug && cs == cudaStreamCaptureStatusNone && worth;
   if (!use_graph) {
-    HOC_TRY(issue(c, p, bd, stream, &max_ctas));
+    HOC_TRY(issue(c, p, bd, stream, nullptr, &max_ctas));
   } else {
     const std::string gkey = graph_key(pkey, bd, p.k);
     auto g = c->graphs.find(gkey);
     if (g == c->graphs.end()) {
       HOC_CK(cudaStreamBeginCapture(c->capture, cudaStreamCaptureModeThreadLocal));
-      hocResult_t r = issue(c, p, bd, c->capture, &max_ctas);
+      hocResult_t r = issue(c, p, bd, c->capture, nullptr, &max_ctas);
       cudaGraph_t graph = nullptr;
       cudaError_t e = cudaStreamEndCapture(c->capture, &graph);
       if (r != HOC_SUCCESS) {

@@ -11,10 +11,17 @@
 // writes FINISH -- on success, on error, or when the deadline passes (the
 // watchdog) -- so the stream is always released.  Slots are reused once the
 // stream has reset end_flag.
+//
+// A stream held at a wait blocks the hardware queue it was mapped to, and
+// every other stream mapped to that queue with it (CUDA maps streams onto a
+// fixed number of queues, CUDA_DEVICE_MAX_CONNECTIONS, in creation order).
+// So before acknowledging, while the caller's stream is known to be held at
+// the start flag, the proxy records a probe event on each of its candidate
+// streams and issues the moves only on streams whose probe completed: a
+// queue that lets an event through while the caller waits is not behind it.
 #include <atomic>
 #include <chrono>
 #include <condition_variable>
-#include <cstdlib>
 #include <cstring>
 #include <thread>
 
@@ -35,6 +42,9 @@ constexpr int kSlots = 16;
 constexpr size_t kFlagBytes = 64;
 constexpr auto kTaskDeadline = std::chrono::seconds(10);
 constexpr auto kShutdownWait = std::chrono::seconds(60);
+constexpr size_t kMaxCandidates = 64;                       // probe streams the proxy may create
+constexpr auto kProbePoll = std::chrono::milliseconds(20);   // wait for probes before adding streams
+constexpr auto kProbeGiveUp = std::chrono::milliseconds(500);
 
 enum SlotState { kFree = 0, kQueued = 1, kRunning = 2, kReleasing = 3 };
 
@@ -68,7 +78,14 @@ struct Proxy {
   void* pinned = nullptr;
   Slot slots[kSlots];
   size_t next = 0;
-  cudaStream_t origin = nullptr;
+  struct Candidate {
+    cudaStream_t s = nullptr;
+    cudaEvent_t probe = nullptr;
+    bool pending = false;  // the last probe has not completed yet
+  };
+  std::vector<Candidate> cand;
+  std::atomic<uint64_t> probes_blocked{0};  // probes found behind a held queue
+  uint64_t n_cand = 0;                       // cand.size(), read under mu by other threads
   MemOpFn write32 = nullptr, wait32 = nullptr;
   std::atomic<uint64_t> completed{0}, released{0};
   std::atomic<int> first_error{0};
@@ -95,7 +112,61 @@ void release(Proxy* P, Slot& s, int err) {
   s.state = kReleasing;
 }
 
-// The stream reached the start flag: acknowledge, plan and issue the moves.
+hocResult_t add_candidate(Proxy* P) {
+  Proxy::Candidate q;
+  if (cudaStreamCreateWithFlags(&q.s, cudaStreamNonBlocking) != cudaSuccess) return HOC_ERR_CUDA;
+  if (cudaEventCreateWithFlags(&q.probe, cudaEventDisableTiming) != cudaSuccess) {
+    cudaStreamDestroy(q.s);
+    return HOC_ERR_CUDA;
+  }
+  P->cand.push_back(q);
+  std::lock_guard<std::mutex> lock(P->mu);
+  P->n_cand = P->cand.size();
+  return HOC_SUCCESS;
+}
+
+// `need` streams whose queues are not held by any waiting stream right now.
+// Called while the caller's stream is held at its start flag.
+hocResult_t pick_streams(Proxy* P, size_t need, std::vector<cudaStream_t>* out) {
+  const auto give_up = std::chrono::steady_clock::now() + kProbeGiveUp;
+  for (;;) {
+    for (auto& q : P->cand)
+      if (!q.pending) {
+        if (cudaEventRecord(q.probe, q.s) != cudaSuccess) return HOC_ERR_CUDA;
+        q.pending = true;
+      }
+    const auto poll_end = std::chrono::steady_clock::now() + kProbePoll;
+    for (;;) {
+      out->clear();
+      for (auto& q : P->cand) {
+        if (q.pending) {
+          const cudaError_t e = cudaEventQuery(q.probe);
+          if (e == cudaSuccess) q.pending = false;
+          else if (e != cudaErrorNotReady) return HOC_ERR_CUDA;
+        }
+        if (!q.pending) out->push_back(q.s);
+      }
+      if (out->size() >= need) {
+        out->resize(need);
+        return HOC_SUCCESS;
+      }
+      if (std::chrono::steady_clock::now() > poll_end) break;
+      std::this_thread::yield();
+    }
+    P->probes_blocked.fetch_add(P->cand.size() - out->size());
+    if (std::chrono::steady_clock::now() > give_up || P->cand.size() >= kMaxCandidates) {
+      set_error_detail("the proxy found no copy streams outside the held hardware queues");
+      return HOC_ERR_UNSUPPORTED;
+    }
+    for (size_t i = out->size(); i < need + 2 && P->cand.size() < kMaxCandidates; ++i) {
+      const hocResult_t r = add_candidate(P);
+      if (r != HOC_SUCCESS) return r;
+    }
+  }
+}
+
+// The stream reached the start flag: pick streams, acknowledge, plan and
+// issue the moves.
 void start_task(Proxy* P, Slot& s) {
   std::atomic_thread_fence(std::memory_order_acquire);
   const int k = P->k;
@@ -103,8 +174,14 @@ void start_task(Proxy* P, Slot& s) {
   for (int a = 0; a < k; ++a)
     for (int b = 0; b < k; ++b)
       cnt[size_t(a) * k + b] = size_t(s.transpose ? s.counts[size_t(b) * k + a] : s.counts[size_t(a) * k + b]);
+  std::vector<cudaStream_t> streams;
+  const hocResult_t picked = pick_streams(P, size_t(P->c->cfg.n_copy) + 1, &streams);
   *s.start = 0;  // acknowledge: the stream moves on to wait for the end flag
   std::atomic_thread_fence(std::memory_order_seq_cst);
+  if (picked != HOC_SUCCESS) {
+    release(P, s, picked);
+    return;
+  }
   {
     std::unique_lock<std::mutex> lock(P->mu);
     if (P->orphaned) {
@@ -148,8 +225,9 @@ void start_task(Proxy* P, Slot& s) {
     const Plan* plan = nullptr;
     r = get_plan(P->c, shape, &plan);
     int mx = 0;
-    if (r == HOC_SUCCESS) r = issue_plan(P->c, *plan, s.bind, P->origin, &mx);
-    if (r == HOC_SUCCESS && cudaEventRecord(s.done, P->origin) != cudaSuccess) r = HOC_ERR_CUDA;
+    const std::vector<cudaStream_t> copy(streams.begin() + 1, streams.end());
+    if (r == HOC_SUCCESS) r = issue_plan(P->c, *plan, s.bind, streams[0], &copy, &mx);
+    if (r == HOC_SUCCESS && cudaEventRecord(s.done, streams[0]) != cudaSuccess) r = HOC_ERR_CUDA;
   }
   if (r != HOC_SUCCESS) {
     release(P, s, r);
@@ -164,7 +242,11 @@ void start_task(Proxy* P, Slot& s) {
 void free_resources(Proxy* P) {
   for (Slot& s : P->slots)
     if (s.done) cudaEventDestroy(s.done);
-  if (P->origin) cudaStreamDestroy(P->origin);
+  for (auto& q : P->cand) {
+    cudaEventDestroy(q.probe);
+    cudaStreamDestroy(q.s);
+  }
+  P->cand.clear();
   if (P->pinned) cudaFreeHost(P->pinned);
 }
 
@@ -224,18 +306,7 @@ void proxy_loop(Proxy* P) {
   }
 }
 
-// While the caller's stream waits on a flag, the copy-engine work the proxy
-// issues must not sit behind that wait in the same hardware queue.  CUDA maps
-// streams onto CUDA_DEVICE_MAX_CONNECTIONS queues (8 unless set before the
-// first CUDA call); with fewer than 16 the proxy refuses to run.
-constexpr int kMinConnections = 16;
-
 hocResult_t proxy_create(hocComm* c, Proxy** out) {
-  const char* conn = getenv("CUDA_DEVICE_MAX_CONNECTIONS");
-  if (!conn || atoi(conn) < kMinConnections) {
-    set_error_detail("the host-proxy handshake needs CUDA_DEVICE_MAX_CONNECTIONS >= 16 set before the first CUDA call");
-    return HOC_ERR_UNSUPPORTED;
-  }
   Proxy* P = new (std::nothrow) Proxy();
   if (!P) return HOC_ERR_OOM;
   P->c = c;
@@ -278,11 +349,13 @@ hocResult_t proxy_create(hocComm* c, Proxy** out) {
     s.d_start = reinterpret_cast<CUdeviceptr>(d);
     s.d_end = reinterpret_cast<CUdeviceptr>(d) + 4;
   }
-  if (cudaStreamCreateWithFlags(&P->origin, cudaStreamNonBlocking) != cudaSuccess) {
-    free_resources(P);
-    delete P;
-    return HOC_ERR_CUDA;
-  }
+  for (int i = 0; i < c->cfg.n_copy + 3; ++i)
+    if (add_candidate(P) != HOC_SUCCESS) {
+      free_resources(P);
+      delete P;
+      set_error_detail("creating the proxy's copy streams failed");
+      return HOC_ERR_CUDA;
+    }
   P->th = std::thread(proxy_loop, P);
   *out = P;
   return HOC_SUCCESS;
@@ -402,5 +475,20 @@ extern "C" hocResult_t hoc_proxy_status(hocComm_t comm, uint64_t* completed, uin
   if (completed) *completed = P ? P->completed.load() : 0;
   if (released_on_error) *released_on_error = P ? P->released.load() : 0;
   if (first_error) *first_error = P ? hocResult_t(P->first_error.exchange(0)) : HOC_SUCCESS;
+  return HOC_SUCCESS;
+}
+
+extern "C" hocResult_t hoc_proxy_queue_stats(hocComm_t comm, uint64_t* candidates, uint64_t* probes_not_clear) {
+  if (!comm) return HOC_ERR_NOT_INITIALIZED;
+  Proxy* P = comm->proxy;
+  if (candidates) {
+    uint64_t n = 0;
+    if (P) {
+      std::lock_guard<std::mutex> lock(P->mu);
+      n = P->n_cand;
+    }
+    *candidates = n;
+  }
+  if (probes_not_clear) *probes_not_clear = P ? P->probes_blocked.load() : 0;
   return HOC_SUCCESS;
 }

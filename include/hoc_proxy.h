@@ -20,14 +20,14 @@
  * hoc_wait() report the error.  The flags live in mapped pinned host memory
  * and the stream operations are cuStreamWriteValue32 / cuStreamWaitValue32.
  *
- * Requirement: while the caller's stream waits on the end flag, the copies the
- * proxy issues must not queue behind that wait in the same hardware work
- * queue.  CUDA spreads streams over CUDA_DEVICE_MAX_CONNECTIONS queues (8 by
- * default); set it to 16 or more (32 is the maximum) in the environment before
- * the process makes its first CUDA call.  Without it the call returns
- * HOC_ERR_UNSUPPORTED.  Should a collision still happen (more streams than
- * queues), the watchdog releases the stream after its deadline and the error
- * is reported; no stream waits forever.
+ * Hardware queues: a stream held at a wait blocks the hardware work queue it
+ * was mapped to, and with it every other stream mapped to that queue (CUDA
+ * maps streams onto CUDA_DEVICE_MAX_CONNECTIONS queues in creation order, so
+ * with many streams alive some always share one).  Before acknowledging a
+ * task, while the caller's stream is held at the start flag, the proxy records
+ * a probe event on each of its own candidate streams and issues the moves only
+ * on streams whose probe completed.  If too few clear within 0.5 s (up to 64
+ * candidates) the task is released with HOC_ERR_UNSUPPORTED and nothing moves.
  */
 #ifndef HOC_PROXY_H
 #define HOC_PROXY_H
@@ -60,6 +60,11 @@ hocResult_t hoc_alltoall_device_counts(hocComm_t comm, const void* const* send, 
  * error, and the first error code seen (then cleared). */
 hocResult_t hoc_proxy_status(hocComm_t comm, uint64_t* completed, uint64_t* released_on_error,
                              hocResult_t* first_error);
+
+/* Stream probing (see "Hardware queues" above): the proxy's candidate streams
+ * so far, and how many probes it found still pending when it picked streams
+ * (each is a candidate skipped because its queue was held or busy). */
+hocResult_t hoc_proxy_queue_stats(hocComm_t comm, uint64_t* candidates, uint64_t* probes_not_clear);
 
 #ifdef __cplusplus
 }

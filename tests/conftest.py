@@ -1,10 +1,6 @@
 import os
 import sys
 
-# The host-proxy handshake needs its copy streams on hardware queues other than
-# the waiting stream's: more queues than the default 8, set before any CUDA call.
-os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
-
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)

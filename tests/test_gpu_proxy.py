@@ -54,6 +54,9 @@ def test_device_count_alltoall_matches_oracle():
             assert np.all(got[lens[d]:] == 0xFFFF)       # nothing written past the received rows
         st = c.proxy_status()
         assert st["completed"] == 1 and st["released_on_error"] == 0
+        qs = c.proxy_queue_stats()
+        assert qs["candidates"] >= 2
+        print("proxy queue stats:", qs)
 
 
 def test_many_tasks_reuse_slots_and_two_streams():
@@ -104,3 +107,29 @@ def test_watchdog_releases_a_stalled_task(monkeypatch):
         assert e.value.code == hoc.ERR_TIMEOUT
         torch.cuda.synchronize()
         assert c.proxy_status()["released_on_error"] == 1
+
+
+def test_callers_on_many_streams():
+    # Torch's stream pool plus the proxy's own streams outnumber the hardware
+    # queues, so some caller streams share a queue with proxy candidates; the
+    # probe must steer the moves off the held queue every time.
+    k, n = 4, 3000
+    rng = np.random.default_rng(17)
+    streams = [torch.cuda.Stream() for _ in range(24)]
+    with hoc.Comm(k, 0) as c:
+        for it, st in enumerate(streams):
+            counts = rng.integers(0, n, size=(k, k))
+            sends = [rng.integers(0, 1 << 31, size=int(counts[s].sum())).astype(np.int32) for s in range(k)]
+            want = o_a2a.alltoallv(sends, counts)
+            with torch.cuda.stream(st):
+                d_counts = torch.from_numpy(counts.astype(np.int64)).cuda()
+                sd = [to_device(x, "int32") if len(x) else torch.zeros(1, dtype=torch.int32, device="cuda") for x in sends]
+                rv = [torch.zeros(max(1, int(counts[:, d].sum())), dtype=torch.int32, device="cuda") for d in range(k)]
+            c.alltoall_device_counts(sd, rv, d_counts, [t.numel() for t in rv], hoc.INT32, stream=st)
+            c.wait(st, timeout_ms=30000)
+            st.synchronize()
+            for d in range(k):
+                assert np.array_equal(to_host(rv[d], "int32")[: len(want[d])], want[d]), (it, d)
+        st = c.proxy_status()
+        assert st["completed"] == len(streams) and st["released_on_error"] == 0
+        print("proxy queue stats:", c.proxy_queue_stats())
