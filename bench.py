@@ -540,12 +540,10 @@ def leg_expert_dispatch(peak):
             c.wait(s, timeout_ms=60000)
             ms = e0.elapsed_time(e1) / 5
             st = c.proxy_status()
-            qs = c.proxy_queue_stats()
         return {
             "ms": round(ms, 4), "host_issue_us": round(statistics.median(host_us), 1),
             "steps": "pack kernels -> dispatch (device counts, host proxy) -> combine exchange -> weighted combine kernel",
-            "proxy_tasks_completed": st["completed"], "proxy_tasks_released_on_error": st["released_on_error"],
-            "proxy_streams": qs["candidates"], "proxy_probes_not_clear": qs["probes_not_clear"]}
+            "proxy_tasks_completed": st["completed"], "proxy_tasks_released_on_error": st["released_on_error"]}
 
     try:
         out["device_round_trip"] = device_round_trip()

@@ -81,8 +81,9 @@ hocResult_t issue_plan(hocComm* c, const Plan& p, const Bind& bd, cudaStream_t s
 void proxy_shutdown(hocComm* c);
 // Free what hoc_allreduce_host set up (staging slots, streams, graphs).
 void host_ar_free(hocComm* c);
-// First error of a proxy task since the last call (0 if none), then cleared.
-int proxy_take_error(hocComm* c);
+// First error of a proxy task since the last call (0 if none) and, in `why`
+// when non-null, what it was; both are then cleared.
+int proxy_take_error(hocComm* c, std::string* why);
 void set_error_detail(const char* what);
 
 }  // namespace hoc

@@ -158,6 +158,19 @@ int grid_for(int items, int per_cta) {
 }
 
 }  // namespace
+
+cudaError_t ep_preload() {
+  const void* fns[] = {reinterpret_cast<const void*>(&ep_count_kernel), reinterpret_cast<const void*>(&ep_place_kernel),
+                       reinterpret_cast<const void*>(&ep_gather_kernel), reinterpret_cast<const void*>(&ep_combine_kernel),
+                       reinterpret_cast<const void*>(&ep_combine_vec_kernel)};
+  for (const void* f : fns) {
+    cudaFuncAttributes a;
+    const cudaError_t e = cudaFuncGetAttributes(&a, f);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 }  // namespace hoc
 
 extern "C" hocResult_t hoc_ep_pack(const int32_t* expert_ids, const void* x, int tokens, int topk, int hidden,

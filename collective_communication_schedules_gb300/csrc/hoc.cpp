@@ -465,6 +465,7 @@ hocResult_t read_cfg(const hocConfig_t* in, int k, Cfg* out) {
     else if (!strcmp(v, "wrong_order")) c.fault = kFaultWrongOrder;
     else if (!strcmp(v, "proxy_stall")) c.fault = kFaultProxyStall;
     else if (!strcmp(v, "tma_stall")) c.fault = kFaultTmaStall;
+    else if (!strcmp(v, "proxy_block")) c.fault = kFaultProxyBlock;
   }
   if (c.order.empty())
     for (int i = 0; i < k; ++i) c.order.push_back(i);
@@ -901,8 +902,9 @@ hocResult_t hoc_wait(hocComm_t comm, void* stream, int timeout_ms) {
       std::this_thread::sleep_for(std::chrono::microseconds(50));
     }
   }
-  if (const int perr = proxy_take_error(comm)) {
-    set_detail("a device-count all-to-all was released by the proxy on an error or its watchdog");
+  std::string why;
+  if (const int perr = proxy_take_error(comm, &why)) {
+    set_detail(("a device-count all-to-all was released by the proxy: " + why).c_str());
     return hocResult_t(perr);
   }
   if (comm->cfg.fault == kFaultProxyStall && !comm->proxy) {

@@ -44,6 +44,16 @@ uint64_t reduce_seg_tiles(int dtype, const ReduceSeg& s, bool wide);
 int reduce_ctas_per_sm(int dtype, int k, int broadcast);
 cudaError_t launch_reduce(const ReduceParams& p, int grid, bool wide, cudaStream_t stream);
 
+// Force-load every kernel of the library (cudaFuncGetAttributes on each).
+// Under lazy module loading the first launch of a kernel loads it, and that
+// load can stall work already queued on other streams until the whole
+// context drains; the host proxy holds a stream at a flag while its moves run,
+// so every kernel that may launch during that window is loaded up front.
+cudaError_t reduce_preload();
+cudaError_t tma_preload();       // TMA copy kernel and TMA-fed reduce kernel
+cudaError_t ep_preload();        // expert-parallel pack and combine kernels
+cudaError_t workload_preload();  // probe and stand-in compute kernels
+
 // TMA-fed variant (reduce_tma.cu): same fold, bulk copies through shared memory.
 uint64_t reduce_tma_seg_tiles(int dtype, const ReduceSeg& s, int k);
 cudaError_t reduce_tma_prepare();  // one-time per device: shared-memory opt-in
@@ -71,6 +81,7 @@ uint64_t tma_job_pieces(const CopyJob& j, uint32_t piece_bytes);
 int tma_ctas_per_sm();
 cudaError_t tma_prepare();  // one-time per device: shared-memory opt-in
 cudaError_t launch_tma_copy(const CopyParams& p, int grid, cudaStream_t stream);
+cudaError_t tma_copy_preload();
 
 // Text for hoc_last_error_detail() (defined with the C ABI).
 void set_error_detail(const char* what);

@@ -45,7 +45,8 @@ enum Fault {
   kFaultDupChunk = 2,
   kFaultWrongOrder = 3,
   kFaultProxyStall = 4,
-  kFaultTmaStall = 5  // the TMA kernel's mbarriers expect bytes that never arrive
+  kFaultTmaStall = 5,   // the TMA kernel's mbarriers expect bytes that never arrive
+  kFaultProxyBlock = 6  // the proxy thread is held up past a task's deadline (host sleep)
 };
 
 enum StepKind { kStepReduce = 0, kStepFused = 1, kStepCopy = 2, kStepTma = 3 };

@@ -6,28 +6,36 @@
 //   copy counts device -> pinned host slot;
 //   write start_flag = START; wait start_flag == 0      (the proxy's ack)
 //   wait end_flag == FINISH; write end_flag = 0          (the proxy's release)
-// The proxy thread polls the start flags of its queued tasks, acknowledges,
-// plans and issues the moves on copy engines, polls their completion event and
-// writes FINISH -- on success, on error, or when the deadline passes (the
-// watchdog) -- so the stream is always released.  Slots are reused once the
-// stream has reset end_flag.
 //
-// A stream held at a wait blocks the hardware queue it was mapped to, and
-// every other stream mapped to that queue with it (CUDA maps streams onto a
-// fixed number of queues, CUDA_DEVICE_MAX_CONNECTIONS, in creation order).
-// So before acknowledging, while the caller's stream is known to be held at
-// the start flag, the proxy records a probe event on each of its candidate
-// streams and issues the moves only on streams whose probe completed: a
-// queue that lets an event through while the caller waits is not behind it.
+// Two host threads serve the slots.  The proxy thread polls the start flags of
+// queued tasks, acknowledges, plans and issues the moves on its own streams,
+// polls their completion event and writes FINISH.  The watchdog thread makes
+// no CUDA call at all: when a task is still unreleased at its deadline it
+// writes the ack and FINISH itself.  So the stream is released even when the
+// proxy thread is stuck inside a driver call that cannot return before the
+// held stream drains -- a kernel's first launch under lazy module loading can
+// wait for the whole context, and a pageable host copy queued behind the held
+// stream blocks its caller until the stream gets past the flags.  Slots are
+// reused once the stream has reset end_flag.
+//
+// Slot states: Free -> Queued (handed to the proxy; the stream has not reached
+// the start flag) -> Starting (start flag seen; planning and issuing) ->
+// Running (moves issued) -> Releasing (FINISH written) -> Free (the stream
+// reset end_flag).  Every transition happens under Proxy::mu; the release
+// writes happen under it too, so exactly one thread releases a task.
 #include <atomic>
 #include <chrono>
 #include <condition_variable>
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
+#include <string>
 #include <thread>
 
 #include <cuda.h>  // CUstream / CUdeviceptr types and memop flags; entry points are resolved at run time
 
 #include "comm.h"
+#include "hoc_internal.h"
 #include "hoc_proxy.h"
 
 namespace hoc {
@@ -35,18 +43,23 @@ namespace hoc {
 namespace {
 
 using MemOpFn = CUresult (*)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+using Clock = std::chrono::steady_clock;
 
 constexpr uint32_t kStartValue = 1;
 constexpr uint32_t kFinishValue = 1;
 constexpr int kSlots = 16;
 constexpr size_t kFlagBytes = 64;
 constexpr auto kTaskDeadline = std::chrono::seconds(10);
+constexpr auto kInjectedDeadline = std::chrono::milliseconds(200);
+constexpr auto kInjectedBlock = std::chrono::milliseconds(1500);
 constexpr auto kShutdownWait = std::chrono::seconds(60);
-constexpr size_t kMaxCandidates = 64;                       // probe streams the proxy may create
-constexpr auto kProbePoll = std::chrono::milliseconds(20);   // wait for probes before adding streams
-constexpr auto kProbeGiveUp = std::chrono::milliseconds(500);
 
-enum SlotState { kFree = 0, kQueued = 1, kRunning = 2, kReleasing = 3 };
+enum SlotState { kFree = 0, kQueued = 1, kStarting = 2, kRunning = 3, kReleasing = 4 };
+
+const char* const kWhyDeadline =
+    "the moves did not finish within 10 s of the stream reaching the start flag; launching a kernel for the first "
+    "time while the stream is held (lazy module loading) or queueing a pageable host copy behind it stalls them: "
+    "load such kernels beforehand (or set CUDA_MODULE_LOADING=EAGER) and keep blocking copies off the held stream";
 
 }  // namespace
 
@@ -62,131 +75,101 @@ struct Slot {
   int transpose = 0;
   cudaEvent_t done = nullptr;
   bool stalled = false;  // host-injected: the moves are never reported complete
-  std::chrono::steady_clock::time_point deadline;
+  uint64_t task = 0;
+  Clock::time_point deadline;
 };
 
 struct Proxy {
   hocComm* c = nullptr;
   int k = 0;
   int device = 0;
+  int fault = 0;  // the communicator's injected fault, copied: the proxy may outlive it
   std::mutex mu;
   std::condition_variable cv;
-  std::thread th;
+  std::thread th;        // the proxy thread
+  std::thread watchdog;  // host memory only
   bool closing = false;
-  bool orphaned = false;   // the communicator is gone: release tasks without moving data
-  bool using_comm = false; // start_task is working with the communicator
+  bool orphaned = false;    // the communicator is gone: release tasks without moving data
+  bool using_comm = false;  // start_task is working with the communicator
+  bool stop_watchdog = false;
   void* pinned = nullptr;
   Slot slots[kSlots];
   size_t next = 0;
-  struct Candidate {
-    cudaStream_t s = nullptr;
-    cudaEvent_t probe = nullptr;
-    bool pending = false;  // the last probe has not completed yet
-  };
-  std::vector<Candidate> cand;
-  std::atomic<uint64_t> probes_blocked{0};  // probes found behind a held queue
-  uint64_t n_cand = 0;                       // cand.size(), read under mu by other threads
+  cudaStream_t origin = nullptr;   // stream 0 of the proxy's plans
+  std::vector<cudaStream_t> copy;  // its copy streams
   MemOpFn write32 = nullptr, wait32 = nullptr;
   std::atomic<uint64_t> completed{0}, released{0};
-  std::atomic<int> first_error{0};
+  int first_error = 0;  // under mu
+  std::string why;      // under mu: what the first error was
+  bool trace = false;   // HOC_PROXY_TRACE=1: one stderr line per task phase
+  uint64_t tasks = 0;
+  Clock::time_point t0 = Clock::now();
 };
 
 namespace {
 
-void note_error(Proxy* P, int err) {
-  int zero = 0;
-  P->first_error.compare_exchange_strong(zero, err);
+void trace(Proxy* P, const Slot& s, const char* what) {
+  if (!P->trace) return;
+  const double ms = std::chrono::duration<double, std::milli>(Clock::now() - P->t0).count();
+  fprintf(stderr, "[hoc proxy %.3f ms] task %llu slot %d: %s\n", ms, (unsigned long long)s.task, int(&s - P->slots),
+          what);
 }
 
-void release(Proxy* P, Slot& s, int err) {
+// Write the release (ack and FINISH) of a task the proxy still holds.  The
+// caller holds P->mu.  Returns false if the task was already released.
+bool release_locked(Proxy* P, Slot& s, int err, const char* why) {
+  if (s.state != kStarting && s.state != kRunning) return false;
   std::atomic_thread_fence(std::memory_order_seq_cst);
-  *s.end = kFinishValue;  // always: the stream is never left waiting
+  *s.start = 0;  // no-op once acknowledged; frees a stream still at the start flag
+  *s.end = kFinishValue;
   std::atomic_thread_fence(std::memory_order_seq_cst);
+  s.state = kReleasing;
   if (err) {
     P->released.fetch_add(1);
-    note_error(P, err);
+    if (!P->first_error) {
+      P->first_error = err;
+      P->why = why ? why : "";
+    }
   } else {
     P->completed.fetch_add(1);
   }
+  return true;
+}
+
+void release(Proxy* P, Slot& s, int err, const char* why) {
   std::lock_guard<std::mutex> lock(P->mu);
-  s.state = kReleasing;
+  release_locked(P, s, err, why);
 }
 
-hocResult_t add_candidate(Proxy* P) {
-  Proxy::Candidate q;
-  if (cudaStreamCreateWithFlags(&q.s, cudaStreamNonBlocking) != cudaSuccess) return HOC_ERR_CUDA;
-  if (cudaEventCreateWithFlags(&q.probe, cudaEventDisableTiming) != cudaSuccess) {
-    cudaStreamDestroy(q.s);
-    return HOC_ERR_CUDA;
-  }
-  P->cand.push_back(q);
-  std::lock_guard<std::mutex> lock(P->mu);
-  P->n_cand = P->cand.size();
-  return HOC_SUCCESS;
-}
-
-// `need` streams whose queues are not held by any waiting stream right now.
-// Called while the caller's stream is held at its start flag.
-hocResult_t pick_streams(Proxy* P, size_t need, std::vector<cudaStream_t>* out) {
-  const auto give_up = std::chrono::steady_clock::now() + kProbeGiveUp;
-  for (;;) {
-    for (auto& q : P->cand)
-      if (!q.pending) {
-        if (cudaEventRecord(q.probe, q.s) != cudaSuccess) return HOC_ERR_CUDA;
-        q.pending = true;
-      }
-    const auto poll_end = std::chrono::steady_clock::now() + kProbePoll;
-    for (;;) {
-      out->clear();
-      for (auto& q : P->cand) {
-        if (q.pending) {
-          const cudaError_t e = cudaEventQuery(q.probe);
-          if (e == cudaSuccess) q.pending = false;
-          else if (e != cudaErrorNotReady) return HOC_ERR_CUDA;
-        }
-        if (!q.pending) out->push_back(q.s);
-      }
-      if (out->size() >= need) {
-        out->resize(need);
-        return HOC_SUCCESS;
-      }
-      if (std::chrono::steady_clock::now() > poll_end) break;
-      std::this_thread::yield();
-    }
-    P->probes_blocked.fetch_add(P->cand.size() - out->size());
-    if (std::chrono::steady_clock::now() > give_up || P->cand.size() >= kMaxCandidates) {
-      set_error_detail("the proxy found no copy streams outside the held hardware queues");
-      return HOC_ERR_UNSUPPORTED;
-    }
-    for (size_t i = out->size(); i < need + 2 && P->cand.size() < kMaxCandidates; ++i) {
-      const hocResult_t r = add_candidate(P);
-      if (r != HOC_SUCCESS) return r;
-    }
-  }
-}
-
-// The stream reached the start flag: pick streams, acknowledge, plan and
-// issue the moves.
+// The stream reached the start flag: acknowledge, plan and issue the moves.
 void start_task(Proxy* P, Slot& s) {
+  bool block = false;
+  {
+    std::lock_guard<std::mutex> lock(P->mu);
+    if (s.state != kQueued) return;
+    s.state = kStarting;
+    s.task = ++P->tasks;
+    block = P->fault == kFaultProxyBlock;
+    const bool injected = P->fault == kFaultProxyStall || block;
+    s.deadline = Clock::now() + (injected ? Clock::duration(kInjectedDeadline) : Clock::duration(kTaskDeadline));
+  }
+  trace(P, s, "start flag seen");
   std::atomic_thread_fence(std::memory_order_acquire);
   const int k = P->k;
   std::vector<size_t> cnt(size_t(k) * k);
   for (int a = 0; a < k; ++a)
     for (int b = 0; b < k; ++b)
       cnt[size_t(a) * k + b] = size_t(s.transpose ? s.counts[size_t(b) * k + a] : s.counts[size_t(a) * k + b]);
-  std::vector<cudaStream_t> streams;
-  const hocResult_t picked = pick_streams(P, size_t(P->c->cfg.n_copy) + 1, &streams);
-  *s.start = 0;  // acknowledge: the stream moves on to wait for the end flag
-  std::atomic_thread_fence(std::memory_order_seq_cst);
-  if (picked != HOC_SUCCESS) {
-    release(P, s, picked);
-    return;
-  }
+  // Injected on the host: the proxy thread is held up past the deadline, as in
+  // a driver call that waits for the held stream; the watchdog must release.
+  if (block) std::this_thread::sleep_for(kInjectedBlock);
   {
-    std::unique_lock<std::mutex> lock(P->mu);
+    std::lock_guard<std::mutex> lock(P->mu);
+    if (s.state != kStarting) return;  // the watchdog released it meanwhile
+    *s.start = 0;                      // acknowledge: the stream moves on to wait for the end flag
+    std::atomic_thread_fence(std::memory_order_seq_cst);
     if (P->orphaned) {
-      lock.unlock();
-      release(P, s, HOC_ERR_NOT_INITIALIZED);
+      release_locked(P, s, HOC_ERR_NOT_INITIALIZED, "the communicator was destroyed before the task started");
       return;
     }
     P->using_comm = true;  // the communicator stays alive until this is cleared
@@ -203,9 +186,17 @@ void start_task(Proxy* P, Slot& s) {
     size_t col = 0;
     for (int a = 0; a < k; ++a) col += cnt[size_t(a) * k + d];
     if (col > s.cap[d]) {
-      release(P, s, HOC_ERR_INVALID_ARG);
+      release(P, s, HOC_ERR_INVALID_ARG, "a receiver's total count exceeds its capacity; nothing was moved");
       return;
     }
+  }
+  if (P->fault == kFaultProxyStall) {  // injected on the host: a completion that never arrives
+    std::lock_guard<std::mutex> lock(P->mu);
+    if (s.state == kStarting) {
+      s.stalled = true;
+      s.state = kRunning;
+    }
+    return;
   }
   CallShape shape;
   shape.op = HOC_OP_ALLTOALL;
@@ -213,41 +204,49 @@ void start_task(Proxy* P, Slot& s) {
   shape.dtype = s.dtype;
   shape.counts = cnt;
   hocResult_t r;
-  if (P->c->cfg.fault == kFaultProxyStall) {  // injected on the host: a completion that never arrives
-    std::lock_guard<std::mutex> lock(P->mu);
-    s.stalled = true;
-    s.deadline = std::chrono::steady_clock::now() + std::chrono::milliseconds(200);
-    s.state = kRunning;
-    return;
-  }
   {
     std::lock_guard<std::mutex> lock(P->c->mu);
     const Plan* plan = nullptr;
     r = get_plan(P->c, shape, &plan);
     int mx = 0;
-    const std::vector<cudaStream_t> copy(streams.begin() + 1, streams.end());
-    if (r == HOC_SUCCESS) r = issue_plan(P->c, *plan, s.bind, streams[0], &copy, &mx);
-    if (r == HOC_SUCCESS && cudaEventRecord(s.done, streams[0]) != cudaSuccess) r = HOC_ERR_CUDA;
+    if (r == HOC_SUCCESS) r = issue_plan(P->c, *plan, s.bind, P->origin, &P->copy, &mx);
+    if (r == HOC_SUCCESS && cudaEventRecord(s.done, P->origin) != cudaSuccess) r = HOC_ERR_CUDA;
   }
   if (r != HOC_SUCCESS) {
-    release(P, s, r);
+    release(P, s, r, "planning or issuing the moves failed");
     return;
   }
+  trace(P, s, "moves issued");
   std::lock_guard<std::mutex> lock(P->mu);
-  s.stalled = false;
-  s.deadline = std::chrono::steady_clock::now() + kTaskDeadline;
-  s.state = kRunning;
+  if (s.state == kStarting) {
+    s.stalled = false;
+    s.state = kRunning;
+  }
 }
 
 void free_resources(Proxy* P) {
   for (Slot& s : P->slots)
     if (s.done) cudaEventDestroy(s.done);
-  for (auto& q : P->cand) {
-    cudaEventDestroy(q.probe);
-    cudaStreamDestroy(q.s);
-  }
-  P->cand.clear();
+  for (cudaStream_t s : P->copy) cudaStreamDestroy(s);
+  P->copy.clear();
+  if (P->origin) cudaStreamDestroy(P->origin);
   if (P->pinned) cudaFreeHost(P->pinned);
+}
+
+void watchdog_loop(Proxy* P) {
+  std::unique_lock<std::mutex> lock(P->mu);
+  while (!P->stop_watchdog) {
+    const auto now = Clock::now();
+    for (Slot& s : P->slots) {
+      if ((s.state != kStarting && s.state != kRunning) || now <= s.deadline) continue;
+      const bool issued = s.state == kRunning;
+      release_locked(P, s, HOC_ERR_TIMEOUT, issued ? kWhyDeadline : "the proxy did not issue the moves before the deadline");
+      if (P->trace)
+        fprintf(stderr, "[hoc proxy] task %llu slot %d: deadline passed, the watchdog released the stream\n",
+                (unsigned long long)s.task, int(&s - P->slots));
+    }
+    P->cv.wait_for(lock, std::chrono::milliseconds(1));
+  }
 }
 
 void proxy_loop(Proxy* P) {
@@ -270,12 +269,11 @@ void proxy_loop(Proxy* P) {
       } else if (st == kRunning) {
         const cudaError_t e = s.stalled ? cudaErrorNotReady : cudaEventQuery(s.done);
         if (e == cudaSuccess) {
-          release(P, s, 0);
+          trace(P, s, "moves complete, releasing");
+          release(P, s, 0, nullptr);
           busy = true;
         } else if (e != cudaErrorNotReady) {
-          release(P, s, HOC_ERR_CUDA);
-        } else if (std::chrono::steady_clock::now() > s.deadline) {
-          release(P, s, HOC_ERR_TIMEOUT);  // watchdog
+          release(P, s, HOC_ERR_CUDA, "querying the completion event of the moves failed");
         }
       } else if (st == kReleasing) {
         if (*s.end == 0) {  // the stream has passed the end flag: slot reusable
@@ -290,11 +288,15 @@ void proxy_loop(Proxy* P) {
     {
       std::lock_guard<std::mutex> lock(P->mu);
       stop = P->closing && all_free;
-      if (stop) P->cv.notify_all();
+      if (stop) {
+        P->stop_watchdog = true;
+        P->cv.notify_all();
+      }
     }
     if (stop) break;
     if (!busy) std::this_thread::sleep_for(std::chrono::microseconds(20));
   }
+  P->watchdog.join();
   bool orphaned;
   {
     std::lock_guard<std::mutex> lock(P->mu);
@@ -306,12 +308,36 @@ void proxy_loop(Proxy* P) {
   }
 }
 
+// Every kernel of the library, loaded once per device before the first task.
+hocResult_t preload_kernels(int device) {
+  static std::mutex mu;
+  static uint64_t loaded = 0;  // bit per device
+  std::lock_guard<std::mutex> lock(mu);
+  const uint64_t bit = device < 64 ? (uint64_t(1) << device) : 0;
+  if (loaded & bit) return HOC_SUCCESS;
+  cudaError_t e = reduce_preload();
+  if (e == cudaSuccess) e = tma_preload();
+  if (e == cudaSuccess) e = ep_preload();
+  if (e == cudaSuccess) e = workload_preload();
+  if (e != cudaSuccess) {
+    set_error_detail("loading the library's kernels before starting the proxy failed");
+    return HOC_ERR_CUDA;
+  }
+  loaded |= bit;
+  return HOC_SUCCESS;
+}
+
 hocResult_t proxy_create(hocComm* c, Proxy** out) {
+  const hocResult_t pre = preload_kernels(c->device);
+  if (pre != HOC_SUCCESS) return pre;
   Proxy* P = new (std::nothrow) Proxy();
   if (!P) return HOC_ERR_OOM;
   P->c = c;
   P->k = c->k;
   P->device = c->device;
+  P->fault = c->cfg.fault;
+  const char* tr = getenv("HOC_PROXY_TRACE");
+  P->trace = tr && atoi(tr) != 0;
   cudaDriverEntryPointQueryResult q;
   void* fw = nullptr;
   void* fv = nullptr;
@@ -340,7 +366,8 @@ hocResult_t proxy_create(hocComm* c, Proxy** out) {
     s.end = reinterpret_cast<volatile uint32_t*>(base + 4);
     s.counts = reinterpret_cast<uint64_t*>(base + kFlagBytes);
     void* d = nullptr;
-    if (cudaHostGetDevicePointer(&d, base, 0) != cudaSuccess || cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming) != cudaSuccess) {
+    if (cudaHostGetDevicePointer(&d, base, 0) != cudaSuccess ||
+        cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming) != cudaSuccess) {
       free_resources(P);
       delete P;
       set_error_detail("mapping the proxy flags failed");
@@ -349,13 +376,19 @@ hocResult_t proxy_create(hocComm* c, Proxy** out) {
     s.d_start = reinterpret_cast<CUdeviceptr>(d);
     s.d_end = reinterpret_cast<CUdeviceptr>(d) + 4;
   }
-  for (int i = 0; i < c->cfg.n_copy + 3; ++i)
-    if (add_candidate(P) != HOC_SUCCESS) {
-      free_resources(P);
-      delete P;
-      set_error_detail("creating the proxy's copy streams failed");
-      return HOC_ERR_CUDA;
-    }
+  bool ok = cudaStreamCreateWithFlags(&P->origin, cudaStreamNonBlocking) == cudaSuccess;
+  for (int i = 0; ok && i < c->cfg.n_copy; ++i) {
+    cudaStream_t s = nullptr;
+    ok = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) == cudaSuccess;
+    if (ok) P->copy.push_back(s);
+  }
+  if (!ok) {
+    free_resources(P);
+    delete P;
+    set_error_detail("creating the proxy's streams failed");
+    return HOC_ERR_CUDA;
+  }
+  P->watchdog = std::thread(watchdog_loop, P);
   P->th = std::thread(proxy_loop, P);
   *out = P;
   return HOC_SUCCESS;
@@ -376,7 +409,7 @@ void proxy_shutdown(hocComm* c) {
   };
   if (P->cv.wait_for(lock, kShutdownWait, all_free)) {
     lock.unlock();
-    P->th.join();
+    P->th.join();  // the proxy thread joins the watchdog before it returns
     free_resources(P);
     delete P;
     return;
@@ -390,7 +423,16 @@ void proxy_shutdown(hocComm* c) {
   P->th.detach();
 }
 
-int proxy_take_error(hocComm* c) { return c->proxy ? c->proxy->first_error.exchange(0) : 0; }
+int proxy_take_error(hocComm* c, std::string* why) {
+  Proxy* P = c->proxy;
+  if (!P) return 0;
+  std::lock_guard<std::mutex> lock(P->mu);
+  const int e = P->first_error;
+  if (why) *why = P->why;
+  P->first_error = 0;
+  P->why.clear();
+  return e;
+}
 
 }  // namespace hoc
 
@@ -474,21 +516,6 @@ extern "C" hocResult_t hoc_proxy_status(hocComm_t comm, uint64_t* completed, uin
   Proxy* P = comm->proxy;
   if (completed) *completed = P ? P->completed.load() : 0;
   if (released_on_error) *released_on_error = P ? P->released.load() : 0;
-  if (first_error) *first_error = P ? hocResult_t(P->first_error.exchange(0)) : HOC_SUCCESS;
-  return HOC_SUCCESS;
-}
-
-extern "C" hocResult_t hoc_proxy_queue_stats(hocComm_t comm, uint64_t* candidates, uint64_t* probes_not_clear) {
-  if (!comm) return HOC_ERR_NOT_INITIALIZED;
-  Proxy* P = comm->proxy;
-  if (candidates) {
-    uint64_t n = 0;
-    if (P) {
-      std::lock_guard<std::mutex> lock(P->mu);
-      n = P->n_cand;
-    }
-    *candidates = n;
-  }
-  if (probes_not_clear) *probes_not_clear = P ? P->probes_blocked.load() : 0;
+  if (first_error) *first_error = hocResult_t(proxy_take_error(comm, nullptr));
   return HOC_SUCCESS;
 }

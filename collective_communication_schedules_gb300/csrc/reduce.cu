@@ -278,6 +278,18 @@ int reduce_ctas_per_sm(int dtype, int k, int /*broadcast*/) {
   return n;
 }
 
+cudaError_t reduce_preload() {
+  const int dtypes[] = {HOC_FLOAT32, HOC_INT32, HOC_BFLOAT16};
+  for (int dt : dtypes)
+    for (int k = 1; k <= kMaxRanks + 1; ++k)  // k outside 2..8 selects the generic-k kernel
+      for (int wide = 0; wide < 2; ++wide) {
+        cudaFuncAttributes a;
+        const cudaError_t e = cudaFuncGetAttributes(&a, kernel_for(dt, k, wide != 0));
+        if (e != cudaSuccess) return e;
+      }
+  return cudaSuccess;
+}
+
 cudaError_t launch_reduce(const ReduceParams& p, int grid, bool wide, cudaStream_t stream) {
   const void* fn = kernel_for(p.dtype, p.k, wide);
   if (!fn) return cudaErrorInvalidValue;

@@ -374,6 +374,12 @@ cudaError_t reduce_tma_prepare() {
                               cudaFuncAttributeMaxDynamicSharedMemorySize, int(most));
 }
 
+cudaError_t tma_preload() {
+  cudaFuncAttributes a;
+  const cudaError_t e = cudaFuncGetAttributes(&a, reinterpret_cast<const void*>(&reduce_tma_kernel));
+  return e != cudaSuccess ? e : tma_copy_preload();
+}
+
 cudaError_t launch_reduce_tma(const ReduceParams& p, int grid, int* status, cudaStream_t stream) {
   if (grid < 1) return cudaSuccess;
   uint32_t tb = reduce_tma_tile_bytes(p.k);

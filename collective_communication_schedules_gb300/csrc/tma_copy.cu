@@ -229,6 +229,11 @@ cudaError_t tma_prepare() {
                               cudaFuncAttributeMaxDynamicSharedMemorySize, int(kStages * kPieceBytes));
 }
 
+cudaError_t tma_copy_preload() {
+  cudaFuncAttributes a;
+  return cudaFuncGetAttributes(&a, reinterpret_cast<const void*>(&tma_copy_kernel));
+}
+
 cudaError_t launch_tma_copy(const CopyParams& p, int grid, cudaStream_t stream) {
   if (grid < 1 || p.njobs < 1) return cudaSuccess;
   if (p.piece_bytes != kPieceBytes) return cudaErrorInvalidValue;

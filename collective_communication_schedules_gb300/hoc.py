@@ -97,7 +97,6 @@ _SIGS["hoc_allreduce_host"] = (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.PO
                                          C.c_int, C.c_int, C.c_void_p])
 _SIGS["hoc_proxy_status"] = (C.c_int, [C.c_void_p, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64),
                                        C.POINTER(C.c_int)])
-_SIGS["hoc_proxy_queue_stats"] = (C.c_int, [C.c_void_p, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64)])
 _SIGS["hoc_topo_schedule"] = (C.c_int, [C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_int), C.POINTER(C.c_uint64),
                                         C.c_uint64, C.c_uint64, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64),
                                         C.POINTER(C.c_double), C.c_int, C.POINTER(C.c_int),
@@ -297,12 +296,6 @@ class Comm:
         err = C.c_int()
         _check(lib().hoc_proxy_status(self._h, C.byref(done), C.byref(rel), C.byref(err)), "hoc_proxy_status")
         return {"completed": done.value, "released_on_error": rel.value, "first_error": err.value}
-
-    def proxy_queue_stats(self) -> dict:
-        cand = C.c_uint64()
-        blocked = C.c_uint64()
-        _check(lib().hoc_proxy_queue_stats(self._h, C.byref(cand), C.byref(blocked)), "hoc_proxy_queue_stats")
-        return {"candidates": cand.value, "probes_not_clear": blocked.value}
 
     # ------------------------------------------------------------- control
     def wait(self, stream=None, timeout_ms: int = 60000):

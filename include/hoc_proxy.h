@@ -20,14 +20,18 @@
  * hoc_wait() report the error.  The flags live in mapped pinned host memory
  * and the stream operations are cuStreamWriteValue32 / cuStreamWaitValue32.
  *
- * Hardware queues: a stream held at a wait blocks the hardware work queue it
- * was mapped to, and with it every other stream mapped to that queue (CUDA
- * maps streams onto CUDA_DEVICE_MAX_CONNECTIONS queues in creation order, so
- * with many streams alive some always share one).  Before acknowledging a
- * task, while the caller's stream is held at the start flag, the proxy records
- * a probe event on each of its own candidate streams and issues the moves only
- * on streams whose probe completed.  If too few clear within 0.5 s (up to 64
- * candidates) the task is released with HOC_ERR_UNSUPPORTED and nothing moves.
+ * Held-stream window: from the start flag to the end flag the caller's
+ * stream is held, and the moves must run meanwhile.  Two things stall them
+ * until the stream is released: launching a kernel for the first time under
+ * lazy module loading (CUDA_MODULE_LOADING=LAZY, the default; the load can
+ * wait for the whole context, the held stream included), and a pageable host
+ * copy queued behind the held stream.  The library loads all of its own
+ * kernels before the proxy starts; load other kernels that run during the
+ * window beforehand (one warm-up launch, or CUDA_MODULE_LOADING=EAGER) and
+ * keep blocking host copies off the held stream.  Should a stall happen
+ * anyway, the proxy's watchdog -- a host thread that makes no CUDA call --
+ * releases the stream after 10 s and the call reports HOC_ERR_TIMEOUT with the
+ * reason; no stream is left waiting and no thread deadlocks.
  */
 #ifndef HOC_PROXY_H
 #define HOC_PROXY_H
@@ -60,11 +64,6 @@ hocResult_t hoc_alltoall_device_counts(hocComm_t comm, const void* const* send, 
  * error, and the first error code seen (then cleared). */
 hocResult_t hoc_proxy_status(hocComm_t comm, uint64_t* completed, uint64_t* released_on_error,
                              hocResult_t* first_error);
-
-/* Stream probing (see "Hardware queues" above): the proxy's candidate streams
- * so far, and how many probes it found still pending when it picked streams
- * (each is a candidate skipped because its queue was held or busy). */
-hocResult_t hoc_proxy_queue_stats(hocComm_t comm, uint64_t* candidates, uint64_t* probes_not_clear);
 
 #ifdef __cplusplus
 }

@@ -91,6 +91,7 @@ def test_dispatch_combine_round_trip_without_host_sync():
                 d_counts[r].copy_(cnt)
                 d_send.append(send.view(-1))
                 d_pos.append(pos_of)
+            w_dev = [torch.from_numpy(ws[r]).cuda() for r in range(k)]   # no pageable copy while the stream is held
             cap = [int(counts[:, d].sum()) + 4096 for d in range(k)]
             d_recv = [torch.empty(cap[d], dtype=torch.bfloat16, device="cuda") for d in range(k)]
             d_back = [torch.empty_like(t) for t in d_send]
@@ -101,7 +102,7 @@ def test_dispatch_combine_round_trip_without_host_sync():
         with torch.cuda.stream(s):
             for r in range(k):
                 y = torch.empty((tokens, hidden), dtype=torch.bfloat16, device="cuda")
-                hoc.ep_combine(d_back[r], d_pos[r], torch.from_numpy(ws[r]).cuda(), tokens, topk, hidden, y, stream=s)
+                hoc.ep_combine(d_back[r], d_pos[r], w_dev[r], tokens, topk, hidden, y, stream=s)
                 ys.append(y)
         c.wait(s, timeout_ms=60000)
         for r in range(k):
