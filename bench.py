@@ -717,18 +717,26 @@ def run_ours(args, world, rank, local):
                 if peak_kind == "measured" else "fallback 6.8 TB/s"}
 
     # ---- end to end: pinned host inputs -> device, allreduce, results -> host
-    # End to end through the host-buffer call: every step copies the 2 GiB of
-    # inputs in from pinned host memory and the 2 GiB of results out, with
-    # the copies pipelined against the reduce inside hoc_allreduce_host.
-    comm.allreduce_host(h_send, h_recv, stream=stream)          # untimed: first touch, graph capture
-    torch.cuda.synchronize()
+    # End to end through the host-buffer call: every step brings the 2 GiB of
+    # inputs in from pinned host memory and the 2 GiB of results out.  With
+    # path AUTO the call runs directly on the host buffers (one fused launch
+    # whose loads and stores cross the host link); the staged copy-engine
+    # pipeline (path CE) is timed beside it.
+    def time_host(c):
+        c.allreduce_host(h_send, h_recv, stream=stream)         # untimed: first touch, graph capture
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            c.allreduce_host(h_send, h_recv, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.e2e_steps, c.last_stats()
+    e2e_ms, e2e_st = time_host(comm)
+    e2e_ms = max_over_ranks(world, e2e_ms, dev)
+    with hoc.Comm(k, local, hoc.Config(path="ce")) as c_ce:
+        staged_ms, staged_st = time_host(c_ce)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        comm.allreduce_host(h_send, h_recv, stream=stream)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1) / args.e2e_steps, dev)
     # the same step done the plain way: all inputs in, allreduce, all results out
     e0.record(stream)
     with torch.cuda.stream(stream):
@@ -741,9 +749,12 @@ def run_ours(args, world, rank, local):
     e1.record(stream)
     torch.cuda.synchronize()
     plain_ms = e0.elapsed_time(e1) / args.e2e_steps
+    mode = "direct: one fused launch on the pinned host buffers" if e2e_st["copies"] == 0 else \
+        "staged: copy-engine pipeline through device slots"
     e2e = {"value": round(world * bus_bytes(k, per_rank) / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
            "h2d_bytes_per_step": k * per_rank, "d2h_bytes_per_step": k * per_rank, "ms_per_step": round(e2e_ms, 3),
-           "call": "hoc_allreduce_host (pinned host buffers, copies pipelined with the reduce)",
+           "call": f"hoc_allreduce_host, path {args.path} ({mode})",
+           "staged_ce_ms_per_step": round(staged_ms, 3), "staged_ce_copies_per_step": staged_st["copies"],
            "unpipelined_ms_per_step": round(plain_ms, 3)}
 
     extras = {}

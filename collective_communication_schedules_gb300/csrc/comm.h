@@ -77,6 +77,10 @@ hocResult_t get_plan(hocComm* c, const CallShape& shape, const Plan** plan);
 // when that is null.
 hocResult_t issue_plan(hocComm* c, const Plan& p, const Bind& bd, cudaStream_t s0,
                        const std::vector<cudaStream_t>* copy_streams, int* max_ctas);
+// One fused allreduce launch on the given rank buffers, whatever the
+// communicator's path (the buffers may be any memory the device can address).
+hocResult_t allreduce_fused(hocComm* c, const void* const* send, void* const* recv, size_t count, int dtype,
+                            cudaStream_t stream);
 // Release the proxy (waits, bounded, for its tasks; see proxy.cpp).
 void proxy_shutdown(hocComm* c);
 // Free what hoc_allreduce_host set up (staging slots, streams, graphs).

@@ -597,7 +597,43 @@ hocResult_t run(hocComm* c, const CallShape& shape, const Bind& bd, void* stream
   return execute(c, shape, bd, static_cast<cudaStream_t>(stream));
 }
 
+// hoc_allreduce with the plan's path set by `path` (-1: the communicator's).
+hocResult_t allreduce_on(hocComm_t comm, const void* const* send, void* const* recv, size_t count,
+                         hocDataType_t dtype, hocRedOp_t op, void* stream, int path) {
+  HOC_TRY(check_reduce_args(comm, dtype, op));
+  if (count == 0) return HOC_SUCCESS;
+  const int k = comm->k;
+  const size_t b = dtype_bytes(dtype);
+  HOC_TRY(check_array(send, k, b));
+  HOC_TRY(check_array(const_cast<const void* const*>(reinterpret_cast<void* const*>(recv)), k, b));
+  std::vector<Range> rs;
+  for (int r = 0; r < k; ++r) {
+    rs.push_back(Range{U(send[r]), U(send[r]) + count * b, false, r});
+    rs.push_back(Range{U(recv[r]), U(recv[r]) + count * b, true, r});
+  }
+  HOC_TRY(check_overlaps(rs, [](const Range& a, const Range& b2) {
+    return a.rank == b2.rank && a.writable != b2.writable && a.lo == b2.lo;  // in place: send[r] == recv[r]
+  }));
+  CallShape s;
+  s.op = HOC_OP_ALLREDUCE;
+  s.k = k;
+  s.dtype = dtype;
+  s.count = count;
+  s.path = path;
+  Bind bd;
+  for (int r = 0; r < k; ++r) {
+    bd.send[r] = send[r];
+    bd.recv[r] = recv[r];
+  }
+  return run(comm, s, bd, stream);
+}
 }  // namespace
+
+hocResult_t allreduce_fused(hocComm* comm, const void* const* send, void* const* recv, size_t count, int dtype,
+                            cudaStream_t stream) {
+  return allreduce_on(comm, send, recv, count, hocDataType_t(dtype), HOC_SUM, stream, HOC_PATH_FUSED);
+}
+
 }  // namespace hoc
 
 using namespace hoc;
@@ -698,31 +734,7 @@ hocResult_t hoc_destroy(hocComm_t comm) {
 
 hocResult_t hoc_allreduce(hocComm_t comm, const void* const* send, void* const* recv, size_t count,
                           hocDataType_t dtype, hocRedOp_t op, void* stream) {
-  HOC_TRY(check_reduce_args(comm, dtype, op));
-  if (count == 0) return HOC_SUCCESS;
-  const int k = comm->k;
-  const size_t b = dtype_bytes(dtype);
-  HOC_TRY(check_array(send, k, b));
-  HOC_TRY(check_array(const_cast<const void* const*>(reinterpret_cast<void* const*>(recv)), k, b));
-  std::vector<Range> rs;
-  for (int r = 0; r < k; ++r) {
-    rs.push_back(Range{U(send[r]), U(send[r]) + count * b, false, r});
-    rs.push_back(Range{U(recv[r]), U(recv[r]) + count * b, true, r});
-  }
-  HOC_TRY(check_overlaps(rs, [](const Range& a, const Range& b2) {
-    return a.rank == b2.rank && a.writable != b2.writable && a.lo == b2.lo;  // in place: send[r] == recv[r]
-  }));
-  CallShape s;
-  s.op = HOC_OP_ALLREDUCE;
-  s.k = k;
-  s.dtype = dtype;
-  s.count = count;
-  Bind bd;
-  for (int r = 0; r < k; ++r) {
-    bd.send[r] = send[r];
-    bd.recv[r] = recv[r];
-  }
-  return run(comm, s, bd, stream);
+  return allreduce_on(comm, send, recv, count, dtype, op, stream, -1);
 }
 
 hocResult_t hoc_reduce_scatter(hocComm_t comm, const void* const* send, void* const* recv, size_t recvcount,

@@ -1,5 +1,14 @@
-// AllReduce over host buffers: the k-way reduce pipelined with the copies
-// that bring the inputs in and the results out.
+// AllReduce over host buffers.
+//
+// Direct mode (path AUTO or FUSED, when the device can address every host
+// buffer: pinned memory, or any memory over a coherent host link with
+// pageable access such as Grace's NVLink-C2C): one fused reduce launch loads
+// the k inputs from host memory and stores the k results there -- the same
+// kernel, fold and bits as the device allreduce, and no staging.
+//
+// Staged mode (path CE or TMA, or host buffers the device cannot address):
+// the k-way reduce pipelined with copy-engine copies that bring the inputs in
+// and the results out.
 //
 // The element range is cut into chunks.  Chunk q runs three steps on three
 // internal streams: the host->device copies of the k input chunks into a
@@ -21,6 +30,29 @@ namespace hoc {
 namespace {
 
 constexpr size_t kHostChunkBytes = size_t(8) << 20;  // per rank and chunk
+
+// The address under which the device loads and stores host buffer `p`, if it
+// has one: registered (pinned) memory, device or managed memory, or pageable
+// memory when the device can access pageable memory.
+bool device_view(const void* p, bool pageable_ok, const void** out) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  switch (a.type) {
+    case cudaMemoryTypeHost:
+      if (!a.devicePointer) return false;
+      *out = a.devicePointer;
+      return true;
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged: *out = p; return true;
+    default:
+      if (!pageable_ok) return false;
+      *out = p;
+      return true;
+  }
+}
 constexpr int kEventRing = 4;
 
 struct HostArState {
@@ -195,7 +227,6 @@ extern "C" hocResult_t hoc_allreduce_host(hocComm_t comm, const void* const* h_s
       }
     }
   }
-  std::lock_guard<std::mutex> lock(comm->mu);
   int prev = -1;
   cudaGetDevice(&prev);
   if (prev != comm->device) cudaSetDevice(comm->device);
@@ -205,6 +236,23 @@ extern "C" hocResult_t hoc_allreduce_host(hocComm_t comm, const void* const* h_s
       if (p >= 0 && p != d) cudaSetDevice(p);
     }
   } restore{prev, comm->device};
+  const int path = comm->cfg.path;
+  if (path == HOC_PATH_AUTO || path == HOC_PATH_FUSED) {
+    int pageable = 0;
+    cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, comm->device);
+    std::vector<const void*> ds(k), dr(k);
+    std::vector<void*> drw(k);
+    bool direct = true;
+    for (int r = 0; r < k && direct; ++r)
+      direct = device_view(h_send[r], pageable != 0, &ds[r]) && device_view(h_recv[r], pageable != 0, &dr[r]);
+    for (int r = 0; r < k && direct; ++r) drw[r] = const_cast<void*>(dr[r]);
+    if (direct) return allreduce_fused(comm, ds.data(), drw.data(), count, dtype, static_cast<cudaStream_t>(stream));
+    if (path == HOC_PATH_FUSED) {
+      set_error_detail("the FUSED host allreduce needs host buffers the device can address (pinned, or pageable memory on a device with pageable access)");
+      return HOC_ERR_UNSUPPORTED;
+    }
+  }
+  std::lock_guard<std::mutex> lock(comm->mu);
   HostArState* st = nullptr;
   hocResult_t r0 = ensure_state(comm, &st);
   if (r0 != HOC_SUCCESS) return r0;

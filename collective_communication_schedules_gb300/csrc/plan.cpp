@@ -69,6 +69,7 @@ std::string plan_key(const CallShape& s) {
   put(&s.count, sizeof s.count);
   put(&s.src_rank, sizeof s.src_rank);
   put(&s.dst_rank, sizeof s.dst_rank);
+  put(&s.path, sizeof s.path);
   const size_t nc = s.counts.size();
   put(&nc, sizeof nc);
   if (nc) put(s.counts.data(), nc * sizeof(size_t));
@@ -360,7 +361,8 @@ hocResult_t build_plan(const Cfg& cfg, const CallShape& s, Plan* p) {
   switch (s.op) {
     case HOC_OP_ALLREDUCE:
       if (s.dtype == HOC_UINT8) return HOC_ERR_UNSUPPORTED;
-      p->path = cfg.path == HOC_PATH_AUTO ? HOC_PATH_FUSED : cfg.path;
+      p->path = s.path >= 0 ? s.path : (cfg.path == HOC_PATH_AUTO ? HOC_PATH_FUSED : cfg.path);
+      if (p->path < HOC_PATH_CE || p->path > HOC_PATH_FUSED) return HOC_ERR_INVALID_ARG;
       r = plan_allreduce(cfg, s, p);
       break;
     case HOC_OP_REDUCE_SCATTER:

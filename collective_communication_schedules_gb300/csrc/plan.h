@@ -84,6 +84,7 @@ struct CallShape {
   std::vector<size_t> counts;  // alltoall: k*k sendcounts (elements); empty = uniform
   std::vector<size_t> sdispls, rdispls;
   int src_rank = 0, dst_rank = 0;  // sendrecv
+  int path = -1;                   // allreduce: path override (-1: the communicator's)
 };
 
 size_t dtype_bytes(int dtype);

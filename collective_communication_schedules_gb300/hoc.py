@@ -244,7 +244,8 @@ class Comm:
                                    _stream(stream)), "hoc_allreduce")
 
     def allreduce_host(self, h_send, h_recv, count=None, dtype=None, stream=None):
-        """AllReduce of host (CPU) tensors, pipelined with the host<->device copies."""
+        """AllReduce of host (CPU) tensors: one fused launch on host memory the GPU can address (path AUTO/FUSED),
+        else the copy-engine pipeline through device staging slots (path CE/TMA)."""
         count = h_send[0].numel() if count is None else count
         dtype = _dtype_code(h_send[0]) if dtype is None else dtype
         ptrs = lambda xs: (C.c_void_p * len(xs))(*[x if isinstance(x, int) else x.data_ptr() for x in xs])

@@ -130,16 +130,22 @@ hocResult_t hoc_destroy(hocComm_t comm);
 hocResult_t hoc_allreduce(hocComm_t comm, const void* const* send, void* const* recv, size_t count,
                           hocDataType_t dtype, hocRedOp_t op, void* stream);
 
-/* AllReduce over HOST buffers: h_send[r], h_recv[r] are host pointers (pinned
- * memory gives the copy engines full speed; pageable memory works, slower).
- * Same fold and bits as hoc_allreduce.  The element range is cut into 8 MiB
- * chunks per rank; the host->device copies of chunk q+1, the reduce of chunk
- * q and the device->host copies of chunk q-1 overlap (both copy directions and
- * the SMs at once), through two device staging slots the communicator
- * allocates on first use.  Stream-ordered like every call; in place:
- * h_send[r] == h_recv[r].  Calls that run at the same time on the GPU (on
- * different streams without ordering between them) share those staging
- * slots and race. */
+/* AllReduce over HOST buffers: h_send[r], h_recv[r] are host pointers.  Same
+ * fold and bits as hoc_allreduce.  Two modes:
+ *  - direct (cfg.path AUTO or FUSED, when the device can address every buffer:
+ *    pinned memory, or pageable memory on a device with pageable memory access
+ *    such as a Grace-attached GPU): one fused reduce launch loads the inputs
+ *    from host memory and stores the results there; no staging, no copies.
+ *    With cfg.path FUSED and a buffer the device cannot address, the call
+ *    returns HOC_ERR_UNSUPPORTED.
+ *  - staged (cfg.path CE or TMA, or AUTO with a buffer the device cannot
+ *    address): the element range is cut into 8 MiB chunks per rank; the
+ *    host->device copies of chunk q+1, the reduce of chunk q and the
+ *    device->host copies of chunk q-1 overlap on copy engines and SMs, through
+ *    two device staging slots the communicator allocates on first use.  Calls
+ *    that run at the same time on the GPU (different streams without ordering
+ *    between them) share those slots and race.
+ * Stream-ordered like every call; in place: h_send[r] == h_recv[r]. */
 hocResult_t hoc_allreduce_host(hocComm_t comm, const void* const* h_send, void* const* h_recv, size_t count,
                                hocDataType_t dtype, hocRedOp_t op, void* stream);
 

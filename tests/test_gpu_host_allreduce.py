@@ -1,4 +1,5 @@
-"""AllReduce over host buffers (copies pipelined with the reduce) against the oracle."""
+"""AllReduce over host buffers against the oracle, in both modes: direct (one fused launch on host memory the
+device addresses) and staged (copy-engine pipeline through device slots)."""
 import numpy as np
 import pytest
 import torch
@@ -23,10 +24,11 @@ def _bits(t, dtype):
 @pytest.mark.parametrize("dtype", ["int32", "float32", "bfloat16"])
 @pytest.mark.parametrize("k", [1, 3, 8])
 @pytest.mark.parametrize("pinned", [True, False])
-def test_host_allreduce_matches_oracle(dtype, k, pinned):
+@pytest.mark.parametrize("path", ["auto", "ce"])
+def test_host_allreduce_matches_oracle(dtype, k, pinned, path):
     rng = np.random.default_rng(k)
     order = list(rng.permutation(k))
-    with hoc.Comm(k, 0, hoc.Config(ring_order=order)) as c:
+    with hoc.Comm(k, 0, hoc.Config(ring_order=order, path=path)) as c:
         for n in (1, 4099, 5_000_003):                   # several 8 MiB chunks and a ragged tail
             xs = inputs.rank_inputs(dtype, k, n, workload=7, slot=(n + k) % 50)
             want = o_ring.allreduce(xs, dtype, order)
@@ -40,6 +42,11 @@ def test_host_allreduce_matches_oracle(dtype, k, pinned):
                 c.allreduce_host(hs, hr)
                 c.wait()
                 torch.cuda.synchronize()
+                st = c.last_stats()
+                if path == "ce":
+                    assert st["copies"] > 0                # staged through the copy engines
+                elif pinned:
+                    assert st["path"] == hoc.PATH_FUSED and st["copies"] == 0 and st["kernels"] == 1   # direct
                 for r in range(k):
                     w = want[r].view(np.uint32) if want[r].dtype in (np.float32, np.int32) else want[r]
                     got = _bits(hr[r], dtype)
