@@ -161,8 +161,8 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def recorded_traffic(kernel: str):
-    """DRAM bytes per launch from a committed ncu summary, if it matches today's kernel source."""
+def recorded_traffic(kernel: str, k: int, count: int):
+    """DRAM bytes per launch from a committed ncu summary, if it matches today's kernel source and workload."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
@@ -170,7 +170,7 @@ def recorded_traffic(kernel: str):
     except (OSError, ValueError):
         return None
     e = d.get(kernel)
-    if not e:
+    if not e or e.get("k") != k or e.get("count") != count:
         return None
     src = os.path.join(ROOT, "collective_communication_schedules_gb300", "csrc", e.get("source", "reduce.cu"))
     try:
@@ -711,7 +711,7 @@ def run_ours(args, world, rank, local):
     achieved = kern_bytes / (avg_launch_ms * 1e-3) / 1e9 if launches else None
     roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1) if achieved else None,
                 "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4) if achieved else None,
-                "traffic": recorded_traffic(kname), "bytes_per_launch": kern_bytes,
+                "traffic": recorded_traffic(kname, k, n_el), "bytes_per_launch": kern_bytes,
                 "avg_launch_ms": round(avg_launch_ms, 4), "launches": launches,
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s"}
