@@ -897,7 +897,10 @@ hocResult_t hoc_wait(hocComm_t comm, void* stream, int timeout_ms) {
   DeviceGuard g(comm->device);
   const auto deadline = std::chrono::steady_clock::now() + std::chrono::milliseconds(timeout_ms < 0 ? 0 : timeout_ms);
   std::vector<cudaStream_t> all;
-  for (auto& set : comm->sets) all.insert(all.end(), set.copy.begin(), set.copy.end());
+  {
+    std::lock_guard<std::mutex> lock(comm->mu);  // another thread's call may add a stream set
+    for (auto& set : comm->sets) all.insert(all.end(), set.copy.begin(), set.copy.end());
+  }
   all.push_back(static_cast<cudaStream_t>(stream));
   for (cudaStream_t s : all) {
     for (;;) {

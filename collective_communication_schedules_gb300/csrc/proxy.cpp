@@ -286,15 +286,18 @@ void proxy_loop(Proxy* P) {
     }
     bool stop;
     {
-      std::lock_guard<std::mutex> lock(P->mu);
+      std::unique_lock<std::mutex> lock(P->mu);
       stop = P->closing && all_free;
       if (stop) {
         P->stop_watchdog = true;
         P->cv.notify_all();
+      } else if (all_free) {
+        // idle: sleep until a task is queued (or shutdown), re-checking every ms
+        P->cv.wait_for(lock, std::chrono::milliseconds(1));
       }
     }
     if (stop) break;
-    if (!busy) std::this_thread::sleep_for(std::chrono::microseconds(20));
+    if (!busy && !all_free) std::this_thread::yield();  // tasks in flight: poll their flags closely
   }
   P->watchdog.join();
   bool orphaned;
@@ -490,6 +493,7 @@ extern "C" hocResult_t hoc_alltoall_device_counts(hocComm_t comm, const void* co
     slot->transpose = transpose != 0;
     slot->cap.assign(recv_capacity, recv_capacity + k);
     slot->state = kQueued;
+    P->cv.notify_all();  // wake an idle proxy thread
   }
   const size_t counts_bytes = size_t(k) * k * sizeof(uint64_t);
   if (cudaMemcpyAsync(slot->counts, d_sendcounts, counts_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
