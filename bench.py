@@ -491,11 +491,22 @@ def leg_expert_dispatch(peak):
             torch.cuda.synchronize()
             ms = e0.elapsed_time(e1) / 5
             st = c.last_stats()
+            # tail of the dispatch: when each copy stream finished, from the fork
+            c.profile_enable(True)
+            c.alltoall(send, recv, sendcounts=ecounts, dtype=hoc.BFLOAT16)
+            fin = c.profile_stream_finish()
+            c.profile_enable(False)
+            torch.cuda.synchronize()
+            tail = {}
+            if fin:
+                tail = {"stream_finish_ms": [round(v, 4) for v in fin],
+                        "finish_spread_ms": round(max(fin) - min(fin), 4),
+                        "last_over_mean": round(max(fin) / (sum(fin) / len(fin)), 3)}
             out[f"{path}{'' if inter else '_fifo'}"] = {
                 "dispatch_plus_combine_ms": round(ms, 4),
                 "algbw_gbs": round(2 * moved / (ms * 1e-3) / 1e9, 1),
                 "hbm_frac": round(2 * st["bytes_exec"] / (ms * 1e-3) / (peak * 1e9), 4),
-                "sms_used": st["sms_used"], "copies_per_call": st["copies"]}
+                "sms_used": st["sms_used"], "copies_per_call": st["copies"], "dispatch_tail": tail}
     ok = all(torch.equal(a.view(torch.int16), b.view(torch.int16)) for a, b in zip(send, back))
     out["combine_restores_dispatch_input"] = bool(ok)
 
@@ -539,9 +550,25 @@ def leg_expert_dispatch(peak):
             e1.record(s)
             c.wait(s, timeout_ms=60000)
             ms = e0.elapsed_time(e1) / 5
+            # one more round with an event between its phases (all on stream s)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            ev[0].record(s)
+            for r in range(k):
+                hoc.ep_pack(ids[r], xs[r], experts, k, psend[r], perm[r], pos[r], d_counts[r], wsp[r], stream=s)
+            ev[1].record(s)
+            c.alltoall_device_counts([t.view(-1) for t in psend], precv, d_counts, cap, hoc.BFLOAT16, stream=s)
+            ev[2].record(s)
+            c.alltoall_device_counts(precv, pback, d_counts, [n * h] * k, hoc.BFLOAT16, stream=s, transpose=True)
+            ev[3].record(s)
+            for r in range(k):
+                hoc.ep_combine(pback[r], pos[r], gate[r], tokens, topk, h, ys[r], stream=s)
+            ev[4].record(s)
+            c.wait(s, timeout_ms=60000)
+            phases = {name: round(ev[i].elapsed_time(ev[i + 1]), 4) for i, name in
+                      enumerate(("pack_ms", "dispatch_ms", "combine_exchange_ms", "combine_kernel_ms"))}
             st = c.proxy_status()
         return {
-            "ms": round(ms, 4), "host_issue_us": round(statistics.median(host_us), 1),
+            "ms": round(ms, 4), "host_issue_us": round(statistics.median(host_us), 1), "phases": phases,
             "steps": "pack kernels -> dispatch (device counts, host proxy) -> combine exchange -> weighted combine kernel",
             "proxy_tasks_completed": st["completed"], "proxy_tasks_released_on_error": st["released_on_error"]}
 

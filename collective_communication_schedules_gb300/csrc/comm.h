@@ -63,6 +63,11 @@ struct hocComm {
   std::vector<cudaEvent_t> prof_free;
   int prof_launches[3] = {0, 0, 0};
   double prof_ms[3] = {0, 0, 0};
+  // While profiling: timing events at the fork of the last multi-stream call
+  // and after the last operation of each of its copy streams.
+  cudaEvent_t prof_fork = nullptr;
+  std::vector<cudaEvent_t> prof_stream_end;
+  int prof_streams = 0;  // copy streams the last profiled call used (0: none)
   int reduce_ctas_per_sm[3][hoc::kMaxRanks + 1][2] = {};
   hoc::Proxy* proxy = nullptr;  // created by the first device-count all-to-all
   void* host_ar = nullptr;      // staging and streams of hoc_allreduce_host (host_ar.cpp)

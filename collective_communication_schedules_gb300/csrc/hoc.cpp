@@ -276,6 +276,17 @@ hocResult_t issue(hocComm* c, const Plan& p, const Bind& bd, cudaStream_t s0, co
     }
     for (int i = 1; i < p.n_streams; ++i) st[i] = given ? (*given)[i - 1] : (*copy)[i - 1];
   }
+  const bool prof_streams = c->profiling && p.n_streams > 1;
+  if (c->profiling) c->prof_streams = 0;
+  if (prof_streams) {
+    if (!c->prof_fork) HOC_CK(cudaEventCreate(&c->prof_fork));
+    while (c->prof_stream_end.size() < size_t(p.n_streams)) {
+      cudaEvent_t e;
+      HOC_CK(cudaEventCreate(&e));
+      c->prof_stream_end.push_back(e);
+    }
+    HOC_CK(cudaEventRecord(c->prof_fork, s0));
+  }
   if (p.n_streams > 1) {
     HOC_CK(cudaEventRecord(c->fork, s0));
     for (int i = 1; i < p.n_streams; ++i) HOC_CK(cudaStreamWaitEvent(st[i], c->fork, 0));
@@ -305,6 +316,10 @@ hocResult_t issue(hocComm* c, const Plan& p, const Bind& bd, cudaStream_t s0, co
       default: return HOC_ERR_INVALID_ARG;
     }
     if (step.record) HOC_CK(cudaEventRecord(c->ev[i], s));
+  }
+  if (prof_streams) {
+    for (int i = 1; i < p.n_streams; ++i) HOC_CK(cudaEventRecord(c->prof_stream_end[i - 1], st[i]));
+    c->prof_streams = p.n_streams - 1;
   }
   if (p.n_streams > 1) {
     HOC_TRY(get_event(c, c->join, size_t(p.n_streams)));
@@ -500,6 +515,8 @@ void free_comm(hocComm* c) {
     cudaEventDestroy(pp.stop);
   }
   if (c->fork) cudaEventDestroy(c->fork);
+  if (c->prof_fork) cudaEventDestroy(c->prof_fork);
+  for (cudaEvent_t e : c->prof_stream_end) cudaEventDestroy(e);
   for (auto& set : c->sets)
     for (cudaStream_t s : set.copy) cudaStreamDestroy(s);
   if (c->capture) cudaStreamDestroy(c->capture);
@@ -974,6 +991,19 @@ hocResult_t hoc_profile_read(hocComm_t comm, hocKernel_t kernel, int* launches, 
   *total_ms = comm->prof_ms[kernel];
   comm->prof_launches[kernel] = 0;
   comm->prof_ms[kernel] = 0;
+  return HOC_SUCCESS;
+}
+
+hocResult_t hoc_profile_stream_finish(hocComm_t comm, float* finish_ms, int max_streams, int* n_streams) {
+  if (!comm) return HOC_ERR_NOT_INITIALIZED;
+  if (!n_streams || (max_streams > 0 && !finish_ms)) return HOC_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(comm->mu);
+  DeviceGuard g(comm->device);
+  *n_streams = comm->prof_streams;
+  for (int i = 0; i < comm->prof_streams && i < max_streams; ++i) {
+    HOC_CK(cudaEventSynchronize(comm->prof_stream_end[i]));
+    HOC_CK(cudaEventElapsedTime(&finish_ms[i], comm->prof_fork, comm->prof_stream_end[i]));
+  }
   return HOC_SUCCESS;
 }
 

@@ -97,6 +97,7 @@ _SIGS["hoc_allreduce_host"] = (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.PO
                                          C.c_int, C.c_int, C.c_void_p])
 _SIGS["hoc_proxy_status"] = (C.c_int, [C.c_void_p, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64),
                                        C.POINTER(C.c_int)])
+_SIGS["hoc_profile_stream_finish"] = (C.c_int, [C.c_void_p, C.POINTER(C.c_float), C.c_int, C.POINTER(C.c_int)])
 _SIGS["hoc_topo_schedule"] = (C.c_int, [C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_int), C.POINTER(C.c_uint64),
                                         C.c_uint64, C.c_uint64, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64),
                                         C.POINTER(C.c_double), C.c_int, C.POINTER(C.c_int),
@@ -315,6 +316,13 @@ class Comm:
         ms = C.c_double()
         _check(lib().hoc_profile_read(self._h, int(kernel), C.byref(n), C.byref(ms)), "hoc_profile_read")
         return n.value, ms.value
+
+    def profile_stream_finish(self) -> list:
+        """Finish time (ms from the fork) of each copy stream of the last call issued while profiling."""
+        buf = (C.c_float * 16)()
+        n = C.c_int()
+        _check(lib().hoc_profile_stream_finish(self._h, buf, 16, C.byref(n)), "hoc_profile_stream_finish")
+        return [buf[i] for i in range(min(n.value, 16))]
 
 
 # ---------------------------------------------------------------- workload

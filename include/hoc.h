@@ -193,6 +193,15 @@ hocResult_t hoc_last_stats(hocComm_t comm, hocOpStats_t* stats);
 hocResult_t hoc_profile_enable(hocComm_t comm, int enable);
 hocResult_t hoc_profile_read(hocComm_t comm, hocKernel_t kernel, int* launches, double* total_ms);
 
+/* Per-stream finish times of the last call issued while profiling was
+ * enabled, when it forked onto internal copy streams: finish_ms[i] = time from
+ * the fork on the caller's stream to the end of copy stream i's last
+ * operation, for i < min(*n_streams, max_streams).  Waits for those events.
+ * *n_streams = 0 if the last profiled call ran on the caller's stream alone.
+ * Their spread is the schedule's tail: how unevenly the moves were spread
+ * over the copy engines (HOCCL section 3.3 on skewed all-to-all flows). */
+hocResult_t hoc_profile_stream_finish(hocComm_t comm, float* finish_ms, int max_streams, int* n_streams);
+
 /* Static description of a result code. */
 const char* hoc_error_string(hocResult_t result);
 

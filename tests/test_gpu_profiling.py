@@ -1,0 +1,41 @@
+"""Per-stream finish profiling (the tail of a schedule over the copy streams), on the GPU."""
+import numpy as np
+import pytest
+import torch
+
+from collective_communication_schedules_gb300 import hoc
+from oracle import alltoall as o_a2a
+from tests.gpu_util import to_device, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+def test_stream_finish_times_of_a_multi_stream_alltoall():
+    k, n = 8, 1 << 20
+    rng = np.random.default_rng(21)
+    counts = rng.integers(0, n // k, size=(k, k))
+    sends = [rng.integers(0, 1 << 31, size=int(counts[s].sum())).astype(np.int32) for s in range(k)]
+    want = o_a2a.alltoallv(sends, counts)
+    s = torch.cuda.Stream()
+    with hoc.Comm(k, 0, hoc.Config(path="ce", n_copy_streams=4, chunk_bytes=1 << 18)) as c:
+        sd = [to_device(x, "int32") for x in sends]
+        rv = [torch.zeros(int(counts[:, d].sum()), dtype=torch.int32, device="cuda") for d in range(k)]
+        torch.cuda.synchronize()
+        c.profile_enable(True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        c.alltoall(sd, rv, sendcounts=counts, dtype=hoc.INT32, stream=s)
+        e1.record(s)
+        fin = c.profile_stream_finish()
+        torch.cuda.synchronize()
+        total = e0.elapsed_time(e1)
+        assert 2 <= len(fin) <= 4                       # the call forked onto the copy streams
+        assert all(0 < v <= total + 0.05 for v in fin)  # each stream ends inside the call
+        for d in range(k):
+            assert np.array_equal(to_host(rv[d], "int32"), want[d]), d
+        # a call on the caller's stream alone reports no copy streams
+        a = torch.ones(1024, dtype=torch.int32, device="cuda")
+        b = torch.zeros(1024, dtype=torch.int32, device="cuda")
+        c.sendrecv(0, a, 1, b, stream=s)
+        assert c.profile_stream_finish() == []
+        c.profile_enable(False)
