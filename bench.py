@@ -522,7 +522,7 @@ def leg_expert_dispatch(peak):
     psend = [torch.empty((n, h), dtype=torch.bfloat16, device="cuda") for _ in range(k)]
     perm = [torch.empty(n, dtype=torch.int32, device="cuda") for _ in range(k)]
     pos = [torch.empty(n, dtype=torch.int32, device="cuda") for _ in range(k)]
-    wsp = [torch.empty(experts, dtype=torch.int32, device="cuda") for _ in range(k)]
+    wsp = [torch.empty(hoc.ep_pack_workspace(tokens, topk, experts), dtype=torch.int32, device="cuda") for _ in range(k)]
     d_counts = torch.empty((k, k), dtype=torch.int64, device="cuda")
     cap = [int(ecounts[:, d].sum()) for d in range(k)]
     precv = [torch.empty(cap[d], dtype=torch.bfloat16, device="cuda") for d in range(k)]

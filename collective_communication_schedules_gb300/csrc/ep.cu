@@ -21,6 +21,14 @@ namespace hoc {
 namespace {
 
 constexpr int kEpThreads = 256;
+constexpr int kEpWarps = kEpThreads / 32;
+// Counting sort by tiles: each CTA owns kTileItems consecutive pairs, each of
+// its warps a contiguous kWarpItems of them, so (tile, warp, step, lane) order
+// is pair order and the sort stays stable.
+constexpr int kTileItems = 2048;
+constexpr int kWarpItems = kTileItems / kEpWarps;
+constexpr int kMaxTileExperts = 1024;  // per-warp counters of this many experts fit in shared memory
+constexpr int kCombineTopk = 8;        // combine: top-k loads issued together up to this k
 
 // One CTA per expert: how many pairs chose it.
 __global__ void ep_count_kernel(const int32_t* __restrict__ ids, int n, int32_t* __restrict__ cnt) {
@@ -64,6 +72,111 @@ __global__ void ep_place_kernel(const int32_t* __restrict__ ids, int n, const in
     __syncthreads();
   }
   if (threadIdx.x == 0 && cnt[e] > 0) atomicAdd(dst_counts + e / per_rank, (unsigned long long)cnt[e] * hidden);
+}
+
+// Tile histogram: hist[b * experts + e] = pairs of tile b that chose expert e.
+__global__ void ep_tile_hist_kernel(const int32_t* __restrict__ ids, int n, int experts, int32_t* __restrict__ hist) {
+  extern __shared__ int sh[];
+  for (int e = threadIdx.x; e < experts; e += blockDim.x) sh[e] = 0;
+  __syncthreads();
+  const int lo = blockIdx.x * kTileItems, hi = min(n, lo + kTileItems);
+  for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+    const int e = ids[i];
+    if (e >= 0 && e < experts) atomicAdd(&sh[e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < experts; e += blockDim.x) hist[size_t(blockIdx.x) * experts + e] = sh[e];
+}
+
+// One CTA: turns the tile histograms into the first output row of each
+// (tile, expert) -- all pairs of smaller experts, then those of expert e in
+// earlier tiles -- and writes the per-expert totals and the per-destination
+// element counts.
+__global__ void ep_scan_kernel(int32_t* __restrict__ hist, int tiles, int experts, int32_t* __restrict__ total,
+                               unsigned long long* __restrict__ dst_counts, int nranks, int per_rank, int hidden) {
+  __shared__ int part[1024];
+  for (int e = threadIdx.x; e < experts; e += blockDim.x) {  // per expert: exclusive scan over tiles
+    int run = 0;
+    for (int b = 0; b < tiles; ++b) {
+      const int c = hist[size_t(b) * experts + e];
+      hist[size_t(b) * experts + e] = run;
+      run += c;
+    }
+    total[e] = run;
+  }
+  __syncthreads();
+  // exclusive scan of the totals over experts: thread t owns a contiguous run of experts
+  const int per = (experts + blockDim.x - 1) / blockDim.x;
+  const int e0 = min(experts, int(threadIdx.x) * per), e1 = min(experts, e0 + per);
+  int mine = 0;
+  for (int e = e0; e < e1; ++e) mine += total[e];
+  part[threadIdx.x] = mine;
+  __syncthreads();
+  for (int off = 1; off < int(blockDim.x); off <<= 1) {
+    const int v = int(threadIdx.x) >= off ? part[threadIdx.x - off] : 0;
+    __syncthreads();
+    part[threadIdx.x] += v;
+    __syncthreads();
+  }
+  int base = part[threadIdx.x] - mine;
+  for (int e = e0; e < e1; ++e) {
+    for (int b = 0; b < tiles; ++b) hist[size_t(b) * experts + e] += base;
+    base += total[e];
+  }
+  for (int d = threadIdx.x; d < nranks; d += blockDim.x) {
+    unsigned long long c = 0;
+    for (int e = d * per_rank; e < (d + 1) * per_rank; ++e) c += (unsigned long long)total[e];
+    dst_counts[d] = c * (unsigned long long)hidden;
+  }
+}
+
+// Stable placement of one tile: a pair's row is its (tile, expert) start, plus
+// the pairs of that expert in earlier warps of the tile, earlier steps of its
+// warp and lower lanes of its step.
+__global__ void ep_tile_place_kernel(const int32_t* __restrict__ ids, int n, int experts,
+                                     const int32_t* __restrict__ start, int32_t* __restrict__ perm,
+                                     int32_t* __restrict__ pos_of) {
+  extern __shared__ int wh[];  // [kEpWarps][experts]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int j = threadIdx.x; j < kEpWarps * experts; j += blockDim.x) wh[j] = 0;
+  __syncthreads();
+  int* mine = wh + warp * experts;
+  const int lo = blockIdx.x * kTileItems + warp * kWarpItems;
+  const int hi = min(n, lo + kWarpItems);
+  const unsigned below = (1u << lane) - 1u;
+  for (int base = lo; base < hi; base += 32) {  // this warp's pairs per expert
+    const int i = base + lane;
+    const int e = i < hi ? ids[i] : -1;
+    const bool ok = e >= 0 && e < experts;
+    const unsigned grp = __match_any_sync(0xFFFFFFFFu, ok ? e : -1);
+    if (ok && (grp & below) == 0) mine[e] += __popc(grp);  // the group's lowest lane counts it
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < experts; e += blockDim.x) {  // per expert: exclusive scan over warps
+    int run = 0;
+    for (int w = 0; w < kEpWarps; ++w) {
+      const int c = wh[w * experts + e];
+      wh[w * experts + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  const int32_t* st = start + size_t(blockIdx.x) * experts;
+  for (int base = lo; base < hi; base += 32) {
+    const int i = base + lane;
+    const int e = i < hi ? ids[i] : -1;
+    const bool ok = e >= 0 && e < experts;
+    const unsigned grp = __match_any_sync(0xFFFFFFFFu, ok ? e : -1);
+    if (ok) {
+      const int pos = st[e] + mine[e] + __popc(grp & below);
+      perm[pos] = i;
+      pos_of[i] = pos;
+    }
+    __syncwarp();
+    if (ok && (grp & below) == 0) mine[e] += __popc(grp);
+    __syncwarp();
+  }
 }
 
 // Warp per row: send[pos] = x[perm[pos] / topk]; rows of `hb` bytes.
@@ -148,6 +261,60 @@ __global__ void ep_combine_vec_kernel(const uint16_t* __restrict__ rows, const i
   }
 }
 
+// Same fold with every one of the token's (at most kCombineTopk) row loads
+// issued before the ordered fold, so a lane keeps topk 16-byte loads in flight.
+__global__ void ep_combine_vec_ilp_kernel(const uint16_t* __restrict__ rows, const int32_t* __restrict__ pos_of,
+                                          const float* __restrict__ w, int tokens, int topk, int hidden, int n_rows,
+                                          uint16_t* __restrict__ y) {
+  const int warps = blockDim.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int hv = hidden / 8;
+  for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < tokens; t += gridDim.x * warps) {
+    const int pl = lane < topk ? pos_of[size_t(t) * topk + lane] : -1;
+    const float wl = lane < topk ? w[size_t(t) * topk + lane] : 0.f;
+    int p[kCombineTopk];
+    float wj[kCombineTopk];
+    bool ok[kCombineTopk];
+#pragma unroll
+    for (int j = 0; j < kCombineTopk; ++j) {
+      p[j] = __shfl_sync(0xFFFFFFFFu, pl, j);
+      wj[j] = __shfl_sync(0xFFFFFFFFu, wl, j);
+      ok[j] = j < topk && p[j] >= 0 && p[j] < n_rows;
+    }
+    for (int v = lane; v < hv; v += 32) {
+      uint4 x[kCombineTopk];
+#pragma unroll
+      for (int j = 0; j < kCombineTopk; ++j)
+        x[j] = ok[j] ? __ldg(reinterpret_cast<const uint4*>(rows + size_t(p[j]) * hidden) + v) : make_uint4(0, 0, 0, 0);
+      float acc[8];
+      bool any = false;
+#pragma unroll
+      for (int j = 0; j < kCombineTopk; ++j) {
+        if (!ok[j]) continue;
+        const uint32_t q[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float lo = __fmul_rn(wj[j], __uint_as_float(q[i] << 16));
+          const float hi = __fmul_rn(wj[j], __uint_as_float(q[i] & 0xFFFF0000u));
+          acc[2 * i] = any ? __fadd_rn(acc[2 * i], lo) : lo;
+          acc[2 * i + 1] = any ? __fadd_rn(acc[2 * i + 1], hi) : hi;
+        }
+        any = true;
+      }
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float a = any ? acc[2 * i] : 0.f, b = any ? acc[2 * i + 1] : 0.f;
+        o[i] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
+               (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
+      }
+      reinterpret_cast<uint4*>(y + size_t(t) * hidden)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+int tiles_of(int n) { return (n + kTileItems - 1) / kTileItems; }
+
 int grid_for(int items, int per_cta) {
   int dev = 0, sms = 1;
   cudaGetDevice(&dev);
@@ -160,9 +327,15 @@ int grid_for(int items, int per_cta) {
 }  // namespace
 
 cudaError_t ep_preload() {
-  const void* fns[] = {reinterpret_cast<const void*>(&ep_count_kernel), reinterpret_cast<const void*>(&ep_place_kernel),
-                       reinterpret_cast<const void*>(&ep_gather_kernel), reinterpret_cast<const void*>(&ep_combine_kernel),
-                       reinterpret_cast<const void*>(&ep_combine_vec_kernel)};
+  const void* fns[] = {reinterpret_cast<const void*>(&ep_count_kernel),
+                       reinterpret_cast<const void*>(&ep_place_kernel),
+                       reinterpret_cast<const void*>(&ep_tile_hist_kernel),
+                       reinterpret_cast<const void*>(&ep_scan_kernel),
+                       reinterpret_cast<const void*>(&ep_tile_place_kernel),
+                       reinterpret_cast<const void*>(&ep_gather_kernel),
+                       reinterpret_cast<const void*>(&ep_combine_kernel),
+                       reinterpret_cast<const void*>(&ep_combine_vec_kernel),
+                       reinterpret_cast<const void*>(&ep_combine_vec_ilp_kernel)};
   for (const void* f : fns) {
     cudaFuncAttributes a;
     const cudaError_t e = cudaFuncGetAttributes(&a, f);
@@ -173,25 +346,53 @@ cudaError_t ep_preload() {
 
 }  // namespace hoc
 
+extern "C" hocResult_t hoc_ep_pack_workspace(int tokens, int topk, int experts, size_t* ints) {
+  using namespace hoc;
+  if (tokens < 0 || topk < 1 || experts < 1 || !ints) return HOC_ERR_INVALID_ARG;
+  if (size_t(tokens) * topk > size_t(INT32_MAX)) return HOC_ERR_INVALID_ARG;
+  const int n = tokens * topk;
+  *ints = experts <= kMaxTileExperts ? size_t(experts) * (1 + size_t(tiles_of(n))) : size_t(experts);
+  return HOC_SUCCESS;
+}
+
 extern "C" hocResult_t hoc_ep_pack(const int32_t* expert_ids, const void* x, int tokens, int topk, int hidden,
                                    int experts, int nranks, void* send, int32_t* perm, int32_t* pos_of,
-                                   uint64_t* dst_counts, int32_t* workspace, void* stream) {
+                                   uint64_t* dst_counts, int32_t* workspace, size_t workspace_ints, void* stream) {
   using namespace hoc;
   if (tokens < 0 || topk < 1 || hidden < 1 || experts < 1 || nranks < 1 || experts % nranks != 0)
     return HOC_ERR_INVALID_ARG;
   if (tokens == 0) return HOC_SUCCESS;
   if (!expert_ids || !x || !send || !perm || !pos_of || !dst_counts || !workspace) return HOC_ERR_INVALID_ARG;
   if (size_t(tokens) * topk > size_t(INT32_MAX)) return HOC_ERR_INVALID_ARG;
+  size_t need = 0;
+  hoc_ep_pack_workspace(tokens, topk, experts, &need);
+  if (workspace_ints < need) {
+    set_error_detail("hoc_ep_pack: workspace smaller than hoc_ep_pack_workspace() asks for");
+    return HOC_ERR_INVALID_ARG;
+  }
   const int n = tokens * topk;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(perm, 0xFF, sizeof(int32_t) * size_t(n), s) != cudaSuccess ||
       cudaMemsetAsync(pos_of, 0xFF, sizeof(int32_t) * size_t(n), s) != cudaSuccess ||
       cudaMemsetAsync(dst_counts, 0, sizeof(uint64_t) * size_t(nranks), s) != cudaSuccess)
     return HOC_ERR_CUDA;
-  ep_count_kernel<<<experts, kEpThreads, 0, s>>>(expert_ids, n, workspace);
-  ep_place_kernel<<<experts, kEpThreads, 0, s>>>(expert_ids, n, workspace, perm, pos_of,
-                                                 reinterpret_cast<unsigned long long*>(dst_counts), hidden,
-                                                 experts / nranks);
+  if (experts <= kMaxTileExperts) {
+    // counting sort by tiles: histograms, one scan, stable placement
+    const int tiles = tiles_of(n);
+    int32_t* total = workspace;
+    int32_t* hist = workspace + experts;
+    ep_tile_hist_kernel<<<tiles, kEpThreads, sizeof(int) * size_t(experts), s>>>(expert_ids, n, experts, hist);
+    ep_scan_kernel<<<1, 1024, 0, s>>>(hist, tiles, experts, total, reinterpret_cast<unsigned long long*>(dst_counts),
+                                      nranks, experts / nranks, hidden);
+    ep_tile_place_kernel<<<tiles, kEpThreads, sizeof(int) * size_t(kEpWarps) * experts, s>>>(expert_ids, n, experts,
+                                                                                          hist, perm, pos_of);
+  } else {
+    // many experts: one CTA per expert scanning every pair
+    ep_count_kernel<<<experts, kEpThreads, 0, s>>>(expert_ids, n, workspace);
+    ep_place_kernel<<<experts, kEpThreads, 0, s>>>(expert_ids, n, workspace, perm, pos_of,
+                                                   reinterpret_cast<unsigned long long*>(dst_counts), hidden,
+                                                   experts / nranks);
+  }
   const int hb = hidden * 2;
   const int vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(send)) & 15u) == 0 && hb % 16 == 0;
   ep_gather_kernel<<<grid_for(n, 8), 256, 0, s>>>(static_cast<const char*>(x), perm, n, topk, hb,
@@ -208,7 +409,11 @@ extern "C" hocResult_t hoc_ep_combine(const void* rows, const int32_t* pos_of, c
   if (size_t(tokens) * topk > size_t(INT32_MAX)) return HOC_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool vec = hidden % 8 == 0 && ((reinterpret_cast<uintptr_t>(rows) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0;
-  if (vec)
+  if (vec && topk <= kCombineTopk)
+    ep_combine_vec_ilp_kernel<<<grid_for(tokens, 8), 256, 0, s>>>(static_cast<const uint16_t*>(rows), pos_of, weights,
+                                                                  tokens, topk, hidden, tokens * topk,
+                                                                  static_cast<uint16_t*>(y));
+  else if (vec)
     ep_combine_vec_kernel<<<grid_for(tokens, 8), 256, 0, s>>>(static_cast<const uint16_t*>(rows), pos_of, weights,
                                                               tokens, topk, hidden, tokens * topk,
                                                               static_cast<uint16_t*>(y));

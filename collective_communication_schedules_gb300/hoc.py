@@ -90,7 +90,8 @@ NOALLOC_MAX_MOVES = 192
 _SIGS["hoc_alltoall_device_counts"] = (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p),
                                                  C.c_void_p, C.c_int, C.POINTER(C.c_size_t), C.c_int, C.c_void_p])
 _SIGS["hoc_ep_pack"] = (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p,
-                                  C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p])
+                                  C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p])
+_SIGS["hoc_ep_pack_workspace"] = (C.c_int, [C.c_int, C.c_int, C.c_int, C.POINTER(C.c_size_t)])
 _SIGS["hoc_ep_combine"] = (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p,
                                      C.c_void_p])
 _SIGS["hoc_allreduce_host"] = (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_size_t,
@@ -370,13 +371,20 @@ def topo_schedule(C_matrix, node_of, sym, bw_nvlink: int, bw_rdma: int):
     return Tm, stages, [ta[s] for s in range(n.value)], tot.value
 
 
+def ep_pack_workspace(tokens: int, topk: int, experts: int) -> int:
+    """int32 entries of scratch that ep_pack needs for this shape."""
+    n = C.c_size_t()
+    _check(lib().hoc_ep_pack_workspace(int(tokens), int(topk), int(experts), C.byref(n)), "hoc_ep_pack_workspace")
+    return n.value
+
+
 def ep_pack(expert_ids, x, experts: int, nranks: int, send, perm, pos_of, dst_counts, workspace, stream=None):
     """Dispatch-side pack of one source rank (device tensors; see include/hoc_ep.h)."""
     tokens, hidden = x.shape
     topk = expert_ids.numel() // tokens
     _check(lib().hoc_ep_pack(_ptr(expert_ids), _ptr(x), int(tokens), int(topk), int(hidden), int(experts),
                              int(nranks), _ptr(send), _ptr(perm), _ptr(pos_of), _ptr(dst_counts), _ptr(workspace),
-                             _stream(stream)), "hoc_ep_pack")
+                             int(workspace.numel()), _stream(stream)), "hoc_ep_pack")
 
 
 def ep_combine(rows, pos_of, weights, tokens: int, topk: int, hidden: int, y, stream=None):

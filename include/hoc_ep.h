@@ -24,11 +24,18 @@ extern "C" {
  *   perm[i]:    t*topk + j of the pair in row i (-1 past the valid pairs);
  *   pos_of[p]:  the row of pair p (-1 for a dropped pair);
  *   dst_counts: [nranks] uint64 elements (rows * hidden) per destination.
- * workspace: device int32 [experts] scratch.  Pairs with an expert id outside
- * [0, experts) are dropped.  experts must be a multiple of nranks. */
+ * workspace: device int32 scratch of workspace_ints entries, at least what
+ * hoc_ep_pack_workspace() returns (else HOC_ERR_INVALID_ARG, nothing queued).
+ * Pairs with an expert id outside [0, experts) are dropped.  experts must be a
+ * multiple of nranks.  The sort is a stable counting sort over tiles of 2048
+ * pairs (tile histograms, one scan, stable placement by warp match); with more
+ * than 1024 experts one CTA per expert scans every pair instead. */
 hocResult_t hoc_ep_pack(const int32_t* expert_ids, const void* x, int tokens, int topk, int hidden, int experts,
                         int nranks, void* send, int32_t* perm, int32_t* pos_of, uint64_t* dst_counts,
-                        int32_t* workspace, void* stream);
+                        int32_t* workspace, size_t workspace_ints, void* stream);
+
+/* int32 entries of the workspace hoc_ep_pack needs for this shape. */
+hocResult_t hoc_ep_pack_workspace(int tokens, int topk, int experts, size_t* ints);
 
 /* Combine (unpack) of one source rank after the inverse exchange.  rows:
  * [tokens*topk, hidden] bf16 in packed order; pos_of from hoc_ep_pack;

@@ -33,14 +33,21 @@ def _pack_on_device(ids, x, experts, k, stream):
     perm = torch.empty(n, dtype=torch.int32, device="cuda")
     pos_of = torch.empty(n, dtype=torch.int32, device="cuda")
     counts = torch.empty(k, dtype=torch.int64, device="cuda")
-    ws = torch.empty(experts, dtype=torch.int32, device="cuda")
+    ws = torch.empty(hoc.ep_pack_workspace(tokens, n // tokens, experts), dtype=torch.int32, device="cuda")
     hoc.ep_pack(ids, x, experts, k, send, perm, pos_of, counts, ws, stream=stream)
     return send, perm, pos_of, counts
 
 
-@pytest.mark.parametrize("tokens,hidden,drop", [(4096, 2048, False), (333, 40, True)])
-def test_pack_and_combine_match_oracle(tokens, hidden, drop):
-    k, experts, topk = 8, 64, 6
+@pytest.mark.parametrize("tokens,hidden,drop,experts,topk", [
+    (4096, 2048, False, 64, 6),   # the EP workload's shape: 12 full tiles of 2048 pairs
+    (333, 40, True, 64, 6),       # one partial tile, dropped pairs
+    (5000, 64, True, 96, 4),      # ragged last tile, experts not a power of two
+    (700, 16, False, 2048, 2),    # more than 1024 experts: the one-CTA-per-expert sort
+    (200, 24, False, 64, 10),     # topk above the combine's batched loads
+    (250, 36, True, 64, 6),       # hidden not a multiple of 8: scalar combine
+])
+def test_pack_and_combine_match_oracle(tokens, hidden, drop, experts, topk):
+    k = 8
     routing, xs, ws = _rank_data(k, tokens, hidden, experts, topk, 1.1)
     ids = routing[0].astype(np.int32)
     if drop:
