@@ -827,20 +827,23 @@ def run_ours(args, world, rank, local):
             c3.close()
         extras["paths"] = paths
         extras["allgather_moves"] = ag
-        # copy-engine allreduce: chunk size and copy-queue sweeps
+        # chunk size sweep, 1-64 MiB (64 is capped at the 32 MiB block), on the copy-engine and
+        # TMA-kernel move paths; then copy-queue counts on the copy-engine path
         sweep = []
-        for chunk_mib, nq in ((1, 4), (4, 4), (16, 4), (32, 4), (32, 8), (8, 8), (8, 16)):
-            c4 = hoc.Comm(k, local, hoc.Config(path="ce", chunk_bytes=chunk_mib << 20, n_copy_streams=nq))
+        grid = [(p, mib, 4) for p in ("ce", "tma") for mib in (1, 2, 4, 8, 16, 32, 64)]
+        grid += [("ce", 32, 8), ("ce", 8, 8), ("ce", 8, 16)]
+        for p, chunk_mib, nq in grid:
+            c4 = hoc.Comm(k, local, hoc.Config(path=p, chunk_bytes=chunk_mib << 20, n_copy_streams=nq))
             for _ in range(3):
                 c4.allreduce(send, recv, stream=stream)
             cm = time_allreduce(c4, send, recv, stream, 10)
             s4 = c4.last_stats()
-            sweep.append({"chunk_mib": chunk_mib, "copy_streams": nq, "ms": round(cm, 4),
+            sweep.append({"path": p, "chunk_mib": chunk_mib, "copy_streams": nq, "ms": round(cm, 4),
                           "bus_gbs": round(bus_bytes(k, per_rank) / (cm * 1e-3) / 1e9, 1),
                           "lower_bound_frac": round(s4["bytes_min"] / (cm * 1e-3) / (peak * 1e9), 4),
-                          "copies_per_step": s4["copies"]})
+                          "copies_per_step": s4["copies"], "kernels_per_step": s4["kernels"]})
             c4.close()
-        extras["ce_sweep"] = sweep
+        extras["chunk_sweep"] = sweep
     if args.workloads and not args.no_extras:
         extras["workloads"] = {"dp_bucket_stream": leg_bucket_stream(bucket_pool, sms, peak),
                                "pp_1f1b": leg_pipeline(sms),
