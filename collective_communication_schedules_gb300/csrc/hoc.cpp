@@ -492,7 +492,7 @@ hocResult_t read_cfg(const hocConfig_t* in, int k, Cfg* out) {
     }
     seen[v] = 1;
   }
-  if (c.path < HOC_PATH_AUTO || c.path > HOC_PATH_FUSED || c.n_copy < 1 || c.n_copy > 16 || c.chunk_bytes < 256 ||
+  if (c.path < HOC_PATH_AUTO || c.path > HOC_PATH_FUSED || c.n_copy < 1 || c.n_copy > 16 || (c.chunk_bytes != 0 && c.chunk_bytes < 256) ||
       c.depth < 0 || c.reduce_max_sms < 0 || c.copy_max_sms < 0 || c.reduce_engine < HOC_REDUCE_AUTO ||
       c.reduce_engine > HOC_REDUCE_TMA) {
     set_detail("configuration value out of range");
@@ -661,7 +661,7 @@ hocResult_t hoc_config_default(hocConfig_t* cfg) {
   if (!cfg) return HOC_ERR_INVALID_ARG;
   memset(cfg, 0, sizeof *cfg);
   cfg->path = HOC_PATH_AUTO;
-  cfg->chunk_bytes = size_t(4) << 20;
+  cfg->chunk_bytes = 0;  // by move path
   cfg->n_copy_streams = 4;
   cfg->pipeline_depth = 0;
   cfg->reduce_max_sms = 0;

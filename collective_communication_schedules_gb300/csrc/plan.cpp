@@ -83,8 +83,8 @@ std::string plan_key(const CallShape& s) {
 
 namespace {
 
-size_t chunk_elems(const Cfg& cfg, size_t b) {
-  size_t ce = cfg.chunk_bytes / b;
+size_t chunk_elems(const Cfg& cfg, size_t b, int path) {
+  size_t ce = chunk_for(cfg, path) / b;
   ce -= ce % 16;  // keep chunk boundaries on 16-element multiples
   return ce < 16 ? 16 : ce;
 }
@@ -209,7 +209,7 @@ hocResult_t plan_allreduce(const Cfg& cfg, const CallShape& s, Plan* p) {
     p->steps.push_back(std::move(st));
     return HOC_SUCCESS;
   }
-  const size_t ce = chunk_elems(cfg, b);
+  const size_t ce = chunk_elems(cfg, b, p->path);
   const size_t nq = (sz[0] + ce - 1) / ce;
   std::vector<std::vector<int>> copy_steps(nq);
   for (size_t q = 0; q < nq; ++q) {
@@ -264,7 +264,7 @@ hocResult_t plan_allgather(const Cfg& cfg, const CallShape& s, Plan* p) {
       const int d = (r + t) % k;
       Move m{r, d, HOC_BUF_SEND, HOC_BUF_RECV, 0, size_t(r) * sc * b, sc * b};
       if (p->path == HOC_PATH_TMA) chunks.push_back(m);
-      else split_move(m, cfg.chunk_bytes, &chunks);
+      else split_move(m, chunk_for(cfg, HOC_PATH_CE), &chunks);
     }
   std::vector<int> ids;
   emit_moves(cfg, p->path, chunks, 0, {}, false, p, &ids);
@@ -309,6 +309,7 @@ hocResult_t plan_alltoall(const Cfg& cfg, const CallShape& s, Plan* p) {
     return HOC_SUCCESS;
   }
   // Shift stages (Eq. 6-8 with one domain): stage st holds flows u -> u+st.
+  const size_t cb = chunk_for(cfg, HOC_PATH_CE);
   std::vector<int> prev;
   for (int st = 0; st < k; ++st) {
     std::vector<Move> flows;
@@ -317,14 +318,14 @@ hocResult_t plan_alltoall(const Cfg& cfg, const CallShape& s, Plan* p) {
       const int v = (u + st) % k;
       const size_t n = cnt(u, v) * b;
       flows.push_back(Move{u, v, HOC_BUF_SEND, HOC_BUF_RECV, sd[size_t(u) * k + v] * b, rd[size_t(v) * k + u] * b, n});
-      nchunks.push_back((n + cfg.chunk_bytes - 1) / cfg.chunk_bytes);
+      nchunks.push_back((n + cb - 1) / cb);
     }
     std::vector<Move> chunks;
     for (const auto& fc : interleave_chunks(nchunks, cfg.a2a_interleave != 0)) {
       const Move& f = flows[fc.first];
-      const size_t o = fc.second * cfg.chunk_bytes;
+      const size_t o = fc.second * cb;
       chunks.push_back(Move{f.src_rank, f.dst_rank, f.src_buf, f.dst_buf, f.src_off + o, f.dst_off + o,
-                            std::min(cfg.chunk_bytes, f.bytes - o)});
+                            std::min(cb, f.bytes - o)});
     }
     std::vector<int> ids;
     emit_moves(cfg, HOC_PATH_CE, chunks, st, cfg.a2a_stage_sync ? prev : std::vector<int>{}, cfg.a2a_stage_sync != 0,
@@ -339,7 +340,7 @@ hocResult_t plan_sendrecv(const Cfg& cfg, const CallShape& s, Plan* p) {
   Move m{s.src_rank, s.dst_rank, HOC_BUF_SEND, HOC_BUF_RECV, 0, 0, bytes};
   std::vector<Move> chunks;
   if (p->path == HOC_PATH_TMA || bytes <= kSendrecvStripeBytes) chunks.push_back(m);
-  else split_move(m, cfg.chunk_bytes, &chunks);
+  else split_move(m, chunk_for(cfg, HOC_PATH_CE), &chunks);
   std::vector<int> ids;
   emit_moves(cfg, p->path, chunks, 0, {}, false, p, &ids);
   if (p->path == HOC_PATH_TMA && !p->steps.empty()) p->steps.back().stream = 0;
@@ -356,7 +357,7 @@ hocResult_t build_plan(const Cfg& cfg, const CallShape& s, Plan* p) {
   p->dtype = s.dtype;
   p->count = s.count;
   if (s.k < 1 || s.k > kMaxRanks || dtype_bytes(s.dtype) == 0) return HOC_ERR_INVALID_ARG;
-  if (cfg.chunk_bytes < 256 || cfg.n_copy < 1 || cfg.n_copy > 16) return HOC_ERR_INVALID_ARG;
+  if ((cfg.chunk_bytes != 0 && cfg.chunk_bytes < 256) || cfg.n_copy < 1 || cfg.n_copy > 16) return HOC_ERR_INVALID_ARG;
   hocResult_t r = HOC_SUCCESS;
   switch (s.op) {
     case HOC_OP_ALLREDUCE:

@@ -21,7 +21,7 @@ namespace hoc {
 
 struct Cfg {
   int path = HOC_PATH_AUTO;
-  size_t chunk_bytes = size_t(4) << 20;
+  size_t chunk_bytes = 0;  // 0: by move path (chunk_for)
   int n_copy = 4;
   int depth = 0;
   int reduce_max_sms = 0;
@@ -34,6 +34,15 @@ struct Cfg {
   int debug = 0;
   int fault = 0;           // host-side fault injection (Fault)
 };
+
+// Pipeline chunk of a move path when the configuration leaves it at 0: the
+// best of the 1-64 MiB sweep of the 8-rank 256 MiB bf16 allreduce on GB300
+// (copy engines 4 MiB: 0.895 ms; TMA kernel 2 MiB: 0.757 ms).
+constexpr size_t kAutoChunkCe = size_t(4) << 20;
+constexpr size_t kAutoChunkTma = size_t(2) << 20;
+inline size_t chunk_for(const Cfg& cfg, int path) {
+  return cfg.chunk_bytes ? cfg.chunk_bytes : (path == HOC_PATH_TMA ? kAutoChunkTma : kAutoChunkCe);
+}
 
 // Send/recv messages up to this size go as one copy on the caller's stream;
 // larger ones are chunked and striped over the copy queues.
