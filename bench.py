@@ -825,8 +825,32 @@ def run_ours(args, world, rank, local):
                      "sms_used": s3["sms_used"], "kernels_per_step": s3["kernels"],
                      "probe": probes(run, am, stream, sms)}
             c3.close()
+        # copy-engine chunk size against interference: larger copies move faster but slow the probe more
+        tradeoff = []
+        for mib, nq in ((4, 4), (8, 4), (16, 4), (32, 4), (32, 8)):
+            c5 = hoc.Comm(k, local, hoc.Config(path="ce", chunk_bytes=mib << 20, n_copy_streams=nq))
+            run = lambda s, c5=c5: c5.allgather(ag_send, recv, stream=s)
+            for _ in range(3):
+                run(stream)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(10):
+                run(stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            am = e0.elapsed_time(e1) / 10
+            s5 = c5.last_stats()
+            pr = probes(run, am, stream, sms)
+            tradeoff.append({"chunk_mib": mib, "copy_streams": nq, "ms": round(am, 4),
+                             "bytes_gbs": round(s5["bytes_exec"] / (am * 1e-3) / 1e9, 1), "copies_per_step": s5["copies"],
+                             "kernels_per_step": s5["kernels"],
+                             "probe_slowdown": {sh: pr[sh]["slowdown"] for sh in pr},
+                             "probe_sm_mhz_with": {sh: pr[sh]["sm_mhz_with"] for sh in pr}})
+            c5.close()
         extras["paths"] = paths
         extras["allgather_moves"] = ag
+        extras["allgather_ce_chunk_vs_probe"] = tradeoff
         # chunk size sweep, 1-64 MiB (64 is capped at the 32 MiB block), on the copy-engine and
         # TMA-kernel move paths; then copy-queue counts on the copy-engine path
         sweep = []
