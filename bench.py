@@ -854,15 +854,18 @@ def run_ours(args, world, rank, local):
         # chunk size sweep, 1-64 MiB (64 is capped at the 32 MiB block), on the copy-engine and
         # TMA-kernel move paths; then copy-queue counts on the copy-engine path
         sweep = []
-        grid = [(p, mib, 4) for p in ("ce", "tma") for mib in (1, 2, 4, 8, 16, 32, 64)]
-        grid += [("ce", 32, 8), ("ce", 8, 8), ("ce", 8, 16)]
-        for p, chunk_mib, nq in grid:
-            c4 = hoc.Comm(k, local, hoc.Config(path=p, chunk_bytes=chunk_mib << 20, n_copy_streams=nq))
+        grid = [(p, mib, 4, 0) for p in ("ce", "tma") for mib in (1, 2, 4, 8, 16, 32, 64)]
+        grid += [("ce", 32, 8, 0), ("ce", 8, 8, 0), ("ce", 8, 16, 0)]
+        grid += [("ce", 4, 4, d) for d in (1, 2, 4)]      # pipeline depth: reduce at most d chunks ahead of the moves
+        for p, chunk_mib, nq, depth in grid:
+            c4 = hoc.Comm(k, local, hoc.Config(path=p, chunk_bytes=chunk_mib << 20, n_copy_streams=nq,
+                                               pipeline_depth=depth))
             for _ in range(3):
                 c4.allreduce(send, recv, stream=stream)
             cm = time_allreduce(c4, send, recv, stream, 10)
             s4 = c4.last_stats()
-            sweep.append({"path": p, "chunk_mib": chunk_mib, "copy_streams": nq, "ms": round(cm, 4),
+            sweep.append({"path": p, "chunk_mib": chunk_mib, "copy_streams": nq, "pipeline_depth": depth or "unbounded",
+                          "ms": round(cm, 4),
                           "bus_gbs": round(bus_bytes(k, per_rank) / (cm * 1e-3) / 1e9, 1),
                           "lower_bound_frac": round(s4["bytes_min"] / (cm * 1e-3) / (peak * 1e9), 4),
                           "copies_per_step": s4["copies"], "kernels_per_step": s4["kernels"]})
