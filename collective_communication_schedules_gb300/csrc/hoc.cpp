@@ -228,24 +228,63 @@ hocResult_t run_reduce(hocComm* c, const Plan& p, const Step& st, const Bind& bd
   return timed_launch(c, kind, s, [&] { return launch_reduce(rp, grid, wide, s); });
 }
 
+// The copy jobs of a TMA step: one job per group of moves that read the same
+// source (source_groups), all of whose destinations share the job's
+// alignment class (co-aligned with the source modulo 16, or not); a member in
+// the other class gets a job of its own.  `more[i]` lists job i's destinations
+// beyond the first.
+void tma_jobs(const Step& st, const Bind& bd, std::vector<CopyJob>* jobs, std::vector<std::vector<char*>>* more) {
+  auto co = [](const char* a, const char* b) {
+    return ((reinterpret_cast<uintptr_t>(a) ^ reinterpret_cast<uintptr_t>(b)) & 15u) == 0;
+  };
+  for (const auto& g : source_groups(st.moves)) {
+    const size_t first = jobs->size();  // jobs of this group start here
+    for (int idx : g) {
+      const Move& m = st.moves[idx];
+      const char* src = static_cast<const char*>(buf_ptr(bd, m.src_rank, m.src_buf)) + m.src_off;
+      char* dst = static_cast<char*>(const_cast<void*>(buf_ptr(bd, m.dst_rank, m.dst_buf))) + m.dst_off;
+      if (!m.bytes || src == dst) continue;  // nothing to move (in-place self block)
+      bool placed = false;
+      for (size_t q = first; q < jobs->size() && !placed; ++q) {
+        if (co(src, (*jobs)[q].dst) == co(src, dst)) {
+          (*more)[q].push_back(dst);
+          placed = true;
+        }
+      }
+      if (!placed) {
+        CopyJob j{};
+        j.src = src;
+        j.dst = dst;
+        j.bytes = m.bytes;
+        jobs->push_back(j);
+        more->emplace_back();
+      }
+    }
+  }
+}
+
 hocResult_t run_tma(hocComm* c, const Step& st, const Bind& bd, cudaStream_t s, int* max_ctas) {
   const uint32_t pb = tma_piece_bytes();
+  std::vector<CopyJob> jobs;
+  std::vector<std::vector<char*>> more;
+  tma_jobs(st, bd, &jobs, &more);
   size_t i = 0;
-  while (i < st.moves.size()) {
+  while (i < jobs.size()) {
     CopyParams cp;
     memset(&cp, 0, sizeof cp);
     cp.piece_bytes = pb;
     cp.status = c->status;
     cp.tx_pad = c->cfg.fault == kFaultTmaStall ? 16u : 0u;
     cp.wait_ns = c->cfg.fault == kFaultTmaStall ? 100000000ull : 2000000000ull;  // 0.1 s under injection, else 2 s
-    int nj = 0;
-    for (; i < st.moves.size() && nj < kMaxCopyJobs; ++i) {
-      const Move& m = st.moves[i];
-      CopyJob j;
-      j.src = static_cast<const char*>(buf_ptr(bd, m.src_rank, m.src_buf)) + m.src_off;
-      j.dst = static_cast<char*>(const_cast<void*>(buf_ptr(bd, m.dst_rank, m.dst_buf))) + m.dst_off;
-      j.bytes = m.bytes;
-      if (!j.bytes || j.src == j.dst) continue;  // nothing to move (in-place self block)
+    int nj = 0, nm = 0;
+    for (; i < jobs.size() && nj < kMaxCopyJobs; ++i) {
+      // the pool is full: the next launch takes this job (a job has fewer than
+      // kMaxRanks extra destinations, so a fresh pool always holds it)
+      if (size_t(nm) + more[i].size() > size_t(kMaxMoreDst)) break;
+      CopyJob j = jobs[i];
+      j.nmore = int32_t(more[i].size());
+      j.more_at = nm;
+      for (char* d : more[i]) cp.more_dst[nm++] = d;
       cp.job[nj] = j;
       cp.piece_start[nj + 1] = cp.piece_start[nj] + tma_job_pieces(j, pb);
       ++nj;

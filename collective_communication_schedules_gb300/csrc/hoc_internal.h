@@ -60,15 +60,23 @@ cudaError_t reduce_tma_prepare();  // one-time per device: shared-memory opt-in
 cudaError_t launch_reduce_tma(const ReduceParams& p, int grid, int* status, cudaStream_t stream);
 
 // -------------------------------------------------------------- TMA copy
+// One copy job of the TMA kernel: `bytes` from `src` to `dst` and, for a
+// broadcast, to CopyParams::more_dst[more_at .. more_at + nmore) too (the
+// bytes are loaded once and stored to every destination).  Every destination
+// is co-aligned with the source modulo 16 bytes, or none is.
 struct CopyJob {
   const char* src;
   char* dst;
   uint64_t bytes;
+  int32_t nmore;
+  int32_t more_at;
 };
+constexpr int kMaxMoreDst = 256;  // broadcast destinations beyond the first, per launch
 
 struct CopyParams {
   CopyJob job[kMaxCopyJobs];
   uint64_t piece_start[kMaxCopyJobs + 1];  // prefix sums of the pieces of each job
+  char* more_dst[kMaxMoreDst];             // further destinations of broadcast jobs
   int32_t njobs;
   uint32_t piece_bytes;  // bytes per piece: one shared-memory stage
   uint32_t tx_pad;       // extra bytes each mbarrier expects (0; >0 only for host-injected stalls)

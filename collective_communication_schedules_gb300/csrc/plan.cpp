@@ -3,6 +3,8 @@
 #include "plan.h"
 
 #include <algorithm>
+#include <map>
+#include <tuple>
 #include <cstring>
 #include <queue>
 
@@ -81,6 +83,23 @@ std::string plan_key(const CallShape& s) {
   return key;
 }
 
+std::vector<std::vector<int>> source_groups(const std::vector<Move>& moves) {
+  std::vector<std::vector<int>> groups;
+  std::map<std::tuple<int, int, size_t, size_t>, size_t> open;  // source -> group still taking members
+  for (size_t i = 0; i < moves.size(); ++i) {
+    const Move& m = moves[i];
+    const auto key = std::make_tuple(m.src_rank, m.src_buf, m.src_off, m.bytes);
+    auto it = open.find(key);
+    if (it != open.end() && groups[it->second].size() < size_t(kMaxRanks)) {
+      groups[it->second].push_back(int(i));
+    } else {
+      open[key] = groups.size();
+      groups.push_back({int(i)});
+    }
+  }
+  return groups;
+}
+
 namespace {
 
 size_t chunk_elems(const Cfg& cfg, size_t b, int path) {
@@ -115,15 +134,18 @@ void account(Plan* p) {
         any = any || g.elems;
       }
       if (any) ++p->kernels;
-    } else {
+    } else if (s.kind == kStepCopy) {
       size_t moved = 0;
       for (const Move& m : s.moves) moved += m.bytes;
       p->bytes_exec += 2 * moved;
-      if (s.kind == kStepCopy) {
-        for (const Move& m : s.moves) p->copies += m.bytes ? 1 : 0;
-      } else if (moved) {
-        p->kernels += int((s.moves.size() + kMaxCopyJobs - 1) / kMaxCopyJobs);
-      }
+      for (const Move& m : s.moves) p->copies += m.bytes ? 1 : 0;
+    } else {  // TMA: a source shared by a group of moves is read once
+      const auto groups = source_groups(s.moves);
+      size_t written = 0, read = 0;
+      for (const Move& m : s.moves) written += m.bytes;
+      for (const auto& g : groups) read += s.moves[g[0]].bytes;
+      p->bytes_exec += read + written;
+      if (written) p->kernels += int((groups.size() + kMaxCopyJobs - 1) / kMaxCopyJobs);
     }
   }
   int streams = 1;

@@ -99,6 +99,12 @@ struct CallShape {
 size_t dtype_bytes(int dtype);
 int dtype_lanes(int dtype);  // elements per 16-byte vector
 
+// The moves of a TMA step that read the same source bytes (same rank, buffer,
+// offset and length), grouped in order of first appearance, at most kMaxRanks
+// per group: the copy kernel loads such a group's bytes once and stores them to
+// every destination (a broadcast job).
+std::vector<std::vector<int>> source_groups(const std::vector<Move>& moves);
+
 // Builds the plan; returns HOC_ERR_INVALID_ARG / UNSUPPORTED for bad shapes.
 hocResult_t build_plan(const Cfg& cfg, const CallShape& shape, Plan* plan);
 

@@ -102,10 +102,9 @@ __device__ __forceinline__ int find_job(const CopyParams& p, uint64_t pc) {
   return lo;
 }
 
-// Bulk part of a piece: [off, off + n) bytes of its job (n == 0: none).
-__device__ __forceinline__ void piece_bulk(const CopyParams& p, uint64_t pc, const char*& src, char*& dst,
-                                           uint32_t& n) {
-  const int j = find_job(p, pc);
+// Bulk part of a piece: `n` bytes at offset `o` of job `j` (n == 0: none).
+__device__ __forceinline__ void piece_bulk(const CopyParams& p, uint64_t pc, int& j, uint64_t& o, uint32_t& n) {
+  j = find_job(p, pc);
   const CopyJob& jb = p.job[j];
   n = 0;
   if (!co_aligned(jb)) return;
@@ -114,14 +113,19 @@ __device__ __forceinline__ void piece_bulk(const CopyParams& p, uint64_t pc, con
   const uint64_t off = i * p.piece_bytes;
   if (off >= body) return;
   const uint64_t len = body - off < p.piece_bytes ? body - off : p.piece_bytes;
-  const uint64_t h = job_head(jb);
-  src = jb.src + h + off;
-  dst = jb.dst + h + off;
+  o = job_head(jb) + off;
   n = static_cast<uint32_t>(len);
 }
 
 __device__ __forceinline__ void copy_bytes(const char* src, char* dst, uint64_t n, int lane) {
   for (uint64_t i = lane; i < n; i += 32) dst[i] = src[i];
+}
+
+// [off, off + n) of a job's source to the same range of each of its destinations.
+__device__ __forceinline__ void copy_bytes_all(const CopyParams& p, const CopyJob& jb, uint64_t off, uint64_t n,
+                                               int lane) {
+  copy_bytes(jb.src + off, jb.dst + off, n, lane);
+  for (int e = 0; e < jb.nmore; ++e) copy_bytes(jb.src + off, p.more_dst[jb.more_at + e] + off, n, lane);
 }
 
 __global__ void __launch_bounds__(kCopyThreads, 1) tma_copy_kernel(const __grid_constant__ CopyParams p) {
@@ -148,37 +152,40 @@ __global__ void __launch_bounds__(kCopyThreads, 1) tma_copy_kernel(const __grid_
       if (!co_aligned(jb)) {
         const uint64_t off = local * p.piece_bytes;
         const uint64_t len = jb.bytes - off < p.piece_bytes ? jb.bytes - off : p.piece_bytes;
-        copy_bytes(jb.src + off, jb.dst + off, len, lane);
+        copy_bytes_all(p, jb, off, len, lane);
       } else if (local == 0) {
         const uint64_t h = job_head(jb);
         const uint64_t end = h + job_body(jb);
-        copy_bytes(jb.src, jb.dst, h, lane);
-        copy_bytes(jb.src + end, jb.dst + end, jb.bytes - end, lane);
+        copy_bytes_all(p, jb, 0, h, lane);
+        copy_bytes_all(p, jb, end, jb.bytes - end, lane);
       }
     }
     return;
   }
   if (lane != 0) return;
 
-  // Bulk pipeline: loads run kStages ahead of stores.
+  // Bulk pipeline: loads run kStages ahead of stores; a piece's stores (one
+  // per destination) form one bulk group.
   uint32_t stage_bytes[kStages];
-  char* stage_dst[kStages];
+  int stage_job[kStages];
+  uint64_t stage_off[kStages];
   uint64_t next = 0;  // next of my pieces to look at for a load
   uint32_t nload = 0, nstore = 0;
   auto issue_next_load = [&]() -> bool {
     while (next < mine) {
       const uint64_t pc = blockIdx.x + next * gridDim.x;
       ++next;
-      const char* src;
-      char* dst;
+      int j;
+      uint64_t o;
       uint32_t n;
-      piece_bulk(p, pc, src, dst, n);
+      piece_bulk(p, pc, j, o, n);
       if (n == 0) continue;
       const int s = nload % kStages;
       stage_bytes[s] = n;
-      stage_dst[s] = dst;
+      stage_job[s] = j;
+      stage_off[s] = o;
       mbar_arrive_expect_tx(&bar[s], n + p.tx_pad);
-      bulk_load(stage_mem + size_t(s) * p.piece_bytes, src, n, &bar[s]);
+      bulk_load(stage_mem + size_t(s) * p.piece_bytes, p.job[j].src + o, n, &bar[s]);
       ++nload;
       return true;
     }
@@ -193,7 +200,10 @@ __global__ void __launch_bounds__(kCopyThreads, 1) tma_copy_kernel(const __grid_
       failed = true;
       break;
     }
-    bulk_store(stage_dst[s], stage_mem + size_t(s) * p.piece_bytes, stage_bytes[s]);
+    const CopyJob& jb = p.job[stage_job[s]];
+    const unsigned char* piece = stage_mem + size_t(s) * p.piece_bytes;
+    bulk_store(jb.dst + stage_off[s], piece, stage_bytes[s]);
+    for (int e = 0; e < jb.nmore; ++e) bulk_store(p.more_dst[jb.more_at + e] + stage_off[s], piece, stage_bytes[s]);
     bulk_commit();
     ++nstore;
     if (nstore >= 2) {
@@ -317,7 +327,10 @@ extern "C" hocResult_t hoc_tma_moves_noalloc(const void* const* src, void* const
       set_error_detail("hoc_tma_moves_noalloc: a move's source and destination overlap");
       return HOC_ERR_INVALID_ARG;
     }
-    CopyJob j{static_cast<const char*>(src[i]), static_cast<char*>(dst[i]), uint64_t(bytes[i])};
+    CopyJob j{};
+    j.src = static_cast<const char*>(src[i]);
+    j.dst = static_cast<char*>(dst[i]);
+    j.bytes = uint64_t(bytes[i]);
     cp.job[nj] = j;
     cp.piece_start[nj + 1] = cp.piece_start[nj] + job_pieces(j, kPieceBytes);
     ++nj;

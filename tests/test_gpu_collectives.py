@@ -142,6 +142,30 @@ def test_allgather_parity(path, k):
                 assert_bits_equal(full[r].host(), want[r], "bfloat16", f"ag in place {path} rank {r}")
 
 
+@pytest.mark.parametrize("k", [3, 8])
+def test_tma_broadcast_with_mixed_destination_alignment(k):
+    # The TMA path loads each source block once and stores it to every
+    # destination; destinations in another 16-byte alignment class than the
+    # first one get a job of their own.  Receive buffers shifted by 0..7 bf16
+    # elements per rank put a block's destinations in several classes.
+    for sc in (8, 4099, 300_001):
+        xs = inputs.rank_inputs("bfloat16", k, sc, workload=8, slot=20 + k)
+        want = o_ring.allgather(xs)
+        with _comm(k, "tma", chunk_bytes=1 << 16) as c:
+            send = [Guarded(sc, "bfloat16", offset_elems=(5 * r) % 8) for r in range(k)]
+            recv = [Guarded(k * sc, "bfloat16", offset_elems=(3 * r) % 8) for r in range(k)]
+            for g, x in zip(send, xs):
+                g.load(x)
+            c.allgather([g.ptr() for g in send], [g.ptr() for g in recv], sc, hoc.BFLOAT16)
+            c.wait()
+            for r in range(k):
+                recv[r].check()
+                assert_bits_equal(recv[r].host(), want[r], "bfloat16", f"ag tma mixed k={k} sc={sc} rank {r}")
+            # every block is read once (whatever the alignment): the schedule reads kS and writes k*kS
+            st = c.last_stats()
+            assert st["bytes_exec"] == (k * sc + k * k * sc) * 2
+
+
 @pytest.mark.parametrize("path", ["ce", "tma"])
 @pytest.mark.parametrize("interleave", [True, False])
 @pytest.mark.parametrize("stage_sync", [True, False])
