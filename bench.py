@@ -51,7 +51,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default="auto", choices=["auto", "ce", "tma", "fused"])
-    ap.add_argument("--chunk-bytes", type=int, default=0, help="0: picked by move path (4 MiB CE, 2 MiB TMA)")
+    ap.add_argument("--chunk-bytes", type=int, default=0, help="0: picked by move path (4 MiB on both)")
     ap.add_argument("--copy-streams", type=int, default=4)
     ap.add_argument("--no-extras", action="store_true", help="skip the per-path, probe and e2e legs")
     ap.add_argument("--e2e-steps", type=int, default=3)
@@ -889,7 +889,7 @@ def run_ours(args, world, rank, local):
                 "config": {"workload": WORKLOAD if n_el == N_ELEMS else f"profiling case: 8 ranks x {n_el:,} bf16",
                            "k": k, "count": n_el, "path": args.path,
                            "resolved_path": {0: "auto", 1: "ce", 2: "tma", 3: "fused"}[st["path"]],
-                           "chunk_bytes": args.chunk_bytes or "auto (4 MiB CE, 2 MiB TMA)", "copy_streams": args.copy_streams,
+                           "chunk_bytes": args.chunk_bytes or "auto (4 MiB)", "copy_streams": args.copy_streams,
                            "l2": "no flush: each step reads 2 GiB of inputs and writes 2 GiB, > 129 MB L2",
                            "parallelism": f"{world} independent replica(s), one per GPU"},
                 "algbw_gbs": round(per_rank / (ms_max * 1e-3) / 1e9, 2),

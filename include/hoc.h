@@ -77,8 +77,8 @@ typedef enum {
  * (lsu|tma|auto), HOC_DEBUG override the values passed in. */
 typedef struct {
   int path;              /* hocPath_t */
-  size_t chunk_bytes;    /* pipeline unit inside a block / flow; 0 (default) picks by move path:
-                            4 MiB on copy engines, 2 MiB on the TMA kernel */
+  size_t chunk_bytes;    /* pipeline unit inside a block / flow; 0 (default) picks by move path
+                            (4 MiB on copy engines and on the TMA kernel, the measured best) */
   int n_copy_streams;    /* internal copy streams (the multi-QP analogue); default 4, max 16 */
   int pipeline_depth;    /* allreduce CE/TMA: reduce of chunk q waits for the moves of
                             chunk q - depth; 0 = no limit */
