@@ -386,7 +386,7 @@ def leg_bucket_stream(host_pool, sms, peak):
     out = {"buckets": nb, "bucket_bytes_per_rank": be * 2, "budgets": []}
     for m, eng in ((4, "lsu"), (4, "tma"), (8, "lsu"), (8, "tma"), (16, "lsu"), (16, "tma"), (32, "lsu"),
                    (32, "tma"), (0, "lsu"), (0, "tma")):
-        with hoc.Comm(k, 0, hoc.Config(reduce_max_sms=m, reduce_engine=eng)) as c:
+        with hoc.Comm(k, torch.cuda.current_device(), hoc.Config(reduce_max_sms=m, reduce_engine=eng)) as c:
             def run(s, c=c):
                 for b in range(nb):
                     c.reduce_scatter(pool_in[b % pool], [outs[b, r] for r in range(k)], rc, stream=s)
@@ -424,7 +424,7 @@ def leg_pipeline(sms):
     xs = [torch.randn(elems, generator=g, device="cuda").to(torch.bfloat16) for _ in range(m)]
     out = {}
     for path in ("ce", "tma"):
-        with hoc.Comm(p, 0, hoc.Config(path=path)) as c:
+        with hoc.Comm(p, torch.cuda.current_device(), hoc.Config(path=path)) as c:
             res = {}
             for label, send in (("with_sends", True), ("compute_only", False)):
                 pipe = Pipeline1F1B(c, p, m, elems, keys, probe_ctas=2 * sms, probe_iters=2000)
@@ -477,7 +477,7 @@ def leg_expert_dispatch(peak):
     moved = int(ecounts.sum()) * 2
     out = {"rows_per_dst": [int(v) for v in counts.sum(axis=0)], "bytes_per_direction": moved}
     for path, inter in (("ce", True), ("ce", False), ("tma", True)):
-        with hoc.Comm(k, 0, hoc.Config(path=path, a2a_interleave=inter)) as c:
+        with hoc.Comm(k, torch.cuda.current_device(), hoc.Config(path=path, a2a_interleave=inter)) as c:
             def run(c=c):
                 c.alltoall(send, recv, sendcounts=ecounts, dtype=hoc.BFLOAT16)
                 c.alltoall(recv, back, sendcounts=ecounts.T.copy(), dtype=hoc.BFLOAT16)
@@ -530,7 +530,7 @@ def leg_expert_dispatch(peak):
     ys = [torch.empty((tokens, h), dtype=torch.bfloat16, device="cuda") for _ in range(k)]
 
     def device_round_trip():
-        with hoc.Comm(k, 0) as c:
+        with hoc.Comm(k, torch.cuda.current_device()) as c:
             def round_trip():
                 for r in range(k):
                     hoc.ep_pack(ids[r], xs[r], experts, k, psend[r], perm[r], pos[r], d_counts[r], wsp[r], stream=s)
@@ -603,7 +603,7 @@ def leg_sweeps(sms):
     out = {"sizes_mb": sizes_mb, "p2p": {}, "allgather": {}, "alltoall": {}}
     for path, ctas in variants:
         name = path if ctas == 0 else f"{path}_{ctas}sm"
-        c = hoc.Comm(k, 0, hoc.Config(path=path, copy_max_sms=ctas))
+        c = hoc.Comm(k, torch.cuda.current_device(), hoc.Config(path=path, copy_max_sms=ctas))
         for op in ("p2p", "allgather", "alltoall"):
             row = []
             for mb in sizes_mb:
@@ -654,7 +654,7 @@ def leg_host_overhead():
         "sendrecv_tma": ("tma", lambda c: c.sendrecv(0, a[0], 1, b[1], stream=stream)),
     }
     for name, (path, fn) in cases.items():
-        with hoc.Comm(k, 0, hoc.Config(path=path, chunk_bytes=1 << 18)) as c:
+        with hoc.Comm(k, torch.cuda.current_device(), hoc.Config(path=path, chunk_bytes=1 << 18)) as c:
             fn(c)
             torch.cuda.synchronize()
             ts = []
@@ -939,6 +939,10 @@ def main():
         run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
         return
     world, rank, local = dist_setup()
+    if world > 1:
+        # N replicas: the timed region and the end-to-end leg run on every rank (max over ranks); the
+        # per-path, probe, sweep and workload legs are single-GPU studies and run at N = 1 only
+        args.no_extras = True
     if args.mode == "allgather":
         run_allgather_only(args, world, rank, local)
     else:
