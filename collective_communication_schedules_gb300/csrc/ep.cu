@@ -192,7 +192,16 @@ __global__ void ep_gather_kernel(const char* __restrict__ x, const int32_t* __re
     if (vec) {
       const uint4* s4 = reinterpret_cast<const uint4*>(s);
       uint4* d4 = reinterpret_cast<uint4*>(d);
-      for (int v = lane; v < hb / 16; v += 32) d4[v] = __ldg(s4 + v);
+      const int nv = hb / 16;
+      int v = lane;
+      for (; v + 96 < nv; v += 128) {  // four 16-byte loads in flight per lane
+        const uint4 a = __ldg(s4 + v), b = __ldg(s4 + v + 32), c = __ldg(s4 + v + 64), e = __ldg(s4 + v + 96);
+        d4[v] = a;
+        d4[v + 32] = b;
+        d4[v + 64] = c;
+        d4[v + 96] = e;
+      }
+      for (; v < nv; v += 32) d4[v] = __ldg(s4 + v);
     } else {
       for (int b = lane; b < hb; b += 32) d[b] = s[b];
     }
@@ -261,35 +270,36 @@ __global__ void ep_combine_vec_kernel(const uint16_t* __restrict__ rows, const i
   }
 }
 
-// Same fold with every one of the token's (at most kCombineTopk) row loads
-// issued before the ordered fold, so a lane keeps topk 16-byte loads in flight.
+// Same fold with every one of the token's TK row loads issued before the
+// ordered fold, so a lane keeps TK 16-byte loads in flight (TK = topk).
+template <int TK>
 __global__ void ep_combine_vec_ilp_kernel(const uint16_t* __restrict__ rows, const int32_t* __restrict__ pos_of,
-                                          const float* __restrict__ w, int tokens, int topk, int hidden, int n_rows,
+                                          const float* __restrict__ w, int tokens, int hidden, int n_rows,
                                           uint16_t* __restrict__ y) {
   const int warps = blockDim.x >> 5;
   const int lane = threadIdx.x & 31;
   const int hv = hidden / 8;
   for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < tokens; t += gridDim.x * warps) {
-    const int pl = lane < topk ? pos_of[size_t(t) * topk + lane] : -1;
-    const float wl = lane < topk ? w[size_t(t) * topk + lane] : 0.f;
-    int p[kCombineTopk];
-    float wj[kCombineTopk];
-    bool ok[kCombineTopk];
+    const int pl = lane < TK ? pos_of[size_t(t) * TK + lane] : -1;
+    const float wl = lane < TK ? w[size_t(t) * TK + lane] : 0.f;
+    int p[TK];
+    float wj[TK];
+    bool ok[TK];
 #pragma unroll
-    for (int j = 0; j < kCombineTopk; ++j) {
+    for (int j = 0; j < TK; ++j) {
       p[j] = __shfl_sync(0xFFFFFFFFu, pl, j);
       wj[j] = __shfl_sync(0xFFFFFFFFu, wl, j);
-      ok[j] = j < topk && p[j] >= 0 && p[j] < n_rows;
+      ok[j] = p[j] >= 0 && p[j] < n_rows;
     }
     for (int v = lane; v < hv; v += 32) {
-      uint4 x[kCombineTopk];
+      uint4 x[TK];
 #pragma unroll
-      for (int j = 0; j < kCombineTopk; ++j)
+      for (int j = 0; j < TK; ++j)
         x[j] = ok[j] ? __ldg(reinterpret_cast<const uint4*>(rows + size_t(p[j]) * hidden) + v) : make_uint4(0, 0, 0, 0);
       float acc[8];
       bool any = false;
 #pragma unroll
-      for (int j = 0; j < kCombineTopk; ++j) {
+      for (int j = 0; j < TK; ++j) {
         if (!ok[j]) continue;
         const uint32_t q[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
 #pragma unroll
@@ -315,6 +325,17 @@ __global__ void ep_combine_vec_ilp_kernel(const uint16_t* __restrict__ rows, con
 
 int tiles_of(int n) { return (n + kTileItems - 1) / kTileItems; }
 
+using CombineIlpFn = void (*)(const uint16_t*, const int32_t*, const float*, int, int, int, uint16_t*);
+const CombineIlpFn kCombineIlp[kCombineTopk] = {
+    ep_combine_vec_ilp_kernel<1>, ep_combine_vec_ilp_kernel<2>, ep_combine_vec_ilp_kernel<3>,
+    ep_combine_vec_ilp_kernel<4>, ep_combine_vec_ilp_kernel<5>, ep_combine_vec_ilp_kernel<6>,
+    ep_combine_vec_ilp_kernel<7>, ep_combine_vec_ilp_kernel<8>};
+
+void launch_combine_ilp(int topk, int grid, cudaStream_t s, const uint16_t* rows, const int32_t* pos_of,
+                        const float* w, int tokens, int hidden, int n_rows, uint16_t* y) {
+  kCombineIlp[topk - 1]<<<grid, 256, 0, s>>>(rows, pos_of, w, tokens, hidden, n_rows, y);
+}
+
 int grid_for(int items, int per_cta) {
   int dev = 0, sms = 1;
   cudaGetDevice(&dev);
@@ -335,7 +356,10 @@ cudaError_t ep_preload() {
                        reinterpret_cast<const void*>(&ep_gather_kernel),
                        reinterpret_cast<const void*>(&ep_combine_kernel),
                        reinterpret_cast<const void*>(&ep_combine_vec_kernel),
-                       reinterpret_cast<const void*>(&ep_combine_vec_ilp_kernel)};
+                       reinterpret_cast<const void*>(kCombineIlp[0]), reinterpret_cast<const void*>(kCombineIlp[1]),
+                       reinterpret_cast<const void*>(kCombineIlp[2]), reinterpret_cast<const void*>(kCombineIlp[3]),
+                       reinterpret_cast<const void*>(kCombineIlp[4]), reinterpret_cast<const void*>(kCombineIlp[5]),
+                       reinterpret_cast<const void*>(kCombineIlp[6]), reinterpret_cast<const void*>(kCombineIlp[7])};
   for (const void* f : fns) {
     cudaFuncAttributes a;
     const cudaError_t e = cudaFuncGetAttributes(&a, f);
@@ -410,9 +434,8 @@ extern "C" hocResult_t hoc_ep_combine(const void* rows, const int32_t* pos_of, c
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool vec = hidden % 8 == 0 && ((reinterpret_cast<uintptr_t>(rows) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0;
   if (vec && topk <= kCombineTopk)
-    ep_combine_vec_ilp_kernel<<<grid_for(tokens, 8), 256, 0, s>>>(static_cast<const uint16_t*>(rows), pos_of, weights,
-                                                                  tokens, topk, hidden, tokens * topk,
-                                                                  static_cast<uint16_t*>(y));
+    launch_combine_ilp(topk, grid_for(tokens, 8), s, static_cast<const uint16_t*>(rows), pos_of, weights, tokens,
+                       hidden, tokens * topk, static_cast<uint16_t*>(y));
   else if (vec)
     ep_combine_vec_kernel<<<grid_for(tokens, 8), 256, 0, s>>>(static_cast<const uint16_t*>(rows), pos_of, weights,
                                                               tokens, topk, hidden, tokens * topk,
