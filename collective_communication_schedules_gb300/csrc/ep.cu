@@ -93,7 +93,8 @@ __global__ void ep_tile_hist_kernel(const int32_t* __restrict__ ids, int n, int 
 // earlier tiles -- and writes the per-expert totals and the per-destination
 // element counts.
 __global__ void ep_scan_kernel(int32_t* __restrict__ hist, int tiles, int experts, int32_t* __restrict__ total,
-                               unsigned long long* __restrict__ dst_counts, int nranks, int per_rank, int hidden) {
+                               int32_t* __restrict__ nvalid, unsigned long long* __restrict__ dst_counts, int nranks,
+                               int per_rank, int hidden) {
   __shared__ int part[1024];
   for (int e = threadIdx.x; e < experts; e += blockDim.x) {  // per expert: exclusive scan over tiles
     int run = 0;
@@ -119,6 +120,7 @@ __global__ void ep_scan_kernel(int32_t* __restrict__ hist, int tiles, int expert
     __syncthreads();
   }
   int base = part[threadIdx.x] - mine;
+  if (threadIdx.x == blockDim.x - 1) *nvalid = part[threadIdx.x];  // every valid pair
   for (int e = e0; e < e1; ++e) {
     for (int b = 0; b < tiles; ++b) hist[size_t(b) * experts + e] += base;
     base += total[e];
@@ -134,8 +136,8 @@ __global__ void ep_scan_kernel(int32_t* __restrict__ hist, int tiles, int expert
 // the pairs of that expert in earlier warps of the tile, earlier steps of its
 // warp and lower lanes of its step.
 __global__ void ep_tile_place_kernel(const int32_t* __restrict__ ids, int n, int experts,
-                                     const int32_t* __restrict__ start, int32_t* __restrict__ perm,
-                                     int32_t* __restrict__ pos_of) {
+                                     const int32_t* __restrict__ start, const int32_t* __restrict__ nvalid,
+                                     int32_t* __restrict__ perm, int32_t* __restrict__ pos_of) {
   extern __shared__ int wh[];  // [kEpWarps][experts]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int j = threadIdx.x; j < kEpWarps * experts; j += blockDim.x) wh[j] = 0;
@@ -172,39 +174,53 @@ __global__ void ep_tile_place_kernel(const int32_t* __restrict__ ids, int n, int
       const int pos = st[e] + mine[e] + __popc(grp & below);
       perm[pos] = i;
       pos_of[i] = pos;
+    } else if (i < hi) {
+      pos_of[i] = -1;  // dropped pair
     }
     __syncwarp();
     if (ok && (grp & below) == 0) mine[e] += __popc(grp);
     __syncwarp();
   }
+  // rows past the valid pairs have no pair
+  for (int r = *nvalid + blockIdx.x * blockDim.x + threadIdx.x; r < n; r += gridDim.x * blockDim.x) perm[r] = -1;
 }
 
-// Warp per row: send[pos] = x[perm[pos] / topk]; rows of `hb` bytes.
+// send[pos] = x[perm[pos] / topk]; rows of `hb` bytes.  Vector path: a work
+// item is (row, 1 KiB slice), spread evenly over the warps of a persistent
+// grid, each lane keeping two 16-byte loads in flight; byte path: warp per row.
+constexpr int kGatherSliceVecs = 64;  // 16-byte vectors per work item
 __global__ void ep_gather_kernel(const char* __restrict__ x, const int32_t* __restrict__ perm, int n, int topk,
                                  int hb, char* __restrict__ send, int vec) {
-  const int warps = blockDim.x >> 5;
   const int lane = threadIdx.x & 31;
-  for (int pos = blockIdx.x * warps + (threadIdx.x >> 5); pos < n; pos += gridDim.x * warps) {
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  const long long first = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (vec) {
+    const int nv = hb / 16;
+    const int slices = (nv + kGatherSliceVecs - 1) / kGatherSliceVecs;
+    const long long items = (long long)n * slices;
+    for (long long it = first; it < items; it += warps) {
+      const int pos = int(it / slices);
+      const int src = perm[pos];
+      if (src < 0) continue;  // dropped pair: nothing to send
+      const uint4* s4 = reinterpret_cast<const uint4*>(x + size_t(src / topk) * hb);
+      uint4* d4 = reinterpret_cast<uint4*>(send + size_t(pos) * hb);
+      const int v0 = int(it % slices) * kGatherSliceVecs + lane;
+      const int v1 = v0 + 32;
+      const bool h0 = v0 < nv, h1 = v1 < nv && v1 < int(it % slices) * kGatherSliceVecs + kGatherSliceVecs;
+      uint4 a, b;
+      if (h0) a = __ldg(s4 + v0);
+      if (h1) b = __ldg(s4 + v1);
+      if (h0) d4[v0] = a;
+      if (h1) d4[v1] = b;
+    }
+    return;
+  }
+  for (long long pos = first; pos < n; pos += warps) {
     const int src = perm[pos];
-    if (src < 0) continue;  // dropped pair: nothing to send
+    if (src < 0) continue;
     const char* s = x + size_t(src / topk) * hb;
     char* d = send + size_t(pos) * hb;
-    if (vec) {
-      const uint4* s4 = reinterpret_cast<const uint4*>(s);
-      uint4* d4 = reinterpret_cast<uint4*>(d);
-      const int nv = hb / 16;
-      int v = lane;
-      for (; v + 96 < nv; v += 128) {  // four 16-byte loads in flight per lane
-        const uint4 a = __ldg(s4 + v), b = __ldg(s4 + v + 32), c = __ldg(s4 + v + 64), e = __ldg(s4 + v + 96);
-        d4[v] = a;
-        d4[v + 32] = b;
-        d4[v + 64] = c;
-        d4[v + 96] = e;
-      }
-      for (; v < nv; v += 32) d4[v] = __ldg(s4 + v);
-    } else {
-      for (int b = lane; b < hb; b += 32) d[b] = s[b];
-    }
+    for (int b = lane; b < hb; b += 32) d[b] = s[b];
   }
 }
 
@@ -276,10 +292,16 @@ template <int TK>
 __global__ void ep_combine_vec_ilp_kernel(const uint16_t* __restrict__ rows, const int32_t* __restrict__ pos_of,
                                           const float* __restrict__ w, int tokens, int hidden, int n_rows,
                                           uint16_t* __restrict__ y) {
-  const int warps = blockDim.x >> 5;
+  // Work item = (token, slice of 32 16-byte vectors of its row): many small
+  // items spread evenly over the warps, so no partial last wave of whole rows.
   const int lane = threadIdx.x & 31;
   const int hv = hidden / 8;
-  for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < tokens; t += gridDim.x * warps) {
+  const int slices = (hv + 31) / 32;
+  const long long items = (long long)tokens * slices;
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long it = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items; it += warps) {
+    const int t = int(it / slices);
+    const int v = int(it % slices) * 32 + lane;
     const int pl = lane < TK ? pos_of[size_t(t) * TK + lane] : -1;
     const float wl = lane < TK ? w[size_t(t) * TK + lane] : 0.f;
     int p[TK];
@@ -289,41 +311,54 @@ __global__ void ep_combine_vec_ilp_kernel(const uint16_t* __restrict__ rows, con
     for (int j = 0; j < TK; ++j) {
       p[j] = __shfl_sync(0xFFFFFFFFu, pl, j);
       wj[j] = __shfl_sync(0xFFFFFFFFu, wl, j);
-      ok[j] = p[j] >= 0 && p[j] < n_rows;
+      ok[j] = p[j] >= 0 && p[j] < n_rows && v < hv;
     }
-    for (int v = lane; v < hv; v += 32) {
-      uint4 x[TK];
+    if (v >= hv) continue;
+    uint4 x[TK];
 #pragma unroll
-      for (int j = 0; j < TK; ++j)
-        x[j] = ok[j] ? __ldg(reinterpret_cast<const uint4*>(rows + size_t(p[j]) * hidden) + v) : make_uint4(0, 0, 0, 0);
-      float acc[8];
-      bool any = false;
+    for (int j = 0; j < TK; ++j)
+      x[j] = ok[j] ? __ldg(reinterpret_cast<const uint4*>(rows + size_t(p[j]) * hidden) + v) : make_uint4(0, 0, 0, 0);
+    float acc[8];
+    bool any = false;
 #pragma unroll
-      for (int j = 0; j < TK; ++j) {
-        if (!ok[j]) continue;
-        const uint32_t q[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float lo = __fmul_rn(wj[j], __uint_as_float(q[i] << 16));
-          const float hi = __fmul_rn(wj[j], __uint_as_float(q[i] & 0xFFFF0000u));
-          acc[2 * i] = any ? __fadd_rn(acc[2 * i], lo) : lo;
-          acc[2 * i + 1] = any ? __fadd_rn(acc[2 * i + 1], hi) : hi;
-        }
-        any = true;
-      }
-      uint32_t o[4];
+    for (int j = 0; j < TK; ++j) {
+      if (!ok[j]) continue;
+      const uint32_t q[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float a = any ? acc[2 * i] : 0.f, b = any ? acc[2 * i + 1] : 0.f;
-        o[i] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
-               (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
+        const float lo = __fmul_rn(wj[j], __uint_as_float(q[i] << 16));
+        const float hi = __fmul_rn(wj[j], __uint_as_float(q[i] & 0xFFFF0000u));
+        acc[2 * i] = any ? __fadd_rn(acc[2 * i], lo) : lo;
+        acc[2 * i + 1] = any ? __fadd_rn(acc[2 * i + 1], hi) : hi;
       }
-      reinterpret_cast<uint4*>(y + size_t(t) * hidden)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+      any = true;
     }
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float a = any ? acc[2 * i] : 0.f, b = any ? acc[2 * i + 1] : 0.f;
+      o[i] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
+             (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
+    }
+    reinterpret_cast<uint4*>(y + size_t(t) * hidden)[v] = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
 int tiles_of(int n) { return (n + kTileItems - 1) / kTileItems; }
+
+// A grid of every CTA the device can hold at once for kernel `fn` (256
+// threads, no dynamic shared memory), but no more than `want`.
+int persistent_grid(const void* fn, long long want) {
+  int dev = 0, sms = 1, occ = 1;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, 256, 0) != cudaSuccess || occ < 1) {
+    cudaGetLastError();
+    occ = 1;
+  }
+  const long long cap = (long long)sms * occ;
+  return int(want < 1 ? 1 : (want < cap ? want : cap));
+}
 
 using CombineIlpFn = void (*)(const uint16_t*, const int32_t*, const float*, int, int, int, uint16_t*);
 const CombineIlpFn kCombineIlp[kCombineTopk] = {
@@ -331,9 +366,12 @@ const CombineIlpFn kCombineIlp[kCombineTopk] = {
     ep_combine_vec_ilp_kernel<4>, ep_combine_vec_ilp_kernel<5>, ep_combine_vec_ilp_kernel<6>,
     ep_combine_vec_ilp_kernel<7>, ep_combine_vec_ilp_kernel<8>};
 
-void launch_combine_ilp(int topk, int grid, cudaStream_t s, const uint16_t* rows, const int32_t* pos_of,
-                        const float* w, int tokens, int hidden, int n_rows, uint16_t* y) {
-  kCombineIlp[topk - 1]<<<grid, 256, 0, s>>>(rows, pos_of, w, tokens, hidden, n_rows, y);
+void launch_combine_ilp(int topk, cudaStream_t s, const uint16_t* rows, const int32_t* pos_of, const float* w,
+                        int tokens, int hidden, int n_rows, uint16_t* y) {
+  const long long items = (long long)tokens * ((hidden / 8 + 31) / 32);  // one warp per item
+  const CombineIlpFn fn = kCombineIlp[topk - 1];
+  fn<<<persistent_grid(reinterpret_cast<const void*>(fn), (items + 7) / 8), 256, 0, s>>>(rows, pos_of, w, tokens,
+                                                                                            hidden, n_rows, y);
 }
 
 int grid_for(int items, int per_cta) {
@@ -375,7 +413,7 @@ extern "C" hocResult_t hoc_ep_pack_workspace(int tokens, int topk, int experts, 
   if (tokens < 0 || topk < 1 || experts < 1 || !ints) return HOC_ERR_INVALID_ARG;
   if (size_t(tokens) * topk > size_t(INT32_MAX)) return HOC_ERR_INVALID_ARG;
   const int n = tokens * topk;
-  *ints = experts <= kMaxTileExperts ? size_t(experts) * (1 + size_t(tiles_of(n))) : size_t(experts);
+  *ints = experts <= kMaxTileExperts ? size_t(experts) * (1 + size_t(tiles_of(n))) + 1 : size_t(experts);
   return HOC_SUCCESS;
 }
 
@@ -396,22 +434,25 @@ extern "C" hocResult_t hoc_ep_pack(const int32_t* expert_ids, const void* x, int
   }
   const int n = tokens * topk;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(perm, 0xFF, sizeof(int32_t) * size_t(n), s) != cudaSuccess ||
-      cudaMemsetAsync(pos_of, 0xFF, sizeof(int32_t) * size_t(n), s) != cudaSuccess ||
-      cudaMemsetAsync(dst_counts, 0, sizeof(uint64_t) * size_t(nranks), s) != cudaSuccess)
-    return HOC_ERR_CUDA;
   if (experts <= kMaxTileExperts) {
-    // counting sort by tiles: histograms, one scan, stable placement
+    // counting sort by tiles: histograms, one scan (which writes every
+    // destination count), stable placement (which writes every pos_of and the
+    // -1 tail of perm)
     const int tiles = tiles_of(n);
     int32_t* total = workspace;
     int32_t* hist = workspace + experts;
+    int32_t* nvalid = hist + size_t(tiles) * experts;
     ep_tile_hist_kernel<<<tiles, kEpThreads, sizeof(int) * size_t(experts), s>>>(expert_ids, n, experts, hist);
-    ep_scan_kernel<<<1, 1024, 0, s>>>(hist, tiles, experts, total, reinterpret_cast<unsigned long long*>(dst_counts),
-                                      nranks, experts / nranks, hidden);
-    ep_tile_place_kernel<<<tiles, kEpThreads, sizeof(int) * size_t(kEpWarps) * experts, s>>>(expert_ids, n, experts,
-                                                                                          hist, perm, pos_of);
+    ep_scan_kernel<<<1, 1024, 0, s>>>(hist, tiles, experts, total, nvalid,
+                                      reinterpret_cast<unsigned long long*>(dst_counts), nranks, experts / nranks, hidden);
+    ep_tile_place_kernel<<<tiles, kEpThreads, sizeof(int) * size_t(kEpWarps) * experts, s>>>(
+        expert_ids, n, experts, hist, nvalid, perm, pos_of);
   } else {
     // many experts: one CTA per expert scanning every pair
+    if (cudaMemsetAsync(perm, 0xFF, sizeof(int32_t) * size_t(n), s) != cudaSuccess ||
+        cudaMemsetAsync(pos_of, 0xFF, sizeof(int32_t) * size_t(n), s) != cudaSuccess ||
+        cudaMemsetAsync(dst_counts, 0, sizeof(uint64_t) * size_t(nranks), s) != cudaSuccess)
+      return HOC_ERR_CUDA;
     ep_count_kernel<<<experts, kEpThreads, 0, s>>>(expert_ids, n, workspace);
     ep_place_kernel<<<experts, kEpThreads, 0, s>>>(expert_ids, n, workspace, perm, pos_of,
                                                    reinterpret_cast<unsigned long long*>(dst_counts), hidden,
@@ -419,8 +460,9 @@ extern "C" hocResult_t hoc_ep_pack(const int32_t* expert_ids, const void* x, int
   }
   const int hb = hidden * 2;
   const int vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(send)) & 15u) == 0 && hb % 16 == 0;
-  ep_gather_kernel<<<grid_for(n, 8), 256, 0, s>>>(static_cast<const char*>(x), perm, n, topk, hb,
-                                                  static_cast<char*>(send), vec);
+  const long long gather_warps = vec ? (long long)n * ((hb / 16 + kGatherSliceVecs - 1) / kGatherSliceVecs) : n;
+  ep_gather_kernel<<<persistent_grid(reinterpret_cast<const void*>(&ep_gather_kernel), (gather_warps + 7) / 8), 256, 0,
+                     s>>>(static_cast<const char*>(x), perm, n, topk, hb, static_cast<char*>(send), vec);
   return cudaGetLastError() == cudaSuccess ? HOC_SUCCESS : HOC_ERR_CUDA;
 }
 
@@ -434,8 +476,8 @@ extern "C" hocResult_t hoc_ep_combine(const void* rows, const int32_t* pos_of, c
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool vec = hidden % 8 == 0 && ((reinterpret_cast<uintptr_t>(rows) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0;
   if (vec && topk <= kCombineTopk)
-    launch_combine_ilp(topk, grid_for(tokens, 8), s, static_cast<const uint16_t*>(rows), pos_of, weights, tokens,
-                       hidden, tokens * topk, static_cast<uint16_t*>(y));
+    launch_combine_ilp(topk, s, static_cast<const uint16_t*>(rows), pos_of, weights, tokens, hidden, tokens * topk,
+                       static_cast<uint16_t*>(y));
   else if (vec)
     ep_combine_vec_kernel<<<grid_for(tokens, 8), 256, 0, s>>>(static_cast<const uint16_t*>(rows), pos_of, weights,
                                                               tokens, topk, hidden, tokens * topk,
