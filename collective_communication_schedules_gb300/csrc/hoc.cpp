@@ -225,7 +225,8 @@ hocResult_t run_reduce(hocComm* c, const Plan& p, const Step& st, const Bind& bd
   else cap = uint64_t(c->sms) * ctas_per_sm(c, p.dtype, k, rp.broadcast) * kReduceWaves;
   const int grid = int(std::min<uint64_t>(tiles, cap));
   *max_ctas = std::max(*max_ctas, grid);
-  return timed_launch(c, kind, s, [&] { return launch_reduce(rp, grid, wide, s); });
+  const bool overlap = !wide && uint64_t(grid) > uint64_t(c->sms) * ctas_per_sm(c, p.dtype, k, rp.broadcast);
+  return timed_launch(c, kind, s, [&] { return launch_reduce(rp, grid, wide, s, overlap); });
 }
 
 // The copy jobs of a TMA step: one job per group of moves that read the same

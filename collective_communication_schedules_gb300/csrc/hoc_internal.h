@@ -42,7 +42,11 @@ struct ReduceParams {
 uint64_t reduce_seg_tiles(int dtype, const ReduceSeg& s, bool wide);
 // Resident CTAs per SM of the whole-GPU reduce kernel for (dtype, k, broadcast).
 int reduce_ctas_per_sm(int dtype, int k, int broadcast);
-cudaError_t launch_reduce(const ReduceParams& p, int grid, bool wide, cudaStream_t stream);
+// overlap_launch: programmatic dependent launch (the kernel may be scheduled
+// while the grid before it in the stream drains; it waits for that grid's
+// completion before touching memory).  Only for multi-wave grids: under an SM
+// budget the waiting CTAs would sit on SMs the budget leaves to other work.
+cudaError_t launch_reduce(const ReduceParams& p, int grid, bool wide, cudaStream_t stream, bool overlap_launch);
 
 // Force-load every kernel of the library (cudaFuncGetAttributes on each).
 // Under lazy module loading the first launch of a kernel loads it, and that

@@ -159,7 +159,7 @@ hocResult_t issue_host_ar(hocComm* c, HostArState* st, const void* const* hs, vo
     const uint64_t tiles = rp.tile_start[rp.nseg];
     const int grid = int(std::min<uint64_t>(tiles, uint64_t(c->sms) * st->ctas_per_sm));
     if (grid > 0) {
-      HCK(launch_reduce(rp, grid, false, st->red));
+      HCK(launch_reduce(rp, grid, false, st->red, false));
       ++*kernels;
       *max_ctas = std::max(*max_ctas, grid);
     }

@@ -168,6 +168,13 @@ __device__ __forceinline__ void scalar_elem(const ReduceParams& p, const uint8_t
 // K > 0: compile-time rank count (all loads hoisted); K == 0: runtime p.k.
 template <class Tr, int K, int kThreads, int kVecPerThread>
 __global__ void __launch_bounds__(kThreads) reduce_kernel(const __grid_constant__ ReduceParams p) {
+  // Programmatic dependent launch (both no-ops for a launch without the
+  // attribute): wait until the grid before this one in the stream has
+  // completed and its writes are visible, then let the next grid launch.  A
+  // multi-wave grid triggers only once its last wave has started, so the next
+  // grid's CTAs take the SM slots this one's last wave frees.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int L = Tr::kLanes;
   constexpr uint64_t kTileVecs = uint64_t(kThreads) * kVecPerThread;
   const int k = K > 0 ? K : p.k;
@@ -290,12 +297,22 @@ cudaError_t reduce_preload() {
   return cudaSuccess;
 }
 
-cudaError_t launch_reduce(const ReduceParams& p, int grid, bool wide, cudaStream_t stream) {
+cudaError_t launch_reduce(const ReduceParams& p, int grid, bool wide, cudaStream_t stream, bool overlap_launch) {
   const void* fn = kernel_for(p.dtype, p.k, wide);
   if (!fn) return cudaErrorInvalidValue;
   if (grid < 1) return cudaSuccess;
   void* args[] = {const_cast<ReduceParams*>(&p)};
-  return cudaLaunchKernel(fn, dim3(grid), dim3(wide ? kThreadsWide : kThreadsNarrow), args, 0, stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(wide ? kThreadsWide : kThreadsNarrow);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap_launch ? 1 : 0;
+  return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 }  // namespace hoc
