@@ -30,8 +30,18 @@ constexpr int kWarpItems = kTileItems / kEpWarps;
 constexpr int kMaxTileExperts = 1024;  // per-warp counters of this many experts fit in shared memory
 constexpr int kCombineTopk = 8;        // combine: top-k loads issued together up to this k
 
+// Programmatic dependent launch (no-ops for a plain launch): wait until the
+// kernel before this one in the stream has completed and its writes are
+// visible, then let the next kernel launch.  The pack and combine are chains
+// of short kernels, so this hides each launch behind its predecessor's tail.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // One CTA per expert: how many pairs chose it.
 __global__ void ep_count_kernel(const int32_t* __restrict__ ids, int n, int32_t* __restrict__ cnt) {
+  pdl_enter();
   const int e = blockIdx.x;
   int total = 0;
   for (int base = 0; base < n; base += kEpThreads) {
@@ -46,6 +56,7 @@ __global__ void ep_count_kernel(const int32_t* __restrict__ ids, int n, int32_t*
 __global__ void ep_place_kernel(const int32_t* __restrict__ ids, int n, const int32_t* __restrict__ cnt,
                                 int32_t* __restrict__ perm, int32_t* __restrict__ pos_of,
                                 unsigned long long* __restrict__ dst_counts, int hidden, int per_rank) {
+  pdl_enter();
   __shared__ int warp_n[kEpThreads / 32];
   const int e = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -76,6 +87,7 @@ __global__ void ep_place_kernel(const int32_t* __restrict__ ids, int n, const in
 
 // Tile histogram: hist[b * experts + e] = pairs of tile b that chose expert e.
 __global__ void ep_tile_hist_kernel(const int32_t* __restrict__ ids, int n, int experts, int32_t* __restrict__ hist) {
+  pdl_enter();
   extern __shared__ int sh[];
   for (int e = threadIdx.x; e < experts; e += blockDim.x) sh[e] = 0;
   __syncthreads();
@@ -95,6 +107,7 @@ __global__ void ep_tile_hist_kernel(const int32_t* __restrict__ ids, int n, int 
 __global__ void ep_scan_kernel(int32_t* __restrict__ hist, int tiles, int experts, int32_t* __restrict__ total,
                                int32_t* __restrict__ nvalid, unsigned long long* __restrict__ dst_counts, int nranks,
                                int per_rank, int hidden) {
+  pdl_enter();
   __shared__ int part[1024];
   for (int e = threadIdx.x; e < experts; e += blockDim.x) {  // per expert: exclusive scan over tiles
     int run = 0;
@@ -138,6 +151,7 @@ __global__ void ep_scan_kernel(int32_t* __restrict__ hist, int tiles, int expert
 __global__ void ep_tile_place_kernel(const int32_t* __restrict__ ids, int n, int experts,
                                      const int32_t* __restrict__ start, const int32_t* __restrict__ nvalid,
                                      int32_t* __restrict__ perm, int32_t* __restrict__ pos_of) {
+  pdl_enter();
   extern __shared__ int wh[];  // [kEpWarps][experts]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int j = threadIdx.x; j < kEpWarps * experts; j += blockDim.x) wh[j] = 0;
@@ -191,6 +205,7 @@ __global__ void ep_tile_place_kernel(const int32_t* __restrict__ ids, int n, int
 constexpr int kGatherSliceVecs = 64;  // 16-byte vectors per work item
 __global__ void ep_gather_kernel(const char* __restrict__ x, const int32_t* __restrict__ perm, int n, int topk,
                                  int hb, char* __restrict__ send, int vec) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
   const long long first = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -228,6 +243,7 @@ __global__ void ep_gather_kernel(const char* __restrict__ x, const int32_t* __re
 __global__ void ep_combine_kernel(const uint16_t* __restrict__ rows, const int32_t* __restrict__ pos_of,
                                   const float* __restrict__ w, int tokens, int topk, int hidden, int n_rows,
                                   uint16_t* __restrict__ y) {
+  pdl_enter();
   const int warps = blockDim.x >> 5;
   const int lane = threadIdx.x & 31;
   for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < tokens; t += gridDim.x * warps) {
@@ -252,6 +268,7 @@ __global__ void ep_combine_kernel(const uint16_t* __restrict__ rows, const int32
 __global__ void ep_combine_vec_kernel(const uint16_t* __restrict__ rows, const int32_t* __restrict__ pos_of,
                                       const float* __restrict__ w, int tokens, int topk, int hidden, int n_rows,
                                       uint16_t* __restrict__ y) {
+  pdl_enter();
   const int warps = blockDim.x >> 5;
   const int lane = threadIdx.x & 31;
   const int hv = hidden / 8;
@@ -292,6 +309,7 @@ template <int TK>
 __global__ void ep_combine_vec_ilp_kernel(const uint16_t* __restrict__ rows, const int32_t* __restrict__ pos_of,
                                           const float* __restrict__ w, int tokens, int hidden, int n_rows,
                                           uint16_t* __restrict__ y) {
+  pdl_enter();
   // Work item = (token, slice of 32 16-byte vectors of its row): many small
   // items spread evenly over the warps, so no partial last wave of whole rows.
   const int lane = threadIdx.x & 31;
@@ -346,6 +364,22 @@ __global__ void ep_combine_vec_ilp_kernel(const uint16_t* __restrict__ rows, con
 
 int tiles_of(int n) { return (n + kTileItems - 1) / kTileItems; }
 
+// Launch with programmatic stream serialization (see pdl_enter).
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // A grid of every CTA the device can hold at once for kernel `fn` (256
 // threads, no dynamic shared memory), but no more than `want`.
 int persistent_grid(const void* fn, long long want) {
@@ -370,8 +404,8 @@ void launch_combine_ilp(int topk, cudaStream_t s, const uint16_t* rows, const in
                         int tokens, int hidden, int n_rows, uint16_t* y) {
   const long long items = (long long)tokens * ((hidden / 8 + 31) / 32);  // one warp per item
   const CombineIlpFn fn = kCombineIlp[topk - 1];
-  fn<<<persistent_grid(reinterpret_cast<const void*>(fn), (items + 7) / 8), 256, 0, s>>>(rows, pos_of, w, tokens,
-                                                                                            hidden, n_rows, y);
+  launch_pdl(fn, persistent_grid(reinterpret_cast<const void*>(fn), (items + 7) / 8), 256, 0, s, rows, pos_of, w, tokens,
+             hidden, n_rows, y);
 }
 
 int grid_for(int items, int per_cta) {
@@ -442,11 +476,11 @@ extern "C" hocResult_t hoc_ep_pack(const int32_t* expert_ids, const void* x, int
     int32_t* total = workspace;
     int32_t* hist = workspace + experts;
     int32_t* nvalid = hist + size_t(tiles) * experts;
-    ep_tile_hist_kernel<<<tiles, kEpThreads, sizeof(int) * size_t(experts), s>>>(expert_ids, n, experts, hist);
-    ep_scan_kernel<<<1, 1024, 0, s>>>(hist, tiles, experts, total, nvalid,
-                                      reinterpret_cast<unsigned long long*>(dst_counts), nranks, experts / nranks, hidden);
-    ep_tile_place_kernel<<<tiles, kEpThreads, sizeof(int) * size_t(kEpWarps) * experts, s>>>(
-        expert_ids, n, experts, hist, nvalid, perm, pos_of);
+    launch_pdl(ep_tile_hist_kernel, tiles, kEpThreads, sizeof(int) * size_t(experts), s, expert_ids, n, experts, hist);
+    launch_pdl(ep_scan_kernel, 1, 1024, 0, s, hist, tiles, experts, total, nvalid,
+               reinterpret_cast<unsigned long long*>(dst_counts), nranks, experts / nranks, hidden);
+    launch_pdl(ep_tile_place_kernel, tiles, kEpThreads, sizeof(int) * size_t(kEpWarps) * experts, s, expert_ids, n,
+               experts, static_cast<const int32_t*>(hist), static_cast<const int32_t*>(nvalid), perm, pos_of);
   } else {
     // many experts: one CTA per expert scanning every pair
     if (cudaMemsetAsync(perm, 0xFF, sizeof(int32_t) * size_t(n), s) != cudaSuccess ||
@@ -461,8 +495,9 @@ extern "C" hocResult_t hoc_ep_pack(const int32_t* expert_ids, const void* x, int
   const int hb = hidden * 2;
   const int vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(send)) & 15u) == 0 && hb % 16 == 0;
   const long long gather_warps = vec ? (long long)n * ((hb / 16 + kGatherSliceVecs - 1) / kGatherSliceVecs) : n;
-  ep_gather_kernel<<<persistent_grid(reinterpret_cast<const void*>(&ep_gather_kernel), (gather_warps + 7) / 8), 256, 0,
-                     s>>>(static_cast<const char*>(x), perm, n, topk, hb, static_cast<char*>(send), vec);
+  launch_pdl(ep_gather_kernel, persistent_grid(reinterpret_cast<const void*>(&ep_gather_kernel), (gather_warps + 7) / 8),
+             256, 0, s, static_cast<const char*>(x), static_cast<const int32_t*>(perm), n, topk, hb,
+             static_cast<char*>(send), int(vec));
   return cudaGetLastError() == cudaSuccess ? HOC_SUCCESS : HOC_ERR_CUDA;
 }
 
