@@ -72,6 +72,7 @@ std::string plan_key(const CallShape& s) {
   put(&s.src_rank, sizeof s.src_rank);
   put(&s.dst_rank, sizeof s.dst_rank);
   put(&s.path, sizeof s.path);
+  put(&s.chunk, sizeof s.chunk);
   const size_t nc = s.counts.size();
   put(&nc, sizeof nc);
   if (nc) put(s.counts.data(), nc * sizeof(size_t));
@@ -372,7 +373,9 @@ hocResult_t plan_sendrecv(const Cfg& cfg, const CallShape& s, Plan* p) {
 
 }  // namespace
 
-hocResult_t build_plan(const Cfg& cfg, const CallShape& s, Plan* p) {
+hocResult_t build_plan(const Cfg& base, const CallShape& s, Plan* p) {
+  Cfg cfg = base;
+  if (s.chunk) cfg.chunk_bytes = s.chunk;
   *p = Plan();
   p->op = s.op;
   p->k = s.k;

@@ -95,6 +95,7 @@ struct CallShape {
   std::vector<size_t> sdispls, rdispls;
   int src_rank = 0, dst_rank = 0;  // sendrecv
   int path = -1;                   // allreduce: path override (-1: the communicator's)
+  size_t chunk = 0;                // chunk override in bytes (0: the communicator's)
 };
 
 size_t dtype_bytes(int dtype);
