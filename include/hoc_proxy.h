@@ -14,7 +14,9 @@
  * the device (for example by an expert-routing kernel).  The counts travel to
  * the proxy through the handshake; the proxy plans the exchange (shift stages
  * and flow-size-aware chunk interleave, as hoc_alltoall) and issues it on copy
- * engines.  A watchdog in the proxy always writes the finish value, so no
+ * engines, in chunks of at least total bytes / 96 so that issuing the copies,
+ * which starts only when the stream reaches the flag, takes no longer than
+ * moving them.  A watchdog in the proxy always writes the finish value, so no
  * stream waits forever: if the moves do not complete within the deadline, or
  * the counts are invalid, the stream is released and hoc_proxy_status() /
  * hoc_wait() report the error.  The flags live in mapped pinned host memory
