@@ -70,6 +70,7 @@ struct hocComm {
   int prof_streams = 0;  // copy streams the last profiled call used (0: none)
   int reduce_ctas_per_sm[3][hoc::kMaxRanks + 1][2] = {};
   hoc::Proxy* proxy = nullptr;  // created by the first device-count all-to-all
+  unsigned detached_next = 0;   // copy stream of the next hoc_sendrecv_async
   void* host_ar = nullptr;      // staging and streams of hoc_allreduce_host (host_ar.cpp)
 };
 

@@ -654,6 +654,46 @@ hocResult_t run(hocComm* c, const CallShape& shape, const Bind& bd, void* stream
   return execute(c, shape, bd, static_cast<cudaStream_t>(stream));
 }
 
+// The plan on one of the caller stream's copy streams: it waits for the work
+// before the call on `stream`, and `done` is recorded when it completes;
+// `stream` itself is not joined.
+hocResult_t run_detached(hocComm* c, const CallShape& shape, const Bind& bd, void* stream, void* done) {
+  NvtxRange range("hoc_sendrecv_async");
+  std::lock_guard<std::mutex> lock(c->mu);
+  DeviceGuard g(c->device);
+  if (!g.ok) {
+    set_detail("cudaSetDevice failed");
+    return HOC_ERR_CUDA;
+  }
+  cudaStream_t s0 = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  HOC_CK(cudaStreamIsCapturing(s0, &cs));
+  if (cs != cudaStreamCaptureStatusNone) {
+    set_detail("hoc_sendrecv_async cannot be captured into a graph (its copy is not joined to the stream)");
+    return HOC_ERR_UNSUPPORTED;
+  }
+  const Plan* pp = nullptr;
+  HOC_TRY(get_plan(c, shape, &pp));
+  std::vector<cudaStream_t>* copy = nullptr;
+  HOC_TRY(copy_streams_for(c, s0, &copy));
+  cudaStream_t cs0 = (*copy)[c->detached_next++ % copy->size()];  // spread consecutive sends over the queues
+  HOC_CK(cudaEventRecord(c->fork, s0));
+  HOC_CK(cudaStreamWaitEvent(cs0, c->fork, 0));
+  int max_ctas = 0;
+  HOC_TRY(issue(c, *pp, bd, cs0, copy, &max_ctas));
+  HOC_CK(cudaEventRecord(static_cast<cudaEvent_t>(done), cs0));
+  hocOpStats_t stats{};
+  stats.path = pp->path;
+  stats.kernels = pp->kernels;
+  stats.copies = pp->copies;
+  stats.bytes_exec = pp->bytes_exec;
+  stats.bytes_min = pp->bytes_min;
+  stats.max_ctas = max_ctas;
+  stats.sms_used = std::min(max_ctas, c->sms);
+  c->last = stats;
+  return HOC_SUCCESS;
+}
+
 // hoc_allreduce with the plan's path set by `path` (-1: the communicator's).
 hocResult_t allreduce_on(hocComm_t comm, const void* const* send, void* const* recv, size_t count,
                          hocDataType_t dtype, hocRedOp_t op, void* stream, int path) {
@@ -683,6 +723,46 @@ hocResult_t allreduce_on(hocComm_t comm, const void* const* send, void* const* r
     bd.recv[r] = recv[r];
   }
   return run(comm, s, bd, stream);
+}
+hocResult_t sendrecv_shape(hocComm_t comm, int src_rank, const void* send, int dst_rank, void* recv, size_t count,
+                           hocDataType_t dtype, CallShape* out, Bind* bind, bool* nothing) {
+  *nothing = false;
+  if (!comm) return HOC_ERR_NOT_INITIALIZED;
+  if (!dtype_ok(dtype, false)) {
+    set_detail("unknown dtype");
+    return HOC_ERR_INVALID_ARG;
+  }
+  if (src_rank < 0 || src_rank >= comm->k || dst_rank < 0 || dst_rank >= comm->k) {
+    set_detail("rank out of range");
+    return HOC_ERR_INVALID_ARG;
+  }
+  if (count == 0) {
+    *nothing = true;
+    return HOC_SUCCESS;
+  }
+  const size_t b = dtype_bytes(dtype);
+  if (!send || !recv || !elem_aligned(send, b) || !elem_aligned(recv, b)) {
+    set_detail("NULL or misaligned buffer");
+    return HOC_ERR_INVALID_ARG;
+  }
+  if (send == recv) {
+    *nothing = true;
+    return HOC_SUCCESS;
+  }
+  const uintptr_t a = U(send), d = U(recv);
+  if (a < d + count * b && d < a + count * b) {
+    set_detail("send and recv overlap");
+    return HOC_ERR_INVALID_ARG;
+  }
+  out->op = HOC_OP_SENDRECV;
+  out->k = comm->k;
+  out->dtype = dtype;
+  out->count = count;
+  out->src_rank = src_rank;
+  out->dst_rank = dst_rank;
+  bind->send[src_rank] = send;
+  bind->recv[dst_rank] = recv;
+  return HOC_SUCCESS;
 }
 }  // namespace
 
@@ -915,39 +995,32 @@ hocResult_t hoc_alltoall(hocComm_t comm, const void* const* send, const size_t* 
 
 hocResult_t hoc_sendrecv(hocComm_t comm, int src_rank, const void* send, int dst_rank, void* recv, size_t count,
                          hocDataType_t dtype, void* stream) {
-  if (!comm) return HOC_ERR_NOT_INITIALIZED;
-  if (!dtype_ok(dtype, false)) {
-    set_detail("unknown dtype");
-    return HOC_ERR_INVALID_ARG;
-  }
-  if (src_rank < 0 || src_rank >= comm->k || dst_rank < 0 || dst_rank >= comm->k) {
-    set_detail("rank out of range");
-    return HOC_ERR_INVALID_ARG;
-  }
-  if (count == 0) return HOC_SUCCESS;
-  const size_t b = dtype_bytes(dtype);
-  if (!send || !recv || !elem_aligned(send, b) || !elem_aligned(recv, b)) {
-    set_detail("NULL or misaligned buffer");
-    return HOC_ERR_INVALID_ARG;
-  }
-  if (send == recv) return HOC_SUCCESS;
-  const uintptr_t a = U(send), d = U(recv);
-  if (a < d + count * b && d < a + count * b) {
-    set_detail("send and recv overlap");
+  CallShape s;
+  Bind bd;
+  bool nothing = false;
+  HOC_TRY(sendrecv_shape(comm, src_rank, send, dst_rank, recv, count, dtype, &s, &bd, &nothing));
+  if (nothing) return HOC_SUCCESS;
+  return run(comm, s, bd, stream);
+}
+
+hocResult_t hoc_sendrecv_async(hocComm_t comm, int src_rank, const void* send, int dst_rank, void* recv, size_t count,
+                               hocDataType_t dtype, void* stream, void* done_event) {
+  if (comm && !done_event) {
+    set_detail("hoc_sendrecv_async: NULL done_event");
     return HOC_ERR_INVALID_ARG;
   }
   CallShape s;
-  s.op = HOC_OP_SENDRECV;
-  s.k = comm->k;
-  s.dtype = dtype;
-  s.count = count;
-  s.src_rank = src_rank;
-  s.dst_rank = dst_rank;
   Bind bd;
-  bd.send[src_rank] = send;
-  bd.recv[dst_rank] = recv;
-  return run(comm, s, bd, stream);
+  bool nothing = false;
+  HOC_TRY(sendrecv_shape(comm, src_rank, send, dst_rank, recv, count, dtype, &s, &bd, &nothing));
+  if (nothing) {  // nothing to move: the event completes with the work before the call
+    DeviceGuard g(comm->device);
+    HOC_CK(cudaEventRecord(static_cast<cudaEvent_t>(done_event), static_cast<cudaStream_t>(stream)));
+    return HOC_SUCCESS;
+  }
+  return run_detached(comm, s, bd, stream, done_event);
 }
+
 
 hocResult_t hoc_wait(hocComm_t comm, void* stream, int timeout_ms) {
   if (!comm) return HOC_ERR_NOT_INITIALIZED;

@@ -72,6 +72,8 @@ _SIGS = {
                                C.POINTER(C.c_void_p), C.POINTER(C.c_size_t), C.c_size_t, C.c_int, C.c_void_p]),
     "hoc_sendrecv": (C.c_int, [C.c_void_p, C.c_int, C.c_void_p, C.c_int, C.c_void_p, C.c_size_t, C.c_int,
                                C.c_void_p]),
+    "hoc_sendrecv_async": (C.c_int, [C.c_void_p, C.c_int, C.c_void_p, C.c_int, C.c_void_p, C.c_size_t, C.c_int,
+                                     C.c_void_p, C.c_void_p]),
     "hoc_wait": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int]),
     "hoc_last_stats": (C.c_int, [C.c_void_p, C.POINTER(_Stats)]),
     "hoc_profile_enable": (C.c_int, [C.c_void_p, C.c_int]),
@@ -280,6 +282,20 @@ class Comm:
         dtype = _dtype_code(send) if dtype is None else dtype
         _check(lib().hoc_sendrecv(self._h, int(src_rank), _ptr(send), int(dst_rank), _ptr(recv), count, dtype,
                                   _stream(stream)), "hoc_sendrecv")
+
+    def sendrecv_async(self, src_rank, send, dst_rank, recv, count=None, dtype=None, stream=None, done=None):
+        """Send/recv completed by an event, not by `stream`: returns the torch.cuda.Event (`done`, or a new
+        one) that the consumer waits on; later work on `stream` does not wait for the copy."""
+        import torch
+        count = send.numel() if count is None else count
+        dtype = _dtype_code(send) if dtype is None else dtype
+        if done is None:
+            done = torch.cuda.Event()
+        if not done.cuda_event:
+            done.record(torch.cuda.current_stream() if stream is None else stream)   # creates the CUDA event
+        _check(lib().hoc_sendrecv_async(self._h, int(src_rank), _ptr(send), int(dst_rank), _ptr(recv), count, dtype,
+                                        _stream(stream), C.c_void_p(done.cuda_event)), "hoc_sendrecv_async")
+        return done
 
     def alltoall_device_counts(self, send, recv, d_counts, recv_capacity, dtype=None, stream=None,
                                transpose: bool = False):

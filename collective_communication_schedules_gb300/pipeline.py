@@ -5,9 +5,14 @@ transfers of one micro-batch with the forward or backward compute of another,
 which is why its communication runs beside compute kernels.  Each stage here
 has its own CUDA stream; a stage's compute is the FMA probe (its SM budget)
 plus an exact XOR transform of the payload, and every activation / gradient
-hand-off is one hoc_sendrecv from the producing stage's buffer into the
+hand-off is one send/recv from the producing stage's buffer into the
 consuming stage's buffer (section 3.3.2, direct copy into the receiver).
-Cross-stage order uses CUDA events only.
+Cross-stage order uses CUDA events only.  With sends="event" (the default)
+each hand-off is hoc_sendrecv_async: the copy waits for the producing
+compute, runs on a copy stream and completes an event the consumer waits on,
+so the producing stage goes on computing while the copy engine moves the
+data (section 3.2); with sends="stream" it is hoc_sendrecv on the producing
+stage's stream, which then waits for the copy before its next compute.
 
 The schedule: stage s of p runs min(p - s - 1, m) warm-up forwards, then
 alternates forward and backward, then drains its backwards.
@@ -39,9 +44,12 @@ class Pipeline1F1B:
     """Buffers and streams for p stages x m micro-batches of `elems` bf16 values."""
 
     def __init__(self, comm: hoc.Comm, p: int, m: int, elems: int, keys, probe_ctas: int = 0,
-                 probe_iters: int = 0, device: int = 0, sentinel: int = 0xA5A5):
+                 probe_iters: int = 0, device: int = 0, sentinel: int = 0xA5A5, sends: str = "event"):
         if comm.k < p:
             raise ValueError("the communicator needs one simulated rank per stage")
+        if sends not in ("event", "stream"):
+            raise ValueError("sends is 'event' or 'stream'")
+        self.sends = sends
         self.comm, self.p, self.m, self.elems = comm, p, m, elems
         self.keys = [[(int(keys[s][i][0]), int(keys[s][i][1])) for i in range(m)] for s in range(p)]
         self.probe_ctas, self.probe_iters = probe_ctas, probe_iters
@@ -75,12 +83,7 @@ class Pipeline1F1B:
         if s > 0:
             st.wait_event(self.sent_f[s - 1][i])
         self._compute(s, self.act_in[s][i], self.act_out[s][i], self.keys[s][i][0], 1)
-        if s + 1 < self.p:
-            self.comm.sendrecv(s, self.act_out[s][i], s + 1, self.act_in[s + 1][i], self.elems, hoc.BFLOAT16,
-                               stream=st)
-        ev = torch.cuda.Event()
-        ev.record(st)
-        self.sent_f[s][i] = ev
+        self.sent_f[s][i] = self._send(st, s, self.act_out[s][i], s + 1, self.act_in[s + 1][i] if s + 1 < self.p else None)
 
     def _backward(self, s, i):
         st = self.streams[s]
@@ -90,12 +93,20 @@ class Pipeline1F1B:
         else:
             src = self.act_out[s][i]         # the last stage starts from its own forward output
         self._compute(s, src, self.grad_out[s][i], self.keys[s][i][1], 2)
-        if s > 0:
-            self.comm.sendrecv(s, self.grad_out[s][i], s - 1, self.grad_in[s - 1][i], self.elems, hoc.BFLOAT16,
-                               stream=st)
+        self.sent_b[s][i] = self._send(st, s, self.grad_out[s][i], s - 1, self.grad_in[s - 1][i] if s > 0 else None)
+
+    def _send(self, st, s, src, d, dst):
+        """Hand `src` to stage d's `dst` after stage s's work so far; returns the event its consumer waits on
+        (the stage's own progress when there is nothing to send)."""
         ev = torch.cuda.Event()
-        ev.record(st)
-        self.sent_b[s][i] = ev
+        if dst is None:
+            ev.record(st)
+        elif self.sends == "event":
+            self.comm.sendrecv_async(s, src, d, dst, self.elems, hoc.BFLOAT16, stream=st, done=ev)
+        else:
+            self.comm.sendrecv(s, src, d, dst, self.elems, hoc.BFLOAT16, stream=st)
+            ev.record(st)
+        return ev
 
     def issue(self, origin: torch.cuda.Stream | None = None):
         """Issue every stage's operations; an operation is issued once the

@@ -178,6 +178,20 @@ hocResult_t hoc_alltoall(hocComm_t comm, const void* const* send, const size_t* 
 hocResult_t hoc_sendrecv(hocComm_t comm, int src_rank, const void* send, int dst_rank, void* recv,
                          size_t count, hocDataType_t dtype, void* stream);
 
+/* Send/recv whose completion is signalled by an event instead of the caller's
+ * stream (HOCCL section 3.2: the stream manager orders communication against
+ * the kernels around it with events).  The copy waits for the work issued on
+ * `stream` before this call, runs on one of the communicator's copy streams
+ * (consecutive calls rotate over them) and records `done_event`, a
+ * cudaEvent_t the caller created, when the data is in `recv`.  Later work on
+ * `stream` does NOT wait for it, so the sender keeps computing while the copy
+ * engine moves the data; consumers wait on `done_event`.  The caller leaves
+ * `send` unchanged and does not touch `recv` until `done_event` has completed.
+ * With nothing to move, `done_event` is recorded on `stream`.  Not allowed
+ * while `stream` is being captured into a graph (HOC_ERR_UNSUPPORTED). */
+hocResult_t hoc_sendrecv_async(hocComm_t comm, int src_rank, const void* send, int dst_rank, void* recv,
+                               size_t count, hocDataType_t dtype, void* stream, void* done_event);
+
 /* Bounded host wait: polls until all work on `stream` (and the communicator's
  * internal streams) has finished, or `timeout_ms` ms pass (HOC_ERR_TIMEOUT).
  * Also reports device-side timeouts of the TMA copy kernel (HOC_ERR_TIMEOUT). */

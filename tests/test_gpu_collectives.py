@@ -376,3 +376,28 @@ def test_two_host_threads_share_a_communicator():
         for t in th:
             t.join()
     assert not errors, errors
+
+
+@pytest.mark.parametrize("path", ["ce", "tma"])
+def test_sendrecv_async_completes_by_event(path):
+    # The copy waits for the work before the call on the sender's stream and
+    # completes `done`; a consumer on another stream waits on `done` alone.
+    k, n = 4, (96 << 20) // 2 + 77                      # above 64 MiB: chunks striped over the copy queues
+    xs = inputs.rank_inputs("bfloat16", k, n, workload=9, slot=3)
+    with _comm(k, path) as c:
+        prod, cons = torch.cuda.Stream(), torch.cuda.Stream()
+        src = torch.zeros(n, dtype=torch.bfloat16, device="cuda")
+        dst = torch.full((n,), -1, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+        x = to_device(xs[1], "bfloat16")
+        with torch.cuda.stream(prod):
+            src.copy_(x)                                    # the producer writes the message ...
+        done = c.sendrecv_async(1, src, 2, dst, stream=prod)   # ... which the copy waits for
+        out = torch.empty_like(dst)
+        cons.wait_event(done)
+        with torch.cuda.stream(cons):
+            out.copy_(dst)                                  # the consumer sees the message
+        torch.cuda.synchronize()
+        assert_bits_equal(to_host(out, "bfloat16"), xs[1], "bfloat16", f"sendrecv_async {path}")
+        # nothing to move: the event still completes
+        e = c.sendrecv_async(0, src[:0], 1, dst[:0], stream=prod)
+        e.synchronize()

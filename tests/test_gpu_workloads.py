@@ -136,7 +136,8 @@ def test_bucket_stream_reduce_scatter_workload(budget, engine):
 
 # ------------------------------------------------------------------ workload 4
 @pytest.mark.parametrize("path", ["ce", "tma"])
-def test_pipeline_1f1b_workload(path):
+@pytest.mark.parametrize("sends", ["event", "stream"])
+def test_pipeline_1f1b_workload(path, sends):
     w = inputs.PP_STAGES
     p, m = w["p"], w["microbatches"]
     elems = w["seq"] * w["hidden"]
@@ -145,7 +146,7 @@ def test_pipeline_1f1b_workload(path):
     want, _ = o_pp.simulate(xs, keys, p, m)
     sms = hoc.sm_count()
     with hoc.Comm(p, 0, hoc.Config(path=path)) as c:
-        pipe = Pipeline1F1B(c, p, m, elems, keys, probe_ctas=2 * sms, probe_iters=2000)
+        pipe = Pipeline1F1B(c, p, m, elems, keys, probe_ctas=2 * sms, probe_iters=2000, sends=sends)
         pipe.load([to_device(x, "bfloat16") for x in xs])
         pipe.issue()
         torch.cuda.synchronize()
