@@ -427,8 +427,9 @@ def leg_pipeline(sms):
         with hoc.Comm(p, torch.cuda.current_device(), hoc.Config(path=path)) as c:
             res = {}
             # sends completed by events (the sender keeps computing), sends on the sender's stream, no sends
-            for label, mode in (("event_sends", "event"), ("stream_sends", "stream"), ("compute_only", None)):
-                pipe = Pipeline1F1B(c, p, m, elems, keys, probe_ctas=2 * sms, probe_iters=2000, sends=mode or "event")
+            for label, mode in (("pull_sends", "pull"), ("event_sends", "event"), ("stream_sends", "stream"),
+                                ("compute_only", None)):
+                pipe = Pipeline1F1B(c, p, m, elems, keys, probe_ctas=2 * sms, probe_iters=2000, sends=mode or "stream")
                 if mode is None:
                     pipe.comm = _NoSend()
                 runs = []
@@ -447,6 +448,7 @@ def leg_pipeline(sms):
             sends = 2 * (p - 1) * m
             res["sends"] = sends
             res["send_bytes"] = sends * elems * 2
+            res["exposed_ms_pull_sends"] = round(res["pull_sends_ms"] - res["compute_only_ms"], 3)
             res["exposed_ms_event_sends"] = round(res["event_sends_ms"] - res["compute_only_ms"], 3)
             res["exposed_ms_stream_sends"] = round(res["stream_sends_ms"] - res["compute_only_ms"], 3)
             out[path] = res

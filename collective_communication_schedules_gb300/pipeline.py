@@ -7,12 +7,14 @@ has its own CUDA stream; a stage's compute is the FMA probe (its SM budget)
 plus an exact XOR transform of the payload, and every activation / gradient
 hand-off is one send/recv from the producing stage's buffer into the
 consuming stage's buffer (section 3.3.2, direct copy into the receiver).
-Cross-stage order uses CUDA events only.  With sends="event" (the default)
-each hand-off is hoc_sendrecv_async: the copy waits for the producing
-compute, runs on a copy stream and completes an event the consumer waits on,
-so the producing stage goes on computing while the copy engine moves the
-data (section 3.2); with sends="stream" it is hoc_sendrecv on the producing
-stage's stream, which then waits for the copy before its next compute.
+Cross-stage order uses CUDA events only.  Three ways to hand over a buffer:
+sends="stream": hoc_sendrecv on the producing stage's stream, which then
+waits for the copy before its next compute; sends="event":
+hoc_sendrecv_async, the copy runs on a copy stream and completes an event the
+consumer waits on (the producer is not held, but the hand-off crosses two
+stream dependencies); sends="pull" (the default): the consuming stage waits
+for the producer's compute and issues the copy on its own stream, so the
+producer is not held and the hand-off crosses one dependency.
 
 The schedule: stage s of p runs min(p - s - 1, m) warm-up forwards, then
 alternates forward and backward, then drains its backwards.
@@ -44,11 +46,11 @@ class Pipeline1F1B:
     """Buffers and streams for p stages x m micro-batches of `elems` bf16 values."""
 
     def __init__(self, comm: hoc.Comm, p: int, m: int, elems: int, keys, probe_ctas: int = 0,
-                 probe_iters: int = 0, device: int = 0, sentinel: int = 0xA5A5, sends: str = "event"):
+                 probe_iters: int = 0, device: int = 0, sentinel: int = 0xA5A5, sends: str = "pull"):
         if comm.k < p:
             raise ValueError("the communicator needs one simulated rank per stage")
-        if sends not in ("event", "stream"):
-            raise ValueError("sends is 'event' or 'stream'")
+        if sends not in ("pull", "event", "stream"):
+            raise ValueError("sends is 'pull', 'event' or 'stream'")
         self.sends = sends
         self.comm, self.p, self.m, self.elems = comm, p, m, elems
         self.keys = [[(int(keys[s][i][0]), int(keys[s][i][1])) for i in range(m)] for s in range(p)]
@@ -82,6 +84,9 @@ class Pipeline1F1B:
         st = self.streams[s]
         if s > 0:
             st.wait_event(self.sent_f[s - 1][i])
+            if self.sends == "pull":
+                self.comm.sendrecv(s - 1, self.act_out[s - 1][i], s, self.act_in[s][i], self.elems, hoc.BFLOAT16,
+                                   stream=st)
         self._compute(s, self.act_in[s][i], self.act_out[s][i], self.keys[s][i][0], 1)
         self.sent_f[s][i] = self._send(st, s, self.act_out[s][i], s + 1, self.act_in[s + 1][i] if s + 1 < self.p else None)
 
@@ -89,6 +94,9 @@ class Pipeline1F1B:
         st = self.streams[s]
         if s + 1 < self.p:
             st.wait_event(self.sent_b[s + 1][i])
+            if self.sends == "pull":
+                self.comm.sendrecv(s + 1, self.grad_out[s + 1][i], s, self.grad_in[s][i], self.elems, hoc.BFLOAT16,
+                                   stream=st)
             src = self.grad_in[s][i]
         else:
             src = self.act_out[s][i]         # the last stage starts from its own forward output
@@ -99,7 +107,7 @@ class Pipeline1F1B:
         """Hand `src` to stage d's `dst` after stage s's work so far; returns the event its consumer waits on
         (the stage's own progress when there is nothing to send)."""
         ev = torch.cuda.Event()
-        if dst is None:
+        if dst is None or self.sends == "pull":       # pull: the consumer issues the copy after this event
             ev.record(st)
         elif self.sends == "event":
             self.comm.sendrecv_async(s, src, d, dst, self.elems, hoc.BFLOAT16, stream=st, done=ev)

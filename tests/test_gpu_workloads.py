@@ -136,7 +136,7 @@ def test_bucket_stream_reduce_scatter_workload(budget, engine):
 
 # ------------------------------------------------------------------ workload 4
 @pytest.mark.parametrize("path", ["ce", "tma"])
-@pytest.mark.parametrize("sends", ["event", "stream"])
+@pytest.mark.parametrize("sends", ["pull", "event", "stream"])
 def test_pipeline_1f1b_workload(path, sends):
     w = inputs.PP_STAGES
     p, m = w["p"], w["microbatches"]
