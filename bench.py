@@ -253,6 +253,23 @@ def cpu_baseline(xs_host, seconds: float, device_out=None):
     return out
 
 
+def cpu_baseline_buckets(host_pool, buckets: int = 2):
+    """The oracle's reduce-scatter on the first `buckets` of the DP stream's 16 pool buckets, timed on
+    the host, and the per-bucket time scaled to the stream's 268 buckets (labelled as scaled)."""
+    from oracle import ring
+
+    k, be = K_RANKS, 13_107_200
+    t0 = time.perf_counter()
+    for s in range(buckets):
+        ring.reduce_scatter([host_pool[s * k + r] for r in range(k)], be // k, "bfloat16")
+    per = (time.perf_counter() - t0) / buckets
+    return {"kind": "oracle", "cores": 1, "ms_per_bucket": round(per * 1e3, 2),
+            "ms_total_scaled": round(per * 268 * 1e3, 1),
+            "rs_bus_gbs": round((k - 1) / k * be * 2 / per / 1e9, 3),
+            "sample": f"{buckets} of the 16 pool buckets (8 ranks x 13,107,200 bf16 each), timed, total scaled "
+                      f"x268/{buckets}"}
+
+
 def run_reference(args, world, rank):
     """--impl reference: the oracle as the reference arm (rank 0 only)."""
     if rank != 0:
@@ -886,6 +903,7 @@ def run_ours(args, world, rank, local):
         extras["workloads"] = {"dp_bucket_stream": leg_bucket_stream(bucket_pool, sms, peak),
                                "pp_1f1b": leg_pipeline(sms),
                                "ep_dispatch_combine": leg_expert_dispatch(peak)}
+        extras["workloads"]["dp_bucket_stream"]["cpu_baseline"] = cpu_baseline_buckets(bucket_pool)
         bucket_pool = None
         extras["sweeps"] = leg_sweeps(sms)
         extras["host_overhead_us"] = leg_host_overhead()
