@@ -31,7 +31,7 @@ def _comm(k, path="auto", **kw):
 
 
 @pytest.mark.parametrize("dtype", ["int32", "float32", "bfloat16"])
-@pytest.mark.parametrize("k", [1, 2, 3, 4, 8])
+@pytest.mark.parametrize("k", [1, 2, 3, 4, 8, 16])
 @pytest.mark.parametrize("path,engine", [("ce", "lsu"), ("tma", "lsu"), ("fused", "lsu"), ("fused", "tma"),
                                          ("ce", "tma")])
 def test_allreduce_parity(dtype, k, path, engine):
@@ -113,7 +113,7 @@ def test_reduce_scatter_parity(dtype, k, engine, budget):
 
 
 @pytest.mark.parametrize("path", ["ce", "tma"])
-@pytest.mark.parametrize("k", [1, 2, 5, 8])
+@pytest.mark.parametrize("k", [1, 2, 5, 8, 16])
 def test_allgather_parity(path, k):
     for sc in (1, 13, 50003):
         xs = inputs.rank_inputs("bfloat16", k, sc, workload=8, slot=k)
@@ -142,7 +142,7 @@ def test_allgather_parity(path, k):
                 assert_bits_equal(full[r].host(), want[r], "bfloat16", f"ag in place {path} rank {r}")
 
 
-@pytest.mark.parametrize("k", [3, 8])
+@pytest.mark.parametrize("k", [3, 8, 16])
 def test_tma_broadcast_with_mixed_destination_alignment(k):
     # The TMA path loads each source block once and stores it to every
     # destination; destinations in another 16-byte alignment class than the
@@ -171,7 +171,7 @@ def test_tma_broadcast_with_mixed_destination_alignment(k):
 @pytest.mark.parametrize("stage_sync", [True, False])
 def test_alltoallv_parity(path, interleave, stage_sync):
     rng = np.random.default_rng(11)
-    for k in (1, 2, 5, 8):
+    for k in (1, 2, 5, 8, 16):
         counts = rng.integers(0, 3000, size=(k, k))
         counts[0, :] = 0 if k > 1 else counts[0, :]
         sends = [rng.integers(0, 1 << 16, size=int(counts[s].sum())).astype(np.uint16) for s in range(k)]
