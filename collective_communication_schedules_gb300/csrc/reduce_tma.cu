@@ -7,12 +7,13 @@
 //   * one producer thread per CTA streams the k operand tiles of a work tile
 //     (tile_bytes each, operand j = ring position j) into a shared-memory
 //     stage with cp.async.bulk, completing on that stage's "full" mbarrier;
-//   * four consumer warps fold the k tiles element by element from shared
-//     memory into an output tile, release the stage on its "empty" mbarrier,
-//     and one consumer thread bulk-stores the output tile to the owner's
-//     buffer (or to all k buffers: the fused allreduce);
-//   * stages cycle, so several tiles of loads are in flight per SM while the
-//     consumers work and earlier stores drain.
+//   * four consumer warps fold the k tiles vector by vector from shared
+//     memory, store each folded 16-byte vector straight to the owner's buffer
+//     (or to all k buffers: the fused allreduce, with streaming stores), and
+//     release the stage on its "empty" mbarrier;
+//   * stages cycle, so up to ~190 KiB of operand loads are in flight per SM
+//     while the consumers fold -- more than per-thread loads can keep in
+//     registers, which is what an SM budget needs.
 // One CTA per SM (persistent over tiles).  Only the 16-byte-aligned body of
 // each segment moves by bulk copies; the few elements before the first
 // aligned element and after the last whole vector go through plain loads.
@@ -27,10 +28,9 @@
 namespace hoc {
 namespace {
 
-constexpr int kConsumerWarps = 4;
+constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kThreadsT = kConsumers + 32;  // + one producer warp
-constexpr int kOutBufs = 2;
 
 __device__ __forceinline__ uint32_t sa(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 __device__ __forceinline__ uint64_t now_ns() {
@@ -68,14 +68,6 @@ __device__ __forceinline__ void bulk_g2s(void* s, const void* g, uint32_t n, uin
                "l"(g), "r"(n), "r"(sa(b))
                : "memory");
 }
-__device__ __forceinline__ void bulk_s2g(void* g, const void* s, uint32_t n) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(g), "r"(sa(s)), "r"(n) : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // Barrier over the consumer warps that also ORs a predicate: every consumer
 // gets the same answer, so they leave the loop together.
 __device__ __forceinline__ bool consumers_sync_or(bool v) {
@@ -153,9 +145,59 @@ __device__ __forceinline__ void scalar_elem(const ReduceParams& p, const uint8_t
   }
 }
 
-// Fold one 16-byte vector position of the k tiles in a stage.
+// Fold one 16-byte vector position of the k tiles in a stage.  K > 0: the
+// rank count is a compile-time constant and all K shared-memory loads are
+// issued before the adds; K == 0: runtime k.
+template <int K>
 __device__ __forceinline__ uint4 fold_vec(const unsigned char* stage, uint32_t tile_bytes, int k, uint32_t off,
                                           int dtype) {
+  if constexpr (K > 0) {
+    uint4 v[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) v[j] = *reinterpret_cast<const uint4*>(stage + size_t(j) * tile_bytes + off);
+    if (dtype == HOC_BFLOAT16) {
+      float a[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t w = (&v[0].x)[i];
+        a[2 * i] = __uint_as_float(w << 16);
+        a[2 * i + 1] = __uint_as_float(w & 0xFFFF0000u);
+      }
+#pragma unroll
+      for (int j = 1; j < K; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t w = (&v[j].x)[i];
+          a[2 * i] = __fadd_rn(a[2 * i], __uint_as_float(w << 16));
+          a[2 * i + 1] = __fadd_rn(a[2 * i + 1], __uint_as_float(w & 0xFFFF0000u));
+        }
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        o[i] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(a[2 * i]))) |
+               (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(a[2 * i + 1]))) << 16);
+      return make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (dtype == HOC_FLOAT32) {
+      float a[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = __uint_as_float((&v[0].x)[i]);
+#pragma unroll
+      for (int j = 1; j < K; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = __fadd_rn(a[i], __uint_as_float((&v[j].x)[i]));
+      return make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]), __float_as_uint(a[3]));
+    }
+    uint4 x = v[0];
+#pragma unroll
+    for (int j = 1; j < K; ++j) {
+      x.x += v[j].x;
+      x.y += v[j].y;
+      x.z += v[j].z;
+      x.w += v[j].w;
+    }
+    return x;
+  }
   const uint4* t0 = reinterpret_cast<const uint4*>(stage + off);
   uint4 x = *t0;
   if (dtype == HOC_BFLOAT16) {
@@ -227,6 +269,7 @@ __device__ __forceinline__ void tile_body(const ReduceParams& p, const ReduceSeg
   n = off_b >= body_bytes ? 0u : uint32_t(body_bytes - off_b < tile_bytes ? body_bytes - off_b : tile_bytes);
 }
 
+template <int K>
 __global__ void __launch_bounds__(kThreadsT, 1)
     reduce_tma_kernel(const __grid_constant__ ReduceParams p, uint32_t tile_bytes, int stages, int* status,
                       uint64_t wait_ns) {
@@ -237,7 +280,6 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   const int k = p.k;
   const int eb = bytes_for(p.dtype);
   const uint32_t stage_bytes = uint32_t(k) * tile_bytes;
-  unsigned char* out_tiles = smem + size_t(stages) * stage_bytes;
   const uint64_t total = p.tile_start[p.nseg];
   const uint64_t mine = total > blockIdx.x ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -295,15 +337,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
 
   // ------------------------------------------------------------ consumers
   const int ct = threadIdx.x - 32;
-  bool prev_stored = false;  // (thread ct == 0) whether the previous tile committed a store group
   for (uint64_t it = 0; it < mine; ++it) {
     const int s = int(it % stages);
-    const int ob = int(it % kOutBufs);
-    if (ct == 0 && it >= kOutBufs) {
-      // the stores of tile it-2 must have read out buffer ob before it is rewritten
-      if (prev_stored) bulk_wait_read1();
-      else bulk_wait_read0();
-    }
     bool bad = !mb_wait(&full[s], uint32_t((it / stages) & 1), now_ns() + wait_ns);
     if (bad) atomicExch(status, kStatusTimeoutLoad);
     bad = bad || *(volatile int*)&abort_flag;
@@ -317,10 +352,16 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     uint64_t e0, off;
     uint32_t n;
     tile_body(p, sg, tr.local, tile_bytes, e0, off, n);
-    unsigned char* stage = smem + size_t(s) * stage_bytes;
-    unsigned char* ot = out_tiles + size_t(ob) * tile_bytes;
-    for (uint32_t v = uint32_t(ct) * 16; v < n; v += kConsumers * 16)
-      *reinterpret_cast<uint4*>(ot + v) = fold_vec(stage, tile_bytes, k, v, p.dtype);
+    const unsigned char* stage = smem + size_t(s) * stage_bytes;
+    const uint64_t gb = (sg.out_off + e0) * eb + off;  // byte offset of the tile in the output buffers
+    for (uint32_t v = uint32_t(ct) * 16; v < n; v += kConsumers * 16) {
+      const uint4 y = fold_vec<K>(stage, tile_bytes, k, v, p.dtype);
+      if (p.broadcast) {
+        for (int r = 0; r < k; ++r) __stcs(reinterpret_cast<uint4*>(static_cast<char*>(p.out[r]) + gb + v), y);
+      } else {
+        *reinterpret_cast<uint4*>(static_cast<char*>(p.out[sg.owner]) + gb + v) = y;
+      }
+    }
     __syncwarp();
     if (lane == 0) mb_arrive(&empty[s]);
     // head and tail elements of the segment (plain loads)
@@ -330,54 +371,60 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       const uint64_t done = e0 + tma_seg_body_vecs(sg, lanes_for(p.dtype)) * lanes_for(p.dtype);
       if (uint64_t(ct) < sg.elems - done) scalar_elem(p, seq, sg.owner, sg.elem_off + done + ct, sg.out_off + done + ct);
     }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // st.shared visible to the bulk stores
-    consumers_sync();
-    if (ct == 0) {
-      prev_stored = n != 0;
-      if (n) {
-        const uint64_t gb = (sg.out_off + e0) * eb + off;
-        if (p.broadcast) {
-          for (int r = 0; r < k; ++r) bulk_s2g(static_cast<char*>(p.out[r]) + gb, ot, n);
-        } else {
-          bulk_s2g(static_cast<char*>(p.out[sg.owner]) + gb, ot, n);
-        }
-        bulk_commit();
-      }
-    }
   }
-  if (ct == 0) bulk_wait_all();
 }
 
 }  // namespace
 
-uint32_t reduce_tma_tile_bytes(int k) { return k <= 8 ? 4096u : 2048u; }
+uint32_t reduce_tma_tile_bytes(int k) { return k <= 8 ? 8192u : 4096u; }
 
 int reduce_tma_stages(int k) {
   const uint32_t stage = uint32_t(k) * reduce_tma_tile_bytes(k);
-  const uint32_t budget = 200u * 1024u - kOutBufs * reduce_tma_tile_bytes(k);
+  const uint32_t budget = 200u * 1024u;
   int s = int(budget / stage);
   return s < 2 ? 2 : (s > 8 ? 8 : s);
 }
 
-size_t reduce_tma_smem(int k) {
-  return size_t(reduce_tma_stages(k)) * k * reduce_tma_tile_bytes(k) + kOutBufs * reduce_tma_tile_bytes(k);
-}
+size_t reduce_tma_smem(int k) { return size_t(reduce_tma_stages(k)) * k * reduce_tma_tile_bytes(k); }
 
 uint64_t reduce_tma_seg_tiles(int dtype, const ReduceSeg& s, int k) {
   return tma_seg_tiles(s, dtype, reduce_tma_tile_bytes(k));
 }
 
+namespace {
+// The kernel for rank count k: compile-time k for 2..8, runtime k otherwise.
+const void* reduce_tma_fn(int k) {
+  switch (k) {
+    case 2: return reinterpret_cast<const void*>(&reduce_tma_kernel<2>);
+    case 3: return reinterpret_cast<const void*>(&reduce_tma_kernel<3>);
+    case 4: return reinterpret_cast<const void*>(&reduce_tma_kernel<4>);
+    case 5: return reinterpret_cast<const void*>(&reduce_tma_kernel<5>);
+    case 6: return reinterpret_cast<const void*>(&reduce_tma_kernel<6>);
+    case 7: return reinterpret_cast<const void*>(&reduce_tma_kernel<7>);
+    case 8: return reinterpret_cast<const void*>(&reduce_tma_kernel<8>);
+    default: return reinterpret_cast<const void*>(&reduce_tma_kernel<0>);
+  }
+}
+}  // namespace
+
 cudaError_t reduce_tma_prepare() {
-  size_t most = 0;
+  for (int k = 1; k <= kMaxRanks + 1; ++k) {  // k = 1 and k > 8 select the runtime-k kernel
+    const cudaError_t e = cudaFuncSetAttribute(reduce_tma_fn(k), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               int(reduce_tma_smem(k > kMaxRanks ? kMaxRanks : k)));
+    if (e != cudaSuccess) return e;
+  }
+  size_t most = 0;  // the runtime-k kernel serves every k outside 2..8
   for (int k = 1; k <= kMaxRanks; ++k) most = reduce_tma_smem(k) > most ? reduce_tma_smem(k) : most;
-  return cudaFuncSetAttribute(reinterpret_cast<const void*>(&reduce_tma_kernel),
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, int(most));
+  return cudaFuncSetAttribute(reduce_tma_fn(0), cudaFuncAttributeMaxDynamicSharedMemorySize, int(most));
 }
 
 cudaError_t tma_preload() {
-  cudaFuncAttributes a;
-  const cudaError_t e = cudaFuncGetAttributes(&a, reinterpret_cast<const void*>(&reduce_tma_kernel));
-  return e != cudaSuccess ? e : tma_copy_preload();
+  for (int k = 0; k <= 8; ++k) {
+    cudaFuncAttributes a;
+    const cudaError_t e = cudaFuncGetAttributes(&a, reduce_tma_fn(k));
+    if (e != cudaSuccess) return e;
+  }
+  return tma_copy_preload();
 }
 
 cudaError_t launch_reduce_tma(const ReduceParams& p, int grid, int* status, cudaStream_t stream) {
@@ -386,8 +433,7 @@ cudaError_t launch_reduce_tma(const ReduceParams& p, int grid, int* status, cuda
   int stages = reduce_tma_stages(p.k);
   uint64_t wait_ns = 2000000000ull;
   void* args[] = {const_cast<ReduceParams*>(&p), &tb, &stages, &status, &wait_ns};
-  return cudaLaunchKernel(reinterpret_cast<const void*>(&reduce_tma_kernel), dim3(grid), dim3(kThreadsT), args,
-                          reduce_tma_smem(p.k), stream);
+  return cudaLaunchKernel(reduce_tma_fn(p.k), dim3(grid), dim3(kThreadsT), args, reduce_tma_smem(p.k), stream);
 }
 
 }  // namespace hoc
