@@ -7,7 +7,10 @@
 // events: the caller's stream records a fork event that the internal copy
 // streams wait on, cross-stream plan edges are event waits, and the caller's
 // stream waits on a join event of every internal stream.  No host thread ever
-// blocks, and no device-side wait is unbounded.
+// blocks, and no device-side wait is unbounded.  hoc_sendrecv_async skips the
+// join and completes a caller's event instead.  The one call whose sizes the
+// host cannot know, an all-to-all with device-computed counts, uses the
+// paper's flag handshake with a host proxy (proxy.cpp).
 //
 // P2P executor (section 3.3): a move is one cudaMemcpyAsync on an internal
 // copy stream (copy engines, zero SMs) or a job of the TMA bulk-copy kernel.

@@ -16,6 +16,10 @@
 //     (k * 8 KiB of loads in flight per CTA);
 //   * SM budget (one CTA per SM): 1024-thread CTAs, 1 vector per thread, so
 //     each of the few SMs keeps k * 16 KiB of loads in flight.
+// The whole-GPU grid is 8 waves of the resident CTAs (a finished CTA is
+// replaced at once), the fused kernel's k outputs use streaming stores, and
+// multi-wave launches use programmatic dependent launch (the next kernel in
+// the stream is scheduled into the slots the last wave frees).
 //
 // Arithmetic: fp32 adds with __fadd_rn (round to nearest even, no contraction,
 // no flush to zero); bf16 widens exactly to fp32, adds in fp32 and rounds once
