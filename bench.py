@@ -25,6 +25,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -174,10 +175,16 @@ def recorded_traffic(kernel: str, k: int, count: int):
         return None
     src = os.path.join(ROOT, "collective_communication_schedules_gb300", "csrc", e.get("source", "reduce.cu"))
     try:
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        digest = hashlib.sha256(source_code(open(src).read())).hexdigest()[:16]
     except OSError:
         return None
-    return e.get("bytes_per_launch") if digest == e.get("source_sha256_16") else None
+    return e.get("bytes_per_launch") if digest == e.get("code_sha256_16") else None
+
+
+def source_code(text: str) -> bytes:
+    """A source file's code without its // comments and blank lines: what the counters depend on."""
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln).encode()
 
 
 # ---------------------------------------------------------------- distributed
