@@ -387,7 +387,11 @@ hocResult_t build_plan(const Cfg& base, const CallShape& s, Plan* p) {
   switch (s.op) {
     case HOC_OP_ALLREDUCE:
       if (s.dtype == HOC_UINT8) return HOC_ERR_UNSUPPORTED;
-      p->path = s.path >= 0 ? s.path : (cfg.path == HOC_PATH_AUTO ? HOC_PATH_FUSED : cfg.path);
+      // AUTO: the fused kernel with the whole GPU; under an SM budget the copy
+      // engines take the moves, so the few SMs only reduce.
+      p->path = s.path >= 0 ? s.path
+                            : (cfg.path != HOC_PATH_AUTO ? cfg.path
+                                                         : (cfg.reduce_max_sms > 0 ? HOC_PATH_CE : HOC_PATH_FUSED));
       if (p->path < HOC_PATH_CE || p->path > HOC_PATH_FUSED) return HOC_ERR_INVALID_ARG;
       r = plan_allreduce(cfg, s, p);
       break;

@@ -58,7 +58,7 @@ typedef enum { HOC_SUM = 0 } hocRedOp_t;
 
 /* How chunk moves are executed. */
 typedef enum {
-  HOC_PATH_AUTO = 0,  /* allreduce -> FUSED; moves -> CE */
+  HOC_PATH_AUTO = 0,  /* allreduce -> FUSED (CE under an SM budget, reduce_max_sms > 0); moves -> CE */
   HOC_PATH_CE = 1,    /* cudaMemcpyAsync on internal copy streams: zero SMs */
   HOC_PATH_TMA = 2,   /* cp.async.bulk kernel: SM-driven comparison path */
   HOC_PATH_FUSED = 3  /* allreduce only: one kernel reduces and writes all k outputs */

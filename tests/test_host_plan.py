@@ -114,6 +114,15 @@ def test_fused_allreduce_is_one_launch():
     assert auto == items
 
 
+def test_auto_allreduce_under_an_sm_budget_moves_on_copy_engines():
+    # with the whole GPU AUTO fuses; with an SM budget the few SMs only reduce
+    budget = hoc.plan_query(8, hoc.OP_ALLREDUCE, 1 << 20, hoc.BFLOAT16,
+                            config=hoc.Config(path="auto", reduce_max_sms=8))
+    ce = hoc.plan_query(8, hoc.OP_ALLREDUCE, 1 << 20, hoc.BFLOAT16, config=hoc.Config(path="ce", reduce_max_sms=8))
+    assert budget == ce
+    assert {it["kind"] for it in budget} == {hoc.ITEM_REDUCE, hoc.ITEM_COPY}
+
+
 def test_pipeline_depth_adds_backpressure_edges():
     cfg = hoc.Config(path="ce", chunk_bytes=1 << 16, pipeline_depth=2)
     items = hoc.plan_query(4, hoc.OP_ALLREDUCE, 1 << 20, hoc.FLOAT32, config=cfg)
