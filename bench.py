@@ -906,6 +906,21 @@ def run_ours(args, world, rank, local):
                           "copies_per_step": s4["copies"], "kernels_per_step": s4["kernels"]})
             c4.close()
         extras["chunk_sweep"] = sweep
+        # allreduce under an SM budget: fused (every move on the few SMs) vs copy engines (SMs only reduce);
+        # AUTO picks the copy engines when a budget is set
+        budget = []
+        for m in (8, 32):
+            for p in ("fused", "ce"):
+                c6 = hoc.Comm(k, local, hoc.Config(path=p, reduce_max_sms=m))
+                for _ in range(2):
+                    c6.allreduce(send, recv, stream=stream)
+                bm = time_allreduce(c6, send, recv, stream, 5)
+                s6 = c6.last_stats()
+                budget.append({"reduce_max_sms": m, "path": p, "ms": round(bm, 3),
+                               "bus_gbs": round(bus_bytes(k, per_rank) / (bm * 1e-3) / 1e9, 1),
+                               "sms_used": s6["sms_used"], "copies_per_step": s6["copies"]})
+                c6.close()
+        extras["allreduce_under_sm_budget"] = budget
     if args.workloads and not args.no_extras:
         extras["workloads"] = {"dp_bucket_stream": leg_bucket_stream(bucket_pool, sms, peak),
                                "pp_1f1b": leg_pipeline(sms),
