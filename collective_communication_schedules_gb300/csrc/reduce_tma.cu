@@ -24,6 +24,7 @@
 #include <cuda_bf16.h>
 
 #include "hoc_internal.h"
+#include "ptx_async.cuh"
 
 namespace hoc {
 namespace {
@@ -32,42 +33,8 @@ constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kThreadsT = kConsumers + 32;  // + one producer warp
 
-__device__ __forceinline__ uint32_t sa(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
-__device__ __forceinline__ uint64_t now_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void mb_init(uint64_t* b, uint32_t n) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(b)), "r"(n) : "memory");
-}
-__device__ __forceinline__ void mb_expect(uint64_t* b, uint32_t tx) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sa(b)), "r"(tx) : "memory");
-}
-__device__ __forceinline__ void mb_arrive(uint64_t* b) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sa(b)) : "memory");
-}
-__device__ __forceinline__ bool mb_try(uint64_t* b, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(sa(b)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool mb_wait(uint64_t* b, uint32_t parity, uint64_t deadline) {
-  while (!mb_try(b, parity))
-    if (now_ns() > deadline) return false;
-  return true;
-}
-__device__ __forceinline__ void bulk_g2s(void* s, const void* g, uint32_t n, uint64_t* b) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(sa(s)),
-               "l"(g), "r"(n), "r"(sa(b))
-               : "memory");
-}
+using namespace ptx;
+
 // Barrier over the consumer warps that also ORs a predicate: every consumer
 // gets the same answer, so they leave the loop together.
 __device__ __forceinline__ bool consumers_sync_or(bool v) {
@@ -285,8 +252,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
-      mb_init(&full[s], 1);
-      mb_init(&empty[s], kConsumerWarps);
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
     }
     abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -301,7 +268,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     for (uint64_t it = 0; it < mine; ++it) {
       const int s = int(it % stages);
       if (it >= uint64_t(stages) &&
-          !mb_wait(&empty[s], uint32_t((it / stages - 1) & 1), now_ns() + wait_ns)) {
+          !mbar_wait_bounded(&empty[s], uint32_t((it / stages - 1) & 1), global_ns() + wait_ns)) {
         atomicExch(status, kStatusTimeoutLoad);
         atomicExch(&abort_flag, 1);
         break;
@@ -313,22 +280,22 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       uint32_t n;
       tile_body(p, sg, tr.local, tile_bytes, e0, off, n);
       if (n == 0) {
-        mb_arrive(&full[s]);  // nothing to load (a segment shorter than one vector)
+        mbar_arrive(&full[s]);  // nothing to load (a segment shorter than one vector)
       } else {
-        mb_expect(&full[s], n * uint32_t(k));
+        mbar_arrive_expect_tx(&full[s], n * uint32_t(k));
         const uint8_t* seq = p.seq[sg.owner];
         const uint64_t gb = (sg.elem_off + e0) * eb + off;
         for (int j = 0; j < k; ++j)
-          bulk_g2s(smem + size_t(s) * stage_bytes + size_t(j) * tile_bytes,
+          bulk_load(smem + size_t(s) * stage_bytes + size_t(j) * tile_bytes,
                    static_cast<const char*>(p.in[seq[j]]) + gb, n, &full[s]);
       }
       issued = it + 1;
     }
     // Do not leave while loads still target this CTA's shared memory.
     const uint64_t first = issued > uint64_t(stages) ? issued - stages : 0;
-    const uint64_t deadline = now_ns() + wait_ns;
+    const uint64_t deadline = global_ns() + wait_ns;
     for (uint64_t it = first; it < issued; ++it)
-      if (!mb_wait(&full[it % stages], uint32_t((it / stages) & 1), deadline)) {
+      if (!mbar_wait_bounded(&full[it % stages], uint32_t((it / stages) & 1), deadline)) {
         atomicExch(status, kStatusTimeoutDrain);
         break;
       }
@@ -339,7 +306,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   const int ct = threadIdx.x - 32;
   for (uint64_t it = 0; it < mine; ++it) {
     const int s = int(it % stages);
-    bool bad = !mb_wait(&full[s], uint32_t((it / stages) & 1), now_ns() + wait_ns);
+    bool bad = !mbar_wait_bounded(&full[s], uint32_t((it / stages) & 1), global_ns() + wait_ns);
     if (bad) atomicExch(status, kStatusTimeoutLoad);
     bad = bad || *(volatile int*)&abort_flag;
     if (consumers_sync_or(bad)) {
@@ -363,7 +330,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       }
     }
     __syncwarp();
-    if (lane == 0) mb_arrive(&empty[s]);
+    if (lane == 0) mbar_arrive(&empty[s]);
     // head and tail elements of the segment (plain loads)
     const uint64_t tiles_here = p.tile_start[tr.seg + 1] - p.tile_start[tr.seg];
     if (tr.local == 0 && uint64_t(ct) < e0) scalar_elem(p, seq, sg.owner, sg.elem_off + ct, sg.out_off + ct);
