@@ -401,3 +401,32 @@ def test_sendrecv_async_completes_by_event(path):
         # nothing to move: the event still completes
         e = c.sendrecv_async(0, src[:0], 1, dst[:0], stream=prod)
         e.synchronize()
+
+
+def test_captured_multiwave_reduce_scatters():
+    # Whole-GPU reduce-scatters large enough for a multi-wave grid launch with
+    # programmatic dependent launch; two of them captured back to back into a
+    # CUDA graph keep their order and bits.
+    k, rc = 8, 1_638_400
+    xs = [inputs.rank_inputs("bfloat16", k, k * rc, workload=3, slot=s) for s in range(2)]
+    want = [o_ring.reduce_scatter(x, rc, "bfloat16") for x in xs]
+    with _comm(k, "auto") as c:
+        send = [[to_device(x, "bfloat16") for x in xs[s]] for s in range(2)]
+        recv = [[torch.empty(rc, dtype=torch.bfloat16, device="cuda") for _ in range(k)] for _ in range(2)]
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            for j in range(2):
+                c.reduce_scatter(send[j], recv[j], rc, stream=s)   # plans and occupancy outside the capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for j in range(2):
+                c.reduce_scatter(send[j], recv[j], rc, stream=s)
+        for j in range(2):
+            for t in recv[j]:
+                t.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for j in range(2):
+            for r in range(k):
+                assert_bits_equal(to_host(recv[j][r], "bfloat16"), want[j][r], "bfloat16", f"captured rs {j} rank {r}")
