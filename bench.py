@@ -458,9 +458,10 @@ def _bucket_stream_graph(hoc, torch, k, nb, pool, rc, pool_in, outs, stream, pea
         runs = []
         for _ in range(3):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            graph.replay()
-            e1.record(stream)
+            with torch.cuda.stream(stream):  # replay() launches on the current stream
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
             torch.cuda.synchronize()
             runs.append(e0.elapsed_time(e1))
         ms = statistics.median(runs)
