@@ -4,7 +4,7 @@
 // pack   (dispatch side): a stable counting sort of the (token, slot) pairs of
 //        one source rank by expert -- experts of a rank are contiguous, so this
 //        is the (destination rank, expert, token, slot) order -- followed by a
-//        row gather into the send buffer and the per-destination element counts
+//        row scatter into the send buffer and the per-destination element counts
 //        that the all-to-all needs (on the device, for hoc_alltoall_device_counts).
 // combine (unpack): every token's output row is the gate-weighted sum of its
 //        topk returned rows, folded in slot order in binary32 (products and sums
@@ -86,68 +86,106 @@ __global__ void ep_place_kernel(const int32_t* __restrict__ ids, int n, const in
 }
 
 // Tile histogram: hist[b * experts + e] = pairs of tile b that chose expert e.
+// A thread issues all of its loads of the tile before counting them.
 __global__ void ep_tile_hist_kernel(const int32_t* __restrict__ ids, int n, int experts, int32_t* __restrict__ hist) {
   pdl_enter();
   extern __shared__ int sh[];
   for (int e = threadIdx.x; e < experts; e += blockDim.x) sh[e] = 0;
-  __syncthreads();
-  const int lo = blockIdx.x * kTileItems, hi = min(n, lo + kTileItems);
-  for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
-    const int e = ids[i];
-    if (e >= 0 && e < experts) atomicAdd(&sh[e], 1);
+  const int lo = blockIdx.x * kTileItems;
+  int ev[kTileItems / kEpThreads];
+#pragma unroll
+  for (int k = 0; k < kTileItems / kEpThreads; ++k) {
+    const int i = lo + k * kEpThreads + int(threadIdx.x);
+    ev[k] = i < n ? ids[i] : -1;
   }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < kTileItems / kEpThreads; ++k)
+    if (ev[k] >= 0 && ev[k] < experts) atomicAdd(&sh[ev[k]], 1);
   __syncthreads();
   for (int e = threadIdx.x; e < experts; e += blockDim.x) hist[size_t(blockIdx.x) * experts + e] = sh[e];
 }
 
 // One CTA: turns the tile histograms into the first output row of each
 // (tile, expert) -- all pairs of smaller experts, then those of expert e in
-// earlier tiles -- and writes the per-expert totals and the per-destination
-// element counts.
+// earlier tiles -- and writes the per-expert totals, the number of valid pairs
+// and the per-destination element counts.  With `staged` the histograms and
+// totals are copied into shared memory once (coalesced), every scan runs on
+// that copy, and the starts go back once; otherwise the scans run in place in
+// global memory (shapes whose histograms exceed the shared budget).
+constexpr int kScanThreads = 1024;
+constexpr int kScanSmemInts = 48 * 1024 / 4 - kScanThreads;  // dynamic ints beside the static warp sums
+
 __global__ void ep_scan_kernel(int32_t* __restrict__ hist, int tiles, int experts, int32_t* __restrict__ total,
                                int32_t* __restrict__ nvalid, unsigned long long* __restrict__ dst_counts, int nranks,
-                               int per_rank, int hidden) {
+                               int per_rank, int hidden, int staged) {
   pdl_enter();
-  __shared__ int part[1024];
+  __shared__ int warp_sum[kScanThreads / 32];
+  extern __shared__ int dyn[];  // staged: [experts] totals, then [tiles][experts] histograms
+  const size_t cells = size_t(tiles) * experts;
+  int* tot = staged ? dyn : total;
+  int* h = staged ? dyn + experts : hist;
+  if (staged) {
+    for (size_t j = threadIdx.x; j < cells; j += blockDim.x) h[j] = hist[j];
+    __syncthreads();
+  }
   for (int e = threadIdx.x; e < experts; e += blockDim.x) {  // per expert: exclusive scan over tiles
     int run = 0;
     for (int b = 0; b < tiles; ++b) {
-      const int c = hist[size_t(b) * experts + e];
-      hist[size_t(b) * experts + e] = run;
+      const int c = h[size_t(b) * experts + e];
+      h[size_t(b) * experts + e] = run;
       run += c;
     }
-    total[e] = run;
+    tot[e] = run;
   }
   __syncthreads();
-  // exclusive scan of the totals over experts: thread t owns a contiguous run of experts
+  // exclusive scan of the totals over experts: thread t owns a contiguous run
+  // of experts; a shuffle scan within each warp, then over the warp sums
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int per = (experts + blockDim.x - 1) / blockDim.x;
   const int e0 = min(experts, int(threadIdx.x) * per), e1 = min(experts, e0 + per);
   int mine = 0;
-  for (int e = e0; e < e1; ++e) mine += total[e];
-  part[threadIdx.x] = mine;
-  __syncthreads();
-  for (int off = 1; off < int(blockDim.x); off <<= 1) {
-    const int v = int(threadIdx.x) >= off ? part[threadIdx.x - off] : 0;
-    __syncthreads();
-    part[threadIdx.x] += v;
-    __syncthreads();
+  for (int e = e0; e < e1; ++e) mine += tot[e];
+  int incl = mine;
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += v;
   }
-  int base = part[threadIdx.x] - mine;
-  if (threadIdx.x == blockDim.x - 1) *nvalid = part[threadIdx.x];  // every valid pair
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int ws = lane < nwarps ? warp_sum[lane] : 0;
+    int wi = ws;
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, wi, off);
+      if (lane >= off) wi += v;
+    }
+    if (lane < nwarps) warp_sum[lane] = wi - ws;  // exclusive over warps
+    if (lane == nwarps - 1) *nvalid = wi;         // every valid pair
+  }
+  __syncthreads();
+  int base = warp_sum[warp] + incl - mine;
   for (int e = e0; e < e1; ++e) {
-    for (int b = 0; b < tiles; ++b) hist[size_t(b) * experts + e] += base;
-    base += total[e];
+    for (int b = 0; b < tiles; ++b) h[size_t(b) * experts + e] += base;
+    base += tot[e];
   }
   for (int d = threadIdx.x; d < nranks; d += blockDim.x) {
     unsigned long long c = 0;
-    for (int e = d * per_rank; e < (d + 1) * per_rank; ++e) c += (unsigned long long)total[e];
+    for (int e = d * per_rank; e < (d + 1) * per_rank; ++e) c += (unsigned long long)tot[e];
     dst_counts[d] = c * (unsigned long long)hidden;
+  }
+  if (staged) {
+    __syncthreads();
+    for (size_t j = threadIdx.x; j < cells; j += blockDim.x) hist[j] = h[j];
+    for (int e = threadIdx.x; e < experts; e += blockDim.x) total[e] = tot[e];
   }
 }
 
 // Stable placement of one tile: a pair's row is its (tile, expert) start, plus
 // the pairs of that expert in earlier warps of the tile, earlier steps of its
-// warp and lower lanes of its step.
+// warp and lower lanes of its step.  A warp loads all of its expert ids, and
+// later all of their starts, before the dependent counting.
+constexpr int kWarpSteps = kWarpItems / 32;
 __global__ void ep_tile_place_kernel(const int32_t* __restrict__ ids, int n, int experts,
                                      const int32_t* __restrict__ start, const int32_t* __restrict__ nvalid,
                                      int32_t* __restrict__ perm, int32_t* __restrict__ pos_of) {
@@ -155,17 +193,23 @@ __global__ void ep_tile_place_kernel(const int32_t* __restrict__ ids, int n, int
   extern __shared__ int wh[];  // [kEpWarps][experts]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int j = threadIdx.x; j < kEpWarps * experts; j += blockDim.x) wh[j] = 0;
-  __syncthreads();
   int* mine = wh + warp * experts;
   const int lo = blockIdx.x * kTileItems + warp * kWarpItems;
   const int hi = min(n, lo + kWarpItems);
   const unsigned below = (1u << lane) - 1u;
-  for (int base = lo; base < hi; base += 32) {  // this warp's pairs per expert
-    const int i = base + lane;
+  int ev[kWarpSteps];
+#pragma unroll
+  for (int k = 0; k < kWarpSteps; ++k) {
+    const int i = lo + k * 32 + lane;
     const int e = i < hi ? ids[i] : -1;
-    const bool ok = e >= 0 && e < experts;
-    const unsigned grp = __match_any_sync(0xFFFFFFFFu, ok ? e : -1);
-    if (ok && (grp & below) == 0) mine[e] += __popc(grp);  // the group's lowest lane counts it
+    ev[k] = e >= 0 && e < experts ? e : -1;  // -1: dropped pair or past the tile
+  }
+  __syncthreads();
+  unsigned grp[kWarpSteps];
+#pragma unroll
+  for (int k = 0; k < kWarpSteps; ++k) {  // this warp's pairs per expert
+    grp[k] = __match_any_sync(0xFFFFFFFFu, ev[k]);
+    if (ev[k] >= 0 && (grp[k] & below) == 0) mine[ev[k]] += __popc(grp[k]);  // the group's lowest lane counts it
     __syncwarp();
   }
   __syncthreads();
@@ -179,63 +223,75 @@ __global__ void ep_tile_place_kernel(const int32_t* __restrict__ ids, int n, int
   }
   __syncthreads();
   const int32_t* st = start + size_t(blockIdx.x) * experts;
-  for (int base = lo; base < hi; base += 32) {
-    const int i = base + lane;
-    const int e = i < hi ? ids[i] : -1;
-    const bool ok = e >= 0 && e < experts;
-    const unsigned grp = __match_any_sync(0xFFFFFFFFu, ok ? e : -1);
-    if (ok) {
-      const int pos = st[e] + mine[e] + __popc(grp & below);
+  int sv[kWarpSteps];
+#pragma unroll
+  for (int k = 0; k < kWarpSteps; ++k) sv[k] = ev[k] >= 0 ? st[ev[k]] : 0;
+#pragma unroll
+  for (int k = 0; k < kWarpSteps; ++k) {
+    const int i = lo + k * 32 + lane;
+    if (ev[k] >= 0) {
+      const int pos = sv[k] + mine[ev[k]] + __popc(grp[k] & below);
       perm[pos] = i;
       pos_of[i] = pos;
     } else if (i < hi) {
       pos_of[i] = -1;  // dropped pair
     }
     __syncwarp();
-    if (ok && (grp & below) == 0) mine[e] += __popc(grp);
+    if (ev[k] >= 0 && (grp[k] & below) == 0) mine[ev[k]] += __popc(grp[k]);
     __syncwarp();
   }
   // rows past the valid pairs have no pair
   for (int r = *nvalid + blockIdx.x * blockDim.x + threadIdx.x; r < n; r += gridDim.x * blockDim.x) perm[r] = -1;
 }
 
-// send[pos] = x[perm[pos] / topk]; rows of `hb` bytes.  Vector path: a work
-// item is (row, 1 KiB slice), spread evenly over the warps of a persistent
-// grid, each lane keeping two 16-byte loads in flight; byte path: warp per row.
-constexpr int kGatherSliceVecs = 64;  // 16-byte vectors per work item
-__global__ void ep_gather_kernel(const char* __restrict__ x, const int32_t* __restrict__ perm, int n, int topk,
-                                 int hb, char* __restrict__ send, int vec) {
+// send[pos_of[t*topk + j]] = x[t] for every valid pair (t, j); rows of `hb`
+// bytes.  Each token row is read once and stored to each of its packed rows.
+// Vector path: a work item is (token, 1 KiB slice of its row), spread evenly
+// over the warps of a persistent grid; a lane loads two 16-byte vectors of
+// the slice and stores them to every destination row.  Byte path: warp per
+// token.
+constexpr int kScatterSliceVecs = 64;  // 16-byte vectors per work item
+__global__ void ep_scatter_kernel(const char* __restrict__ x, const int32_t* __restrict__ pos_of, int tokens,
+                                  int topk, int hb, char* __restrict__ send, int vec) {
   pdl_enter();
   const int lane = threadIdx.x & 31;
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
   const long long first = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (vec) {
     const int nv = hb / 16;
-    const int slices = (nv + kGatherSliceVecs - 1) / kGatherSliceVecs;
-    const long long items = (long long)n * slices;
+    const int slices = (nv + kScatterSliceVecs - 1) / kScatterSliceVecs;
+    const long long items = (long long)tokens * slices;
     for (long long it = first; it < items; it += warps) {
-      const int pos = int(it / slices);
-      const int src = perm[pos];
-      if (src < 0) continue;  // dropped pair: nothing to send
-      const uint4* s4 = reinterpret_cast<const uint4*>(x + size_t(src / topk) * hb);
-      uint4* d4 = reinterpret_cast<uint4*>(send + size_t(pos) * hb);
-      const int v0 = int(it % slices) * kGatherSliceVecs + lane;
-      const int v1 = v0 + 32;
-      const bool h0 = v0 < nv, h1 = v1 < nv && v1 < int(it % slices) * kGatherSliceVecs + kGatherSliceVecs;
+      const int t = int(it / slices);
+      const int v0 = int(it % slices) * kScatterSliceVecs + lane;
+      const int v1 = v0 + 32;  // still inside the slice
+      const bool h0 = v0 < nv, h1 = v1 < nv;
+      const uint4* s4 = reinterpret_cast<const uint4*>(x + size_t(t) * hb);
       uint4 a, b;
       if (h0) a = __ldg(s4 + v0);
       if (h1) b = __ldg(s4 + v1);
-      if (h0) d4[v0] = a;
-      if (h1) d4[v1] = b;
+      for (int j0 = 0; j0 < topk; j0 += 32) {
+        const int pl = j0 + lane < topk ? pos_of[size_t(t) * topk + j0 + lane] : -1;
+        const int nj = min(32, topk - j0);
+        for (int j = 0; j < nj; ++j) {
+          const int pos = __shfl_sync(0xFFFFFFFFu, pl, j);
+          if (pos < 0) continue;  // dropped pair: nothing to send
+          uint4* d4 = reinterpret_cast<uint4*>(send + size_t(pos) * hb);
+          if (h0) d4[v0] = a;
+          if (h1) d4[v1] = b;
+        }
+      }
     }
     return;
   }
-  for (long long pos = first; pos < n; pos += warps) {
-    const int src = perm[pos];
-    if (src < 0) continue;
-    const char* s = x + size_t(src / topk) * hb;
-    char* d = send + size_t(pos) * hb;
-    for (int b = lane; b < hb; b += 32) d[b] = s[b];
+  for (long long t = first; t < tokens; t += warps) {
+    const char* src = x + size_t(t) * hb;
+    for (int j = 0; j < topk; ++j) {
+      const int pos = pos_of[size_t(t) * topk + j];
+      if (pos < 0) continue;
+      char* d = send + size_t(pos) * hb;
+      for (int b = lane; b < hb; b += 32) d[b] = src[b];
+    }
   }
 }
 
@@ -425,7 +481,7 @@ cudaError_t ep_preload() {
                        reinterpret_cast<const void*>(&ep_tile_hist_kernel),
                        reinterpret_cast<const void*>(&ep_scan_kernel),
                        reinterpret_cast<const void*>(&ep_tile_place_kernel),
-                       reinterpret_cast<const void*>(&ep_gather_kernel),
+                       reinterpret_cast<const void*>(&ep_scatter_kernel),
                        reinterpret_cast<const void*>(&ep_combine_kernel),
                        reinterpret_cast<const void*>(&ep_combine_vec_kernel),
                        reinterpret_cast<const void*>(kCombineIlp[0]), reinterpret_cast<const void*>(kCombineIlp[1]),
@@ -477,8 +533,10 @@ extern "C" hocResult_t hoc_ep_pack(const int32_t* expert_ids, const void* x, int
     int32_t* hist = workspace + experts;
     int32_t* nvalid = hist + size_t(tiles) * experts;
     launch_pdl(ep_tile_hist_kernel, tiles, kEpThreads, sizeof(int) * size_t(experts), s, expert_ids, n, experts, hist);
-    launch_pdl(ep_scan_kernel, 1, 1024, 0, s, hist, tiles, experts, total, nvalid,
-               reinterpret_cast<unsigned long long*>(dst_counts), nranks, experts / nranks, hidden);
+    const size_t stage_ints = size_t(experts) + size_t(tiles) * experts;
+    const int staged = stage_ints <= size_t(kScanSmemInts);
+    launch_pdl(ep_scan_kernel, 1, kScanThreads, staged ? sizeof(int) * stage_ints : 0, s, hist, tiles, experts, total,
+               nvalid, reinterpret_cast<unsigned long long*>(dst_counts), nranks, experts / nranks, hidden, staged);
     launch_pdl(ep_tile_place_kernel, tiles, kEpThreads, sizeof(int) * size_t(kEpWarps) * experts, s, expert_ids, n,
                experts, static_cast<const int32_t*>(hist), static_cast<const int32_t*>(nvalid), perm, pos_of);
   } else {
@@ -494,9 +552,11 @@ extern "C" hocResult_t hoc_ep_pack(const int32_t* expert_ids, const void* x, int
   }
   const int hb = hidden * 2;
   const int vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(send)) & 15u) == 0 && hb % 16 == 0;
-  const long long gather_warps = vec ? (long long)n * ((hb / 16 + kGatherSliceVecs - 1) / kGatherSliceVecs) : n;
-  launch_pdl(ep_gather_kernel, persistent_grid(reinterpret_cast<const void*>(&ep_gather_kernel), (gather_warps + 7) / 8),
-             256, 0, s, static_cast<const char*>(x), static_cast<const int32_t*>(perm), n, topk, hb,
+  const long long scatter_warps = vec ? (long long)tokens * ((hb / 16 + kScatterSliceVecs - 1) / kScatterSliceVecs)
+                                      : tokens;
+  launch_pdl(ep_scatter_kernel,
+             persistent_grid(reinterpret_cast<const void*>(&ep_scatter_kernel), (scatter_warps + 7) / 8), 256, 0, s,
+             static_cast<const char*>(x), static_cast<const int32_t*>(pos_of), tokens, topk, hb,
              static_cast<char*>(send), int(vec));
   return cudaGetLastError() == cudaSuccess ? HOC_SUCCESS : HOC_ERR_CUDA;
 }

@@ -43,6 +43,7 @@ def _pack_on_device(ids, x, experts, k, stream):
     (333, 40, True, 64, 6),       # one partial tile, dropped pairs
     (5000, 64, True, 96, 4),      # ragged last tile, experts not a power of two
     (700, 16, False, 2048, 2),    # more than 1024 experts: the one-CTA-per-expert sort
+    (3000, 16, True, 1024, 8),    # 12 tiles x 1024 experts: histograms past the shared budget, scanned in place
     (200, 24, False, 64, 10),     # topk above the combine's batched loads
     (250, 36, True, 64, 6),       # hidden not a multiple of 8: scalar combine
 ])
