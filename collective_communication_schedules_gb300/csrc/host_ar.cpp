@@ -212,6 +212,10 @@ extern "C" hocResult_t hoc_allreduce_host(hocComm_t comm, const void* const* h_s
   const size_t b = dtype_bytes(dtype);
   for (int r = 0; r < k; ++r)
     if (!h_send[r] || !h_recv[r]) return HOC_ERR_INVALID_ARG;
+  if (count > kMaxSpanBytes / b) {  // the staged pipeline issues its copies without a plan
+    set_error_detail("a rank's buffer span exceeds 2^40 bytes");
+    return HOC_ERR_INVALID_ARG;
+  }
   // A result buffer may only coincide with its own input (in place); it may
   // not overlap any other input or result.
   for (int r = 0; r < k; ++r) {

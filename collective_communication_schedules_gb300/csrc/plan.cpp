@@ -3,6 +3,7 @@
 #include "plan.h"
 
 #include <algorithm>
+#include <new>
 #include <map>
 #include <tuple>
 #include <cstring>
@@ -371,9 +372,85 @@ hocResult_t plan_sendrecv(const Cfg& cfg, const CallShape& s, Plan* p) {
   return HOC_SUCCESS;
 }
 
+// The spans a call names stay within kMaxSpanBytes, and the largest one
+// within kMaxChunksPerSpan chunks.  Every count is checked on its own before
+// any sum, so no sum can wrap.
+hocResult_t check_sizes(const Cfg& cfg, const CallShape& s) {
+  const uint64_t b = dtype_bytes(s.dtype);
+  const uint64_t lim = kMaxSpanBytes / b;  // elements in the largest span
+  const uint64_t k = uint64_t(s.k);
+  auto too_big = [] {
+    set_error_detail("a rank's buffer span exceeds 2^40 bytes");
+    return HOC_ERR_INVALID_ARG;
+  };
+  uint64_t span = 0;  // bytes of the largest rank buffer span
+  switch (s.op) {
+    case HOC_OP_ALLREDUCE:
+    case HOC_OP_SENDRECV:
+      if (s.count > lim) return too_big();
+      span = s.count * b;
+      break;
+    case HOC_OP_REDUCE_SCATTER:
+    case HOC_OP_ALLGATHER:
+      if (s.count > lim / k) return too_big();
+      span = s.count * k * b;
+      break;
+    case HOC_OP_ALLTOALL: {
+      if (s.counts.empty()) {
+        if (s.count > lim / k) return too_big();
+        span = s.count * k * b;
+        break;
+      }
+      if (s.counts.size() != k * k || (!s.sdispls.empty() && s.sdispls.size() != k * k) ||
+          (!s.rdispls.empty() && s.rdispls.size() != k * k))
+        return HOC_ERR_INVALID_ARG;
+      std::vector<uint64_t> col(k, 0);
+      for (uint64_t a = 0; a < k; ++a) {
+        uint64_t row = 0;
+        for (uint64_t d = 0; d < k; ++d) {
+          const uint64_t c = s.counts[a * k + d];
+          if (c > lim) return too_big();
+          if (!s.sdispls.empty() && (s.sdispls[a * k + d] > lim || s.sdispls[a * k + d] + c > lim)) return too_big();
+          if (!s.rdispls.empty() && (s.rdispls[d * k + a] > lim || s.rdispls[d * k + a] + c > lim)) return too_big();
+          row += c;
+          col[d] += c;
+        }
+        if (row > lim) return too_big();
+        span = std::max(span, row * b);
+      }
+      for (uint64_t c : col) {
+        if (c > lim) return too_big();
+        span = std::max(span, c * b);
+      }
+      break;
+    }
+    default: return HOC_ERR_INVALID_ARG;
+  }
+  const uint64_t chunk = cfg.chunk_bytes ? cfg.chunk_bytes : std::min(kAutoChunkCe, kAutoChunkTma);
+  if (span / chunk > kMaxChunksPerSpan) {
+    set_error_detail("chunk_bytes too small for this size: more than 2^24 chunks per rank buffer");
+    return HOC_ERR_INVALID_ARG;
+  }
+  return HOC_SUCCESS;
+}
+
+hocResult_t build_plan_checked(const Cfg& base, const CallShape& s, Plan* p);
+
 }  // namespace
 
 hocResult_t build_plan(const Cfg& base, const CallShape& s, Plan* p) {
+  try {
+    return build_plan_checked(base, s, p);
+  } catch (const std::bad_alloc&) {
+    *p = Plan();
+    set_error_detail("out of host memory while building the plan");
+    return HOC_ERR_OOM;
+  }
+}
+
+namespace {
+
+hocResult_t build_plan_checked(const Cfg& base, const CallShape& s, Plan* p) {
   Cfg cfg = base;
   if (s.chunk) cfg.chunk_bytes = s.chunk;
   *p = Plan();
@@ -383,7 +460,8 @@ hocResult_t build_plan(const Cfg& base, const CallShape& s, Plan* p) {
   p->count = s.count;
   if (s.k < 1 || s.k > kMaxRanks || dtype_bytes(s.dtype) == 0) return HOC_ERR_INVALID_ARG;
   if ((cfg.chunk_bytes != 0 && cfg.chunk_bytes < 256) || cfg.n_copy < 1 || cfg.n_copy > 16) return HOC_ERR_INVALID_ARG;
-  hocResult_t r = HOC_SUCCESS;
+  hocResult_t r = check_sizes(cfg, s);
+  if (r != HOC_SUCCESS) return r;
   switch (s.op) {
     case HOC_OP_ALLREDUCE:
       if (s.dtype == HOC_UINT8) return HOC_ERR_UNSUPPORTED;
@@ -447,5 +525,7 @@ hocResult_t build_plan(const Cfg& base, const CallShape& s, Plan* p) {
   account(p);
   return HOC_SUCCESS;
 }
+
+}  // namespace
 
 }  // namespace hoc

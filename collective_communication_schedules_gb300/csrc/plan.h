@@ -108,7 +108,19 @@ int dtype_lanes(int dtype);  // elements per 16-byte vector
 std::vector<std::vector<int>> source_groups(const std::vector<Move>& moves);
 
 // Builds the plan; returns HOC_ERR_INVALID_ARG / UNSUPPORTED for bad shapes.
+// Largest span of one rank's buffer a call may name (1 TiB, beyond any one
+// device's memory) and most pipeline chunks one rank's span may be cut into:
+// together they keep every size and offset sum far from overflow and the
+// plan's host memory bounded.  build_plan rejects a shape past either with
+// HOC_ERR_INVALID_ARG, before anything is issued.
+constexpr uint64_t kMaxSpanBytes = uint64_t(1) << 40;
+constexpr uint64_t kMaxChunksPerSpan = uint64_t(1) << 24;
+
+// Builds the plan of a call shape.  Returns HOC_ERR_OOM (never throws) if the
+// host runs out of memory while building it.
 hocResult_t build_plan(const Cfg& cfg, const CallShape& shape, Plan* plan);
+
+void set_error_detail(const char* what);
 
 // Block partition of n elements over k owners (sizes differ by at most one).
 void block_partition(size_t n, int k, std::vector<size_t>* sizes, std::vector<size_t>* offs);

@@ -189,11 +189,14 @@ void start_task(Proxy* P, Slot& s) {
     }
   } done_guard{P};
   for (int d = 0; d < k; ++d) {
-    size_t col = 0;
-    for (int a = 0; a < k; ++a) col += cnt[size_t(a) * k + d];
-    if (col > s.cap[d]) {
-      release(P, s, HOC_ERR_INVALID_ARG, "a receiver's total count exceeds its capacity; nothing was moved");
-      return;
+    size_t col = 0;  // stays <= cap[d]: each count is compared with the room left, so no sum wraps
+    for (int a = 0; a < k; ++a) {
+      const size_t c = cnt[size_t(a) * k + d];
+      if (c > s.cap[d] - col) {
+        release(P, s, HOC_ERR_INVALID_ARG, "a receiver's total count exceeds its capacity; nothing was moved");
+        return;
+      }
+      col += c;
     }
   }
   if (P->fault == kFaultProxyStall) {  // injected on the host: a completion that never arrives

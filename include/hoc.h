@@ -20,6 +20,9 @@
  *     simulated rank, owned by the caller.  Pointer arrays are host arrays
  *     read during the call and not retained.
  *   - Counts are in elements of `dtype`; a count of 0 is a successful no-op.
+ *     No rank buffer a call names may span more than 2^40 bytes, and no rank
+ *     buffer may be cut into more than 2^24 chunks of `chunk_bytes`; past
+ *     either limit the call returns HOC_ERR_INVALID_ARG and issues nothing.
  *   - Work is ordered after all prior work on `stream` and later work on
  *     `stream` sees the results.  Calls never block the host (except the
  *     first call of a new shape in graph mode, which builds a CUDA graph).

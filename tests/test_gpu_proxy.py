@@ -82,13 +82,17 @@ def test_many_tasks_reuse_slots_and_two_streams():
         assert c.proxy_status()["completed"] == 40
 
 
-def test_capacity_overflow_releases_the_stream():
+@pytest.mark.parametrize("counts,cap", [
+    ([[10, 10], [10, 10]], [5, 20]),                # receiver 0 gets 20 elements into room for 5
+    ([[-(1 << 63), 1], [-(1 << 63), 1]], [20, 20]),  # two counts of 2^63 (as uint64): their sum wraps to 0
+])
+def test_capacity_overflow_releases_the_stream(counts, cap):
     k = 2
     with hoc.Comm(k, 0) as c:
-        d_counts = torch.tensor([[10, 10], [10, 10]], dtype=torch.int64, device="cuda")
+        d_counts = torch.tensor(counts, dtype=torch.int64, device="cuda")
         sd = [torch.ones(20, dtype=torch.int32, device="cuda") for _ in range(k)]
         rv = [torch.zeros(20, dtype=torch.int32, device="cuda") for _ in range(k)]
-        c.alltoall_device_counts(sd, rv, d_counts, [5, 20], hoc.INT32)
+        c.alltoall_device_counts(sd, rv, d_counts, cap, hoc.INT32)
         with pytest.raises(hoc.HocError) as e:
             c.wait(timeout_ms=30000)
         assert e.value.code == hoc.ERR_INVALID_ARG

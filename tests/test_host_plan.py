@@ -261,3 +261,50 @@ def test_bad_config_rejected():
     with pytest.raises(hoc.HocError) as e:
         hoc.plan_query(3, hoc.OP_ALLREDUCE, 10, hoc.UINT8)
     assert e.value.code == hoc.ERR_UNSUPPORTED
+
+
+# ------------------------------------------------------------------ sizes
+SPAN = 1 << 40  # largest rank buffer span a call may name
+
+
+@pytest.mark.parametrize("op,count,dtype", [
+    (hoc.OP_ALLREDUCE, SPAN // 2 + 1, hoc.BFLOAT16),
+    (hoc.OP_SENDRECV, SPAN + 1, hoc.UINT8),
+    (hoc.OP_REDUCE_SCATTER, SPAN // (4 * 8) + 1, hoc.FLOAT32),   # the send span is k * recvcount
+    (hoc.OP_ALLGATHER, SPAN // (2 * 8) + 1, hoc.BFLOAT16),      # the recv span is k * sendcount
+    (hoc.OP_ALLTOALL, SPAN // 8 + 1, hoc.UINT8),                # uniform: k counts per rank
+    (hoc.OP_ALLREDUCE, (1 << 64) - 1, hoc.FLOAT32),             # count * 4 wraps size_t
+])
+def test_oversized_spans_are_rejected_before_any_plan(op, count, dtype):
+    with pytest.raises(hoc.HocError) as e:
+        hoc.plan_query(8, op, count, dtype)
+    assert e.value.code == hoc.ERR_INVALID_ARG and "2^40" in str(e.value)
+
+
+def test_span_limit_is_inclusive():
+    # exactly 2^40 bytes per rank plans (in 4 MiB chunks: 2^18 per rank buffer)
+    items = hoc.plan_query(2, hoc.OP_SENDRECV, SPAN, hoc.UINT8)
+    assert sum(it["bytes"] for it in items) == SPAN
+
+
+@pytest.mark.parametrize("counts", [
+    lambda k: [[1 << 62 if (a, d) == (0, 1) else 3 for d in range(k)] for a in range(k)],
+    # two counts whose sum wraps 2^64 to a small column total
+    lambda k: [[1 << 63 if d == 2 and a in (0, 1) else 5 for d in range(k)] for a in range(k)],
+    # each count fits, but one receiver's column is over the span
+    lambda k: [[SPAN // 4 if d == 0 else 1 for d in range(k)] for a in range(k)],
+])
+def test_alltoall_counts_that_overflow_are_rejected(counts):
+    k = 8
+    with pytest.raises(hoc.HocError) as e:
+        hoc.plan_query(k, hoc.OP_ALLTOALL, 0, hoc.UINT8, counts=np.array(counts(k), dtype=np.uint64))
+    assert e.value.code == hoc.ERR_INVALID_ARG
+
+
+def test_chunk_count_per_span_is_bounded():
+    n = (1 << 33) // 4  # 8 GiB of fp32 per rank
+    with pytest.raises(hoc.HocError) as e:
+        hoc.plan_query(8, hoc.OP_ALLREDUCE, n, hoc.FLOAT32, config=hoc.Config(path="ce", chunk_bytes=256))
+    assert e.value.code == hoc.ERR_INVALID_ARG and "chunk_bytes" in str(e.value)
+    # the same size with the default chunk plans
+    assert hoc.plan_query(8, hoc.OP_ALLREDUCE, n, hoc.FLOAT32, config=hoc.Config(path="fused"))
