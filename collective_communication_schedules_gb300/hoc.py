@@ -145,16 +145,33 @@ def _dtype_code(x) -> int:
     return m[x.dtype]
 
 
-def _ptr(x) -> int:
+DTYPE_BYTES = {INT32: 4, FLOAT32: 4, BFLOAT16: 2, UINT8: 1}
+
+
+def _ptr(x, nbytes: int = 0, what: str = "buffer", device: bool = True) -> int:
+    """Address of `x`.  A tensor must be contiguous, hold at least `nbytes`
+    bytes (the span the call touches) and live on the GPU (`device`) or the
+    host; an int is taken as a raw address, unchecked."""
     if isinstance(x, int):
         return x
-    if not x.is_cuda:
-        raise ValueError("rank buffers must be CUDA tensors")
+    if not x.is_contiguous():
+        raise ValueError(f"{what}: tensor must be contiguous")
+    have = x.numel() * x.element_size()
+    if have < nbytes:
+        raise ValueError(f"{what}: tensor holds {have} bytes, the call touches {nbytes}")
+    if device and not x.is_cuda:
+        raise ValueError(f"{what}: rank buffers must be CUDA tensors")
+    if not device and x.is_cuda:
+        raise ValueError(f"{what}: host buffers must be CPU tensors")
     return x.data_ptr()
 
 
-def _ptr_array(xs: Sequence) -> C.Array:
-    return (C.c_void_p * len(xs))(*[_ptr(x) for x in xs])
+def _ptr_array(xs: Sequence, nbytes=0, what: str = "buffer", device: bool = True) -> C.Array:
+    """Addresses of the rank buffers; `nbytes` is one span for all ranks or a list, one per rank."""
+    spans = list(nbytes) if isinstance(nbytes, (list, tuple)) else [nbytes] * len(xs)
+    if len(spans) != len(xs):
+        raise ValueError(f"{what}: expected {len(spans)} rank buffers, got {len(xs)}")
+    return (C.c_void_p * len(xs))(*[_ptr(x, n, f"{what}[{r}]", device) for r, (x, n) in enumerate(zip(xs, spans))])
 
 
 def _stream(stream) -> int:
@@ -223,6 +240,11 @@ class Comm:
         _check(lib().hoc_init(C.byref(h), nranks, device, C.byref(cfg)), "hoc_init")
         self._h = h
 
+    def _ranks(self, xs, nbytes, what, device=True):
+        if len(xs) != self.k:
+            raise ValueError(f"{what}: expected {self.k} rank buffers, got {len(xs)}")
+        return _ptr_array(xs, nbytes, what, device)
+
     def close(self):
         if getattr(self, "_h", None):
             _check(lib().hoc_destroy(self._h), "hoc_destroy")
@@ -244,44 +266,57 @@ class Comm:
     def allreduce(self, send, recv, count=None, dtype=None, stream=None):
         count = send[0].numel() if count is None else count
         dtype = _dtype_code(send[0]) if dtype is None else dtype
-        _check(lib().hoc_allreduce(self._h, _ptr_array(send), _ptr_array(recv), count, dtype, SUM,
-                                   _stream(stream)), "hoc_allreduce")
+        n = int(count) * DTYPE_BYTES[dtype]
+        _check(lib().hoc_allreduce(self._h, self._ranks(send, n, "send"), self._ranks(recv, n, "recv"), count, dtype,
+                                   SUM, _stream(stream)), "hoc_allreduce")
 
     def allreduce_host(self, h_send, h_recv, count=None, dtype=None, stream=None):
         """AllReduce of host (CPU) tensors: one fused launch on host memory the GPU can address (path AUTO/FUSED),
         else the copy-engine pipeline through device staging slots (path CE/TMA)."""
         count = h_send[0].numel() if count is None else count
         dtype = _dtype_code(h_send[0]) if dtype is None else dtype
-        ptrs = lambda xs: (C.c_void_p * len(xs))(*[x if isinstance(x, int) else x.data_ptr() for x in xs])
-        _check(lib().hoc_allreduce_host(self._h, ptrs(h_send), ptrs(h_recv), count, dtype, SUM, _stream(stream)),
-               "hoc_allreduce_host")
+        n = int(count) * DTYPE_BYTES[dtype]
+        _check(lib().hoc_allreduce_host(self._h, self._ranks(h_send, n, "h_send", device=False),
+                                        self._ranks(h_recv, n, "h_recv", device=False), count, dtype, SUM,
+                                        _stream(stream)), "hoc_allreduce_host")
 
     def reduce_scatter(self, send, recv, recvcount=None, dtype=None, stream=None):
         recvcount = recv[0].numel() if recvcount is None else recvcount
         dtype = _dtype_code(send[0]) if dtype is None else dtype
-        _check(lib().hoc_reduce_scatter(self._h, _ptr_array(send), _ptr_array(recv), recvcount, dtype, SUM,
-                                        _stream(stream)), "hoc_reduce_scatter")
+        n = int(recvcount) * DTYPE_BYTES[dtype]
+        _check(lib().hoc_reduce_scatter(self._h, self._ranks(send, self.k * n, "send"), self._ranks(recv, n, "recv"),
+                                        recvcount, dtype, SUM, _stream(stream)), "hoc_reduce_scatter")
 
     def allgather(self, send, recv, sendcount=None, dtype=None, stream=None):
         sendcount = send[0].numel() if sendcount is None else sendcount
         dtype = _dtype_code(send[0]) if dtype is None else dtype
-        _check(lib().hoc_allgather(self._h, _ptr_array(send), _ptr_array(recv), sendcount, dtype,
-                                   _stream(stream)), "hoc_allgather")
+        n = int(sendcount) * DTYPE_BYTES[dtype]
+        _check(lib().hoc_allgather(self._h, self._ranks(send, n, "send"), self._ranks(recv, self.k * n, "recv"),
+                                   sendcount, dtype, _stream(stream)), "hoc_allgather")
 
     def alltoall(self, send, recv, sendcounts=None, sdispls=None, rdispls=None, count=0, dtype=None,
                  stream=None):
         """sendcounts: k x k (row = source) in elements; None = uniform `count`."""
         dtype = _dtype_code(send[0]) if dtype is None else dtype
-        kk = self.k * self.k
-        _check(lib().hoc_alltoall(self._h, _ptr_array(send), _sizes(sendcounts, kk), _sizes(sdispls, kk),
-                                  _ptr_array(recv), _sizes(rdispls, kk), int(count), dtype, _stream(stream)),
+        k, kk, b = self.k, self.k * self.k, DTYPE_BYTES[dtype]
+        cnt = _sizes(sendcounts, kk)
+        sd, rd = _sizes(sdispls, kk), _sizes(rdispls, kk)
+        c = [cnt[i] for i in range(kk)] if cnt is not None else [int(count)] * kk
+        # the span of each rank's buffer: the end of its furthest segment
+        s_end = [max((sd[a * k + d] if sd is not None else sum(c[a * k: a * k + d])) + c[a * k + d]
+                     for d in range(k)) * b for a in range(k)]
+        r_end = [max((rd[d * k + a] if rd is not None else sum(c[x * k + d] for x in range(a))) + c[a * k + d]
+                     for a in range(k)) * b for d in range(k)]
+        _check(lib().hoc_alltoall(self._h, self._ranks(send, s_end, "send"), cnt, sd,
+                                  self._ranks(recv, r_end, "recv"), rd, int(count), dtype, _stream(stream)),
                "hoc_alltoall")
 
     def sendrecv(self, src_rank, send, dst_rank, recv, count=None, dtype=None, stream=None):
         count = send.numel() if count is None else count
         dtype = _dtype_code(send) if dtype is None else dtype
-        _check(lib().hoc_sendrecv(self._h, int(src_rank), _ptr(send), int(dst_rank), _ptr(recv), count, dtype,
-                                  _stream(stream)), "hoc_sendrecv")
+        n = int(count) * DTYPE_BYTES[dtype]
+        _check(lib().hoc_sendrecv(self._h, int(src_rank), _ptr(send, n, "send"), int(dst_rank), _ptr(recv, n, "recv"),
+                                  count, dtype, _stream(stream)), "hoc_sendrecv")
 
     def sendrecv_async(self, src_rank, send, dst_rank, recv, count=None, dtype=None, stream=None, done=None):
         """Send/recv completed by an event, not by `stream`: returns the torch.cuda.Event (`done`, or a new
@@ -293,8 +328,10 @@ class Comm:
             done = torch.cuda.Event()
         if not done.cuda_event:
             done.record(torch.cuda.current_stream() if stream is None else stream)   # creates the CUDA event
-        _check(lib().hoc_sendrecv_async(self._h, int(src_rank), _ptr(send), int(dst_rank), _ptr(recv), count, dtype,
-                                        _stream(stream), C.c_void_p(done.cuda_event)), "hoc_sendrecv_async")
+        n = int(count) * DTYPE_BYTES[dtype]
+        _check(lib().hoc_sendrecv_async(self._h, int(src_rank), _ptr(send, n, "send"), int(dst_rank),
+                                        _ptr(recv, n, "recv"), count, dtype, _stream(stream),
+                                        C.c_void_p(done.cuda_event)), "hoc_sendrecv_async")
         return done
 
     def alltoall_device_counts(self, send, recv, d_counts, recv_capacity, dtype=None, stream=None,
@@ -304,8 +341,13 @@ class Comm:
         The counts reach a host proxy through the stream-memory-operation
         handshake; the call returns without waiting (see include/hoc_proxy.h)."""
         dtype = _dtype_code(send[0]) if dtype is None else dtype
-        cap = (C.c_size_t * self.k)(*[int(v) for v in recv_capacity])
-        _check(lib().hoc_alltoall_device_counts(self._h, _ptr_array(send), _ptr_array(recv), _ptr(d_counts),
+        caps = [int(v) for v in recv_capacity]
+        if len(caps) != self.k:
+            raise ValueError(f"recv_capacity: expected {self.k} values, got {len(caps)}")
+        cap = (C.c_size_t * self.k)(*caps)
+        _check(lib().hoc_alltoall_device_counts(self._h, self._ranks(send, 0, "send"),
+                                                self._ranks(recv, [v * DTYPE_BYTES[dtype] for v in caps], "recv"),
+                                                _ptr(d_counts, 8 * self.k * self.k, "d_counts"),
                                                 int(bool(transpose)), cap, dtype, _stream(stream)),
                "hoc_alltoall_device_counts")
 
@@ -345,12 +387,12 @@ class Comm:
 # ---------------------------------------------------------------- workload
 def probe_launch(ctas: int, threads: int, iters: int, sink=None, stream=None, whole_sm: bool = False):
     _check(lib().hoc_probe_launch(_stream(stream), int(ctas), int(threads), int(iters), int(bool(whole_sm)),
-                                  None if sink is None else _ptr(sink)), "hoc_probe_launch")
+                                  None if sink is None else _ptr(sink, 12, "sink")), "hoc_probe_launch")
 
 
 def xor16(src, dst, n: int, key: int, stream=None):
-    _check(lib().hoc_xor16_launch(_stream(stream), _ptr(src), _ptr(dst), int(n), int(key) & 0xFFFF),
-           "hoc_xor16_launch")
+    _check(lib().hoc_xor16_launch(_stream(stream), _ptr(src, 2 * int(n), "src"), _ptr(dst, 2 * int(n), "dst"), int(n),
+                                  int(key) & 0xFFFF), "hoc_xor16_launch")
 
 
 def tma_moves_noalloc(src, dst, nbytes, max_ctas: int = 0, stream=None, wait: bool = True):
@@ -359,9 +401,10 @@ def tma_moves_noalloc(src, dst, nbytes, max_ctas: int = 0, stream=None, wait: bo
     n = len(nbytes)
     if len(src) != n or len(dst) != n:
         raise ValueError("src, dst and nbytes must have the same length")
-    sizes = (C.c_size_t * max(1, n))(*[int(b) for b in nbytes])
-    _check(lib().hoc_tma_moves_noalloc(_ptr_array(src), _ptr_array(dst), sizes, n, int(max_ctas), _stream(stream),
-                                       int(bool(wait))), "hoc_tma_moves_noalloc")
+    spans = [int(b) for b in nbytes]
+    sizes = (C.c_size_t * max(1, n))(*spans)
+    _check(lib().hoc_tma_moves_noalloc(_ptr_array(src, spans, "src"), _ptr_array(dst, spans, "dst"), sizes, n,
+                                       int(max_ctas), _stream(stream), int(bool(wait))), "hoc_tma_moves_noalloc")
 
 
 def topo_schedule(C_matrix, node_of, sym, bw_nvlink: int, bw_rdma: int):
@@ -397,16 +440,21 @@ def ep_pack_workspace(tokens: int, topk: int, experts: int) -> int:
 def ep_pack(expert_ids, x, experts: int, nranks: int, send, perm, pos_of, dst_counts, workspace, stream=None):
     """Dispatch-side pack of one source rank (device tensors; see include/hoc_ep.h)."""
     tokens, hidden = x.shape
-    topk = expert_ids.numel() // tokens
-    _check(lib().hoc_ep_pack(_ptr(expert_ids), _ptr(x), int(tokens), int(topk), int(hidden), int(experts),
-                             int(nranks), _ptr(send), _ptr(perm), _ptr(pos_of), _ptr(dst_counts), _ptr(workspace),
+    topk = expert_ids.numel() // tokens if tokens else 1
+    n = tokens * topk
+    _check(lib().hoc_ep_pack(_ptr(expert_ids, 4 * n, "expert_ids"), _ptr(x, 2 * tokens * hidden, "x"), int(tokens),
+                             int(topk), int(hidden), int(experts), int(nranks), _ptr(send, 2 * n * hidden, "send"),
+                             _ptr(perm, 4 * n, "perm"), _ptr(pos_of, 4 * n, "pos_of"),
+                             _ptr(dst_counts, 8 * int(nranks), "dst_counts"), _ptr(workspace, 0, "workspace"),
                              int(workspace.numel()), _stream(stream)), "hoc_ep_pack")
 
 
 def ep_combine(rows, pos_of, weights, tokens: int, topk: int, hidden: int, y, stream=None):
     """Gate-weighted top-k combine of one source rank (see include/hoc_ep.h)."""
-    _check(lib().hoc_ep_combine(_ptr(rows), _ptr(pos_of), _ptr(weights), int(tokens), int(topk), int(hidden),
-                                _ptr(y), _stream(stream)), "hoc_ep_combine")
+    n = int(tokens) * int(topk)
+    _check(lib().hoc_ep_combine(_ptr(rows, 2 * n * int(hidden), "rows"), _ptr(pos_of, 4 * n, "pos_of"),
+                                _ptr(weights, 4 * n, "weights"), int(tokens), int(topk), int(hidden),
+                                _ptr(y, 2 * int(tokens) * int(hidden), "y"), _stream(stream)), "hoc_ep_combine")
 
 
 def sm_count(device: int = 0) -> int:
