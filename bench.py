@@ -260,7 +260,7 @@ def cpu_baseline(xs_host, seconds: float, device_out=None):
     return out
 
 
-def cpu_baseline_buckets(host_pool, buckets: int = 2):
+def cpu_baseline_buckets(host_pool, buckets: int = 16):
     """The oracle's reduce-scatter on the first `buckets` of the DP stream's 16 pool buckets, timed on
     the host, and the per-bucket time scaled to the stream's 268 buckets (labelled as scaled)."""
     from oracle import ring
@@ -483,6 +483,8 @@ def leg_pipeline(sms):
     g = torch.Generator(device="cuda").manual_seed(4100)
     xs = [torch.randn(elems, generator=g, device="cuda").to(torch.bfloat16) for _ in range(m)]
     out = {}
+    first = None  # results of the first run with sends: every mode and path must give the same bits
+    same = True
     for path in ("ce", "tma"):
         with hoc.Comm(p, torch.cuda.current_device(), hoc.Config(path=path)) as c:
             res = {}
@@ -503,6 +505,12 @@ def leg_pipeline(sms):
                     torch.cuda.synchronize()
                     runs.append(e0.elapsed_time(e1))
                 res[label + "_ms"] = round(statistics.median(runs), 3)
+                if mode is not None:
+                    if first is None:
+                        first = [pipe.result(i).clone() for i in range(m)]
+                    else:
+                        same = same and all(torch.equal(pipe.result(i).view(torch.int16), first[i].view(torch.int16))
+                                            for i in range(m))
                 del pipe
                 torch.cuda.empty_cache()
             sends = 2 * (p - 1) * m
@@ -512,6 +520,7 @@ def leg_pipeline(sms):
             res["exposed_ms_event_sends"] = round(res["event_sends_ms"] - res["compute_only_ms"], 3)
             res["exposed_ms_stream_sends"] = round(res["stream_sends_ms"] - res["compute_only_ms"], 3)
             out[path] = res
+    out["results_identical_across_modes_and_paths"] = bool(same)
     return out
 
 
