@@ -513,8 +513,13 @@ extern "C" hocResult_t hoc_ep_pack(const int32_t* expert_ids, const void* x, int
   using namespace hoc;
   if (tokens < 0 || topk < 1 || hidden < 1 || experts < 1 || nranks < 1 || experts % nranks != 0)
     return HOC_ERR_INVALID_ARG;
-  if (tokens == 0) return HOC_SUCCESS;
-  if (!expert_ids || !x || !send || !perm || !pos_of || !dst_counts || !workspace) return HOC_ERR_INVALID_ARG;
+  if (!dst_counts) return HOC_ERR_INVALID_ARG;
+  if (tokens == 0)  // nothing to pack: the rank sends nothing to anyone
+    return cudaMemsetAsync(dst_counts, 0, sizeof(uint64_t) * size_t(nranks), static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? HOC_SUCCESS
+               : HOC_ERR_CUDA;
+  if (!expert_ids || !x || !send || !perm || !pos_of || !workspace) return HOC_ERR_INVALID_ARG;
   if (size_t(tokens) * topk > size_t(INT32_MAX)) return HOC_ERR_INVALID_ARG;
   size_t need = 0;
   hoc_ep_pack_workspace(tokens, topk, experts, &need);

@@ -27,7 +27,7 @@ extern "C" {
  * workspace: device int32 scratch of workspace_ints entries, at least what
  * hoc_ep_pack_workspace() returns (else HOC_ERR_INVALID_ARG, nothing queued).
  * Pairs with an expert id outside [0, experts) are dropped.  experts must be a
- * multiple of nranks.  The sort is a stable counting sort over tiles of 2048
+ * multiple of nranks.  With tokens == 0 only dst_counts is written (all 0).  The sort is a stable counting sort over tiles of 2048
  * pairs (tile histograms, one scan, stable placement by warp match); with more
  * than 1024 experts one CTA per expert scans every pair instead. */
 hocResult_t hoc_ep_pack(const int32_t* expert_ids, const void* x, int tokens, int topk, int hidden, int experts,

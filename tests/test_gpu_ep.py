@@ -46,6 +46,7 @@ def _pack_on_device(ids, x, experts, k, stream):
     (3000, 16, True, 1024, 8),    # 12 tiles x 1024 experts: histograms past the shared budget, scanned in place
     (200, 24, False, 64, 10),     # topk above the combine's batched loads
     (250, 36, True, 64, 6),       # hidden not a multiple of 8: scalar combine
+    (100, 16, True, 64, 40),      # topk above a warp: the scatter takes its destinations 32 at a time
 ])
 def test_pack_and_combine_match_oracle(tokens, hidden, drop, experts, topk):
     k = 8
@@ -74,6 +75,22 @@ def test_pack_and_combine_match_oracle(tokens, hidden, drop, experts, topk):
     torch.cuda.synchronize()
     want_y = o_ep.combine(want_send, want_pos, ws[0], topk)
     assert np.array_equal(to_host(y, "bfloat16"), want_y)
+
+
+def test_zero_tokens_is_a_no_op():
+    k, hidden, experts = 8, 64, 64
+    x = torch.empty((0, hidden), dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty(0, dtype=torch.int32, device="cuda")
+    counts = torch.full((k,), 7, dtype=torch.int64, device="cuda")
+    ws = torch.empty(max(1, hoc.ep_pack_workspace(0, 6, experts)), dtype=torch.int32, device="cuda")
+    empty = torch.empty(0, dtype=torch.int32, device="cuda")
+    hoc.ep_pack(ids, x, experts, k, torch.empty((0, hidden), dtype=torch.bfloat16, device="cuda"), empty, empty,
+                counts, ws)
+    y = torch.empty((0, hidden), dtype=torch.bfloat16, device="cuda")
+    hoc.ep_combine(torch.empty((0, hidden), dtype=torch.bfloat16, device="cuda"), empty,
+                   torch.empty(0, device="cuda"), 0, 6, hidden, y)
+    torch.cuda.synchronize()
+    assert counts.tolist() == [0] * k  # a rank without tokens sends nothing
 
 
 def test_dispatch_combine_round_trip_without_host_sync():
