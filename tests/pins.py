@@ -282,3 +282,102 @@ def check_1f1b_shape(one_f_one_b):
                     inflight += 1 if kind == "F" else -1
                     peak = max(peak, inflight)
                 assert peak == min(w + 1, m)
+
+
+# ------------------------------------------------------------------ EP pack / combine
+def _widen_bf16(b) -> np.ndarray:
+    """bf16 bit patterns to binary32 (exact: the 16 bits become the high half)."""
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def _narrow_bf16_torch(f32) -> np.ndarray:
+    """binary32 to bf16 bit patterns by PyTorch's CPU cast (round to nearest even)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(f32, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def brute_ep_pack(x, ids, experts, k):
+    """Rows by a literal loop over experts, then tokens, then slots; counts by a per-pair loop."""
+    tokens, topk = ids.shape
+    perm, rows = [], []
+    for e in range(experts):                    # (destination rank, expert) order = expert order
+        for t in range(tokens):
+            for j in range(topk):
+                if ids[t][j] == e:
+                    perm.append(t * topk + j)
+                    rows.append(x[t])
+    counts = [0] * k
+    for e in ids.reshape(-1):
+        if 0 <= e < experts:
+            counts[e // (experts // k)] += x.shape[1]
+    return perm, rows, counts
+
+
+def check_ep_pack_brute(pack, rng, trials=20):
+    for _ in range(trials):
+        k, per = int(rng.integers(1, 5)), int(rng.integers(1, 4))
+        experts, tokens, topk, hidden = k * per, int(rng.integers(1, 12)), int(rng.integers(1, 4)), 3
+        ids = rng.integers(-1, experts + 1, size=(tokens, topk))          # includes dropped pairs
+        x = rng.integers(0, 1 << 16, size=(tokens, hidden)).astype(np.uint16)
+        send, perm, pos_of, counts = pack(x, ids, experts, k)
+        bperm, brows, bcounts = brute_ep_pack(x, ids, experts, k)
+        assert list(perm) == bperm
+        assert np.array_equal(send, np.array(brows, dtype=np.uint16).reshape(-1, hidden))
+        assert list(counts) == bcounts
+        for row, p in enumerate(perm):
+            assert pos_of[p] == row
+        assert all(pos_of[p] == -1 for p in range(tokens * topk) if p not in set(bperm))
+
+
+def check_ep_combine_scalar(pack, combine, rng):
+    """Every output element by a scalar loop of numpy binary32 products and sums, narrowed by PyTorch."""
+    tokens, topk, hidden = 7, 3, 5
+    ids = rng.integers(0, 4, size=(tokens, topk))
+    ids[2, 1] = -1                                              # a dropped pair
+    x = _narrow_bf16_torch(rng.standard_normal((tokens, hidden)).astype(np.float32))
+    wts = rng.random(tokens * topk).astype(np.float32)
+    send, perm, pos_of, _ = pack(x, ids, 4, 2)
+    y = combine(send, pos_of, wts, topk)
+    for t in range(tokens):
+        for h in range(hidden):
+            acc = None
+            for j in range(topk):
+                p = pos_of[t * topk + j]
+                if p < 0:
+                    continue
+                prod = np.float32(wts[t * topk + j] * _widen_bf16(send[p:p + 1, h])[0])
+                acc = prod if acc is None else np.float32(acc + prod)
+            want = _narrow_bf16_torch(np.array([0.0 if acc is None else acc], dtype=np.float32))[0]
+            assert y[t, h] == want, (t, h)
+
+
+def check_ep_combine_identity(pack, combine, rng):
+    """Top-1 with unit weight returns the token rows."""
+    x = _narrow_bf16_torch(rng.standard_normal((9, 4)).astype(np.float32))
+    ids = rng.integers(0, 8, size=(9, 1))
+    send, _, pos_of, _ = pack(x, ids, 8, 4)
+    assert np.array_equal(combine(send, pos_of, np.ones(9, np.float32), 1), x)
+
+
+def load_ep_combine_cases():
+    cases = []
+    with open(os.path.join(GOLDEN, "ep_combine_cases.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            name, topk, rows, pos_of, wts, y = [p.strip() for p in line.split("|")]
+            cases.append(dict(
+                name=name, topk=int(topk),
+                rows=np.array([int(v, 16) for v in rows.split(";")], dtype=np.uint16).reshape(-1, 1),
+                pos_of=np.array([int(v) for v in pos_of.split(",")], dtype=np.int64),
+                weights=np.array([int(v, 16) for v in wts.split(",")], dtype=np.uint32).view(np.float32),
+                y=np.array([int(v, 16) for v in y.split(",")], dtype=np.uint16)))
+    return cases
+
+
+def check_ep_combine_golden(combine):
+    for c in load_ep_combine_cases():
+        got = np.asarray(combine(c["rows"], c["pos_of"], c["weights"], c["topk"])).reshape(-1)
+        assert np.array_equal(got, c["y"]), (c["name"], [hex(int(v)) for v in got])

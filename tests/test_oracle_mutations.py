@@ -157,3 +157,86 @@ def test_topo_dropped_degree_constraint_caught():
         assert caught
     finally:
         topo.greedy_matching = real
+
+
+# ------------------------------------------------------------ EP pack / combine
+def _combine_reverse_slots(rows, pos_of, weights, topk):
+    from oracle import ep
+    pos = np.asarray(pos_of).reshape(-1, topk)[:, ::-1].reshape(-1)
+    w = np.asarray(weights, dtype=np.float32).reshape(-1, topk)[:, ::-1].reshape(-1)
+    return ep.combine(rows, pos, w, topk)
+
+
+def _combine_round_every_add(rows, pos_of, weights, topk):
+    tokens = len(pos_of) // topk
+    w = np.asarray(weights, dtype=np.float32).reshape(tokens, topk)
+    pos = np.asarray(pos_of).reshape(tokens, topk)
+    acc = np.zeros((tokens, rows.shape[1]), dtype=np.uint16)
+    for j in range(topk):
+        ok = (pos[:, j] >= 0)[:, None]
+        prod = np.multiply(w[:, j:j + 1], bf16.widen(rows[np.where(pos[:, j] >= 0, pos[:, j], 0)]), dtype=np.float32)
+        acc = np.where(ok, bf16.narrow(np.add(bf16.widen(acc), prod, dtype=np.float32)), acc)
+    return acc
+
+
+def _combine_ignore_weights(rows, pos_of, weights, topk):
+    from oracle import ep
+    return ep.combine(rows, pos_of, np.ones(len(pos_of), np.float32), topk)
+
+
+def _combine_drop_first_slot(rows, pos_of, weights, topk):
+    from oracle import ep
+    pos = np.asarray(pos_of).reshape(-1, topk).copy()
+    pos[:, 0] = -1
+    return ep.combine(rows, pos.reshape(-1), weights, topk)
+
+
+def _combine_unchecked_drop(rows, pos_of, weights, topk):
+    # a dropped slot read as row -1 (the last row) instead of skipped
+    tokens = len(pos_of) // topk
+    w = np.asarray(weights, dtype=np.float32).reshape(tokens, topk)
+    pos = np.asarray(pos_of).reshape(tokens, topk)
+    acc = np.zeros((tokens, rows.shape[1]), dtype=np.float32)
+    for j in range(topk):
+        acc = np.add(acc, np.multiply(w[:, j:j + 1], bf16.widen(rows[pos[:, j]]), dtype=np.float32), dtype=np.float32)
+    return bf16.narrow(acc)
+
+
+@pytest.mark.parametrize("bad", [_combine_reverse_slots, _combine_round_every_add, _combine_ignore_weights,
+                                 _combine_drop_first_slot, _combine_unchecked_drop])
+def test_ep_combine_mistakes_caught(bad):
+    from oracle import ep
+    assert (_fails(pins.check_ep_combine_golden, bad)
+            or _fails(pins.check_ep_combine_scalar, ep.pack, bad, np.random.default_rng(7))
+            or _fails(pins.check_ep_combine_identity, ep.pack, bad, np.random.default_rng(8)))
+
+
+def _pack_tokens_reversed(x, ids, experts, k):
+    # unstable within an expert: later tokens first
+    from oracle import ep
+    tokens, topk = ids.shape
+    flat = np.asarray(ids).reshape(-1)
+    valid = np.nonzero((flat >= 0) & (flat < experts))[0][::-1]
+    perm = valid[np.argsort(flat[valid], kind="stable")].astype(np.int64)
+    pos_of = np.full(tokens * topk, -1, dtype=np.int64)
+    pos_of[perm] = np.arange(len(perm))
+    counts = np.bincount(flat[perm] // (experts // k), minlength=k).astype(np.int64) * x.shape[1]
+    return np.ascontiguousarray(x[perm // topk]), perm, pos_of, counts
+
+
+def _pack_clip_instead_of_drop(x, ids, experts, k):
+    from oracle import ep
+    return ep.pack(x, np.clip(ids, 0, experts - 1), experts, k)
+
+
+def _pack_round_robin_ranks(x, ids, experts, k):
+    from oracle import ep
+    send, perm, pos_of, _ = ep.pack(x, ids, experts, k)
+    flat = np.asarray(ids).reshape(-1)
+    counts = np.bincount(flat[perm] % k, minlength=k).astype(np.int64) * x.shape[1]   # expert e on rank e % k
+    return send, perm, pos_of, counts
+
+
+@pytest.mark.parametrize("bad", [_pack_tokens_reversed, _pack_clip_instead_of_drop, _pack_round_robin_ranks])
+def test_ep_pack_mistakes_caught(bad):
+    assert _fails(pins.check_ep_pack_brute, bad, np.random.default_rng(9))
