@@ -430,3 +430,30 @@ def test_captured_multiwave_reduce_scatters():
         for j in range(2):
             for r in range(k):
                 assert_bits_equal(to_host(recv[j][r], "bfloat16"), want[j][r], "bfloat16", f"captured rs {j} rank {r}")
+
+
+@pytest.mark.parametrize("path,engine", [("ce", "lsu"), ("tma", "lsu"), ("fused", "lsu"), ("fused", "tma")])
+def test_ring_golden_cases(path, engine):
+    """The hand-derived order- and rounding-sensitive cases straight from the golden file (no oracle)."""
+    from tests import pins
+    torch_dt = {"float32": torch.float32, "int32": torch.int32, "bfloat16": torch.bfloat16}
+    view_dt = {"float32": torch.int32, "int32": torch.int32, "bfloat16": torch.int16}
+    for c in pins.load_ring_cases():
+        k, dt = c["k"], c["dtype"]
+        bits_in = [np.asarray(x).view(np.uint32 if dt != "bfloat16" else np.uint16) for x in c["xs"]]
+        send = [torch.from_numpy(np.ascontiguousarray(x).view(np.int32 if dt != "bfloat16" else np.int16).copy())
+                .cuda().view(torch_dt[dt]) for x in bits_in]
+        recv = [torch.zeros_like(t) for t in send]
+        with _comm(k, path, ring_order=c["order"], reduce_engine=engine) as comm:
+            comm.allreduce(send, recv)
+            comm.wait()
+        want = c["y"].astype(np.int64)
+        for r in range(k):
+            got = recv[r].view(view_dt[dt]).cpu().numpy().astype(np.int64) & (0xFFFFFFFF if dt != "bfloat16" else 0xFFFF)
+            if dt == "bfloat16":  # a NaN result is compared by class, its payload is free
+                nan_w = ((want & 0x7F80) == 0x7F80) & ((want & 0x7F) != 0)
+                nan_g = ((got & 0x7F80) == 0x7F80) & ((got & 0x7F) != 0)
+                assert np.array_equal(nan_w, nan_g), (c["name"], path)
+                assert np.array_equal(got[~nan_w], want[~nan_w]), (c["name"], path, [hex(v) for v in got])
+            else:
+                assert np.array_equal(got, want), (c["name"], path, [hex(v) for v in got])

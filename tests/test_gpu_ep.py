@@ -133,3 +133,21 @@ def test_dispatch_combine_round_trip_without_host_sync():
         for r in range(k):
             assert np.array_equal(to_host(ys[r], "bfloat16"), want_y[r]), r
         assert c.proxy_status()["completed"] == 2
+
+
+@pytest.mark.parametrize("hidden", [1, 8])   # the scalar combine, and the vector combine with the value in every lane
+def test_combine_golden_cases(hidden):
+    """The hand-derived combine cases straight from the golden file (no oracle)."""
+    from tests import pins
+    for c in pins.load_ep_combine_cases():
+        rows = torch.from_numpy(np.ascontiguousarray(np.repeat(c["rows"], hidden, axis=1)).view(np.int16).copy())
+        rows = rows.cuda().view(torch.bfloat16)
+        pos = torch.from_numpy(c["pos_of"].astype(np.int32)).cuda()
+        w = torch.from_numpy(c["weights"].copy()).cuda()
+        tokens = len(c["y"])
+        y = torch.empty((tokens, hidden), dtype=torch.bfloat16, device="cuda")
+        hoc.ep_combine(rows, pos, w, tokens, c["topk"], hidden, y)
+        torch.cuda.synchronize()
+        got = y.view(torch.int16).cpu().numpy().astype(np.int64) & 0xFFFF
+        assert np.array_equal(got, np.repeat(c["y"].astype(np.int64)[:, None], hidden, axis=1)), \
+            (c["name"], hidden, [hex(int(v)) for v in got.reshape(-1)])
