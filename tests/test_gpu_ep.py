@@ -140,11 +140,12 @@ def test_combine_golden_cases(hidden):
     """The hand-derived combine cases straight from the golden file (no oracle)."""
     from tests import pins
     for c in pins.load_ep_combine_cases():
-        rows = torch.from_numpy(np.ascontiguousarray(np.repeat(c["rows"], hidden, axis=1)).view(np.int16).copy())
-        rows = rows.cuda().view(torch.bfloat16)
+        tokens = len(c["y"])
+        packed = np.zeros((tokens * c["topk"], hidden), dtype=np.uint16)  # the API's [tokens*topk, hidden] rows
+        packed[: len(c["rows"])] = np.repeat(c["rows"], hidden, axis=1)
+        rows = torch.from_numpy(packed.view(np.int16).copy()).cuda().view(torch.bfloat16)
         pos = torch.from_numpy(c["pos_of"].astype(np.int32)).cuda()
         w = torch.from_numpy(c["weights"].copy()).cuda()
-        tokens = len(c["y"])
         y = torch.empty((tokens, hidden), dtype=torch.bfloat16, device="cuda")
         hoc.ep_combine(rows, pos, w, tokens, c["topk"], hidden, y)
         torch.cuda.synchronize()
