@@ -44,6 +44,42 @@ def test_every_declared_symbol_is_exported():
     assert set(hoc._SIGS) <= names
 
 
+def _prototypes():
+    """name -> list of parameter declarations of every function the headers declare."""
+    protos = {}
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:hocResult_t|const char\s*\*)\s+(hoc_\w+)\s*\(([^;]*?)\)\s*;", text, re.M | re.S):
+            params = " ".join(m.group(2).split())
+            protos[m.group(1)] = [] if params in ("", "void") else [q.strip() for q in params.split(",")]
+    return protos
+
+
+def test_binding_signatures_match_the_headers():
+    """Each ctypes entry has the header's parameter count, pointer-ness and integer widths."""
+    import ctypes as C
+    protos = _prototypes()
+    for name, (res, args) in hoc._SIGS.items():
+        params = protos[name]
+        assert len(args) == len(params), (name, len(args), params)
+        for a, q in zip(args, params):
+            is_ptr = "*" in q or q.split()[0] == "hocComm_t"   # hocComm_t is a pointer typedef
+            ctype_ptr = a in (C.c_void_p, C.c_char_p) or (isinstance(a, type) and issubclass(a, C._Pointer))
+            assert is_ptr == ctype_ptr, (name, q, a)
+            if not is_ptr:
+                want = {"size_t": C.c_size_t, "uint64_t": C.c_uint64, "uint16_t": C.c_uint16}
+                base = q.split()[0]
+                if base in want:
+                    assert C.sizeof(a) == C.sizeof(want[base]), (name, q, a)
+                elif base in ("int", "hocDataType_t", "hocRedOp_t", "hocResult_t", "hocKernel_t"):
+                    assert C.sizeof(a) == C.sizeof(C.c_int), (name, q, a)
+                else:
+                    raise AssertionError(f"{name}: unchecked parameter type {q!r}")
+
+
 def test_no_device_is_a_clean_error():
     import torch
     if torch.cuda.is_available():
