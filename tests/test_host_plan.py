@@ -233,6 +233,92 @@ def test_alltoall_plan_stages_and_coverage(interleave, stage_sync):
                 assert it["n_waits"] >= 1 and first[it["wait0"]]["stage"] < it["stage"]
 
 
+def test_random_alltoall_plans_cover_every_flow_exactly():
+    """Random shapes: k = 1..16, empty rows and columns, odd chunk sizes, both move paths. Every flow's
+    bytes leave send[s] at its prefix-sum displacement and land in recv[d] at its own, exactly once."""
+    rng = np.random.default_rng(11)
+    for trial in range(60):
+        k = int(rng.integers(1, 17))
+        counts = rng.integers(0, 400, size=(k, k)) * (rng.random((k, k)) < 0.7)
+        if trial % 7 == 0:
+            counts[int(rng.integers(0, k)), :] = 0          # a rank that sends nothing
+        if trial % 11 == 0:
+            counts[:, int(rng.integers(0, k))] = 0          # a rank that receives nothing
+        dtype, b = [(hoc.BFLOAT16, 2), (hoc.FLOAT32, 4), (hoc.UINT8, 1)][trial % 3]
+        chunk = int(rng.choice([256, 1000, 4096, 65536, 0]))
+        path = "ce" if trial % 2 else "tma"
+        cfg = hoc.Config(path=path, chunk_bytes=chunk, n_copy_streams=int(rng.integers(1, 5)))
+        items = hoc.plan_query(k, hoc.OP_ALLTOALL, 0, dtype, counts=counts, config=cfg)
+        src, dst = defaultdict(list), defaultdict(list)
+        for it in items:
+            key = (it["src_rank"], it["dst_rank"])
+            assert it["src_buf"] == hoc.BUF_SEND and it["dst_buf"] == hoc.BUF_RECV
+            src[key].append((it["src_off"], it["src_off"] + it["bytes"]))
+            dst[key].append((it["dst_off"], it["dst_off"] + it["bytes"]))
+        for s_ in range(k):
+            for d in range(k):
+                n = int(counts[s_][d]) * b
+                sd = int(counts[s_][:d].sum()) * b                  # prefix sums in rank order
+                rd = int(counts[:s_, d].sum()) * b
+                if n == 0:
+                    assert (s_, d) not in src, (trial, s_, d)
+                    continue
+                for iv, at in ((src[(s_, d)], sd), (dst[(s_, d)], rd)):
+                    merged, ov = _cover(iv)   # no overlap + total n + first and last byte = exact cover
+                    assert not ov and _total(merged) == n, (trial, k, s_, d)
+                    assert merged[0][0] == at and merged[-1][1] == at + n, (trial, k, s_, d, at, n)
+
+
+def test_random_block_plans_cover_exactly():
+    """Random k, counts and chunks: the reduce-scatter reduces every block once; the all-gather sends
+    every rank's block to every rank once; the allreduce reduces every block once and copies it to the
+    k - 1 other ranks once (block partition by the closed form, not the oracle's helper)."""
+    rng = np.random.default_rng(12)
+    for trial in range(40):
+        k = int(rng.integers(1, 17))
+        n = int(rng.integers(1, 20)) if trial % 5 == 0 else int(rng.integers(1, 50000))  # n < k: empty blocks
+        dtype, b = [(hoc.BFLOAT16, 2), (hoc.FLOAT32, 4), (hoc.INT32, 4)][trial % 3]
+        chunk = int(rng.choice([256, 1000, 4096, 0]))
+        path = "ce" if trial % 2 else "tma"
+        cfg = hoc.Config(path=path, chunk_bytes=chunk)
+        # reduce-scatter: recvcount n per rank; block r = elements [r*n, (r+1)*n) of every send buffer
+        red = defaultdict(list)
+        for it in hoc.plan_query(k, hoc.OP_REDUCE_SCATTER, n, dtype, config=cfg):
+            assert it["kind"] in (hoc.ITEM_REDUCE, hoc.ITEM_FUSED)
+            red[it["dst_rank"]].append((it["src_off"], it["src_off"] + it["bytes"]))
+        for r in range(k):
+            iv, ov = _cover(red[r])
+            assert not ov and _total(iv) == n * b and iv[0][0] == r * n * b, (trial, r)
+        # all-gather: send[s] (n elements) lands at recv[d] + s*n for every (s, d)
+        got = defaultdict(list)
+        for it in hoc.plan_query(k, hoc.OP_ALLGATHER, n, dtype, config=cfg):
+            assert it["dst_off"] - it["src_off"] == it["src_rank"] * n * b
+            got[(it["src_rank"], it["dst_rank"])].append((it["src_off"], it["src_off"] + it["bytes"]))
+        for s_ in range(k):
+            for d in range(k):
+                iv, ov = _cover(got[(s_, d)])
+                assert not ov and _total(iv) == n * b and iv[0][0] == 0, (trial, s_, d)
+        # allreduce on the move path: block r = floor(n/k) + [r < n mod k] elements at prefix offsets
+        sizes = [n // k + (1 if r < n % k else 0) for r in range(k)]
+        offs = [sum(sizes[:r]) for r in range(k)]
+        red, mv = defaultdict(list), defaultdict(list)
+        for it in hoc.plan_query(k, hoc.OP_ALLREDUCE, n, dtype, config=cfg):
+            if it["kind"] == hoc.ITEM_REDUCE:
+                red[it["dst_rank"]].append((it["src_off"], it["src_off"] + it["bytes"]))
+            else:
+                mv[(it["src_rank"], it["dst_rank"])].append((it["src_off"], it["src_off"] + it["bytes"]))
+        for r in range(k):
+            iv, ov = _cover(red[r])
+            if sizes[r] == 0:
+                assert not red[r] and not any(mv[(r, d)] for d in range(k))
+                continue
+            assert not ov and _total(iv) == sizes[r] * b and iv[0][0] == offs[r] * b, (trial, r)
+            for d in range(k):
+                if d != r:
+                    iv, ov = _cover(mv[(r, d)])
+                    assert not ov and _total(iv) == sizes[r] * b and iv[0][0] == offs[r] * b, (trial, r, d)
+
+
 def test_flow_size_aware_interleave_spreads_small_flows():
     k = 2
     counts = np.array([[0, 8 * 512], [2 * 512, 0]])        # flows of 8 and 2 chunks of 1 KiB (bf16)
