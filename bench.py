@@ -79,7 +79,8 @@ def generate_inputs(k: int, n: int):
     import multiprocessing as mp
     from concurrent.futures import ProcessPoolExecutor
 
-    workers = max(1, min(k, os.cpu_count() or 1))
+    local_ranks = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))  # replicas on this host share its cores
+    workers = max(1, min(k, (os.cpu_count() or 1) // max(1, local_ranks)))
     with ProcessPoolExecutor(max_workers=workers, mp_context=mp.get_context("spawn")) as ex:
         return list(ex.map(_gen_rank, [(r, n) for r in range(k)]))
 
