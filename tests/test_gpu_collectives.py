@@ -457,3 +457,42 @@ def test_ring_golden_cases(path, engine):
                 assert np.array_equal(got[~nan_w], want[~nan_w]), (c["name"], path, [hex(v) for v in got])
             else:
                 assert np.array_equal(got, want), (c["name"], path, [hex(v) for v in got])
+
+
+@pytest.mark.parametrize("path", ["ce", "tma"])
+def test_alltoallv_explicit_displacements(path):
+    """Segments placed by explicit displacements: reversed order and gaps on both sides; the gaps of the
+    receive buffers keep their fill."""
+    from tests.gpu_util import SENTINEL
+    rng = np.random.default_rng(12)
+    fill = SENTINEL | (SENTINEL << 8)                     # a bf16 element of fill bytes
+    for k in (3, 8):
+        counts = rng.integers(0, 2000, size=(k, k))
+        counts[k - 1, 0] = 0
+        sd = np.zeros((k, k), dtype=np.int64)
+        rd = np.zeros((k, k), dtype=np.int64)
+        for s in range(k):                                # send: destinations in reverse order, gaps of 5
+            at = 7
+            for d in reversed(range(k)):
+                sd[s][d] = at
+                at += counts[s][d] + 5
+        for d in range(k):                                # receive: sources in reverse order, gaps of 3
+            at = 3
+            for s in reversed(range(k)):
+                rd[d][s] = at
+                at += counts[s][d] + 3
+        send_len = [int(max(sd[s][d] + counts[s][d] for d in range(k))) for s in range(k)]
+        recv_len = [int(max(rd[d][s] + counts[s][d] for s in range(k))) for d in range(k)]
+        sends = [rng.integers(0, 1 << 16, size=send_len[s]).astype(np.uint16) for s in range(k)]
+        want = o_a2a.alltoallv(sends, counts, sd, rd, recv_len, fill=fill)
+        with _comm(k, path, chunk_bytes=1024) as c:
+            sb = [Guarded(n, "bfloat16") for n in send_len]
+            rb = [Guarded(n, "bfloat16") for n in recv_len]
+            for g, x in zip(sb, sends):
+                g.load(x)
+            c.alltoall([g.ptr() for g in sb], [g.ptr() for g in rb], sendcounts=counts, sdispls=sd, rdispls=rd,
+                       dtype=hoc.BFLOAT16)
+            c.wait()
+            for d in range(k):
+                rb[d].check()
+                assert_bits_equal(rb[d].host(), want[d], "bfloat16", f"a2a displs {path} k={k} dst {d}")
