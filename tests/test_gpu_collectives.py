@@ -496,3 +496,27 @@ def test_alltoallv_explicit_displacements(path):
             for d in range(k):
                 rb[d].check()
                 assert_bits_equal(rb[d].host(), want[d], "bfloat16", f"a2a displs {path} k={k} dst {d}")
+
+
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
+@pytest.mark.parametrize("engine,budget", [("lsu", 0), ("tma", 0), ("lsu", 4)])
+def test_reduce_scatter_with_a_permuted_ring(dtype, engine, budget):
+    """Block r folds from succ(r) around a non-identity ring, as in the allreduce."""
+    code = hoc.__dict__[dtype.upper()]
+    rng = np.random.default_rng(21)
+    for k in (4, 8):
+        # k = 4: the reversed ring (with k = 3 every ring gives the same bits: (x_a + x_b) + x_r)
+        order = [0, 3, 2, 1] if k == 4 else [int(v) for v in rng.permutation(k)]
+        rc = 4099
+        xs = _inputs(dtype, k, k * rc, seed=17 + k)
+        want = o_ring.reduce_scatter(xs, rc, dtype, order)
+        with _comm(k, ring_order=order, reduce_engine=engine, reduce_max_sms=budget) as c:
+            send = [Guarded(k * rc, dtype) for _ in range(k)]
+            recv = [Guarded(rc, dtype) for _ in range(k)]
+            for g, x in zip(send, xs):
+                g.load(x)
+            c.reduce_scatter([g.ptr() for g in send], [g.ptr() for g in recv], rc, code)
+            c.wait()
+            for r in range(k):
+                recv[r].check()
+                assert_bits_equal(recv[r].host(), want[r], dtype, f"rs ring {order} rank {r}")
