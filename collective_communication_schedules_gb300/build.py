@@ -9,6 +9,7 @@ without a GPU.
 from __future__ import annotations
 
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -20,6 +21,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libhoc.so")
+STAMP = LIB + ".stamp"  # the machine the library was built for: a copy from another machine is rebuilt
 
 SOURCES = ["reduce.cu", "reduce_tma.cu", "tma_copy.cu", "workload.cu", "plan.cpp", "hoc.cpp", "topo_sched.cpp", "proxy.cpp", "ep.cu", "host_ar.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -41,8 +43,18 @@ def _inputs() -> list[str]:
     return files + [os.path.abspath(__file__)]
 
 
+def _machine() -> str:
+    return platform.machine()
+
+
 def up_to_date() -> bool:
     if not os.path.exists(LIB):
+        return False
+    try:
+        with open(STAMP) as f:
+            if f.read().strip() != _machine():
+                return False
+    except OSError:
         return False
     t = os.path.getmtime(LIB)
     return all(os.path.getmtime(f) <= t for f in _inputs())
@@ -74,6 +86,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(_machine() + "\n")
     if verbose:
         print("built", LIB)
     return LIB
