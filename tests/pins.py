@@ -381,3 +381,20 @@ def check_ep_combine_golden(combine):
     for c in load_ep_combine_cases():
         got = np.asarray(combine(c["rows"], c["pos_of"], c["weights"], c["topk"])).reshape(-1)
         assert np.array_equal(got, c["y"]), (c["name"], [hex(int(v)) for v in got])
+
+
+def check_ep_combine_error_bound(pack, combine, rng):
+    """|y - s| <= 2^-8 |s| + (topk + 1) 2^-24 sum |w x| against the exact float64 weighted sum s: one
+    bf16 rounding of a binary32 fold of topk rounded products (standard error bound of recursive sums)."""
+    tokens, topk, hidden = 300, 6, 64
+    ids = np.stack([rng.permutation(16)[:topk] for _ in range(tokens)])
+    x = _narrow_bf16_torch(rng.standard_normal((tokens, hidden)).astype(np.float32))
+    wts = rng.random(tokens * topk).astype(np.float32)
+    send, _, pos_of, _ = pack(x, ids, 16, 4)
+    y = _widen_bf16(combine(send, pos_of, wts, topk)).astype(np.float64)
+    rows = _widen_bf16(send).astype(np.float64)[pos_of.reshape(tokens, topk)]        # [tokens, topk, hidden]
+    w = wts.astype(np.float64).reshape(tokens, topk, 1)
+    s = (w * rows).sum(axis=1)
+    mag = (np.abs(w) * np.abs(rows)).sum(axis=1)
+    bound = 2.0 ** -8 * np.abs(s) + (topk + 1) * 2.0 ** -24 * mag * (1 + 2.0 ** -8)
+    assert np.all(np.abs(y - s) <= bound + 1e-30)

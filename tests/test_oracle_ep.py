@@ -32,3 +32,7 @@ def test_combine_topk1_unit_weight_is_identity():
 
 def test_combine_golden_cases():
     pins.check_ep_combine_golden(ep.combine)
+
+
+def test_combine_within_the_error_bound():
+    pins.check_ep_combine_error_bound(ep.pack, ep.combine, np.random.default_rng(3))

@@ -208,7 +208,8 @@ def test_ep_combine_mistakes_caught(bad):
     from oracle import ep
     assert (_fails(pins.check_ep_combine_golden, bad)
             or _fails(pins.check_ep_combine_scalar, ep.pack, bad, np.random.default_rng(7))
-            or _fails(pins.check_ep_combine_identity, ep.pack, bad, np.random.default_rng(8)))
+            or _fails(pins.check_ep_combine_identity, ep.pack, bad, np.random.default_rng(8))
+            or _fails(pins.check_ep_combine_error_bound, ep.pack, bad, np.random.default_rng(10)))
 
 
 def _pack_tokens_reversed(x, ids, experts, k):
