@@ -42,6 +42,18 @@ int main(void) {
   CHECK(copied == (size_t)(1u << 20) * 2 * 7);  /* and copied to the 7 other ranks */
   printf("allreduce plan ok: %zu items\n", n);
 
+  /* sizes past the library's limits are rejected before any plan: a rank
+   * span above 2^40 bytes, a count whose byte size wraps size_t, and more
+   * than 2^24 chunks per rank buffer */
+  CHECK(hoc_plan_query(8, &cfg, HOC_OP_ALLREDUCE, ((size_t)1 << 39) + 1, HOC_BFLOAT16, NULL, NULL, 0, &n) ==
+        HOC_ERR_INVALID_ARG);
+  CHECK(hoc_plan_query(8, &cfg, HOC_OP_ALLREDUCE, (size_t)-1, HOC_FLOAT32, NULL, NULL, 0, &n) == HOC_ERR_INVALID_ARG);
+  cfg.chunk_bytes = 256;
+  CHECK(hoc_plan_query(8, &cfg, HOC_OP_SENDRECV, ((size_t)1 << 32) + 256, HOC_UINT8, NULL, NULL, 0, &n) ==
+        HOC_ERR_INVALID_ARG);
+  cfg.chunk_bytes = 256 * 1024;
+  printf("size limits ok\n");
+
   /* 4 GPUs in 2 nodes (peers 0-1 and 2-3): GPU 0 sends 100 bytes to GPU 2 and
    * GPU 2 sends 100 to GPU 0.  Each inter-node flow is staged through the
    * sender's peer (Eqs. 2-5), so T carries it on NVLink 0 -> 1 and 2 -> 3 and
