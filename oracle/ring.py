@@ -131,8 +131,17 @@ def sendrecv(x: np.ndarray) -> np.ndarray:
     return np.asarray(x).copy()
 
 
+# The tolerance metric.  The workloads bound the result's error against a
+# float64 naive sum (1e-6 for float32, 8e-3 for bfloat16); int32 results are
+# compared bit for bit, so these functions take floating-point dtypes only.
+def _check_float(dtype: str):
+    if dtype not in TOL:
+        raise ValueError(f"the tolerance metric is defined for {sorted(TOL)}, not {dtype}")
+
+
 def naive_sum_f64(xs: list[np.ndarray], dtype: str) -> np.ndarray:
     """Elementwise float64 sum of all ranks (reference for the error bound)."""
+    _check_float(dtype)
     acc = np.zeros(len(xs[0]), dtype=np.float64)
     for x in xs:
         acc += _widen(x, dtype).astype(np.float64)
@@ -140,6 +149,7 @@ def naive_sum_f64(xs: list[np.ndarray], dtype: str) -> np.ndarray:
 
 
 def abs_sum_f64(xs: list[np.ndarray], dtype: str) -> np.ndarray:
+    _check_float(dtype)
     acc = np.zeros(len(xs[0]), dtype=np.float64)
     for x in xs:
         acc += np.abs(_widen(x, dtype).astype(np.float64))
@@ -149,6 +159,7 @@ def abs_sum_f64(xs: list[np.ndarray], dtype: str) -> np.ndarray:
 def normalized_error(y: np.ndarray, xs: list[np.ndarray], dtype: str) -> np.ndarray:
     """err_i = |y_i - s_i| / sum_r |x_{r,i}|; elements with a zero denominator
     must have y_i == 0 and then score 0 (else +inf)."""
+    _check_float(dtype)
     s = naive_sum_f64(xs, dtype)
     d = abs_sum_f64(xs, dtype)
     yv = _widen(y, dtype).astype(np.float64)

@@ -138,6 +138,35 @@ def check_error_bound(allreduce, normalized_error, xs, dtype, tol):
     return float(err.max())
 
 
+# ------------------------------------------------------- the tolerance metric
+def load_tolerance_cases():
+    cases = []
+    with open(os.path.join(GOLDEN, "tolerance_cases.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            name, dtype, inputs, y, err = [p.strip() for p in line.split("|")]
+            npdt, view = {"float32": (np.uint32, np.float32), "bfloat16": (np.uint16, np.uint16)}[dtype]
+            xs = [np.array([int(v, 16) for v in rank.split(",")], dtype=npdt).view(view) for rank in inputs.split(";")]
+            yv = np.array([int(v, 16) for v in y.split(",")], dtype=npdt).view(view)
+            want = [None if e == "inf" else Fraction(e) for e in err.split(",")]
+            cases.append(dict(name=name, dtype=dtype, xs=xs, y=yv, err=want))
+    return cases
+
+
+def check_tolerance_golden(normalized_error):
+    """The metric on the hand-derived cases, compared exactly (None = +inf)."""
+    for c in load_tolerance_cases():
+        got = np.asarray(normalized_error(c["y"], c["xs"], c["dtype"]), dtype=np.float64)
+        assert got.shape == (len(c["err"]),), c["name"]
+        for i, want in enumerate(c["err"]):
+            if want is None:
+                assert np.isposinf(got[i]), (c["name"], i, got[i])
+            else:
+                assert got[i] == float(want), (c["name"], i, got[i], float(want))
+
+
 def check_k1_k2(allreduce, rng):
     x = rng.standard_normal(33).astype(np.float32)
     assert np.array_equal(allreduce([x], "float32", None)[0].view(np.uint32), x.view(np.uint32))

@@ -241,3 +241,34 @@ def _pack_round_robin_ranks(x, ids, experts, k):
 @pytest.mark.parametrize("bad", [_pack_tokens_reversed, _pack_clip_instead_of_drop, _pack_round_robin_ranks])
 def test_ep_pack_mistakes_caught(bad):
     assert _fails(pins.check_ep_pack_brute, bad, np.random.default_rng(9))
+
+
+# ------------------------------------------------------------ tolerance metric
+def _error_with(num=None, den=None, widen=None, zero=None):
+    """normalized_error with one part replaced: numerator, denominator, operand widening or zero rule."""
+    def normalized_error(y, xs, dtype):
+        wid = widen or (lambda a: ring._widen(a, dtype).astype(np.float64))
+        s = sum(wid(x) for x in xs)
+        d = den(xs, wid) if den else sum(np.abs(wid(x)) for x in xs)
+        yv = wid(y)
+        e = num(yv, s) if num else np.abs(yv - s)
+        out = np.zeros(len(yv))
+        nz = d > 0
+        out[nz] = e[nz] / d[nz]
+        out[~nz] = zero(yv[~nz]) if zero else np.where(yv[~nz] == 0, 0.0, np.inf)
+        return out
+    return normalized_error
+
+
+@pytest.mark.parametrize("bad", [
+    _error_with(den=lambda xs, wid: np.abs(sum(wid(x) for x in xs))),            # |s| instead of sum |x|
+    _error_with(num=lambda yv, s: np.abs(yv - yv)),                               # y compared with itself
+    _error_with(den=lambda xs, wid: sum(wid(x) for x in xs)),                     # the absolute value dropped
+    _error_with(num=lambda yv, s: np.abs(yv + s)),                                # sign slip in the numerator
+    _error_with(widen=lambda a: np.asarray(a).astype(np.float64)),                # bf16 bit patterns read as integers
+    _error_with(widen=lambda a: ring._widen(a, "float32" if np.asarray(a).dtype == np.float32 else "bfloat16")
+                .astype(np.float32)),                                             # sums in float32, not float64
+    _error_with(zero=lambda yv: np.where(yv == 0, np.inf, 0.0)),                  # zero-denominator rule inverted
+])
+def test_tolerance_metric_mistakes_caught(bad):
+    assert _fails(pins.check_tolerance_golden, bad)

@@ -50,6 +50,16 @@ def test_int32_wraps():
     pins.check_int32_wrap(ring.allreduce, np.random.default_rng(5))
 
 
+def test_tolerance_metric_golden_cases():
+    pins.check_tolerance_golden(ring.normalized_error)
+
+
+def test_tolerance_metric_refuses_int32():
+    # int32 results are compared bit for bit; the metric is defined for floating point only
+    with pytest.raises(ValueError):
+        ring.normalized_error(np.zeros(2, np.int32), [np.zeros(2, np.int32)] * 2, "int32")
+
+
 def test_error_bound_fp32_small_workload():
     w = inputs.AR_SMALL
     xs = inputs.rank_inputs("float32", w["k"], w["n"], workload=1)
