@@ -43,6 +43,7 @@ SIGMA = 1e-3
 WORKLOAD = ("ring allreduce (sum), 8 simulated ranks, 134,217,728 bf16 elements (256 MiB) per rank, "
             "N(0, 1e-3), fp32 accumulation")
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0      # GB300 HBM3e, nominal
 
 
 def parse():
@@ -224,14 +225,32 @@ def bus_bytes(k: int, per_rank_bytes: int) -> float:
 
 
 # ------------------------------------------------------------- CPU baseline
+CPU_SAMPLE = 8 << 20   # elements per rank the oracle folds: the first 8,388,608 of every rank's buffer
+
+
+def cpu_sample_text(reps=None, secs=None):
+    """The one definition of the oracle's sample, shared by cpu_baseline and the reference arm."""
+    s = (f"numpy ring-order fold of the first {CPU_SAMPLE:,} of the {N_ELEMS:,} bf16 elements per rank "
+         f"(8 ranks, 1/{N_ELEMS // CPU_SAMPLE} of the workload)")
+    if reps is not None:
+        s += f", {reps} repetitions, {secs:.3f} s each"
+    return s + f"; host has {os.cpu_count()} cores, numpy elementwise runs on 1"
+
+
+def oracle_config():
+    """`config` of both arms: the workload, not how either arm runs it."""
+    return {"workload": WORKLOAD, "k": K_RANKS, "count": N_ELEMS,
+            "l2": "no flush: each step reads 2 GiB of inputs and writes 2 GiB, > 129 MB L2",
+            "parallelism": "independent replicas, one per GPU"}
+
+
 def cpu_baseline(xs_host, seconds: float, device_out=None):
-    """The oracle, as it stands, on the first quarter of every rank's buffer."""
+    """The oracle, as it stands, on the CPU_SAMPLE elements at the start of every rank's buffer."""
     import numpy as np
 
     from oracle import ring
 
-    total = len(xs_host[0])
-    n = total // 4
+    n = CPU_SAMPLE
     xs = [x[:n] for x in xs_host]
     t0 = time.perf_counter()
     reps = 0
@@ -243,10 +262,7 @@ def cpu_baseline(xs_host, seconds: float, device_out=None):
             break
     dt = (time.perf_counter() - t0) / reps
     out = {"value": round(bus_bytes(K_RANKS, n * 2) / dt / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
-           "sample": f"numpy ring-order fold of the first {n:,} of {total:,} bf16 elements per rank "
-                     f"(8 ranks), {reps} repetitions, {dt:.2f} s each; host has {os.cpu_count()} cores, "
-                     "numpy elementwise runs on 1",
-           "seconds_per_step": round(dt, 4)}
+           "sample": cpu_sample_text(reps, dt), "seconds_per_step": round(dt, 4)}
     if device_out is not None:
         # The GPU result on the same sample must equal the oracle bit for bit.
         import torch
@@ -279,14 +295,14 @@ def cpu_baseline_buckets(host_pool, buckets: int = 16):
 
 
 def run_reference(args, world, rank):
-    """--impl reference: the oracle as the reference arm (rank 0 only)."""
+    """--impl reference: the oracle as the reference arm (rank 0 only), on the same sample as cpu_baseline."""
     if rank != 0:
         return
     from collective_communication_schedules_gb300 import inputs
     from oracle import ring
 
-    n = 8 << 20
-    xs = [inputs.normal_bf16(n, inputs.seed_for(2, 0, r), SIGMA) for r in range(K_RANKS)]
+    n = CPU_SAMPLE
+    xs = [inputs.normal_bf16(n, inputs.seed_for(2, 0, r), SIGMA) for r in range(K_RANKS)]   # the draws' first n
     for _ in range(args.warmup):
         ring.allreduce(xs, "bfloat16")
     t0 = time.perf_counter()
@@ -294,14 +310,12 @@ def run_reference(args, world, rank):
         ring.allreduce(xs, "bfloat16")
     dt = (time.perf_counter() - t0) / args.steps
     v = bus_bytes(K_RANKS, n * 2) / dt / 1e9
-    sample = (f"numpy ring-order fold of 8,388,608 of the 134,217,728 bf16 elements per rank (8 ranks) per step; "
-              f"host has {os.cpu_count()} cores, numpy elementwise runs on 1")
     line = {"metric": METRIC, "value": round(v, 3), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "k": K_RANKS, "count": N_ELEMS, "sample_count": n},
-            "impl": "reference",
-            "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "config": oracle_config(), "impl": "reference",
+            "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": cpu_sample_text() + "; one fold per step"},
             "e2e": {"value": round(v, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -821,8 +835,11 @@ def run_ours(args, world, rank, local):
                 "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4) if achieved else None,
                 "traffic": recorded_traffic(kname, k, n_el), "bytes_per_launch": kern_bytes,
                 "avg_launch_ms": round(avg_launch_ms, 4), "launches": launches,
-                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
-                if peak_kind == "measured" else "fallback 6.8 TB/s"}
+                "peak_source": f"{peak_kind}: MEASURED_PEAKS.json hbm_gbs, the copy rate a STREAM-style copy reaches "
+                               "on this GPU (an empirical ceiling, which a kernel can slightly exceed)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s",
+                "nominal_peak": NOMINAL_HBM_GBS,
+                "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4) if achieved else None}
 
     # ---- end to end: pinned host inputs -> device, allreduce, results -> host
     # End to end through the host-buffer call: every step brings the 2 GiB of
@@ -983,12 +1000,11 @@ def run_ours(args, world, rank, local):
         line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": WORKLOAD if n_el == N_ELEMS else f"profiling case: 8 ranks x {n_el:,} bf16",
-                           "k": k, "count": n_el, "path": args.path,
-                           "resolved_path": {0: "auto", 1: "ce", 2: "tma", 3: "fused"}[st["path"]],
-                           "chunk_bytes": args.chunk_bytes or "auto (4 MiB)", "copy_streams": args.copy_streams,
-                           "l2": "no flush: each step reads 2 GiB of inputs and writes 2 GiB, > 129 MB L2",
-                           "parallelism": f"{world} independent replica(s), one per GPU"},
+                "config": oracle_config() if n_el == N_ELEMS else
+                {"workload": f"profiling case: 8 ranks x {n_el:,} bf16", "k": k, "count": n_el},
+                "schedule": {"path": args.path,
+                             "resolved_path": {0: "auto", 1: "ce", 2: "tma", 3: "fused"}[st["path"]],
+                             "chunk_bytes": args.chunk_bytes or "auto (4 MiB)", "copy_streams": args.copy_streams},
                 "algbw_gbs": round(per_rank / (ms_max * 1e-3) / 1e9, 2),
                 "hbm_frac": round(hbm_frac, 4), "lower_bound_frac": round(lb_frac, 4),
                 "sms_used": st["sms_used"], "gpu_launches": st["kernels"] * args.steps,

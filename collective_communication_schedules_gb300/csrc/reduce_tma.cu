@@ -7,7 +7,7 @@
 //   * one producer thread per CTA streams the k operand tiles of a work tile
 //     (tile_bytes each, operand j = ring position j) into a shared-memory
 //     stage with cp.async.bulk, completing on that stage's "full" mbarrier;
-//   * four consumer warps fold the k tiles vector by vector from shared
+//   * eight consumer warps fold the k tiles vector by vector from shared
 //     memory, store each folded 16-byte vector straight to the owner's buffer
 //     (or to all k buffers: the fused allreduce, with streaming stores), and
 //     release the stage on its "empty" mbarrier;

@@ -135,33 +135,6 @@ def ep_routing(k: int, tokens: int, experts: int, topk: int, s: float,
     return out
 
 
-def ep_pack(routing: np.ndarray, tokens_x: np.ndarray, experts: int, k: int):
-    """Expand (token, slot) rows and sort them stably by (dst rank, expert, token, slot).
-
-    ``tokens_x`` is [tokens, hidden] bf16 bits.  Returns the packed send rows
-    [tokens*topk, hidden], the row order (token, slot) and the per-destination
-    row counts (length k).
-    """
-    tokens, topk = routing.shape
-    per_rank = experts // k
-    tok = np.repeat(np.arange(tokens), topk)
-    slot = np.tile(np.arange(topk), tokens)
-    exp = routing.reshape(-1)
-    dst = exp // per_rank
-    order = np.lexsort((slot, tok, exp, dst))
-    packed = tokens_x[tok[order]]
-    counts = np.bincount(dst[order], minlength=k).astype(np.int64)
-    return np.ascontiguousarray(packed), np.stack([tok[order], slot[order]], 1), counts
-
-
-def ep_inputs(k: int, tokens: int, hidden: int, experts: int, topk: int, s: float,
-              seed_base: int = 5000):
-    """Packed send buffers (bf16 bits, [rows, hidden]) and the k x k row-count matrix."""
-    routing = ep_routing(k, tokens, experts, topk, s, seed_base)
-    sends, counts = [], np.zeros((k, k), dtype=np.int64)
-    for r in range(k):
-        x = normal_bf16(tokens * hidden, seed_base + 500 + r).reshape(tokens, hidden)
-        packed, _, c = ep_pack(routing[r], x, experts, k)
-        sends.append(packed)
-        counts[r] = c
-    return sends, counts, routing
+def ep_token_rows(k: int, tokens: int, hidden: int, seed_base: int = 5000) -> list[np.ndarray]:
+    """Per source rank, the token rows [tokens, hidden] as bf16 bits, N(0, 1)."""
+    return [normal_bf16(tokens * hidden, seed_base + 500 + r).reshape(tokens, hidden) for r in range(k)]

@@ -359,6 +359,20 @@ def check_ep_pack_brute(pack, rng, trials=20):
         assert all(pos_of[p] == -1 for p in range(tokens * topk) if p not in set(bperm))
 
 
+def check_ep_pack_four_key_sort(pack, x, ids, experts, k):
+    """The pack order as a sort on the four keys (destination rank, expert, token, slot) spelled out."""
+    tokens, topk = ids.shape
+    tok = np.repeat(np.arange(tokens), topk)
+    slot = np.tile(np.arange(topk), tokens)
+    exp = np.asarray(ids).reshape(-1)
+    dst = exp // (experts // k)
+    order = np.lexsort((slot, tok, exp, dst))                 # last key is the primary one
+    send, perm, _, counts = pack(x, ids, experts, k)
+    assert np.array_equal(perm, tok[order] * topk + slot[order])
+    assert np.array_equal(send, x[tok[order]])
+    assert np.array_equal(counts, np.bincount(dst, minlength=k) * x.shape[1])
+
+
 def check_ep_combine_scalar(pack, combine, rng):
     """Every output element by a scalar loop of numpy binary32 products and sums, narrowed by PyTorch."""
     tokens, topk, hidden = 7, 3, 5

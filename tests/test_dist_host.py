@@ -63,3 +63,7 @@ def test_reference_arm_under_torchrun_prints_one_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+    # the same workload description and the same oracle sample as the GPU arm's cpu_baseline
+    import bench
+    assert d["config"] == bench.oracle_config()
+    assert d["cpu_baseline"]["sample"].startswith(bench.cpu_sample_text().split(";")[0])

@@ -20,6 +20,7 @@ import torch
 from collective_communication_schedules_gb300 import hoc, inputs
 from collective_communication_schedules_gb300.pipeline import Pipeline1F1B
 from oracle import alltoall as o_a2a
+from oracle import ep as o_ep
 from oracle import pipeline as o_pp
 from oracle import ring as o_ring
 from tests.gpu_util import assert_bits_equal, to_device, to_host
@@ -163,7 +164,11 @@ def test_pipeline_1f1b_workload(path, sends):
 @pytest.fixture(scope="module")
 def ep_data():
     w = inputs.EP_DISPATCH
-    sends, counts, routing = inputs.ep_inputs(w["k"], w["tokens"], w["hidden"], w["experts"], w["topk"], w["zipf"])
+    routing = inputs.ep_routing(w["k"], w["tokens"], w["experts"], w["topk"], w["zipf"])
+    xs = inputs.ep_token_rows(w["k"], w["tokens"], w["hidden"])
+    packs = [o_ep.pack(xs[r], routing[r], w["experts"], w["k"]) for r in range(w["k"])]
+    sends = [p[0] for p in packs]
+    counts = np.stack([p[3] for p in packs]) // w["hidden"]         # rows per (source, destination)
     return w, sends, counts, routing
 
 
