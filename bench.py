@@ -343,7 +343,7 @@ PROBE_SHAPES = {
 PROBE_KERNELS = 40          # the probe is a train of one-wave kernels, ~0.25 ms each
 
 
-def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int, shape: str = "whole_sm"):
+def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int, shape: str = "whole_sm", n_kernels: int = 0):
     """Slowdown of the FMA probe train while the collective runs back to back beside it.
 
     The probe is a train of short one-wave kernels, like a sequence of layer
@@ -357,6 +357,7 @@ def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int, shape: str = "w
 
     cfg = PROBE_SHAPES[shape]
     ctas, threads, whole = cfg["ctas_per_sm"] * sms, cfg["threads"], cfg["whole_sm"]
+    nk = n_kernels or PROBE_KERNELS
     sp = torch.cuda.Stream()
     gate = torch.cuda.Stream()
     sink = torch.zeros(4, dtype=torch.float32, device="cuda")
@@ -374,7 +375,7 @@ def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int, shape: str = "w
             for _ in range(n_coll):
                 run_coll(stream_c)
         a.record(sp)
-        for _ in range(PROBE_KERNELS):
+        for _ in range(nk):
             hoc.probe_launch(ctas, threads, iters, stream=sp, whole_sm=whole, sink=sink)
         b.record(sp)
         torch.cuda.synchronize()
@@ -391,15 +392,85 @@ def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int, shape: str = "w
     n_coll = int(math.ceil(1.5 * alone / max(coll_ms, 1e-3))) + 2
     with_c = statistics.median(run_probe(iters, True, n_coll) for _ in range(3))
     mhz_with = [m for m in mhz if m]
-    return {"shape": f"{PROBE_KERNELS} kernels x {ctas} CTAs x {threads} threads" + (", whole SM each" if whole else ""),
+    return {"shape": f"{nk} kernels x {ctas} CTAs x {threads} threads" + (", whole SM each" if whole else ""),
             "probe_alone_ms": round(alone, 3), "probe_with_ms": round(with_c, 3),
             "slowdown": round(with_c / alone - 1.0, 4), "collectives_beside": n_coll,
             "sm_mhz_alone": round(statistics.median(mhz_alone), 1) if mhz_alone else None,
             "sm_mhz_with": round(statistics.median(mhz_with), 1) if mhz_with else None}
 
 
-def probes(run_coll, coll_ms, stream_c, sms):
-    return {shape: probe_slowdown(run_coll, coll_ms, stream_c, sms, shape) for shape in PROBE_SHAPES}
+def probes(run_coll, coll_ms, stream_c, sms, n_kernels=0):
+    return {shape: probe_slowdown(run_coll, coll_ms, stream_c, sms, shape, n_kernels) for shape in PROBE_SHAPES}
+
+
+def leg_ce_interference(send, recv, n_el, k, local, stream, sms):
+    """What slows the probe train beside copy-engine moves that use no SM.
+
+    (a) the same probe work as 10 / 40 / 160 kernels beside the default moves:
+        a cost paid per kernel launch grows with the count;
+    (b) copy size x copy queues of the all-gather moves (8 x 32 MiB blocks);
+    (c) the probe's own SM clock (cycles / ns in its first CTA) with each;
+    (d) 512 KiB copies whose buffers stay in L2 against 512 KiB copies through HBM:
+        separates the copies' HBM traffic from their number and size;
+    (e) the default moves issued copy by copy instead of as one CUDA graph per call.
+    """
+    import torch
+
+    from collective_communication_schedules_gb300 import hoc
+
+    blk = n_el // k
+
+    def moves(chunk, nq, block=blk, graphs=True):
+        c = hoc.Comm(k, local, hoc.Config(path="ce", chunk_bytes=chunk, n_copy_streams=nq, use_graphs=graphs))
+        s_ = [t[:block] for t in send]
+        r_ = [t[:k * block] for t in recv]
+        run = lambda st, c=c: c.allgather(s_, r_, stream=st)
+        for _ in range(3):
+            run(stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(10):
+            run(stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / 10
+        st = c.last_stats()
+        return c, run, ms, {"ms": round(ms, 4), "bytes_gbs": round(st["bytes_exec"] / (ms * 1e-3) / 1e9, 1),
+                            "copies_per_call": st["copies"], "kernels_per_call": st["kernels"]}
+
+    def slow(pr):
+        return {sh: pr[sh]["slowdown"] for sh in pr}
+
+    def mhz(pr):
+        return {sh: [pr[sh]["sm_mhz_alone"], pr[sh]["sm_mhz_with"]] for sh in pr}
+
+    out = {"launch_count": [], "copy_shape": [], "l2_vs_hbm": [], "issue": []}
+    c, run, ms, info = moves(4 << 20, 4)
+    for nk in (10, 40, 160):
+        pr = probes(run, ms, stream, sms, nk)
+        out["launch_count"].append({"probe_kernels": nk, "slowdown": slow(pr), "sm_mhz_alone_with": mhz(pr),
+                                    "probe_alone_ms": {sh: pr[sh]["probe_alone_ms"] for sh in pr}})
+    c.close()
+    for mib, nq in ((4, 4), (4, 8), (4, 16), (2, 8), (2, 16), (8, 8), (8, 16), (16, 16)):
+        c, run, ms, info = moves(mib << 20, nq)
+        pr = probes(run, ms, stream, sms)
+        out["copy_shape"].append(dict(chunk_mib=mib, copy_streams=nq, slowdown=slow(pr), sm_mhz_alone_with=mhz(pr),
+                                      **info))
+        c.close()
+    small = 512 << 10
+    for label, block in (("l2_resident", small), ("hbm", blk)):
+        # l2_resident: 8 blocks of 512 KiB gathered to 8 ranks (36 MiB in all, inside L2)
+        c, run, ms, info = moves(small, 4, block=block)
+        pr = probes(run, ms, stream, sms)
+        out["l2_vs_hbm"].append(dict(buffers=label, chunk_kib=512, copy_streams=4, slowdown=slow(pr), **info))
+        c.close()
+    for graphs in (True, False):
+        c, run, ms, info = moves(4 << 20, 4, graphs=graphs)
+        pr = probes(run, ms, stream, sms)
+        out["issue"].append(dict(graphs=graphs, slowdown=slow(pr), **info))
+        c.close()
+    return out
 
 
 # ------------------------------------------------------ the other workloads
@@ -675,12 +746,50 @@ def leg_expert_dispatch(peak):
     return out
 
 
+SWEEP_ROTATION_BYTES = 320 << 20   # > 2x the 126 MB L2: each timed pass cycles through this much memory
+
+
+def _sweep_call(c, hoc, op, src, dst, k, n, reg, stream):
+    """One op of the sweep on region `reg` of the rank buffers (every region is n bytes per rank)."""
+    o = reg * n
+    if op == "p2p":
+        c.sendrecv(0, src[0][o:], 1, dst[1][o:], n, hoc.UINT8, stream=stream)
+    elif op == "allgather":
+        cs = n // k
+        c.allgather([t[reg * cs:] for t in src], [t[o:] for t in dst], cs, hoc.UINT8, stream=stream)
+    else:
+        c.alltoall([t[o:] for t in src], [t[o:] for t in dst], count=n // k, dtype=hoc.UINT8, stream=stream)
+
+
+def _sweep_footprint(op, n, k):
+    """Bytes one op reads and writes (all ranks)."""
+    return {"p2p": 2 * n, "allgather": n + k * n, "alltoall": 2 * k * n}[op]
+
+
+def _sweep_verify(torch, op, src, dst, k, n):
+    """Region 0 of the destinations holds exactly what the op must deliver."""
+    if op == "p2p":
+        return bool(torch.equal(dst[1][:n], src[0][:n]))
+    cs = n // k
+    for d in range(k):
+        for r in range(k):
+            want = src[r][:cs] if op == "allgather" else src[r][d * cs:(d + 1) * cs]
+            if not torch.equal(dst[d][r * cs:(r + 1) * cs], want):
+                return False
+    return True
+
+
 def leg_sweeps(sms):
     """Bandwidth vs size, 2 MB - 1 GB: copy engines vs TMA (all SMs, or 1/2/4/8 SMs).
 
     Sizes follow the nccl-tests convention of the paper's benchmarks: P2P = the
     message, AllGather = each rank's receive buffer, All-to-All = each rank's
-    send buffer; algorithm bandwidth = size / time.  8 simulated ranks.
+    send buffer; algorithm bandwidth = size / time.  8 simulated ranks.  Each
+    timed pass is one CUDA graph of back-to-back ops that cycle through
+    regions of the rank buffers totalling >= 320 MB, so every op reads and
+    writes HBM, not L2; the L2-warm figures (the same region every time) are
+    separate rows for the sizes L2 can hold.  After timing, every point is
+    run once more into zeroed destinations and checked byte for byte.
     """
     import torch
 
@@ -688,42 +797,162 @@ def leg_sweeps(sms):
 
     k = 8
     sizes_mb = [2, 8, 32, 128, 512, 1024]
+    l2_sizes_mb = [2, 8, 32]
     variants = [("ce", 0), ("tma", 0), ("tma", 1), ("tma", 2), ("tma", 4), ("tma", 8)]
     big = max(sizes_mb) << 20
-    src = [torch.empty(big, dtype=torch.uint8, device="cuda") for _ in range(k)]
-    dst = [torch.empty(big, dtype=torch.uint8, device="cuda") for _ in range(k)]
-    for t in src:
-        t.fill_(7)
+    g = torch.Generator(device="cuda").manual_seed(77)
+    src = [torch.randint(0, 256, (big,), dtype=torch.uint8, device="cuda", generator=g) for _ in range(k)]
+    dst = [torch.zeros(big, dtype=torch.uint8, device="cuda") for _ in range(k)]
     stream = torch.cuda.Stream()
-    out = {"sizes_mb": sizes_mb, "p2p": {}, "allgather": {}, "alltoall": {}}
+    out = {"sizes_mb": sizes_mb, "l2": f"each timed pass cycles through >= {SWEEP_ROTATION_BYTES >> 20} MB of "
+                                        "buffers (> 2x L2); the *_l2_warm rows reuse one region",
+           "p2p": {}, "allgather": {}, "alltoall": {}, "regions_per_pass": {},
+           "p2p_l2_warm": {}, "allgather_l2_warm": {}, "alltoall_l2_warm": {}, "l2_warm_sizes_mb": l2_sizes_mb,
+           "verified": {}}
+
+    def timed_graph(c, op, n, regions):
+        with torch.cuda.stream(stream):
+            for reg in sorted(set(regions)):                      # plans built outside the capture
+                _sweep_call(c, hoc, op, src, dst, k, n, reg, stream)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for reg in regions:
+                _sweep_call(c, hoc, op, src, dst, k, n, reg, stream)
+        runs = []
+        for i in range(4):                                        # one untimed replay, then the median of three
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            if i:
+                runs.append(e0.elapsed_time(e1))
+        del graph
+        return statistics.median(runs) / len(regions)
+
     for path, ctas in variants:
         name = path if ctas == 0 else f"{path}_{ctas}sm"
         c = hoc.Comm(k, torch.cuda.current_device(), hoc.Config(path=path, copy_max_sms=ctas))
         for op in ("p2p", "allgather", "alltoall"):
-            row = []
+            row, warm, regs, ok = [], [], [], True
             for mb in sizes_mb:
                 n = mb << 20
-                if op == "p2p":
-                    run = lambda n=n: c.sendrecv(0, src[0], 1, dst[1], n, hoc.UINT8, stream=stream)
-                elif op == "allgather":
-                    run = lambda n=n: c.allgather(src, dst, n // k, hoc.UINT8, stream=stream)
-                else:
-                    run = lambda n=n: c.alltoall(src, dst, count=n // k, dtype=hoc.UINT8, stream=stream)
-                run()
-                torch.cuda.synchronize()
-                reps = 3 if mb >= 512 else 10
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                for _ in range(reps):
-                    run()
-                e1.record(stream)
-                torch.cuda.synchronize()
-                ms = e0.elapsed_time(e1) / reps
+                nreg = max(1, min(big // n, -(-SWEEP_ROTATION_BYTES // _sweep_footprint(op, n, k))))
+                reps = max(nreg, 3 if mb >= 512 else 10)
+                ms = timed_graph(c, op, n, [i % nreg for i in range(reps)])
                 row.append(round(n / (ms * 1e-3) / 1e9, 1))
+                regs.append(nreg)
+                if mb in l2_sizes_mb:
+                    wms = timed_graph(c, op, n, [0] * 10)
+                    warm.append(round(n / (wms * 1e-3) / 1e9, 1))
+                with torch.cuda.stream(stream):                   # zeroed on the stream the op runs on
+                    for t in dst:
+                        t[:n].zero_()
+                    _sweep_call(c, hoc, op, src, dst, k, n, 0, stream)
+                torch.cuda.synchronize()
+                ok = ok and _sweep_verify(torch, op, src, dst, k, n)
             out[op][name] = row
+            out[op + "_l2_warm"][name] = warm
+            out["regions_per_pass"].setdefault(op, regs)
+            out["verified"].setdefault(op, {})[name] = ok
         c.close()
     del src, dst
     torch.cuda.empty_cache()
+    return out
+
+
+def leg_ce_allreduce_timeline(send, recv, k, local, stream, per_rank, peak):
+    """When each chunk of the copy-engine allreduce is reduced and moved (the per-step timeline).
+
+    One call with profiling on (events around every step; no graph), after a
+    few unprofiled ones.  Per chunk: the reduce kernel's start and end on the
+    caller's stream, and the first start and last end of that chunk's copies
+    over the copy queues.  Beside it, what the schedule's bytes cost at the
+    measured copy rate: (3k - 1) S with no L2 reuse, 2kS if every all-gather
+    read of a freshly reduced chunk hit L2.
+    """
+    import torch
+
+    from collective_communication_schedules_gb300 import hoc
+
+    out = {}
+    for depth in (0, 2):
+        with hoc.Comm(k, local, hoc.Config(path="ce", pipeline_depth=depth)) as c:
+            for _ in range(3):
+                c.allreduce(send, recv, stream=stream)
+            ms = time_allreduce(c, send, recv, stream, 5)
+            c.profile_enable(True)
+            c.allreduce(send, recv, stream=stream)
+            tl = c.profile_timeline()
+            c.profile_enable(False)
+            torch.cuda.synchronize()
+        chunks = sorted({t["stage"] for t in tl})
+        rows = []
+        for q in chunks:
+            red = [t for t in tl if t["stage"] == q and t["kind"] == "reduce"]
+            mv = [t for t in tl if t["stage"] == q and t["kind"] == "copy"]
+            rows.append({"chunk": q,
+                         "reduce_ms": [round(red[0]["start_ms"], 4), round(red[0]["end_ms"], 4)] if red else None,
+                         "moves_ms": [round(min(t["start_ms"] for t in mv), 4), round(max(t["end_ms"] for t in mv), 4)]
+                         if mv else None})
+        end = max(t["end_ms"] for t in tl)
+        red_busy = sum(t["end_ms"] - t["start_ms"] for t in tl if t["kind"] == "reduce")
+        out[f"depth_{depth or 'unbounded'}"] = {
+            "ms_unprofiled": round(ms, 4), "ms_profiled": round(end, 4), "reduce_busy_ms": round(red_busy, 4),
+            "chunks": rows}
+    S = per_rank
+    out["bytes_at_measured_copy_rate_ms"] = {
+        "3k-1_S_no_l2_reuse": round((3 * k - 1) * S / (peak * 1e9) * 1e3, 4),
+        "2kS_full_l2_reuse": round(2 * k * S / (peak * 1e9) * 1e3, 4)}
+    return out
+
+
+def leg_startup_latency():
+    """Time of ONE small copy, alone: copy engine vs the TMA kernel on 1 CTA and on every SM.
+
+    HOCCL section 1 puts the DMA engines' startup latency at about 5x that of an
+    SM-driven copy.  Each trial queues a ~80 us spin kernel first, so the
+    events bracket only the copy (the host's issue of it is hidden behind the
+    spin); the figure is the median over 50 trials minus the median of the
+    same window with nothing in it.
+    """
+    import torch
+
+    from collective_communication_schedules_gb300 import hoc
+
+    sizes = [4 << 10, 16 << 10, 64 << 10, 256 << 10, 1 << 20]
+    a = torch.randint(0, 256, (1 << 20,), dtype=torch.uint8, device="cuda")
+    b = torch.zeros_like(a)
+    stream = torch.cuda.Stream()
+    sink = torch.zeros(4, dtype=torch.float32, device="cuda")
+
+    def window(fn, trials=50):
+        ts = []
+        for _ in range(trials):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            hoc.probe_launch(1, 32, 40000, stream=stream, sink=sink)     # keeps the GPU busy while we queue
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.median(ts)
+
+    empty = window(lambda: None)
+    out = {"sizes_bytes": sizes, "empty_window_us": round(empty, 2), "us": {}}
+    for name, path, ctas in (("ce", "ce", 0), ("tma_1cta", "tma", 1), ("tma_all_sms", "tma", 0)):
+        with hoc.Comm(2, torch.cuda.current_device(), hoc.Config(path=path, copy_max_sms=ctas)) as c:
+            row = []
+            for n in sizes:
+                fn = lambda n=n: c.sendrecv(0, a, 1, b, n, hoc.UINT8, stream=stream)
+                fn()
+                torch.cuda.synchronize()
+                row.append(round(max(0.0, window(fn) - empty), 2))
+            out["us"][name] = row
+    out["ce_over_tma_1cta"] = [round(x / y, 2) if y > 0 else None for x, y in zip(out["us"]["ce"], out["us"]["tma_1cta"])]
+    out["verified"] = bool(torch.equal(a, b))
     return out
 
 
@@ -949,6 +1178,7 @@ def run_ours(args, world, rank, local):
         extras["paths"] = paths
         extras["allgather_moves"] = ag
         extras["allgather_ce_chunk_vs_probe"] = tradeoff
+        extras["ce_interference"] = leg_ce_interference(send, recv, n_el, k, local, stream, sms)
         # chunk size sweep, 1-64 MiB (64 is capped at the 32 MiB block), on the copy-engine and
         # TMA-kernel move paths; then copy-queue counts on the copy-engine path
         sweep = []
@@ -984,6 +1214,7 @@ def run_ours(args, world, rank, local):
                                "sms_used": s6["sms_used"], "copies_per_step": s6["copies"]})
                 c6.close()
         extras["allreduce_under_sm_budget"] = budget
+        extras["ce_allreduce_timeline"] = leg_ce_allreduce_timeline(send, recv, k, local, stream, per_rank, peak)
     if args.workloads and not args.no_extras:
         extras["workloads"] = {"dp_bucket_stream": leg_bucket_stream(bucket_pool, sms, peak),
                                "pp_1f1b": leg_pipeline(sms),
@@ -991,6 +1222,7 @@ def run_ours(args, world, rank, local):
         extras["workloads"]["dp_bucket_stream"]["cpu_baseline"] = cpu_baseline_buckets(bucket_pool)
         bucket_pool = None
         extras["sweeps"] = leg_sweeps(sms)
+        extras["startup_latency"] = leg_startup_latency()
         extras["host_overhead_us"] = leg_host_overhead()
 
     cpu = None

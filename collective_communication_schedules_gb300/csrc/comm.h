@@ -68,6 +68,16 @@ struct hocComm {
   cudaEvent_t prof_fork = nullptr;
   std::vector<cudaEvent_t> prof_stream_end;
   int prof_streams = 0;  // copy streams the last profiled call used (0: none)
+  // While profiling: the fork of the last profiled call (recorded on the
+  // caller's stream before anything else) and an event pair around each of its
+  // steps, recorded on the step's stream after its waits.
+  cudaEvent_t prof_origin = nullptr;
+  struct StepTiming {
+    int kind, stream, stage;
+    cudaEvent_t start, end;
+  };
+  std::vector<StepTiming> prof_steps;
+  std::vector<cudaEvent_t> prof_step_events;  // pool, reused call after call
   int reduce_ctas_per_sm[3][hoc::kMaxRanks + 1][2] = {};
   hoc::Proxy* proxy = nullptr;  // created by the first device-count all-to-all
   unsigned detached_next = 0;   // copy stream of the next hoc_sendrecv_async

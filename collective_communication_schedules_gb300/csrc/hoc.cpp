@@ -320,7 +320,17 @@ hocResult_t issue(hocComm* c, const Plan& p, const Bind& bd, cudaStream_t s0, co
     for (int i = 1; i < p.n_streams; ++i) st[i] = given ? (*given)[i - 1] : (*copy)[i - 1];
   }
   const bool prof_streams = c->profiling && p.n_streams > 1;
-  if (c->profiling) c->prof_streams = 0;
+  if (c->profiling) {
+    c->prof_streams = 0;
+    c->prof_steps.clear();
+    if (!c->prof_origin) HOC_CK(cudaEventCreate(&c->prof_origin));
+    while (c->prof_step_events.size() < 2 * p.steps.size()) {
+      cudaEvent_t e;
+      HOC_CK(cudaEventCreate(&e));
+      c->prof_step_events.push_back(e);
+    }
+    HOC_CK(cudaEventRecord(c->prof_origin, s0));
+  }
   if (prof_streams) {
     if (!c->prof_fork) HOC_CK(cudaEventCreate(&c->prof_fork));
     while (c->prof_stream_end.size() < size_t(p.n_streams)) {
@@ -340,6 +350,12 @@ hocResult_t issue(hocComm* c, const Plan& p, const Bind& bd, cudaStream_t s0, co
     cudaStream_t s = st[step.stream];
     for (int w : step.waits)
       if (p.steps[w].stream != step.stream) HOC_CK(cudaStreamWaitEvent(s, c->ev[w], 0));
+    if (c->profiling) {
+      hocComm::StepTiming t{step.kind, step.stream, step.stage, c->prof_step_events[2 * i],
+                            c->prof_step_events[2 * i + 1]};
+      HOC_CK(cudaEventRecord(t.start, s));
+      c->prof_steps.push_back(t);
+    }
     switch (step.kind) {
       case kStepReduce:
       case kStepFused: HOC_TRY(run_reduce(c, p, step, bd, s, max_ctas)); break;
@@ -358,6 +374,7 @@ hocResult_t issue(hocComm* c, const Plan& p, const Bind& bd, cudaStream_t s0, co
         break;
       default: return HOC_ERR_INVALID_ARG;
     }
+    if (c->profiling) HOC_CK(cudaEventRecord(c->prof_steps.back().end, s));
     if (step.record) HOC_CK(cudaEventRecord(c->ev[i], s));
   }
   if (prof_streams) {
@@ -524,6 +541,8 @@ hocResult_t read_cfg(const hocConfig_t* in, int k, Cfg* out) {
     else if (!strcmp(v, "proxy_stall")) c.fault = kFaultProxyStall;
     else if (!strcmp(v, "tma_stall")) c.fault = kFaultTmaStall;
     else if (!strcmp(v, "proxy_block")) c.fault = kFaultProxyBlock;
+    else if (!strcmp(v, "proxy_memop")) c.fault = kFaultProxyMemop;
+    else if (!strcmp(v, "proxy_memop_reset")) c.fault = kFaultProxyMemopReset;
   }
   if (c.order.empty())
     for (int i = 0; i < k; ++i) c.order.push_back(i);
@@ -1119,6 +1138,26 @@ hocResult_t hoc_profile_stream_finish(hocComm_t comm, float* finish_ms, int max_
   for (int i = 0; i < comm->prof_streams && i < max_streams; ++i) {
     HOC_CK(cudaEventSynchronize(comm->prof_stream_end[i]));
     HOC_CK(cudaEventElapsedTime(&finish_ms[i], comm->prof_fork, comm->prof_stream_end[i]));
+  }
+  return HOC_SUCCESS;
+}
+
+hocResult_t hoc_profile_timeline(hocComm_t comm, hocStepTime_t* items, size_t cap, size_t* n_items) {
+  if (!comm) return HOC_ERR_NOT_INITIALIZED;
+  if (!n_items || (cap > 0 && !items)) return HOC_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(comm->mu);
+  DeviceGuard g(comm->device);
+  *n_items = comm->prof_steps.size();
+  for (size_t i = 0; i < comm->prof_steps.size() && i < cap; ++i) {
+    const hocComm::StepTiming& t = comm->prof_steps[i];
+    hocStepTime_t& o = items[i];
+    o.kind = t.kind == kStepReduce ? HOC_ITEM_REDUCE : t.kind == kStepFused ? HOC_ITEM_FUSED
+           : t.kind == kStepTma ? HOC_ITEM_TMA : HOC_ITEM_COPY;
+    o.stream = t.stream;
+    o.stage = t.stage;
+    HOC_CK(cudaEventSynchronize(t.end));
+    HOC_CK(cudaEventElapsedTime(&o.start_ms, comm->prof_origin, t.start));
+    HOC_CK(cudaEventElapsedTime(&o.end_ms, comm->prof_origin, t.end));
   }
   return HOC_SUCCESS;
 }

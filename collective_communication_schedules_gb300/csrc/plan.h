@@ -56,7 +56,9 @@ enum Fault {
   kFaultWrongOrder = 3,
   kFaultProxyStall = 4,
   kFaultTmaStall = 5,   // the TMA kernel's mbarriers expect bytes that never arrive
-  kFaultProxyBlock = 6  // the proxy thread is held up past a task's deadline (host sleep)
+  kFaultProxyBlock = 6,  // the proxy thread is held up past a task's deadline (host sleep)
+  kFaultProxyMemop = 7,  // the first device-count call: its wait for FINISH fails to queue
+  kFaultProxyMemopReset = 8  // the first device-count call: its reset of end_flag fails to queue
 };
 
 enum StepKind { kStepReduce = 0, kStepFused = 1, kStepCopy = 2, kStepTma = 3 };

@@ -23,6 +23,13 @@
 // Running (moves issued) -> Releasing (FINISH written) -> Free (the stream
 // reset end_flag).  Every transition happens under Proxy::mu; the release
 // writes happen under it too, so exactly one thread releases a task.
+// If queueing the four stream operations fails part way, the call returns
+// HOC_ERR_CUDA and the slot is abandoned: once the stream writes the start
+// flag the proxy acknowledges it and, without moving anything, frees the
+// slot -- or retires it for good when the stream waits for FINISH but the
+// reset of end_flag was never queued (nothing would ever reset it), or when
+// not even the start flag was queued (the counts copy may still land in it).
+// Retired slots are skipped when a call picks its slot.
 #include <atomic>
 #include <chrono>
 #include <condition_variable>
@@ -60,7 +67,8 @@ constexpr auto kShutdownWait = std::chrono::seconds(60);
 constexpr size_t kProxyTaskCopies = 96;
 constexpr size_t kChunkGrain = size_t(1) << 20;
 
-enum SlotState { kFree = 0, kQueued = 1, kStarting = 2, kRunning = 3, kReleasing = 4 };
+enum SlotState { kFree = 0, kQueued = 1, kStarting = 2, kRunning = 3, kReleasing = 4, kRetired = 5 };
+constexpr int kStreamOps = 4;  // write start, wait ack, wait finish, reset end
 
 const char* const kWhyDeadline =
     "the moves did not finish within 10 s of the stream reaching the start flag; launching a kernel for the first "
@@ -77,7 +85,9 @@ struct Slot {
   int state = kFree;
   Bind bind;
   int dtype = 0;
-  std::vector<size_t> cap;
+  std::vector<size_t> cap;   // receive capacities, elements
+  std::vector<size_t> scap;  // send capacities, elements
+  int abandoned_ops = 0;     // > 0: queueing failed after this many stream operations
   int transpose = 0;
   cudaEvent_t done = nullptr;
   bool stalled = false;  // host-injected: the moves are never reported complete
@@ -90,6 +100,7 @@ struct Proxy {
   int k = 0;
   int device = 0;
   int fault = 0;  // the communicator's injected fault, copied: the proxy may outlive it
+  bool memop_fault_used = false;  // the stream-operation fault is injected into the first call only
   std::mutex mu;
   std::condition_variable cv;
   std::thread th;        // the proxy thread
@@ -199,6 +210,17 @@ void start_task(Proxy* P, Slot& s) {
       col += c;
     }
   }
+  for (int a = 0; a < k; ++a) {  // the same for what each source reads from its send buffer
+    size_t row = 0;
+    for (int d = 0; d < k; ++d) {
+      const size_t c = cnt[size_t(a) * k + d];
+      if (c > s.scap[a] - row) {
+        release(P, s, HOC_ERR_INVALID_ARG, "a sender's total count exceeds its send buffer; nothing was moved");
+        return;
+      }
+      row += c;
+    }
+  }
   if (P->fault == kFaultProxyStall) {  // injected on the host: a completion that never arrives
     std::lock_guard<std::mutex> lock(P->mu);
     if (s.state == kStarting) {
@@ -238,6 +260,22 @@ void start_task(Proxy* P, Slot& s) {
   }
 }
 
+// The stream of an abandoned slot reached its start flag: let it pass without
+// moving anything.  The caller holds P->mu.
+void abandon_locked(Proxy* P, Slot& s) {
+  std::atomic_thread_fence(std::memory_order_seq_cst);
+  *s.start = 0;                   // the ack, if the stream waits for it
+  if (s.abandoned_ops >= 3) {     // the stream waits for FINISH, but nothing will reset end_flag
+    *s.end = kFinishValue;
+    s.state = kRetired;
+  } else {                        // nothing waits on end_flag
+    s.state = kFree;
+  }
+  std::atomic_thread_fence(std::memory_order_seq_cst);
+  s.abandoned_ops = 0;
+  P->cv.notify_all();
+}
+
 void free_resources(Proxy* P) {
   for (Slot& s : P->slots)
     if (s.done) cudaEventDestroy(s.done);
@@ -273,11 +311,17 @@ void proxy_loop(Proxy* P) {
         std::lock_guard<std::mutex> lock(P->mu);
         st = s.state;
       }
-      if (st == kFree) continue;
+      if (st == kFree || st == kRetired) continue;
       all_free = false;
       if (st == kQueued) {
         if (*s.start == kStartValue) {
-          start_task(P, s);
+          bool abandoned;
+          {
+            std::lock_guard<std::mutex> lock(P->mu);
+            abandoned = s.abandoned_ops > 0;
+            if (abandoned) abandon_locked(P, s);
+          }
+          if (!abandoned) start_task(P, s);
           busy = true;
         }
       } else if (st == kRunning) {
@@ -421,7 +465,7 @@ void proxy_shutdown(hocComm* c) {
   P->closing = true;
   auto all_free = [P] {
     for (const Slot& s : P->slots)
-      if (s.state != kFree) return false;
+      if (s.state != kFree && s.state != kRetired) return false;
     return true;
   };
   if (P->cv.wait_for(lock, kShutdownWait, all_free)) {
@@ -457,9 +501,11 @@ using namespace hoc;
 
 extern "C" hocResult_t hoc_alltoall_device_counts(hocComm_t comm, const void* const* send, void* const* recv,
                                                   const uint64_t* d_sendcounts, int transpose,
-                                                  const size_t* recv_capacity, hocDataType_t dtype, void* stream) {
+                                                  const size_t* send_capacity, const size_t* recv_capacity,
+                                                  hocDataType_t dtype, void* stream) {
   if (!comm) return HOC_ERR_NOT_INITIALIZED;
-  if (!send || !recv || !d_sendcounts || !recv_capacity || dtype_bytes(dtype) == 0) return HOC_ERR_INVALID_ARG;
+  if (!send || !recv || !d_sendcounts || !send_capacity || !recv_capacity || dtype_bytes(dtype) == 0)
+    return HOC_ERR_INVALID_ARG;
   const int k = comm->k;
   for (int r = 0; r < k; ++r)
     if (!send[r] || !recv[r]) return HOC_ERR_INVALID_ARG;
@@ -490,15 +536,34 @@ extern "C" hocResult_t hoc_alltoall_device_counts(hocComm_t comm, const void* co
   }
   Proxy* P = comm->proxy;
   Slot* slot = nullptr;
+  int inject_fail_at = 0;  // host-injected: the stream operation of this number (1-based) fails to queue
   {
     std::unique_lock<std::mutex> lock(P->mu);
-    Slot& cand = P->slots[P->next % kSlots];
-    if (!P->cv.wait_for(lock, std::chrono::seconds(30), [&] { return cand.state == kFree; })) {
-      set_error_detail("no free proxy slot within 30 s");
-      return HOC_ERR_TIMEOUT;
+    const auto give_up = Clock::now() + std::chrono::seconds(30);
+    while (!slot) {  // the next slot in turn that is not retired, once it is free
+      Slot* cand = nullptr;
+      for (int i = 0; i < kSlots && !cand; ++i) {
+        Slot& c2 = P->slots[(P->next + i) % kSlots];
+        if (c2.state != kRetired) {
+          cand = &c2;
+          P->next += i;
+        }
+      }
+      if (!cand) {
+        set_error_detail("every proxy slot was retired after stream operations failed to queue");
+        return HOC_ERR_CUDA;
+      }
+      if (!P->cv.wait_until(lock, give_up, [&] { return cand->state == kFree || cand->state == kRetired; })) {
+        set_error_detail("no free proxy slot within 30 s");
+        return HOC_ERR_TIMEOUT;
+      }
+      if (cand->state == kFree) slot = cand;
     }
     ++P->next;
-    slot = &cand;
+    if ((P->fault == kFaultProxyMemop || P->fault == kFaultProxyMemopReset) && !P->memop_fault_used) {
+      P->memop_fault_used = true;
+      inject_fail_at = P->fault == kFaultProxyMemop ? 3 : 4;
+    }
     for (int r = 0; r < k; ++r) {
       slot->bind.send[r] = send[r];
       slot->bind.recv[r] = recv[r];
@@ -506,6 +571,8 @@ extern "C" hocResult_t hoc_alltoall_device_counts(hocComm_t comm, const void* co
     slot->dtype = dtype;
     slot->transpose = transpose != 0;
     slot->cap.assign(recv_capacity, recv_capacity + k);
+    slot->scap.assign(send_capacity, send_capacity + k);
+    slot->abandoned_ops = 0;
     slot->state = kQueued;
     P->cv.notify_all();  // wake an idle proxy thread
   }
@@ -517,12 +584,30 @@ extern "C" hocResult_t hoc_alltoall_device_counts(hocComm_t comm, const void* co
     return HOC_ERR_CUDA;
   }
   CUstream cu = reinterpret_cast<CUstream>(s);
-  bool ok = P->write32(cu, slot->d_start, kStartValue, CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS;
-  ok = ok && P->wait32(cu, slot->d_start, 0, CU_STREAM_WAIT_VALUE_EQ) == CUDA_SUCCESS;
-  ok = ok && P->wait32(cu, slot->d_end, kFinishValue, CU_STREAM_WAIT_VALUE_EQ) == CUDA_SUCCESS;
-  ok = ok && P->write32(cu, slot->d_end, 0, CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS;
-  if (!ok) {
-    set_error_detail("queueing the stream memory operations failed");
+  int queued = 0;  // stream operations queued so far, in order
+  for (int op = 1; op <= kStreamOps; ++op) {
+    if (op == inject_fail_at) break;
+    CUresult e;
+    switch (op) {
+      case 1: e = P->write32(cu, slot->d_start, kStartValue, CU_STREAM_WRITE_VALUE_DEFAULT); break;
+      case 2: e = P->wait32(cu, slot->d_start, 0, CU_STREAM_WAIT_VALUE_EQ); break;
+      case 3: e = P->wait32(cu, slot->d_end, kFinishValue, CU_STREAM_WAIT_VALUE_EQ); break;
+      default: e = P->write32(cu, slot->d_end, 0, CU_STREAM_WRITE_VALUE_DEFAULT); break;
+    }
+    if (e != CUDA_SUCCESS) break;
+    ++queued;
+  }
+  if (queued < kStreamOps) {
+    std::lock_guard<std::mutex> lock(P->mu);
+    if (queued == 0) {
+      // The stream will never write the start flag, but the counts copy queued
+      // on it may still land in the slot: retire it rather than hand it out.
+      slot->state = kRetired;
+    } else {
+      slot->abandoned_ops = queued;  // the proxy lets the stream pass its flags and moves nothing
+    }
+    P->cv.notify_all();
+    set_error_detail("queueing the stream memory operations failed; nothing will be moved");
     return HOC_ERR_CUDA;
   }
   return HOC_SUCCESS;

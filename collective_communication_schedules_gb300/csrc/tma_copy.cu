@@ -17,6 +17,8 @@
 // fault injection (p.tx_pad > 0) makes every mbarrier expect more bytes than
 // its load delivers, so the phase never completes and this path runs without
 // any fault on the GPU.
+#include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -225,6 +227,7 @@ constexpr int kNoAllocStatusWords = HOC_NOALLOC_SCRATCH_BYTES / int(sizeof(int))
 static __device__ __align__(256) int g_noalloc_status[kNoAllocStatusWords];
 
 constexpr int kMaxDevices = 64;
+constexpr uint64_t kMaxMoveBytes = uint64_t(1) << 40;  // the span limit of every other call
 std::mutex g_noalloc_mu;
 int* g_noalloc_ptr[kMaxDevices] = {};  // device address of g_noalloc_status, per device
 
@@ -272,13 +275,27 @@ extern "C" hocResult_t hoc_tma_moves_noalloc(const void* const* src, void* const
   CopyParams cp;
   memset(&cp, 0, sizeof cp);
   cp.piece_bytes = kPieceBytes;
-  cp.wait_ns = 2000000000ull;
+  // Host-side fault injection (HOC_FAULT=tma_stall), as for the communicator's
+  // moves: every mbarrier expects 16 bytes more than its load brings, so the
+  // bounded waits give up after 0.1 s and the status word reports it.
+  const char* fault = getenv("HOC_FAULT");
+  const bool stall = fault && !strcmp(fault, "tma_stall");
+  cp.tx_pad = stall ? 16u : 0u;
+  cp.wait_ns = stall ? 100000000ull : 2000000000ull;
   cp.status = status;
   int nj = 0;
   for (int i = 0; i < n; ++i) {
     if (bytes[i] == 0) continue;
-    if (!src[i] || !dst[i]) return HOC_ERR_INVALID_ARG;
+    if (!src[i] || !dst[i]) {
+      set_error_detail("hoc_tma_moves_noalloc: NULL source or destination of a non-empty move");
+      return HOC_ERR_INVALID_ARG;
+    }
     const uintptr_t a = reinterpret_cast<uintptr_t>(src[i]), d = reinterpret_cast<uintptr_t>(dst[i]);
+    const uintptr_t hi = a > d ? a : d;
+    if (uint64_t(bytes[i]) > kMaxMoveBytes || bytes[i] > UINTPTR_MAX - hi) {  // no end address below wraps
+      set_error_detail("hoc_tma_moves_noalloc: a move of more than 2^40 bytes, or one that runs past the address space");
+      return HOC_ERR_INVALID_ARG;
+    }
     if (a < d + bytes[i] && d < a + bytes[i]) {  // a move may not overlap itself
       set_error_detail("hoc_tma_moves_noalloc: a move's source and destination overlap");
       return HOC_ERR_INVALID_ARG;

@@ -55,6 +55,11 @@ class _PlanItem(C.Structure):
                 ("n_waits", C.c_int), ("wait0", C.c_int)]
 
 
+class _StepTime(C.Structure):
+    _fields_ = [("kind", C.c_int), ("stream", C.c_int), ("stage", C.c_int), ("start_ms", C.c_float),
+                ("end_ms", C.c_float)]
+
+
 _lib = None
 
 # Exported symbol -> (restype, argtypes)
@@ -90,7 +95,8 @@ _SIGS = {
 }
 NOALLOC_MAX_MOVES = 192
 _SIGS["hoc_alltoall_device_counts"] = (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p),
-                                                 C.c_void_p, C.c_int, C.POINTER(C.c_size_t), C.c_int, C.c_void_p])
+                                                 C.c_void_p, C.c_int, C.POINTER(C.c_size_t), C.POINTER(C.c_size_t),
+                                                 C.c_int, C.c_void_p])
 _SIGS["hoc_ep_pack"] = (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p,
                                   C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p])
 _SIGS["hoc_ep_pack_workspace"] = (C.c_int, [C.c_int, C.c_int, C.c_int, C.POINTER(C.c_size_t)])
@@ -101,6 +107,7 @@ _SIGS["hoc_allreduce_host"] = (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.PO
 _SIGS["hoc_proxy_status"] = (C.c_int, [C.c_void_p, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64),
                                        C.POINTER(C.c_int)])
 _SIGS["hoc_profile_stream_finish"] = (C.c_int, [C.c_void_p, C.POINTER(C.c_float), C.c_int, C.POINTER(C.c_int)])
+_SIGS["hoc_profile_timeline"] = (C.c_int, [C.c_void_p, C.POINTER(_StepTime), C.c_size_t, C.POINTER(C.c_size_t)])
 _SIGS["hoc_topo_schedule"] = (C.c_int, [C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_int), C.POINTER(C.c_uint64),
                                         C.c_uint64, C.c_uint64, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64),
                                         C.POINTER(C.c_double), C.c_int, C.POINTER(C.c_int),
@@ -335,20 +342,32 @@ class Comm:
         return done
 
     def alltoall_device_counts(self, send, recv, d_counts, recv_capacity, dtype=None, stream=None,
-                               transpose: bool = False):
+                               transpose: bool = False, send_capacity=None):
         """All-to-all(v) whose k x k counts (uint64/int64, elements, row = source) live on the device.
 
         The counts reach a host proxy through the stream-memory-operation
-        handshake; the call returns without waiting (see include/hoc_proxy.h)."""
+        handshake; the call returns without waiting (see include/hoc_proxy.h).
+        send_capacity defaults to the elements each send tensor holds."""
         dtype = _dtype_code(send[0]) if dtype is None else dtype
         caps = [int(v) for v in recv_capacity]
         if len(caps) != self.k:
             raise ValueError(f"recv_capacity: expected {self.k} values, got {len(caps)}")
+        if send_capacity is None:
+            scaps = [t.numel() * t.element_size() // DTYPE_BYTES[dtype] if not isinstance(t, int) else None
+                     for t in send]
+            if any(v is None for v in scaps):
+                raise ValueError("send_capacity is needed when send buffers are raw addresses")
+        else:
+            scaps = [int(v) for v in send_capacity]
+        if len(scaps) != self.k:
+            raise ValueError(f"send_capacity: expected {self.k} values, got {len(scaps)}")
         cap = (C.c_size_t * self.k)(*caps)
-        _check(lib().hoc_alltoall_device_counts(self._h, self._ranks(send, 0, "send"),
+        scap = (C.c_size_t * self.k)(*scaps)
+        _check(lib().hoc_alltoall_device_counts(self._h,
+                                                self._ranks(send, [v * DTYPE_BYTES[dtype] for v in scaps], "send"),
                                                 self._ranks(recv, [v * DTYPE_BYTES[dtype] for v in caps], "recv"),
                                                 _ptr(d_counts, 8 * self.k * self.k, "d_counts"),
-                                                int(bool(transpose)), cap, dtype, _stream(stream)),
+                                                int(bool(transpose)), scap, cap, dtype, _stream(stream)),
                "hoc_alltoall_device_counts")
 
     def proxy_status(self) -> dict:
@@ -382,6 +401,16 @@ class Comm:
         n = C.c_int()
         _check(lib().hoc_profile_stream_finish(self._h, buf, 16, C.byref(n)), "hoc_profile_stream_finish")
         return [buf[i] for i in range(min(n.value, 16))]
+
+    def profile_timeline(self) -> list:
+        """Per-step (kind, stream, stage, start_ms, end_ms) of the last call issued while profiling."""
+        n = C.c_size_t()
+        _check(lib().hoc_profile_timeline(self._h, None, 0, C.byref(n)), "hoc_profile_timeline")
+        buf = (_StepTime * max(1, n.value))()
+        _check(lib().hoc_profile_timeline(self._h, buf, n.value, C.byref(n)), "hoc_profile_timeline")
+        kinds = {ITEM_REDUCE: "reduce", ITEM_FUSED: "fused", ITEM_COPY: "copy", ITEM_TMA: "tma"}
+        return [dict(kind=kinds.get(b.kind, b.kind), stream=b.stream, stage=b.stage, start_ms=b.start_ms,
+                     end_ms=b.end_ms) for b in buf[: n.value]]
 
 
 # ---------------------------------------------------------------- workload

@@ -220,6 +220,24 @@ hocResult_t hoc_profile_read(hocComm_t comm, hocKernel_t kernel, int* launches, 
  * over the copy engines (HOCCL section 3.3 on skewed all-to-all flows). */
 hocResult_t hoc_profile_stream_finish(hocComm_t comm, float* finish_ms, int max_streams, int* n_streams);
 
+/* Per-step timeline of the last call issued while profiling was enabled: one
+ * item per plan step (a reduce or fused kernel, a bulk-copy kernel, or the
+ * copy-engine copies of one copy queue for one chunk), in issue order, with
+ * start and end in milliseconds from the moment the caller's stream reached
+ * the call.  A step's start is recorded on its stream after the waits it
+ * depends on, so start..end is when the step could run and when it finished.
+ * Waits for those events.  Writes at most `cap` items; *n_items = all of them.
+ * Used to see how the chunks of a pipelined allreduce overlap (HOCCL section
+ * 3.3.1 on chunk pipelining). */
+typedef struct {
+  int kind;     /* hocItemKind_t: HOC_ITEM_REDUCE, HOC_ITEM_FUSED, HOC_ITEM_COPY or HOC_ITEM_TMA */
+  int stream;   /* 0 = caller stream, 1..n = internal copy streams */
+  int stage;    /* chunk index (allreduce, allgather) or shift stage (alltoall) */
+  float start_ms;
+  float end_ms;
+} hocStepTime_t;
+hocResult_t hoc_profile_timeline(hocComm_t comm, hocStepTime_t* items, size_t cap, size_t* n_items);
+
 /* Static description of a result code. */
 const char* hoc_error_string(hocResult_t result);
 
@@ -242,7 +260,9 @@ const char* hoc_last_error_detail(void);
  * holds until the process exits.
  *   - At most HOC_NOALLOC_MAX_MOVES moves per call (what one launch's
  *     parameters carry); more returns HOC_ERR_INVALID_ARG.  A move whose
- *     source and destination overlap is rejected the same way.
+ *     source and destination overlap, a non-empty move with a NULL pointer and
+ *     a move of more than 2^40 bytes are rejected the same way, before
+ *     anything is queued.
  *   - The first call on a device sets that device up (kernel attributes and
  *     the scratch array's device address); make that first call before any
  *     stream capture.

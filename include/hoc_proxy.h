@@ -51,16 +51,21 @@ extern "C" {
  * k*k uint64 element counts (row = source), valid when the work before this
  * call on `stream` has finished; with transpose != 0 the matrix is read
  * transposed (row = destination), so the counts of a dispatch serve the
- * inverse exchange (the combine) unchanged.  recv_capacity: host array of k element
- * capacities of the receive buffers (the counts are unknown at call time);
- * if a receiver's total exceeds its capacity nothing is moved and the error is
- * reported.  Displacements are prefix sums in rank order.  Returns as soon as
- * the handshake is queued on `stream`; later work on `stream` sees the moved
- * data.  The first call starts the proxy thread and allocates its pinned host
- * flags.  Not allowed while `stream` is being captured into a graph. */
+ * inverse exchange (the combine) unchanged.  send_capacity / recv_capacity:
+ * host arrays of k element capacities of the send and receive buffers (the
+ * counts are unknown at call time); if a sender's row total exceeds its send
+ * capacity, or a receiver's column total its receive capacity, nothing is
+ * moved and the error (HOC_ERR_INVALID_ARG) is reported by hoc_wait.  The
+ * totals are compared without overflow.  Displacements are prefix sums in
+ * rank order.  Returns as soon as the handshake is queued on `stream`; later
+ * work on `stream` sees the moved data.  The first call starts the proxy
+ * thread and allocates its pinned host flags.  Not allowed while `stream` is
+ * being captured into a graph.  If the stream operations cannot all be
+ * queued, the call returns HOC_ERR_CUDA and moves nothing; the proxy lets the
+ * stream pass whatever flags it did queue. */
 hocResult_t hoc_alltoall_device_counts(hocComm_t comm, const void* const* send, void* const* recv,
-                                       const uint64_t* d_sendcounts, int transpose, const size_t* recv_capacity,
-                                       hocDataType_t dtype, void* stream);
+                                       const uint64_t* d_sendcounts, int transpose, const size_t* send_capacity,
+                                       const size_t* recv_capacity, hocDataType_t dtype, void* stream);
 
 /* Proxy bookkeeping: tasks completed, tasks released by the watchdog or an
  * error, and the first error code seen (then cleared). */

@@ -221,6 +221,60 @@ def test_sendrecv_parity(path):
             assert np.array_equal(dst.host(), x)
 
 
+@pytest.mark.parametrize("cap", [1, 3, 8])
+def test_sm_capped_tma_moves_parity(cap):
+    """The TMA copy kernel capped at `cap` CTAs (the 1/2/4/8-SM curves of the sweeps): all-gather,
+    all-to-all(v) and send/recv, ragged sizes, misaligned buffers, against the oracle bit for bit."""
+    rng = np.random.default_rng(100 + cap)
+    for k in (3, 8):
+        with _comm(k, "tma", chunk_bytes=1 << 16, copy_max_sms=cap) as c:
+            # all-gather: sources and destinations in several 16-byte alignment classes
+            for sc in (13, 50_003, 400_001):
+                xs = inputs.rank_inputs("bfloat16", k, sc, workload=8, slot=60 + cap)
+                want = o_ring.allgather(xs)
+                send = [Guarded(sc, "bfloat16", offset_elems=(5 * r + cap) % 8) for r in range(k)]
+                recv = [Guarded(k * sc, "bfloat16", offset_elems=(3 * r) % 8) for r in range(k)]
+                for g, x in zip(send, xs):
+                    g.load(x)
+                c.allgather([g.ptr() for g in send], [g.ptr() for g in recv], sc, hoc.BFLOAT16)
+                c.wait()
+                st = c.last_stats()
+                assert st["kernels"] >= 1 and 1 <= st["max_ctas"] <= cap and st["sms_used"] <= cap
+                for r in range(k):
+                    recv[r].check()
+                    assert_bits_equal(recv[r].host(), want[r], "bfloat16", f"capped ag {cap} k={k} sc={sc} rank {r}")
+            # all-to-all(v): ragged counts, an empty row and an empty column, misaligned buffers
+            counts = rng.integers(0, 40_000, size=(k, k))
+            counts[1, :] = 0
+            counts[:, 2] = 0
+            sends = [rng.integers(0, 1 << 16, size=int(counts[s].sum())).astype(np.uint16) for s in range(k)]
+            want = o_a2a.alltoallv(sends, counts)
+            lens = o_a2a.recv_lengths(counts)
+            sb = [Guarded(max(1, len(x)), "bfloat16", offset_elems=(s + 1) % 8) for s, x in enumerate(sends)]
+            rb = [Guarded(max(1, n), "bfloat16", offset_elems=(7 * d) % 8) for d, n in enumerate(lens)]
+            for g, x in zip(sb, sends):
+                if len(x):
+                    g.tensor[: len(x)].copy_(to_device(x, "bfloat16"))
+            c.alltoall([g.ptr() for g in sb], [g.ptr() for g in rb], sendcounts=counts, dtype=hoc.BFLOAT16)
+            c.wait()
+            assert 1 <= c.last_stats()["max_ctas"] <= cap
+            for d in range(k):
+                rb[d].check()
+                assert_bits_equal(rb[d].host()[: lens[d]], want[d], "bfloat16", f"capped a2a {cap} k={k} dst {d}")
+            # send/recv: odd byte counts, source and destination misaligned differently
+            for n in (1, 4097, 3_000_017):
+                x = rng.integers(0, 256, size=n).astype(np.uint8)
+                src = Guarded(n, "uint8", offset_elems=3)
+                dst = Guarded(n, "uint8", offset_elems=11)
+                src.load(x)
+                c.sendrecv(0, src.ptr(), k - 1, dst.ptr(), n, hoc.UINT8)
+                c.wait()
+                assert 1 <= c.last_stats()["max_ctas"] <= cap
+                dst.check()
+                src.check()
+                assert np.array_equal(dst.host(), x), (cap, k, n)
+
+
 def test_graph_replay_and_profiling_agree():
     k, n = 8, 1 << 20
     xs = inputs.rank_inputs("bfloat16", k, n, workload=2, slot=60, sigma=1e-3)

@@ -39,3 +39,39 @@ def test_stream_finish_times_of_a_multi_stream_alltoall():
         c.sendrecv(0, a, 1, b, stream=s)
         assert c.profile_stream_finish() == []
         c.profile_enable(False)
+
+
+def test_timeline_of_a_pipelined_allreduce():
+    # Copy-engine allreduce in 4 chunks per block: one reduce step per chunk on
+    # the caller's stream, then that chunk's copies on the copy queues, each
+    # starting only once its chunk's reduce has ended; results stay exact.
+    from oracle import ring as o_ring
+    from collective_communication_schedules_gb300 import inputs
+    k, n, chunks = 4, 1 << 18, 4
+    xs = inputs.rank_inputs("float32", k, n, workload=7, slot=62)
+    want = o_ring.allreduce(xs, "float32")
+    s = torch.cuda.Stream()
+    with hoc.Comm(k, 0, hoc.Config(path="ce", n_copy_streams=2, chunk_bytes=(n // k) * 4 // chunks)) as c:
+        send = [to_device(x, "float32") for x in xs]
+        recv = [torch.empty_like(t) for t in send]
+        torch.cuda.synchronize()
+        c.profile_enable(True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        c.allreduce(send, recv, stream=s)
+        e1.record(s)
+        tl = c.profile_timeline()
+        torch.cuda.synchronize()
+        total = e0.elapsed_time(e1)
+        c.profile_enable(False)
+        reduces = [t for t in tl if t["kind"] == "reduce"]
+        copies = [t for t in tl if t["kind"] == "copy"]
+        assert [t["stage"] for t in reduces] == list(range(chunks))
+        assert all(t["stream"] == 0 for t in reduces)
+        assert {t["stage"] for t in copies} == set(range(chunks)) and all(t["stream"] >= 1 for t in copies)
+        for t in tl:
+            assert -0.01 <= t["start_ms"] <= t["end_ms"] <= total + 0.05, t
+        for t in copies:                                  # a chunk's moves wait for its reduce
+            assert t["start_ms"] >= reduces[t["stage"]]["end_ms"] - 1e-3, (t, reduces[t["stage"]])
+        for r in range(k):
+            assert np.array_equal(to_host(recv[r], "float32").view(np.uint32), want[r].view(np.uint32))

@@ -158,3 +158,59 @@ def test_watchdog_releases_while_the_proxy_thread_is_blocked(monkeypatch):
         torch.cuda.synchronize()                         # the stream was released
         assert c.proxy_status()["released_on_error"] == 1
         assert int(rv[0].sum()) == 0 and int(rv[1].sum()) == 0   # nothing was moved
+
+
+def test_send_overflow_releases_the_stream():
+    # rank 0's row asks for 20 elements from a send buffer of 15: released before any move
+    k = 2
+    with hoc.Comm(k, 0) as c:
+        d_counts = torch.tensor([[10, 10], [5, 5]], dtype=torch.int64, device="cuda")
+        sd = [torch.ones(15, dtype=torch.int32, device="cuda") for _ in range(k)]
+        rv = [torch.zeros(20, dtype=torch.int32, device="cuda") for _ in range(k)]
+        c.alltoall_device_counts(sd, rv, d_counts, [20, 20], hoc.INT32)     # send capacity: 15 per rank
+        with pytest.raises(hoc.HocError) as e:
+            c.wait(timeout_ms=30000)
+        assert e.value.code == hoc.ERR_INVALID_ARG and "send buffer" in str(e.value)
+        torch.cuda.synchronize()
+        assert int(rv[0].sum()) == 0 and int(rv[1].sum()) == 0
+        # an explicit send capacity below the tensors' size is what counts
+        d_small = torch.tensor([[5, 5], [5, 5]], dtype=torch.int64, device="cuda")
+        c.alltoall_device_counts(sd, rv, d_small, [20, 20], hoc.INT32, send_capacity=[9, 15])
+        with pytest.raises(hoc.HocError) as e:
+            c.wait(timeout_ms=30000)
+        assert e.value.code == hoc.ERR_INVALID_ARG and "send buffer" in str(e.value)
+        torch.cuda.synchronize()
+        assert int(rv[0].sum()) == 0 and int(rv[1].sum()) == 0
+
+
+@pytest.mark.parametrize("fault", ["proxy_memop", "proxy_memop_reset"])
+def test_failed_stream_operations_release_their_slot(monkeypatch, fault):
+    # Injected on the host: the first call's wait for FINISH (or its reset of
+    # the end flag) fails to queue.  The call reports HOC_ERR_CUDA and moves
+    # nothing; the stream is not held; the slot is freed (or retired, when the
+    # end flag would never be reset) and every later call still works.
+    monkeypatch.setenv("HOC_FAULT", fault)
+    k, n = 2, 64
+    rng = np.random.default_rng(23)
+    with hoc.Comm(k, 0) as c:
+        d_counts = torch.tensor([[n, n], [n, n]], dtype=torch.int64, device="cuda")
+        sd = [torch.ones(2 * n, dtype=torch.int32, device="cuda") for _ in range(k)]
+        rv = [torch.zeros(2 * n, dtype=torch.int32, device="cuda") for _ in range(k)]
+        with pytest.raises(hoc.HocError) as e:
+            c.alltoall_device_counts(sd, rv, d_counts, [2 * n, 2 * n], hoc.INT32)
+        assert e.value.code == hoc.ERR_CUDA
+        torch.cuda.synchronize()                         # the stream passed its flags
+        assert int(rv[0].sum()) == 0 and int(rv[1].sum()) == 0
+        for it in range(20):                             # more calls than slots: no slot is stuck
+            counts = rng.integers(0, 100, size=(k, k))
+            sends = [rng.integers(0, 1 << 31, size=int(counts[s].sum())).astype(np.int32) for s in range(k)]
+            want = o_a2a.alltoallv(sends, counts)
+            dc = torch.from_numpy(counts.astype(np.int64)).cuda()
+            sdv = [to_device(x, "int32") if len(x) else torch.zeros(1, dtype=torch.int32, device="cuda") for x in sends]
+            rvv = [torch.zeros(max(1, int(counts[:, d].sum())), dtype=torch.int32, device="cuda") for d in range(k)]
+            c.alltoall_device_counts(sdv, rvv, dc, [t.numel() for t in rvv], hoc.INT32)
+            c.wait(timeout_ms=30000)
+            for d in range(k):
+                assert np.array_equal(to_host(rvv[d], "int32")[: len(want[d])], want[d]), (it, d)
+        st = c.proxy_status()
+        assert st["completed"] == 20 and st["released_on_error"] == 0

@@ -59,3 +59,51 @@ def test_noalloc_rejects_too_many_moves():
         hoc.tma_moves_noalloc([a] * n, [b] * n, [16] * n)
     assert e.value.code == hoc.ERR_INVALID_ARG
     assert "192" in str(e.value)
+
+
+def test_noalloc_allocates_no_device_memory():
+    # The entry point's promise: after the first call on the device (which sets
+    # it up), calls leave the device's free memory unchanged.
+    n = 1 << 22
+    a = torch.arange(n, dtype=torch.int32, device="cuda").view(torch.uint8)
+    b = torch.zeros_like(a)
+    src, dst, nb = [a.data_ptr()], [b.data_ptr()], [a.numel()]
+    for _ in range(2):
+        hoc.tma_moves_noalloc(src, dst, nb, wait=True)
+    torch.cuda.synchronize()
+    free_before, _ = torch.cuda.mem_get_info()
+    for _ in range(5):
+        hoc.tma_moves_noalloc(src, dst, nb, wait=True)
+    torch.cuda.synchronize()
+    free_after, _ = torch.cuda.mem_get_info()
+    assert free_after == free_before
+    assert torch.equal(a, b)
+
+
+def test_noalloc_bounded_wait_reports_timeout_then_recovers(monkeypatch):
+    # Injected on the host: every mbarrier of the bulk-copy kernel expects 16
+    # bytes more than its load brings, so its bounded waits give up (0.1 s) and
+    # the status word in the shared scratch array reports it.  The next call
+    # clears the array and moves the bytes.
+    n = 1 << 20
+    a = torch.full((n,), 7, dtype=torch.uint8, device="cuda")
+    b = torch.zeros_like(a)
+    monkeypatch.setenv("HOC_FAULT", "tma_stall")
+    with pytest.raises(hoc.HocError) as e:
+        hoc.tma_moves_noalloc([a], [b], [n], wait=True)
+    assert e.value.code == hoc.ERR_TIMEOUT
+    monkeypatch.delenv("HOC_FAULT")
+    b.zero_()
+    hoc.tma_moves_noalloc([a], [b], [n], wait=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_noalloc_rejects_null_and_huge_moves():
+    a = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(hoc.HocError) as e:
+        hoc.tma_moves_noalloc([0], [a.data_ptr()], [16])
+    assert e.value.code == hoc.ERR_INVALID_ARG and "NULL" in str(e.value)
+    with pytest.raises(hoc.HocError) as e:                 # nothing is queued: the size check comes first
+        hoc.tma_moves_noalloc([a.data_ptr()], [a.data_ptr() + (1 << 41)], [(1 << 40) + 1])
+    assert e.value.code == hoc.ERR_INVALID_ARG and "2^40" in str(e.value)
