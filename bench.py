@@ -58,9 +58,10 @@ def parse():
     ap.add_argument("--no-extras", action="store_true", help="skip the per-path, probe and e2e legs")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--mode", default="allreduce", choices=["allreduce", "allgather"],
+    ap.add_argument("--mode", default="allreduce", choices=["allreduce", "allgather", "ep_fused"],
                     help="allgather: time only the all-gather moves of the workload's 32 MiB blocks "
-                         "(a profiling case: the copy-engine path launches no kernel)")
+                         "(a profiling case: the copy-engine path launches no kernel); ep_fused: time only the "
+                         "EP dispatch + combine fused with the exchange (8 ranks x 4096 tokens x 2048, top-6 of 64)")
     ap.add_argument("--no-workloads", dest="workloads", action="store_false",
                     help="skip the DP bucket stream, 1F1B pipeline and EP dispatch/combine legs")
     ap.add_argument("--count", type=int, default=N_ELEMS,
@@ -452,7 +453,7 @@ def leg_ce_interference(send, recv, n_el, k, local, stream, sms):
         out["launch_count"].append({"probe_kernels": nk, "slowdown": slow(pr), "sm_mhz_alone_with": mhz(pr),
                                     "probe_alone_ms": {sh: pr[sh]["probe_alone_ms"] for sh in pr}})
     c.close()
-    for mib, nq in ((4, 4), (4, 8), (4, 16), (2, 8), (2, 16), (8, 8), (8, 16), (16, 16)):
+    for mib, nq in ((4, 4), (4, 2), (4, 3), (2, 4), (2, 8), (8, 2), (8, 1), (16, 1), (4, 8), (8, 8), (16, 16)):
         c, run, ms, info = moves(mib << 20, nq)
         pr = probes(run, ms, stream, sms)
         out["copy_shape"].append(dict(chunk_mib=mib, copy_streams=nq, slowdown=slow(pr), sm_mhz_alone_with=mhz(pr),
@@ -743,6 +744,65 @@ def leg_expert_dispatch(peak):
     except hoc.HocError as e:  # reported in the line; the other legs stand
         torch.cuda.synchronize()
         out["device_round_trip"] = {"error": str(e)}
+
+    # The same round trip fused with the exchange: the dispatch scatters every
+    # token row straight into the destination ranks' receive buffers and the
+    # combine reads the rows where the experts left them (SMs; no send buffer,
+    # no copies).  Identity experts, as above; the results must be the same bits.
+    fcap = [int(ecounts[:, d].sum()) for d in range(k)]
+    frecv = [torch.empty(fcap[d], dtype=torch.bfloat16, device="cuda") for d in range(k)]
+    fpos = [torch.empty(n, dtype=torch.int32, device="cuda") for _ in range(k)]
+    fcounts = torch.empty((k, k), dtype=torch.int64, device="cuda")
+    fws = torch.empty(k * hoc.ep_pack_workspace(tokens, topk, experts), dtype=torch.int32, device="cuda")
+    fstatus = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fys = [torch.empty((tokens, h), dtype=torch.bfloat16, device="cuda") for _ in range(k)]
+    ids_flat = [t.view(-1) for t in ids]
+
+    def fused_once():
+        hoc.ep_dispatch_fused(ids_flat, xs, experts, frecv, fcap, fpos, fcounts, fws, fstatus, stream=s)
+        hoc.ep_combine_fused(frecv, fcap, ids_flat, fpos, fcounts, gate, tokens, topk, h, experts, fys, fstatus,
+                             stream=s)
+
+    fused_once()
+    torch.cuda.synchronize()
+    host_us = []
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(10):
+        t0 = time.perf_counter()
+        fused_once()
+        host_us.append((time.perf_counter() - t0) * 1e6)
+    e1.record(s)
+    torch.cuda.synchronize()
+    f_ms = e0.elapsed_time(e1) / 10
+    ph = []
+    for _ in range(5):  # phases: dispatch (sort + scatter), combine
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record(s)
+        hoc.ep_dispatch_fused(ids_flat, xs, experts, frecv, fcap, fpos, fcounts, fws, fstatus, stream=s)
+        ev[1].record(s)
+        hoc.ep_combine_fused(frecv, fcap, ids_flat, fpos, fcounts, gate, tokens, topk, h, experts, fys, fstatus,
+                             stream=s)
+        ev[2].record(s)
+        torch.cuda.synchronize()
+        ph.append((ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])))
+    d_ms = statistics.median(p[0] for p in ph)
+    c_ms = statistics.median(p[1] for p in ph)
+    rows_moved = int(ecounts.sum()) // h                     # valid (token, slot) pairs of all ranks
+    row_b = h * 2
+    disp_bytes = k * tokens * row_b + rows_moved * row_b + k * n * 12      # rows read once, written per pair; ids, pos
+    comb_bytes = rows_moved * row_b + k * tokens * row_b + k * n * 12      # rows read per pair, outputs written; ids, pos, w
+    same = all(torch.equal(a.view(torch.int16), b.view(torch.int16)) for a, b in zip(fys, ys))
+    out["fused_round_trip"] = {
+        "ms": round(f_ms, 4), "host_issue_us": round(statistics.median(host_us), 1),
+        "phases": {"dispatch_ms": round(d_ms, 4), "combine_ms": round(c_ms, 4)},
+        "dispatch_bytes": disp_bytes, "combine_bytes": comb_bytes,
+        "dispatch_hbm_frac": round(disp_bytes / (d_ms * 1e-3) / (peak * 1e9), 4),
+        "combine_hbm_frac": round(comb_bytes / (c_ms * 1e-3) / (peak * 1e9), 4),
+        "status": int(fstatus.item()), "results_equal_copy_engine_round_trip": bool(same),
+        "steps": "fused dispatch (sort of every rank's pairs, rows scattered into the receive buffers) -> "
+                 "fused combine (rows read in place from the expert ranks' buffers)",
+        "kernels": 5, "copies": 0}
     return out
 
 
@@ -867,7 +927,8 @@ def leg_ce_allreduce_timeline(send, recv, k, local, stream, per_rank, peak):
     """When each chunk of the copy-engine allreduce is reduced and moved (the per-step timeline).
 
     One call with profiling on (events around every step; no graph), after a
-    few unprofiled ones.  Per chunk: the reduce kernel's start and end on the
+    few unprofiled ones, queued behind a 5 ms spin kernel so that the host has
+    issued all of it before the GPU starts.  Per chunk: the reduce kernel's start and end on the
     caller's stream, and the first start and last end of that chunk's copies
     over the copy queues.  Beside it, what the schedule's bytes cost at the
     measured copy rate: (3k - 1) S with no L2 reuse, 2kS if every all-gather
@@ -884,6 +945,7 @@ def leg_ce_allreduce_timeline(send, recv, k, local, stream, per_rank, peak):
                 c.allreduce(send, recv, stream=stream)
             ms = time_allreduce(c, send, recv, stream, 5)
             c.profile_enable(True)
+            gpu_spin(stream, 5.0)          # the host issues every step while the GPU spins: the timeline is the GPU's
             c.allreduce(send, recv, stream=stream)
             tl = c.profile_timeline()
             c.profile_enable(False)
@@ -909,39 +971,47 @@ def leg_ce_allreduce_timeline(send, recv, k, local, stream, per_rank, peak):
     return out
 
 
+_SPIN = {}
+
+
+def gpu_spin(stream, ms: float):
+    """Queue a one-CTA FMA kernel that keeps `stream` busy for about `ms` ms, so that
+    work the host queues behind it starts back to back, whatever the host's issue cost."""
+    import torch
+
+    from collective_communication_schedules_gb300 import hoc
+    if "iters_per_ms" not in _SPIN:
+        sink = torch.zeros(4, dtype=torch.float32, device="cuda")
+        hoc.probe_launch(1, 32, 1000, stream=stream, sink=sink)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        hoc.probe_launch(1, 32, 20000, stream=stream, sink=sink)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        _SPIN["iters_per_ms"] = 20000 / max(e0.elapsed_time(e1), 1e-3)
+        _SPIN["sink"] = sink
+    hoc.probe_launch(1, 32, int(ms * _SPIN["iters_per_ms"]), stream=stream, sink=_SPIN["sink"])
+
+
 def leg_startup_latency():
-    """Time of ONE small copy, alone: copy engine vs the TMA kernel on 1 CTA and on every SM.
+    """Time per copy of a chain of small copies on one stream, each waiting for the one before.
 
     HOCCL section 1 puts the DMA engines' startup latency at about 5x that of an
-    SM-driven copy.  Each trial queues a ~80 us spin kernel first, so the
-    events bracket only the copy (the host's issue of it is hidden behind the
-    spin); the figure is the median over 50 trials minus the median of the
-    same window with nothing in it.
+    SM-driven copy.  A chain of 100 copies of one size is queued behind a 3 ms
+    spin kernel (so the host's issue cost is hidden) and timed with events
+    around the chain: per copy = startup + transfer.  Copy engine vs the TMA
+    kernel on 1 CTA and on every SM.
     """
     import torch
 
     from collective_communication_schedules_gb300 import hoc
 
     sizes = [4 << 10, 16 << 10, 64 << 10, 256 << 10, 1 << 20]
+    chain = 100
     a = torch.randint(0, 256, (1 << 20,), dtype=torch.uint8, device="cuda")
     b = torch.zeros_like(a)
     stream = torch.cuda.Stream()
-    sink = torch.zeros(4, dtype=torch.float32, device="cuda")
-
-    def window(fn, trials=50):
-        ts = []
-        for _ in range(trials):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            hoc.probe_launch(1, 32, 40000, stream=stream, sink=sink)     # keeps the GPU busy while we queue
-            e0.record(stream)
-            fn()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1) * 1e3)
-        return statistics.median(ts)
-
-    empty = window(lambda: None)
-    out = {"sizes_bytes": sizes, "empty_window_us": round(empty, 2), "us": {}}
+    out = {"sizes_bytes": sizes, "chain": chain, "us_per_copy": {}}
     for name, path, ctas in (("ce", "ce", 0), ("tma_1cta", "tma", 1), ("tma_all_sms", "tma", 0)):
         with hoc.Comm(2, torch.cuda.current_device(), hoc.Config(path=path, copy_max_sms=ctas)) as c:
             row = []
@@ -949,9 +1019,22 @@ def leg_startup_latency():
                 fn = lambda n=n: c.sendrecv(0, a, 1, b, n, hoc.UINT8, stream=stream)
                 fn()
                 torch.cuda.synchronize()
-                row.append(round(max(0.0, window(fn) - empty), 2))
-            out["us"][name] = row
-    out["ce_over_tma_1cta"] = [round(x / y, 2) if y > 0 else None for x, y in zip(out["us"]["ce"], out["us"]["tma_1cta"])]
+                runs = []
+                for _ in range(3):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    gpu_spin(stream, 3.0)
+                    e0.record(stream)
+                    for _ in range(chain):
+                        fn()
+                    e1.record(stream)
+                    torch.cuda.synchronize()
+                    runs.append(e0.elapsed_time(e1) * 1e3 / chain)
+                row.append(round(statistics.median(runs), 3))
+            out["us_per_copy"][name] = row
+    ce, t1 = out["us_per_copy"]["ce"], out["us_per_copy"]["tma_1cta"]
+    out["ce_over_tma_1cta"] = [round(x / y, 2) if y > 0 else None for x, y in zip(ce, t1)]
+    out["ce_over_tma_all_sms"] = [round(x / y, 2) if y > 0 else None
+                                  for x, y in zip(ce, out["us_per_copy"]["tma_all_sms"])]
     out["verified"] = bool(torch.equal(a, b))
     return out
 
@@ -1278,6 +1361,52 @@ def run_allgather_only(args, world, rank, local):
                           "copies_per_step": st["copies"], "sms_used": st["sms_used"]}), flush=True)
 
 
+def run_ep_fused_only(args, world, rank, local):
+    """The EP round trip fused with the exchange alone (a profiling case): dispatch + combine."""
+    import numpy as np
+    import torch
+
+    from collective_communication_schedules_gb300 import hoc, inputs
+
+    torch.cuda.set_device(local)
+    w = inputs.EP_DISPATCH
+    k, tokens, h, experts, topk = w["k"], w["tokens"], w["hidden"], w["experts"], w["topk"]
+    routing = inputs.ep_routing(k, tokens, experts, topk, w["zipf"])
+    g = torch.Generator(device="cuda").manual_seed(5500)
+    xs = [torch.randn((tokens, h), generator=g, device="cuda").to(torch.bfloat16) for _ in range(k)]
+    ids = [torch.from_numpy(routing[r].astype(np.int32).reshape(-1)).cuda() for r in range(k)]
+    gate = [torch.rand(tokens * topk, generator=g, device="cuda") for _ in range(k)]
+    cnt = np.stack([np.bincount(routing[r].reshape(-1) // (experts // k), minlength=k) for r in range(k)])
+    cap = [int(cnt[:, d].sum()) * h for d in range(k)]
+    recv = [torch.empty(cap[d], dtype=torch.bfloat16, device="cuda") for d in range(k)]
+    pos = [torch.empty(tokens * topk, dtype=torch.int32, device="cuda") for _ in range(k)]
+    counts = torch.empty((k, k), dtype=torch.int64, device="cuda")
+    wsp = torch.empty(k * hoc.ep_pack_workspace(tokens, topk, experts), dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ys = [torch.empty((tokens, h), dtype=torch.bfloat16, device="cuda") for _ in range(k)]
+    stream = torch.cuda.Stream()
+
+    def step():
+        hoc.ep_dispatch_fused(ids, xs, experts, recv, cap, pos, counts, wsp, status, stream=stream)
+        hoc.ep_combine_fused(recv, cap, ids, pos, counts, gate, tokens, topk, h, experts, ys, status, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    if rank == 0:
+        print(json.dumps({"metric": "EP dispatch + combine fused with the exchange (profiling case)", "unit": "ms",
+                          "value": round(ms, 4), "steps": args.steps, "status": int(status.item()),
+                          "config": {"k": k, "tokens": tokens, "hidden": h, "experts": experts, "topk": topk}}),
+              flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -1290,6 +1419,8 @@ def main():
         args.no_extras = True
     if args.mode == "allgather":
         run_allgather_only(args, world, rank, local)
+    elif args.mode == "ep_fused":
+        run_ep_fused_only(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

@@ -12,6 +12,17 @@
 //        bf16.
 // Pairs whose expert id lies outside [0, experts) are dropped: they are sent
 // nowhere and add nothing to the combine.
+//
+// Fused with the exchange (hoc_ep_dispatch_fused / hoc_ep_combine_fused): all k
+// simulated ranks share one HBM, so the dispatch's row scatter writes each
+// token row straight to its place in the destination rank's receive buffer
+// -- the place the all-to-all would have copied it to -- and the combine
+// reads each of a token's rows straight from the expert rank's buffer.  The
+// places follow from the k x k counts on the device: row i of source s's
+// packed order, bound for rank d, lands at row rdispl[d][s] + i - sdispl[s][d]
+// of rank d's buffer, with rdispl[d][s] = sum of counts[s'][d] over s' < s and
+// sdispl[s][d] = sum of counts[s][d'] over d' < d (prefix sums in rank order,
+// the all-to-all's default displacements).
 #include <cuda_bf16.h>
 
 #include "hoc_internal.h"
@@ -39,9 +50,22 @@ __device__ __forceinline__ void pdl_enter() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Per-source pointers of the sort kernels; blockIdx.y selects the source, so
+// one launch sorts the pairs of every source rank (a single source: y = 0).
+struct EpSort {
+  const int32_t* ids[kMaxRanks];
+  int32_t* perm[kMaxRanks];    // null: not wanted (the fused dispatch needs only pos_of)
+  int32_t* pos_of[kMaxRanks];
+  unsigned long long* counts;  // [sources][nranks] element counts, row = source
+  int32_t* ws;                 // scratch of source s at ws + s * ws_stride
+  size_t ws_stride;
+};
+
 // One CTA per expert: how many pairs chose it.
-__global__ void ep_count_kernel(const int32_t* __restrict__ ids, int n, int32_t* __restrict__ cnt) {
+__global__ void ep_count_kernel(const __grid_constant__ EpSort P, int n) {
   pdl_enter();
+  const int32_t* __restrict__ ids = P.ids[blockIdx.y];
+  int32_t* __restrict__ cnt = P.ws + blockIdx.y * P.ws_stride;
   const int e = blockIdx.x;
   int total = 0;
   for (int base = 0; base < n; base += kEpThreads) {
@@ -53,10 +77,13 @@ __global__ void ep_count_kernel(const int32_t* __restrict__ ids, int n, int32_t*
 
 // One CTA per expert: place its pairs, in (token, slot) order, after the pairs
 // of all smaller experts.
-__global__ void ep_place_kernel(const int32_t* __restrict__ ids, int n, const int32_t* __restrict__ cnt,
-                                int32_t* __restrict__ perm, int32_t* __restrict__ pos_of,
-                                unsigned long long* __restrict__ dst_counts, int hidden, int per_rank) {
+__global__ void ep_place_kernel(const __grid_constant__ EpSort P, int n, int hidden, int per_rank, int nranks) {
   pdl_enter();
+  const int32_t* __restrict__ ids = P.ids[blockIdx.y];
+  const int32_t* __restrict__ cnt = P.ws + blockIdx.y * P.ws_stride;
+  int32_t* __restrict__ perm = P.perm[blockIdx.y];
+  int32_t* __restrict__ pos_of = P.pos_of[blockIdx.y];
+  unsigned long long* __restrict__ dst_counts = P.counts + size_t(blockIdx.y) * nranks;
   __shared__ int warp_n[kEpThreads / 32];
   const int e = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -76,7 +103,7 @@ __global__ void ep_place_kernel(const int32_t* __restrict__ ids, int n, const in
     }
     if (mine) {
       const int pos = offset + running + before + __popc(ballot & ((1u << lane) - 1u));
-      perm[pos] = i;
+      if (perm) perm[pos] = i;
       pos_of[i] = pos;
     }
     running += chunk;
@@ -87,8 +114,10 @@ __global__ void ep_place_kernel(const int32_t* __restrict__ ids, int n, const in
 
 // Tile histogram: hist[b * experts + e] = pairs of tile b that chose expert e.
 // A thread issues all of its loads of the tile before counting them.
-__global__ void ep_tile_hist_kernel(const int32_t* __restrict__ ids, int n, int experts, int32_t* __restrict__ hist) {
+__global__ void ep_tile_hist_kernel(const __grid_constant__ EpSort P, int n, int experts) {
   pdl_enter();
+  const int32_t* __restrict__ ids = P.ids[blockIdx.y];
+  int32_t* __restrict__ hist = P.ws + blockIdx.y * P.ws_stride + experts;
   extern __shared__ int sh[];
   for (int e = threadIdx.x; e < experts; e += blockDim.x) sh[e] = 0;
   const int lo = blockIdx.x * kTileItems;
@@ -106,20 +135,23 @@ __global__ void ep_tile_hist_kernel(const int32_t* __restrict__ ids, int n, int 
   for (int e = threadIdx.x; e < experts; e += blockDim.x) hist[size_t(blockIdx.x) * experts + e] = sh[e];
 }
 
-// One CTA: turns the tile histograms into the first output row of each
-// (tile, expert) -- all pairs of smaller experts, then those of expert e in
-// earlier tiles -- and writes the per-expert totals, the number of valid pairs
-// and the per-destination element counts.  With `staged` the histograms and
+// One CTA per source: turns the tile histograms into the first output row of
+// each (tile, expert) -- all pairs of smaller experts, then those of expert e
+// in earlier tiles -- and writes the per-expert totals, the number of valid
+// pairs and the per-destination element counts.  With `staged` the histograms and
 // totals are copied into shared memory once (coalesced), every scan runs on
 // that copy, and the starts go back once; otherwise the scans run in place in
 // global memory (shapes whose histograms exceed the shared budget).
 constexpr int kScanThreads = 1024;
 constexpr int kScanSmemInts = 48 * 1024 / 4 - kScanThreads;  // dynamic ints beside the static warp sums
 
-__global__ void ep_scan_kernel(int32_t* __restrict__ hist, int tiles, int experts, int32_t* __restrict__ total,
-                               int32_t* __restrict__ nvalid, unsigned long long* __restrict__ dst_counts, int nranks,
-                               int per_rank, int hidden, int staged) {
+__global__ void ep_scan_kernel(const __grid_constant__ EpSort P, int tiles, int experts, int nranks, int per_rank,
+                               int hidden, int staged) {
   pdl_enter();
+  int32_t* __restrict__ total = P.ws + blockIdx.x * P.ws_stride;
+  int32_t* __restrict__ hist = total + experts;
+  int32_t* __restrict__ nvalid = hist + size_t(tiles) * experts;
+  unsigned long long* __restrict__ dst_counts = P.counts + size_t(blockIdx.x) * nranks;
   __shared__ int warp_sum[kScanThreads / 32];
   extern __shared__ int dyn[];  // staged: [experts] totals, then [tiles][experts] histograms
   const size_t cells = size_t(tiles) * experts;
@@ -186,10 +218,13 @@ __global__ void ep_scan_kernel(int32_t* __restrict__ hist, int tiles, int expert
 // warp and lower lanes of its step.  A warp loads all of its expert ids, and
 // later all of their starts, before the dependent counting.
 constexpr int kWarpSteps = kWarpItems / 32;
-__global__ void ep_tile_place_kernel(const int32_t* __restrict__ ids, int n, int experts,
-                                     const int32_t* __restrict__ start, const int32_t* __restrict__ nvalid,
-                                     int32_t* __restrict__ perm, int32_t* __restrict__ pos_of) {
+__global__ void ep_tile_place_kernel(const __grid_constant__ EpSort P, int n, int experts, int tiles) {
   pdl_enter();
+  const int32_t* __restrict__ ids = P.ids[blockIdx.y];
+  const int32_t* __restrict__ start = P.ws + blockIdx.y * P.ws_stride + experts;
+  const int32_t* __restrict__ nvalid = start + size_t(tiles) * experts;
+  int32_t* __restrict__ perm = P.perm[blockIdx.y];
+  int32_t* __restrict__ pos_of = P.pos_of[blockIdx.y];
   extern __shared__ int wh[];  // [kEpWarps][experts]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int j = threadIdx.x; j < kEpWarps * experts; j += blockDim.x) wh[j] = 0;
@@ -231,7 +266,7 @@ __global__ void ep_tile_place_kernel(const int32_t* __restrict__ ids, int n, int
     const int i = lo + k * 32 + lane;
     if (ev[k] >= 0) {
       const int pos = sv[k] + mine[ev[k]] + __popc(grp[k] & below);
-      perm[pos] = i;
+      if (perm) perm[pos] = i;
       pos_of[i] = pos;
     } else if (i < hi) {
       pos_of[i] = -1;  // dropped pair
@@ -241,7 +276,8 @@ __global__ void ep_tile_place_kernel(const int32_t* __restrict__ ids, int n, int
     __syncwarp();
   }
   // rows past the valid pairs have no pair
-  for (int r = *nvalid + blockIdx.x * blockDim.x + threadIdx.x; r < n; r += gridDim.x * blockDim.x) perm[r] = -1;
+  if (perm)
+    for (int r = *nvalid + blockIdx.x * blockDim.x + threadIdx.x; r < n; r += gridDim.x * blockDim.x) perm[r] = -1;
 }
 
 // send[pos_of[t*topk + j]] = x[t] for every valid pair (t, j); rows of `hb`
@@ -418,16 +454,243 @@ __global__ void ep_combine_vec_ilp_kernel(const uint16_t* __restrict__ rows, con
   }
 }
 
+// ---------------------------------------------------------------------------
+// Fused with the exchange.  Per-source inputs and per-rank receive buffers of
+// one dispatch / combine over all k simulated ranks.
+struct EpRoute {
+  const char* x[kMaxRanks];         // dispatch: token rows of each source, [tokens, hidden] bf16
+  const int32_t* ids[kMaxRanks];    // expert id of every (token, slot) pair of each source
+  const int32_t* pos_of[kMaxRanks]; // packed row of every pair (-1: dropped)
+  const float* w[kMaxRanks];        // combine: gate weights of every pair
+  char* buf[kMaxRanks];             // receive buffer of each rank (dispatch writes, combine reads)
+  char* y[kMaxRanks];               // combine: output rows of each source
+  unsigned long long cap_rows[kMaxRanks];  // rows each receive buffer holds
+  const unsigned long long* counts;        // [k][k] element counts, row = source
+  int32_t* status;                  // bit 0: a dispatched row did not fit; bit 1: a combine row out of range
+  int k, tokens, topk, hidden, per_rank;
+};
+
+// base[s * k + d] = rdispl[d][s] - sdispl[s][d] in rows: packed row i of source
+// s bound for rank d goes to row base[s * k + d] + i of rank d's buffer.
+__device__ __forceinline__ void route_bases(const EpRoute& R, long long* base) {
+  for (int c = threadIdx.x; c < R.k * R.k; c += blockDim.x) {
+    const int s = c / R.k, d = c % R.k;
+    unsigned long long rd = 0, sd = 0;
+    for (int a = 0; a < s; ++a) rd += R.counts[a * R.k + d];
+    for (int b = 0; b < d; ++b) sd += R.counts[s * R.k + b];
+    base[c] = (long long)(rd / (unsigned long long)R.hidden) - (long long)(sd / (unsigned long long)R.hidden);
+  }
+  __syncthreads();
+}
+
+// Row of rank d's buffer that packed row `pos` (bound for rank d) of source s
+// occupies, or -1 (and the status bit `bit`) when it lies outside the buffer
+// or d is no rank (inputs that disagree with the dispatch that made them).
+__device__ __forceinline__ long long route_row(const EpRoute& R, const long long* base, int s, int d, int pos,
+                                               int bit) {
+  if (unsigned(d) >= unsigned(R.k)) {
+    atomicOr(R.status, bit);
+    return -1;
+  }
+  const long long row = base[s * R.k + d] + pos;
+  if (row < 0 || (unsigned long long)row >= R.cap_rows[d]) {
+    atomicOr(R.status, bit);
+    return -1;
+  }
+  return row;
+}
+
+// Dispatch: every token row of every source, read once, stored to each of its
+// valid pairs' rows in the destination ranks' buffers.  Vector path: a work
+// item is (source, token, 1 KiB slice), a lane moves two 16-byte vectors of
+// the slice; byte path: a warp per (source, token).
+__global__ void ep_dispatch_fused_kernel(const __grid_constant__ EpRoute R, int vec) {
+  pdl_enter();
+  __shared__ long long base[kMaxRanks * kMaxRanks];
+  route_bases(R, base);
+  const int lane = threadIdx.x & 31;
+  const int hb = R.hidden * 2;
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  const long long first = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int nv = hb / 16;
+  const int slices = vec ? (nv + kScatterSliceVecs - 1) / kScatterSliceVecs : 1;
+  const long long per_src = (long long)R.tokens * slices;
+  const long long items = per_src * R.k;
+  for (long long it = first; it < items; it += warps) {
+    const int s = int(it / per_src);
+    const long long rem = it % per_src;
+    const int t = int(rem / slices);
+    const char* src = R.x[s] + size_t(t) * hb;
+    uint4 a = make_uint4(0, 0, 0, 0), b = a;
+    int v0 = 0, v1 = 0;
+    bool h0 = false, h1 = false;
+    if (vec) {
+      v0 = int(rem % slices) * kScatterSliceVecs + lane;
+      v1 = v0 + 32;
+      h0 = v0 < nv;
+      h1 = v1 < nv;
+      if (h0) a = __ldg(reinterpret_cast<const uint4*>(src) + v0);
+      if (h1) b = __ldg(reinterpret_cast<const uint4*>(src) + v1);
+    }
+    for (int j0 = 0; j0 < R.topk; j0 += 32) {
+      const size_t pr = size_t(t) * R.topk + j0 + lane;
+      const bool in = j0 + lane < R.topk;
+      const int pl = in ? R.pos_of[s][pr] : -1;
+      const int el = in ? R.ids[s][pr] : 0;
+      const int nj = min(32, R.topk - j0);
+      for (int j = 0; j < nj; ++j) {
+        const int pos = __shfl_sync(0xFFFFFFFFu, pl, j);
+        const int e = __shfl_sync(0xFFFFFFFFu, el, j);
+        if (pos < 0) continue;  // dropped pair: sent nowhere
+        const int d = e / R.per_rank;
+        const long long row = route_row(R, base, s, d, pos, 1);
+        if (row < 0) continue;
+        char* dst = R.buf[d] + size_t(row) * hb;
+        if (vec) {
+          if (h0) reinterpret_cast<uint4*>(dst)[v0] = a;
+          if (h1) reinterpret_cast<uint4*>(dst)[v1] = b;
+        } else {
+          for (int i = lane; i < hb; i += 32) dst[i] = src[i];
+        }
+      }
+    }
+  }
+}
+
+// Combine, reading every row straight from the expert rank's buffer; the same
+// fold as the packed-order combine.  TK > 0: vector path with all TK row loads
+// of a lane issued before the ordered fold (work item = (source, token, 512 B
+// slice)); TK == 0: vector path for any topk, one load at a time.
+template <int TK>
+__global__ void ep_combine_fused_vec_kernel(const __grid_constant__ EpRoute R) {
+  pdl_enter();
+  __shared__ long long base[kMaxRanks * kMaxRanks];
+  route_bases(R, base);
+  const int lane = threadIdx.x & 31;
+  const int hv = R.hidden / 8;
+  const int slices = (hv + 31) / 32;
+  const long long per_src = (long long)R.tokens * slices;
+  const long long items = per_src * R.k;
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long it = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items; it += warps) {
+    const int s = int(it / per_src);
+    const long long rem = it % per_src;
+    const int t = int(rem / slices);
+    const int v = int(rem % slices) * 32 + lane;
+    float acc[8];
+    bool any = false;
+    if constexpr (TK > 0) {
+      const size_t pr = size_t(t) * TK + lane;
+      const int pl = lane < TK ? R.pos_of[s][pr] : -1;
+      const int el = lane < TK ? R.ids[s][pr] : 0;
+      const float wl = lane < TK ? R.w[s][pr] : 0.f;
+      const char* src[TK];
+      float wj[TK];
+#pragma unroll
+      for (int j = 0; j < TK; ++j) {
+        const int p = __shfl_sync(0xFFFFFFFFu, pl, j);
+        const int e = __shfl_sync(0xFFFFFFFFu, el, j);
+        wj[j] = __shfl_sync(0xFFFFFFFFu, wl, j);
+        src[j] = nullptr;
+        if (p >= 0) {
+          const int d = e / R.per_rank;
+          const long long row = route_row(R, base, s, d, p, 2);
+          if (row >= 0) src[j] = R.buf[d] + size_t(row) * R.hidden * 2;
+        }
+      }
+      if (v >= hv) continue;
+      uint4 x[TK];
+#pragma unroll
+      for (int j = 0; j < TK; ++j)
+        x[j] = src[j] ? __ldg(reinterpret_cast<const uint4*>(src[j]) + v) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int j = 0; j < TK; ++j) {
+        if (!src[j]) continue;
+        const uint32_t q[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float lo = __fmul_rn(wj[j], __uint_as_float(q[i] << 16));
+          const float hi = __fmul_rn(wj[j], __uint_as_float(q[i] & 0xFFFF0000u));
+          acc[2 * i] = any ? __fadd_rn(acc[2 * i], lo) : lo;
+          acc[2 * i + 1] = any ? __fadd_rn(acc[2 * i + 1], hi) : hi;
+        }
+        any = true;
+      }
+    } else {
+      for (int j = 0; j < R.topk; ++j) {
+        const size_t pr = size_t(t) * R.topk + j;
+        const int p = R.pos_of[s][pr];
+        if (p < 0) continue;
+        const int d = R.ids[s][pr] / R.per_rank;
+        const long long row = route_row(R, base, s, d, p, 2);
+        if (row < 0 || v >= hv) continue;
+        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(R.buf[d] + size_t(row) * R.hidden * 2) + v);
+        const float wj = R.w[s][pr];
+        const uint32_t q[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float lo = __fmul_rn(wj, __uint_as_float(q[i] << 16));
+          const float hi = __fmul_rn(wj, __uint_as_float(q[i] & 0xFFFF0000u));
+          acc[2 * i] = any ? __fadd_rn(acc[2 * i], lo) : lo;
+          acc[2 * i + 1] = any ? __fadd_rn(acc[2 * i + 1], hi) : hi;
+        }
+        any = true;
+      }
+      if (v >= hv) continue;
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float lo = any ? acc[2 * i] : 0.f, hi = any ? acc[2 * i + 1] : 0.f;
+      o[i] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+             (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+    }
+    reinterpret_cast<uint4*>(R.y[s] + size_t(t) * R.hidden * 2)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Combine, scalar path (hidden not a multiple of 8 or buffers not 16-byte
+// aligned): a warp per (source, token), a lane per element.
+__global__ void ep_combine_fused_kernel(const __grid_constant__ EpRoute R) {
+  pdl_enter();
+  __shared__ long long base[kMaxRanks * kMaxRanks];
+  route_bases(R, base);
+  const int lane = threadIdx.x & 31;
+  const long long items = (long long)R.tokens * R.k;
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long it = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items; it += warps) {
+    const int s = int(it / R.tokens), t = int(it % R.tokens);
+    uint16_t* yrow = reinterpret_cast<uint16_t*>(R.y[s] + size_t(t) * R.hidden * 2);
+    for (int h = lane; h < R.hidden; h += 32) {
+      float acc = 0.f;
+      bool any = false;
+      for (int j = 0; j < R.topk; ++j) {
+        const size_t pr = size_t(t) * R.topk + j;
+        const int p = R.pos_of[s][pr];
+        if (p < 0) continue;
+        const int d = R.ids[s][pr] / R.per_rank;
+        const long long row = route_row(R, base, s, d, p, 2);
+        if (row < 0) continue;
+        const uint16_t* src = reinterpret_cast<const uint16_t*>(R.buf[d] + size_t(row) * R.hidden * 2);
+        const float prod = __fmul_rn(R.w[s][pr], __uint_as_float(uint32_t(src[h]) << 16));
+        acc = any ? __fadd_rn(acc, prod) : prod;
+        any = true;
+      }
+      yrow[h] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+    }
+  }
+}
+
 int tiles_of(int n) { return (n + kTileItems - 1) / kTileItems; }
 
 // Launch with programmatic stream serialization (see pdl_enter).
 template <class... KArgs, class... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, size_t smem, cudaStream_t s, Args... args) {
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, int block, size_t smem, cudaStream_t s, Args... args) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = grid;
   cfg.blockDim = dim3(block);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -473,6 +736,51 @@ int grid_for(int items, int per_cta) {
   return want < 1 ? 1 : (want < cap ? want : cap);
 }
 
+// Per-source scratch of the sort: tile path [experts] totals, [tiles][experts]
+// histograms and one valid-pair count; many-experts path [experts] counts.
+size_t sort_ws_ints(int n, int experts) {
+  return experts <= kMaxTileExperts ? size_t(experts) * (1 + size_t(tiles_of(n))) + 1 : size_t(experts);
+}
+
+// Stable counting sort of the n = tokens * topk pairs of `sources` sources in
+// one set of launches: pos_of (and perm where wanted) of every source, and the
+// per-destination element counts (row s of P.counts).
+cudaError_t sort_pairs(const EpSort& P, int sources, int n, int experts, int nranks, int hidden, cudaStream_t s) {
+  if (experts <= kMaxTileExperts) {
+    // histograms, one scan per source (which writes every destination count),
+    // stable placement (which writes every pos_of and the -1 tail of perm)
+    const int tiles = tiles_of(n);
+    cudaError_t e = launch_pdl(ep_tile_hist_kernel, dim3(tiles, sources), kEpThreads, sizeof(int) * size_t(experts), s,
+                               P, n, experts);
+    const size_t stage_ints = size_t(experts) + size_t(tiles) * experts;
+    const int staged = stage_ints <= size_t(kScanSmemInts);
+    if (e == cudaSuccess)
+      e = launch_pdl(ep_scan_kernel, dim3(sources), kScanThreads, staged ? sizeof(int) * stage_ints : 0, s, P, tiles,
+                     experts, nranks, experts / nranks, hidden, staged);
+    if (e == cudaSuccess)
+      e = launch_pdl(ep_tile_place_kernel, dim3(tiles, sources), kEpThreads, sizeof(int) * size_t(kEpWarps) * experts,
+                     s, P, n, experts, tiles);
+    return e;
+  }
+  // many experts: one CTA per (expert, source) scanning every pair of its source
+  for (int src = 0; src < sources; ++src) {
+    if (P.perm[src] && cudaMemsetAsync(P.perm[src], 0xFF, sizeof(int32_t) * size_t(n), s) != cudaSuccess)
+      return cudaGetLastError();
+    if (cudaMemsetAsync(P.pos_of[src], 0xFF, sizeof(int32_t) * size_t(n), s) != cudaSuccess) return cudaGetLastError();
+  }
+  if (cudaMemsetAsync(P.counts, 0, sizeof(uint64_t) * size_t(sources) * nranks, s) != cudaSuccess)
+    return cudaGetLastError();
+  ep_count_kernel<<<dim3(experts, sources), kEpThreads, 0, s>>>(P, n);
+  ep_place_kernel<<<dim3(experts, sources), kEpThreads, 0, s>>>(P, n, hidden, experts / nranks, nranks);
+  return cudaGetLastError();
+}
+
+using CombineFusedFn = void (*)(EpRoute);
+const CombineFusedFn kCombineFused[kCombineTopk + 1] = {
+    ep_combine_fused_vec_kernel<0>, ep_combine_fused_vec_kernel<1>, ep_combine_fused_vec_kernel<2>,
+    ep_combine_fused_vec_kernel<3>, ep_combine_fused_vec_kernel<4>, ep_combine_fused_vec_kernel<5>,
+    ep_combine_fused_vec_kernel<6>, ep_combine_fused_vec_kernel<7>, ep_combine_fused_vec_kernel<8>};
+
 }  // namespace
 
 cudaError_t ep_preload() {
@@ -487,7 +795,14 @@ cudaError_t ep_preload() {
                        reinterpret_cast<const void*>(kCombineIlp[0]), reinterpret_cast<const void*>(kCombineIlp[1]),
                        reinterpret_cast<const void*>(kCombineIlp[2]), reinterpret_cast<const void*>(kCombineIlp[3]),
                        reinterpret_cast<const void*>(kCombineIlp[4]), reinterpret_cast<const void*>(kCombineIlp[5]),
-                       reinterpret_cast<const void*>(kCombineIlp[6]), reinterpret_cast<const void*>(kCombineIlp[7])};
+                       reinterpret_cast<const void*>(kCombineIlp[6]), reinterpret_cast<const void*>(kCombineIlp[7]),
+                       reinterpret_cast<const void*>(&ep_dispatch_fused_kernel),
+                       reinterpret_cast<const void*>(&ep_combine_fused_kernel),
+                       reinterpret_cast<const void*>(kCombineFused[0]), reinterpret_cast<const void*>(kCombineFused[1]),
+                       reinterpret_cast<const void*>(kCombineFused[2]), reinterpret_cast<const void*>(kCombineFused[3]),
+                       reinterpret_cast<const void*>(kCombineFused[4]), reinterpret_cast<const void*>(kCombineFused[5]),
+                       reinterpret_cast<const void*>(kCombineFused[6]), reinterpret_cast<const void*>(kCombineFused[7]),
+                       reinterpret_cast<const void*>(kCombineFused[8])};
   for (const void* f : fns) {
     cudaFuncAttributes a;
     const cudaError_t e = cudaFuncGetAttributes(&a, f);
@@ -502,8 +817,7 @@ extern "C" hocResult_t hoc_ep_pack_workspace(int tokens, int topk, int experts, 
   using namespace hoc;
   if (tokens < 0 || topk < 1 || experts < 1 || !ints) return HOC_ERR_INVALID_ARG;
   if (size_t(tokens) * topk > size_t(INT32_MAX)) return HOC_ERR_INVALID_ARG;
-  const int n = tokens * topk;
-  *ints = experts <= kMaxTileExperts ? size_t(experts) * (1 + size_t(tiles_of(n))) + 1 : size_t(experts);
+  *ints = sort_ws_ints(tokens * topk, experts);
   return HOC_SUCCESS;
 }
 
@@ -529,31 +843,16 @@ extern "C" hocResult_t hoc_ep_pack(const int32_t* expert_ids, const void* x, int
   }
   const int n = tokens * topk;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (experts <= kMaxTileExperts) {
-    // counting sort by tiles: histograms, one scan (which writes every
-    // destination count), stable placement (which writes every pos_of and the
-    // -1 tail of perm)
-    const int tiles = tiles_of(n);
-    int32_t* total = workspace;
-    int32_t* hist = workspace + experts;
-    int32_t* nvalid = hist + size_t(tiles) * experts;
-    launch_pdl(ep_tile_hist_kernel, tiles, kEpThreads, sizeof(int) * size_t(experts), s, expert_ids, n, experts, hist);
-    const size_t stage_ints = size_t(experts) + size_t(tiles) * experts;
-    const int staged = stage_ints <= size_t(kScanSmemInts);
-    launch_pdl(ep_scan_kernel, 1, kScanThreads, staged ? sizeof(int) * stage_ints : 0, s, hist, tiles, experts, total,
-               nvalid, reinterpret_cast<unsigned long long*>(dst_counts), nranks, experts / nranks, hidden, staged);
-    launch_pdl(ep_tile_place_kernel, tiles, kEpThreads, sizeof(int) * size_t(kEpWarps) * experts, s, expert_ids, n,
-               experts, static_cast<const int32_t*>(hist), static_cast<const int32_t*>(nvalid), perm, pos_of);
-  } else {
-    // many experts: one CTA per expert scanning every pair
-    if (cudaMemsetAsync(perm, 0xFF, sizeof(int32_t) * size_t(n), s) != cudaSuccess ||
-        cudaMemsetAsync(pos_of, 0xFF, sizeof(int32_t) * size_t(n), s) != cudaSuccess ||
-        cudaMemsetAsync(dst_counts, 0, sizeof(uint64_t) * size_t(nranks), s) != cudaSuccess)
-      return HOC_ERR_CUDA;
-    ep_count_kernel<<<experts, kEpThreads, 0, s>>>(expert_ids, n, workspace);
-    ep_place_kernel<<<experts, kEpThreads, 0, s>>>(expert_ids, n, workspace, perm, pos_of,
-                                                   reinterpret_cast<unsigned long long*>(dst_counts), hidden,
-                                                   experts / nranks);
+  EpSort P{};
+  P.ids[0] = expert_ids;
+  P.perm[0] = perm;
+  P.pos_of[0] = pos_of;
+  P.counts = reinterpret_cast<unsigned long long*>(dst_counts);
+  P.ws = workspace;
+  P.ws_stride = need;
+  if (sort_pairs(P, 1, n, experts, nranks, hidden, s) != cudaSuccess) {
+    set_error_detail("hoc_ep_pack: launching the sort failed");
+    return HOC_ERR_CUDA;
   }
   const int hb = hidden * 2;
   const int vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(send)) & 15u) == 0 && hb % 16 == 0;
@@ -586,4 +885,124 @@ extern "C" hocResult_t hoc_ep_combine(const void* rows, const int32_t* pos_of, c
     ep_combine_kernel<<<grid_for(tokens, 8), 256, 0, s>>>(static_cast<const uint16_t*>(rows), pos_of, weights, tokens,
                                                           topk, hidden, tokens * topk, static_cast<uint16_t*>(y));
   return cudaGetLastError() == cudaSuccess ? HOC_SUCCESS : HOC_ERR_CUDA;
+}
+
+extern "C" hocResult_t hoc_ep_dispatch_fused(int nranks, const int32_t* const* expert_ids, const void* const* x,
+                                             int tokens, int topk, int hidden, int experts, void* const* recv,
+                                             const size_t* recv_capacity, int32_t* const* pos_of, uint64_t* counts,
+                                             int32_t* workspace, size_t workspace_ints, int32_t* status, void* stream) {
+  using namespace hoc;
+  if (nranks < 1 || nranks > kMaxRanks || tokens < 0 || topk < 1 || hidden < 1 || experts < 1 ||
+      experts % nranks != 0) {
+    set_error_detail("hoc_ep_dispatch_fused: bad rank count, shape or expert count");
+    return HOC_ERR_INVALID_ARG;
+  }
+  if (!expert_ids || !x || !recv || !recv_capacity || !pos_of || !counts || !status) return HOC_ERR_INVALID_ARG;
+  if (size_t(tokens) * topk > size_t(INT32_MAX)) return HOC_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return HOC_ERR_CUDA;
+  if (tokens == 0)  // nobody sends anything
+    return cudaMemsetAsync(counts, 0, sizeof(uint64_t) * size_t(nranks) * nranks, s) == cudaSuccess ? HOC_SUCCESS
+                                                                                                     : HOC_ERR_CUDA;
+  const int n = tokens * topk;
+  const size_t per = sort_ws_ints(n, experts);
+  if (!workspace || workspace_ints < per * size_t(nranks)) {
+    set_error_detail("hoc_ep_dispatch_fused: workspace smaller than nranks * hoc_ep_pack_workspace()");
+    return HOC_ERR_INVALID_ARG;
+  }
+  EpSort P{};
+  EpRoute R{};
+  bool vec = (size_t(hidden) * 2) % 16 == 0;
+  for (int r = 0; r < nranks; ++r) {
+    if (!expert_ids[r] || !x[r] || !recv[r] || !pos_of[r]) {
+      set_error_detail("hoc_ep_dispatch_fused: NULL per-rank pointer");
+      return HOC_ERR_INVALID_ARG;
+    }
+    P.ids[r] = expert_ids[r];
+    P.pos_of[r] = pos_of[r];
+    R.x[r] = static_cast<const char*>(x[r]);
+    R.ids[r] = expert_ids[r];
+    R.pos_of[r] = pos_of[r];
+    R.buf[r] = static_cast<char*>(recv[r]);
+    R.cap_rows[r] = recv_capacity[r] / size_t(hidden);
+    vec = vec && ((reinterpret_cast<uintptr_t>(x[r]) | reinterpret_cast<uintptr_t>(recv[r])) & 15u) == 0;
+  }
+  P.counts = reinterpret_cast<unsigned long long*>(counts);
+  P.ws = workspace;
+  P.ws_stride = per;
+  if (sort_pairs(P, nranks, n, experts, nranks, hidden, s) != cudaSuccess) {
+    set_error_detail("hoc_ep_dispatch_fused: launching the sort failed");
+    return HOC_ERR_CUDA;
+  }
+  R.counts = P.counts;
+  R.status = status;
+  R.k = nranks;
+  R.tokens = tokens;
+  R.topk = topk;
+  R.hidden = hidden;
+  R.per_rank = experts / nranks;
+  const int hb = hidden * 2;
+  const long long warps = (long long)nranks * tokens *
+                          (vec ? (hb / 16 + kScatterSliceVecs - 1) / kScatterSliceVecs : 1);
+  const void* fn = reinterpret_cast<const void*>(&ep_dispatch_fused_kernel);
+  if (launch_pdl(ep_dispatch_fused_kernel, dim3(persistent_grid(fn, (warps + 7) / 8)), 256, 0, s, R, int(vec)) !=
+      cudaSuccess) {
+    set_error_detail("hoc_ep_dispatch_fused: launching the row scatter failed");
+    return HOC_ERR_CUDA;
+  }
+  return HOC_SUCCESS;
+}
+
+extern "C" hocResult_t hoc_ep_combine_fused(int nranks, const void* const* rows, const size_t* rows_capacity,
+                                            const int32_t* const* expert_ids, const int32_t* const* pos_of,
+                                            const uint64_t* counts, const float* const* weights, int tokens, int topk,
+                                            int hidden, int experts, void* const* y, int32_t* status, void* stream) {
+  using namespace hoc;
+  if (nranks < 1 || nranks > kMaxRanks || tokens < 0 || topk < 1 || hidden < 1 || experts < 1 ||
+      experts % nranks != 0) {
+    set_error_detail("hoc_ep_combine_fused: bad rank count, shape or expert count");
+    return HOC_ERR_INVALID_ARG;
+  }
+  if (tokens == 0) return HOC_SUCCESS;
+  if (!rows || !rows_capacity || !expert_ids || !pos_of || !counts || !weights || !y || !status)
+    return HOC_ERR_INVALID_ARG;
+  if (size_t(tokens) * topk > size_t(INT32_MAX)) return HOC_ERR_INVALID_ARG;
+  EpRoute R{};
+  bool vec = hidden % 8 == 0;
+  for (int r = 0; r < nranks; ++r) {
+    if (!rows[r] || !expert_ids[r] || !pos_of[r] || !weights[r] || !y[r]) {
+      set_error_detail("hoc_ep_combine_fused: NULL per-rank pointer");
+      return HOC_ERR_INVALID_ARG;
+    }
+    R.buf[r] = static_cast<char*>(const_cast<void*>(rows[r]));
+    R.cap_rows[r] = rows_capacity[r] / size_t(hidden);
+    R.ids[r] = expert_ids[r];
+    R.pos_of[r] = pos_of[r];
+    R.w[r] = weights[r];
+    R.y[r] = static_cast<char*>(y[r]);
+    vec = vec && ((reinterpret_cast<uintptr_t>(rows[r]) | reinterpret_cast<uintptr_t>(y[r])) & 15u) == 0;
+  }
+  R.counts = reinterpret_cast<const unsigned long long*>(counts);
+  R.status = status;
+  R.k = nranks;
+  R.tokens = tokens;
+  R.topk = topk;
+  R.hidden = hidden;
+  R.per_rank = experts / nranks;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (vec) {
+    const CombineFusedFn fn = kCombineFused[topk <= kCombineTopk ? topk : 0];
+    const long long items = (long long)nranks * tokens * ((hidden / 8 + 31) / 32);  // one warp per item
+    e = launch_pdl(fn, dim3(persistent_grid(reinterpret_cast<const void*>(fn), (items + 7) / 8)), 256, 0, s, R);
+  } else {
+    const void* fn = reinterpret_cast<const void*>(&ep_combine_fused_kernel);
+    e = launch_pdl(ep_combine_fused_kernel, dim3(persistent_grid(fn, ((long long)nranks * tokens + 7) / 8)), 256, 0,
+                   s, R);
+  }
+  if (e != cudaSuccess) {
+    set_error_detail("hoc_ep_combine_fused: launch failed");
+    return HOC_ERR_CUDA;
+  }
+  return HOC_SUCCESS;
 }

@@ -102,6 +102,14 @@ _SIGS["hoc_ep_pack"] = (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_
 _SIGS["hoc_ep_pack_workspace"] = (C.c_int, [C.c_int, C.c_int, C.c_int, C.POINTER(C.c_size_t)])
 _SIGS["hoc_ep_combine"] = (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p,
                                      C.c_void_p])
+_SIGS["hoc_ep_dispatch_fused"] = (C.c_int, [C.c_int, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_int, C.c_int,
+                                            C.c_int, C.c_int, C.POINTER(C.c_void_p), C.POINTER(C.c_size_t),
+                                            C.POINTER(C.c_void_p), C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p,
+                                            C.c_void_p])
+_SIGS["hoc_ep_combine_fused"] = (C.c_int, [C.c_int, C.POINTER(C.c_void_p), C.POINTER(C.c_size_t),
+                                           C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_void_p,
+                                           C.POINTER(C.c_void_p), C.c_int, C.c_int, C.c_int, C.c_int,
+                                           C.POINTER(C.c_void_p), C.c_void_p, C.c_void_p])
 _SIGS["hoc_allreduce_host"] = (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_size_t,
                                          C.c_int, C.c_int, C.c_void_p])
 _SIGS["hoc_proxy_status"] = (C.c_int, [C.c_void_p, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64),
@@ -484,6 +492,45 @@ def ep_combine(rows, pos_of, weights, tokens: int, topk: int, hidden: int, y, st
     _check(lib().hoc_ep_combine(_ptr(rows, 2 * n * int(hidden), "rows"), _ptr(pos_of, 4 * n, "pos_of"),
                                 _ptr(weights, 4 * n, "weights"), int(tokens), int(topk), int(hidden),
                                 _ptr(y, 2 * int(tokens) * int(hidden), "y"), _stream(stream)), "hoc_ep_combine")
+
+
+def ep_dispatch_fused(expert_ids, x, experts: int, recv, recv_capacity, pos_of, counts, workspace, status,
+                      stream=None):
+    """Dispatch of every source rank straight into the receive buffers (see include/hoc_ep.h).
+
+    Lists of k device tensors: expert_ids [tokens*topk] int32, x [tokens, hidden] bf16, recv (room for
+    recv_capacity[d] elements each), pos_of [tokens*topk] int32; counts: [k, k] int64; status: int32."""
+    k = len(x)
+    tokens, hidden = x[0].shape
+    topk = expert_ids[0].numel() // tokens if tokens else 1
+    n = tokens * topk
+    caps = [int(v) for v in recv_capacity]
+    if len(caps) != k or len(expert_ids) != k or len(recv) != k or len(pos_of) != k:
+        raise ValueError(f"expected {k} per-rank tensors and capacities")
+    cap = (C.c_size_t * k)(*caps)
+    _check(lib().hoc_ep_dispatch_fused(k, _ptr_array(expert_ids, 4 * n, "expert_ids"),
+                                       _ptr_array(x, 2 * tokens * hidden, "x"), int(tokens), int(topk), int(hidden),
+                                       int(experts), _ptr_array(recv, [2 * c for c in caps], "recv"), cap,
+                                       _ptr_array(pos_of, 4 * n, "pos_of"), _ptr(counts, 8 * k * k, "counts"),
+                                       _ptr(workspace, 0, "workspace"), int(workspace.numel()),
+                                       _ptr(status, 4, "status"), _stream(stream)), "hoc_ep_dispatch_fused")
+
+
+def ep_combine_fused(rows, rows_capacity, expert_ids, pos_of, counts, weights, tokens: int, topk: int, hidden: int,
+                     experts: int, y, status, stream=None):
+    """Combine of every source rank reading the expert ranks' rows in place (see include/hoc_ep.h)."""
+    k = len(rows)
+    n = int(tokens) * int(topk)
+    caps = [int(v) for v in rows_capacity]
+    if len(caps) != k or len(expert_ids) != k or len(pos_of) != k or len(weights) != k or len(y) != k:
+        raise ValueError(f"expected {k} per-rank tensors and capacities")
+    cap = (C.c_size_t * k)(*caps)
+    _check(lib().hoc_ep_combine_fused(k, _ptr_array(rows, [2 * c for c in caps], "rows"), cap,
+                                      _ptr_array(expert_ids, 4 * n, "expert_ids"), _ptr_array(pos_of, 4 * n, "pos_of"),
+                                      _ptr(counts, 8 * k * k, "counts"), _ptr_array(weights, 4 * n, "weights"),
+                                      int(tokens), int(topk), int(hidden), int(experts),
+                                      _ptr_array(y, 2 * int(tokens) * int(hidden), "y"), _ptr(status, 4, "status"),
+                                      _stream(stream)), "hoc_ep_combine_fused")
 
 
 def sm_count(device: int = 0) -> int:

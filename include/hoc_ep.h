@@ -46,6 +46,55 @@ hocResult_t hoc_ep_pack_workspace(int tokens, int topk, int experts, size_t* int
 hocResult_t hoc_ep_combine(const void* rows, const int32_t* pos_of, const float* weights, int tokens, int topk,
                            int hidden, void* y, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Dispatch and combine fused with the all-to-all.  All k simulated ranks live
+ * in one GPU's memory, so no send buffer and no exchange is needed: the row
+ * scatter writes every token row straight to the place in the destination
+ * rank's receive buffer that the dispatch all-to-all (default displacements:
+ * prefix sums in rank order) would have copied it to, and the combine reads a
+ * token's top-k rows straight from the expert ranks' buffers, where the
+ * inverse exchange would have fetched them.  Both run on SMs; the copy-engine
+ * exchange (hoc_ep_pack + hoc_alltoall_device_counts + hoc_ep_combine) stays
+ * the zero-SM way.  Results are bit for bit those of pack -> all-to-all ->
+ * inverse all-to-all -> combine.  Every rank has `tokens` tokens; all pointer
+ * arrays are host arrays of nranks (1..HOC_MAX_RANKS) device pointers, read
+ * during the call.
+ * ------------------------------------------------------------------------- */
+
+/* Dispatch of every source rank in one pass.  expert_ids[s]: [tokens*topk]
+ * int32; x[s]: [tokens, hidden] bf16; recv[d]: receive buffer of rank d, room
+ * for recv_capacity[d] elements (host array).  Writes
+ *   recv[d]:   the rows bound for rank d, source by source, each source's rows
+ *              in (expert, token, slot) order -- the layout of hoc_ep_pack's
+ *              send buffers after the all-to-all;
+ *   pos_of[s]: [tokens*topk] int32, the packed row of each pair of source s
+ *              (-1 for a dropped pair), as hoc_ep_pack;
+ *   counts:    device [nranks*nranks] uint64 element counts, row = source;
+ *   *status:   device int32, cleared first; bit 0 set if a row did not fit its
+ *              receive buffer (that row is not written).
+ * workspace: device int32 scratch of at least nranks * hoc_ep_pack_workspace()
+ * entries (else HOC_ERR_INVALID_ARG, nothing queued).  Pairs with an expert id
+ * outside [0, experts) are dropped; experts is a multiple of nranks.  Stream-
+ * ordered; the host does not wait. */
+hocResult_t hoc_ep_dispatch_fused(int nranks, const int32_t* const* expert_ids, const void* const* x, int tokens,
+                                  int topk, int hidden, int experts, void* const* recv, const size_t* recv_capacity,
+                                  int32_t* const* pos_of, uint64_t* counts, int32_t* workspace,
+                                  size_t workspace_ints, int32_t* status, void* stream);
+
+/* Combine of every source rank in one pass, reading rows[d] -- rank d's rows
+ * after its experts, in the receive layout the dispatch wrote, room for
+ * rows_capacity[d] elements -- at the places the dispatch's counts give.
+ * expert_ids, pos_of and counts are those of the dispatch; weights[s]:
+ * [tokens*topk] fp32 gate weights; y[s]: [tokens, hidden] bf16 output.  The
+ * fold is hoc_ep_combine's: y[s][t] = bf16 of the binary32 sum, in slot order,
+ * of fp32(weight * row) over the token's valid pairs (+0 when none).  Bit 1 of
+ * *status (not cleared here) is set if a row lies outside its buffer (it then
+ * adds nothing). */
+hocResult_t hoc_ep_combine_fused(int nranks, const void* const* rows, const size_t* rows_capacity,
+                                 const int32_t* const* expert_ids, const int32_t* const* pos_of,
+                                 const uint64_t* counts, const float* const* weights, int tokens, int topk,
+                                 int hidden, int experts, void* const* y, int32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

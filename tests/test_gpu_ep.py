@@ -152,3 +152,104 @@ def test_combine_golden_cases(hidden):
         got = y.view(torch.int16).cpu().numpy().astype(np.int64) & 0xFFFF
         assert np.array_equal(got, np.repeat(c["y"].astype(np.int64)[:, None], hidden, axis=1)), \
             (c["name"], hidden, [hex(int(v)) for v in got.reshape(-1)])
+
+
+# ---------------------------------------------------------------- fused with the exchange
+def _oracle_round_trip(xs, routing, ws, experts, k, topk, hidden):
+    """pack -> all-to-all -> (identity experts) -> inverse all-to-all -> combine, on the CPU."""
+    packs = [o_ep.pack(xs[r], routing[r], experts, k) for r in range(k)]
+    counts = np.stack([p[3] for p in packs])
+    recv = o_a2a.alltoallv([p[0].reshape(-1) for p in packs], counts)
+    back = o_a2a.alltoallv(recv, o_a2a.transpose_counts(counts))
+    ys = [o_ep.combine(back[r].reshape(-1, hidden), packs[r][2], ws[r], topk) for r in range(k)]
+    return packs, counts, recv, ys
+
+
+def _fused_on_device(k, xs, routing, ws, experts, topk, caps, recv_offset=0, y_offset=0):
+    from tests.gpu_util import Guarded
+    tokens, hidden = xs[0].shape
+    n = tokens * topk
+    d_ids = [torch.from_numpy(np.ascontiguousarray(r, dtype=np.int32).reshape(-1)).cuda() for r in routing]
+    d_x = [to_device(x, "bfloat16") for x in xs]
+    recv = [Guarded(max(1, c), "bfloat16", offset_elems=recv_offset) for c in caps]
+    pos = [torch.full((max(1, n),), -7, dtype=torch.int32, device="cuda") for _ in range(k)]
+    counts = torch.full((k, k), -1, dtype=torch.int64, device="cuda")
+    wsp = torch.empty(max(1, k * hoc.ep_pack_workspace(tokens, topk, experts)), dtype=torch.int32, device="cuda")
+    status = torch.full((1,), 99, dtype=torch.int32, device="cuda")
+    hoc.ep_dispatch_fused(d_ids, d_x, experts, [g.tensor for g in recv], caps, pos, counts, wsp, status)
+    w = [torch.from_numpy(x).cuda() for x in ws]
+    ys = [Guarded(tokens * hidden, "bfloat16", offset_elems=y_offset) for _ in range(k)]
+    hoc.ep_combine_fused([g.tensor for g in recv], caps, d_ids, pos, counts, w, tokens, topk, hidden, experts,
+                         [g.tensor for g in ys], status)
+    torch.cuda.synchronize()
+    return recv, pos, counts, status, ys
+
+
+@pytest.mark.parametrize("k,tokens,hidden,drop,experts,topk,recv_offset", [
+    (8, 4096, 2048, False, 64, 6, 0),   # the EP workload's shape
+    (8, 333, 40, True, 64, 6, 0),       # partial tile, dropped pairs; rows of 80 B: one partial slice each
+    (8, 250, 36, True, 64, 6, 0),       # rows of 72 B: byte dispatch, scalar combine
+    (8, 5000, 64, True, 96, 4, 0),      # ragged last tile, 12 experts per rank
+    (3, 1000, 64, True, 48, 4, 0),      # three ranks
+    (8, 700, 16, False, 2048, 2, 0),    # more than 1024 experts: the one-CTA-per-expert sort
+    (8, 200, 24, False, 64, 10, 0),     # topk above the batched loads: the one-load-at-a-time combine
+    (8, 100, 16, True, 64, 40, 0),      # topk above a warp
+    (8, 777, 64, True, 64, 6, 1),       # receive buffers 2 bytes off alignment: byte dispatch, scalar combine
+    (1, 300, 64, True, 8, 3, 0),        # one rank: everything stays home
+])
+def test_fused_dispatch_and_combine_match_oracle(k, tokens, hidden, drop, experts, topk, recv_offset):
+    routing = [r.copy() for r in inputs.ep_routing(k, tokens, experts, topk, 1.1, seed_base=5200 + k)]
+    if drop:
+        routing[0][3 % tokens, 0] = -5
+        routing[k - 1][7 % tokens, topk - 1] = experts
+    xs = [inputs.normal_bf16(tokens * hidden, 5700 + r).reshape(tokens, hidden) for r in range(k)]
+    rng = np.random.default_rng(5800 + k)
+    ws = [rng.random(tokens * topk).astype(np.float32) for _ in range(k)]
+    packs, counts, want_recv, want_y = _oracle_round_trip(xs, routing, ws, experts, k, topk, hidden)
+    caps = [int(counts[:, d].sum()) + 3 * hidden for d in range(k)]     # room to spare: the guard must stay
+    recv, pos, d_counts, status, ys = _fused_on_device(k, xs, routing, ws, experts, topk, caps, recv_offset)
+    assert int(status.item()) == 0
+    assert np.array_equal(d_counts.cpu().numpy(), counts)
+    for r in range(k):
+        assert np.array_equal(pos[r].cpu().numpy()[: tokens * topk], packs[r][2]), r
+    for d in range(k):
+        got = recv[d].host()
+        n = len(want_recv[d])
+        assert np.array_equal(got[:n], want_recv[d]), f"dispatch rank {d}"
+        assert np.all(got[n:] == 0xA5A5), f"rank {d}: written past its rows"
+        recv[d].check()
+    for r in range(k):
+        ys[r].check()
+        assert np.array_equal(ys[r].host().reshape(tokens, hidden), want_y[r]), f"combine rank {r}"
+
+
+def test_fused_dispatch_reports_rows_that_do_not_fit():
+    k, tokens, hidden, experts, topk = 4, 300, 64, 32, 4
+    routing = inputs.ep_routing(k, tokens, experts, topk, 1.1, seed_base=5300)
+    xs = [inputs.normal_bf16(tokens * hidden, 5900 + r).reshape(tokens, hidden) for r in range(k)]
+    ws = [np.ones(tokens * topk, np.float32) for _ in range(k)]
+    packs, counts, want_recv, _ = _oracle_round_trip(xs, routing, ws, experts, k, topk, hidden)
+    need = [int(counts[:, d].sum()) for d in range(k)]
+    caps = list(need)
+    caps[0] = need[0] - 5 * hidden                                      # rank 0 lacks room for five rows
+    recv, _, _, status, _ = _fused_on_device(k, xs, routing, ws, experts, topk, caps)
+    st = int(status.item())
+    assert st & 1 and st & 2                                            # dispatch and combine both saw it
+    for d in range(k):
+        recv[d].check()                                                 # nothing written outside a buffer
+        if d:
+            assert np.array_equal(recv[d].host(), want_recv[d])         # the other ranks are complete
+    assert np.array_equal(recv[0].host(), want_recv[0][: caps[0]])      # rank 0 holds the rows that fit
+
+
+def test_fused_zero_tokens():
+    k, hidden, experts = 4, 64, 16
+    ids = [torch.empty(0, dtype=torch.int32, device="cuda") for _ in range(k)]
+    xs = [torch.empty((0, hidden), dtype=torch.bfloat16, device="cuda") for _ in range(k)]
+    recv = [torch.empty(hidden, dtype=torch.bfloat16, device="cuda") for _ in range(k)]
+    counts = torch.full((k, k), 5, dtype=torch.int64, device="cuda")
+    status = torch.full((1,), 3, dtype=torch.int32, device="cuda")
+    ws = torch.empty(1, dtype=torch.int32, device="cuda")
+    hoc.ep_dispatch_fused(ids, xs, experts, recv, [hidden] * k, ids, counts, ws, status)
+    torch.cuda.synchronize()
+    assert counts.abs().sum().item() == 0 and int(status.item()) == 0
