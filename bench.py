@@ -1400,9 +1400,21 @@ def run_ep_fused_only(args, world, rank, local):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
+    ph = []
+    for _ in range(args.steps):   # the two phases apart, each between events
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record(stream)
+        hoc.ep_dispatch_fused(ids, xs, experts, recv, cap, pos, counts, wsp, status, stream=stream)
+        ev[1].record(stream)
+        hoc.ep_combine_fused(recv, cap, ids, pos, counts, gate, tokens, topk, h, experts, ys, status, stream=stream)
+        ev[2].record(stream)
+        torch.cuda.synchronize()
+        ph.append((ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])))
     if rank == 0:
         print(json.dumps({"metric": "EP dispatch + combine fused with the exchange (profiling case)", "unit": "ms",
                           "value": round(ms, 4), "steps": args.steps, "status": int(status.item()),
+                          "dispatch_ms": round(statistics.median(p[0] for p in ph), 4),
+                          "combine_ms": round(statistics.median(p[1] for p in ph), 4),
                           "config": {"k": k, "tokens": tokens, "hidden": h, "experts": experts, "topk": topk}}),
               flush=True)
 

@@ -23,10 +23,14 @@
 // of rank d's buffer, with rdispl[d][s] = sum of counts[s'][d] over s' < s and
 // sdispl[s][d] = sum of counts[s][d'] over d' < d (prefix sums in rank order,
 // the all-to-all's default displacements).
+#include <cstdlib>
+#include <cstring>
+
 #include <cuda_bf16.h>
 
 #include "hoc_internal.h"
 #include "hoc_ep.h"
+#include "ptx_async.cuh"
 
 namespace hoc {
 namespace {
@@ -502,8 +506,12 @@ __device__ __forceinline__ long long route_row(const EpRoute& R, const long long
 
 // Dispatch: every token row of every source, read once, stored to each of its
 // valid pairs' rows in the destination ranks' buffers.  Vector path: a work
-// item is (source, token, 1 KiB slice), a lane moves two 16-byte vectors of
-// the slice; byte path: a warp per (source, token).
+// item is (source, token, 2 KiB chunk of the row); a lane loads its
+// kDispVecs 16-byte vectors of the chunk up front, resolves the pairs'
+// destinations once, and stores the vectors to each.  Byte path: a warp per
+// (source, token).
+constexpr int kDispVecs = 4;                      // 16-byte vectors per lane per item
+constexpr int kDispChunk = 32 * kDispVecs * 16;   // bytes of a row per item
 __global__ void ep_dispatch_fused_kernel(const __grid_constant__ EpRoute R, int vec) {
   pdl_enter();
   __shared__ long long base[kMaxRanks * kMaxRanks];
@@ -513,42 +521,40 @@ __global__ void ep_dispatch_fused_kernel(const __grid_constant__ EpRoute R, int 
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
   const long long first = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int nv = hb / 16;
-  const int slices = vec ? (nv + kScatterSliceVecs - 1) / kScatterSliceVecs : 1;
-  const long long per_src = (long long)R.tokens * slices;
-  const long long items = per_src * R.k;
+  const int chunks = vec ? (hb + kDispChunk - 1) / kDispChunk : 1;
+  const long long rows = (long long)R.tokens * R.k;
+  const long long items = rows * chunks;
   for (long long it = first; it < items; it += warps) {
-    const int s = int(it / per_src);
-    const long long rem = it % per_src;
-    const int t = int(rem / slices);
+    const long long row_it = it / chunks;
+    const int c = int(it - row_it * chunks);
+    const int s = int(row_it / R.tokens), t = int(row_it - (long long)s * R.tokens);
     const char* src = R.x[s] + size_t(t) * hb;
-    uint4 a = make_uint4(0, 0, 0, 0), b = a;
-    int v0 = 0, v1 = 0;
-    bool h0 = false, h1 = false;
+    uint4 a[kDispVecs];
+    const int v0 = c * (kDispChunk / 16) + lane;
     if (vec) {
-      v0 = int(rem % slices) * kScatterSliceVecs + lane;
-      v1 = v0 + 32;
-      h0 = v0 < nv;
-      h1 = v1 < nv;
-      if (h0) a = __ldg(reinterpret_cast<const uint4*>(src) + v0);
-      if (h1) b = __ldg(reinterpret_cast<const uint4*>(src) + v1);
+#pragma unroll
+      for (int q = 0; q < kDispVecs; ++q)
+        if (v0 + 32 * q < nv) a[q] = __ldg(reinterpret_cast<const uint4*>(src) + v0 + 32 * q);
     }
     for (int j0 = 0; j0 < R.topk; j0 += 32) {
       const size_t pr = size_t(t) * R.topk + j0 + lane;
       const bool in = j0 + lane < R.topk;
       const int pl = in ? R.pos_of[s][pr] : -1;
       const int el = in ? R.ids[s][pr] : 0;
+      // each lane resolves its own pair's destination row once
+      long long myrow = -1;
+      if (pl >= 0) myrow = route_row(R, base, s, el / R.per_rank, pl, 1);
+      const int md = pl >= 0 ? el / R.per_rank : 0;
       const int nj = min(32, R.topk - j0);
       for (int j = 0; j < nj; ++j) {
-        const int pos = __shfl_sync(0xFFFFFFFFu, pl, j);
-        const int e = __shfl_sync(0xFFFFFFFFu, el, j);
-        if (pos < 0) continue;  // dropped pair: sent nowhere
-        const int d = e / R.per_rank;
-        const long long row = route_row(R, base, s, d, pos, 1);
-        if (row < 0) continue;
+        const long long row = __shfl_sync(0xFFFFFFFFu, myrow, j);
+        const int d = __shfl_sync(0xFFFFFFFFu, md, j);
+        if (row < 0) continue;  // dropped pair, or no room: sent nowhere
         char* dst = R.buf[d] + size_t(row) * hb;
         if (vec) {
-          if (h0) reinterpret_cast<uint4*>(dst)[v0] = a;
-          if (h1) reinterpret_cast<uint4*>(dst)[v1] = b;
+#pragma unroll
+          for (int q = 0; q < kDispVecs; ++q)
+            if (v0 + 32 * q < nv) reinterpret_cast<uint4*>(dst)[v0 + 32 * q] = a[q];
         } else {
           for (int i = lane; i < hb; i += 32) dst[i] = src[i];
         }
@@ -557,10 +563,150 @@ __global__ void ep_dispatch_fused_kernel(const __grid_constant__ EpRoute R, int 
   }
 }
 
+// Dispatch through the tensor-memory accelerator: a CTA of one warp streams
+// its share of the (source, token, piece) work items; lane 0 bulk-loads each
+// piece (a row, or a part of a long row) into a shared-memory stage, waits for
+// it on the stage's mbarrier and issues one bulk store per valid pair to the
+// destination row, the stores of one piece forming one bulk group; a stage is
+// refilled once the stores before the last have read it, so loads run up to
+// kBulkStages pieces ahead.  Every 32 items the warp resolves the next 32
+// items' destinations together (one lane per item).  Needs rows and buffers
+// aligned to 16 bytes and topk <= kBulkMaxTopk.  Every mbarrier wait is
+// bounded; on a timeout the kernel sets status bit 2, waits (bounded) for its
+// own loads and returns.
+constexpr int kBulkStages = 16;
+constexpr int kBulkBatch = 32;
+constexpr int kBulkMaxTopk = 16;
+constexpr uint32_t kBulkPiece = 4096;  // bytes per stage
+constexpr uint64_t kBulkWaitNs = 2000000000ull;
+
+__global__ void __launch_bounds__(32) ep_dispatch_bulk_kernel(const __grid_constant__ EpRoute R) {
+  using namespace ptx;
+  pdl_enter();
+  extern __shared__ __align__(128) unsigned char stage_mem[];  // kBulkStages x kBulkPiece
+  __shared__ __align__(8) uint64_t bar[kBulkStages];
+  __shared__ long long base[kMaxRanks * kMaxRanks];
+  __shared__ char* dst_tab[kBulkBatch][kBulkMaxTopk];
+  __shared__ uint32_t len_tab[kBulkBatch];
+  const int lane = threadIdx.x;
+  route_bases(R, base);
+  if (lane == 0) {
+    for (int st = 0; st < kBulkStages; ++st) mbar_init(&bar[st], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncwarp();
+  const uint32_t hb = uint32_t(R.hidden) * 2;
+  const uint32_t pieces = (hb + kBulkPiece - 1) / kBulkPiece;
+  const uint64_t items = uint64_t(R.k) * uint64_t(R.tokens) * pieces;
+  const uint64_t mine = items > blockIdx.x ? (items - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  // item i of this CTA: global item blockIdx.x + i * gridDim.x = (row, piece), row = s * tokens + t
+  auto locate = [&](uint64_t i, int& s, int& t, uint32_t& off, uint32_t& n) {
+    const uint64_t g = blockIdx.x + i * gridDim.x;
+    const uint64_t row = g / pieces;
+    off = uint32_t(g - row * pieces) * kBulkPiece;
+    n = hb - off < kBulkPiece ? hb - off : kBulkPiece;
+    s = int(row / uint64_t(R.tokens));
+    t = int(row - uint64_t(s) * uint64_t(R.tokens));
+  };
+  uint64_t nload = 0, nstore = 0;
+  auto issue_load = [&]() {
+    int s, t;
+    uint32_t off, n;
+    locate(nload, s, t, off, n);
+    uint64_t* b = &bar[nload % kBulkStages];
+    mbar_arrive_expect_tx(b, n);
+    bulk_load(stage_mem + size_t(nload % kBulkStages) * kBulkPiece, R.x[s] + size_t(t) * hb + off, n, b);
+    ++nload;
+  };
+  if (lane == 0)
+    while (nload < mine && nload < uint64_t(kBulkStages)) issue_load();
+  bool failed = false;
+  for (uint64_t b0 = 0; b0 < mine && !failed; b0 += kBulkBatch) {
+    const uint64_t i = b0 + lane;
+    if (i < mine) {  // this lane's item: the destination of each of its pairs
+      int s, t;
+      uint32_t off, n;
+      locate(i, s, t, off, n);
+      len_tab[lane] = n;
+      for (int j = 0; j < R.topk; ++j) {
+        const size_t pr = size_t(t) * R.topk + j;
+        const int p = R.pos_of[s][pr];
+        char* d = nullptr;
+        if (p >= 0) {
+          const int rk = R.ids[s][pr] / R.per_rank;
+          const long long row = route_row(R, base, s, rk, p, 1);
+          if (row >= 0) d = R.buf[rk] + size_t(row) * hb + off;
+        }
+        dst_tab[lane][j] = d;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      const uint64_t b1 = mine < b0 + kBulkBatch ? mine : b0 + kBulkBatch;
+      for (uint64_t it = b0; it < b1; ++it) {
+        const int st = int(it % kBulkStages);
+        if (!mbar_wait_bounded(&bar[st], uint32_t(it / kBulkStages) & 1u, global_ns() + kBulkWaitNs)) {
+          failed = true;
+          break;
+        }
+        const unsigned char* piece = stage_mem + size_t(st) * kBulkPiece;
+        const int slot = int(it - b0);
+        for (int j = 0; j < R.topk; ++j)
+          if (dst_tab[slot][j]) bulk_store(dst_tab[slot][j], piece, len_tab[slot]);
+        bulk_commit();
+        ++nstore;
+        if (nstore >= 2) {  // the stage of the item before the last is read: refill it
+          bulk_wait_read_1();
+          if (nload < mine) issue_load();
+        }
+      }
+    }
+    failed = __shfl_sync(0xFFFFFFFFu, failed, 0);
+    __syncwarp();
+  }
+  if (lane == 0) {
+    if (failed) {
+      atomicOr(R.status, 4);
+      const uint64_t deadline = global_ns() + kBulkWaitNs;
+      for (uint64_t b = nstore; b < nload; ++b)
+        if (!mbar_wait_bounded(&bar[b % kBulkStages], uint32_t(b / kBulkStages) & 1u, deadline)) break;
+    }
+    bulk_wait_all();
+  }
+}
+
 // Combine, reading every row straight from the expert rank's buffer; the same
-// fold as the packed-order combine.  TK > 0: vector path with all TK row loads
-// of a lane issued before the ordered fold (work item = (source, token, 512 B
-// slice)); TK == 0: vector path for any topk, one load at a time.
+// fold as the packed-order combine.  A work item is (source, token, 1 KiB
+// chunk of the row): the token's pairs are resolved once (lanes < topk load
+// their pair, then broadcast source row and weight), and a lane folds two
+// 16-byte vectors per row.  TK > 0: all TK x 2 row loads of a lane are issued
+// before the ordered fold; TK == 0: any topk, one row at a time.
+constexpr int kCombVecs = 2;                      // 16-byte vectors per lane per item
+constexpr int kCombChunk = 32 * kCombVecs;        // vectors of a row per item
+
+__device__ __forceinline__ void fold_bf16x8(float* acc, const uint4& x, float w, bool first) {
+  const uint32_t q[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = __fmul_rn(w, __uint_as_float(q[i] << 16));
+    const float hi = __fmul_rn(w, __uint_as_float(q[i] & 0xFFFF0000u));
+    acc[2 * i] = first ? lo : __fadd_rn(acc[2 * i], lo);
+    acc[2 * i + 1] = first ? hi : __fadd_rn(acc[2 * i + 1], hi);
+  }
+}
+
+__device__ __forceinline__ uint4 narrow_bf16x8(const float* acc, bool any) {
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = any ? acc[2 * i] : 0.f, hi = any ? acc[2 * i + 1] : 0.f;
+    o[i] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+           (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 template <int TK>
 __global__ void ep_combine_fused_vec_kernel(const __grid_constant__ EpRoute R) {
   pdl_enter();
@@ -568,52 +714,50 @@ __global__ void ep_combine_fused_vec_kernel(const __grid_constant__ EpRoute R) {
   route_bases(R, base);
   const int lane = threadIdx.x & 31;
   const int hv = R.hidden / 8;
-  const int slices = (hv + 31) / 32;
-  const long long per_src = (long long)R.tokens * slices;
-  const long long items = per_src * R.k;
+  const int chunks = (hv + kCombChunk - 1) / kCombChunk;
+  const long long rows = (long long)R.tokens * R.k;
+  const long long items = rows * chunks;
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
   for (long long it = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items; it += warps) {
-    const int s = int(it / per_src);
-    const long long rem = it % per_src;
-    const int t = int(rem / slices);
-    const int v = int(rem % slices) * 32 + lane;
-    float acc[8];
+    const long long row_it = it / chunks;
+    const int c = int(it - row_it * chunks);
+    const int s = int(row_it / R.tokens), t = int(row_it - (long long)s * R.tokens);
+    const int v0 = c * kCombChunk + lane;
+    float acc[kCombVecs][8];
     bool any = false;
     if constexpr (TK > 0) {
+      // lane j < TK resolves pair j: its source row (or none) and weight
       const size_t pr = size_t(t) * TK + lane;
-      const int pl = lane < TK ? R.pos_of[s][pr] : -1;
-      const int el = lane < TK ? R.ids[s][pr] : 0;
-      const float wl = lane < TK ? R.w[s][pr] : 0.f;
+      const char* mine = nullptr;
+      float wl = 0.f;
+      if (lane < TK) {
+        const int p = R.pos_of[s][pr];
+        wl = R.w[s][pr];
+        if (p >= 0) {
+          const int d = R.ids[s][pr] / R.per_rank;
+          const long long row = route_row(R, base, s, d, p, 2);
+          if (row >= 0) mine = R.buf[d] + size_t(row) * R.hidden * 2;
+        }
+      }
       const char* src[TK];
       float wj[TK];
 #pragma unroll
       for (int j = 0; j < TK; ++j) {
-        const int p = __shfl_sync(0xFFFFFFFFu, pl, j);
-        const int e = __shfl_sync(0xFFFFFFFFu, el, j);
+        src[j] = reinterpret_cast<const char*>(__shfl_sync(0xFFFFFFFFu, reinterpret_cast<uintptr_t>(mine), j));
         wj[j] = __shfl_sync(0xFFFFFFFFu, wl, j);
-        src[j] = nullptr;
-        if (p >= 0) {
-          const int d = e / R.per_rank;
-          const long long row = route_row(R, base, s, d, p, 2);
-          if (row >= 0) src[j] = R.buf[d] + size_t(row) * R.hidden * 2;
-        }
       }
-      if (v >= hv) continue;
-      uint4 x[TK];
+      uint4 x[TK][kCombVecs];
 #pragma unroll
       for (int j = 0; j < TK; ++j)
-        x[j] = src[j] ? __ldg(reinterpret_cast<const uint4*>(src[j]) + v) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int q = 0; q < kCombVecs; ++q)
+          x[j][q] = src[j] && v0 + 32 * q < hv ? __ldg(reinterpret_cast<const uint4*>(src[j]) + v0 + 32 * q)
+                                               : make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int j = 0; j < TK; ++j) {
         if (!src[j]) continue;
-        const uint32_t q[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float lo = __fmul_rn(wj[j], __uint_as_float(q[i] << 16));
-          const float hi = __fmul_rn(wj[j], __uint_as_float(q[i] & 0xFFFF0000u));
-          acc[2 * i] = any ? __fadd_rn(acc[2 * i], lo) : lo;
-          acc[2 * i + 1] = any ? __fadd_rn(acc[2 * i + 1], hi) : hi;
-        }
+        for (int q = 0; q < kCombVecs; ++q) fold_bf16x8(acc[q], x[j][q], wj[j], !any);
         any = true;
       }
     } else {
@@ -623,29 +767,142 @@ __global__ void ep_combine_fused_vec_kernel(const __grid_constant__ EpRoute R) {
         if (p < 0) continue;
         const int d = R.ids[s][pr] / R.per_rank;
         const long long row = route_row(R, base, s, d, p, 2);
-        if (row < 0 || v >= hv) continue;
-        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(R.buf[d] + size_t(row) * R.hidden * 2) + v);
+        if (row < 0) continue;
+        const uint4* src = reinterpret_cast<const uint4*>(R.buf[d] + size_t(row) * R.hidden * 2);
         const float wj = R.w[s][pr];
-        const uint32_t q[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float lo = __fmul_rn(wj, __uint_as_float(q[i] << 16));
-          const float hi = __fmul_rn(wj, __uint_as_float(q[i] & 0xFFFF0000u));
-          acc[2 * i] = any ? __fadd_rn(acc[2 * i], lo) : lo;
-          acc[2 * i + 1] = any ? __fadd_rn(acc[2 * i + 1], hi) : hi;
-        }
+        for (int q = 0; q < kCombVecs; ++q)
+          if (v0 + 32 * q < hv) fold_bf16x8(acc[q], __ldg(src + v0 + 32 * q), wj, !any);
         any = true;
       }
-      if (v >= hv) continue;
     }
-    uint32_t o[4];
+    uint4* y = reinterpret_cast<uint4*>(R.y[s] + size_t(t) * R.hidden * 2);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float lo = any ? acc[2 * i] : 0.f, hi = any ? acc[2 * i + 1] : 0.f;
-      o[i] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
-             (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+    for (int q = 0; q < kCombVecs; ++q)
+      if (v0 + 32 * q < hv) y[v0 + 32 * q] = narrow_bf16x8(acc[q], any);
+  }
+}
+
+// Combine fed by the tensor-memory accelerator.  Each warp owns two
+// shared-memory stages of topk x 1 KiB; for its work item (source,
+// token, 1 KiB chunk of the row) lane 0 bulk-loads the chunk of every valid
+// pair's row into a stage, completing on the stage's mbarrier, and the warp
+// folds from shared memory in slot order while the next item's loads are in
+// flight.  So the bytes in flight do not take registers: 2 x topk KiB per
+// warp.  Needs 16-byte-aligned rows, hidden % 8 == 0 and topk <= kBulkTopk.
+// Waits are bounded: on a timeout the warp sets status bit 2, waits (bounded)
+// for its own loads and stops.
+constexpr int kBulkTopk = 8;
+constexpr int kCombWarps = 4;                 // warps per CTA
+// Bytes of a row per item.  Measured at the EP workload's shape (4 KiB rows,
+// top-6): 1 KiB slices 0.187 ms, 2 KiB 0.216 ms, whole rows 0.289 ms -- the
+// number of warps folding per SM matters more than the length of each read.
+constexpr uint32_t kCombSlice = 1024;
+
+__global__ void __launch_bounds__(32 * kCombWarps) ep_combine_bulk_kernel(const __grid_constant__ EpRoute R,
+                                                                         uint32_t slice) {
+  using namespace ptx;
+  pdl_enter();
+  extern __shared__ __align__(128) unsigned char comb_mem[];  // [warps][2 stages][topk][slice]
+  __shared__ __align__(8) uint64_t bar[kCombWarps][2];
+  __shared__ long long base[kMaxRanks * kMaxRanks];
+  route_bases(R, base);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    mbar_init(&bar[warp][0], 1);
+    mbar_init(&bar[warp][1], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncwarp();
+  const uint32_t stage_bytes = uint32_t(R.topk) * slice;
+  unsigned char* stages = comb_mem + size_t(warp) * 2 * stage_bytes;
+  const uint32_t hb = uint32_t(R.hidden) * 2;
+  const uint32_t chunks = (hb + slice - 1) / slice;
+  const uint64_t items = uint64_t(R.k) * uint64_t(R.tokens) * chunks;
+  const uint64_t warps = uint64_t(gridDim.x) * kCombWarps;
+  const uint64_t first = uint64_t(blockIdx.x) * kCombWarps + warp;
+  // what an item needs after its loads land: where it is and its pairs' weights
+  struct Item {
+    int s, t;
+    uint32_t off, n;
+    unsigned valid;  // bit j: pair j has a row in the stage
+    float w;         // lane j < topk: weight of pair j
+  };
+  // Resolve item `it` (all lanes) and, on lane 0, issue its loads into stage `st`.
+  auto start = [&](uint64_t it, int st, Item& I) {
+    const uint64_t row_it = it / chunks;
+    I.off = uint32_t(it - row_it * chunks) * slice;
+    I.n = hb - I.off < slice ? hb - I.off : slice;
+    I.s = int(row_it / uint64_t(R.tokens));
+    I.t = int(row_it - uint64_t(I.s) * uint64_t(R.tokens));
+    const char* src = nullptr;
+    I.w = 0.f;
+    if (lane < R.topk) {
+      const size_t pr = size_t(I.t) * R.topk + lane;
+      const int p = R.pos_of[I.s][pr];
+      I.w = R.w[I.s][pr];
+      if (p >= 0) {
+        const int d = R.ids[I.s][pr] / R.per_rank;
+        const long long row = route_row(R, base, I.s, d, p, 2);
+        if (row >= 0) src = R.buf[d] + size_t(row) * hb + I.off;
+      }
     }
-    reinterpret_cast<uint4*>(R.y[s] + size_t(t) * R.hidden * 2)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+    I.valid = __ballot_sync(0xFFFFFFFFu, src != nullptr);
+    uint64_t* b = &bar[warp][st];
+    if (lane == 0) mbar_arrive_expect_tx(b, uint32_t(__popc(I.valid)) * I.n);
+    __syncwarp();
+    if (src) bulk_load(stages + size_t(st) * stage_bytes + size_t(lane) * slice, src, I.n, b);
+  };
+  uint64_t k_items = first < items ? (items - first + warps - 1) / warps : 0;
+  Item cur{}, nxt{};
+  bool failed = false;
+  uint64_t issued = 0, done = 0;
+  if (k_items) {
+    start(first, 0, cur);
+    issued = 1;
+  }
+  for (uint64_t i = 0; i < k_items && !failed; ++i) {
+    const int st = int(i & 1);
+    if (i + 1 < k_items) {  // the next item's loads go out before this one is folded
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // earlier reads of that stage come first
+      start(first + (i + 1) * warps, st ^ 1, nxt);
+      ++issued;
+    }
+    // every lane waits for the stage itself before reading what the bulk loads wrote
+    const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bar[warp][st], uint32_t(i >> 1) & 1u,
+                                                              global_ns() + kBulkWaitNs));
+    if (!ok) {
+      failed = true;
+      break;
+    }
+    ++done;
+    float wj[kBulkTopk];
+#pragma unroll
+    for (int j = 0; j < kBulkTopk; ++j) wj[j] = __shfl_sync(0xFFFFFFFFu, cur.w, j);
+    const unsigned char* stage = stages + size_t(st) * stage_bytes;
+    const uint32_t nvec = cur.n / 16;
+    uint4* y = reinterpret_cast<uint4*>(R.y[cur.s] + size_t(cur.t) * hb + cur.off);
+    for (uint32_t v = lane; v < nvec; v += 32) {
+      float acc[8];
+      bool any = false;
+#pragma unroll
+      for (int j = 0; j < kBulkTopk; ++j) {
+        if (j >= R.topk || !(cur.valid >> j & 1u)) continue;
+        const uint4 x = *reinterpret_cast<const uint4*>(stage + size_t(j) * slice + size_t(v) * 16);
+        fold_bf16x8(acc, x, wj[j], !any);
+        any = true;
+      }
+      y[v] = narrow_bf16x8(acc, any);
+    }
+    __syncwarp();
+    cur = nxt;
+  }
+  if (failed && lane == 0) {
+    atomicOr(R.status, 4);
+    const uint64_t deadline = global_ns() + kBulkWaitNs;
+    for (uint64_t b = done; b < issued; ++b)  // the loads still in flight: bounded again
+      if (!mbar_wait_bounded(&bar[warp][b & 1], uint32_t(b >> 1) & 1u, deadline)) break;
   }
 }
 
@@ -797,6 +1054,8 @@ cudaError_t ep_preload() {
                        reinterpret_cast<const void*>(kCombineIlp[4]), reinterpret_cast<const void*>(kCombineIlp[5]),
                        reinterpret_cast<const void*>(kCombineIlp[6]), reinterpret_cast<const void*>(kCombineIlp[7]),
                        reinterpret_cast<const void*>(&ep_dispatch_fused_kernel),
+                       reinterpret_cast<const void*>(&ep_dispatch_bulk_kernel),
+                       reinterpret_cast<const void*>(&ep_combine_bulk_kernel),
                        reinterpret_cast<const void*>(&ep_combine_fused_kernel),
                        reinterpret_cast<const void*>(kCombineFused[0]), reinterpret_cast<const void*>(kCombineFused[1]),
                        reinterpret_cast<const void*>(kCombineFused[2]), reinterpret_cast<const void*>(kCombineFused[3]),
@@ -942,11 +1201,30 @@ extern "C" hocResult_t hoc_ep_dispatch_fused(int nranks, const int32_t* const* e
   R.hidden = hidden;
   R.per_rank = experts / nranks;
   const int hb = hidden * 2;
-  const long long warps = (long long)nranks * tokens *
-                          (vec ? (hb / 16 + kScatterSliceVecs - 1) / kScatterSliceVecs : 1);
-  const void* fn = reinterpret_cast<const void*>(&ep_dispatch_fused_kernel);
-  if (launch_pdl(ep_dispatch_fused_kernel, dim3(persistent_grid(fn, (warps + 7) / 8)), 256, 0, s, R, int(vec)) !=
-      cudaSuccess) {
+  // Row scatter: per-thread vector copies; with HOC_EP_DISPATCH=bulk (rows and
+  // buffers aligned, topk <= 16) bulk copies through shared memory instead --
+  // measured equal on GB300 at the EP workload's shape, kept as the TMA engine.
+  const char* eng = getenv("HOC_EP_DISPATCH");
+  const bool bulk = vec && topk <= kBulkMaxTopk && eng && !strcmp(eng, "bulk");
+  cudaError_t e;
+  if (bulk) {
+    const void* fn = reinterpret_cast<const void*>(&ep_dispatch_bulk_kernel);
+    const size_t smem = size_t(kBulkStages) * kBulkPiece;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    int dev = 0, sms = 1, occ = 0;
+    if (e == cudaSuccess) e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, 32, smem);
+    const long long items = (long long)nranks * tokens * ((hb + kBulkPiece - 1) / kBulkPiece);
+    const long long cap = (long long)sms * (occ > 0 ? occ : 1);
+    if (e == cudaSuccess)
+      e = launch_pdl(ep_dispatch_bulk_kernel, dim3(unsigned(items < cap ? items : cap)), 32, smem, s, R);
+  } else {
+    const long long warps = (long long)nranks * tokens * (vec ? (hb + kDispChunk - 1) / kDispChunk : 1);
+    const void* fn = reinterpret_cast<const void*>(&ep_dispatch_fused_kernel);
+    e = launch_pdl(ep_dispatch_fused_kernel, dim3(persistent_grid(fn, (warps + 7) / 8)), 256, 0, s, R, int(vec));
+  }
+  if (e != cudaSuccess) {
     set_error_detail("hoc_ep_dispatch_fused: launching the row scatter failed");
     return HOC_ERR_CUDA;
   }
@@ -991,9 +1269,27 @@ extern "C" hocResult_t hoc_ep_combine_fused(int nranks, const void* const* rows,
   R.per_rank = experts / nranks;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (vec) {
+  // Rows through shared memory by TMA bulk copies where shapes allow (the
+  // default), else (or with HOC_EP_COMBINE=lsu) per-thread vector loads.
+  const char* eng = getenv("HOC_EP_COMBINE");
+  if (vec && topk <= kBulkTopk && !(eng && !strcmp(eng, "lsu"))) {
+    const void* fn = reinterpret_cast<const void*>(&ep_combine_bulk_kernel);
+    const uint32_t slice = kCombSlice;
+    const size_t smem = size_t(kCombWarps) * 2 * size_t(topk) * slice;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    int dev = 0, sms = 1, occ = 0;
+    if (e == cudaSuccess) e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, 32 * kCombWarps, smem);
+    const long long items = (long long)nranks * tokens * ((size_t(hidden) * 2 + slice - 1) / slice);
+    const long long want = (items + kCombWarps - 1) / kCombWarps;
+    const long long cap = (long long)sms * (occ > 0 ? occ : 1);
+    if (e == cudaSuccess)
+      e = launch_pdl(ep_combine_bulk_kernel, dim3(unsigned(want < cap ? want : cap)), 32 * kCombWarps, smem, s, R,
+                     slice);
+  } else if (vec) {
     const CombineFusedFn fn = kCombineFused[topk <= kCombineTopk ? topk : 0];
-    const long long items = (long long)nranks * tokens * ((hidden / 8 + 31) / 32);  // one warp per item
+    const long long items = (long long)nranks * tokens * ((hidden / 8 + kCombChunk - 1) / kCombChunk);  // warps
     e = launch_pdl(fn, dim3(persistent_grid(reinterpret_cast<const void*>(fn), (items + 7) / 8)), 256, 0, s, R);
   } else {
     const void* fn = reinterpret_cast<const void*>(&ep_combine_fused_kernel);

@@ -75,7 +75,12 @@ hocResult_t hoc_ep_combine(const void* rows, const int32_t* pos_of, const float*
  * workspace: device int32 scratch of at least nranks * hoc_ep_pack_workspace()
  * entries (else HOC_ERR_INVALID_ARG, nothing queued).  Pairs with an expert id
  * outside [0, experts) are dropped; experts is a multiple of nranks.  Stream-
- * ordered; the host does not wait. */
+ * ordered; the host does not wait.  Each token row is read once and stored
+ * to each of its pairs' rows by per-thread 16-byte vector copies (rows and
+ * buffers aligned to 16 bytes; byte copies otherwise).  HOC_EP_DISPATCH=bulk
+ * selects TMA bulk copies through shared memory instead (one bulk load per
+ * row, one bulk store per pair; topk <= 16), equally fast on GB300; bit 2 of
+ * *status is set if one of that kernel's bounded waits gave up. */
 hocResult_t hoc_ep_dispatch_fused(int nranks, const int32_t* const* expert_ids, const void* const* x, int tokens,
                                   int topk, int hidden, int experts, void* const* recv, const size_t* recv_capacity,
                                   int32_t* const* pos_of, uint64_t* counts, int32_t* workspace,
@@ -89,7 +94,10 @@ hocResult_t hoc_ep_dispatch_fused(int nranks, const int32_t* const* expert_ids, 
  * fold is hoc_ep_combine's: y[s][t] = bf16 of the binary32 sum, in slot order,
  * of fp32(weight * row) over the token's valid pairs (+0 when none).  Bit 1 of
  * *status (not cleared here) is set if a row lies outside its buffer (it then
- * adds nothing). */
+ * adds nothing).  With hidden % 8 == 0, 16-byte-aligned rows and outputs and
+ * topk <= 8, each warp's rows arrive by TMA bulk copies into shared memory
+ * (two stages of topk x 1 KiB per warp; bit 2 of *status if a bounded wait
+ * gave up); HOC_EP_COMBINE=lsu selects per-thread vector loads instead. */
 hocResult_t hoc_ep_combine_fused(int nranks, const void* const* rows, const size_t* rows_capacity,
                                  const int32_t* const* expert_ids, const int32_t* const* pos_of,
                                  const uint64_t* counts, const float* const* weights, int tokens, int topk,

@@ -197,7 +197,12 @@ def _fused_on_device(k, xs, routing, ws, experts, topk, caps, recv_offset=0, y_o
     (8, 777, 64, True, 64, 6, 1),       # receive buffers 2 bytes off alignment: byte dispatch, scalar combine
     (1, 300, 64, True, 8, 3, 0),        # one rank: everything stays home
 ])
-def test_fused_dispatch_and_combine_match_oracle(k, tokens, hidden, drop, experts, topk, recv_offset):
+@pytest.mark.parametrize("engines", [None, ("bulk", "lsu")])
+def test_fused_dispatch_and_combine_match_oracle(k, tokens, hidden, drop, experts, topk, recv_offset, engines,
+                                                 monkeypatch):
+    if engines:   # the other engines: TMA bulk-copy dispatch, vector-load combine
+        monkeypatch.setenv("HOC_EP_DISPATCH", engines[0])
+        monkeypatch.setenv("HOC_EP_COMBINE", engines[1])
     routing = [r.copy() for r in inputs.ep_routing(k, tokens, experts, topk, 1.1, seed_base=5200 + k)]
     if drop:
         routing[0][3 % tokens, 0] = -5
