@@ -926,9 +926,8 @@ def leg_sweeps(sms):
 def leg_ce_allreduce_timeline(send, recv, k, local, stream, per_rank, peak):
     """When each chunk of the copy-engine allreduce is reduced and moved (the per-step timeline).
 
-    One call with profiling on (events around every step; no graph), after a
-    few unprofiled ones, queued behind a 5 ms spin kernel so that the host has
-    issued all of it before the GPU starts.  Per chunk: the reduce kernel's start and end on the
+    One call with profiling on (events around every step), captured into a
+    CUDA graph and replayed, after a few unprofiled calls.  Per chunk: the reduce kernel's start and end on the
     caller's stream, and the first start and last end of that chunk's copies
     over the copy queues.  Beside it, what the schedule's bytes cost at the
     measured copy rate: (3k - 1) S with no L2 reuse, 2kS if every all-gather
@@ -944,12 +943,25 @@ def leg_ce_allreduce_timeline(send, recv, k, local, stream, per_rank, peak):
             for _ in range(3):
                 c.allreduce(send, recv, stream=stream)
             ms = time_allreduce(c, send, recv, stream, 5)
+            # The profiled call is captured into a CUDA graph (the library issues into the caller's
+            # capture, the step events become graph nodes) and replayed: the same graph execution as
+            # the library's own cached graphs, so the events do not change how the copies run.
             c.profile_enable(True)
-            gpu_spin(stream, 5.0)          # the host issues every step while the GPU spins: the timeline is the GPU's
-            c.allreduce(send, recv, stream=stream)
-            tl = c.profile_timeline()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                c.allreduce(send, recv, stream=stream)
             c.profile_enable(False)
-            torch.cuda.synchronize()
+            runs = []
+            for _ in range(4):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    e0.record(stream)
+                    graph.replay()
+                    e1.record(stream)
+                torch.cuda.synchronize()
+                runs.append(e0.elapsed_time(e1))
+            tl = c.profile_timeline()         # the events of the last replay
+            del graph
         chunks = sorted({t["stage"] for t in tl})
         rows = []
         for q in chunks:
@@ -962,8 +974,8 @@ def leg_ce_allreduce_timeline(send, recv, k, local, stream, per_rank, peak):
         end = max(t["end_ms"] for t in tl)
         red_busy = sum(t["end_ms"] - t["start_ms"] for t in tl if t["kind"] == "reduce")
         out[f"depth_{depth or 'unbounded'}"] = {
-            "ms_unprofiled": round(ms, 4), "ms_profiled": round(end, 4), "reduce_busy_ms": round(red_busy, 4),
-            "chunks": rows}
+            "ms_unprofiled": round(ms, 4), "ms_profiled_graph_replay": round(statistics.median(runs[1:]), 4),
+            "timeline_end_ms": round(end, 4), "reduce_busy_ms": round(red_busy, 4), "chunks": rows}
     S = per_rank
     out["bytes_at_measured_copy_rate_ms"] = {
         "3k-1_S_no_l2_reuse": round((3 * k - 1) * S / (peak * 1e9) * 1e3, 4),
