@@ -696,15 +696,24 @@ def leg_expert_dispatch(peak):
     pback = [torch.empty(n * h, dtype=torch.bfloat16, device="cuda") for _ in range(k)]
     ys = [torch.empty((tokens, h), dtype=torch.bfloat16, device="cuda") for _ in range(k)]
 
+    ids_flat = [t.view(-1) for t in ids]
+    wsp_all = torch.empty(k * hoc.ep_pack_workspace(tokens, topk, experts), dtype=torch.int32, device="cuda")
+    st_all = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def pack_all():    # every rank's pack in one set of launches
+        hoc.ep_pack_all(ids_flat, xs, experts, [t.view(-1) for t in psend], [n * h] * k, pos, d_counts, wsp_all,
+                        st_all, stream=s)
+
+    def combine_all():
+        hoc.ep_combine_all(pback, [n * h] * k, pos, gate, tokens, topk, h, ys, st_all, stream=s)
+
     def device_round_trip():
         with hoc.Comm(k, torch.cuda.current_device()) as c:
             def round_trip():
-                for r in range(k):
-                    hoc.ep_pack(ids[r], xs[r], experts, k, psend[r], perm[r], pos[r], d_counts[r], wsp[r], stream=s)
+                pack_all()
                 c.alltoall_device_counts([t.view(-1) for t in psend], precv, d_counts, cap, hoc.BFLOAT16, stream=s)
                 c.alltoall_device_counts(precv, pback, d_counts, [n * h] * k, hoc.BFLOAT16, stream=s, transpose=True)
-                for r in range(k):
-                    hoc.ep_combine(pback[r], pos[r], gate[r], tokens, topk, h, ys[r], stream=s)
+                combine_all()
             round_trip()
             c.wait(s, timeout_ms=60000)
             host_us = []
@@ -720,23 +729,37 @@ def leg_expert_dispatch(peak):
             # one more round with an event between its phases (all on stream s)
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
             ev[0].record(s)
-            for r in range(k):
-                hoc.ep_pack(ids[r], xs[r], experts, k, psend[r], perm[r], pos[r], d_counts[r], wsp[r], stream=s)
+            pack_all()
             ev[1].record(s)
             c.alltoall_device_counts([t.view(-1) for t in psend], precv, d_counts, cap, hoc.BFLOAT16, stream=s)
             ev[2].record(s)
             c.alltoall_device_counts(precv, pback, d_counts, [n * h] * k, hoc.BFLOAT16, stream=s, transpose=True)
             ev[3].record(s)
+            combine_all()
+            ev[4].record(s)
+            # the same pack and combine rank by rank (one set of launches per rank), for comparison
+            ev2 = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            ev2[0].record(s)
+            for r in range(k):
+                hoc.ep_pack(ids[r], xs[r], experts, k, psend[r], perm[r], pos[r], d_counts[r], wsp[r], stream=s)
+            ev2[1].record(s)
+            c.alltoall_device_counts([t.view(-1) for t in psend], precv, d_counts, cap, hoc.BFLOAT16, stream=s)
+            c.alltoall_device_counts(precv, pback, d_counts, [n * h] * k, hoc.BFLOAT16, stream=s, transpose=True)
+            ev2[2].record(s)
             for r in range(k):
                 hoc.ep_combine(pback[r], pos[r], gate[r], tokens, topk, h, ys[r], stream=s)
-            ev[4].record(s)
+            ev2[3].record(s)
             c.wait(s, timeout_ms=60000)
             phases = {name: round(ev[i].elapsed_time(ev[i + 1]), 4) for i, name in
                       enumerate(("pack_ms", "dispatch_ms", "combine_exchange_ms", "combine_kernel_ms"))}
+            per_rank = {"pack_ms": round(ev2[0].elapsed_time(ev2[1]), 4),
+                        "combine_kernel_ms": round(ev2[2].elapsed_time(ev2[3]), 4)}
             st = c.proxy_status()
         return {
             "ms": round(ms, 4), "host_issue_us": round(statistics.median(host_us), 1), "phases": phases,
-            "steps": "pack kernels -> dispatch (device counts, host proxy) -> combine exchange -> weighted combine kernel",
+            "pack_and_combine_rank_by_rank": per_rank, "status": int(st_all.item()),
+            "steps": "pack of every rank (one set of launches) -> dispatch (device counts, host proxy, copy engines) "
+                     "-> combine exchange (copy engines) -> weighted combine of every rank",
             "proxy_tasks_completed": st["completed"], "proxy_tasks_released_on_error": st["released_on_error"]}
 
     try:

@@ -23,6 +23,7 @@
 // of rank d's buffer, with rdispl[d][s] = sum of counts[s'][d] over s' < s and
 // sdispl[s][d] = sum of counts[s][d'] over d' < d (prefix sums in rank order,
 // the all-to-all's default displacements).
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 
@@ -472,12 +473,13 @@ struct EpRoute {
   const unsigned long long* counts;        // [k][k] element counts, row = source
   int32_t* status;                  // bit 0: a dispatched row did not fit; bit 1: a combine row out of range
   int k, tokens, topk, hidden, per_rank;
+  int packed;  // 1: each source's own buffer buf[s], rows in its packed order (no exchange to fuse)
 };
 
 // base[s * k + d] = rdispl[d][s] - sdispl[s][d] in rows: packed row i of source
 // s bound for rank d goes to row base[s * k + d] + i of rank d's buffer.
 __device__ __forceinline__ void route_bases(const EpRoute& R, long long* base) {
-  for (int c = threadIdx.x; c < R.k * R.k; c += blockDim.x) {
+  for (int c = threadIdx.x; !R.packed && c < R.k * R.k; c += blockDim.x) {
     const int s = c / R.k, d = c % R.k;
     unsigned long long rd = 0, sd = 0;
     for (int a = 0; a < s; ++a) rd += R.counts[a * R.k + d];
@@ -487,16 +489,22 @@ __device__ __forceinline__ void route_bases(const EpRoute& R, long long* base) {
   __syncthreads();
 }
 
-// Row of rank d's buffer that packed row `pos` (bound for rank d) of source s
-// occupies, or -1 (and the status bit `bit`) when it lies outside the buffer
-// or d is no rank (inputs that disagree with the dispatch that made them).
-__device__ __forceinline__ long long route_row(const EpRoute& R, const long long* base, int s, int d, int pos,
-                                               int bit) {
+// Expert of pair `pr` of source s (routing only: packed mode reads no ids).
+__device__ __forceinline__ int pair_expert(const EpRoute& R, int s, size_t pr) { return R.packed ? 0 : R.ids[s][pr]; }
+
+// Where packed row `pos` of source s, a pair with expert e, lives: buffer *b
+// (the destination rank e / per_rank, or s itself in packed mode) and the row
+// returned; -1 (and the status bit `bit`) when it lies outside that buffer or
+// e names no rank (inputs that disagree with the dispatch that made them).
+__device__ __forceinline__ long long route_row(const EpRoute& R, const long long* base, int s, int e, int pos,
+                                               int bit, int* b) {
+  const int d = R.packed ? s : e / R.per_rank;
+  *b = d;
   if (unsigned(d) >= unsigned(R.k)) {
     atomicOr(R.status, bit);
     return -1;
   }
-  const long long row = base[s * R.k + d] + pos;
+  const long long row = R.packed ? (long long)pos : base[s * R.k + d] + pos;
   if (row < 0 || (unsigned long long)row >= R.cap_rows[d]) {
     atomicOr(R.status, bit);
     return -1;
@@ -540,11 +548,11 @@ __global__ void ep_dispatch_fused_kernel(const __grid_constant__ EpRoute R, int 
       const size_t pr = size_t(t) * R.topk + j0 + lane;
       const bool in = j0 + lane < R.topk;
       const int pl = in ? R.pos_of[s][pr] : -1;
-      const int el = in ? R.ids[s][pr] : 0;
+      const int el = in ? pair_expert(R, s, pr) : 0;
       // each lane resolves its own pair's destination row once
       long long myrow = -1;
-      if (pl >= 0) myrow = route_row(R, base, s, el / R.per_rank, pl, 1);
-      const int md = pl >= 0 ? el / R.per_rank : 0;
+      int md = 0;
+      if (pl >= 0) myrow = route_row(R, base, s, el, pl, 1, &md);
       const int nj = min(32, R.topk - j0);
       for (int j = 0; j < nj; ++j) {
         const long long row = __shfl_sync(0xFFFFFFFFu, myrow, j);
@@ -634,8 +642,8 @@ __global__ void __launch_bounds__(32) ep_dispatch_bulk_kernel(const __grid_const
         const int p = R.pos_of[s][pr];
         char* d = nullptr;
         if (p >= 0) {
-          const int rk = R.ids[s][pr] / R.per_rank;
-          const long long row = route_row(R, base, s, rk, p, 1);
+          int rk;
+          const long long row = route_row(R, base, s, pair_expert(R, s, pr), p, 1, &rk);
           if (row >= 0) d = R.buf[rk] + size_t(row) * hb + off;
         }
         dst_tab[lane][j] = d;
@@ -734,8 +742,8 @@ __global__ void ep_combine_fused_vec_kernel(const __grid_constant__ EpRoute R) {
         const int p = R.pos_of[s][pr];
         wl = R.w[s][pr];
         if (p >= 0) {
-          const int d = R.ids[s][pr] / R.per_rank;
-          const long long row = route_row(R, base, s, d, p, 2);
+          int d;
+          const long long row = route_row(R, base, s, pair_expert(R, s, pr), p, 2, &d);
           if (row >= 0) mine = R.buf[d] + size_t(row) * R.hidden * 2;
         }
       }
@@ -765,8 +773,8 @@ __global__ void ep_combine_fused_vec_kernel(const __grid_constant__ EpRoute R) {
         const size_t pr = size_t(t) * R.topk + j;
         const int p = R.pos_of[s][pr];
         if (p < 0) continue;
-        const int d = R.ids[s][pr] / R.per_rank;
-        const long long row = route_row(R, base, s, d, p, 2);
+        int d;
+        const long long row = route_row(R, base, s, pair_expert(R, s, pr), p, 2, &d);
         if (row < 0) continue;
         const uint4* src = reinterpret_cast<const uint4*>(R.buf[d] + size_t(row) * R.hidden * 2);
         const float wj = R.w[s][pr];
@@ -843,8 +851,8 @@ __global__ void __launch_bounds__(32 * kCombWarps) ep_combine_bulk_kernel(const 
       const int p = R.pos_of[I.s][pr];
       I.w = R.w[I.s][pr];
       if (p >= 0) {
-        const int d = R.ids[I.s][pr] / R.per_rank;
-        const long long row = route_row(R, base, I.s, d, p, 2);
+        int d;
+        const long long row = route_row(R, base, I.s, pair_expert(R, I.s, pr), p, 2, &d);
         if (row >= 0) src = R.buf[d] + size_t(row) * hb + I.off;
       }
     }
@@ -925,8 +933,8 @@ __global__ void ep_combine_fused_kernel(const __grid_constant__ EpRoute R) {
         const size_t pr = size_t(t) * R.topk + j;
         const int p = R.pos_of[s][pr];
         if (p < 0) continue;
-        const int d = R.ids[s][pr] / R.per_rank;
-        const long long row = route_row(R, base, s, d, p, 2);
+        int d;
+        const long long row = route_row(R, base, s, pair_expert(R, s, pr), p, 2, &d);
         if (row < 0) continue;
         const uint16_t* src = reinterpret_cast<const uint16_t*>(R.buf[d] + size_t(row) * R.hidden * 2);
         const float prod = __fmul_rn(R.w[s][pr], __uint_as_float(uint32_t(src[h]) << 16));
@@ -1146,19 +1154,25 @@ extern "C" hocResult_t hoc_ep_combine(const void* rows, const int32_t* pos_of, c
   return cudaGetLastError() == cudaSuccess ? HOC_SUCCESS : HOC_ERR_CUDA;
 }
 
-extern "C" hocResult_t hoc_ep_dispatch_fused(int nranks, const int32_t* const* expert_ids, const void* const* x,
-                                             int tokens, int topk, int hidden, int experts, void* const* recv,
-                                             const size_t* recv_capacity, int32_t* const* pos_of, uint64_t* counts,
-                                             int32_t* workspace, size_t workspace_ints, int32_t* status, void* stream) {
-  using namespace hoc;
+namespace hoc {
+namespace {
+
+// Sort of every source's pairs, then the row scatter: into the destination
+// ranks' receive buffers (packed = 0, the dispatch fused with the exchange) or
+// into each source's own send buffer in packed order (packed = 1).
+hocResult_t dispatch_ranks(const char* who, int packed, int nranks, const int32_t* const* expert_ids,
+                           const void* const* x, int tokens, int topk, int hidden, int experts, void* const* out,
+                           const size_t* out_capacity, int32_t* const* pos_of, uint64_t* counts, int32_t* workspace,
+                           size_t workspace_ints, int32_t* status, cudaStream_t s) {
+  char msg[160];
   if (nranks < 1 || nranks > kMaxRanks || tokens < 0 || topk < 1 || hidden < 1 || experts < 1 ||
       experts % nranks != 0) {
-    set_error_detail("hoc_ep_dispatch_fused: bad rank count, shape or expert count");
+    snprintf(msg, sizeof msg, "%s: bad rank count, shape or expert count", who);
+    set_error_detail(msg);
     return HOC_ERR_INVALID_ARG;
   }
-  if (!expert_ids || !x || !recv || !recv_capacity || !pos_of || !counts || !status) return HOC_ERR_INVALID_ARG;
+  if (!expert_ids || !x || !out || !out_capacity || !pos_of || !counts || !status) return HOC_ERR_INVALID_ARG;
   if (size_t(tokens) * topk > size_t(INT32_MAX)) return HOC_ERR_INVALID_ARG;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return HOC_ERR_CUDA;
   if (tokens == 0)  // nobody sends anything
     return cudaMemsetAsync(counts, 0, sizeof(uint64_t) * size_t(nranks) * nranks, s) == cudaSuccess ? HOC_SUCCESS
@@ -1166,15 +1180,17 @@ extern "C" hocResult_t hoc_ep_dispatch_fused(int nranks, const int32_t* const* e
   const int n = tokens * topk;
   const size_t per = sort_ws_ints(n, experts);
   if (!workspace || workspace_ints < per * size_t(nranks)) {
-    set_error_detail("hoc_ep_dispatch_fused: workspace smaller than nranks * hoc_ep_pack_workspace()");
+    snprintf(msg, sizeof msg, "%s: workspace smaller than nranks * hoc_ep_pack_workspace()", who);
+    set_error_detail(msg);
     return HOC_ERR_INVALID_ARG;
   }
   EpSort P{};
   EpRoute R{};
   bool vec = (size_t(hidden) * 2) % 16 == 0;
   for (int r = 0; r < nranks; ++r) {
-    if (!expert_ids[r] || !x[r] || !recv[r] || !pos_of[r]) {
-      set_error_detail("hoc_ep_dispatch_fused: NULL per-rank pointer");
+    if (!expert_ids[r] || !x[r] || !out[r] || !pos_of[r]) {
+      snprintf(msg, sizeof msg, "%s: NULL per-rank pointer", who);
+      set_error_detail(msg);
       return HOC_ERR_INVALID_ARG;
     }
     P.ids[r] = expert_ids[r];
@@ -1182,15 +1198,16 @@ extern "C" hocResult_t hoc_ep_dispatch_fused(int nranks, const int32_t* const* e
     R.x[r] = static_cast<const char*>(x[r]);
     R.ids[r] = expert_ids[r];
     R.pos_of[r] = pos_of[r];
-    R.buf[r] = static_cast<char*>(recv[r]);
-    R.cap_rows[r] = recv_capacity[r] / size_t(hidden);
-    vec = vec && ((reinterpret_cast<uintptr_t>(x[r]) | reinterpret_cast<uintptr_t>(recv[r])) & 15u) == 0;
+    R.buf[r] = static_cast<char*>(out[r]);
+    R.cap_rows[r] = out_capacity[r] / size_t(hidden);
+    vec = vec && ((reinterpret_cast<uintptr_t>(x[r]) | reinterpret_cast<uintptr_t>(out[r])) & 15u) == 0;
   }
   P.counts = reinterpret_cast<unsigned long long*>(counts);
   P.ws = workspace;
   P.ws_stride = per;
   if (sort_pairs(P, nranks, n, experts, nranks, hidden, s) != cudaSuccess) {
-    set_error_detail("hoc_ep_dispatch_fused: launching the sort failed");
+    snprintf(msg, sizeof msg, "%s: launching the sort failed", who);
+    set_error_detail(msg);
     return HOC_ERR_CUDA;
   }
   R.counts = P.counts;
@@ -1200,6 +1217,7 @@ extern "C" hocResult_t hoc_ep_dispatch_fused(int nranks, const int32_t* const* e
   R.topk = topk;
   R.hidden = hidden;
   R.per_rank = experts / nranks;
+  R.packed = packed;
   const int hb = hidden * 2;
   // Row scatter: per-thread vector copies; with HOC_EP_DISPATCH=bulk (rows and
   // buffers aligned, topk <= 16) bulk copies through shared memory instead --
@@ -1225,49 +1243,56 @@ extern "C" hocResult_t hoc_ep_dispatch_fused(int nranks, const int32_t* const* e
     e = launch_pdl(ep_dispatch_fused_kernel, dim3(persistent_grid(fn, (warps + 7) / 8)), 256, 0, s, R, int(vec));
   }
   if (e != cudaSuccess) {
-    set_error_detail("hoc_ep_dispatch_fused: launching the row scatter failed");
+    snprintf(msg, sizeof msg, "%s: launching the row scatter failed", who);
+    set_error_detail(msg);
     return HOC_ERR_CUDA;
   }
   return HOC_SUCCESS;
 }
 
-extern "C" hocResult_t hoc_ep_combine_fused(int nranks, const void* const* rows, const size_t* rows_capacity,
-                                            const int32_t* const* expert_ids, const int32_t* const* pos_of,
-                                            const uint64_t* counts, const float* const* weights, int tokens, int topk,
-                                            int hidden, int experts, void* const* y, int32_t* status, void* stream) {
-  using namespace hoc;
+// The combine of every source: rows read from the expert ranks' buffers
+// (packed = 0, fused with the combine exchange) or from each source's own
+// buffer of returned rows in packed order (packed = 1; ids and counts unused).
+hocResult_t combine_ranks(const char* who, int packed, int nranks, const void* const* rows,
+                          const size_t* rows_capacity, const int32_t* const* expert_ids,
+                          const int32_t* const* pos_of, const uint64_t* counts, const float* const* weights,
+                          int tokens, int topk, int hidden, int experts, void* const* y, int32_t* status,
+                          cudaStream_t s) {
+  char msg[160];
   if (nranks < 1 || nranks > kMaxRanks || tokens < 0 || topk < 1 || hidden < 1 || experts < 1 ||
       experts % nranks != 0) {
-    set_error_detail("hoc_ep_combine_fused: bad rank count, shape or expert count");
+    snprintf(msg, sizeof msg, "%s: bad rank count, shape or expert count", who);
+    set_error_detail(msg);
     return HOC_ERR_INVALID_ARG;
   }
   if (tokens == 0) return HOC_SUCCESS;
-  if (!rows || !rows_capacity || !expert_ids || !pos_of || !counts || !weights || !y || !status)
+  if (!rows || !rows_capacity || (!packed && (!expert_ids || !counts)) || !pos_of || !weights || !y || !status)
     return HOC_ERR_INVALID_ARG;
   if (size_t(tokens) * topk > size_t(INT32_MAX)) return HOC_ERR_INVALID_ARG;
   EpRoute R{};
   bool vec = hidden % 8 == 0;
   for (int r = 0; r < nranks; ++r) {
-    if (!rows[r] || !expert_ids[r] || !pos_of[r] || !weights[r] || !y[r]) {
-      set_error_detail("hoc_ep_combine_fused: NULL per-rank pointer");
+    if (!rows[r] || (!packed && !expert_ids[r]) || !pos_of[r] || !weights[r] || !y[r]) {
+      snprintf(msg, sizeof msg, "%s: NULL per-rank pointer", who);
+      set_error_detail(msg);
       return HOC_ERR_INVALID_ARG;
     }
     R.buf[r] = static_cast<char*>(const_cast<void*>(rows[r]));
     R.cap_rows[r] = rows_capacity[r] / size_t(hidden);
-    R.ids[r] = expert_ids[r];
+    R.ids[r] = packed ? nullptr : expert_ids[r];
     R.pos_of[r] = pos_of[r];
     R.w[r] = weights[r];
     R.y[r] = static_cast<char*>(y[r]);
     vec = vec && ((reinterpret_cast<uintptr_t>(rows[r]) | reinterpret_cast<uintptr_t>(y[r])) & 15u) == 0;
   }
-  R.counts = reinterpret_cast<const unsigned long long*>(counts);
+  R.counts = packed ? nullptr : reinterpret_cast<const unsigned long long*>(counts);
   R.status = status;
   R.k = nranks;
   R.tokens = tokens;
   R.topk = topk;
   R.hidden = hidden;
   R.per_rank = experts / nranks;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  R.packed = packed;
   cudaError_t e;
   // Rows through shared memory by TMA bulk copies where shapes allow (the
   // default), else (or with HOC_EP_COMBINE=lsu) per-thread vector loads.
@@ -1297,8 +1322,45 @@ extern "C" hocResult_t hoc_ep_combine_fused(int nranks, const void* const* rows,
                    s, R);
   }
   if (e != cudaSuccess) {
-    set_error_detail("hoc_ep_combine_fused: launch failed");
+    snprintf(msg, sizeof msg, "%s: launch failed", who);
+    set_error_detail(msg);
     return HOC_ERR_CUDA;
   }
   return HOC_SUCCESS;
+}
+
+}  // namespace
+}  // namespace hoc
+
+extern "C" hocResult_t hoc_ep_dispatch_fused(int nranks, const int32_t* const* expert_ids, const void* const* x,
+                                             int tokens, int topk, int hidden, int experts, void* const* recv,
+                                             const size_t* recv_capacity, int32_t* const* pos_of, uint64_t* counts,
+                                             int32_t* workspace, size_t workspace_ints, int32_t* status, void* stream) {
+  return hoc::dispatch_ranks("hoc_ep_dispatch_fused", 0, nranks, expert_ids, x, tokens, topk, hidden, experts, recv,
+                             recv_capacity, pos_of, counts, workspace, workspace_ints, status,
+                             static_cast<cudaStream_t>(stream));
+}
+
+extern "C" hocResult_t hoc_ep_pack_all(int nranks, const int32_t* const* expert_ids, const void* const* x, int tokens,
+                                       int topk, int hidden, int experts, void* const* send,
+                                       const size_t* send_capacity, int32_t* const* pos_of, uint64_t* counts,
+                                       int32_t* workspace, size_t workspace_ints, int32_t* status, void* stream) {
+  return hoc::dispatch_ranks("hoc_ep_pack_all", 1, nranks, expert_ids, x, tokens, topk, hidden, experts, send,
+                             send_capacity, pos_of, counts, workspace, workspace_ints, status,
+                             static_cast<cudaStream_t>(stream));
+}
+
+extern "C" hocResult_t hoc_ep_combine_fused(int nranks, const void* const* rows, const size_t* rows_capacity,
+                                            const int32_t* const* expert_ids, const int32_t* const* pos_of,
+                                            const uint64_t* counts, const float* const* weights, int tokens, int topk,
+                                            int hidden, int experts, void* const* y, int32_t* status, void* stream) {
+  return hoc::combine_ranks("hoc_ep_combine_fused", 0, nranks, rows, rows_capacity, expert_ids, pos_of, counts,
+                            weights, tokens, topk, hidden, experts, y, status, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" hocResult_t hoc_ep_combine_all(int nranks, const void* const* rows, const size_t* rows_capacity,
+                                          const int32_t* const* pos_of, const float* const* weights, int tokens,
+                                          int topk, int hidden, void* const* y, int32_t* status, void* stream) {
+  return hoc::combine_ranks("hoc_ep_combine_all", 1, nranks, rows, rows_capacity, nullptr, pos_of, nullptr, weights,
+                            tokens, topk, hidden, nranks, y, status, static_cast<cudaStream_t>(stream));
 }

@@ -110,6 +110,10 @@ _SIGS["hoc_ep_combine_fused"] = (C.c_int, [C.c_int, C.POINTER(C.c_void_p), C.POI
                                            C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_void_p,
                                            C.POINTER(C.c_void_p), C.c_int, C.c_int, C.c_int, C.c_int,
                                            C.POINTER(C.c_void_p), C.c_void_p, C.c_void_p])
+_SIGS["hoc_ep_pack_all"] = _SIGS["hoc_ep_dispatch_fused"]
+_SIGS["hoc_ep_combine_all"] = (C.c_int, [C.c_int, C.POINTER(C.c_void_p), C.POINTER(C.c_size_t), C.POINTER(C.c_void_p),
+                                         C.POINTER(C.c_void_p), C.c_int, C.c_int, C.c_int, C.POINTER(C.c_void_p),
+                                         C.c_void_p, C.c_void_p])
 _SIGS["hoc_allreduce_host"] = (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_size_t,
                                          C.c_int, C.c_int, C.c_void_p])
 _SIGS["hoc_proxy_status"] = (C.c_int, [C.c_void_p, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64),
@@ -492,6 +496,45 @@ def ep_combine(rows, pos_of, weights, tokens: int, topk: int, hidden: int, y, st
     _check(lib().hoc_ep_combine(_ptr(rows, 2 * n * int(hidden), "rows"), _ptr(pos_of, 4 * n, "pos_of"),
                                 _ptr(weights, 4 * n, "weights"), int(tokens), int(topk), int(hidden),
                                 _ptr(y, 2 * int(tokens) * int(hidden), "y"), _stream(stream)), "hoc_ep_combine")
+
+
+def _ep_scatter_call(fn_name, expert_ids, x, experts, out, out_capacity, pos_of, counts, workspace, status, stream):
+    k = len(x)
+    tokens, hidden = x[0].shape
+    topk = expert_ids[0].numel() // tokens if tokens else 1
+    n = tokens * topk
+    caps = [int(v) for v in out_capacity]
+    if len(caps) != k or len(expert_ids) != k or len(out) != k or len(pos_of) != k:
+        raise ValueError(f"expected {k} per-rank tensors and capacities")
+    cap = (C.c_size_t * k)(*caps)
+    _check(getattr(lib(), fn_name)(k, _ptr_array(expert_ids, 4 * n, "expert_ids"),
+                                   _ptr_array(x, 2 * tokens * hidden, "x"), int(tokens), int(topk), int(hidden),
+                                   int(experts), _ptr_array(out, [2 * c for c in caps], "out"), cap,
+                                   _ptr_array(pos_of, 4 * n, "pos_of"), _ptr(counts, 8 * k * k, "counts"),
+                                   _ptr(workspace, 0, "workspace"), int(workspace.numel()),
+                                   _ptr(status, 4, "status"), _stream(stream)), fn_name)
+
+
+def ep_pack_all(expert_ids, x, experts: int, send, send_capacity, pos_of, counts, workspace, status, stream=None):
+    """hoc_ep_pack for every source rank in one pass (see include/hoc_ep.h): lists of k device tensors."""
+    _ep_scatter_call("hoc_ep_pack_all", expert_ids, x, experts, send, send_capacity, pos_of, counts, workspace,
+                     status, stream)
+
+
+def ep_combine_all(rows, rows_capacity, pos_of, weights, tokens: int, topk: int, hidden: int, y, status,
+                   stream=None):
+    """hoc_ep_combine for every source rank in one pass (see include/hoc_ep.h)."""
+    k = len(rows)
+    n = int(tokens) * int(topk)
+    caps = [int(v) for v in rows_capacity]
+    if len(caps) != k or len(pos_of) != k or len(weights) != k or len(y) != k:
+        raise ValueError(f"expected {k} per-rank tensors and capacities")
+    cap = (C.c_size_t * k)(*caps)
+    _check(lib().hoc_ep_combine_all(k, _ptr_array(rows, [2 * c for c in caps], "rows"), cap,
+                                    _ptr_array(pos_of, 4 * n, "pos_of"), _ptr_array(weights, 4 * n, "weights"),
+                                    int(tokens), int(topk), int(hidden),
+                                    _ptr_array(y, 2 * int(tokens) * int(hidden), "y"), _ptr(status, 4, "status"),
+                                    _stream(stream)), "hoc_ep_combine_all")
 
 
 def ep_dispatch_fused(expert_ids, x, experts: int, recv, recv_capacity, pos_of, counts, workspace, status,

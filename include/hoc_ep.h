@@ -103,6 +103,33 @@ hocResult_t hoc_ep_combine_fused(int nranks, const void* const* rows, const size
                                  const uint64_t* counts, const float* const* weights, int tokens, int topk,
                                  int hidden, int experts, void* const* y, int32_t* status, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * The same pack and combine for every rank in one pass, around the copy-engine
+ * exchange (hoc_alltoall_device_counts): the zero-SM way of moving the rows,
+ * with the SM work of all k ranks in one set of launches instead of k.
+ * ------------------------------------------------------------------------- */
+
+/* hoc_ep_pack for every source rank at once: send[s] receives source s's rows
+ * in (destination rank, expert, token, slot) order -- what hoc_ep_pack writes
+ * -- with room for send_capacity[s] elements (host array; a row past it is not
+ * written and sets bit 0 of *status, which is cleared first); pos_of[s] and
+ * row s of counts (device [nranks*nranks] uint64 elements) as hoc_ep_pack.  No
+ * perm is written.  workspace: nranks * hoc_ep_pack_workspace() int32 entries.
+ * The row scatter engine follows HOC_EP_DISPATCH as for hoc_ep_dispatch_fused. */
+hocResult_t hoc_ep_pack_all(int nranks, const int32_t* const* expert_ids, const void* const* x, int tokens, int topk,
+                            int hidden, int experts, void* const* send, const size_t* send_capacity,
+                            int32_t* const* pos_of, uint64_t* counts, int32_t* workspace, size_t workspace_ints,
+                            int32_t* status, void* stream);
+
+/* hoc_ep_combine for every source rank at once: rows[s] holds source s's rows
+ * back from the experts in packed order (room for rows_capacity[s] elements;
+ * a row past it adds nothing and sets bit 1 of *status, not cleared here);
+ * pos_of[s], weights[s] and y[s] as hoc_ep_combine.  The engine follows
+ * HOC_EP_COMBINE as for hoc_ep_combine_fused. */
+hocResult_t hoc_ep_combine_all(int nranks, const void* const* rows, const size_t* rows_capacity,
+                               const int32_t* const* pos_of, const float* const* weights, int tokens, int topk,
+                               int hidden, void* const* y, int32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -258,3 +258,108 @@ def test_fused_zero_tokens():
     hoc.ep_dispatch_fused(ids, xs, experts, recv, [hidden] * k, ids, counts, ws, status)
     torch.cuda.synchronize()
     assert counts.abs().sum().item() == 0 and int(status.item()) == 0
+
+
+@pytest.mark.parametrize("engines", [None, ("bulk", "lsu")])
+def test_fused_sixteen_ranks_and_misaligned_outputs(engines, monkeypatch):
+    # the most ranks a call takes, and outputs 2 bytes off alignment (vector dispatch, scalar combine)
+    if engines:
+        monkeypatch.setenv("HOC_EP_DISPATCH", engines[0])
+        monkeypatch.setenv("HOC_EP_COMBINE", engines[1])
+    k, tokens, hidden, experts, topk = 16, 300, 128, 64, 4
+    routing = [r.copy() for r in inputs.ep_routing(k, tokens, experts, topk, 1.1, seed_base=5400)]
+    xs = [inputs.normal_bf16(tokens * hidden, 6000 + r).reshape(tokens, hidden) for r in range(k)]
+    rng = np.random.default_rng(6100)
+    ws = [rng.random(tokens * topk).astype(np.float32) for _ in range(k)]
+    packs, counts, want_recv, want_y = _oracle_round_trip(xs, routing, ws, experts, k, topk, hidden)
+    caps = [int(counts[:, d].sum()) for d in range(k)]
+    for y_offset in (0, 1):
+        recv, pos, d_counts, status, ys = _fused_on_device(k, xs, routing, ws, experts, topk, caps, 0, y_offset)
+        assert int(status.item()) == 0
+        for d in range(k):
+            assert np.array_equal(recv[d].host(), want_recv[d]), d
+        for r in range(k):
+            ys[r].check()
+            assert np.array_equal(ys[r].host().reshape(tokens, hidden), want_y[r]), (y_offset, r)
+
+
+def test_fused_combine_reports_rows_outside_its_buffers():
+    # the dispatch fits; the combine is told a smaller buffer for rank 0: the rows past it add nothing,
+    # bit 1 of the status is set, and nothing is written outside the outputs
+    from tests.gpu_util import Guarded
+    k, tokens, hidden, experts, topk = 4, 200, 64, 16, 3
+    routing = inputs.ep_routing(k, tokens, experts, topk, 1.1, seed_base=5500)
+    xs = [inputs.normal_bf16(tokens * hidden, 6200 + r).reshape(tokens, hidden) for r in range(k)]
+    ws = [np.ones(tokens * topk, np.float32) for _ in range(k)]
+    packs, counts, want_recv, want_y = _oracle_round_trip(xs, routing, ws, experts, k, topk, hidden)
+    caps = [int(counts[:, d].sum()) for d in range(k)]
+    d_ids = [torch.from_numpy(np.ascontiguousarray(r, dtype=np.int32).reshape(-1)).cuda() for r in routing]
+    d_x = [to_device(x, "bfloat16") for x in xs]
+    recv = [torch.empty(c, dtype=torch.bfloat16, device="cuda") for c in caps]
+    pos = [torch.empty(tokens * topk, dtype=torch.int32, device="cuda") for _ in range(k)]
+    d_counts = torch.empty((k, k), dtype=torch.int64, device="cuda")
+    wsp = torch.empty(k * hoc.ep_pack_workspace(tokens, topk, experts), dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hoc.ep_dispatch_fused(d_ids, d_x, experts, recv, caps, pos, d_counts, wsp, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    small = list(caps)
+    small[0] = caps[0] - 4 * hidden
+    ys = [Guarded(tokens * hidden, "bfloat16") for _ in range(k)]
+    w = [torch.from_numpy(x).cuda() for x in ws]
+    hoc.ep_combine_fused(recv, small, d_ids, pos, d_counts, w, tokens, topk, hidden, experts, [g.tensor for g in ys],
+                         status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 2
+    for r in range(k):
+        ys[r].check()
+
+
+@pytest.mark.parametrize("engines", [None, ("bulk", "lsu")])
+@pytest.mark.parametrize("k,tokens,hidden,experts,topk", [(8, 4096, 2048, 64, 6), (3, 500, 36, 48, 4),
+                                                          (8, 300, 64, 2048, 2)])
+def test_pack_all_and_combine_all_match_oracle(k, tokens, hidden, experts, topk, engines, monkeypatch):
+    # every rank's pack in one pass, the two copy-engine exchanges, every rank's combine in one pass
+    if engines:
+        monkeypatch.setenv("HOC_EP_DISPATCH", engines[0])
+        monkeypatch.setenv("HOC_EP_COMBINE", engines[1])
+    from tests.gpu_util import Guarded
+    routing = [r.copy() for r in inputs.ep_routing(k, tokens, experts, topk, 1.1, seed_base=5600 + k)]
+    routing[0][1, 0] = -1
+    xs = [inputs.normal_bf16(tokens * hidden, 6300 + r).reshape(tokens, hidden) for r in range(k)]
+    rng = np.random.default_rng(6400)
+    ws = [rng.random(tokens * topk).astype(np.float32) for _ in range(k)]
+    packs, counts, want_recv, want_y = _oracle_round_trip(xs, routing, ws, experts, k, topk, hidden)
+    n = tokens * topk
+    d_ids = [torch.from_numpy(np.ascontiguousarray(r, dtype=np.int32).reshape(-1)).cuda() for r in routing]
+    d_x = [to_device(x, "bfloat16") for x in xs]
+    send = [Guarded(n * hidden, "bfloat16") for _ in range(k)]
+    pos = [torch.empty(n, dtype=torch.int32, device="cuda") for _ in range(k)]
+    d_counts = torch.empty((k, k), dtype=torch.int64, device="cuda")
+    wsp = torch.empty(k * hoc.ep_pack_workspace(tokens, topk, experts), dtype=torch.int32, device="cuda")
+    status = torch.full((1,), 9, dtype=torch.int32, device="cuda")
+    hoc.ep_pack_all(d_ids, d_x, experts, [g.tensor for g in send], [n * hidden] * k, pos, d_counts, wsp, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(d_counts.cpu().numpy(), counts)
+    for r in range(k):
+        nv = len(packs[r][1])
+        assert np.array_equal(send[r].host()[: nv * hidden], packs[r][0].reshape(-1)), r
+        assert np.all(send[r].host()[nv * hidden:] == 0xA5A5), r      # nothing past the valid rows
+        assert np.array_equal(pos[r].cpu().numpy(), packs[r][2]), r
+        send[r].check()
+    caps = [int(counts[:, d].sum()) for d in range(k)]
+    with hoc.Comm(k, 0) as c:
+        recv = [torch.empty(max(1, v), dtype=torch.bfloat16, device="cuda") for v in caps]
+        back = [torch.empty(n * hidden, dtype=torch.bfloat16, device="cuda") for _ in range(k)]
+        c.alltoall([g.tensor for g in send], recv, sendcounts=counts, dtype=hoc.BFLOAT16)
+        c.alltoall(recv, back, sendcounts=counts.T.copy(), dtype=hoc.BFLOAT16)
+        c.wait()
+    ys = [Guarded(tokens * hidden, "bfloat16") for _ in range(k)]
+    w = [torch.from_numpy(x).cuda() for x in ws]
+    hoc.ep_combine_all(back, [n * hidden] * k, pos, w, tokens, topk, hidden, [g.tensor for g in ys], status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for r in range(k):
+        ys[r].check()
+        assert np.array_equal(ys[r].host().reshape(tokens, hidden), want_y[r]), r
