@@ -149,10 +149,14 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 template <class F>
 hocResult_t timed_launch(hocComm* c, int kind, cudaStream_t s, F&& launch) {
   cudaEvent_t a = nullptr, b = nullptr;
+  unsigned flags = cudaEventRecordDefault;  // external event nodes when the caller captures the call
   if (c->profiling) {
     HOC_TRY(prof_event(c, &a));
     HOC_TRY(prof_event(c, &b));
-    HOC_CK(cudaEventRecord(a, s));
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    HOC_CK(cudaStreamIsCapturing(s, &cap));
+    if (cap != cudaStreamCaptureStatusNone) flags = cudaEventRecordExternal;
+    HOC_CK(cudaEventRecordWithFlags(a, s, flags));
   }
   cudaError_t e = launch();
   if (e != cudaSuccess) {
@@ -160,7 +164,7 @@ hocResult_t timed_launch(hocComm* c, int kind, cudaStream_t s, F&& launch) {
     return HOC_ERR_CUDA;
   }
   if (c->profiling) {
-    HOC_CK(cudaEventRecord(b, s));
+    HOC_CK(cudaEventRecordWithFlags(b, s, flags));
     c->prof_pending.push_back(ProfPair{a, b, kind});
   }
   if (c->cfg.debug) {
@@ -320,6 +324,9 @@ hocResult_t issue(hocComm* c, const Plan& p, const Bind& bd, cudaStream_t s0, co
     for (int i = 1; i < p.n_streams; ++i) st[i] = given ? (*given)[i - 1] : (*copy)[i - 1];
   }
   const bool prof_streams = c->profiling && p.n_streams > 1;
+  // Timeline events of a call the caller is capturing into a graph are
+  // recorded as external event nodes, so that they can be read after a replay.
+  unsigned tl_flags = cudaEventRecordDefault;
   if (c->profiling) {
     c->prof_streams = 0;
     c->prof_steps.clear();
@@ -329,7 +336,10 @@ hocResult_t issue(hocComm* c, const Plan& p, const Bind& bd, cudaStream_t s0, co
       HOC_CK(cudaEventCreate(&e));
       c->prof_step_events.push_back(e);
     }
-    HOC_CK(cudaEventRecord(c->prof_origin, s0));
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    HOC_CK(cudaStreamIsCapturing(s0, &cap));
+    if (cap != cudaStreamCaptureStatusNone) tl_flags = cudaEventRecordExternal;
+    HOC_CK(cudaEventRecordWithFlags(c->prof_origin, s0, tl_flags));
   }
   if (prof_streams) {
     if (!c->prof_fork) HOC_CK(cudaEventCreate(&c->prof_fork));
@@ -353,7 +363,7 @@ hocResult_t issue(hocComm* c, const Plan& p, const Bind& bd, cudaStream_t s0, co
     if (c->profiling) {
       hocComm::StepTiming t{step.kind, step.stream, step.stage, c->prof_step_events[2 * i],
                             c->prof_step_events[2 * i + 1]};
-      HOC_CK(cudaEventRecord(t.start, s));
+      HOC_CK(cudaEventRecordWithFlags(t.start, s, tl_flags));
       c->prof_steps.push_back(t);
     }
     switch (step.kind) {
@@ -374,7 +384,7 @@ hocResult_t issue(hocComm* c, const Plan& p, const Bind& bd, cudaStream_t s0, co
         break;
       default: return HOC_ERR_INVALID_ARG;
     }
-    if (c->profiling) HOC_CK(cudaEventRecord(c->prof_steps.back().end, s));
+    if (c->profiling) HOC_CK(cudaEventRecordWithFlags(c->prof_steps.back().end, s, tl_flags));
     if (step.record) HOC_CK(cudaEventRecord(c->ev[i], s));
   }
   if (prof_streams) {

@@ -228,7 +228,9 @@ hocResult_t hoc_profile_stream_finish(hocComm_t comm, float* finish_ms, int max_
  * depends on, so start..end is when the step could run and when it finished.
  * Waits for those events.  Writes at most `cap` items; *n_items = all of them.
  * Used to see how the chunks of a pipelined allreduce overlap (HOCCL section
- * 3.3.1 on chunk pipelining). */
+ * 3.3.1 on chunk pipelining).  A profiled call that the caller captures into a
+ * CUDA graph records these events as external event nodes: after a replay of
+ * that graph, this call returns the replay's timeline. */
 typedef struct {
   int kind;     /* hocItemKind_t: HOC_ITEM_REDUCE, HOC_ITEM_FUSED, HOC_ITEM_COPY or HOC_ITEM_TMA */
   int stream;   /* 0 = caller stream, 1..n = internal copy streams */

@@ -75,3 +75,31 @@ def test_timeline_of_a_pipelined_allreduce():
             assert t["start_ms"] >= reduces[t["stage"]]["end_ms"] - 1e-3, (t, reduces[t["stage"]])
         for r in range(k):
             assert np.array_equal(to_host(recv[r], "float32").view(np.uint32), want[r].view(np.uint32))
+
+
+def test_timeline_of_a_captured_call_after_replay():
+    # profiled inside the caller's graph capture: the timeline is that of the last replay
+    k, n = 4, 1 << 16
+    s = torch.cuda.Stream()
+    with hoc.Comm(k, 0, hoc.Config(path="ce", n_copy_streams=2, chunk_bytes=(n // k) * 4 // 2)) as c:
+        send = [torch.ones(n, device="cuda") for _ in range(k)]
+        recv = [torch.zeros(n, device="cuda") for _ in range(k)]
+        with torch.cuda.stream(s):
+            c.allreduce(send, recv, stream=s)          # plans built outside the capture
+        torch.cuda.synchronize()
+        c.profile_enable(True)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            c.allreduce(send, recv, stream=s)
+        c.profile_enable(False)
+        for t in recv:
+            t.zero_()
+        with torch.cuda.stream(s):
+            g.replay()
+        torch.cuda.synchronize()
+        tl = c.profile_timeline()
+        assert {t["kind"] for t in tl} == {"reduce", "copy"}
+        assert all(0 <= t["start_ms"] <= t["end_ms"] < 100 for t in tl)
+        assert all(bool((r == k).all()) for r in recv)
+        launches, ms = c.profile_read(hoc.KERNEL_REDUCE)     # the kernel events of the capture are readable too
+        assert launches == 2 and ms > 0
