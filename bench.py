@@ -344,13 +344,16 @@ PROBE_SHAPES = {
 PROBE_KERNELS = 40          # the probe is a train of one-wave kernels, ~0.25 ms each
 
 
-def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int, shape: str = "whole_sm", n_kernels: int = 0):
+def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int, shape: str = "whole_sm", n_kernels: int = 0,
+                   priority: int = 0, graph: bool = False):
     """Slowdown of the FMA probe train while the collective runs back to back beside it.
 
     The probe is a train of short one-wave kernels, like a sequence of layer
     kernels: between two probe kernels the block scheduler hands SMs to
     whichever kernel launched first, so a collective that needs SMs takes them
     from the probe, and one that needs none (copy engines) leaves it alone.
+    `priority`: the probe stream's priority (lower is higher, as for CUDA);
+    `graph`: the train is captured once into a CUDA graph and replayed.
     """
     import torch
 
@@ -359,12 +362,32 @@ def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int, shape: str = "w
     cfg = PROBE_SHAPES[shape]
     ctas, threads, whole = cfg["ctas_per_sm"] * sms, cfg["threads"], cfg["whole_sm"]
     nk = n_kernels or PROBE_KERNELS
-    sp = torch.cuda.Stream()
+    sp = torch.cuda.Stream(priority=priority)
     gate = torch.cuda.Stream()
     sink = torch.zeros(4, dtype=torch.float32, device="cuda")
     mhz = []
+    trains = {}
+
+    def capture(iters):   # the train as one CUDA graph, captured before the timed runs
+        if graph and iters not in trains:
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=sp):
+                for _ in range(nk):
+                    hoc.probe_launch(ctas, threads, iters, stream=sp, whole_sm=whole, sink=sink)
+            trains[iters] = g
+            torch.cuda.synchronize()
+
+    def train(iters):
+        if graph:
+            with torch.cuda.stream(sp):
+                trains[iters].replay()
+        else:
+            for _ in range(nk):
+                hoc.probe_launch(ctas, threads, iters, stream=sp, whole_sm=whole, sink=sink)
 
     def run_probe(iters, with_coll=False, n_coll=0):
+        capture(iters)
         ev_gate = torch.cuda.Event()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
@@ -376,8 +399,7 @@ def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int, shape: str = "w
             for _ in range(n_coll):
                 run_coll(stream_c)
         a.record(sp)
-        for _ in range(nk):
-            hoc.probe_launch(ctas, threads, iters, stream=sp, whole_sm=whole, sink=sink)
+        train(iters)
         b.record(sp)
         torch.cuda.synchronize()
         cyc, ns = sink[0].item(), sink[1].item()
@@ -400,8 +422,9 @@ def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int, shape: str = "w
             "sm_mhz_with": round(statistics.median(mhz_with), 1) if mhz_with else None}
 
 
-def probes(run_coll, coll_ms, stream_c, sms, n_kernels=0):
-    return {shape: probe_slowdown(run_coll, coll_ms, stream_c, sms, shape, n_kernels) for shape in PROBE_SHAPES}
+def probes(run_coll, coll_ms, stream_c, sms, n_kernels=0, priority=0, graph=False):
+    return {shape: probe_slowdown(run_coll, coll_ms, stream_c, sms, shape, n_kernels, priority, graph)
+            for shape in PROBE_SHAPES}
 
 
 def leg_ce_interference(send, recv, n_el, k, local, stream, sms):
@@ -471,6 +494,14 @@ def leg_ce_interference(send, recv, n_el, k, local, stream, sms):
         pr = probes(run, ms, stream, sms)
         out["issue"].append(dict(graphs=graphs, slowdown=slow(pr), **info))
         c.close()
+    # (f) the probe's stream at the highest priority; (g) the probe train launched as one CUDA graph
+    out["probe_side"] = []
+    c, run, ms, info = moves(4 << 20, 4)
+    for label, kw in (("high_priority_stream", dict(priority=-100)), ("graph_launched_train", dict(graph=True)),
+                      ("both", dict(priority=-100, graph=True))):
+        pr = probes(run, ms, stream, sms, **kw)
+        out["probe_side"].append(dict(probe=label, slowdown=slow(pr), sm_mhz_alone_with=mhz(pr), **info))
+    c.close()
     return out
 
 
