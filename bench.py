@@ -1299,7 +1299,10 @@ def run_ours(args, world, rank, local):
             s3 = c3.last_stats()
             ag[p] = {"ms": round(am, 4), "bytes_gbs": round(s3["bytes_exec"] / (am * 1e-3) / 1e9, 1),
                      "sms_used": s3["sms_used"], "kernels_per_step": s3["kernels"],
-                     "probe": probes(run, am, stream, sms)}
+                     "probe": probes(run, am, stream, sms),
+                     # the same probe train on a stream of the highest priority (the moves' streams keep
+                     # the default, lowest one): compute first wherever the GPU arbitrates between streams
+                     "probe_high_priority": probes(run, am, stream, sms, priority=-100)}
             c3.close()
         # copy-engine chunk size against interference: larger copies move faster but slow the probe more
         tradeoff = []

@@ -82,7 +82,11 @@ typedef struct {
   int path;              /* hocPath_t */
   size_t chunk_bytes;    /* pipeline unit inside a block / flow; 0 (default) picks by move path
                             (4 MiB on copy engines and on the TMA kernel, the measured best) */
-  int n_copy_streams;    /* internal copy streams (the multi-QP analogue); default 4, max 16 */
+  int n_copy_streams;    /* internal copy streams (the multi-QP analogue); default 4, max 16.
+                            They run at the default stream priority, the lowest: a caller's
+                            compute stream created with a higher priority gets its kernel
+                            launches served ahead of the moves' work, which keeps the moves'
+                            cost to short compute kernels beside them lowest */
   int pipeline_depth;    /* allreduce CE/TMA: reduce of chunk q waits for the moves of
                             chunk q - depth; 0 = no limit */
   int reduce_max_sms;    /* cap on CTAs of reduce kernels (one 1024-thread CTA per SM); 0 = whole GPU */
