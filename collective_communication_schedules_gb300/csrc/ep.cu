@@ -460,18 +460,20 @@ __global__ void ep_combine_vec_ilp_kernel(const uint16_t* __restrict__ rows, con
 }
 
 // ---------------------------------------------------------------------------
-// Fused with the exchange.  Per-source inputs and per-rank receive buffers of
+// Fused with the exchange (and, in packed mode, the all-rank pack / combine
+// around a copy-engine exchange).  Per-source inputs and per-rank buffers of
 // one dispatch / combine over all k simulated ranks.
 struct EpRoute {
   const char* x[kMaxRanks];         // dispatch: token rows of each source, [tokens, hidden] bf16
   const int32_t* ids[kMaxRanks];    // expert id of every (token, slot) pair of each source
   const int32_t* pos_of[kMaxRanks]; // packed row of every pair (-1: dropped)
   const float* w[kMaxRanks];        // combine: gate weights of every pair
-  char* buf[kMaxRanks];             // receive buffer of each rank (dispatch writes, combine reads)
+  char* buf[kMaxRanks];             // row buffer of each rank: receive buffers, or (packed) each source's own
   char* y[kMaxRanks];               // combine: output rows of each source
-  unsigned long long cap_rows[kMaxRanks];  // rows each receive buffer holds
-  const unsigned long long* counts;        // [k][k] element counts, row = source
-  int32_t* status;                  // bit 0: a dispatched row did not fit; bit 1: a combine row out of range
+  unsigned long long cap_rows[kMaxRanks];  // rows each buffer holds
+  const unsigned long long* counts;        // [k][k] element counts, row = source (unused when packed)
+  int32_t* status;  // bit 0: a dispatched row did not fit; bit 1: a combine row out of range;
+                    // bit 2: a bounded wait of a bulk-copy kernel gave up
   int k, tokens, topk, hidden, per_rank;
   int packed;  // 1: each source's own buffer buf[s], rows in its packed order (no exchange to fuse)
 };
