@@ -28,7 +28,11 @@
 namespace hoc {
 namespace {
 
-constexpr int kStages = 4;
+// Pieces in flight per CTA (one CTA per SM, 192 KiB of shared memory).  Measured on GB300: the
+// all-gather moves of 8 x 32 MiB blocks run at 5.93-5.96 TB/s with 4, 6 or 8 stages alike, and the
+// TMA allreduce, whose moves interleave with the reduce kernels, takes 0.679 ms with 6 stages
+// against 0.695 with 4 (3 stages on two CTAs per SM: 0.685; 8 x 16 KiB: 0.714).
+constexpr int kStages = 6;
 constexpr uint32_t kPieceBytes = 32768;
 constexpr int kCopyThreads = 64;
 
