@@ -269,12 +269,16 @@ def cpu_baseline(xs_host, seconds: float, device_out=None):
         import torch
         rng = np.random.default_rng(123)
         idx = np.sort(rng.choice(n, size=min(n, 1 << 20), replace=False))
-        ti = torch.from_numpy(idx).to(device_out[0].device)
-        ok = True
-        for r in range(K_RANKS):
-            got = device_out[r].view(torch.int16).index_select(0, ti).cpu().numpy().view(np.uint16)
-            ok = ok and bool(np.array_equal(got, y[r][idx]))
-        out["parity_sample_ok"] = ok
+        try:
+            ti = torch.from_numpy(idx).to(device_out[0].device)
+            ok = True
+            for r in range(K_RANKS):
+                got = device_out[r].view(torch.int16).index_select(0, ti).cpu().numpy().view(np.uint16)
+                ok = ok and bool(np.array_equal(got, y[r][idx]))
+            out["parity_sample_ok"] = ok
+        except Exception as e:  # noqa: BLE001 -- reported; the baseline's timing stands
+            out["parity_sample_ok"] = None
+            out["parity_error"] = f"{type(e).__name__}: {e}"
     return out
 
 
@@ -1142,6 +1146,117 @@ def leg_host_overhead():
     return out
 
 
+def leg_paths_and_moves(args, send, recv, n_el, k, local, stream, sms, peak, per_rank):
+    """Per-path allreduce figures with probes, the move half alone, copy size against interference,
+    the chunk-size sweep and the allreduce under an SM budget."""
+    import torch
+
+    from collective_communication_schedules_gb300 import hoc
+
+    # per-path figures
+    paths = {}
+    for p, eng in (("fused", "lsu"), ("fused", "tma"), ("ce", "lsu"), ("tma", "lsu")):
+        c2 = hoc.Comm(k, local, hoc.Config(path=p, chunk_bytes=args.chunk_bytes, n_copy_streams=args.copy_streams,
+                                           reduce_engine=eng))
+        for _ in range(3):
+            c2.allreduce(send, recv, stream=stream)
+        pm = time_allreduce(c2, send, recv, stream, max(5, args.steps // 2))
+        s2 = c2.last_stats()
+        p = p if eng == "lsu" else f"{p}_{eng}"
+        paths[p] = {"ms": round(pm, 4), "bus_gbs": round(bus_bytes(k, per_rank) / (pm * 1e-3) / 1e9, 1),
+                    "hbm_frac": round(s2["bytes_exec"] / (pm * 1e-3) / (peak * 1e9), 4),
+                    "lower_bound_frac": round(s2["bytes_min"] / (pm * 1e-3) / (peak * 1e9), 4),
+                    "sms_used": s2["sms_used"], "kernels_per_step": s2["kernels"],
+                    "copies_per_step": s2["copies"]}
+        paths[p]["probe"] = probes(lambda s, c2=c2: c2.allreduce(send, recv, stream=s), pm, stream, sms)
+        c2.close()
+    # the move half alone: all-gather of the 32 MiB blocks, copy engines vs TMA
+    ag = {}
+    blk = n_el // k
+    ag_send = [t[:blk] for t in send]
+    for p in ("ce", "tma"):
+        c3 = hoc.Comm(k, local, hoc.Config(path=p, chunk_bytes=args.chunk_bytes, n_copy_streams=args.copy_streams))
+        run = lambda s, c3=c3: c3.allgather(ag_send, recv, stream=s)
+        for _ in range(3):
+            run(stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(10):
+            run(stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        am = e0.elapsed_time(e1) / 10
+        s3 = c3.last_stats()
+        ag[p] = {"ms": round(am, 4), "bytes_gbs": round(s3["bytes_exec"] / (am * 1e-3) / 1e9, 1),
+                 "sms_used": s3["sms_used"], "kernels_per_step": s3["kernels"],
+                 "probe": probes(run, am, stream, sms),
+                 # the same probe train on a stream of the highest priority (the moves' streams keep
+                 # the default, lowest one): compute first wherever the GPU arbitrates between streams
+                 "probe_high_priority": probes(run, am, stream, sms, priority=-100)}
+        c3.close()
+    # copy-engine chunk size against interference: larger copies move faster but slow the probe more
+    tradeoff = []
+    for mib, nq in ((4, 4), (8, 4), (16, 4), (32, 4), (32, 8)):
+        c5 = hoc.Comm(k, local, hoc.Config(path="ce", chunk_bytes=mib << 20, n_copy_streams=nq))
+        run = lambda s, c5=c5: c5.allgather(ag_send, recv, stream=s)
+        for _ in range(3):
+            run(stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(10):
+            run(stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        am = e0.elapsed_time(e1) / 10
+        s5 = c5.last_stats()
+        pr = probes(run, am, stream, sms)
+        tradeoff.append({"chunk_mib": mib, "copy_streams": nq, "ms": round(am, 4),
+                         "bytes_gbs": round(s5["bytes_exec"] / (am * 1e-3) / 1e9, 1), "copies_per_step": s5["copies"],
+                         "kernels_per_step": s5["kernels"],
+                         "probe_slowdown": {sh: pr[sh]["slowdown"] for sh in pr},
+                         "probe_sm_mhz_with": {sh: pr[sh]["sm_mhz_with"] for sh in pr}})
+        c5.close()
+    out = {"paths": paths, "allgather_moves": ag, "allgather_ce_chunk_vs_probe": tradeoff}
+    # chunk size sweep, 1-64 MiB (64 is capped at the 32 MiB block), on the copy-engine and
+    # TMA-kernel move paths; then copy-queue counts on the copy-engine path
+    sweep = []
+    grid = [(p, mib, 4, 0) for p in ("ce", "tma") for mib in (1, 2, 4, 8, 16, 32, 64)]
+    grid += [("ce", 32, 8, 0), ("ce", 8, 8, 0), ("ce", 8, 16, 0)]
+    grid += [("ce", 4, 4, d) for d in (1, 2, 4)]      # pipeline depth: reduce at most d chunks ahead of the moves
+    for p, chunk_mib, nq, depth in grid:
+        c4 = hoc.Comm(k, local, hoc.Config(path=p, chunk_bytes=chunk_mib << 20, n_copy_streams=nq,
+                                           pipeline_depth=depth))
+        for _ in range(3):
+            c4.allreduce(send, recv, stream=stream)
+        cm = time_allreduce(c4, send, recv, stream, 10)
+        s4 = c4.last_stats()
+        sweep.append({"path": p, "chunk_mib": chunk_mib, "copy_streams": nq, "pipeline_depth": depth or "unbounded",
+                      "ms": round(cm, 4),
+                      "bus_gbs": round(bus_bytes(k, per_rank) / (cm * 1e-3) / 1e9, 1),
+                      "lower_bound_frac": round(s4["bytes_min"] / (cm * 1e-3) / (peak * 1e9), 4),
+                      "copies_per_step": s4["copies"], "kernels_per_step": s4["kernels"]})
+        c4.close()
+    out["chunk_sweep"] = sweep
+    # allreduce under an SM budget: fused (every move on the few SMs) vs copy engines (SMs only reduce);
+    # AUTO picks the copy engines when a budget is set
+    budget = []
+    for m in (8, 32):
+        for p in ("fused", "ce"):
+            c6 = hoc.Comm(k, local, hoc.Config(path=p, reduce_max_sms=m))
+            for _ in range(2):
+                c6.allreduce(send, recv, stream=stream)
+            bm = time_allreduce(c6, send, recv, stream, 5)
+            s6 = c6.last_stats()
+            budget.append({"reduce_max_sms": m, "path": p, "ms": round(bm, 3),
+                           "bus_gbs": round(bus_bytes(k, per_rank) / (bm * 1e-3) / 1e9, 1),
+                           "sms_used": s6["sms_used"], "copies_per_step": s6["copies"]})
+            c6.close()
+    out["allreduce_under_sm_budget"] = budget
+    return out
+
+
 def run_ours(args, world, rank, local):
     import numpy as np
     import torch
@@ -1261,121 +1376,38 @@ def run_ours(args, world, rank, local):
            "unpipelined_ms_per_step": round(plain_ms, 3)}
 
     extras = {}
+
+    def study(fn, *a):
+        """Run one study leg; a leg that fails is reported in the line and the headline stands."""
+        try:
+            return fn(*a)
+        except Exception as e:  # noqa: BLE001 -- any failure of a study leg is data for the line
+            try:
+                torch.cuda.synchronize()
+                torch.cuda.empty_cache()
+            except Exception:  # noqa: BLE001
+                pass
+            return {"error": f"{type(e).__name__}: {e}"}
+
     if not args.no_extras:
-        # per-path figures
-        paths = {}
-        for p, eng in (("fused", "lsu"), ("fused", "tma"), ("ce", "lsu"), ("tma", "lsu")):
-            c2 = hoc.Comm(k, local, hoc.Config(path=p, chunk_bytes=args.chunk_bytes, n_copy_streams=args.copy_streams,
-                                               reduce_engine=eng))
-            for _ in range(3):
-                c2.allreduce(send, recv, stream=stream)
-            pm = time_allreduce(c2, send, recv, stream, max(5, args.steps // 2))
-            s2 = c2.last_stats()
-            p = p if eng == "lsu" else f"{p}_{eng}"
-            paths[p] = {"ms": round(pm, 4), "bus_gbs": round(bus_bytes(k, per_rank) / (pm * 1e-3) / 1e9, 1),
-                        "hbm_frac": round(s2["bytes_exec"] / (pm * 1e-3) / (peak * 1e9), 4),
-                        "lower_bound_frac": round(s2["bytes_min"] / (pm * 1e-3) / (peak * 1e9), 4),
-                        "sms_used": s2["sms_used"], "kernels_per_step": s2["kernels"],
-                        "copies_per_step": s2["copies"]}
-            paths[p]["probe"] = probes(lambda s, c2=c2: c2.allreduce(send, recv, stream=s), pm, stream, sms)
-            c2.close()
-        # the move half alone: all-gather of the 32 MiB blocks, copy engines vs TMA
-        ag = {}
-        blk = n_el // k
-        ag_send = [t[:blk] for t in send]
-        for p in ("ce", "tma"):
-            c3 = hoc.Comm(k, local, hoc.Config(path=p, chunk_bytes=args.chunk_bytes, n_copy_streams=args.copy_streams))
-            run = lambda s, c3=c3: c3.allgather(ag_send, recv, stream=s)
-            for _ in range(3):
-                run(stream)
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(10):
-                run(stream)
-            e1.record(stream)
-            torch.cuda.synchronize()
-            am = e0.elapsed_time(e1) / 10
-            s3 = c3.last_stats()
-            ag[p] = {"ms": round(am, 4), "bytes_gbs": round(s3["bytes_exec"] / (am * 1e-3) / 1e9, 1),
-                     "sms_used": s3["sms_used"], "kernels_per_step": s3["kernels"],
-                     "probe": probes(run, am, stream, sms),
-                     # the same probe train on a stream of the highest priority (the moves' streams keep
-                     # the default, lowest one): compute first wherever the GPU arbitrates between streams
-                     "probe_high_priority": probes(run, am, stream, sms, priority=-100)}
-            c3.close()
-        # copy-engine chunk size against interference: larger copies move faster but slow the probe more
-        tradeoff = []
-        for mib, nq in ((4, 4), (8, 4), (16, 4), (32, 4), (32, 8)):
-            c5 = hoc.Comm(k, local, hoc.Config(path="ce", chunk_bytes=mib << 20, n_copy_streams=nq))
-            run = lambda s, c5=c5: c5.allgather(ag_send, recv, stream=s)
-            for _ in range(3):
-                run(stream)
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(10):
-                run(stream)
-            e1.record(stream)
-            torch.cuda.synchronize()
-            am = e0.elapsed_time(e1) / 10
-            s5 = c5.last_stats()
-            pr = probes(run, am, stream, sms)
-            tradeoff.append({"chunk_mib": mib, "copy_streams": nq, "ms": round(am, 4),
-                             "bytes_gbs": round(s5["bytes_exec"] / (am * 1e-3) / 1e9, 1), "copies_per_step": s5["copies"],
-                             "kernels_per_step": s5["kernels"],
-                             "probe_slowdown": {sh: pr[sh]["slowdown"] for sh in pr},
-                             "probe_sm_mhz_with": {sh: pr[sh]["sm_mhz_with"] for sh in pr}})
-            c5.close()
-        extras["paths"] = paths
-        extras["allgather_moves"] = ag
-        extras["allgather_ce_chunk_vs_probe"] = tradeoff
-        extras["ce_interference"] = leg_ce_interference(send, recv, n_el, k, local, stream, sms)
-        # chunk size sweep, 1-64 MiB (64 is capped at the 32 MiB block), on the copy-engine and
-        # TMA-kernel move paths; then copy-queue counts on the copy-engine path
-        sweep = []
-        grid = [(p, mib, 4, 0) for p in ("ce", "tma") for mib in (1, 2, 4, 8, 16, 32, 64)]
-        grid += [("ce", 32, 8, 0), ("ce", 8, 8, 0), ("ce", 8, 16, 0)]
-        grid += [("ce", 4, 4, d) for d in (1, 2, 4)]      # pipeline depth: reduce at most d chunks ahead of the moves
-        for p, chunk_mib, nq, depth in grid:
-            c4 = hoc.Comm(k, local, hoc.Config(path=p, chunk_bytes=chunk_mib << 20, n_copy_streams=nq,
-                                               pipeline_depth=depth))
-            for _ in range(3):
-                c4.allreduce(send, recv, stream=stream)
-            cm = time_allreduce(c4, send, recv, stream, 10)
-            s4 = c4.last_stats()
-            sweep.append({"path": p, "chunk_mib": chunk_mib, "copy_streams": nq, "pipeline_depth": depth or "unbounded",
-                          "ms": round(cm, 4),
-                          "bus_gbs": round(bus_bytes(k, per_rank) / (cm * 1e-3) / 1e9, 1),
-                          "lower_bound_frac": round(s4["bytes_min"] / (cm * 1e-3) / (peak * 1e9), 4),
-                          "copies_per_step": s4["copies"], "kernels_per_step": s4["kernels"]})
-            c4.close()
-        extras["chunk_sweep"] = sweep
-        # allreduce under an SM budget: fused (every move on the few SMs) vs copy engines (SMs only reduce);
-        # AUTO picks the copy engines when a budget is set
-        budget = []
-        for m in (8, 32):
-            for p in ("fused", "ce"):
-                c6 = hoc.Comm(k, local, hoc.Config(path=p, reduce_max_sms=m))
-                for _ in range(2):
-                    c6.allreduce(send, recv, stream=stream)
-                bm = time_allreduce(c6, send, recv, stream, 5)
-                s6 = c6.last_stats()
-                budget.append({"reduce_max_sms": m, "path": p, "ms": round(bm, 3),
-                               "bus_gbs": round(bus_bytes(k, per_rank) / (bm * 1e-3) / 1e9, 1),
-                               "sms_used": s6["sms_used"], "copies_per_step": s6["copies"]})
-                c6.close()
-        extras["allreduce_under_sm_budget"] = budget
-        extras["ce_allreduce_timeline"] = leg_ce_allreduce_timeline(send, recv, k, local, stream, per_rank, peak)
+        pm = study(leg_paths_and_moves, args, send, recv, n_el, k, local, stream, sms, peak, per_rank)
+        if "error" in pm:
+            extras["paths_and_moves"] = pm
+        else:
+            extras.update(pm)
+        extras["ce_interference"] = study(leg_ce_interference, send, recv, n_el, k, local, stream, sms)
+        extras["ce_allreduce_timeline"] = study(leg_ce_allreduce_timeline, send, recv, k, local, stream, per_rank,
+                                                peak)
     if args.workloads and not args.no_extras:
-        extras["workloads"] = {"dp_bucket_stream": leg_bucket_stream(bucket_pool, sms, peak),
-                               "pp_1f1b": leg_pipeline(sms),
-                               "ep_dispatch_combine": leg_expert_dispatch(peak)}
-        extras["workloads"]["dp_bucket_stream"]["cpu_baseline"] = cpu_baseline_buckets(bucket_pool)
+        extras["workloads"] = {"dp_bucket_stream": study(leg_bucket_stream, bucket_pool, sms, peak),
+                               "pp_1f1b": study(leg_pipeline, sms),
+                               "ep_dispatch_combine": study(leg_expert_dispatch, peak)}
+        if isinstance(extras["workloads"]["dp_bucket_stream"], dict):
+            extras["workloads"]["dp_bucket_stream"]["cpu_baseline"] = study(cpu_baseline_buckets, bucket_pool)
         bucket_pool = None
-        extras["sweeps"] = leg_sweeps(sms)
-        extras["startup_latency"] = leg_startup_latency()
-        extras["host_overhead_us"] = leg_host_overhead()
+        extras["sweeps"] = study(leg_sweeps, sms)
+        extras["startup_latency"] = study(leg_startup_latency)
+        extras["host_overhead_us"] = study(leg_host_overhead)
 
     cpu = None
     if rank == 0:
