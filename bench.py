@@ -54,7 +54,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default="auto", choices=["auto", "ce", "tma", "fused"])
     ap.add_argument("--chunk-bytes", type=int, default=0, help="0: picked by move path (4 MiB on both)")
-    ap.add_argument("--copy-streams", type=int, default=4)
+    ap.add_argument("--copy-streams", type=int, default=0, help="0: picked per call by copy size (8 or 4 queues)")
     ap.add_argument("--no-extras", action="store_true", help="skip the per-path, probe and e2e legs")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -1420,7 +1420,8 @@ def run_ours(args, world, rank, local):
                 {"workload": f"profiling case: 8 ranks x {n_el:,} bf16", "k": k, "count": n_el},
                 "schedule": {"path": args.path,
                              "resolved_path": {0: "auto", 1: "ce", 2: "tma", 3: "fused"}[st["path"]],
-                             "chunk_bytes": args.chunk_bytes or "auto (4 MiB)", "copy_streams": args.copy_streams},
+                             "chunk_bytes": args.chunk_bytes or "auto (4 MiB)",
+                             "copy_streams": args.copy_streams or "auto (8 for copies of at most 2 MiB, else 4)"},
                 "algbw_gbs": round(per_rank / (ms_max * 1e-3) / 1e9, 2),
                 "hbm_frac": round(hbm_frac, 4), "lower_bound_frac": round(lb_frac, 4),
                 "sms_used": st["sms_used"], "gpu_launches": st["kernels"] * args.steps,

@@ -517,6 +517,7 @@ hocResult_t read_cfg(const hocConfig_t* in, int k, Cfg* out) {
     c.path = in->path;
     if (in->chunk_bytes) c.chunk_bytes = in->chunk_bytes;
     if (in->n_copy_streams) c.n_copy = in->n_copy_streams;
+    else c.n_copy_auto = 1;
     c.depth = in->pipeline_depth;
     c.reduce_max_sms = in->reduce_max_sms;
     c.copy_max_sms = in->copy_max_sms;
@@ -533,7 +534,12 @@ hocResult_t read_cfg(const hocConfig_t* in, int k, Cfg* out) {
     else if (!strcmp(v, "auto")) c.path = HOC_PATH_AUTO;
   }
   if (const char* v = getenv("HOC_CHUNK_BYTES")) c.chunk_bytes = size_t(strtoull(v, nullptr, 10));
-  c.n_copy = env_int("HOC_COPY_STREAMS", c.n_copy);
+  if (!in) c.n_copy_auto = 1;
+  if (getenv("HOC_COPY_STREAMS")) {
+    c.n_copy = env_int("HOC_COPY_STREAMS", c.n_copy);
+    c.n_copy_auto = 0;
+  }
+  if (c.n_copy_auto) c.n_copy = std::max(kAutoQueuesSmall, kAutoQueuesLarge);  // streams for either choice
   c.use_graphs = env_int("HOC_USE_GRAPHS", c.use_graphs);
   c.reduce_max_sms = env_int("HOC_REDUCE_MAX_SMS", c.reduce_max_sms);
   c.copy_max_sms = env_int("HOC_COPY_MAX_SMS", c.copy_max_sms);
@@ -814,7 +820,7 @@ hocResult_t hoc_config_default(hocConfig_t* cfg) {
   memset(cfg, 0, sizeof *cfg);
   cfg->path = HOC_PATH_AUTO;
   cfg->chunk_bytes = 0;  // by move path
-  cfg->n_copy_streams = 4;
+  cfg->n_copy_streams = 0;  // the scheduler picks per call (copy_queues)
   cfg->pipeline_depth = 0;
   cfg->reduce_max_sms = 0;
   cfg->copy_max_sms = 0;

@@ -189,8 +189,15 @@ int move_path(const Cfg& cfg) { return cfg.path == HOC_PATH_TMA ? HOC_PATH_TMA :
 
 // Chunks of one flow set dealt round-robin over the copy streams (CE) or
 // gathered into one bulk-copy launch (TMA).
+// The largest copy of a chunk list (what the copy-queue count is chosen by).
+size_t largest_copy(const std::vector<Move>& chunks) {
+  size_t m = 0;
+  for (const Move& c : chunks) m = std::max(m, c.bytes);
+  return m;
+}
+
 void emit_moves(const Cfg& cfg, int path, const std::vector<Move>& chunks, int stage, const std::vector<int>& waits,
-                bool record, Plan* p, std::vector<int>* step_ids) {
+                bool record, Plan* p, std::vector<int>* step_ids, int queues) {
   if (chunks.empty()) return;
   if (path == HOC_PATH_TMA) {
     Step s;
@@ -204,7 +211,7 @@ void emit_moves(const Cfg& cfg, int path, const std::vector<Move>& chunks, int s
     p->steps.push_back(std::move(s));
     return;
   }
-  const int n = std::max(1, cfg.n_copy);
+  const int n = std::max(1, queues);
   std::vector<Step> per(n);
   for (size_t i = 0; i < chunks.size(); ++i) per[i % n].moves.push_back(chunks[i]);
   for (int q = 0; q < n; ++q) {
@@ -235,6 +242,7 @@ hocResult_t plan_allreduce(const Cfg& cfg, const CallShape& s, Plan* p) {
   }
   const size_t ce = chunk_elems(cfg, b, p->path);
   const size_t nq = (sz[0] + ce - 1) / ce;
+  const int queues = copy_queues(cfg, std::min(ce, sz[0]) * b);
   std::vector<std::vector<int>> copy_steps(nq);
   for (size_t q = 0; q < nq; ++q) {
     Step red;
@@ -260,7 +268,7 @@ hocResult_t plan_allreduce(const Cfg& cfg, const CallShape& s, Plan* p) {
       }
     const int red_id = int(p->steps.size());
     p->steps.push_back(std::move(red));
-    emit_moves(cfg, p->path, moves, int(q), {red_id}, cfg.depth > 0, p, &copy_steps[q]);
+    emit_moves(cfg, p->path, moves, int(q), {red_id}, cfg.depth > 0, p, &copy_steps[q], queues);
   }
   return HOC_SUCCESS;
 }
@@ -291,7 +299,7 @@ hocResult_t plan_allgather(const Cfg& cfg, const CallShape& s, Plan* p) {
       else split_move(m, chunk_for(cfg, HOC_PATH_CE), &chunks);
     }
   std::vector<int> ids;
-  emit_moves(cfg, p->path, chunks, 0, {}, false, p, &ids);
+  emit_moves(cfg, p->path, chunks, 0, {}, false, p, &ids, copy_queues(cfg, largest_copy(chunks)));
   if (p->path == HOC_PATH_TMA && !p->steps.empty()) p->steps.back().stream = 0;
   p->bytes_min = (size_t(k) * sc + size_t(k) * k * sc) * b;
   return HOC_SUCCESS;
@@ -328,12 +336,16 @@ hocResult_t plan_alltoall(const Cfg& cfg, const CallShape& s, Plan* p) {
         if (n) all.push_back(Move{u, v, HOC_BUF_SEND, HOC_BUF_RECV, sd[size_t(u) * k + v] * b, rd[size_t(v) * k + u] * b, n});
       }
     std::vector<int> ids;
-    emit_moves(cfg, HOC_PATH_TMA, all, 0, {}, false, p, &ids);
+    emit_moves(cfg, HOC_PATH_TMA, all, 0, {}, false, p, &ids, 1);
     if (!p->steps.empty()) p->steps.back().stream = 0;
     return HOC_SUCCESS;
   }
   // Shift stages (Eq. 6-8 with one domain): stage st holds flows u -> u+st.
   const size_t cb = chunk_for(cfg, HOC_PATH_CE);
+  size_t biggest = 0;
+  for (int a = 0; a < k; ++a)
+    for (int d = 0; d < k; ++d) biggest = std::max(biggest, std::min(cb, cnt(a, d) * b));
+  const int queues = copy_queues(cfg, biggest);
   std::vector<int> prev;
   for (int st = 0; st < k; ++st) {
     std::vector<Move> flows;
@@ -353,7 +365,7 @@ hocResult_t plan_alltoall(const Cfg& cfg, const CallShape& s, Plan* p) {
     }
     std::vector<int> ids;
     emit_moves(cfg, HOC_PATH_CE, chunks, st, cfg.a2a_stage_sync ? prev : std::vector<int>{}, cfg.a2a_stage_sync != 0,
-               p, &ids);
+               p, &ids, queues);
     if (!ids.empty()) prev = ids;
   }
   return HOC_SUCCESS;
@@ -366,7 +378,7 @@ hocResult_t plan_sendrecv(const Cfg& cfg, const CallShape& s, Plan* p) {
   if (p->path == HOC_PATH_TMA || bytes <= kSendrecvStripeBytes) chunks.push_back(m);
   else split_move(m, chunk_for(cfg, HOC_PATH_CE), &chunks);
   std::vector<int> ids;
-  emit_moves(cfg, p->path, chunks, 0, {}, false, p, &ids);
+  emit_moves(cfg, p->path, chunks, 0, {}, false, p, &ids, copy_queues(cfg, largest_copy(chunks)));
   if (p->path == HOC_PATH_TMA && !p->steps.empty()) p->steps.back().stream = 0;
   p->bytes_min = 2 * bytes;
   return HOC_SUCCESS;

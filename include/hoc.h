@@ -82,7 +82,9 @@ typedef struct {
   int path;              /* hocPath_t */
   size_t chunk_bytes;    /* pipeline unit inside a block / flow; 0 (default) picks by move path
                             (4 MiB on copy engines and on the TMA kernel, the measured best) */
-  int n_copy_streams;    /* internal copy streams (the multi-QP analogue); default 4, max 16.
+  int n_copy_streams;    /* internal copy streams (the multi-QP analogue), max 16; 0 (default):
+                            the scheduler picks per call -- 8 while every copy of the call is at
+                            most 2 MiB (small messages: per-copy startup dominates), else 4.
                             They run at the default stream priority, the lowest: a caller's
                             compute stream created with a higher priority gets its kernel
                             launches served ahead of the moves' work, which keeps the moves'

@@ -430,3 +430,26 @@ def test_chunk_count_per_span_is_bounded():
     assert e.value.code == hoc.ERR_INVALID_ARG and "chunk_bytes" in str(e.value)
     # the same size with the default chunk plans
     assert hoc.plan_query(8, hoc.OP_ALLREDUCE, n, hoc.FLOAT32, config=hoc.Config(path="fused"))
+
+
+def test_copy_queue_count_follows_copy_size_when_left_to_the_scheduler():
+    """n_copy_streams = 0: 8 copy queues while every copy of the call is at most 2 MiB, else 4; an explicit
+    count is kept whatever the size."""
+    def queues(op, count, config, counts=None):
+        items = hoc.plan_query(8, op, count, hoc.UINT8, counts=counts, config=config)
+        return {it["stream"] for it in items if it["kind"] == hoc.ITEM_COPY}
+    auto = hoc.Config(path="ce")
+    assert queues(hoc.OP_ALLGATHER, 1 << 20, auto) == set(range(1, 9))        # 1 MiB blocks: 64 small copies
+    assert queues(hoc.OP_ALLGATHER, 2 << 20, auto) == set(range(1, 9))        # exactly the threshold
+    assert queues(hoc.OP_ALLGATHER, (2 << 20) + 16, auto) == set(range(1, 5))  # past it: one 2 MiB+16 copy each
+    assert queues(hoc.OP_ALLGATHER, 32 << 20, auto) == set(range(1, 5))       # 4 MiB chunks
+    assert queues(hoc.OP_ALLGATHER, 1 << 20, hoc.Config(path="ce", n_copy_streams=4)) == set(range(1, 5))
+    assert queues(hoc.OP_ALLGATHER, 32 << 20, hoc.Config(path="ce", n_copy_streams=6)) == set(range(1, 7))
+    small = np.full((8, 8), 1 << 20, dtype=np.uint64)
+    assert queues(hoc.OP_ALLTOALL, 0, auto, small) == set(range(1, 9))
+    mixed = small.copy()
+    mixed[3, 5] = 5 << 20                                                     # one flow of 4 MiB chunks
+    assert queues(hoc.OP_ALLTOALL, 0, auto, mixed) == set(range(1, 5))
+    # the allreduce's moves: 4 MiB chunks of 32 MiB blocks stay on 4 queues
+    items = hoc.plan_query(8, hoc.OP_ALLREDUCE, 1 << 27, hoc.BFLOAT16, config=auto)
+    assert {it["stream"] for it in items if it["kind"] == hoc.ITEM_COPY} == set(range(1, 5))
