@@ -363,3 +363,59 @@ def test_pack_all_and_combine_all_match_oracle(k, tokens, hidden, experts, topk,
     for r in range(k):
         ys[r].check()
         assert np.array_equal(ys[r].host().reshape(tokens, hidden), want_y[r]), r
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_fused_and_all_rank_paths_on_random_shapes(seed, monkeypatch):
+    """Random rank counts, token counts, row widths, expert counts, topk, dropped pairs and buffer
+    offsets; both engine sets; the fused path and the all-rank pack / combine against the oracle."""
+    rng = np.random.default_rng(9100 + seed)
+    k = int(rng.choice([1, 2, 3, 5, 8, 16]))
+    per = int(rng.integers(1, 9))
+    experts = k * per
+    topk = int(rng.integers(1, min(experts, 12) + 1))
+    tokens = int(rng.integers(1, 700))
+    hidden = int(rng.choice([8, 16, 24, 40, 64, 72, 136, 520]))
+    if seed % 2:
+        monkeypatch.setenv("HOC_EP_DISPATCH", "bulk")
+        monkeypatch.setenv("HOC_EP_COMBINE", "lsu")
+    routing = [np.stack([rng.permutation(experts)[:topk] for _ in range(tokens)]) for _ in range(k)]
+    for r in range(k):                                   # a few dropped pairs
+        for _ in range(int(rng.integers(0, 4))):
+            routing[r][int(rng.integers(tokens)), int(rng.integers(topk))] = int(rng.choice([-1, experts, -7]))
+    xs = [inputs.normal_bf16(tokens * hidden, 9200 + 17 * seed + r).reshape(tokens, hidden) for r in range(k)]
+    ws = [rng.random(tokens * topk).astype(np.float32) for _ in range(k)]
+    packs, counts, want_recv, want_y = _oracle_round_trip(xs, routing, ws, experts, k, topk, hidden)
+    caps = [int(counts[:, d].sum()) + int(rng.integers(0, 3)) * hidden for d in range(k)]
+    off = int(rng.integers(0, 2))
+    recv, pos, d_counts, status, ys = _fused_on_device(k, xs, routing, ws, experts, topk, caps, off, off)
+    assert int(status.item()) == 0, (seed, k, tokens, hidden, experts, topk)
+    assert np.array_equal(d_counts.cpu().numpy(), counts)
+    for d in range(k):
+        recv[d].check()
+        assert np.array_equal(recv[d].host()[: len(want_recv[d])], want_recv[d]), (seed, d)
+    for r in range(k):
+        ys[r].check()
+        assert np.array_equal(ys[r].host().reshape(tokens, hidden), want_y[r]), (seed, r)
+    # the all-rank pack and combine, with the oracle's exchange in between
+    n = tokens * topk
+    d_ids = [torch.from_numpy(np.ascontiguousarray(rr, dtype=np.int32).reshape(-1)).cuda() for rr in routing]
+    d_x = [to_device(x, "bfloat16") for x in xs]
+    send = [torch.empty(max(1, n * hidden), dtype=torch.bfloat16, device="cuda") for _ in range(k)]
+    pos2 = [torch.empty(n, dtype=torch.int32, device="cuda") for _ in range(k)]
+    c2 = torch.empty((k, k), dtype=torch.int64, device="cuda")
+    wsp = torch.empty(k * hoc.ep_pack_workspace(tokens, topk, experts), dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hoc.ep_pack_all(d_ids, d_x, experts, send, [n * hidden] * k, pos2, c2, wsp, st)
+    torch.cuda.synchronize()
+    back_host = o_a2a.alltoallv(o_a2a.alltoallv([to_host(send[r], "bfloat16")[: len(packs[r][1]) * hidden]
+                                                 for r in range(k)], counts), o_a2a.transpose_counts(counts))
+    back = [to_device(np.concatenate([b_, np.zeros(n * hidden - len(b_), np.uint16)]) if n * hidden else
+                      np.zeros(1, np.uint16), "bfloat16") for b_ in back_host]
+    y2 = [torch.empty((tokens, hidden), dtype=torch.bfloat16, device="cuda") for _ in range(k)]
+    hoc.ep_combine_all(back, [max(1, n * hidden)] * k, pos2, [torch.from_numpy(w).cuda() for w in ws], tokens, topk,
+                       hidden, y2, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for r in range(k):
+        assert np.array_equal(to_host(y2[r], "bfloat16").reshape(tokens, hidden), want_y[r]), (seed, r)
