@@ -154,6 +154,35 @@ def test_combine_golden_cases(hidden):
             (c["name"], hidden, [hex(int(v)) for v in got.reshape(-1)])
 
 
+@pytest.mark.parametrize("hidden", [1, 8, 520])   # scalar; one vector per lane; a 1 KiB slice and a 16-byte tail
+@pytest.mark.parametrize("engine", [None, "lsu"])   # TMA-fed combine (default), vector-load combine
+def test_fused_combine_golden_cases(hidden, engine, monkeypatch):
+    """The hand-derived combine cases through the combine that reads the rows in place: one rank,
+    one expert, every row where the case puts it."""
+    from tests import pins
+    if engine:
+        monkeypatch.setenv("HOC_EP_COMBINE", engine)
+    for c in pins.load_ep_combine_cases():
+        tokens, topk = len(c["y"]), c["topk"]
+        n_rows = len(c["rows"])
+        cap = (n_rows + 2) * hidden
+        rows = np.zeros((n_rows + 2, hidden), dtype=np.uint16)
+        rows[:n_rows] = np.repeat(c["rows"], hidden, axis=1)
+        recv = torch.from_numpy(rows.view(np.int16).reshape(-1).copy()).cuda().view(torch.bfloat16)
+        ids = torch.zeros(tokens * topk, dtype=torch.int32, device="cuda")
+        pos = torch.from_numpy(c["pos_of"].astype(np.int32)).cuda()
+        counts = torch.tensor([[n_rows * hidden]], dtype=torch.int64, device="cuda")
+        w = torch.from_numpy(c["weights"].copy()).cuda()
+        y = torch.full((tokens, hidden), 7.0, dtype=torch.bfloat16, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        hoc.ep_combine_fused([recv], [cap], [ids], [pos], counts, [w], tokens, topk, hidden, 1, [y], status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0, c["name"]
+        got = y.view(torch.int16).cpu().numpy().astype(np.int64) & 0xFFFF
+        assert np.array_equal(got, np.repeat(c["y"].astype(np.int64)[:, None], hidden, axis=1)), \
+            (c["name"], hidden, engine, [hex(int(v)) for v in got.reshape(-1)[:16]])
+
+
 # ---------------------------------------------------------------- fused with the exchange
 def _oracle_round_trip(xs, routing, ws, experts, k, topk, hidden):
     """pack -> all-to-all -> (identity experts) -> inverse all-to-all -> combine, on the CPU."""

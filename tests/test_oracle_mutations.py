@@ -202,8 +202,24 @@ def _combine_unchecked_drop(rows, pos_of, weights, topk):
     return bf16.narrow(acc)
 
 
+def _combine_fused_multiply_add(rows, pos_of, weights, topk):
+    # each product added unrounded (one rounding per slot, as a fused multiply-add gives)
+    tokens = len(pos_of) // topk
+    w = np.asarray(weights, dtype=np.float32).reshape(tokens, topk).astype(np.float64)
+    pos = np.asarray(pos_of).reshape(tokens, topk)
+    acc = np.zeros((tokens, rows.shape[1]), dtype=np.float32)
+    seen = np.zeros(tokens, dtype=bool)
+    for j in range(topk):
+        ok = pos[:, j] >= 0
+        prod = w[:, j:j + 1] * bf16.widen(rows[np.where(ok, pos[:, j], 0)]).astype(np.float64)   # exact
+        summed = (acc.astype(np.float64) + prod).astype(np.float32)
+        acc = np.where((ok & seen)[:, None], summed, np.where(ok[:, None], prod.astype(np.float32), acc))
+        seen |= ok
+    return bf16.narrow(acc)
+
+
 @pytest.mark.parametrize("bad", [_combine_reverse_slots, _combine_round_every_add, _combine_ignore_weights,
-                                 _combine_drop_first_slot, _combine_unchecked_drop])
+                                 _combine_drop_first_slot, _combine_unchecked_drop, _combine_fused_multiply_add])
 def test_ep_combine_mistakes_caught(bad):
     from oracle import ep
     assert (_fails(pins.check_ep_combine_golden, bad)
