@@ -761,8 +761,10 @@ def leg_expert_dispatch(peak):
             e1.record(s)
             c.wait(s, timeout_ms=60000)
             ms = e0.elapsed_time(e1) / 5
-            # one more round with an event between its phases (all on stream s)
+            # one more round with an event between its phases (all on stream s), queued
+            # behind a spin kernel so that the host's issue time stays out of the phases
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            gpu_spin(s, 2.0)
             ev[0].record(s)
             pack_all()
             ev[1].record(s)
@@ -774,6 +776,7 @@ def leg_expert_dispatch(peak):
             ev[4].record(s)
             # the same pack and combine rank by rank (one set of launches per rank), for comparison
             ev2 = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            gpu_spin(s, 2.0)
             ev2[0].record(s)
             for r in range(k):
                 hoc.ep_pack(ids[r], xs[r], experts, k, psend[r], perm[r], pos[r], d_counts[r], wsp[r], stream=s)
@@ -834,8 +837,9 @@ def leg_expert_dispatch(peak):
     torch.cuda.synchronize()
     f_ms = e0.elapsed_time(e1) / 10
     ph = []
-    for _ in range(5):  # phases: dispatch (sort + scatter), combine
+    for _ in range(5):  # phases: dispatch (sort + scatter), combine; queued behind a spin kernel
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        gpu_spin(s, 1.0)
         ev[0].record(s)
         hoc.ep_dispatch_fused(ids_flat, xs, experts, frecv, fcap, fpos, fcounts, fws, fstatus, stream=s)
         ev[1].record(s)
@@ -857,6 +861,8 @@ def leg_expert_dispatch(peak):
         "dispatch_bytes": disp_bytes, "combine_bytes": comb_bytes,
         "dispatch_hbm_frac": round(disp_bytes / (d_ms * 1e-3) / (peak * 1e9), 4),
         "combine_hbm_frac": round(comb_bytes / (c_ms * 1e-3) / (peak * 1e9), 4),
+        "phase_timing": "events between the phases, the launches queued behind a spin kernel (host issue time "
+                        "excluded); the dispatch phase includes the sort",
         "status": int(fstatus.item()), "results_equal_copy_engine_round_trip": bool(same),
         "steps": "fused dispatch (sort of every rank's pairs, rows scattered into the receive buffers) -> "
                  "fused combine (rows read in place from the expert ranks' buffers)",
