@@ -42,7 +42,10 @@ hocResult_t hoc_ep_pack_workspace(int tokens, int topk, int experts, size_t* int
  * weights: [tokens*topk] fp32 gate weights.  y[t] = bf16 of the binary32 fold,
  * in slot order, of fp32(weights[t*topk+j] * row[pos_of[t*topk+j]]) over the
  * token's valid pairs (products and sums rounded to nearest even, no fused
- * multiply-add; +0 when no pair is valid). */
+ * multiply-add; +0 when no pair is valid).  Runs on register-fed vector loads
+ * and has no status word, so it never waits on anything; hoc_ep_combine_all
+ * (nranks = 1 for one rank) gives the same bits on the faster TMA-fed kernel,
+ * with a status word for its bounded waits and row checks. */
 hocResult_t hoc_ep_combine(const void* rows, const int32_t* pos_of, const float* weights, int tokens, int topk,
                            int hidden, void* y, void* stream);
 
