@@ -3,6 +3,10 @@
  * all-to-all (HOCCL section 2.1 and Table 1: EP token dispatch and combine are
  * all-to-all traffic).  Device pointers, stream-ordered, no host
  * synchronisation, so the counts can feed hoc_alltoall_device_counts directly.
+ * Every call here may be captured into a CUDA graph and replayed on new data
+ * in the same buffers (the sort, the counts and the row positions are
+ * recomputed on the device at each replay); make one call of each kind before
+ * the capture, so that its kernels are loaded and their attributes set.
  */
 #ifndef HOC_EP_H
 #define HOC_EP_H

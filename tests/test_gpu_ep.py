@@ -448,3 +448,90 @@ def test_fused_and_all_rank_paths_on_random_shapes(seed, monkeypatch):
     assert int(st.item()) == 0
     for r in range(k):
         assert np.array_equal(to_host(y2[r], "bfloat16").reshape(tokens, hidden), want_y[r]), (seed, r)
+
+
+def test_fused_round_trip_replays_from_a_cuda_graph():
+    """The fused dispatch and combine captured once into a CUDA graph, then replayed on other
+    routings and rows copied into the captured buffers: every replay matches the oracle of its
+    own inputs (the sort, the counts and every row position are recomputed on the device)."""
+    k, tokens, hidden, experts, topk = 8, 512, 256, 64, 6
+    cases = []
+    for seed in (0, 1, 2):
+        routing = [r.copy() for r in inputs.ep_routing(k, tokens, experts, topk, 1.1, seed_base=7000 + 100 * seed)]
+        if seed == 2:
+            routing[3][5, 2] = -1                       # a dropped pair
+        xs = [inputs.normal_bf16(tokens * hidden, 7300 + 100 * seed + r).reshape(tokens, hidden) for r in range(k)]
+        rng = np.random.default_rng(7600 + seed)
+        ws = [rng.random(tokens * topk).astype(np.float32) for _ in range(k)]
+        cases.append((routing, xs, ws, _oracle_round_trip(xs, routing, ws, experts, k, topk, hidden)[3]))
+    cap = k * tokens * topk * hidden                    # room for any routing
+    d_ids = [torch.empty(tokens * topk, dtype=torch.int32, device="cuda") for _ in range(k)]
+    d_x = [torch.empty((tokens, hidden), dtype=torch.bfloat16, device="cuda") for _ in range(k)]
+    d_w = [torch.empty(tokens * topk, dtype=torch.float32, device="cuda") for _ in range(k)]
+    recv = [torch.empty(cap, dtype=torch.bfloat16, device="cuda") for _ in range(k)]
+    pos = [torch.empty(tokens * topk, dtype=torch.int32, device="cuda") for _ in range(k)]
+    counts = torch.empty((k, k), dtype=torch.int64, device="cuda")
+    wsp = torch.empty(k * hoc.ep_pack_workspace(tokens, topk, experts), dtype=torch.int32, device="cuda")
+    status = torch.full((1,), 99, dtype=torch.int32, device="cuda")
+    ys = [torch.empty((tokens, hidden), dtype=torch.bfloat16, device="cuda") for _ in range(k)]
+    s = torch.cuda.Stream()
+
+    def load(case):
+        routing, xs, ws, _ = case
+        for r in range(k):
+            d_ids[r].copy_(torch.from_numpy(np.ascontiguousarray(routing[r], dtype=np.int32).reshape(-1)))
+            d_x[r].copy_(to_device(xs[r], "bfloat16"))
+            d_w[r].copy_(torch.from_numpy(ws[r]))
+        torch.cuda.synchronize()
+
+    def round_trip():
+        hoc.ep_dispatch_fused(d_ids, d_x, experts, recv, [cap] * k, pos, counts, wsp, status, stream=s)
+        hoc.ep_combine_fused(recv, [cap] * k, d_ids, pos, counts, d_w, tokens, topk, hidden, experts, ys, status,
+                             stream=s)
+
+    load(cases[0])
+    with torch.cuda.stream(s):
+        round_trip()                                    # first calls outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        round_trip()
+    for case in (cases[1], cases[2], cases[0]):
+        load(case)
+        for y in ys:
+            y.fill_(7.0)
+        status.fill_(99)                                # the graph clears it
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            g.replay()
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        for r in range(k):
+            assert np.array_equal(to_host(ys[r], "bfloat16").reshape(tokens, hidden), case[3][r]), r
+    # the all-rank pack and combine, with the rows left in place between them (the two exchanges of
+    # the round trip bring every row back where the pack put it): the same results
+    send = [torch.empty(tokens * topk * hidden, dtype=torch.bfloat16, device="cuda") for _ in range(k)]
+    scap = [tokens * topk * hidden] * k
+
+    def pack_combine():
+        hoc.ep_pack_all(d_ids, d_x, experts, send, scap, pos, counts, wsp, status, stream=s)
+        hoc.ep_combine_all(send, scap, pos, d_w, tokens, topk, hidden, ys, status, stream=s)
+
+    load(cases[0])
+    with torch.cuda.stream(s):
+        pack_combine()
+    torch.cuda.synchronize()
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2, stream=s):
+        pack_combine()
+    for case in (cases[2], cases[1]):
+        load(case)
+        for y in ys:
+            y.fill_(7.0)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            g2.replay()
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        for r in range(k):
+            assert np.array_equal(to_host(ys[r], "bfloat16").reshape(tokens, hidden), case[3][r]), r
