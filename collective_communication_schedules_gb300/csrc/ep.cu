@@ -148,6 +148,10 @@ __global__ void ep_tile_hist_kernel(const __grid_constant__ EpSort P, int n, int
 // that copy, and the starts go back once; otherwise the scans run in place in
 // global memory (shapes whose histograms exceed the shared budget).
 constexpr int kScanThreads = 1024;
+// Up to this many (tile, expert) histogram cells per source, each placement
+// CTA derives its own starts from the raw histograms instead of a separate scan
+// launch (at the EP workload: 12 tiles x 64 experts).
+constexpr int kPlaceScanCells = 8192;
 constexpr int kScanSmemInts = 48 * 1024 / 4 - kScanThreads;  // dynamic ints beside the static warp sums
 
 __global__ void ep_scan_kernel(const __grid_constant__ EpSort P, int tiles, int experts, int nranks, int per_rank,
@@ -218,21 +222,90 @@ __global__ void ep_scan_kernel(const __grid_constant__ EpSort P, int tiles, int 
   }
 }
 
+// Exclusive prefix sum of v[0, n) in place by the whole CTA (blockDim.x a
+// multiple of 32, at most 1024); returns the sum of all n to every thread.
+// sh: shared scratch of blockDim.x / 32 + 1 ints.
+__device__ int block_exclusive_scan(int* v, int n, int* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int per = (n + blockDim.x - 1) / blockDim.x;
+  const int e0 = min(n, int(threadIdx.x) * per), e1 = min(n, e0 + per);
+  int mine = 0;
+  for (int e = e0; e < e1; ++e) mine += v[e];
+  int incl = mine;
+  for (int off = 1; off < 32; off <<= 1) {
+    const int x = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += x;
+  }
+  if (lane == 31) sh[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int ws = lane < nwarps ? sh[lane] : 0;
+    int wi = ws;
+    for (int off = 1; off < 32; off <<= 1) {
+      const int x = __shfl_up_sync(0xFFFFFFFFu, wi, off);
+      if (lane >= off) wi += x;
+    }
+    if (lane < nwarps) sh[lane] = wi - ws;  // exclusive over warps
+    if (lane == 31) sh[nwarps] = wi;        // everything
+  }
+  __syncthreads();
+  int run = sh[warp] + incl - mine;
+  for (int e = e0; e < e1; ++e) {
+    const int c = v[e];
+    v[e] = run;
+    run += c;
+  }
+  const int all = sh[nwarps];
+  __syncthreads();
+  return all;
+}
+
 // Stable placement of one tile: a pair's row is its (tile, expert) start, plus
 // the pairs of that expert in earlier warps of the tile, earlier steps of its
 // warp and lower lanes of its step.  A warp loads all of its expert ids, and
 // later all of their starts, before the dependent counting.
 constexpr int kWarpSteps = kWarpItems / 32;
-__global__ void ep_tile_place_kernel(const __grid_constant__ EpSort P, int n, int experts, int tiles) {
+__global__ void ep_tile_place_kernel(const __grid_constant__ EpSort P, int n, int experts, int tiles, int scan_here,
+                                     int nranks, int per_rank, int hidden) {
   pdl_enter();
   const int32_t* __restrict__ ids = P.ids[blockIdx.y];
   const int32_t* __restrict__ start = P.ws + blockIdx.y * P.ws_stride + experts;
   const int32_t* __restrict__ nvalid = start + size_t(tiles) * experts;
   int32_t* __restrict__ perm = P.perm[blockIdx.y];
   int32_t* __restrict__ pos_of = P.pos_of[blockIdx.y];
-  extern __shared__ int wh[];  // [kEpWarps][experts]
+  extern __shared__ int wh[];  // [kEpWarps][experts]; with scan_here then [experts] starts, [experts] totals
+  __shared__ int scan_sh[kEpWarps + 1];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int j = threadIdx.x; j < kEpWarps * experts; j += blockDim.x) wh[j] = 0;
+  int valid_pairs = 0;
+  const int32_t* st = start + size_t(blockIdx.x) * experts;
+  if (scan_here) {  // this tile's starts from the raw tile histograms (`start` holds them)
+    int* my_start = wh + kEpWarps * experts;
+    int* tot = my_start + experts;
+    for (int e = threadIdx.x; e < experts; e += blockDim.x) {
+      int before = 0, all = 0;
+      for (int b = 0; b < tiles; ++b) {
+        const int c = start[size_t(b) * experts + e];
+        before += b < int(blockIdx.x) ? c : 0;
+        all += c;
+      }
+      my_start[e] = before;
+      tot[e] = all;
+    }
+    __syncthreads();
+    if (blockIdx.x == 0)  // one CTA per source writes its destination counts
+      for (int d = threadIdx.x; d < nranks; d += blockDim.x) {
+        unsigned long long c = 0;
+        for (int e = d * per_rank; e < (d + 1) * per_rank; ++e) c += (unsigned long long)tot[e];
+        P.counts[size_t(blockIdx.y) * nranks + d] = c * (unsigned long long)hidden;
+      }
+    valid_pairs = block_exclusive_scan(tot, experts, scan_sh);  // tot[e]: pairs of smaller experts
+    for (int e = threadIdx.x; e < experts; e += blockDim.x) my_start[e] += tot[e];
+    __syncthreads();
+    st = my_start;
+  } else {
+    valid_pairs = *nvalid;
+  }
   int* mine = wh + warp * experts;
   const int lo = blockIdx.x * kTileItems + warp * kWarpItems;
   const int hi = min(n, lo + kWarpItems);
@@ -262,7 +335,6 @@ __global__ void ep_tile_place_kernel(const __grid_constant__ EpSort P, int n, in
     }
   }
   __syncthreads();
-  const int32_t* st = start + size_t(blockIdx.x) * experts;
   int sv[kWarpSteps];
 #pragma unroll
   for (int k = 0; k < kWarpSteps; ++k) sv[k] = ev[k] >= 0 ? st[ev[k]] : 0;
@@ -282,7 +354,7 @@ __global__ void ep_tile_place_kernel(const __grid_constant__ EpSort P, int n, in
   }
   // rows past the valid pairs have no pair
   if (perm)
-    for (int r = *nvalid + blockIdx.x * blockDim.x + threadIdx.x; r < n; r += gridDim.x * blockDim.x) perm[r] = -1;
+    for (int r = valid_pairs + blockIdx.x * blockDim.x + threadIdx.x; r < n; r += gridDim.x * blockDim.x) perm[r] = -1;
 }
 
 // send[pos_of[t*topk + j]] = x[t] for every valid pair (t, j); rows of `hb`
@@ -1091,14 +1163,17 @@ cudaError_t sort_pairs(const EpSort& P, int sources, int n, int experts, int nra
     const int tiles = tiles_of(n);
     cudaError_t e = launch_pdl(ep_tile_hist_kernel, dim3(tiles, sources), kEpThreads, sizeof(int) * size_t(experts), s,
                                P, n, experts);
+    // few histogram cells: every placement CTA scans them itself (no scan launch)
+    const int scan_here = size_t(tiles) * experts <= size_t(kPlaceScanCells);
     const size_t stage_ints = size_t(experts) + size_t(tiles) * experts;
     const int staged = stage_ints <= size_t(kScanSmemInts);
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && !scan_here)
       e = launch_pdl(ep_scan_kernel, dim3(sources), kScanThreads, staged ? sizeof(int) * stage_ints : 0, s, P, tiles,
                      experts, nranks, experts / nranks, hidden, staged);
+    const size_t place_smem = sizeof(int) * (size_t(kEpWarps) + (scan_here ? 2 : 0)) * experts;
     if (e == cudaSuccess)
-      e = launch_pdl(ep_tile_place_kernel, dim3(tiles, sources), kEpThreads, sizeof(int) * size_t(kEpWarps) * experts,
-                     s, P, n, experts, tiles);
+      e = launch_pdl(ep_tile_place_kernel, dim3(tiles, sources), kEpThreads, place_smem, s, P, n, experts, tiles,
+                     scan_here, nranks, experts / nranks, hidden);
     return e;
   }
   // many experts: one CTA per (expert, source) scanning every pair of its source

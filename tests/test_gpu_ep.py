@@ -44,6 +44,8 @@ def _pack_on_device(ids, x, experts, k, stream):
     (5000, 64, True, 96, 4),      # ragged last tile, experts not a power of two
     (700, 16, False, 2048, 2),    # more than 1024 experts: the one-CTA-per-expert sort
     (3000, 16, True, 1024, 8),    # 12 tiles x 1024 experts: histograms past the shared budget, scanned in place
+    (5120, 16, True, 512, 8),     # 20 tiles x 512 experts: the separate scan, on its shared-memory copy
+    (2048, 16, True, 1024, 8),    # 8 tiles x 1024 experts: the largest histograms the placement scans itself
     (200, 24, False, 64, 10),     # topk above the combine's batched loads
     (250, 36, True, 64, 6),       # hidden not a multiple of 8: scalar combine
     (100, 16, True, 64, 40),      # topk above a warp: the scatter takes its destinations 32 at a time
