@@ -473,6 +473,29 @@ __global__ void ep_combine_vec_kernel(const uint16_t* __restrict__ rows, const i
 
 // Same fold with every one of the token's TK row loads issued before the
 // ordered fold, so a lane keeps TK 16-byte loads in flight (TK = topk).
+// Two binary32 sums per instruction (IEEE, round to nearest even, no flush
+// to zero): the same bits as two scalar sums.
+__device__ __forceinline__ unsigned long long add_f32x2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long pack_f32x2(float lo, float hi) {
+  unsigned long long d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(__float_as_uint(lo)), "r"(__float_as_uint(hi)));
+  return d;
+}
+// acc + w * x for the two bf16 values packed in q: each product rounded to
+// binary32 on its own, then both sums in one instruction.  The products stay
+// scalar on purpose: the code generator fuses a packed multiply that feeds a
+// packed add into one multiply-add, which rounds once (measured: about a
+// quarter of random operands then differ, although both instructions name
+// their rounding, and an empty statement between them did not stop it),
+// while a scalar product with its rounding named is never fused.
+__device__ __forceinline__ unsigned long long mul_add_bf16x2(unsigned long long acc, float w, uint32_t q) {
+  return add_f32x2(acc, pack_f32x2(__fmul_rn(w, __uint_as_float(q << 16)), __fmul_rn(w, __uint_as_float(q & 0xFFFF0000u))));
+}
+
 template <int TK>
 __global__ void ep_combine_vec_ilp_kernel(const uint16_t* __restrict__ rows, const int32_t* __restrict__ pos_of,
                                           const float* __restrict__ w, int tokens, int hidden, int n_rows,
@@ -480,14 +503,20 @@ __global__ void ep_combine_vec_ilp_kernel(const uint16_t* __restrict__ rows, con
   pdl_enter();
   // Work item = (token, slice of 32 16-byte vectors of its row): many small
   // items spread evenly over the warps, so no partial last wave of whole rows.
+  // A warp walks its items as (token, slice), moved on by the grid's warps at
+  // a time in that mixed radix (no division per item).
   const int lane = threadIdx.x & 31;
   const int hv = hidden / 8;
-  const int slices = (hv + 31) / 32;
+  const uint32_t slices = uint32_t(hv + 31) / 32;
   const long long items = (long long)tokens * slices;
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-  for (long long it = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items; it += warps) {
-    const int t = int(it / slices);
-    const int v = int(it % slices) * 32 + lane;
+  const long long first = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  long long t = first / slices;
+  uint32_t sl = uint32_t(first - t * slices);
+  const long long dt = warps / slices;
+  const uint32_t dsl = uint32_t(warps - dt * slices);
+  for (long long it = first; it < items; it += warps) {
+    const int v = int(sl) * 32 + lane;
     const int pl = lane < TK ? pos_of[size_t(t) * TK + lane] : -1;
     const float wl = lane < TK ? w[size_t(t) * TK + lane] : 0.f;
     int p[TK];
@@ -499,34 +528,36 @@ __global__ void ep_combine_vec_ilp_kernel(const uint16_t* __restrict__ rows, con
       wj[j] = __shfl_sync(0xFFFFFFFFu, wl, j);
       ok[j] = p[j] >= 0 && p[j] < n_rows && v < hv;
     }
+    const long long tt = t;
+    sl += dsl;  // the warp's next item
+    t += dt + (sl >= slices);
+    if (sl >= slices) sl -= slices;
     if (v >= hv) continue;
     uint4 x[TK];
 #pragma unroll
     for (int j = 0; j < TK; ++j)
       x[j] = ok[j] ? __ldg(reinterpret_cast<const uint4*>(rows + size_t(p[j]) * hidden) + v) : make_uint4(0, 0, 0, 0);
-    float acc[8];
+    unsigned long long acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = 0x8000000080000000ull;  // -0 in both lanes: x + -0 = x
     bool any = false;
 #pragma unroll
     for (int j = 0; j < TK; ++j) {
       if (!ok[j]) continue;
       const uint32_t q[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float lo = __fmul_rn(wj[j], __uint_as_float(q[i] << 16));
-        const float hi = __fmul_rn(wj[j], __uint_as_float(q[i] & 0xFFFF0000u));
-        acc[2 * i] = any ? __fadd_rn(acc[2 * i], lo) : lo;
-        acc[2 * i + 1] = any ? __fadd_rn(acc[2 * i + 1], hi) : hi;
-      }
+      for (int i = 0; i < 4; ++i) acc[i] = mul_add_bf16x2(acc[i], wj[j], q[i]);
       any = true;
     }
     uint32_t o[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float a = any ? acc[2 * i] : 0.f, b = any ? acc[2 * i + 1] : 0.f;
+      const float a = any ? __uint_as_float(uint32_t(acc[i])) : 0.f;
+      const float b = any ? __uint_as_float(uint32_t(acc[i] >> 32)) : 0.f;
       o[i] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
              (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
     }
-    reinterpret_cast<uint4*>(y + size_t(t) * hidden)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+    reinterpret_cast<uint4*>(y + size_t(tt) * hidden)[v] = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -862,29 +893,6 @@ __global__ void ep_combine_fused_vec_kernel(const __grid_constant__ EpRoute R) {
     for (int q = 0; q < kCombVecs; ++q)
       if (v0 + 32 * q < hv) y[v0 + 32 * q] = narrow_bf16x8(acc[q], any);
   }
-}
-
-// Two binary32 sums per instruction (IEEE, round to nearest even, no flush
-// to zero): the same bits as two scalar sums.
-__device__ __forceinline__ unsigned long long add_f32x2(unsigned long long a, unsigned long long b) {
-  unsigned long long d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ unsigned long long pack_f32x2(float lo, float hi) {
-  unsigned long long d;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(__float_as_uint(lo)), "r"(__float_as_uint(hi)));
-  return d;
-}
-// acc + w * x for the two bf16 values packed in q: each product rounded to
-// binary32 on its own, then both sums in one instruction.  The products stay
-// scalar on purpose: the code generator fuses a packed multiply that feeds a
-// packed add into one multiply-add, which rounds once (measured: about a
-// quarter of random operands then differ, although both instructions name
-// their rounding, and an empty statement between them did not stop it),
-// while a scalar product with its rounding named is never fused.
-__device__ __forceinline__ unsigned long long mul_add_bf16x2(unsigned long long acc, float w, uint32_t q) {
-  return add_f32x2(acc, pack_f32x2(__fmul_rn(w, __uint_as_float(q << 16)), __fmul_rn(w, __uint_as_float(q & 0xFFFF0000u))));
 }
 
 // Combine fed by the tensor-memory accelerator.  Each warp owns two
