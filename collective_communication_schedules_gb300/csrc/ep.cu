@@ -578,6 +578,11 @@ struct EpRoute {
                     // bit 2: a bounded wait of a bulk-copy kernel gave up
   int k, tokens, topk, hidden, per_rank;
   int packed;  // 1: each source's own buffer buf[s], rows in its packed order (no exchange to fuse)
+  // bulk-copy kernels: the limit of each mbarrier wait, and bytes every
+  // mbarrier expects beyond its loads (0; 16 under HOC_FAULT=ep_stall, so no
+  // wait completes and the timeout path runs with no fault on the GPU)
+  unsigned long long wait_ns;
+  uint32_t tx_pad;
 };
 
 // base[s * k + d] = rdispl[d][s] - sdispl[s][d] in rows: packed row i of source
@@ -727,7 +732,7 @@ __global__ void __launch_bounds__(32) ep_dispatch_bulk_kernel(const __grid_const
     uint32_t off, n;
     locate(nload, s, t, off, n);
     uint64_t* b = &bar[nload % kBulkStages];
-    mbar_arrive_expect_tx(b, n);
+    mbar_arrive_expect_tx(b, n + R.tx_pad);
     bulk_load(stage_mem + size_t(nload % kBulkStages) * kBulkPiece, R.x[s] + size_t(t) * hb + off, n, b);
     ++nload;
   };
@@ -758,7 +763,7 @@ __global__ void __launch_bounds__(32) ep_dispatch_bulk_kernel(const __grid_const
       const uint64_t b1 = mine < b0 + kBulkBatch ? mine : b0 + kBulkBatch;
       for (uint64_t it = b0; it < b1; ++it) {
         const int st = int(it % kBulkStages);
-        if (!mbar_wait_bounded(&bar[st], uint32_t(it / kBulkStages) & 1u, global_ns() + kBulkWaitNs)) {
+        if (!mbar_wait_bounded(&bar[st], uint32_t(it / kBulkStages) & 1u, global_ns() + R.wait_ns)) {
           failed = true;
           break;
         }
@@ -780,7 +785,7 @@ __global__ void __launch_bounds__(32) ep_dispatch_bulk_kernel(const __grid_const
   if (lane == 0) {
     if (failed) {
       atomicOr(R.status, 4);
-      const uint64_t deadline = global_ns() + kBulkWaitNs;
+      const uint64_t deadline = global_ns() + R.wait_ns;
       for (uint64_t b = nstore; b < nload; ++b)
         if (!mbar_wait_bounded(&bar[b % kBulkStages], uint32_t(b / kBulkStages) & 1u, deadline)) break;
     }
@@ -985,7 +990,7 @@ __global__ void __launch_bounds__(32 * kCombWarps) ep_combine_bulk_kernel(const 
     }
     I.valid = __ballot_sync(0xFFFFFFFFu, src != nullptr);
     uint64_t* b = &bar[warp][st];
-    if (lane == 0) mbar_arrive_expect_tx(b, uint32_t(__popc(I.valid)) * I.n);
+    if (lane == 0) mbar_arrive_expect_tx(b, uint32_t(__popc(I.valid)) * I.n + R.tx_pad);
     __syncwarp();
     if (src) bulk_load(stages + size_t(st) * stage_bytes + size_t(lane) * slice, src, I.n, b);
   };
@@ -1010,7 +1015,7 @@ __global__ void __launch_bounds__(32 * kCombWarps) ep_combine_bulk_kernel(const 
     }
     // every lane waits for the stage itself before reading what the bulk loads wrote
     const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bar[warp][st], uint32_t(i >> 1) & 1u,
-                                                              global_ns() + kBulkWaitNs));
+                                                              global_ns() + R.wait_ns));
     if (!ok) {
       failed = true;
       break;
@@ -1051,7 +1056,7 @@ __global__ void __launch_bounds__(32 * kCombWarps) ep_combine_bulk_kernel(const 
   }
   if (failed && lane == 0) {
     atomicOr(R.status, 4);
-    const uint64_t deadline = global_ns() + kBulkWaitNs;
+    const uint64_t deadline = global_ns() + R.wait_ns;
     for (uint64_t b = done; b < issued; ++b)  // the loads still in flight: bounded again
       if (!mbar_wait_bounded(&bar[warp][b & 1], uint32_t(b >> 1) & 1u, deadline)) break;
   }
@@ -1313,6 +1318,16 @@ extern "C" hocResult_t hoc_ep_combine(const void* rows, const int32_t* pos_of, c
 namespace hoc {
 namespace {
 
+// Bounded waits of the bulk-copy kernels: 2 s, or with HOC_FAULT=ep_stall
+// (host-side fault injection, as for the communicator's TMA moves) 0.1 s with
+// every mbarrier expecting 16 bytes more than its loads bring.
+void set_bulk_waits(EpRoute& R) {
+  const char* fault = getenv("HOC_FAULT");
+  const bool stall = fault && !strcmp(fault, "ep_stall");
+  R.tx_pad = stall ? 16u : 0u;
+  R.wait_ns = stall ? 100000000ull : kBulkWaitNs;
+}
+
 // Sort of every source's pairs, then the row scatter: into the destination
 // ranks' receive buffers (packed = 0, the dispatch fused with the exchange) or
 // into each source's own send buffer in packed order (packed = 1).
@@ -1374,6 +1389,7 @@ hocResult_t dispatch_ranks(const char* who, int packed, int nranks, const int32_
   R.hidden = hidden;
   R.per_rank = experts / nranks;
   R.packed = packed;
+  set_bulk_waits(R);
   const int hb = hidden * 2;
   // Row scatter: per-thread vector copies; with HOC_EP_DISPATCH=bulk (rows and
   // buffers aligned, topk <= 16) bulk copies through shared memory instead --
@@ -1448,6 +1464,7 @@ hocResult_t combine_ranks(const char* who, int packed, int nranks, const void* c
   R.hidden = hidden;
   R.per_rank = experts / nranks;
   R.packed = packed;
+  set_bulk_waits(R);
   cudaError_t e;
   // Rows through shared memory by TMA bulk copies where shapes allow (the
   // default), else (or with HOC_EP_COMBINE=lsu) per-thread vector loads.

@@ -537,3 +537,55 @@ def test_fused_round_trip_replays_from_a_cuda_graph():
         assert int(status.item()) == 0
         for r in range(k):
             assert np.array_equal(to_host(ys[r], "bfloat16").reshape(tokens, hidden), case[3][r]), r
+
+
+@pytest.mark.parametrize("stage", ["dispatch", "combine"])
+def test_bulk_copy_waits_give_up_into_the_status_word(stage, monkeypatch):
+    """HOC_FAULT=ep_stall (injected on the host): every mbarrier of the TMA bulk-copy dispatch or
+    combine expects 16 bytes more than its loads bring, so no wait completes; each gives up after
+    its 0.1 s limit, sets status bit 2 and drains its own loads, and the next call is exact."""
+    k, tokens, hidden, experts, topk = 4, 300, 64, 32, 4
+    routing = inputs.ep_routing(k, tokens, experts, topk, 1.1, seed_base=7900)
+    xs = [inputs.normal_bf16(tokens * hidden, 7950 + r).reshape(tokens, hidden) for r in range(k)]
+    rng = np.random.default_rng(7990)
+    ws = [rng.random(tokens * topk).astype(np.float32) for _ in range(k)]
+    packs, counts, want_recv, want_y = _oracle_round_trip(xs, routing, ws, experts, k, topk, hidden)
+    caps = [int(counts[:, d].sum()) for d in range(k)]
+    monkeypatch.setenv("HOC_EP_DISPATCH", "bulk")      # the dispatch's bulk-copy engine (the combine's is the default)
+    d_ids = [torch.from_numpy(np.ascontiguousarray(r, dtype=np.int32).reshape(-1)).cuda() for r in routing]
+    d_x = [to_device(x, "bfloat16") for x in xs]
+    d_w = [torch.from_numpy(x).cuda() for x in ws]
+    recv = [torch.zeros(c, dtype=torch.bfloat16, device="cuda") for c in caps]
+    pos = [torch.empty(tokens * topk, dtype=torch.int32, device="cuda") for _ in range(k)]
+    d_counts = torch.empty((k, k), dtype=torch.int64, device="cuda")
+    wsp = torch.empty(k * hoc.ep_pack_workspace(tokens, topk, experts), dtype=torch.int32, device="cuda")
+    ys = [torch.zeros((tokens, hidden), dtype=torch.bfloat16, device="cuda") for _ in range(k)]
+
+    def dispatch(status):
+        hoc.ep_dispatch_fused(d_ids, d_x, experts, recv, caps, pos, d_counts, wsp, status)
+
+    def combine(status):
+        hoc.ep_combine_fused(recv, caps, d_ids, pos, d_counts, d_w, tokens, topk, hidden, experts, ys, status)
+
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if stage == "dispatch":
+        monkeypatch.setenv("HOC_FAULT", "ep_stall")
+        dispatch(status)
+    else:
+        dispatch(status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        monkeypatch.setenv("HOC_FAULT", "ep_stall")
+        combine(status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 4, int(status.item())
+    monkeypatch.delenv("HOC_FAULT")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dispatch(status)
+    combine(status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for d in range(k):
+        assert np.array_equal(to_host(recv[d], "bfloat16"), want_recv[d]), d
+    for r in range(k):
+        assert np.array_equal(to_host(ys[r], "bfloat16").reshape(tokens, hidden), want_y[r]), r
