@@ -349,7 +349,7 @@ PROBE_KERNELS = 40          # the probe is a train of one-wave kernels, ~0.25 ms
 
 
 def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int, shape: str = "whole_sm", n_kernels: int = 0,
-                   priority: int = 0, graph: bool = False):
+                   priority: int = 0, graph: bool = False, pdl: bool = False):
     """Slowdown of the FMA probe train while the collective runs back to back beside it.
 
     The probe is a train of short one-wave kernels, like a sequence of layer
@@ -357,7 +357,9 @@ def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int, shape: str = "w
     whichever kernel launched first, so a collective that needs SMs takes them
     from the probe, and one that needs none (copy engines) leaves it alone.
     `priority`: the probe stream's priority (lower is higher, as for CUDA);
-    `graph`: the train is captured once into a CUDA graph and replayed.
+    `graph`: the train is captured once into a CUDA graph and replayed;
+    `pdl`: each probe kernel is launched with programmatic dependent launch
+    (it waits for the one before it, only the launch overlaps).
     """
     import torch
 
@@ -378,7 +380,7 @@ def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int, shape: str = "w
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=sp):
                 for _ in range(nk):
-                    hoc.probe_launch(ctas, threads, iters, stream=sp, whole_sm=whole, sink=sink)
+                    hoc.probe_launch(ctas, threads, iters, stream=sp, whole_sm=whole, sink=sink, pdl=pdl)
             trains[iters] = g
             torch.cuda.synchronize()
 
@@ -388,7 +390,7 @@ def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int, shape: str = "w
                 trains[iters].replay()
         else:
             for _ in range(nk):
-                hoc.probe_launch(ctas, threads, iters, stream=sp, whole_sm=whole, sink=sink)
+                hoc.probe_launch(ctas, threads, iters, stream=sp, whole_sm=whole, sink=sink, pdl=pdl)
 
     def run_probe(iters, with_coll=False, n_coll=0):
         capture(iters)
@@ -419,15 +421,16 @@ def probe_slowdown(run_coll, coll_ms: float, stream_c, sms: int, shape: str = "w
     n_coll = int(math.ceil(1.5 * alone / max(coll_ms, 1e-3))) + 2
     with_c = statistics.median(run_probe(iters, True, n_coll) for _ in range(3))
     mhz_with = [m for m in mhz if m]
-    return {"shape": f"{nk} kernels x {ctas} CTAs x {threads} threads" + (", whole SM each" if whole else ""),
+    return {"shape": f"{nk} kernels x {ctas} CTAs x {threads} threads" + (", whole SM each" if whole else "")
+                     + (", programmatic dependent launches" if pdl else ""),
             "probe_alone_ms": round(alone, 3), "probe_with_ms": round(with_c, 3),
             "slowdown": round(with_c / alone - 1.0, 4), "collectives_beside": n_coll,
             "sm_mhz_alone": round(statistics.median(mhz_alone), 1) if mhz_alone else None,
             "sm_mhz_with": round(statistics.median(mhz_with), 1) if mhz_with else None}
 
 
-def probes(run_coll, coll_ms, stream_c, sms, n_kernels=0, priority=0, graph=False):
-    return {shape: probe_slowdown(run_coll, coll_ms, stream_c, sms, shape, n_kernels, priority, graph)
+def probes(run_coll, coll_ms, stream_c, sms, n_kernels=0, priority=0, graph=False, pdl=False):
+    return {shape: probe_slowdown(run_coll, coll_ms, stream_c, sms, shape, n_kernels, priority, graph, pdl)
             for shape in PROBE_SHAPES}
 
 
@@ -1199,7 +1202,10 @@ def leg_paths_and_moves(args, send, recv, n_el, k, local, stream, sms, peak, per
                  "probe": probes(run, am, stream, sms),
                  # the same probe train on a stream of the highest priority (the moves' streams keep
                  # the default, lowest one): compute first wherever the GPU arbitrates between streams
-                 "probe_high_priority": probes(run, am, stream, sms, priority=-100)}
+                 "probe_high_priority": probes(run, am, stream, sms, priority=-100),
+                 # the same train at default priority, each kernel launched with programmatic dependent
+                 # launch: the launch overlaps the kernel before it
+                 "probe_pdl": probes(run, am, stream, sms, pdl=True)}
         c3.close()
     # copy-engine chunk size against interference: larger copies move faster but slow the probe more
     tradeoff = []

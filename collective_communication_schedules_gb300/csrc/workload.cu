@@ -26,7 +26,8 @@ __device__ __forceinline__ void report_clock(float* sink, long long c0, uint64_t
 // clock report.  The chains' result is stored only if it equals a sentinel
 // the chains cannot reach (their values stay in (0, 1]), which keeps the
 // compiler from removing the work.
-__global__ void probe_kernel(int iters, float* sink) {
+__global__ void probe_kernel(int iters, float* sink, int pdl) {
+  if (pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
   const long long c0 = clock64();
   const uint64_t t0 = gtimer();
   float a[8];
@@ -49,7 +50,8 @@ __global__ void probe_kernel(int iters, float* sink) {
 // other kernel's CTA can share the SM while one of these runs -- the
 // footprint of a GEMM tile.
 constexpr int kWideChains = 48;
-__global__ void __launch_bounds__(1024, 1) probe_wide_kernel(int iters, float* sink) {
+__global__ void __launch_bounds__(1024, 1) probe_wide_kernel(int iters, float* sink, int pdl) {
+  if (pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
   const long long c0 = clock64();
   const uint64_t t0 = gtimer();
   float a[kWideChains];
@@ -103,13 +105,40 @@ cudaError_t workload_preload() {
 
 }  // namespace hoc
 
-extern "C" hocResult_t hoc_probe_launch(void* stream, int ctas, int threads, int iters, int whole_sm, float* sink) {
+namespace hoc {
+namespace {
+
+// Launch with programmatic dependent launch allowed when `pdl`: the probe
+// kernel waits (griddepcontrol.wait) for the previous kernel on the stream to
+// finish before its FMA work, so only the launch itself overlaps.
+template <typename... Args>
+cudaError_t probe_start(void (*kernel)(Args...), int ctas, int threads, size_t smem, cudaStream_t s, bool pdl,
+                        Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+}  // namespace
+}  // namespace hoc
+
+extern "C" hocResult_t hoc_probe_launch(void* stream, int ctas, int threads, int iters, int flags, float* sink) {
   if (ctas < 1 || threads < 32 || threads > 1024 || (threads % 32) != 0 || iters < 0) return HOC_ERR_INVALID_ARG;
+  if (flags & ~(HOC_PROBE_WHOLE_SM | HOC_PROBE_PDL)) return HOC_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (!whole_sm) {
-    hoc::probe_kernel<<<ctas, threads, 0, s>>>(iters, sink);
-    return cudaGetLastError() == cudaSuccess ? HOC_SUCCESS : HOC_ERR_CUDA;
-  }
+  const bool pdl = (flags & HOC_PROBE_PDL) != 0;
+  if (!(flags & HOC_PROBE_WHOLE_SM))
+    return hoc::probe_start(hoc::probe_kernel, ctas, threads, 0, s, pdl, iters, sink, int(pdl)) == cudaSuccess
+               ? HOC_SUCCESS
+               : HOC_ERR_CUDA;
   if (threads != 1024) return HOC_ERR_INVALID_ARG;
   int dev = 0, smem = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -119,8 +148,10 @@ extern "C" hocResult_t hoc_probe_launch(void* stream, int ctas, int threads, int
   if (cudaFuncSetAttribute(reinterpret_cast<const void*>(&hoc::probe_wide_kernel),
                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return HOC_ERR_CUDA;
-  hoc::probe_wide_kernel<<<ctas, 1024, size_t(smem), s>>>(iters, sink);
-  return cudaGetLastError() == cudaSuccess ? HOC_SUCCESS : HOC_ERR_CUDA;
+  return hoc::probe_start(hoc::probe_wide_kernel, ctas, 1024, size_t(smem), s, pdl, iters, sink, int(pdl)) ==
+                 cudaSuccess
+             ? HOC_SUCCESS
+             : HOC_ERR_CUDA;
 }
 
 extern "C" hocResult_t hoc_xor16_launch(void* stream, const uint16_t* in, uint16_t* out, size_t n, uint16_t key) {

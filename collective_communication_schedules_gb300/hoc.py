@@ -426,8 +426,13 @@ class Comm:
 
 
 # ---------------------------------------------------------------- workload
-def probe_launch(ctas: int, threads: int, iters: int, sink=None, stream=None, whole_sm: bool = False):
-    _check(lib().hoc_probe_launch(_stream(stream), int(ctas), int(threads), int(iters), int(bool(whole_sm)),
+PROBE_WHOLE_SM, PROBE_PDL = 1, 2
+
+
+def probe_launch(ctas: int, threads: int, iters: int, sink=None, stream=None, whole_sm: bool = False,
+                 pdl: bool = False):
+    flags = (PROBE_WHOLE_SM if whole_sm else 0) | (PROBE_PDL if pdl else 0)
+    _check(lib().hoc_probe_launch(_stream(stream), int(ctas), int(threads), int(iters), flags,
                                   None if sink is None else _ptr(sink, 12, "sink")), "hoc_probe_launch")
 
 

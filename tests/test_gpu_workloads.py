@@ -193,3 +193,20 @@ def test_expert_dispatch_combine_workload(ep_data, path, interleave):
             assert_bits_equal(to_host(rv[d], "bfloat16"), want[d], "bfloat16", f"dispatch dst {d}")
         for s in range(k):
             assert torch.equal(back[s].view(torch.int16), sd[s].view(torch.int16)), f"combine src {s}"
+
+
+@pytest.mark.parametrize("whole_sm", [False, True])
+def test_probe_launch_flags(whole_sm):
+    """The FMA probe with and without programmatic dependent launch: a train of each runs and
+    reports the clock it ran at; a flag bit the call does not know is refused."""
+    sms = hoc.sm_count()
+    threads = 1024 if whole_sm else 256
+    s = torch.cuda.Stream()
+    for pdl in (False, True):
+        sink = torch.zeros(4, dtype=torch.float32, device="cuda")
+        for _ in range(3):
+            hoc.probe_launch(sms, threads, 2000, sink=sink, stream=s, whole_sm=whole_sm, pdl=pdl)
+        torch.cuda.synchronize()
+        cyc, ns = float(sink[0]), float(sink[1])
+        assert cyc > 0 and ns > 0 and 500 < 1e3 * cyc / ns < 3000, (pdl, cyc, ns)   # MHz
+    assert hoc.lib().hoc_probe_launch(s.cuda_stream, 1, 32, 1, 4, None) == hoc.ERR_INVALID_ARG
