@@ -31,7 +31,10 @@ namespace {
 // Pieces in flight per CTA (one CTA per SM, 192 KiB of shared memory).  Measured on GB300: the
 // all-gather moves of 8 x 32 MiB blocks run at 5.93-5.96 TB/s with 4, 6 or 8 stages alike, and the
 // TMA allreduce, whose moves interleave with the reduce kernels, takes 0.679 ms with 6 stages
-// against 0.695 with 4 (3 stages on two CTAs per SM: 0.685; 8 x 16 KiB: 0.714).
+// against 0.695 with 4 (3 stages on two CTAs per SM: 0.685; 8 x 16 KiB: 0.714).  Neither 2-3 CTAs
+// per SM (2-4 stages of 16-32 KiB each) nor 2-3 store groups in flight moved the all-gather or a
+// 1-SM copy, which stays at about 52 GB/s: one SM writes at most about 63 GB/s, by bulk stores or
+// by plain 16-byte stores alike.
 constexpr int kStages = 6;
 constexpr uint32_t kPieceBytes = 32768;
 constexpr int kCopyThreads = 64;
