@@ -441,3 +441,35 @@ def check_ep_combine_error_bound(pack, combine, rng):
     mag = (np.abs(w) * np.abs(rows)).sum(axis=1)
     bound = 2.0 ** -8 * np.abs(s) + (topk + 1) * 2.0 ** -24 * mag * (1 + 2.0 ** -8)
     assert np.all(np.abs(y - s) <= bound + 1e-30)
+
+
+def random_two_domain_topology(rng):
+    """G GPUs in n nodes of equal size (2 or more GPUs each), peers paired within each node."""
+    n_nodes = int(rng.choice([2, 3, 4]))
+    per = int(rng.choice([2, 4]))
+    G = n_nodes * per
+    node_of = [u // per for u in range(G)]
+    sym = [u ^ 1 for u in range(G)]                 # consecutive pairs, always inside one node
+    C = [[0 if u == v else int(rng.integers(0, 40)) * int(rng.integers(0, 2)) for v in range(G)] for u in range(G)]
+    return C, node_of, sym
+
+
+def check_traffic_matrix_by_flows(traffic_matrix, rng, trials=40):
+    """Eqs. 2-5 by brute force: route every flow of the origin matrix on its own and add up what each
+    GPU pair carries.  A flow inside a node is one NVLink transfer u -> v; a flow between nodes is the
+    sender's copy u -> sym[u], the RDMA transfer u -> v (accounted at cell (u, v)) and the receiver's
+    copy sym[v] -> v."""
+    for _ in range(trials):
+        C, node_of, sym = random_two_domain_topology(rng)
+        G = len(C)
+        load = [[0] * G for _ in range(G)]
+        for u in range(G):
+            for v in range(G):
+                f = C[u][v]
+                if u == v or f == 0:
+                    continue
+                load[u][v] += f
+                if node_of[u] != node_of[v]:
+                    load[u][sym[u]] += f
+                    load[sym[v]][v] += f
+        assert traffic_matrix(C, node_of, sym) == load, (C, node_of, sym)

@@ -140,6 +140,35 @@ def test_topo_wrong_forwarding_cell_caught():
     assert T[0][1] != tt.f(1, 2, 3, 8, 11)
 
 
+def _traffic_receiver_copy_reversed(C, node_of, sym):
+    # the receiver-side forwarding copy counted v -> sym[v] instead of sym[v] -> v
+    from oracle import topo
+    G = len(C)
+    inter, _ = topo.domains(node_of)
+    T = [row[:] for row in C]
+    for u in range(G):
+        for v in range(G):
+            if (u, v) in inter and C[u][v]:
+                T[u][sym[u]] += C[u][v]
+                T[v][sym[v]] += C[u][v]
+    return T
+
+
+def _traffic_no_receiver_copy(C, node_of, sym):
+    from oracle import topo
+    G = len(C)
+    inter, _ = topo.domains(node_of)
+    T = [row[:] for row in C]
+    for u in range(G):
+        T[u][sym[u]] += sum(C[u][v] for v in range(G) if (u, v) in inter)
+    return T
+
+
+@pytest.mark.parametrize("bad", [_traffic_receiver_copy_reversed, _traffic_no_receiver_copy])
+def test_topo_traffic_matrix_mistakes_caught(bad):
+    assert _fails(pins.check_traffic_matrix_by_flows, bad, np.random.default_rng(11))
+
+
 def test_topo_dropped_degree_constraint_caught():
     import numpy as np
     from oracle import topo

@@ -46,6 +46,11 @@ def test_eq5_worked_example():
             assert T[u][v] == f(i)
 
 
+def test_traffic_matrix_by_flows():
+    from tests import pins
+    pins.check_traffic_matrix_by_flows(topo.traffic_matrix, np.random.default_rng(11))
+
+
 def _check_invariants(C, nodes, sym, T, stages):
     G = len(C)
     # Eq. 7: the stages sum to T element-wise
