@@ -4,9 +4,10 @@
 // with round to nearest even, bf16 rounded once at the end; int32 modulo 2^32)
 // and the same segments, but the bytes move by bulk asynchronous copies
 // instead of per-thread loads and stores:
-//   * one producer thread per CTA streams the k operand tiles of a work tile
-//     (tile_bytes each, operand j = ring position j) into a shared-memory
-//     stage with cp.async.bulk, completing on that stage's "full" mbarrier;
+//   * one producer warp per CTA streams the k operand tiles of a work tile
+//     (tile_bytes each, operand j = ring position j, issued by lane j) into
+//     a shared-memory stage with cp.async.bulk, completing on that stage's
+//     "full" mbarrier;
 //   * eight consumer warps fold the k tiles vector by vector from shared
 //     memory, store each folded 16-byte vector straight to the owner's buffer
 //     (or to all k buffers: the fused allreduce, with streaming stores), and
@@ -263,42 +264,53 @@ __global__ void __launch_bounds__(kThreadsT, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
-    if (lane != 0) return;
+    // The whole warp: every lane waits for the stage to be free, lane 0 sets
+    // the stage's expected bytes, and lane j < k issues operand j's bulk load,
+    // so the k loads of a stage go out in parallel (one thread issuing them
+    // one after another was what bounded this kernel under an SM budget).
     uint64_t issued = 0;
     for (uint64_t it = 0; it < mine; ++it) {
       const int s = int(it % stages);
-      if (it >= uint64_t(stages) &&
-          !mbar_wait_bounded(&empty[s], uint32_t((it / stages - 1) & 1), global_ns() + wait_ns)) {
-        atomicExch(status, kStatusTimeoutLoad);
-        atomicExch(&abort_flag, 1);
+      bool ok = true;
+      if (it >= uint64_t(stages))
+        ok = mbar_wait_bounded(&empty[s], uint32_t((it / stages - 1) & 1), global_ns() + wait_ns);
+      if (!__all_sync(0xFFFFFFFFu, ok)) {
+        if (lane == 0) {
+          atomicExch(status, kStatusTimeoutLoad);
+          atomicExch(&abort_flag, 1);
+        }
         break;
       }
-      if (*(volatile int*)&abort_flag) break;
+      if (__any_sync(0xFFFFFFFFu, *(volatile int*)&abort_flag != 0)) break;
       const TileRef tr = tile_of(p, blockIdx.x + it * gridDim.x);
       const ReduceSeg& sg = p.seg[tr.seg];
       uint64_t e0, off;
       uint32_t n;
       tile_body(p, sg, tr.local, tile_bytes, e0, off, n);
       if (n == 0) {
-        mbar_arrive(&full[s]);  // nothing to load (a segment shorter than one vector)
+        if (lane == 0) mbar_arrive(&full[s]);  // nothing to load (a segment shorter than one vector)
       } else {
-        mbar_arrive_expect_tx(&full[s], n * uint32_t(k));
-        const uint8_t* seq = p.seq[sg.owner];
-        const uint64_t gb = (sg.elem_off + e0) * eb + off;
-        for (int j = 0; j < k; ++j)
-          bulk_load(smem + size_t(s) * stage_bytes + size_t(j) * tile_bytes,
-                   static_cast<const char*>(p.in[seq[j]]) + gb, n, &full[s]);
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], n * uint32_t(k));
+        __syncwarp();
+        if (lane < k) {
+          const uint8_t* seq = p.seq[sg.owner];
+          const uint64_t gb = (sg.elem_off + e0) * eb + off;
+          bulk_load(smem + size_t(s) * stage_bytes + size_t(lane) * tile_bytes,
+                    static_cast<const char*>(p.in[seq[lane]]) + gb, n, &full[s]);
+        }
       }
       issued = it + 1;
     }
     // Do not leave while loads still target this CTA's shared memory.
-    const uint64_t first = issued > uint64_t(stages) ? issued - stages : 0;
-    const uint64_t deadline = global_ns() + wait_ns;
-    for (uint64_t it = first; it < issued; ++it)
-      if (!mbar_wait_bounded(&full[it % stages], uint32_t((it / stages) & 1), deadline)) {
-        atomicExch(status, kStatusTimeoutDrain);
-        break;
-      }
+    if (lane == 0) {
+      const uint64_t first = issued > uint64_t(stages) ? issued - stages : 0;
+      const uint64_t deadline = global_ns() + wait_ns;
+      for (uint64_t it = first; it < issued; ++it)
+        if (!mbar_wait_bounded(&full[it % stages], uint32_t((it / stages) & 1), deadline)) {
+          atomicExch(status, kStatusTimeoutDrain);
+          break;
+        }
+    }
     return;
   }
 
@@ -344,11 +356,12 @@ __global__ void __launch_bounds__(kThreadsT, 1)
 }  // namespace
 
 // Operand tile per rank: as large as two stages of k tiles allow in ~200 KiB of
-// shared memory.  One producer thread issues the bulk loads, and on GB300 its
-// rate is bounded by the number of pieces (about 4.8 M per second per SM, measured
-// with a probe kernel), so larger tiles feed more bytes: at 8 ranks under a
-// 4-SM budget, 12 KiB tiles run a 25 MiB reduce-scatter in 0.92 ms against
-// 1.16 ms with 8 KiB tiles (register-fed kernel: 0.77 ms).
+// shared memory.  A stage is folded only once all k of its tiles are in, so
+// while the consumers fold one stage about one stage of loads is in flight,
+// and the time per tile grows with a fixed part (load latency, the stage
+// handshake) plus its bytes: at 8 ranks under a 4-SM budget a 25 MiB
+// reduce-scatter takes 1.82 / 1.39 / 1.12 / 0.92 ms with 4 / 6 / 8 / 12 KiB
+// tiles (register-fed kernel: 0.77 ms).
 uint32_t reduce_tma_tile_bytes(int k) { return k <= 4 ? 16384u : (k <= 8 ? 12288u : 4096u); }
 
 int reduce_tma_stages(int k) {
