@@ -31,6 +31,7 @@
 
 #include "hoc_internal.h"
 #include "hoc_ep.h"
+#include "f32x2.cuh"
 #include "ptx_async.cuh"
 
 namespace hoc {
@@ -473,25 +474,13 @@ __global__ void ep_combine_vec_kernel(const uint16_t* __restrict__ rows, const i
 
 // Same fold with every one of the token's TK row loads issued before the
 // ordered fold, so a lane keeps TK 16-byte loads in flight (TK = topk).
-// Two binary32 sums per instruction (IEEE, round to nearest even, no flush
-// to zero): the same bits as two scalar sums.
-__device__ __forceinline__ unsigned long long add_f32x2(unsigned long long a, unsigned long long b) {
-  unsigned long long d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ unsigned long long pack_f32x2(float lo, float hi) {
-  unsigned long long d;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(__float_as_uint(lo)), "r"(__float_as_uint(hi)));
-  return d;
-}
 // acc + w * x for the two bf16 values packed in q: each product rounded to
 // binary32 on its own, then both sums in one instruction.  The products stay
-// scalar on purpose: the code generator fuses a packed multiply that feeds a
-// packed add into one multiply-add, which rounds once (measured: about a
-// quarter of random operands then differ, although both instructions name
-// their rounding, and an empty statement between them did not stop it),
-// while a scalar product with its rounding named is never fused.
+// scalar on purpose (f32x2.cuh): with a packed multiply the code generator
+// fused it into the add -- about a quarter of random operands then differed,
+// although both instructions name their rounding, and an empty statement
+// between them did not stop it -- while a scalar product with its rounding
+// named is never fused.
 __device__ __forceinline__ unsigned long long mul_add_bf16x2(unsigned long long acc, float w, uint32_t q) {
   return add_f32x2(acc, pack_f32x2(__fmul_rn(w, __uint_as_float(q << 16)), __fmul_rn(w, __uint_as_float(q & 0xFFFF0000u))));
 }

@@ -21,11 +21,13 @@
 // multi-wave launches use programmatic dependent launch (the next kernel in
 // the stream is scheduled into the slots the last wave frees).
 //
-// Arithmetic: fp32 adds with __fadd_rn (round to nearest even, no contraction,
-// no flush to zero); bf16 widens exactly to fp32, adds in fp32 and rounds once
+// Arithmetic: fp32 adds rounded to nearest even, no flush to zero, two lanes per
+// instruction (add.rn.f32x2, the same bits as __fadd_rn; scalar __fadd_rn on the
+// scalar path); bf16 widens exactly to fp32, adds in fp32 and rounds once
 // with __float2bfloat16_rn; int32 adds modulo 2^32 in uint32.
 #include <cuda_bf16.h>
 
+#include "f32x2.cuh"
 #include "hoc_internal.h"
 
 namespace hoc {
@@ -62,20 +64,15 @@ struct TrF32 {
   static constexpr int kLanes = 4;
   static constexpr int kBytes = 4;
   using Elem = uint32_t;
-  struct Acc { float v[4]; };
+  struct Acc { unsigned long long v[2]; };  // lanes (0, 1) and (2, 3), two binary32 sums per add
   struct Acc1 { float v; };
-  __device__ static Acc widen(uint4 x) {
-    return {{__uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z), __uint_as_float(x.w)}};
-  }
+  __device__ static Acc widen(uint4 x) { return {{pack_f32x2(x.x, x.y), pack_f32x2(x.z, x.w)}}; }
   __device__ static void add(Acc& a, uint4 x) {
-    a.v[0] = __fadd_rn(a.v[0], __uint_as_float(x.x));
-    a.v[1] = __fadd_rn(a.v[1], __uint_as_float(x.y));
-    a.v[2] = __fadd_rn(a.v[2], __uint_as_float(x.z));
-    a.v[3] = __fadd_rn(a.v[3], __uint_as_float(x.w));
+    a.v[0] = add_f32x2(a.v[0], pack_f32x2(x.x, x.y));
+    a.v[1] = add_f32x2(a.v[1], pack_f32x2(x.z, x.w));
   }
   __device__ static uint4 narrow(const Acc& a) {
-    return make_uint4(__float_as_uint(a.v[0]), __float_as_uint(a.v[1]), __float_as_uint(a.v[2]),
-                      __float_as_uint(a.v[3]));
+    return make_uint4(uint32_t(a.v[0]), uint32_t(a.v[0] >> 32), uint32_t(a.v[1]), uint32_t(a.v[1] >> 32));
   }
   __device__ static Acc1 widen1(Elem e) { return {__uint_as_float(e)}; }
   __device__ static void add1(Acc1& a, Elem e) { a.v = __fadd_rn(a.v, __uint_as_float(e)); }
@@ -105,21 +102,16 @@ struct TrBF16 {
   static constexpr int kLanes = 8;
   static constexpr int kBytes = 2;
   using Elem = uint16_t;
-  struct Acc { float v[8]; };
+  // Element 2w is the low half of 32-bit word w (little endian); acc.v[w]
+  // holds elements (2w, 2w + 1) widened, two binary32 sums per add.
+  struct Acc { unsigned long long v[4]; };
   struct Acc1 { float v; };
-  // Element 2w is the low half of 32-bit word w (little endian).
-  __device__ static float lo(uint32_t w) { return __uint_as_float(w << 16); }
-  __device__ static float hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-  __device__ static Acc widen(uint4 x) {
-    return {{lo(x.x), hi(x.x), lo(x.y), hi(x.y), lo(x.z), hi(x.z), lo(x.w), hi(x.w)}};
-  }
+  __device__ static unsigned long long pair(uint32_t w) { return pack_f32x2(w << 16, w & 0xFFFF0000u); }
+  __device__ static Acc widen(uint4 x) { return {{pair(x.x), pair(x.y), pair(x.z), pair(x.w)}}; }
   __device__ static void add(Acc& a, uint4 x) {
     const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      a.v[2 * i] = __fadd_rn(a.v[2 * i], lo(w[i]));
-      a.v[2 * i + 1] = __fadd_rn(a.v[2 * i + 1], hi(w[i]));
-    }
+    for (int i = 0; i < 4; ++i) a.v[i] = add_f32x2(a.v[i], pair(w[i]));
   }
   __device__ static uint32_t pack(float a, float b) {
     const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(a));
@@ -127,7 +119,8 @@ struct TrBF16 {
     return l | (h << 16);
   }
   __device__ static uint4 narrow(const Acc& a) {
-    return make_uint4(pack(a.v[0], a.v[1]), pack(a.v[2], a.v[3]), pack(a.v[4], a.v[5]), pack(a.v[6], a.v[7]));
+    return make_uint4(pack(lo_f32(a.v[0]), hi_f32(a.v[0])), pack(lo_f32(a.v[1]), hi_f32(a.v[1])),
+                      pack(lo_f32(a.v[2]), hi_f32(a.v[2])), pack(lo_f32(a.v[3]), hi_f32(a.v[3])));
   }
   __device__ static Acc1 widen1(Elem e) { return {__uint_as_float(uint32_t(e) << 16)}; }
   __device__ static void add1(Acc1& a, Elem e) { a.v = __fadd_rn(a.v, __uint_as_float(uint32_t(e) << 16)); }

@@ -24,6 +24,7 @@
 // loads in flight and returns.
 #include <cuda_bf16.h>
 
+#include "f32x2.cuh"
 #include "hoc_internal.h"
 #include "ptx_async.cuh"
 
@@ -115,46 +116,42 @@ __device__ __forceinline__ void scalar_elem(const ReduceParams& p, const uint8_t
 
 // Fold one 16-byte vector position of the k tiles in a stage.  K > 0: the
 // rank count is a compile-time constant and all K shared-memory loads are
-// issued before the adds; K == 0: runtime k.
+// issued before the adds; K == 0: runtime k.  Floating-point sums run two
+// binary32 lanes per instruction (f32x2.cuh), the same bits as scalar adds.
+__device__ __forceinline__ unsigned long long bf16_pair(uint32_t w) { return pack_f32x2(w << 16, w & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t bf16_narrow_pair(unsigned long long a) {
+  return uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(lo_f32(a)))) |
+         (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(hi_f32(a)))) << 16);
+}
+
 template <int K>
 __device__ __forceinline__ uint4 fold_vec(const unsigned char* stage, uint32_t tile_bytes, int k, uint32_t off,
                                           int dtype) {
+  const int n = K > 0 ? K : k;
+  auto tile = [&](int j) { return *reinterpret_cast<const uint4*>(stage + size_t(j) * tile_bytes + off); };
   if constexpr (K > 0) {
     uint4 v[K];
 #pragma unroll
-    for (int j = 0; j < K; ++j) v[j] = *reinterpret_cast<const uint4*>(stage + size_t(j) * tile_bytes + off);
+    for (int j = 0; j < K; ++j) v[j] = tile(j);
     if (dtype == HOC_BFLOAT16) {
-      float a[8];
+      unsigned long long a[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t w = (&v[0].x)[i];
-        a[2 * i] = __uint_as_float(w << 16);
-        a[2 * i + 1] = __uint_as_float(w & 0xFFFF0000u);
-      }
+      for (int i = 0; i < 4; ++i) a[i] = bf16_pair((&v[0].x)[i]);
 #pragma unroll
       for (int j = 1; j < K; ++j)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t w = (&v[j].x)[i];
-          a[2 * i] = __fadd_rn(a[2 * i], __uint_as_float(w << 16));
-          a[2 * i + 1] = __fadd_rn(a[2 * i + 1], __uint_as_float(w & 0xFFFF0000u));
-        }
-      uint32_t o[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        o[i] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(a[2 * i]))) |
-               (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(a[2 * i + 1]))) << 16);
-      return make_uint4(o[0], o[1], o[2], o[3]);
+        for (int i = 0; i < 4; ++i) a[i] = add_f32x2(a[i], bf16_pair((&v[j].x)[i]));
+      return make_uint4(bf16_narrow_pair(a[0]), bf16_narrow_pair(a[1]), bf16_narrow_pair(a[2]),
+                        bf16_narrow_pair(a[3]));
     }
     if (dtype == HOC_FLOAT32) {
-      float a[4];
+      unsigned long long a0 = pack_f32x2(v[0].x, v[0].y), a1 = pack_f32x2(v[0].z, v[0].w);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = __uint_as_float((&v[0].x)[i]);
-#pragma unroll
-      for (int j = 1; j < K; ++j)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) a[i] = __fadd_rn(a[i], __uint_as_float((&v[j].x)[i]));
-      return make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]), __float_as_uint(a[3]));
+      for (int j = 1; j < K; ++j) {
+        a0 = add_f32x2(a0, pack_f32x2(v[j].x, v[j].y));
+        a1 = add_f32x2(a1, pack_f32x2(v[j].z, v[j].w));
+      }
+      return make_uint4(uint32_t(a0), uint32_t(a0 >> 32), uint32_t(a1), uint32_t(a1 >> 32));
     }
     uint4 x = v[0];
 #pragma unroll
@@ -166,45 +163,29 @@ __device__ __forceinline__ uint4 fold_vec(const unsigned char* stage, uint32_t t
     }
     return x;
   }
-  const uint4* t0 = reinterpret_cast<const uint4*>(stage + off);
-  uint4 x = *t0;
+  uint4 x = tile(0);
   if (dtype == HOC_BFLOAT16) {
-    float a[8];
-    const uint32_t w0[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      a[2 * i] = __uint_as_float(w0[i] << 16);
-      a[2 * i + 1] = __uint_as_float(w0[i] & 0xFFFF0000u);
+    unsigned long long a[4] = {bf16_pair(x.x), bf16_pair(x.y), bf16_pair(x.z), bf16_pair(x.w)};
+    for (int j = 1; j < n; ++j) {
+      const uint4 y = tile(j);
+      a[0] = add_f32x2(a[0], bf16_pair(y.x));
+      a[1] = add_f32x2(a[1], bf16_pair(y.y));
+      a[2] = add_f32x2(a[2], bf16_pair(y.z));
+      a[3] = add_f32x2(a[3], bf16_pair(y.w));
     }
-    for (int j = 1; j < k; ++j) {
-      const uint4 y = *reinterpret_cast<const uint4*>(stage + size_t(j) * tile_bytes + off);
-      const uint32_t w[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        a[2 * i] = __fadd_rn(a[2 * i], __uint_as_float(w[i] << 16));
-        a[2 * i + 1] = __fadd_rn(a[2 * i + 1], __uint_as_float(w[i] & 0xFFFF0000u));
-      }
-    }
-    uint32_t o[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      o[i] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(a[2 * i]))) |
-             (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(a[2 * i + 1]))) << 16);
-    return make_uint4(o[0], o[1], o[2], o[3]);
+    return make_uint4(bf16_narrow_pair(a[0]), bf16_narrow_pair(a[1]), bf16_narrow_pair(a[2]), bf16_narrow_pair(a[3]));
   }
   if (dtype == HOC_FLOAT32) {
-    float a0 = __uint_as_float(x.x), a1 = __uint_as_float(x.y), a2 = __uint_as_float(x.z), a3 = __uint_as_float(x.w);
-    for (int j = 1; j < k; ++j) {
-      const uint4 y = *reinterpret_cast<const uint4*>(stage + size_t(j) * tile_bytes + off);
-      a0 = __fadd_rn(a0, __uint_as_float(y.x));
-      a1 = __fadd_rn(a1, __uint_as_float(y.y));
-      a2 = __fadd_rn(a2, __uint_as_float(y.z));
-      a3 = __fadd_rn(a3, __uint_as_float(y.w));
+    unsigned long long a0 = pack_f32x2(x.x, x.y), a1 = pack_f32x2(x.z, x.w);
+    for (int j = 1; j < n; ++j) {
+      const uint4 y = tile(j);
+      a0 = add_f32x2(a0, pack_f32x2(y.x, y.y));
+      a1 = add_f32x2(a1, pack_f32x2(y.z, y.w));
     }
-    return make_uint4(__float_as_uint(a0), __float_as_uint(a1), __float_as_uint(a2), __float_as_uint(a3));
+    return make_uint4(uint32_t(a0), uint32_t(a0 >> 32), uint32_t(a1), uint32_t(a1 >> 32));
   }
-  for (int j = 1; j < k; ++j) {
-    const uint4 y = *reinterpret_cast<const uint4*>(stage + size_t(j) * tile_bytes + off);
+  for (int j = 1; j < n; ++j) {
+    const uint4 y = tile(j);
     x.x += y.x;
     x.y += y.y;
     x.z += y.z;
