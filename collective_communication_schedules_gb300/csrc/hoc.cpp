@@ -223,7 +223,10 @@ hocResult_t run_reduce(hocComm* c, const Plan& p, const Step& st, const Bind& bd
     const uint64_t cap = uint64_t(budget > 0 ? std::min(budget, c->sms) : c->sms);
     const int grid = int(std::min<uint64_t>(tiles, cap));
     *max_ctas = std::max(*max_ctas, grid);
-    return timed_launch(c, kind, s, [&] { return launch_reduce_tma(rp, grid, c->status, s); });
+    const bool stall = c->cfg.fault == kFaultTmaStall;  // host-injected: mbarriers that never complete
+    return timed_launch(c, kind, s, [&] {
+      return launch_reduce_tma(rp, grid, c->status, s, stall ? 16u : 0u, stall ? 100000000ull : 2000000000ull);
+    });
   }
   // Whole GPU: several waves of CTAs rather than one persistent wave, so a CTA
   // that finishes its tiles is replaced at once and loads keep streaming.

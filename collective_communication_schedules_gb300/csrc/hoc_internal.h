@@ -61,7 +61,10 @@ cudaError_t workload_preload();  // probe and stand-in compute kernels
 // TMA-fed variant (reduce_tma.cu): same fold, bulk copies through shared memory.
 uint64_t reduce_tma_seg_tiles(int dtype, const ReduceSeg& s, int k);
 cudaError_t reduce_tma_prepare();  // one-time per device: shared-memory opt-in
-cudaError_t launch_reduce_tma(const ReduceParams& p, int grid, int* status, cudaStream_t stream);
+// tx_pad: extra bytes every mbarrier expects (0; > 0 only for host-injected
+// stalls); wait_ns: the bound of every mbarrier wait.
+cudaError_t launch_reduce_tma(const ReduceParams& p, int grid, int* status, cudaStream_t stream, uint32_t tx_pad,
+                              uint64_t wait_ns);
 
 // -------------------------------------------------------------- TMA copy
 // One copy job of the TMA kernel: `bytes` from `src` to `dst` and, for a

@@ -221,7 +221,7 @@ __device__ __forceinline__ void tile_body(const ReduceParams& p, const ReduceSeg
 template <int K>
 __global__ void __launch_bounds__(kThreadsT, 1)
     reduce_tma_kernel(const __grid_constant__ ReduceParams p, uint32_t tile_bytes, int stages, int* status,
-                      uint64_t wait_ns) {
+                      uint64_t wait_ns, uint32_t tx_pad) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full[8];
   __shared__ __align__(8) uint64_t empty[8];
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       if (n == 0) {
         if (lane == 0) mbar_arrive(&full[s]);  // nothing to load (a segment shorter than one vector)
       } else {
-        if (lane == 0) mbar_arrive_expect_tx(&full[s], n * uint32_t(k));
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], n * uint32_t(k) + tx_pad);  // tx_pad: injected stalls only
         __syncwarp();
         if (lane < k) {
           const uint8_t* seq = p.seq[sg.owner];
@@ -394,12 +394,12 @@ cudaError_t tma_preload() {
   return tma_copy_preload();
 }
 
-cudaError_t launch_reduce_tma(const ReduceParams& p, int grid, int* status, cudaStream_t stream) {
+cudaError_t launch_reduce_tma(const ReduceParams& p, int grid, int* status, cudaStream_t stream, uint32_t tx_pad,
+                              uint64_t wait_ns) {
   if (grid < 1) return cudaSuccess;
   uint32_t tb = reduce_tma_tile_bytes(p.k);
   int stages = reduce_tma_stages(p.k);
-  uint64_t wait_ns = 2000000000ull;
-  void* args[] = {const_cast<ReduceParams*>(&p), &tb, &stages, &status, &wait_ns};
+  void* args[] = {const_cast<ReduceParams*>(&p), &tb, &stages, &status, &wait_ns, &tx_pad};
   return cudaLaunchKernel(reduce_tma_fn(p.k), dim3(grid), dim3(kThreadsT), args, reduce_tma_smem(p.k), stream);
 }
 

@@ -66,3 +66,27 @@ def test_tma_bounded_wait_reports_and_context_survives(monkeypatch):
         c.wait()
     torch.cuda.synchronize()
     assert bool((b[0] == 1).all()) and bool((b[1] == 1).all())
+
+
+def test_tma_fed_reduce_bounded_wait_reports_and_context_survives(monkeypatch):
+    """The same injected stall in the TMA-fed reduce: every operand slot's mbarrier expects 16 bytes
+    that never arrive, the consumers' and the producer's bounded waits give up, the status reaches
+    hoc_wait, and the next reduce-scatter is exact."""
+    k, n = 4, 1 << 16
+    xs = inputs.rank_inputs("float32", k, n, workload=7, slot=71)
+    want = o_ring.reduce_scatter(xs, n // k, "float32")
+    send = [to_device(x, "float32") for x in xs]
+    recv = [torch.full((n // k,), float("nan"), device="cuda") for _ in range(k)]
+    monkeypatch.setenv("HOC_FAULT", "tma_stall")
+    with hoc.Comm(k, 0, hoc.Config(path="ce", reduce_engine="tma")) as c:
+        c.reduce_scatter(send, recv, n // k)
+        with pytest.raises(hoc.HocError) as e:
+            c.wait(timeout_ms=30000)
+        assert e.value.code == hoc.ERR_TIMEOUT
+        assert "bounded wait" in str(e.value)
+    monkeypatch.delenv("HOC_FAULT")
+    with hoc.Comm(k, 0, hoc.Config(path="ce", reduce_engine="tma")) as c:
+        c.reduce_scatter(send, recv, n // k)
+        c.wait()
+    for r in range(k):
+        assert np.array_equal(to_host(recv[r], "float32").view(np.uint32), want[r].view(np.uint32)), r
