@@ -63,8 +63,10 @@ constexpr auto kShutdownWait = std::chrono::seconds(60);
 // The proxy issues a task's copies only once the stream is at the start flag,
 // so the exchange is bound by whichever is longer: issuing the copies (about
 // 1.5 us of host time each) or moving the bytes (copy engines, ~5.8 TB/s).
-// It sizes the chunks so that a task takes at most this many copies.
-constexpr size_t kProxyTaskCopies = 96;
+// It sizes the chunks so that a task takes at most about this many copies.
+// Measured on the EP round trip (2 x 805 MB exchanges): 96 -> 0.96 ms,
+// 48 -> 0.90 ms, 32 -> 0.92 ms.
+constexpr size_t kProxyTaskCopies = 48;
 constexpr size_t kChunkGrain = size_t(1) << 20;
 
 enum SlotState { kFree = 0, kQueued = 1, kStarting = 2, kRunning = 3, kReleasing = 4, kRetired = 5 };
