@@ -32,6 +32,10 @@ import sys
 import threading
 import time
 
+# The host proxy's copies must not share a hardware work queue with a stream
+# held at its start flag (see include/hoc_proxy.h); set before CUDA starts.
+os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)

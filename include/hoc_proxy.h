@@ -14,7 +14,7 @@
  * the device (for example by an expert-routing kernel).  The counts travel to
  * the proxy through the handshake; the proxy plans the exchange (shift stages
  * and flow-size-aware chunk interleave, as hoc_alltoall) and issues it on copy
- * engines, in chunks of at least total bytes / 96 so that issuing the copies,
+ * engines, in chunks of at least total bytes / 48 so that issuing the copies,
  * which starts only when the stream reaches the flag, takes no longer than
  * moving them.  A watchdog in the proxy always writes the finish value, so no
  * stream waits forever: if the moves do not complete within the deadline, or
@@ -23,14 +23,19 @@
  * and the stream operations are cuStreamWriteValue32 / cuStreamWaitValue32.
  *
  * Held-stream window: from the start flag to the end flag the caller's
- * stream is held, and the moves must run meanwhile.  Two things stall them
- * until the stream is released: launching a kernel for the first time under
- * lazy module loading (CUDA_MODULE_LOADING=LAZY, the default; the load can
- * wait for the whole context, the held stream included), and a pageable host
- * copy queued behind the held stream.  The library loads all of its own
- * kernels before the proxy starts; load other kernels that run during the
- * window beforehand (one warm-up launch, or CUDA_MODULE_LOADING=EAGER) and
- * keep blocking host copies off the held stream.  Should a stall happen
+ * stream is held, and the moves must run meanwhile.  Three things stall them
+ * until the stream is released: a proxy copy stream that shares the held
+ * stream's hardware work queue (CUDA maps streams onto
+ * CUDA_DEVICE_MAX_CONNECTIONS queues, 8 by default; the wait blocks its whole
+ * queue -- on GB300 about 3 in 10 fresh processes hit it at 8 queues, none in
+ * 8 at 32, all at 1: run with CUDA_DEVICE_MAX_CONNECTIONS=32, set before the
+ * process starts CUDA); launching a kernel for the first time under lazy
+ * module loading (CUDA_MODULE_LOADING=LAZY, the default; the load can wait for
+ * the whole context, the held stream included); and a pageable host copy
+ * queued behind the held stream.  The library loads all of its own kernels
+ * before the proxy starts; load other kernels that run during the window
+ * beforehand (one warm-up launch, or CUDA_MODULE_LOADING=EAGER) and keep
+ * blocking host copies off the held stream.  Should a stall happen
  * anyway, the proxy's watchdog -- a host thread that makes no CUDA call --
  * releases the stream after 10 s and the call reports HOC_ERR_TIMEOUT with the
  * reason; no stream is left waiting and no thread deadlocks.

@@ -35,9 +35,16 @@ def test_device_count_alltoall_matches_oracle():
     want = o_a2a.alltoallv(sends, counts)
     lens = o_a2a.recv_lengths(counts)
     # The kernels that run while the stream is held are loaded first: under
-    # lazy module loading a first launch can wait for the held stream.
+    # lazy module loading a first launch can wait for the held stream.  Every
+    # operation of the held window below runs once beforehand, on both streams.
     after = torch.zeros(1, device="cuda")
     after += 1
+    after.zero_()
+    warm = torch.cuda.Stream()
+    with torch.cuda.stream(warm):
+        after += 1
+        after.zero_()
+    torch.cuda.synchronize()
     with hoc.Comm(k, 0, hoc.Config(chunk_bytes=1 << 16)) as c:
         s = torch.cuda.Stream()
         with torch.cuda.stream(s):
