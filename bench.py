@@ -535,6 +535,8 @@ def leg_bucket_stream(host_pool, sms, peak):
     pool_in = [[torch.from_numpy(host_pool[s * k + r].view("int16")).view(torch.bfloat16).to(dev)
                 for r in range(k)] for s in range(pool)]
     outs = torch.empty((nb, k, rc), dtype=torch.bfloat16, device=dev)
+    # each bucket's k output views, made once: building them per call costs more host time than the call
+    out_views = [[outs[b, r] for r in range(k)] for b in range(nb)]
     stream = torch.cuda.Stream()
     out = {"buckets": nb, "bucket_bytes_per_rank": be * 2, "budgets": []}
     for m, eng in ((4, "lsu"), (4, "tma"), (8, "lsu"), (8, "tma"), (16, "lsu"), (16, "tma"), (32, "lsu"),
@@ -542,7 +544,7 @@ def leg_bucket_stream(host_pool, sms, peak):
         with hoc.Comm(k, torch.cuda.current_device(), hoc.Config(reduce_max_sms=m, reduce_engine=eng)) as c:
             def run(s, c=c):
                 for b in range(nb):
-                    c.reduce_scatter(pool_in[b % pool], [outs[b, r] for r in range(k)], rc, stream=s)
+                    c.reduce_scatter(pool_in[b % pool], out_views[b], rc, stream=s)
             run(stream)
             torch.cuda.synchronize()
             runs = []
@@ -565,20 +567,20 @@ def leg_bucket_stream(host_pool, sms, peak):
     # the whole stream of 268 reduce-scatters (whole GPU) captured once into a CUDA graph and replayed:
     # one launch for the stream instead of 268 host calls
     try:
-        out["graph_replay"] = _bucket_stream_graph(hoc, torch, k, nb, pool, rc, pool_in, outs, stream, peak)
+        out["graph_replay"] = _bucket_stream_graph(hoc, torch, k, nb, pool, rc, pool_in, out_views, stream, peak)
     except Exception as e:  # reported in the line; the other legs stand
         torch.cuda.synchronize()
         out["graph_replay"] = {"error": str(e)}
-    del pool_in, outs
+    del pool_in, outs, out_views
     torch.cuda.empty_cache()
     return out
 
 
-def _bucket_stream_graph(hoc, torch, k, nb, pool, rc, pool_in, outs, stream, peak):
+def _bucket_stream_graph(hoc, torch, k, nb, pool, rc, pool_in, out_views, stream, peak):
     with hoc.Comm(k, torch.cuda.current_device()) as c:
         def run_all(s, c=c):
             for b in range(nb):
-                c.reduce_scatter(pool_in[b % pool], [outs[b, r] for r in range(k)], rc, stream=s)
+                c.reduce_scatter(pool_in[b % pool], out_views[b], rc, stream=s)
         run_all(stream)                                    # plans built before the capture
         torch.cuda.synchronize()
         graph = torch.cuda.CUDAGraph()
