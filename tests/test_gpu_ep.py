@@ -589,3 +589,26 @@ def test_bulk_copy_waits_give_up_into_the_status_word(stage, monkeypatch):
         assert np.array_equal(to_host(recv[d], "bfloat16"), want_recv[d]), d
     for r in range(k):
         assert np.array_equal(to_host(ys[r], "bfloat16").reshape(tokens, hidden), want_y[r]), r
+
+
+def test_fused_dispatch_past_the_grid_cap():
+    """More (source, token) work items than the dispatch grid's 2^20 CTAs x 8 warps: 8 ranks x
+    1,100,000 tokens of 6-byte rows (the byte path, one warp per token), so warps loop over
+    several items; results against the oracle."""
+    k, tokens, hidden, experts, topk = 8, 1_100_000, 3, 16, 1
+    assert k * tokens > (1 << 20) * 8
+    rng = np.random.default_rng(9900)
+    routing = [rng.integers(0, experts, size=(tokens, topk)) for _ in range(k)]
+    routing[2][17, 0] = -1                                   # a dropped pair
+    xs = [inputs.normal_bf16(tokens * hidden, 9910 + r).reshape(tokens, hidden) for r in range(k)]
+    ws = [rng.random(tokens * topk).astype(np.float32) for _ in range(k)]
+    packs, counts, want_recv, want_y = _oracle_round_trip(xs, routing, ws, experts, k, topk, hidden)
+    caps = [int(counts[:, d].sum()) for d in range(k)]
+    recv, pos, d_counts, status, ys = _fused_on_device(k, xs, routing, ws, experts, topk, caps)
+    assert int(status.item()) == 0
+    assert np.array_equal(d_counts.cpu().numpy(), counts)
+    for d in range(k):
+        assert np.array_equal(recv[d].host()[: len(want_recv[d])], want_recv[d]), d
+        recv[d].check()
+    for r in range(k):
+        assert np.array_equal(ys[r].host().reshape(tokens, hidden), want_y[r]), r
