@@ -7,6 +7,8 @@
 
 #include <cstdint>
 
+#include <cuda_bf16.h>
+
 namespace hoc {
 
 __device__ __forceinline__ unsigned long long pack_f32x2(uint32_t lo, uint32_t hi) {
@@ -24,5 +26,14 @@ __device__ __forceinline__ unsigned long long add_f32x2(unsigned long long a, un
 }
 __device__ __forceinline__ float lo_f32(unsigned long long v) { return __uint_as_float(uint32_t(v)); }
 __device__ __forceinline__ float hi_f32(unsigned long long v) { return __uint_as_float(uint32_t(v >> 32)); }
+
+// The two bf16 values of a 32-bit word (element 2w in the low half), widened
+// exactly to binary32 lanes; and back, each lane rounded once to bf16
+// (nearest even).
+__device__ __forceinline__ unsigned long long bf16_pair(uint32_t w) { return pack_f32x2(w << 16, w & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t bf16_narrow_pair(unsigned long long a) {
+  return uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(lo_f32(a)))) |
+         (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(hi_f32(a)))) << 16);
+}
 
 }  // namespace hoc

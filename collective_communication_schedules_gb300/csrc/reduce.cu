@@ -106,21 +106,15 @@ struct TrBF16 {
   // holds elements (2w, 2w + 1) widened, two binary32 sums per add.
   struct Acc { unsigned long long v[4]; };
   struct Acc1 { float v; };
-  __device__ static unsigned long long pair(uint32_t w) { return pack_f32x2(w << 16, w & 0xFFFF0000u); }
-  __device__ static Acc widen(uint4 x) { return {{pair(x.x), pair(x.y), pair(x.z), pair(x.w)}}; }
+  __device__ static Acc widen(uint4 x) { return {{bf16_pair(x.x), bf16_pair(x.y), bf16_pair(x.z), bf16_pair(x.w)}}; }
   __device__ static void add(Acc& a, uint4 x) {
     const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) a.v[i] = add_f32x2(a.v[i], pair(w[i]));
-  }
-  __device__ static uint32_t pack(float a, float b) {
-    const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(a));
-    const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(b));
-    return l | (h << 16);
+    for (int i = 0; i < 4; ++i) a.v[i] = add_f32x2(a.v[i], bf16_pair(w[i]));
   }
   __device__ static uint4 narrow(const Acc& a) {
-    return make_uint4(pack(lo_f32(a.v[0]), hi_f32(a.v[0])), pack(lo_f32(a.v[1]), hi_f32(a.v[1])),
-                      pack(lo_f32(a.v[2]), hi_f32(a.v[2])), pack(lo_f32(a.v[3]), hi_f32(a.v[3])));
+    return make_uint4(bf16_narrow_pair(a.v[0]), bf16_narrow_pair(a.v[1]), bf16_narrow_pair(a.v[2]),
+                      bf16_narrow_pair(a.v[3]));
   }
   __device__ static Acc1 widen1(Elem e) { return {__uint_as_float(uint32_t(e) << 16)}; }
   __device__ static void add1(Acc1& a, Elem e) { a.v = __fadd_rn(a.v, __uint_as_float(uint32_t(e) << 16)); }

@@ -118,11 +118,6 @@ __device__ __forceinline__ void scalar_elem(const ReduceParams& p, const uint8_t
 // rank count is a compile-time constant and all K shared-memory loads are
 // issued before the adds; K == 0: runtime k.  Floating-point sums run two
 // binary32 lanes per instruction (f32x2.cuh), the same bits as scalar adds.
-__device__ __forceinline__ unsigned long long bf16_pair(uint32_t w) { return pack_f32x2(w << 16, w & 0xFFFF0000u); }
-__device__ __forceinline__ uint32_t bf16_narrow_pair(unsigned long long a) {
-  return uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(lo_f32(a)))) |
-         (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(hi_f32(a)))) << 16);
-}
 
 template <int K>
 __device__ __forceinline__ uint4 fold_vec(const unsigned char* stage, uint32_t tile_bytes, int k, uint32_t off,
