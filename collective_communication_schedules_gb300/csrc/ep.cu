@@ -890,11 +890,11 @@ __global__ void ep_combine_fused_vec_kernel(const __grid_constant__ EpRoute R) {
 }
 
 // Combine fed by the tensor-memory accelerator.  Each warp owns two
-// shared-memory stages of topk x 1 KiB; for its work item (source,
-// token, 1 KiB chunk of the row) lane 0 bulk-loads the chunk of every valid
-// pair's row into a stage, completing on the stage's mbarrier, and the warp
-// folds from shared memory in slot order while the next item's loads are in
-// flight.  So the bytes in flight do not take registers: 2 x topk KiB per
+// shared-memory stages of topk slices (1-4 KiB, by topk); for its work item
+// (source, token, slice of the row) lane 0 bulk-loads the slice of every
+// valid pair's row into a stage, completing on the stage's mbarrier, and the
+// warp folds from shared memory in slot order while the next item's loads are
+// in flight.  So the bytes in flight do not take registers: two stages per
 // warp.  The pairs' positions, experts and weights are loaded one item
 // earlier still, so resolving where an item's rows are costs no wait (at
 // the EP workload's shape the combine went from 0.187 to 0.158 ms).  The
@@ -905,10 +905,21 @@ __global__ void ep_combine_fused_vec_kernel(const __grid_constant__ EpRoute R) {
 // for its own loads and stops.
 constexpr int kBulkTopk = 8;
 constexpr int kCombWarps = 4;                 // warps per CTA
-// Bytes of a row per item.  Measured at the EP workload's shape (4 KiB rows,
-// top-6): 1 KiB slices 0.187 ms, 2 KiB 0.216 ms, whole rows 0.289 ms -- the
-// number of warps folding per SM matters more than the length of each read.
+// Bytes of a row per item: the largest of 4, 2 and 1 KiB whose topk slices
+// fit a 6 KiB stage (1 KiB from top-4 on).  A stage of about 4-6 KiB per warp
+// is what the measurements favour: at 4 KiB rows, top-6, 1 KiB slices took
+// 0.187 ms, 2 KiB 0.216 ms, whole rows 0.289 ms (fewer CTAs fit per SM); at
+// top-1 and top-2, 1 KiB slices left too few bytes in flight (0.084 and
+// 0.092 ms, against 0.049 ms for 4 KiB and 0.069 ms for 2 KiB slices), and
+// at top-2 and top-4 the next size up was slower again (4 KiB: 0.078 ms;
+// 2 KiB: 0.115 against 0.112 ms).
 constexpr uint32_t kCombSlice = 1024;
+constexpr uint32_t kCombStage = 6144;
+inline uint32_t comb_slice(int topk) {
+  uint32_t slice = 4096;
+  while (slice > kCombSlice && uint32_t(topk) * slice > kCombStage) slice /= 2;
+  return slice;
+}
 
 __global__ void __launch_bounds__(32 * kCombWarps) ep_combine_bulk_kernel(const __grid_constant__ EpRoute R,
                                                                          uint32_t slice) {
@@ -1460,7 +1471,7 @@ hocResult_t combine_ranks(const char* who, int packed, int nranks, const void* c
   const char* eng = getenv("HOC_EP_COMBINE");
   if (vec && topk <= kBulkTopk && !(eng && !strcmp(eng, "lsu"))) {
     const void* fn = reinterpret_cast<const void*>(&ep_combine_bulk_kernel);
-    const uint32_t slice = kCombSlice;
+    const uint32_t slice = comb_slice(topk);
     const size_t smem = size_t(kCombWarps) * 2 * size_t(topk) * slice;
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     int dev = 0, sms = 1, occ = 0;

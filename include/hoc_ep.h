@@ -103,8 +103,9 @@ hocResult_t hoc_ep_dispatch_fused(int nranks, const int32_t* const* expert_ids, 
  * *status (not cleared here) is set if a row lies outside its buffer (it then
  * adds nothing).  With hidden % 8 == 0, 16-byte-aligned rows and outputs and
  * topk <= 8, each warp's rows arrive by TMA bulk copies into shared memory
- * (two stages of topk x 1 KiB per warp; bit 2 of *status if a bounded wait
- * gave up); HOC_EP_COMBINE=lsu selects per-thread vector loads instead. */
+ * (two stages per warp of topk row slices, 4 KiB at topk 1, 2 KiB at topk 2-3,
+ * 1 KiB from topk 4 on; bit 2 of *status if a bounded wait gave up);
+ * HOC_EP_COMBINE=lsu selects per-thread vector loads instead. */
 hocResult_t hoc_ep_combine_fused(int nranks, const void* const* rows, const size_t* rows_capacity,
                                  const int32_t* const* expert_ids, const int32_t* const* pos_of,
                                  const uint64_t* counts, const float* const* weights, int tokens, int topk,

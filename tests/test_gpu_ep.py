@@ -156,7 +156,9 @@ def test_combine_golden_cases(hidden):
             (c["name"], hidden, [hex(int(v)) for v in got.reshape(-1)])
 
 
-@pytest.mark.parametrize("hidden", [1, 8, 520])   # scalar; one vector per lane; a 1 KiB slice and a 16-byte tail
+# scalar; one vector per lane; one slice and a 16-byte tail (1 KiB slices at topk 4, 2 KiB at 2-3);
+# rows of 4112 B: several whole slices and a 16-byte tail
+@pytest.mark.parametrize("hidden", [1, 8, 520, 2056])
 @pytest.mark.parametrize("engine", [None, "lsu"])   # TMA-fed combine (default), vector-load combine
 def test_fused_combine_golden_cases(hidden, engine, monkeypatch):
     """The hand-derived combine cases through the combine that reads the rows in place: one rank,
@@ -227,6 +229,8 @@ def _fused_on_device(k, xs, routing, ws, experts, topk, caps, recv_offset=0, y_o
     (8, 100, 16, True, 64, 40, 0),      # topk above a warp
     (8, 777, 64, True, 64, 6, 1),       # receive buffers 2 bytes off alignment: byte dispatch, scalar combine
     (1, 300, 64, True, 8, 3, 0),        # one rank: everything stays home
+    (4, 300, 4100, True, 32, 1, 0),     # top-1: 4 KiB combine slices, rows of 8200 B (two whole, one ragged)
+    (4, 300, 2100, True, 32, 2, 0),     # top-2: 2 KiB combine slices, rows of 4200 B
 ])
 @pytest.mark.parametrize("engines", [None, ("bulk", "lsu")])
 def test_fused_dispatch_and_combine_match_oracle(k, tokens, hidden, drop, experts, topk, recv_offset, engines,
@@ -348,7 +352,7 @@ def test_fused_combine_reports_rows_outside_its_buffers():
 
 @pytest.mark.parametrize("engines", [None, ("bulk", "lsu")])
 @pytest.mark.parametrize("k,tokens,hidden,experts,topk", [(8, 4096, 2048, 64, 6), (3, 500, 36, 48, 4),
-                                                          (8, 300, 64, 2048, 2)])
+                                                          (8, 300, 64, 2048, 2), (4, 300, 4100, 32, 1)])
 def test_pack_all_and_combine_all_match_oracle(k, tokens, hidden, experts, topk, engines, monkeypatch):
     # every rank's pack in one pass, the two copy-engine exchanges, every rank's combine in one pass
     if engines:
