@@ -57,7 +57,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default="auto", choices=["auto", "ce", "tma", "fused"])
-    ap.add_argument("--chunk-bytes", type=int, default=0, help="0: picked by move path (4 MiB on both)")
+    ap.add_argument("--chunk-bytes", type=int, default=0, help="0: picked by the scheduler (allreduce: by move path and rank count)")
     ap.add_argument("--copy-streams", type=int, default=0, help="0: picked per call by copy size (8 or 4 queues)")
     ap.add_argument("--no-extras", action="store_true", help="skip the per-path, probe and e2e legs")
     ap.add_argument("--e2e-steps", type=int, default=3)

@@ -104,8 +104,8 @@ std::vector<std::vector<int>> source_groups(const std::vector<Move>& moves) {
 
 namespace {
 
-size_t chunk_elems(const Cfg& cfg, size_t b, int path) {
-  size_t ce = chunk_for(cfg, path) / b;
+size_t chunk_elems(size_t chunk_bytes, size_t b) {
+  size_t ce = chunk_bytes / b;
   ce -= ce % 16;  // keep chunk boundaries on 16-element multiples
   return ce < 16 ? 16 : ce;
 }
@@ -240,7 +240,7 @@ hocResult_t plan_allreduce(const Cfg& cfg, const CallShape& s, Plan* p) {
     p->steps.push_back(std::move(st));
     return HOC_SUCCESS;
   }
-  const size_t ce = chunk_elems(cfg, b, p->path);
+  const size_t ce = chunk_elems(allreduce_chunk(cfg, p->path, k), b);
   const size_t nq = (sz[0] + ce - 1) / ce;
   const int queues = copy_queues(cfg, std::min(ce, sz[0]) * b);
   std::vector<std::vector<int>> copy_steps(nq);

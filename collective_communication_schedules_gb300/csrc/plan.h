@@ -9,6 +9,7 @@
 // dtype, configuration), never on buffer addresses, so they are cached.
 #pragma once
 
+#include <algorithm>
 #include <cstddef>
 #include <cstdint>
 #include <string>
@@ -36,14 +37,34 @@ struct Cfg {
   int fault = 0;           // host-side fault injection (Fault)
 };
 
-// Pipeline chunk of a move path when the configuration leaves it at 0: the
-// best of the 1-64 MiB sweep of the 8-rank 256 MiB bf16 allreduce on GB300,
-// 4 MiB on both move paths (copy engines 0.89 ms, TMA kernel 0.69 ms).  Kept
-// per path so the two can part when a path changes.
+// Copy size of the all-gather, all-to-all and send/recv moves when the
+// configuration leaves chunk_bytes at 0: 4 MiB on both move paths.
 constexpr size_t kAutoChunkCe = size_t(4) << 20;
 constexpr size_t kAutoChunkTma = size_t(4) << 20;
 inline size_t chunk_for(const Cfg& cfg, int path) {
   return cfg.chunk_bytes ? cfg.chunk_bytes : (path == HOC_PATH_TMA ? kAutoChunkTma : kAutoChunkCe);
+}
+
+// Pipeline chunk of the copy-engine and TMA allreduce when the configuration
+// leaves chunk_bytes at 0, by move path and rank count.  Each chunk costs a
+// reduce kernel and a round of k(k-1) copies; with few ranks a chunk's kernel
+// is small and its launch and tail show, with many the copies are many and
+// small.  From sweeps of 1-64 MiB chunks (bf16, 16 / 64 / 256 MiB per rank,
+// k = 2, 4, 8, 16, GB300): copy engines want 32 MiB / k within 2-8 MiB (k = 2:
+// 8 MiB, 0.180 ms at 256 MiB against 0.243 at 4 MiB; k = 4: 8 MiB, 0.100 ms at
+// 64 MiB against 0.106; k = 16: 2 MiB, 0.490 ms at 64 MiB against 0.543; at
+// k = 8, 2 and 4 MiB are equal and 4 MiB runs half the reduce kernels beside
+// the caller's), the TMA kernel 64 MiB / k^2 within 4-16 MiB (k = 2: 16 MiB,
+// 0.199 ms at 256 MiB against 0.278).  A block smaller than the chunk is one
+// chunk.
+constexpr size_t kArChunkCeBytesTimesK = size_t(32) << 20;
+constexpr size_t kArChunkTmaBytesTimesK2 = size_t(64) << 20;
+inline size_t allreduce_chunk(const Cfg& cfg, int path, int k) {
+  if (cfg.chunk_bytes) return cfg.chunk_bytes;
+  const size_t kk = size_t(k < 1 ? 1 : k);
+  if (path == HOC_PATH_TMA)
+    return std::min(size_t(16) << 20, std::max(size_t(4) << 20, kArChunkTmaBytesTimesK2 / (kk * kk)));
+  return std::min(size_t(8) << 20, std::max(size_t(2) << 20, kArChunkCeBytesTimesK / kk));
 }
 
 // Copy queues of a plan when the configuration leaves their number to the

@@ -214,7 +214,7 @@ def _sizes(vals, n) -> Optional[C.Array]:
 @dataclass
 class Config:
     path: str = "auto"
-    chunk_bytes: int = 0  # 0: by move path (4 MiB on both, the measured best)
+    chunk_bytes: int = 0  # 0: picked by the scheduler (allreduce: by move path and rank count)
     n_copy_streams: int = 0  # 0: the scheduler picks per call (8 queues for copies of at most 2 MiB, else 4)
     pipeline_depth: int = 0
     reduce_max_sms: int = 0

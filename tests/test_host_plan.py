@@ -450,6 +450,22 @@ def test_copy_queue_count_follows_copy_size_when_left_to_the_scheduler():
     mixed = small.copy()
     mixed[3, 5] = 5 << 20                                                     # one flow of 4 MiB chunks
     assert queues(hoc.OP_ALLTOALL, 0, auto, mixed) == set(range(1, 5))
-    # the allreduce's moves: 4 MiB chunks of 32 MiB blocks stay on 4 queues
+    # the allreduce's moves: at 8 ranks its chunks are 4 MiB, so 4 queues; at 16 ranks 2 MiB, so 8
     items = hoc.plan_query(8, hoc.OP_ALLREDUCE, 1 << 27, hoc.BFLOAT16, config=auto)
     assert {it["stream"] for it in items if it["kind"] == hoc.ITEM_COPY} == set(range(1, 5))
+    items = hoc.plan_query(16, hoc.OP_ALLREDUCE, 1 << 27, hoc.BFLOAT16, config=auto)
+    assert {it["stream"] for it in items if it["kind"] == hoc.ITEM_COPY} == set(range(1, 9))
+
+
+@pytest.mark.parametrize("path,k,chunk_mib", [("ce", 2, 8), ("ce", 4, 8), ("ce", 8, 4), ("ce", 16, 2),
+                                              ("tma", 2, 16), ("tma", 4, 4), ("tma", 8, 4), ("tma", 16, 4)])
+def test_allreduce_chunk_left_to_the_scheduler_follows_the_rank_count(path, k, chunk_mib):
+    """chunk_bytes = 0: copy engines take 32 MiB / k within 2-8 MiB, the TMA kernel 64 MiB / k^2 within
+    4-16 MiB; an explicit size is kept; a block smaller than the chunk is one chunk."""
+    def reduce_steps(count, cfg):
+        items = hoc.plan_query(k, hoc.OP_ALLREDUCE, count, hoc.BFLOAT16, config=cfg)
+        return len({it["step"] for it in items if it["kind"] == hoc.ITEM_REDUCE})
+    n = 1 << 27                                                    # 256 MiB of bf16 per rank
+    assert reduce_steps(n, hoc.Config(path=path)) == (n // k * 2) // (chunk_mib << 20)
+    assert reduce_steps(n, hoc.Config(path=path, chunk_bytes=1 << 20)) == (n // k * 2) // (1 << 20)
+    assert reduce_steps(k * 1024, hoc.Config(path=path)) == 1
