@@ -45,27 +45,6 @@ inline size_t chunk_for(const Cfg& cfg, int path) {
   return cfg.chunk_bytes ? cfg.chunk_bytes : (path == HOC_PATH_TMA ? kAutoChunkTma : kAutoChunkCe);
 }
 
-// Pipeline chunk of the copy-engine and TMA allreduce when the configuration
-// leaves chunk_bytes at 0, by move path and rank count.  Each chunk costs a
-// reduce kernel and a round of k(k-1) copies; with few ranks a chunk's kernel
-// is small and its launch and tail show, with many the copies are many and
-// small.  From sweeps of 1-64 MiB chunks (bf16, 16 / 64 / 256 MiB per rank,
-// k = 2, 4, 8, 16, GB300): copy engines want 32 MiB / k within 2-8 MiB (k = 2:
-// 8 MiB, 0.180 ms at 256 MiB against 0.243 at 4 MiB; k = 4: 8 MiB, 0.100 ms at
-// 64 MiB against 0.106; k = 16: 2 MiB, 0.490 ms at 64 MiB against 0.543; at
-// k = 8, 2 and 4 MiB are equal and 4 MiB runs half the reduce kernels beside
-// the caller's), the TMA kernel 64 MiB / k^2 within 4-16 MiB (k = 2: 16 MiB,
-// 0.199 ms at 256 MiB against 0.278).  A block smaller than the chunk is one
-// chunk.
-constexpr size_t kArChunkCeBytesTimesK = size_t(32) << 20;
-constexpr size_t kArChunkTmaBytesTimesK2 = size_t(64) << 20;
-inline size_t allreduce_chunk(const Cfg& cfg, int path, int k) {
-  if (cfg.chunk_bytes) return cfg.chunk_bytes;
-  const size_t kk = size_t(k < 1 ? 1 : k);
-  if (path == HOC_PATH_TMA)
-    return std::min(size_t(16) << 20, std::max(size_t(4) << 20, kArChunkTmaBytesTimesK2 / (kk * kk)));
-  return std::min(size_t(8) << 20, std::max(size_t(2) << 20, kArChunkCeBytesTimesK / kk));
-}
 
 // Copy queues of a plan when the configuration leaves their number to the
 // scheduler: copies are started back to back on each queue at about 4 us per
@@ -81,6 +60,34 @@ constexpr size_t kAutoSmallCopyBytes = size_t(2) << 20;
 inline int copy_queues(const Cfg& cfg, size_t largest_copy) {
   if (!cfg.n_copy_auto) return cfg.n_copy;
   return largest_copy <= kAutoSmallCopyBytes ? kAutoQueuesSmall : kAutoQueuesLarge;
+}
+
+// Pipeline chunk of the copy-engine and TMA allreduce when the configuration
+// leaves chunk_bytes at 0, by move path and rank count.  Each chunk costs a
+// reduce kernel and a round of k(k-1) copies; with few ranks a chunk's kernel
+// is small and its launch and tail show, with many the copies are many and
+// small.  From sweeps of 1-64 MiB chunks (bf16, 16 / 64 / 256 MiB per rank,
+// k = 2, 4, 8, 16, GB300): copy engines want 32 MiB / k within 2-8 MiB (k = 2:
+// 8 MiB, 0.180 ms at 256 MiB against 0.243 at 4 MiB; k = 16: 2 MiB, 0.490 ms
+// at 64 MiB against 0.543), the TMA kernel 64 MiB / k^2 within 4-16 MiB (k = 2:
+// 16 MiB, 0.199 ms at 256 MiB against 0.278).  The copy engines' chunk is
+// also held to 16 MiB in flight over the queues one chunk's copies spread
+// over -- what 4 queues of the 4 MiB all-gather copies hold: a compute kernel
+// beside the moves slows with the bytes in flight (k = 4 keeps 4 MiB, which
+// 8 MiB beat by at most 6 %).  A block smaller than the chunk is one chunk.
+constexpr size_t kArChunkCeBytesTimesK = size_t(32) << 20;
+constexpr size_t kArChunkTmaBytesTimesK2 = size_t(64) << 20;
+constexpr size_t kArCeInFlightBytes = size_t(16) << 20;
+inline size_t allreduce_chunk(const Cfg& cfg, int path, int k) {
+  if (cfg.chunk_bytes) return cfg.chunk_bytes;
+  const size_t kk = size_t(k < 1 ? 1 : k);
+  const size_t lo = size_t(2) << 20;
+  if (path == HOC_PATH_TMA)
+    return std::min(size_t(16) << 20, std::max(size_t(4) << 20, kArChunkTmaBytesTimesK2 / (kk * kk)));
+  size_t c = std::min(size_t(8) << 20, std::max(lo, kArChunkCeBytesTimesK / kk));
+  const size_t spread = std::min(kk * (kk - 1), size_t(std::max(1, copy_queues(cfg, c))));
+  if (spread > 0) c = std::min(c, std::max(lo, kArCeInFlightBytes / spread));
+  return c;
 }
 
 // Send/recv messages up to this size go as one copy on the caller's stream;

@@ -457,11 +457,12 @@ def test_copy_queue_count_follows_copy_size_when_left_to_the_scheduler():
     assert {it["stream"] for it in items if it["kind"] == hoc.ITEM_COPY} == set(range(1, 9))
 
 
-@pytest.mark.parametrize("path,k,chunk_mib", [("ce", 2, 8), ("ce", 4, 8), ("ce", 8, 4), ("ce", 16, 2),
+@pytest.mark.parametrize("path,k,chunk_mib", [("ce", 2, 8), ("ce", 4, 4), ("ce", 8, 4), ("ce", 16, 2),
                                               ("tma", 2, 16), ("tma", 4, 4), ("tma", 8, 4), ("tma", 16, 4)])
 def test_allreduce_chunk_left_to_the_scheduler_follows_the_rank_count(path, k, chunk_mib):
-    """chunk_bytes = 0: copy engines take 32 MiB / k within 2-8 MiB, the TMA kernel 64 MiB / k^2 within
-    4-16 MiB; an explicit size is kept; a block smaller than the chunk is one chunk."""
+    """chunk_bytes = 0: copy engines take 32 MiB / k within 2-8 MiB and at most 16 MiB over the queues one
+    chunk's copies use (k = 4: 4 MiB on 4 queues), the TMA kernel 64 MiB / k^2 within 4-16 MiB; an explicit
+    size is kept; a block smaller than the chunk is one chunk."""
     def reduce_steps(count, cfg):
         items = hoc.plan_query(k, hoc.OP_ALLREDUCE, count, hoc.BFLOAT16, config=cfg)
         return len({it["step"] for it in items if it["kind"] == hoc.ITEM_REDUCE})
@@ -469,3 +470,5 @@ def test_allreduce_chunk_left_to_the_scheduler_follows_the_rank_count(path, k, c
     assert reduce_steps(n, hoc.Config(path=path)) == (n // k * 2) // (chunk_mib << 20)
     assert reduce_steps(n, hoc.Config(path=path, chunk_bytes=1 << 20)) == (n // k * 2) // (1 << 20)
     assert reduce_steps(k * 1024, hoc.Config(path=path)) == 1
+    if path == "ce" and k == 8:   # 8 explicit queues: 2 MiB chunks keep the 16 MiB in flight
+        assert reduce_steps(n, hoc.Config(path=path, n_copy_streams=8)) == (n // k * 2) // (2 << 20)
