@@ -105,8 +105,11 @@ std::vector<std::vector<int>> source_groups(const std::vector<Move>& moves) {
 namespace {
 
 size_t chunk_elems(size_t chunk_bytes, size_t b) {
+  // whole kCopyAlignBytes units where the chunk holds one (so that chunks cut
+  // from an aligned offset stay aligned), else 16-element multiples
+  if (chunk_bytes >= kCopyAlignBytes) return chunk_bytes / kCopyAlignBytes * kCopyAlignBytes / b;
   size_t ce = chunk_bytes / b;
-  ce -= ce % 16;  // keep chunk boundaries on 16-element multiples
+  ce -= ce % 16;
   return ce < 16 ? 16 : ce;
 }
 
@@ -241,7 +244,28 @@ hocResult_t plan_allreduce(const Cfg& cfg, const CallShape& s, Plan* p) {
     return HOC_SUCCESS;
   }
   const size_t ce = chunk_elems(allreduce_chunk(cfg, p->path, k), b);
-  const size_t nq = (sz[0] + ce - 1) / ce;
+  // Chunk boundaries inside a block sit on kCopyAlignBytes offsets of the
+  // buffers: chunk 0 of owner r runs from the block's start to the first
+  // aligned offset past it plus one chunk, the rest are whole chunks from
+  // there.  Which rank owns an element (and so its fold order) is the
+  // block's; only where the pipeline cuts it moves.
+  const size_t ae = kCopyAlignBytes / b;
+  std::vector<size_t> body(k);  // first aligned element of each block (clamped to its end)
+  size_t nq = 1;
+  for (int r = 0; r < k; ++r) {
+    const size_t end = off[r] + sz[r];
+    body[r] = std::min(end, (off[r] + ae - 1) / ae * ae);
+    nq = std::max(nq, sz[r] ? std::max<size_t>(1, (end - body[r] + ce - 1) / ce) : size_t(1));
+  }
+  // chunk q of owner r: [*lo, *lo + *n); false if the block has no chunk q
+  auto chunk_of = [&](int r, size_t q, size_t* lo, size_t* n) {
+    const size_t end = off[r] + sz[r];
+    const size_t a = q == 0 ? off[r] : body[r] + q * ce;
+    if (sz[r] == 0 || a >= end) return false;
+    *lo = a;
+    *n = std::min(end, body[r] + (q + 1) * ce) - a;
+    return true;
+  };
   const int queues = copy_queues(cfg, std::min(ce, sz[0]) * b);
   std::vector<std::vector<int>> copy_steps(nq);
   for (size_t q = 0; q < nq; ++q) {
@@ -252,18 +276,15 @@ hocResult_t plan_allreduce(const Cfg& cfg, const CallShape& s, Plan* p) {
     if (cfg.depth > 0 && q >= size_t(cfg.depth)) red.waits = copy_steps[q - cfg.depth];
     std::vector<Move> moves;
     for (int r = 0; r < k; ++r) {
-      const size_t lo = q * ce;
-      if (lo >= sz[r]) continue;
-      const size_t n = std::min(ce, sz[r] - lo);
-      red.segs.push_back(ReduceSeg{off[r] + lo, n, off[r] + lo, uint32_t(r), 0});
+      size_t lo, n;
+      if (chunk_of(r, q, &lo, &n)) red.segs.push_back(ReduceSeg{lo, n, lo, uint32_t(r), 0});
     }
     // owner r's finished chunk goes to every other rank, shift by shift
     for (int t = 1; t < k; ++t)
       for (int r = 0; r < k; ++r) {
-        const size_t lo = q * ce;
-        if (lo >= sz[r]) continue;
-        const size_t n = std::min(ce, sz[r] - lo);
-        const size_t byte_off = (off[r] + lo) * b;
+        size_t lo, n;
+        if (!chunk_of(r, q, &lo, &n)) continue;
+        const size_t byte_off = lo * b;
         moves.push_back(Move{r, (r + t) % k, HOC_BUF_RECV, HOC_BUF_RECV, byte_off, byte_off, n * b});
       }
     const int red_id = int(p->steps.size());

@@ -67,10 +67,12 @@ inline int copy_queues(const Cfg& cfg, size_t largest_copy) {
 // reduce kernel and a round of k(k-1) copies; with few ranks a chunk's kernel
 // is small and its launch and tail show, with many the copies are many and
 // small.  From sweeps of 1-64 MiB chunks (bf16, 16 / 64 / 256 MiB per rank,
-// k = 2, 4, 8, 16, GB300): copy engines want 32 MiB / k within 2-8 MiB (k = 2:
-// 8 MiB, 0.180 ms at 256 MiB against 0.243 at 4 MiB; k = 16: 2 MiB, 0.490 ms
-// at 64 MiB against 0.543), the TMA kernel 64 MiB / k^2 within 4-16 MiB (k = 2:
-// 16 MiB, 0.199 ms at 256 MiB against 0.278).  The copy engines' chunk is
+// k = 2..16, GB300): copy engines want 32 MiB / k within 2-8 MiB, rounded down
+// to a power of two (k = 2: 8 MiB, 0.180 ms at 256 MiB against 0.243 at 4 MiB;
+// k = 9 and 12: 2 MiB on 8 queues, 1.12 and 1.69 ms against 1.20 and 1.77 at
+// 3-4 MiB on 4; k = 16: 2 MiB, 0.490 ms at 64 MiB against 0.543), the TMA
+// kernel 64 MiB / k^2 within 4-16 MiB (k = 2: 16 MiB, 0.199 ms at 256 MiB
+// against 0.278).  The copy engines' chunk is
 // also held to 16 MiB in flight over the queues one chunk's copies spread
 // over -- what 4 queues of the 4 MiB all-gather copies hold: a compute kernel
 // beside the moves slows with the bytes in flight (k = 4 keeps 4 MiB, which
@@ -85,10 +87,18 @@ inline size_t allreduce_chunk(const Cfg& cfg, int path, int k) {
   if (path == HOC_PATH_TMA)
     return std::min(size_t(16) << 20, std::max(size_t(4) << 20, kArChunkTmaBytesTimesK2 / (kk * kk)));
   size_t c = std::min(size_t(8) << 20, std::max(lo, kArChunkCeBytesTimesK / kk));
+  while (c & (c - 1)) c &= c - 1;  // the power of two at or below
   const size_t spread = std::min(kk * (kk - 1), size_t(std::max(1, copy_queues(cfg, c))));
   if (spread > 0) c = std::min(c, std::max(lo, kArCeInFlightBytes / spread));
   return c;
 }
+
+// Allreduce chunk boundaries sit on multiples of this many bytes into the
+// rank buffers.  A copy-engine copy that starts off such a boundary runs at
+// about two thirds of the rate: the copy-engine allreduce of 256 MiB bf16 per
+// rank at k = 6 took 1.046 ms with blocks 32 B aligned and 0.699 ms with them
+// 4 KiB aligned (64 KiB and 2 MiB: 0.699 and 0.688 ms).
+constexpr size_t kCopyAlignBytes = 4096;
 
 // Send/recv messages up to this size go as one copy on the caller's stream;
 // larger ones are chunked and striped over the copy queues.

@@ -82,7 +82,7 @@ typedef struct {
   int path;              /* hocPath_t */
   size_t chunk_bytes;    /* pipeline unit inside a block / flow; 0 (default): the scheduler
                             picks -- allreduce chunks by move path and rank count k (copy
-                            engines 32 MiB / k within 2-8 MiB and at most 16 MiB in flight
+                            engines 32 MiB / k within 2-8 MiB, a power of two, at most 16 MiB in flight
                             over the copy queues, TMA kernel 64 MiB / k^2 within 4-16 MiB),
                             4 MiB copies for the other collectives */
   int n_copy_streams;    /* internal copy streams (the multi-QP analogue), max 16; 0 (default):

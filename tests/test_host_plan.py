@@ -93,7 +93,8 @@ def test_no_device_is_a_clean_error():
 
 # ---------------------------------------------------------------- allreduce
 @pytest.mark.parametrize("path", ["ce", "tma"])
-@pytest.mark.parametrize("k,n,chunk", [(4, 1 << 20, 1 << 18), (8, 1000003, 1 << 16), (3, 17, 256), (5, 4096 * 5 + 3, 4096)])
+@pytest.mark.parametrize("k,n,chunk", [(4, 1 << 20, 1 << 18), (8, 1000003, 1 << 16), (3, 17, 256), (5, 4096 * 5 + 3, 4096),
+                                       (6, 300007, 1 << 14), (7, 50000, 0)])
 def test_allreduce_plan_covers_every_block_once(path, k, n, chunk):
     b = 4
     items = hoc.plan_query(k, hoc.OP_ALLREDUCE, n, hoc.FLOAT32, config=hoc.Config(path=path, chunk_bytes=chunk))
@@ -125,6 +126,30 @@ def test_allreduce_plan_covers_every_block_once(path, k, n, chunk):
             iv, ov = _cover(moves[(r, d)])
             assert not ov and _total(iv) == sizes[r] * b
             assert iv[0][0] == offs[r] * b
+
+
+@pytest.mark.parametrize("path", ["ce", "tma"])
+def test_allreduce_chunk_boundaries_sit_on_4_kib_offsets(path):
+    """Blocks that start off a 4 KiB boundary (k = 6, 2^27 bf16): every chunk of a block but its first starts
+    on one, the first runs from the block's start to one chunk past the block's first boundary, and the
+    blocks (which rank folds what) are the oracle's."""
+    k, n, b = 6, 1 << 27, 2
+    items = hoc.plan_query(k, hoc.OP_ALLREDUCE, n, hoc.BFLOAT16, config=hoc.Config(path=path))
+    sizes, offs = o_ring.block_partition(n, k)
+    assert any((offs[r] * b) % 4096 for r in range(k))
+    for r in range(k):
+        segs = sorted((it["src_off"], it["bytes"]) for it in items
+                      if it["kind"] == hoc.ITEM_REDUCE and it["dst_rank"] == r)
+        assert segs[0][0] == offs[r] * b
+        assert all(off % 4096 == 0 for off, _ in segs[1:])
+        assert sum(nb for _, nb in segs) == sizes[r] * b
+        ce = segs[1][1]
+        assert segs[0][0] + segs[0][1] == -(-offs[r] * b // 4096) * 4096 + ce
+    # a chunk size that is not a whole number of 4 KiB units is cut down to one (k = 12: 32 MiB / 12)
+    items = hoc.plan_query(12, hoc.OP_ALLREDUCE, n, hoc.BFLOAT16, config=hoc.Config(path=path))
+    offs12 = [it["src_off"] for it in items if it["kind"] == hoc.ITEM_REDUCE]
+    sizes12, starts12 = o_ring.block_partition(n, 12)
+    assert all(o % 4096 == 0 for o in offs12 if o not in {s * b for s in starts12})
 
 
 def test_allreduce_chunking_and_striping():
@@ -457,18 +482,25 @@ def test_copy_queue_count_follows_copy_size_when_left_to_the_scheduler():
     assert {it["stream"] for it in items if it["kind"] == hoc.ITEM_COPY} == set(range(1, 9))
 
 
-@pytest.mark.parametrize("path,k,chunk_mib", [("ce", 2, 8), ("ce", 4, 4), ("ce", 8, 4), ("ce", 16, 2),
+@pytest.mark.parametrize("path,k,chunk_mib", [("ce", 2, 8), ("ce", 4, 4), ("ce", 8, 4), ("ce", 16, 2), ("ce", 12, 2),
                                               ("tma", 2, 16), ("tma", 4, 4), ("tma", 8, 4), ("tma", 16, 4)])
 def test_allreduce_chunk_left_to_the_scheduler_follows_the_rank_count(path, k, chunk_mib):
-    """chunk_bytes = 0: copy engines take 32 MiB / k within 2-8 MiB and at most 16 MiB over the queues one
-    chunk's copies use (k = 4: 4 MiB on 4 queues), the TMA kernel 64 MiB / k^2 within 4-16 MiB; an explicit
-    size is kept; a block smaller than the chunk is one chunk."""
+    """chunk_bytes = 0: copy engines take 32 MiB / k within 2-8 MiB, rounded down to a power of two (k = 12:
+    2 MiB), and at most 16 MiB over the queues one chunk's copies use (k = 4: 4 MiB on 4 queues); the TMA
+    kernel 64 MiB / k^2 within 4-16 MiB; an explicit size is kept; a block smaller than the chunk is one
+    chunk."""
     def reduce_steps(count, cfg):
         items = hoc.plan_query(k, hoc.OP_ALLREDUCE, count, hoc.BFLOAT16, config=cfg)
         return len({it["step"] for it in items if it["kind"] == hoc.ITEM_REDUCE})
+    def expect(n, chunk):   # chunks cut from each block's first 4 KiB offset (the first one absorbs the head)
+        sizes, offs = o_ring.block_partition(n, k)
+        return max(max(1, -(-((o + z) * 2 - min((o + z) * 2, -(-o * 2 // 4096) * 4096)) // chunk))
+                   for z, o in zip(sizes, offs))
     n = 1 << 27                                                    # 256 MiB of bf16 per rank
-    assert reduce_steps(n, hoc.Config(path=path)) == (n // k * 2) // (chunk_mib << 20)
-    assert reduce_steps(n, hoc.Config(path=path, chunk_bytes=1 << 20)) == (n // k * 2) // (1 << 20)
+    assert reduce_steps(n, hoc.Config(path=path)) == expect(n, chunk_mib << 20)
+    assert reduce_steps(n, hoc.Config(path=path, chunk_bytes=1 << 20)) == expect(n, 1 << 20)
+    if k in (2, 4, 8, 16):
+        assert expect(n, chunk_mib << 20) == (n // k * 2) // (chunk_mib << 20)
     assert reduce_steps(k * 1024, hoc.Config(path=path)) == 1
     if path == "ce" and k == 8:   # 8 explicit queues: 2 MiB chunks keep the 16 MiB in flight
         assert reduce_steps(n, hoc.Config(path=path, n_copy_streams=8)) == (n // k * 2) // (2 << 20)
