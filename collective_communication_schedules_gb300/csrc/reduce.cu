@@ -157,6 +157,7 @@ __device__ __forceinline__ void scalar_elem(const ReduceParams& p, const uint8_t
 }
 
 // K > 0: compile-time rank count (all loads hoisted); K == 0: runtime p.k.
+constexpr int kRuntimeGroup = 4;
 template <class Tr, int K, int kThreads, int kVecPerThread>
 __global__ void __launch_bounds__(kThreads) reduce_kernel(const __grid_constant__ ReduceParams p) {
   // Programmatic dependent launch (both no-ops for a launch without the
@@ -204,15 +205,38 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const __grid_constant_
           }
         }
       } else {
+        // Runtime k: the operands after the first come in groups of
+        // kRuntimeGroup, every load of a group issued before its adds (which
+        // stay in ring order), so that a thread keeps as many loads in flight
+        // as the compile-time kernels do.
+        typename Tr::Acc acc[kVecPerThread];
 #pragma unroll
         for (int i = 0; i < kVecPerThread; ++i) {
           const uint64_t v = vbase + uint64_t(i) * kThreads;
-          if (v < nvec) {
-            typename Tr::Acc acc = Tr::widen(__ldcs(static_cast<const uint4*>(at(p.in[seq[0]], e0 + v * L, Tr::kBytes))));
-            for (int j = 1; j < k; ++j)
-              Tr::add(acc, __ldcs(static_cast<const uint4*>(at(p.in[seq[j]], e0 + v * L, Tr::kBytes))));
-            store_vec<Tr>(p, sg.owner, k, o0 + v * L, Tr::narrow(acc));
-          }
+          if (v < nvec) acc[i] = Tr::widen(__ldcs(static_cast<const uint4*>(at(p.in[seq[0]], e0 + v * L, Tr::kBytes))));
+        }
+        for (int j0 = 1; j0 < k; j0 += kRuntimeGroup) {
+          uint4 x[kRuntimeGroup][kVecPerThread];
+#pragma unroll
+          for (int g = 0; g < kRuntimeGroup; ++g)
+#pragma unroll
+            for (int i = 0; i < kVecPerThread; ++i) {
+              const uint64_t v = vbase + uint64_t(i) * kThreads;
+              if (j0 + g < k && v < nvec)
+                x[g][i] = __ldcs(static_cast<const uint4*>(at(p.in[seq[j0 + g]], e0 + v * L, Tr::kBytes)));
+            }
+#pragma unroll
+          for (int g = 0; g < kRuntimeGroup; ++g)
+#pragma unroll
+            for (int i = 0; i < kVecPerThread; ++i) {
+              const uint64_t v = vbase + uint64_t(i) * kThreads;
+              if (j0 + g < k && v < nvec) Tr::add(acc[i], x[g][i]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kVecPerThread; ++i) {
+          const uint64_t v = vbase + uint64_t(i) * kThreads;
+          if (v < nvec) store_vec<Tr>(p, sg.owner, k, o0 + v * L, Tr::narrow(acc[i]));
         }
       }
       if (lt == 0 && threadIdx.x < head) scalar_elem<Tr>(p, seq, sg.owner, k, sg.elem_off + threadIdx.x, sg.out_off + threadIdx.x);

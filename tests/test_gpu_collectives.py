@@ -31,7 +31,7 @@ def _comm(k, path="auto", **kw):
 
 
 @pytest.mark.parametrize("dtype", ["int32", "float32", "bfloat16"])
-@pytest.mark.parametrize("k", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("k", [1, 2, 3, 4, 8, 9, 12, 16])   # 9, 12: the runtime-k fold with a partial last group
 @pytest.mark.parametrize("path,engine", [("ce", "lsu"), ("tma", "lsu"), ("fused", "lsu"), ("fused", "tma"),
                                          ("ce", "tma")])
 def test_allreduce_parity(dtype, k, path, engine):
