@@ -113,14 +113,36 @@ size_t chunk_elems(size_t chunk_bytes, size_t b) {
   return ce < 16 ? 16 : ce;
 }
 
-// Split `m` into pieces of at most `chunk` bytes.
+// Pieces of a move of about `chunk` bytes: cut on kCopyAlignBytes offsets of
+// the destination (the first piece runs from the move's start to one chunk
+// past the first such offset), a last piece under a quarter chunk merged into
+// the one before.  (Copying the bytes before the first aligned offset as a
+// piece of their own was tried for destinations not even 16-byte aligned:
+// all-gathers gained, all-to-alls of single-piece flows lost, 0.416 -> 0.456
+// ms.)  (offset into the move, bytes) each.
+std::vector<std::pair<size_t, size_t>> move_pieces(size_t dst_off, size_t bytes, size_t chunk) {
+  std::vector<std::pair<size_t, size_t>> v;
+  if (bytes == 0) return v;
+  const size_t head = (kCopyAlignBytes - dst_off % kCopyAlignBytes) % kCopyAlignBytes;
+  size_t off = 0;
+  size_t next = std::min(bytes, head + chunk);
+  for (;;) {
+    if (bytes - next < chunk / 4) next = bytes;
+    v.emplace_back(off, next - off);
+    if (next == bytes) break;
+    off = next;
+    next = std::min(bytes, off + chunk);
+  }
+  return v;
+}
+
+// Split `m` into its pieces (move_pieces).
 void split_move(const Move& m, size_t chunk, std::vector<Move>* out) {
-  if (m.bytes == 0) return;
-  for (size_t off = 0; off < m.bytes; off += chunk) {
+  for (const auto& pc : move_pieces(m.dst_off, m.bytes, chunk)) {
     Move c = m;
-    c.src_off += off;
-    c.dst_off += off;
-    c.bytes = std::min(chunk, m.bytes - off);
+    c.src_off += pc.first;
+    c.dst_off += pc.first;
+    c.bytes = pc.second;
     out->push_back(c);
   }
 }
@@ -370,19 +392,21 @@ hocResult_t plan_alltoall(const Cfg& cfg, const CallShape& s, Plan* p) {
   std::vector<int> prev;
   for (int st = 0; st < k; ++st) {
     std::vector<Move> flows;
+    std::vector<std::vector<std::pair<size_t, size_t>>> pieces;
     std::vector<size_t> nchunks;
     for (int u = 0; u < k; ++u) {
       const int v = (u + st) % k;
       const size_t n = cnt(u, v) * b;
       flows.push_back(Move{u, v, HOC_BUF_SEND, HOC_BUF_RECV, sd[size_t(u) * k + v] * b, rd[size_t(v) * k + u] * b, n});
-      nchunks.push_back((n + cb - 1) / cb);
+      pieces.push_back(move_pieces(flows.back().dst_off, n, cb));
+      nchunks.push_back(pieces.back().size());
     }
     std::vector<Move> chunks;
     for (const auto& fc : interleave_chunks(nchunks, cfg.a2a_interleave != 0)) {
       const Move& f = flows[fc.first];
-      const size_t o = fc.second * cb;
-      chunks.push_back(Move{f.src_rank, f.dst_rank, f.src_buf, f.dst_buf, f.src_off + o, f.dst_off + o,
-                            std::min(cb, f.bytes - o)});
+      const auto& pc = pieces[fc.first][fc.second];
+      chunks.push_back(Move{f.src_rank, f.dst_rank, f.src_buf, f.dst_buf, f.src_off + pc.first, f.dst_off + pc.first,
+                            pc.second});
     }
     std::vector<int> ids;
     emit_moves(cfg, HOC_PATH_CE, chunks, st, cfg.a2a_stage_sync ? prev : std::vector<int>{}, cfg.a2a_stage_sync != 0,

@@ -152,6 +152,36 @@ def test_allreduce_chunk_boundaries_sit_on_4_kib_offsets(path):
     assert all(o % 4096 == 0 for o in offs12 if o not in {s * b for s in starts12})
 
 
+@pytest.mark.parametrize("op", ["allgather", "alltoall"])
+def test_move_pieces_start_on_4_kib_destination_offsets(op):
+    """Copy-engine moves whose destinations start off a 4 KiB boundary: each move's pieces cover it once,
+    every piece but the first starts on a 4 KiB destination offset, and no piece is left under a quarter
+    chunk unless the whole move is."""
+    k, chunk, b = 4, 4 << 20, 2
+    cfg = hoc.Config(path="ce", chunk_bytes=chunk)
+    if op == "allgather":
+        count = (9 << 20) // b + 8                          # blocks of 9 MiB + 16 B: destinations r * that
+        items = hoc.plan_query(k, hoc.OP_ALLGATHER, count, hoc.BFLOAT16, config=cfg)
+    else:
+        counts = np.full((k, k), (9 << 20) // b + 8, dtype=np.uint64)
+        counts[1, 2] = 3                                    # a flow far under a quarter chunk
+        items = hoc.plan_query(k, hoc.OP_ALLTOALL, 0, hoc.BFLOAT16, counts=counts, config=cfg)
+    moves = defaultdict(list)
+    for it in items:
+        if it["kind"] == hoc.ITEM_COPY:
+            moves[(it["src_rank"], it["dst_rank"])].append((it["dst_off"], it["src_off"], it["bytes"]))
+    assert moves
+    for key, ps in moves.items():
+        ps.sort()
+        total = sum(p[2] for p in ps)
+        for (d0, s0, n0), (d1, s1, n1) in zip(ps, ps[1:]):
+            assert d0 + n0 == d1 and s0 + n0 == s1, key           # contiguous on both sides
+        for d, _, n in ps[1:]:
+            assert d % 4096 == 0, key
+        assert all(n >= chunk // 4 for _, _, n in ps) or len(ps) == 1, key
+        assert total == (3 * b if (op, key) == ("alltoall", (1, 2)) else ((9 << 20) // b + 8) * b), key
+
+
 def test_allreduce_chunking_and_striping():
     k, n = 8, 134_217_728
     cfg = hoc.Config(path="ce", chunk_bytes=4 << 20, n_copy_streams=4)
