@@ -1438,7 +1438,7 @@ def run_ours(args, world, rank, local):
                 {"workload": f"profiling case: 8 ranks x {n_el:,} bf16", "k": k, "count": n_el},
                 "schedule": {"path": args.path,
                              "resolved_path": {0: "auto", 1: "ce", 2: "tma", 3: "fused"}[st["path"]],
-                             "chunk_bytes": args.chunk_bytes or "auto (4 MiB)",
+                             "chunk_bytes": args.chunk_bytes or "auto (by move path and rank count; 4 MiB at 8 ranks)",
                              "copy_streams": args.copy_streams or "auto (8 for copies of at most 2 MiB, else 4)"},
                 "algbw_gbs": round(per_rank / (ms_max * 1e-3) / 1e9, 2),
                 "hbm_frac": round(hbm_frac, 4), "lower_bound_frac": round(lb_frac, 4),

@@ -483,7 +483,8 @@ hocResult_t check_sizes(const Cfg& cfg, const CallShape& s) {
     }
     default: return HOC_ERR_INVALID_ARG;
   }
-  const uint64_t chunk = cfg.chunk_bytes ? cfg.chunk_bytes : std::min(kAutoChunkCe, kAutoChunkTma);
+  const uint64_t chunk =
+      cfg.chunk_bytes ? cfg.chunk_bytes : std::min(std::min(kAutoChunkCe, kAutoChunkTma), kArChunkMinBytes);
   if (span / chunk > kMaxChunksPerSpan) {
     set_error_detail("chunk_bytes too small for this size: more than 2^24 chunks per rank buffer");
     return HOC_ERR_INVALID_ARG;

@@ -80,10 +80,11 @@ inline int copy_queues(const Cfg& cfg, size_t largest_copy) {
 constexpr size_t kArChunkCeBytesTimesK = size_t(32) << 20;
 constexpr size_t kArChunkTmaBytesTimesK2 = size_t(64) << 20;
 constexpr size_t kArCeInFlightBytes = size_t(16) << 20;
+constexpr size_t kArChunkMinBytes = size_t(2) << 20;  // the smallest chunk the scheduler picks
 inline size_t allreduce_chunk(const Cfg& cfg, int path, int k) {
   if (cfg.chunk_bytes) return cfg.chunk_bytes;
   const size_t kk = size_t(k < 1 ? 1 : k);
-  const size_t lo = size_t(2) << 20;
+  const size_t lo = kArChunkMinBytes;
   if (path == HOC_PATH_TMA)
     return std::min(size_t(16) << 20, std::max(size_t(4) << 20, kArChunkTmaBytesTimesK2 / (kk * kk)));
   size_t c = std::min(size_t(8) << 20, std::max(lo, kArChunkCeBytesTimesK / kk));
