@@ -534,3 +534,67 @@ def test_allreduce_chunk_left_to_the_scheduler_follows_the_rank_count(path, k, c
     assert reduce_steps(k * 1024, hoc.Config(path=path)) == 1
     if path == "ce" and k == 8:   # 8 explicit queues: 2 MiB chunks keep the 16 MiB in flight
         assert reduce_steps(n, hoc.Config(path=path, n_copy_streams=8)) == (n // k * 2) // (2 << 20)
+
+
+# ------------------------------------------------------------ random plans
+def test_random_large_allreduce_plans_cover_every_block_once():
+    """Random rank counts, element counts up to unaligned megabytes (blocks of many chunks, cut on 4 KiB
+    offsets), dtypes, move paths and chunk settings: the reduce segments cover each owner's block once
+    (the oracle's partition), every other rank receives each block once, and each move waits for the
+    reduce of its own chunk."""
+    rng = np.random.default_rng(4321)
+    dtypes = [(hoc.BFLOAT16, 2), (hoc.FLOAT32, 4), (hoc.INT32, 4)]
+    for _ in range(60):
+        k = int(rng.integers(2, 17))
+        n = int(rng.choice([rng.integers(1 << 16, 1 << 20), rng.integers(1 << 20, 1 << 23)]))
+        code, b = dtypes[int(rng.integers(0, 3))]
+        path = ["ce", "tma"][int(rng.integers(0, 2))]
+        chunk = int(rng.choice([0, 0, 65536 + 16, 1 << 20, 3 << 20]))
+        cfg = hoc.Config(path=path, chunk_bytes=chunk)
+        items = hoc.plan_query(k, hoc.OP_ALLREDUCE, n, code, config=cfg)
+        sizes, offs = o_ring.block_partition(n, k)
+        steps = {}
+        red, moves = defaultdict(list), defaultdict(list)
+        for it in items:
+            steps.setdefault(it["step"], it)
+            if it["kind"] == hoc.ITEM_REDUCE:
+                red[it["dst_rank"]].append((it["src_off"], it["src_off"] + it["bytes"]))
+            else:
+                moves[(it["src_rank"], it["dst_rank"])].append((it["src_off"], it["src_off"] + it["bytes"]))
+                w = steps[it["wait0"]]
+                assert w["kind"] == hoc.ITEM_REDUCE and w["stage"] == it["stage"], (k, n, path, chunk)
+                assert it["src_off"] == it["dst_off"]
+        for r in range(k):
+            if sizes[r] == 0:
+                assert not red[r]
+                continue
+            iv, ov = _cover(red[r])
+            assert not ov and _total(iv) == sizes[r] * b and iv[0][0] == offs[r] * b, (k, n, path, chunk, r)
+            for d in range(k):
+                if d != r:
+                    iv, ov = _cover(moves[(r, d)])
+                    assert not ov and _total(iv) == sizes[r] * b, (k, n, path, chunk, r, d)
+
+
+def test_random_large_alltoallv_plans_cut_pieces_on_4_kib_destinations():
+    """Random counts up to several chunks (zeros, tiny, unaligned): each flow's pieces cover it once,
+    contiguously on both sides, and every piece but a flow's first starts on a 4 KiB destination offset."""
+    rng = np.random.default_rng(8765)
+    for _ in range(60):
+        k = int(rng.integers(1, 9))
+        counts = rng.integers(0, 5 << 20, size=(k, k)).astype(np.uint64)
+        counts[rng.random((k, k)) < 0.2] = 0
+        counts[rng.random((k, k)) < 0.2] = rng.integers(1, 100)
+        chunk = int(rng.choice([0, 1 << 20, 3 << 20]))
+        items = hoc.plan_query(k, hoc.OP_ALLTOALL, 0, hoc.UINT8, counts=counts,
+                               config=hoc.Config(path="ce", chunk_bytes=chunk))
+        got = defaultdict(list)
+        for it in items:
+            if it["kind"] == hoc.ITEM_COPY:
+                got[(it["src_rank"], it["dst_rank"])].append((it["dst_off"], it["src_off"], it["bytes"]))
+        for a in range(k):
+            for d in range(k):
+                ps = sorted(got[(a, d)])
+                assert sum(p[2] for p in ps) == int(counts[a, d]), (k, a, d)
+                for (d0, s0, n0), (d1, s1, n1) in zip(ps, ps[1:]):
+                    assert d0 + n0 == d1 and s0 + n0 == s1 and d1 % 4096 == 0, (k, a, d)
