@@ -598,3 +598,27 @@ def test_random_large_alltoallv_plans_cut_pieces_on_4_kib_destinations():
                 assert sum(p[2] for p in ps) == int(counts[a, d]), (k, a, d)
                 for (d0, s0, n0), (d1, s1, n1) in zip(ps, ps[1:]):
                     assert d0 + n0 == d1 and s0 + n0 == s1 and d1 % 4096 == 0, (k, a, d)
+
+
+def test_allreduce_chunk_rule_at_every_rank_count():
+    """chunk_bytes = 0 at k = 2..16 (256 MiB bf16 per rank): the copy engines' chunk is a power of two in
+    2-8 MiB whose queues hold at most 16 MiB in flight, the TMA kernel's 4-16 MiB; every chunk after a
+    block's first is one whole chunk of that size (the last may be shorter)."""
+    n = 1 << 27
+    for k in range(2, 17):
+        sizes, offs = o_ring.block_partition(n, k)
+        for path, lo, hi in (("ce", 2 << 20, 8 << 20), ("tma", 4 << 20, 16 << 20)):
+            items = hoc.plan_query(k, hoc.OP_ALLREDUCE, n, hoc.BFLOAT16, config=hoc.Config(path=path))
+            segs = defaultdict(list)
+            for it in items:
+                if it["kind"] == hoc.ITEM_REDUCE:
+                    segs[it["dst_rank"]].append((it["src_off"], it["bytes"]))
+            chunk = max(nb for r in segs for _, nb in sorted(segs[r])[1:-1]) if len(segs[0]) > 2 else None
+            assert chunk is not None and lo <= chunk <= hi, (k, path, chunk)
+            if path == "ce":
+                assert chunk & (chunk - 1) == 0, (k, chunk)
+                queues = {it["stream"] for it in items if it["kind"] == hoc.ITEM_COPY}
+                assert chunk * min(len(queues), k * (k - 1)) <= 16 << 20, (k, chunk, len(queues))
+            for r in range(k):
+                mid = sorted(segs[r])[1:-1]
+                assert all(nb == chunk for _, nb in mid), (k, path, r)
