@@ -340,10 +340,11 @@ __global__ void __launch_bounds__(kThreadsT, 1)
 // tiles (register-fed kernel: 0.77 ms).  Across rank counts a stage of about
 // 64-96 KiB did best in the fused allreduce of 256 MiB bf16 per rank on all
 // SMs: at k = 2, 32 KiB tiles read 0.96 of the measured copy rate against
-// 0.80 with 16 KiB; at k = 4, 20 KiB 0.90 against 0.88; at k = 12 and 16,
-// 6 KiB 0.94 and 0.91 against 0.87 and 0.89 with 4 KiB.
+// 0.80 with 16 KiB; at k = 3, 24 KiB 0.89 against 0.85 (16 KiB) and 0.86
+// (32 KiB); at k = 4, 20 KiB 0.90 against 0.88; at k = 12 and 16, 6 KiB 0.94
+// and 0.91 against 0.87 and 0.89 with 4 KiB.
 uint32_t reduce_tma_tile_bytes(int k) {
-  return k <= 2 ? 32768u : (k <= 4 ? 20480u : (k <= 8 ? 12288u : 6144u));
+  return k <= 2 ? 32768u : (k <= 3 ? 24576u : (k <= 4 ? 20480u : (k <= 8 ? 12288u : 6144u)));
 }
 
 int reduce_tma_stages(int k) {
